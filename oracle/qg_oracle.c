@@ -1,0 +1,450 @@
+/*
+ * qg_oracle.c -- plain CPU oracle (TEST INFRASTRUCTURE ONLY; see qg_oracle.h).
+ *
+ * Written for a reader to check by eye against the definitions: one element at a
+ * time, no blocking, no SIMD, fp64 throughout except where the method fixes fp32.
+ * The only parallelism is an OpenMP loop over independent output rows, which does
+ * not change any result.
+ */
+#include "qg_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int g_threads = 0; /* 0: OpenMP default */
+
+void or_set_threads(int n) { g_threads = n; }
+
+int or_get_threads(void) {
+#ifdef _OPENMP
+    return g_threads > 0 ? g_threads : omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int or_block_elems(int fmt) {
+    switch (fmt) {
+    case OR_Q4_0: case OR_Q8_0: return 32;
+    case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: case OR_IQ4_XS: return 256;
+    default: return 0;
+    }
+}
+
+int or_block_bytes(int fmt) {
+    switch (fmt) {
+    case OR_Q4_0: return 18;    /* fp16 d + 16 bytes of nibbles              */
+    case OR_Q8_0: return 34;    /* fp16 d + 32 int8                          */
+    case OR_Q4_K: return 144;   /* d, dmin, 12 B scales/mins, 128 B nibbles   */
+    case OR_Q5_K: return 176;   /* Q4_K fields + 32 B of fifth bits           */
+    case OR_Q6_K: return 210;   /* 128 B ql, 64 B qh, 16 int8 scales, fp16 d  */
+    case OR_IQ4_XS: return 136; /* d, u16 scales_h, 4 B scales_l, 128 B index */
+    default: return 0;
+    }
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double or_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 31;
+    int frac = h & 1023;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);                 /* subnormal: frac * 2^-14 * 2^-10 */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);  /* (1 + frac/1024) * 2^(expo-15) */
+    }
+    return sign ? -v : v;
+}
+
+static uint16_t rd_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static double rd_half(const uint8_t *p) { return or_half_to_double(rd_u16(p)); }
+
+/* The 16-entry non-linear codebook of IQ4_NL / IQ4_XS (public GGUF definition;
+ * the page speaks only of "a tiny codebook kept in registers"). */
+static const int8_t kIQ4NL[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
+                                  1,    13,   25,  38,  53,  69,  89,  113};
+
+/* Q4_K / Q5_K: 6-bit scale S_j and min M_j of sub-block j (0..7) packed in 12 bytes. */
+static void kquant_scale_min(const uint8_t *sc12, int j, int *S, int *M) {
+    if (j < 4) {
+        *S = sc12[j] & 63;
+        *M = sc12[j + 4] & 63;
+    } else {
+        *S = (sc12[j + 4] & 15) | ((sc12[j - 4] >> 6) << 4);
+        *M = (sc12[j + 4] >> 4) | ((sc12[j] >> 6) << 4);
+    }
+}
+
+void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double *A, double *B) {
+    int QK = or_block_elems(fmt);
+    for (int e = 0; e < QK; ++e) {
+        int u = e / 32;        /* 32-element unit (= one activation block) */
+        int code = 0;          /* contract code c_e                        */
+        double a = 0, b = 0;   /* w_e = a * c_e - b                        */
+        switch (fmt) {
+        case OR_Q8_0: {
+            a = rd_half(blk);
+            code = (int8_t)blk[2 + e];
+            break;
+        }
+        case OR_Q4_0: {
+            a = rd_half(blk);
+            int nib = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);
+            code = nib - 8;
+            break;
+        }
+        case OR_Q4_K:
+        case OR_Q5_K: {
+            double d = rd_half(blk), dmin = rd_half(blk + 2);
+            const uint8_t *sc12 = blk + 4;
+            const uint8_t *qh = blk + 16;                       /* Q5_K only */
+            const uint8_t *qs = blk + (fmt == OR_Q4_K ? 16 : 48);
+            int j = e / 32, l = e % 32, S, M;
+            kquant_scale_min(sc12, j, &S, &M);
+            int byte = qs[32 * (j / 2) + l];
+            int nib = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
+            if (fmt == OR_Q5_K) nib += 16 * ((qh[l] >> j) & 1);
+            code = nib;
+            a = d * S;
+            b = dmin * M;
+            break;
+        }
+        case OR_Q6_K: {
+            const uint8_t *ql = blk, *qh = blk + 128;
+            const int8_t *sc = (const int8_t *)(blk + 192);
+            double d = rd_half(blk + 208);
+            int h = e / 128, r = e % 128, l = r % 32, t = r / 32;
+            int lbyte = ql[64 * h + l + 32 * (t & 1)];
+            int low4 = (t < 2) ? (lbyte & 15) : (lbyte >> 4);
+            int hi2 = (qh[32 * h + l] >> (2 * t)) & 3;
+            int q6 = low4 | (hi2 << 4);
+            code = sc[e / 16] * (q6 - 32);
+            a = d;
+            break;
+        }
+        case OR_IQ4_XS: {
+            double d = rd_half(blk);
+            int scales_h = rd_u16(blk + 2);
+            const uint8_t *scales_l = blk + 4, *qs = blk + 8;
+            int ib = e / 32, j = e % 32;
+            int ls = ((scales_l[ib / 2] >> (4 * (ib % 2))) & 15) | (((scales_h >> (2 * ib)) & 3) << 4);
+            int byte = qs[16 * ib + (j % 16)];
+            int idx = (j < 16) ? (byte & 15) : (byte >> 4);
+            code = kIQ4NL[idx];
+            a = d * (ls - 32);
+            break;
+        }
+        default:
+            return;
+        }
+        if (w) w[e] = a * code - b;
+        if (c) c[e] = code;
+        if (e % 32 == 0) {
+            if (A) A[u] = a;
+            if (B) B[u] = b;
+        }
+    }
+}
+
+void or_dequant_matrix(int fmt, const uint8_t *W, int N, int K, double *out) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b)
+            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, out + (size_t)n * K + (size_t)b * QK,
+                            NULL, NULL, NULL);
+}
+
+/* Activation quantization, one 32-element block at a time.  The page names the
+ * activation format "Q8_F32S" only; the per-32 block, the fp32 scale, round half
+ * away from zero and true division are the readings taken here. */
+void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs) {
+    int nb = K / 32;
+    for (int m = 0; m < M; ++m) {
+        for (int b = 0; b < nb; ++b) {
+            const float *xb = x + (size_t)m * K + (size_t)b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(xb[i]);
+                if (a > amax) amax = a;
+            }
+            float d = amax / 127.0f;                /* fp32, round to nearest even */
+            int32_t s = 0;
+            for (int i = 0; i < 32; ++i) {
+                int q = 0;
+                if (d != 0.0f) {
+                    float v = xb[i] / d;            /* fp32 IEEE division */
+                    q = (int)roundf(v);             /* half away from zero */
+                    if (q > 127) q = 127;
+                    if (q < -127) q = -127;
+                }
+                xq[(size_t)m * K + (size_t)b * 32 + i] = (int8_t)q;
+                s += q;
+            }
+            xd[(size_t)m * nb + b] = d;
+            xs[(size_t)m * nb + b] = s;
+        }
+    }
+}
+
+static int has_min_term(int fmt) { return fmt == OR_Q4_K || fmt == OR_Q5_K; }
+
+void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *xs,
+                   int N, int K, int M, int32_t *dots, int32_t *aux) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
+    int upb = QK / 32;
+#pragma omp parallel for schedule(static) num_threads(or_get_threads())
+    for (int n = 0; n < N; ++n) {
+        int32_t c[256];
+        for (int b = 0; b < nb; ++b) {
+            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, NULL, NULL);
+            for (int ub = 0; ub < upb; ++ub) {
+                int u = b * upb + ub;
+                for (int m = 0; m < M; ++m) {
+                    const int8_t *q = xq + (size_t)m * K + (size_t)u * 32;
+                    int32_t dot = 0;
+                    for (int i = 0; i < 32; ++i) dot += c[ub * 32 + i] * (int32_t)q[i];
+                    size_t o = ((size_t)m * N + n) * nu + u;
+                    dots[o] = dot;
+                    if (aux) aux[o] = has_min_term(fmt) ? xs[(size_t)m * nu + u] : 0;
+                }
+            }
+        }
+    }
+}
+
+void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, const int32_t *xs,
+               int N, int K, int M, double *y) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
+    int upb = QK / 32;
+#pragma omp parallel for schedule(static) num_threads(or_get_threads())
+    for (int n = 0; n < N; ++n) {
+        int32_t c[256];
+        double A[8], B[8];
+        for (int m = 0; m < M; ++m) y[(size_t)m * N + n] = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, A, B);
+            for (int ub = 0; ub < upb; ++ub) {
+                int u = b * upb + ub;
+                for (int m = 0; m < M; ++m) {
+                    const int8_t *q = xq + (size_t)m * K + (size_t)u * 32;
+                    int32_t dot = 0;
+                    for (int i = 0; i < 32; ++i) dot += c[ub * 32 + i] * (int32_t)q[i];
+                    double d_x = xd[(size_t)m * nu + u];
+                    double s_x = xs[(size_t)m * nu + u];
+                    y[(size_t)m * N + n] += d_x * (A[ub] * (double)dot - B[ub] * s_x);
+                }
+            }
+        }
+    }
+}
+
+void or_gemv_deq(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
+                 int N, int K, int M, double *y) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
+#pragma omp parallel for schedule(static) num_threads(or_get_threads())
+    for (int n = 0; n < N; ++n) {
+        double w[256];
+        for (int m = 0; m < M; ++m) y[(size_t)m * N + n] = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, w, NULL, NULL, NULL);
+            for (int e = 0; e < QK; ++e) {
+                int k = b * QK + e;
+                for (int m = 0; m < M; ++m) {
+                    double xhat = (double)xq[(size_t)m * K + k] * (double)xd[(size_t)m * nu + k / 32];
+                    y[(size_t)m * N + n] += w[e] * xhat;
+                }
+            }
+        }
+    }
+}
+
+void or_absdot(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
+               int N, int K, int M, double *sabs) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
+#pragma omp parallel for schedule(static) num_threads(or_get_threads())
+    for (int n = 0; n < N; ++n) {
+        double w[256];
+        for (int m = 0; m < M; ++m) sabs[(size_t)m * N + n] = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, w, NULL, NULL, NULL);
+            for (int e = 0; e < QK; ++e) {
+                int k = b * QK + e;
+                for (int m = 0; m < M; ++m) {
+                    double xhat = (double)xq[(size_t)m * K + k] * (double)xd[(size_t)m * nu + k / 32];
+                    sabs[(size_t)m * N + n] += fabs(w[e] * xhat);
+                }
+            }
+        }
+    }
+}
+
+void or_gemv(int fmt, const uint8_t *W, const float *x, int N, int K, int M, double *y) {
+    int8_t *xq = (int8_t *)malloc((size_t)M * K);
+    float *xd = (float *)malloc(sizeof(float) * (size_t)M * (K / 32));
+    int32_t *xs = (int32_t *)malloc(sizeof(int32_t) * (size_t)M * (K / 32));
+    or_quantize_act(x, M, K, xq, xd, xs);
+    or_gemv_q(fmt, W, xq, xd, xs, N, K, M, y);
+    free(xq);
+    free(xd);
+    free(xs);
+}
+
+void or_router(const float *x, int M, int H, const float *Wr, int E, int topk,
+               double *logits, double *probs, int32_t *ids, double *w) {
+    double *l = (double *)malloc(sizeof(double) * E);
+    double *p = (double *)malloc(sizeof(double) * E);
+    char *taken = (char *)malloc(E);
+    for (int m = 0; m < M; ++m) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int k = 0; k < H; ++k) acc += (double)Wr[(size_t)e * H + k] * (double)x[(size_t)m * H + k];
+            l[e] = acc;
+        }
+        double lmax = l[0];
+        for (int e = 1; e < E; ++e) if (l[e] > lmax) lmax = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - lmax); z += p[e]; }
+        for (int e = 0; e < E; ++e) p[e] /= z;
+        if (logits) for (int e = 0; e < E; ++e) logits[(size_t)m * E + e] = l[e];
+        if (probs) for (int e = 0; e < E; ++e) probs[(size_t)m * E + e] = p[e];
+        /* top-k by repeated selection of the largest remaining probability; a tie
+         * keeps the lower expert id because only a strictly larger value replaces it */
+        memset(taken, 0, E);
+        double wsum = 0.0;
+        for (int s = 0; s < topk; ++s) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || p[e] > p[best])) best = e;
+            taken[best] = 1;
+            ids[(size_t)m * topk + s] = best;
+            w[(size_t)m * topk + s] = p[best];
+            wsum += p[best];
+        }
+        for (int s = 0; s < topk; ++s) w[(size_t)m * topk + s] /= wsum;
+    }
+    free(l);
+    free(p);
+    free(taken);
+}
+
+double or_swiglu(double g, double u) { return g * u / (1.0 + exp(-g)); }
+
+static size_t matrix_bytes(int fmt, int rows, int cols) {
+    return (size_t)rows * (size_t)(cols / or_block_elems(fmt)) * (size_t)or_block_bytes(fmt);
+}
+
+void or_moe_gateup(int fmt, const float *x, int M, int H, int E, int topk, int I,
+                   const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
+                   const uint8_t *Wg_sh, const uint8_t *Wu_sh,
+                   double *g, double *u, double *h) {
+    (void)E;
+    int S = topk + 1;
+    size_t eb = matrix_bytes(fmt, I, H);
+    int8_t *xq = (int8_t *)malloc((size_t)H);
+    float *xd = (float *)malloc(sizeof(float) * (H / 32));
+    int32_t *xs = (int32_t *)malloc(sizeof(int32_t) * (H / 32));
+    double *gg = (double *)malloc(sizeof(double) * I);
+    double *uu = (double *)malloc(sizeof(double) * I);
+    for (int m = 0; m < M; ++m) {
+        or_quantize_act(x + (size_t)m * H, 1, H, xq, xd, xs);   /* x quantized once per token */
+        for (int s = 0; s < S; ++s) {
+            const uint8_t *Wg = s < topk ? Wg_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wg_sh;
+            const uint8_t *Wu = s < topk ? Wu_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wu_sh;
+            or_gemv_q(fmt, Wg, xq, xd, xs, I, H, 1, gg);
+            or_gemv_q(fmt, Wu, xq, xd, xs, I, H, 1, uu);
+            for (int j = 0; j < I; ++j) {
+                size_t o = ((size_t)m * S + s) * I + j;
+                if (g) g[o] = gg[j];
+                if (u) u[o] = uu[j];
+                if (h) h[o] = or_swiglu(gg[j], uu[j]);
+            }
+        }
+    }
+    free(xq); free(xd); free(xs); free(gg); free(uu);
+}
+
+void or_requant(const double *h, int R, int I, int8_t *hq, float *hd, int32_t *hs) {
+    float *hf = (float *)malloc(sizeof(float) * (size_t)R * I);
+    for (size_t i = 0; i < (size_t)R * I; ++i) hf[i] = (float)h[i];   /* round to nearest fp32 */
+    or_quantize_act(hf, R, I, hq, hd, hs);
+    free(hf);
+}
+
+void or_moe_down(int fmt, int M, int H, int E, int topk, int I,
+                 const int32_t *ids, const double *w,
+                 const int8_t *hq, const float *hd, const int32_t *hs,
+                 const uint8_t *Wd_exps, const uint8_t *Wd_sh,
+                 double *y, double *o, double *yabs) {
+    (void)E;
+    int S = topk + 1, nu = I / 32;
+    size_t eb = matrix_bytes(fmt, H, I);
+    double *oo = (double *)malloc(sizeof(double) * H);
+    double *aa = (double *)malloc(sizeof(double) * H);
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < H; ++n) {
+            y[(size_t)m * H + n] = 0.0;
+            if (yabs) yabs[(size_t)m * H + n] = 0.0;
+        }
+        for (int s = 0; s < S; ++s) {
+            const uint8_t *Wd = s < topk ? Wd_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wd_sh;
+            double ws = s < topk ? w[(size_t)m * topk + s] : 1.0;     /* shared expert: weight 1 */
+            size_t r = (size_t)m * S + s;
+            or_gemv_q(fmt, Wd, hq + r * I, hd + r * nu, hs + r * nu, H, I, 1, oo);
+            if (yabs) or_absdot(fmt, Wd, hq + r * I, hd + r * nu, H, I, 1, aa);
+            for (int n = 0; n < H; ++n) {
+                y[(size_t)m * H + n] += ws * oo[n];
+                if (o) o[r * H + n] = oo[n];
+                if (yabs) yabs[(size_t)m * H + n] += fabs(ws) * aa[n];
+            }
+        }
+    }
+    free(oo);
+    free(aa);
+}
+
+void or_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
+                const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
+                const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
+                double *y, int32_t *ids, double *w) {
+    int S = topk + 1;
+    or_router(x, M, H, Wr, E, topk, NULL, NULL, ids, w);
+    double *h = (double *)malloc(sizeof(double) * (size_t)M * S * I);
+    int8_t *hq = (int8_t *)malloc((size_t)M * S * I);
+    float *hd = (float *)malloc(sizeof(float) * (size_t)M * S * (I / 32));
+    int32_t *hs = (int32_t *)malloc(sizeof(int32_t) * (size_t)M * S * (I / 32));
+    or_moe_gateup(fmt, x, M, H, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh, NULL, NULL, h);
+    or_requant(h, M * S, I, hq, hd, hs);
+    or_moe_down(fmt, M, H, E, topk, I, ids, w, hq, hd, hs, Wd_exps, Wd_sh, y, NULL, NULL);
+    free(h); free(hq); free(hd); free(hs);
+}
+
+void or_ffn_sublayer(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,
+                     const float *x, int M, int H, int I,
+                     double *y, double *g, double *u, double *h) {
+    double *gg = (double *)malloc(sizeof(double) * (size_t)M * I);
+    double *uu = (double *)malloc(sizeof(double) * (size_t)M * I);
+    double *hh = (double *)malloc(sizeof(double) * (size_t)M * I);
+    int8_t *xq = (int8_t *)malloc((size_t)M * H);
+    float *xd = (float *)malloc(sizeof(float) * (size_t)M * (H / 32));
+    int32_t *xs = (int32_t *)malloc(sizeof(int32_t) * (size_t)M * (H / 32));
+    int8_t *hq = (int8_t *)malloc((size_t)M * I);
+    float *hd = (float *)malloc(sizeof(float) * (size_t)M * (I / 32));
+    int32_t *hs = (int32_t *)malloc(sizeof(int32_t) * (size_t)M * (I / 32));
+    or_quantize_act(x, M, H, xq, xd, xs);
+    or_gemv_q(fmt, Wg, xq, xd, xs, I, H, M, gg);
+    or_gemv_q(fmt, Wu, xq, xd, xs, I, H, M, uu);
+    for (size_t i = 0; i < (size_t)M * I; ++i) hh[i] = or_swiglu(gg[i], uu[i]);
+    or_requant(hh, M, I, hq, hd, hs);
+    or_gemv_q(fmt, Wd, hq, hd, hs, H, I, M, y);
+    if (g) memcpy(g, gg, sizeof(double) * (size_t)M * I);
+    if (u) memcpy(u, uu, sizeof(double) * (size_t)M * I);
+    if (h) memcpy(h, hh, sizeof(double) * (size_t)M * I);
+    free(gg); free(uu); free(hh); free(xq); free(xd); free(xs); free(hq); free(hd); free(hs);
+}

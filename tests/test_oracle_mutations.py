@@ -1,0 +1,76 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case edits one line of a copy of the oracle source (a dropped term, a wrong
+sign, a wrong or transposed index, the wrong rounding mode), compiles the copy on
+the CPU, and runs the pin tests against it: at least one pin must fail.  Nothing
+here touches the real oracle build or any GPU.
+"""
+import os
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+# (name, original text, mutated text)
+MUTATIONS = [
+    ("q4_0 offset", "code = nib - 8;", "code = nib - 7;"),
+    ("q8_0 scale field", "a = rd_half(blk);\n            code = (int8_t)blk[2 + e];",
+     "a = rd_half(blk + 1);\n            code = (int8_t)blk[2 + e];"),
+    ("q4_k high scale bits", "((sc12[j - 4] >> 6) << 4)", "((sc12[j - 4] >> 6) << 3)"),
+    ("q4_k min bits from wrong byte", "((sc12[j] >> 6) << 4)", "((sc12[j - 4] >> 6) << 4)"),
+    ("k-quant min term dropped", "b = dmin * M;", "b = 0;"),
+    ("k-quant nibble half swapped", "(j % 2 == 0) ? (byte & 15) : (byte >> 4)",
+     "(j % 2 == 1) ? (byte & 15) : (byte >> 4)"),
+    ("q5_k qh index transposed", "((qh[l] >> j) & 1)", "((qh[j] >> l) & 1)"),
+    ("q6_k ql half", "32 * (t & 1)", "32 * (t >> 1)"),
+    ("q6_k qh shift", "(2 * t)) & 3", "(t)) & 3"),
+    ("q6_k scale index", "sc[e / 16]", "sc[e / 32]"),
+    ("iq4 nibble order", "(j < 16) ? (byte & 15) : (byte >> 4)", "(j < 16) ? (byte >> 4) : (byte & 15)"),
+    ("iq4 scale offset", "a = d * (ls - 32);", "a = d * (ls - 31);"),
+    ("quant rounding mode", "q = (int)roundf(v);", "q = (int)rintf(v);"),
+    ("quant reciprocal", "float v = xb[i] / d;", "float v = xb[i] * (1.0f / d);"),
+    ("gemv min sign", "- B[ub] * s_x", "+ B[ub] * s_x"),
+    ("router tie order", "p[e] > p[best]", "p[e] >= p[best]"),
+    ("router no renorm", "w[(size_t)m * topk + s] /= wsum;", "w[(size_t)m * topk + s] /= 1.0;"),
+    ("swiglu sign", "1.0 + exp(-g)", "1.0 + exp(g)"),
+    ("shared expert weighted", "double ws = s < topk ? w[(size_t)m * topk + s] : 1.0;",
+     "double ws = s < topk ? w[(size_t)m * topk + s] : 0.5;"),
+    ("fp16 exponent bias", "expo - 25", "expo - 24"),
+]
+
+PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]
+
+
+def _run_pins(orc):
+    """Run every pin (all parametrizations); return the names of those that failed."""
+    failed = []
+    for name in PIN_TESTS:
+        fn = getattr(pins, name)
+        params = [None]
+        if "fmt" in fn.__code__.co_varnames[:fn.__code__.co_argcount]:
+            params = pins.FMTS
+        for p in params:
+            try:
+                fn(orc, p) if p is not None else fn(orc)
+            except (AssertionError, ValueError, IndexError, OverflowError):
+                failed.append(f"{name}[{p}]")
+            except Exception as exc:  # noqa: BLE001 - any exception is a caught mistake
+                failed.append(f"{name}[{p}]:{type(exc).__name__}")
+    return failed
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(tmp_path, name, orig, mut):
+    src = oracle.source_text()
+    assert src.count(orig) >= 1, f"mutation anchor not found: {orig!r}"
+    path = oracle.build_variant(src.replace(orig, mut, 1), os.path.join(str(tmp_path), "libvariant.so"))
+    with oracle.use_library(path):
+        failed = _run_pins(oracle)
+    assert failed, f"no pin caught the planted mistake '{name}'"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    path = oracle.build_variant(oracle.source_text(), os.path.join(str(tmp_path), "libvariant.so"))
+    with oracle.use_library(path):
+        assert _run_pins(oracle) == []
