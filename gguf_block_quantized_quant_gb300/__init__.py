@@ -1,0 +1,198 @@
+"""Python binding of libqg: decode GEMV on raw GGUF blocks for GB300 (sm_103a).
+
+Thin marshalling layer over the C ABI declared in ``include/qg.h``: every function here
+has the name of the C entry point it calls, takes torch CUDA tensors, passes their device
+pointers and the current CUDA stream, and raises ``QGError`` on a non-zero status.  All
+arithmetic runs in the library's CUDA kernels; PyTorch only provides device memory and
+streams.  If ``libqg.so`` has not been built, every call raises: there is no fallback.
+
+Block formats (GGUF type ids): Q4_0=2, Q8_0=8, Q4_K=12, Q5_K=13, Q6_K=14, IQ4_XS=23.
+A weight matrix of N rows and K columns is passed as a uint8 CUDA tensor holding the N
+rows of raw blocks back to back (``row_bytes(fmt, K)`` bytes per row).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_XS = 2, 8, 12, 13, 14, 23
+FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "IQ4_XS": IQ4_XS}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_XS: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_XS: 136}
+
+QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER = 1, 2, 3, 4
+QG_OK, QG_EINVAL, QG_EWORKSPACE, QG_EALIGN, QG_ECUDA, QG_EDEVICE = 0, -1, -2, -3, -4, -5
+WS_INVALID = ctypes.c_size_t(-1).value
+
+LIB_PATH = _build.LIB
+
+# every symbol declared in include/qg.h
+EXPORTS = ("qg_quantize_act", "qg_gemv", "qg_gemv_q", "qg_moe_ffn", "qg_ffn_sublayer", "qg_workspace_size",
+           "qg_moe_ws_layout", "qg_ffn_ws_layout", "qg_block_dots", "qg_device_error", "qg_strerror",
+           "qg_version")
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: status {status} ({strerror(status)})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if libqg.so is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libqg.so not found at {LIB_PATH}; build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()'). There is no CPU fallback.")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qg_quantize_act.argtypes = [P, I, I, P, P, P, P]
+        L.qg_gemv.argtypes = [I, P, P, P, I, I, I, P, S, P]
+        L.qg_gemv_q.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
+        L.qg_moe_ffn.argtypes = [I, P, I, I, P, I, I, P, P, P, P, P, P, I, P, P, P, P, S, P]
+        L.qg_ffn_sublayer.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
+        L.qg_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        L.qg_workspace_size.restype = S
+        L.qg_moe_ws_layout.argtypes = [I, I, I, I, I, ctypes.POINTER(S)]
+        L.qg_ffn_ws_layout.argtypes = [I, I, I, I, ctypes.POINTER(S)]
+        L.qg_block_dots.argtypes = [I, P, P, P, I, I, I, P, P, P]
+        L.qg_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        L.qg_strerror.argtypes = [I]
+        L.qg_strerror.restype = ctypes.c_char_p
+        L.qg_version.restype = I
+        for name in EXPORTS:
+            getattr(L, name)
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().qg_strerror(int(status)).decode()
+    except RuntimeError:
+        return "libqg not loaded"
+
+
+def row_bytes(fmt: int, K: int) -> int:
+    return (K // BLOCK_ELEMS[fmt]) * BLOCK_BYTES[fmt]
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libqg takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libqg takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise QGError(rc, what)
+
+
+def _ws(ws, nbytes: int, device):
+    if nbytes == WS_INVALID:
+        raise QGError(QG_EINVAL, "qg_workspace_size")
+    if ws is None and nbytes > 0:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, (0 if ws is None else ws.numel())
+
+
+# ----------------------------------------------------------------------------- entry points
+def qg_workspace_size(op: int, fmt: int, M: int, N: int, K: int, E: int = 0, topk: int = 0, I: int = 0) -> int:
+    return int(lib().qg_workspace_size(op, fmt, M, N, K, E, topk, I))
+
+
+def qg_quantize_act(x, xq=None, xd=None, xs=None, stream=None):
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
+    xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device) if xd is None else xd
+    xs = torch.empty((M, K // 32), dtype=torch.int32, device=x.device) if xs is None else xs
+    _check(lib().qg_quantize_act(_ptr(x), M, K, _ptr(xq), _ptr(xd), _ptr(xs), _stream(stream)),
+           "qg_quantize_act")
+    return xq, xd, xs
+
+
+def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
+    M, K = x.shape
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), x.device)
+    _check(lib().qg_gemv(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _ptr(ws), nws, _stream(stream)), "qg_gemv")
+    return y
+
+
+def qg_gemv_q(fmt: int, W, xq, xd, xs, N: int, y=None, ws=None, stream=None):
+    M, K = xq.shape
+    y = torch.empty((M, N), dtype=torch.float32, device=xq.device) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV_Q, fmt, M, N, K), xq.device)
+    _check(lib().qg_gemv_q(fmt, _ptr(W), _ptr(xq), _ptr(xd), _ptr(xs), _ptr(y), N, K, M, _ptr(ws), nws,
+                           _stream(stream)), "qg_gemv_q")
+    return y
+
+
+def qg_moe_ffn(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I: int,
+               y=None, topk_ids=None, topk_w=None, ws=None, stream=None):
+    M, H = x.shape
+    E = Wr.shape[0]
+    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), x.device)
+    _check(lib().qg_moe_ffn(fmt, _ptr(x), M, H, _ptr(Wr), E, topk, _ptr(Wg_exps), _ptr(Wu_exps), _ptr(Wd_exps),
+                            _ptr(Wg_sh), _ptr(Wu_sh), _ptr(Wd_sh), I, _ptr(y), _ptr(topk_ids), _ptr(topk_w),
+                            _ptr(ws), nws, _stream(stream)), "qg_moe_ffn")
+    return y
+
+
+def qg_ffn_sublayer(fmt: int, Wg, Wu, Wd, x, I: int, y=None, ws=None, stream=None):
+    M, H = x.shape
+    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), x.device)
+    _check(lib().qg_ffn_sublayer(fmt, _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(x), _ptr(y), M, H, I, _ptr(ws), nws,
+                                 _stream(stream)), "qg_ffn_sublayer")
+    return y
+
+
+def qg_moe_ws_layout(M: int, H: int, E: int, topk: int, I: int):
+    off = (ctypes.c_size_t * 7)()
+    _check(lib().qg_moe_ws_layout(M, H, E, topk, I, off), "qg_moe_ws_layout")
+    return list(off)
+
+
+def qg_ffn_ws_layout(fmt: int, M: int, H: int, I: int):
+    off = (ctypes.c_size_t * 3)()
+    _check(lib().qg_ffn_ws_layout(fmt, M, H, I, off), "qg_ffn_ws_layout")
+    return list(off)
+
+
+def qg_block_dots(fmt: int, W, xq, xs, N: int, stream=None):
+    M, K = xq.shape
+    dots = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
+    aux = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
+    _check(lib().qg_block_dots(fmt, _ptr(W), _ptr(xq), _ptr(xs), N, K, M, _ptr(dots), _ptr(aux), _stream(stream)),
+           "qg_block_dots")
+    return dots, aux
+
+
+def qg_device_error() -> int:
+    v = ctypes.c_uint(0)
+    _check(lib().qg_device_error(ctypes.byref(v)), "qg_device_error")
+    return int(v.value)
+
+
+def qg_version() -> int:
+    return int(lib().qg_version())

@@ -1,0 +1,349 @@
+// qg_abi.cu -- the extern "C" boundary of libqg (declared in include/qg.h) and the
+// format-independent kernels: activation quantization, split-K reduction, router logits.
+//
+// The boundary follows "01 · 阶段总览：从 2B 到 8B 再到 MoE", section 一: a pure C ABI module
+// whose device call reports one status (0 = done on the GPU).  The page's host-side
+// mapping of a failure to "the caller runs the CPU path" is deliberately not reproduced:
+// a failure is returned as a negative status and nothing runs elsewhere.
+#include <mutex>
+
+#include "../../include/qg.h"
+#include "qg_jobs.cuh"
+#include "qg_launch.h"
+
+namespace qg {
+
+// ----------------------------------------------------------------------------- kernels
+// One warp per 32-element block (see quant_block_warp).
+__global__ void __launch_bounds__(256) quant_act_kernel(const float *x, int M, int K, long ldx, int8_t *xq,
+                                                        float *xd, int32_t *xs) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32;
+    const long total = (long)M * nb;
+    const long wpg = (long)gridDim.x * (blockDim.x >> 5);
+    for (long w = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += wpg) {
+        const int m = (int)(w / nb), b = (int)(w % nb);
+        const float v = x[(long)m * ldx + 32 * b + lane];
+        int q, s;
+        float d;
+        quant_block_warp(v, q, d, s);
+        xq[(long)m * K + 32 * b + lane] = (int8_t)q;
+        if (lane == 0) {
+            xd[(long)m * nb + b] = d;
+            xs[(long)m * nb + b] = s;
+        }
+    }
+}
+
+// y[i] = sum over the K-slices in slice order.
+__global__ void splitk_reduce_kernel(const float *part, int KS, long MN, float *y) {
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < MN; i += (long)gridDim.x * blockDim.x) {
+        float s = 0.0f;
+        for (int k = 0; k < KS; ++k) s += part[(long)k * MN + i];
+        y[i] = s;
+    }
+}
+
+// logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32, one warp per expert row.
+__global__ void __launch_bounds__(256) router_logits_kernel(const float *x, int M, int H, const float *Wr, int E,
+                                                            float *logits) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= E) return;
+    float acc[M_MAX];
+#pragma unroll
+    for (int m = 0; m < M_MAX; ++m) acc[m] = 0.0f;
+    const float *wr = Wr + (long)e * H;
+    for (int k = lane; k < H; k += 32) {
+        const float wv = __ldg(wr + k);
+#pragma unroll
+        for (int m = 0; m < M_MAX; ++m)
+            if (m < M) acc[m] = fmaf(wv, __ldg(x + (long)m * H + k), acc[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < M_MAX; ++m) {
+        if (m < M) {
+            const float v = warp_sum(acc[m]);
+            if (lane == 0) logits[(long)m * E + e] = v;
+        }
+    }
+}
+
+int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *xd, int32_t *xs, cudaStream_t s) {
+    const long blocks = (long)M * (K / 32);
+    const int grid = (int)std::min<long>((blocks + 7) / 8, 4096);
+    quant_act_kernel<<<grid, 256, 0, s>>>(x, M, K, ldx, xq, xd, xs);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
+int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStream_t s) {
+    const int grid = (int)std::min<long>((MN + 255) / 256, 1024);
+    splitk_reduce_kernel<<<grid, 256, 0, s>>>(part, KS, MN, y);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
+int launch_router_logits(const float *x, int M, int H, const float *Wr, int E, float *logits, cudaStream_t s) {
+    router_logits_kernel<<<(E + 7) / 8, 256, 0, s>>>(x, M, H, Wr, E, logits);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
+// ----------------------------------------------------------------------------- host helpers
+namespace {
+
+struct DevCache {
+    std::mutex mu;
+    int sms[64] = {};
+    int ok[64] = {};  // 0 unknown, 1 supported, -1 not an sm_103 device
+};
+DevCache g_dev;
+
+// SM count of the current device, or a negative status.
+int current_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QG_ECUDA;
+    if (dev < 0 || dev >= 64) return QG_EDEVICE;
+    std::lock_guard<std::mutex> lock(g_dev.mu);
+    if (g_dev.ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QG_ECUDA;
+        g_dev.ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_dev.sms[dev] = sms;
+    }
+    return g_dev.ok[dev] == 1 ? g_dev.sms[dev] : QG_EDEVICE;
+}
+
+// SM count for planning when no device is usable (workspace queries on any host).
+int planning_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+        return sms;
+    cudaGetLastError();
+    return G_PLAN;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+template <class Fn>
+int by_format(int fmt, Fn &&fn) {
+    switch (fmt) {
+    case QG_Q4_0: return fn(std::integral_constant<int, QG_Q4_0>{});
+    case QG_Q8_0: return fn(std::integral_constant<int, QG_Q8_0>{});
+    case QG_Q4_K: return fn(std::integral_constant<int, QG_Q4_K>{});
+    case QG_Q5_K: return fn(std::integral_constant<int, QG_Q5_K>{});
+    case QG_Q6_K: return fn(std::integral_constant<int, QG_Q6_K>{});
+    case QG_IQ4_XS: return fn(std::integral_constant<int, QG_IQ4_XS>{});
+    default: return QG_EINVAL;
+    }
+}
+
+bool shape_ok(int fmt, int K) {
+    FmtInfo f;
+    return fmt_info(fmt, f) && K >= f.qk && K % f.qk == 0;
+}
+
+}  // namespace
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+int qg_version(void) { return 100; }
+
+const char *qg_strerror(int status) {
+    switch (status) {
+    case QG_OK: return "ok";
+    case QG_EINVAL: return "invalid argument (format, shape, token count, pointer or top-k)";
+    case QG_EWORKSPACE: return "workspace missing or smaller than qg_workspace_size()";
+    case QG_EALIGN: return "pointer alignment (W and ws: 16 bytes; activations and outputs: 4 bytes)";
+    case QG_ECUDA: return "CUDA runtime error or kernel launch failure";
+    case QG_EDEVICE: return "current device is not an sm_103 (GB300-class) GPU";
+    default: return "unknown status";
+    }
+}
+
+int qg_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs, void *stream) {
+    if (!x || !xq || !xd || !xs || M < 1 || K < 32 || K % 32) return QG_EINVAL;
+    if (!aligned(x, 4) || !aligned(xd, 4) || !aligned(xs, 4)) return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    return launch_quant_act(x, M, K, K, xq, xd, xs, (cudaStream_t)stream);
+}
+
+size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, int I) {
+    const size_t bad = (size_t)-1;
+    switch (op) {
+    case QG_OP_GEMV:
+    case QG_OP_GEMV_Q: {
+        const GemvPlan p = plan_gemv(fmt, N, K, M, op == QG_OP_GEMV_Q, planning_sms());
+        return p.ok ? p.ws_total : bad;
+    }
+    case QG_OP_MOE_FFN: {
+        const MoePlan p = plan_moe(fmt, M, K, E, topk, I, planning_sms());
+        return p.ok ? p.ws_total : bad;
+    }
+    case QG_OP_FFN_SUBLAYER: {
+        const FfnPlan p = plan_ffn(fmt, M, K, I, planning_sms());
+        return p.ok ? p.ws_total : bad;
+    }
+    default: return bad;
+    }
+}
+
+static int gemv_common(int fmt, const void *W, const float *x, const int8_t *xq, const float *xd,
+                       const int32_t *xs, float *y, int N, int K, int M, void *ws, size_t ws_bytes, void *stream) {
+    if (!W || !y || N < 1 || M < 1 || M > M_MAX || !shape_ok(fmt, K)) return QG_EINVAL;
+    if (!x && (!xq || !xd || !xs)) return QG_EINVAL;
+    if (!aligned(W, 16) || !aligned(y, 4) || (ws && !aligned(ws, 16))) return QG_EALIGN;
+    if (x && !aligned(x, 4)) return QG_EALIGN;
+    if (!x && (!aligned(xq, 16) || !aligned(xd, 4) || !aligned(xs, 4))) return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    GemvCall c{};
+    c.W = static_cast<const uint8_t *>(W);
+    c.N = N;
+    c.K = K;
+    c.M = M;
+    c.x = x;
+    c.xq = x ? nullptr : xq;
+    c.xd = x ? nullptr : xd;
+    c.xs = x ? nullptr : xs;
+    c.y = y;
+    c.ws = static_cast<uint8_t *>(ws);
+    c.ws_bytes = ws ? ws_bytes : 0;
+    c.stream = (cudaStream_t)stream;
+    return by_format(fmt, [&](auto F) { return gemv_run<decltype(F)::value>(c, sms); });
+}
+
+int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M, void *ws, size_t ws_bytes,
+            void *stream) {
+    if (!x) return QG_EINVAL;
+    return gemv_common(fmt, W_blocks, x, nullptr, nullptr, nullptr, y, N, K, M, ws, ws_bytes, stream);
+}
+
+int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, const int32_t *xs, float *y, int N,
+              int K, int M, void *ws, size_t ws_bytes, void *stream) {
+    if (!xq || !xd || !xs) return QG_EINVAL;
+    return gemv_common(fmt, W_blocks, nullptr, xq, xd, xs, y, N, K, M, ws, ws_bytes, stream);
+}
+
+int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd, const float *x, float *y, int M, int H,
+                    int I, void *ws, size_t ws_bytes, void *stream) {
+    if (!Wg || !Wu || !Wd || !x || !y || M < 1 || M > M_MAX || !shape_ok(fmt, H) || !shape_ok(fmt, I))
+        return QG_EINVAL;
+    if (!ws) return QG_EWORKSPACE;
+    if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(ws, 16) || !aligned(x, 4) ||
+        !aligned(y, 4))
+        return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    FfnCall c{};
+    c.Wg = static_cast<const uint8_t *>(Wg);
+    c.Wu = static_cast<const uint8_t *>(Wu);
+    c.Wd = static_cast<const uint8_t *>(Wd);
+    c.x = x;
+    c.y = y;
+    c.M = M;
+    c.H = H;
+    c.I = I;
+    c.ws = static_cast<uint8_t *>(ws);
+    c.ws_bytes = ws_bytes;
+    c.stream = (cudaStream_t)stream;
+    return by_format(fmt, [&](auto F) { return ffn_run<decltype(F)::value>(c, sms); });
+}
+
+int qg_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk, const void *Wg_exps,
+               const void *Wu_exps, const void *Wd_exps, const void *Wg_sh, const void *Wu_sh, const void *Wd_sh,
+               int I, float *y, int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+    if (!x || !Wr || !Wg_exps || !Wu_exps || !Wd_exps || !Wg_sh || !Wu_sh || !Wd_sh || !y) return QG_EINVAL;
+    if (M < 1 || M > M_MAX || E < 1 || E > E_MAX || topk < 1 || topk > TOPK_MAX || topk > E) return QG_EINVAL;
+    if (!shape_ok(fmt, H) || !shape_ok(fmt, I)) return QG_EINVAL;
+    if (!ws) return QG_EWORKSPACE;
+    const void *w16[] = {Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, ws};
+    for (const void *p : w16)
+        if (!aligned(p, 16)) return QG_EALIGN;
+    if (!aligned(x, 4) || !aligned(Wr, 4) || !aligned(y, 4) || (topk_ids && !aligned(topk_ids, 4)) ||
+        (topk_w && !aligned(topk_w, 4)))
+        return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    MoeCall c{};
+    c.x = x;
+    c.M = M;
+    c.H = H;
+    c.Wr = Wr;
+    c.E = E;
+    c.topk = topk;
+    c.Wg_exps = static_cast<const uint8_t *>(Wg_exps);
+    c.Wu_exps = static_cast<const uint8_t *>(Wu_exps);
+    c.Wd_exps = static_cast<const uint8_t *>(Wd_exps);
+    c.Wg_sh = static_cast<const uint8_t *>(Wg_sh);
+    c.Wu_sh = static_cast<const uint8_t *>(Wu_sh);
+    c.Wd_sh = static_cast<const uint8_t *>(Wd_sh);
+    c.I = I;
+    c.y = y;
+    c.ids_out = topk_ids;
+    c.w_out = topk_w;
+    c.ws = static_cast<uint8_t *>(ws);
+    c.ws_bytes = ws_bytes;
+    c.stream = (cudaStream_t)stream;
+    return by_format(fmt, [&](auto F) { return moe_run<decltype(F)::value>(c, sms); });
+}
+
+int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]) {
+    if (!off) return QG_EINVAL;
+    // the layout does not depend on the block format or the SM count
+    const MoePlan p = plan_moe(QG_Q8_0, M, H, E, topk, I, G_PLAN);
+    if (!p.ok) return QG_EINVAL;
+    off[0] = p.ws_g;
+    off[1] = p.ws_u;
+    off[2] = p.ws_h;
+    off[3] = p.ws_hq;
+    off[4] = p.ws_hd;
+    off[5] = p.ws_hs;
+    off[6] = p.ws_logits;
+    return QG_OK;
+}
+
+int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]) {
+    if (!off) return QG_EINVAL;
+    const FfnPlan p = plan_ffn(fmt, M, H, I, G_PLAN);
+    if (!p.ok) return QG_EINVAL;
+    off[0] = p.ws_g;
+    off[1] = p.ws_u;
+    off[2] = p.ws_h;
+    return QG_OK;
+}
+
+int qg_block_dots(int fmt, const void *W, const int8_t *xq, const int32_t *xs, int N, int K, int M, int32_t *dots,
+                  int32_t *aux, void *stream) {
+    if (!W || !xq || !xs || !dots || !aux || N < 1 || M < 1 || M > M_MAX || !shape_ok(fmt, K)) return QG_EINVAL;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(xs, 4) || !aligned(dots, 4) || !aligned(aux, 4))
+        return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    DotsCall c{static_cast<const uint8_t *>(W), xq, xs, N, K, M, dots, aux, (cudaStream_t)stream};
+    return by_format(fmt, [&](auto F) { return dots_run<decltype(F)::value>(c); });
+}
+
+int qg_device_error(unsigned int *err) {
+    if (!err) return QG_EINVAL;
+    unsigned int v = 0, zero = 0, all = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qg_dev_err, sizeof(v)) != cudaSuccess) return QG_ECUDA;
+    if (cudaMemcpyToSymbol(g_qg_dev_err, &zero, sizeof(zero)) != cudaSuccess) return QG_ECUDA;
+    all |= v;
+    const int fmts[] = {QG_Q4_0, QG_Q8_0, QG_Q4_K, QG_Q5_K, QG_Q6_K, QG_IQ4_XS};
+    for (int f : fmts) {
+        const int rc = by_format(f, [&](auto F) { return dev_err_take<decltype(F)::value>(&v); });
+        if (rc) return rc;
+        all |= v;
+    }
+    *err = all;
+    return QG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// qg_launch.h -- host interface between the C ABI (qg_abi.cu) and the per-format
+// launchers (qg_fmt.cu, compiled once per block format).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qg_plan.h"
+
+namespace qg {
+
+struct GemvCall {
+    const uint8_t *W;
+    int N, K, M;
+    const float *x;     // fp32 activations, or NULL when xq/xd/xs are given
+    const int8_t *xq;
+    const float *xd;
+    const int32_t *xs;
+    float *y;
+    uint8_t *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+struct FfnCall {
+    const uint8_t *Wg, *Wu, *Wd;
+    const float *x;
+    float *y;
+    int M, H, I;
+    uint8_t *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+struct MoeCall {
+    const float *x;
+    int M, H;
+    const float *Wr;
+    int E, topk;
+    const uint8_t *Wg_exps, *Wu_exps, *Wd_exps, *Wg_sh, *Wu_sh, *Wd_sh;
+    int I;
+    float *y;
+    int32_t *ids_out;
+    float *w_out;
+    uint8_t *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+struct DotsCall {
+    const uint8_t *W;
+    const int8_t *xq;
+    const int32_t *xs;
+    int N, K, M;
+    int32_t *dots, *aux;
+    cudaStream_t stream;
+};
+
+// Per-format launchers (status codes as in qg.h).
+template <int FMT>
+int gemv_run(const GemvCall &c, int sms);
+template <int FMT>
+int gemv_run_planned(const GemvPlan &p, const GemvCall &c);
+template <int FMT>
+int ffn_run(const FfnCall &c, int sms);
+template <int FMT>
+int moe_run(const MoeCall &c, int sms);
+template <int FMT>
+int dots_run(const DotsCall &c);
+template <int FMT>
+int dev_err_take(unsigned int *err);  // read and clear the format's device error word
+
+// Format-independent kernels (qg_abi.cu).
+int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *xd, int32_t *xs,
+                     cudaStream_t s);
+int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStream_t s);
+int launch_router_logits(const float *x, int M, int H, const float *Wr, int E, float *logits, cudaStream_t s);
+
+}  // namespace qg

@@ -1,0 +1,162 @@
+/*
+ * qg.h -- C ABI of libqg: decode-time GEMV computed in place on raw GGUF blocks,
+ * with activations quantized on the GPU, plus the MoE FFN and the FFN sublayer
+ * built from the same kernels.  Target: NVIDIA GB300 (sm_103a), one GPU.
+ *
+ * Sources (Chinese web pages, cited by title and section):
+ *  [D27] "为什么专家缓存救不了稠密模型：16GB 显存跑 27B Dense 模型的推理优化实践"
+ *        (xhh.club): section "原位量化计算与单流融合的实际收益" and the Q&A
+ *        "如何让CUDA直接计算GGUF混合量化块而不展开为FP16？" -- GEMV directly on the
+ *        GGUF blocks with no FP16 copy of W; activations quantized on the GPU to
+ *        "Q8_F32S"; int8 dot products; K-quant correction term; I-quant codebook
+ *        in registers; FFN sublayer on one stream with a reused workspace.
+ *  [A3B] "参悟llama.cpp中的Qwen3.6-35B-A3B" (cnblogs), section 1.1: 256 experts,
+ *        8 routed + 1 shared active per token, expert inter size 512, hidden 2048.
+ *  [KES] "01 · 阶段总览：从 2B 到 8B 再到 MoE" (icman.com.cn): section 一 (a pure
+ *        C ABI module whose device call returns 0 on success), section 二 issue ⑦
+ *        (no cudaFree on the hot path: reuse buffers), section 四 issue ⑪ (router ->
+ *        top-k -> expert gate/up -> swiglu -> down, weighted aggregation).
+ *
+ * Conventions for every call below:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates, frees or synchronizes; each call only validates its arguments on the
+ *    host and enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Results are ready when the stream reaches them.
+ *  - Return value: QG_OK (0) or a negative QG_E* status.  Every argument check happens
+ *    on the host before any launch, so a failed call has enqueued nothing.  There is no
+ *    CPU fallback: a GPU problem is reported, never silently computed elsewhere.
+ *  - Layouts: x is M x K fp32 row-major; y is M x N fp32 row-major.  A weight matrix
+ *    W with N rows and K columns is N rows of K/QK blocks each, rows contiguous, no
+ *    padding, raw GGUF byte order (QK = 32 for Q4_0/Q8_0, 256 for the others).  Expert
+ *    tensors are E such matrices stacked contiguously.
+ *  - Alignment: W and ws must be 16-byte aligned (QG_EALIGN otherwise); x, y and the
+ *    quantized-activation arrays must be 4-byte aligned.
+ *  - Limits: 1 <= M <= 16 tokens; K a positive multiple of the block size; N >= 1.
+ *  - The workspace `ws` (device, caller-owned, >= qg_workspace_size(...) bytes) may be
+ *    reused by back-to-back calls on the same stream; concurrent calls on different
+ *    streams need separate workspaces.
+ */
+#ifndef QG_H
+#define QG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Block formats, numbered by their GGUF type ids. */
+enum qg_format {
+    QG_Q4_0 = 2,    /* 32 elements, 18 B: fp16 d, 16 B of 4-bit codes; w = d*(c-8)           */
+    QG_Q8_0 = 8,    /* 32 elements, 34 B: fp16 d, 32 int8 codes; w = d*q                     */
+    QG_Q4_K = 12,   /* 256 elements, 144 B: fp16 d, dmin, 8 x 6-bit scale/min, 4-bit codes   */
+    QG_Q5_K = 13,   /* 256 elements, 176 B: as Q4_K plus one high bit per code              */
+    QG_Q6_K = 14,   /* 256 elements, 210 B: 6-bit codes, 16 int8 sub-scales, fp16 d          */
+    QG_IQ4_XS = 23  /* 256 elements, 136 B: fp16 d, 6-bit sub-scales, 4-bit codebook indices */
+};
+
+/* Status codes. */
+enum qg_status {
+    QG_OK = 0,
+    QG_EINVAL = -1,     /* bad format, shape, token count, pointer or top-k           */
+    QG_EWORKSPACE = -2, /* ws is NULL or ws_bytes is below qg_workspace_size()         */
+    QG_EALIGN = -3,     /* a pointer breaks the alignment rule above                   */
+    QG_ECUDA = -4,      /* a CUDA runtime call or kernel launch failed                 */
+    QG_EDEVICE = -5     /* the current device is not an sm_103 GPU the library targets */
+};
+
+/* Operations for qg_workspace_size(). */
+enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBLAYER = 4 };
+
+/* Activation quantization "Q8_F32S" [D27 Q&A]: for each token m and each 32-element
+ * block b of K, d = amax|x| / 127 (fp32, IEEE division), q = clamp(roundf(x / d),
+ * -127, 127) with round-half-away-from-zero (all q = 0 and d = 0 for an all-zero
+ * block), s = sum of the 32 codes.
+ *   x:  M x K fp32.   xq: M x K int8.   xd: M x K/32 fp32.   xs: M x K/32 int32.
+ * K must be a multiple of 32. */
+int qg_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs, void *stream);
+
+/* y = W x for M tokens [D27 Q&A; KES section 一]: x is quantized on the GPU as by
+ * qg_quantize_act (inside the GEMV kernel when it fits in shared memory, else into ws),
+ * then each 32-element unit contributes
+ *   Q8_0, Q4_0, Q6_K, IQ4_XS:  y += d_unit * xd * dot
+ *   Q4_K, Q5_K:                y += xd * (d*S_j * dot - dmin*M_j * xs)
+ * where dot is the exact int32 sum of weight codes times activation codes.
+ *   fmt: qg_format.  W: N x K blocks.  x: M x K fp32.  y: M x N fp32 (overwritten). */
+int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
+            void *ws, size_t ws_bytes, void *stream);
+
+/* Same as qg_gemv with the activations already quantized (xq, xd, xs laid out as
+ * produced by qg_quantize_act). */
+int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, const int32_t *xs,
+              float *y, int N, int K, int M, void *ws, size_t ws_bytes, void *stream);
+
+/* MoE FFN for M tokens [KES section 四 ⑪; A3B section 1.1]:
+ *   logits = Wr x (fp32); probabilities = softmax over the E experts; the topk largest
+ *   (ties: lower expert id) are renormalized to weights w summing to 1;
+ *   for each routed slot and for the shared expert: g = Wg x, u = Wu x (x quantized
+ *   once per token), h = silu(g) * u, h requantized per 32 as in qg_quantize_act,
+ *   o = Wd h; y = sum over routed slots (in rank order) of w * o, plus 1.0 * o of the
+ *   shared expert (ungated).
+ *   x: M x H fp32.  Wr: E x H fp32.  Wg_exps, Wu_exps: E stacked I x H matrices;
+ *   Wd_exps: E stacked H x I matrices.  Wg_sh, Wu_sh: I x H; Wd_sh: H x I.
+ *   y: M x H fp32.  topk_ids (int32) / topk_w (fp32): M x topk, may be NULL.
+ *   Limits: 1 <= topk <= 16, topk <= E <= 1024, H and I multiples of the block size.
+ * The intermediates stay in ws; qg_moe_ws_layout() gives their offsets. */
+int qg_moe_ffn(int fmt, const float *x, int M, int H,
+               const float *Wr, int E, int topk,
+               const void *Wg_exps, const void *Wu_exps, const void *Wd_exps,
+               const void *Wg_sh, const void *Wu_sh, const void *Wd_sh, int I,
+               float *y, int32_t *topk_ids, float *topk_w,
+               void *ws, size_t ws_bytes, void *stream);
+
+/* FFN sublayer on one stream with a reused workspace [D27 section
+ * "原位量化计算与单流融合的实际收益"]: x quantized once, g = Wg x and u = Wu x in one
+ * launch, h = silu(g) * u, h requantized, y = Wd h.
+ *   Wg, Wu: I x H blocks; Wd: H x I blocks; x: M x H fp32; y: M x H fp32. */
+int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd,
+                    const float *x, float *y, int M, int H, int I,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace an operation needs; 0 means the call needs none (ws may then be
+ * NULL); (size_t)-1 means the arguments are invalid.  The size depends on the shape and
+ * on the current device's SM count (152 is assumed when no device is usable).
+ *   QG_OP_GEMV / QG_OP_GEMV_Q: (fmt, M, N, K)            E, topk, I ignored
+ *   QG_OP_MOE_FFN:             (fmt, M, N=H, K=H, E, topk, I)
+ *   QG_OP_FFN_SUBLAYER:        (fmt, M, N=H, K=H, I)      E, topk ignored */
+size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, int I);
+
+/* Offsets (bytes from ws) of the MoE intermediates, written by qg_moe_ffn:
+ *   off[0] g, off[1] u, off[2] h : fp32, M x (topk+1) x I (slot topk = shared expert)
+ *   off[3] hq (int8), off[4] hd (fp32), off[5] hs (int32): requantized h,
+ *          M x (topk+1) x I  and  M x (topk+1) x I/32
+ *   off[6] logits: fp32 M x E
+ * Returns QG_OK or QG_EINVAL. */
+int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]);
+
+/* Offsets of the FFN sublayer intermediates: off[0] g, off[1] u, off[2] h (fp32 M x I). */
+int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]);
+
+/* Test hook, exact integer contract: dots[m][n][u] = sum over the 32 elements of unit
+ * u of (weight code) * xq, where the weight code is q (Q8_0), nibble-8 (Q4_0), the
+ * unsigned code (Q4_K, Q5_K), sub-scale*(code-32) (Q6_K) or the codebook value
+ * (IQ4_XS); aux[m][n][u] = xs[m][u] for Q4_K/Q5_K, else 0.  dots, aux: M x N x K/32
+ * int32.  Uses the same block decoders as the GEMV kernels. */
+int qg_block_dots(int fmt, const void *W_blocks, const int8_t *xq, const int32_t *xs,
+                  int N, int K, int M, int32_t *dots, int32_t *aux, void *stream);
+
+/* Device-side error word (bit 1: a bounded wait in a kernel gave up), read and cleared.
+ * Synchronizes the current device; for tests and diagnostics, not for the hot path. */
+int qg_device_error(unsigned int *err);
+
+/* Human-readable text of a status code. */
+const char *qg_strerror(int status);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int qg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QG_H */
