@@ -44,10 +44,31 @@ __global__ void splitk_reduce_kernel(const float *part, int KS, long MN, float *
     }
 }
 
-// logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32, one warp per expert row.
-__global__ void __launch_bounds__(256) router_logits_kernel(const float *x, int M, int H, const float *Wr, int E,
-                                                            float *logits) {
+// Activation tile image (see prep_tiles_warp); lets the dependent engine kernel start.
+__global__ void __launch_bounds__(256) prep_tiles_kernel(const float *x, const float *u, float *h_out,
+                                                         const int8_t *xq, const float *xd, const int32_t *xs,
+                                                         int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq,
+                                                         float *md, int32_t *ms) {
+    griddep_launch_dependents();
+    const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+    const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    prep_tiles_warp(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
+}
+
+// Blocks [0, ceil(E/8)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32, one warp per
+// expert row.  The remaining blocks write the activation tile image of x.
+__global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M, int H, const float *Wr, int E,
+                                                          float *logits, int xgt_log2, uint8_t *img) {
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
+    const int nrouter = (E + 7) / 8;
+    if ((int)blockIdx.x >= nrouter) {
+        const long nwarps = (long)(gridDim.x - nrouter) * (blockDim.x >> 5);
+        const long wid = (long)(blockIdx.x - nrouter) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        prep_tiles_warp(x, nullptr, nullptr, nullptr, nullptr, nullptr, M, H, xgt_log2, img, nullptr, nullptr, nullptr,
+                        wid, nwarps);
+        return;
+    }
     const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (e >= E) return;
     float acc[M_MAX];
@@ -82,8 +103,20 @@ int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStrea
     return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
 }
 
-int launch_router_logits(const float *x, int M, int H, const float *Wr, int E, float *logits, cudaStream_t s) {
-    router_logits_kernel<<<(E + 7) / 8, 256, 0, s>>>(x, M, H, Wr, E, logits);
+int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t *xq, const float *xd,
+                      const int32_t *xs, int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq, float *md,
+                      int32_t *ms, cudaStream_t s) {
+    const long blocks = (long)rows * (K / 32);
+    const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
+    prep_tiles_kernel<<<grid, 256, 0, s>>>(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
+int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,
+                       uint8_t *img, cudaStream_t s) {
+    const long blocks = (long)M * (H / 32);
+    const int nprep = (int)std::min<long>((blocks + 7) / 8, 512);
+    router_prep_kernel<<<(E + 7) / 8 + nprep, 256, 0, s>>>(x, M, H, Wr, E, logits, xgt_log2, img);
     return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
 }
 
@@ -179,7 +212,7 @@ size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, 
     switch (op) {
     case QG_OP_GEMV:
     case QG_OP_GEMV_Q: {
-        const GemvPlan p = plan_gemv(fmt, N, K, M, op == QG_OP_GEMV_Q, planning_sms());
+        const GemvPlan p = plan_gemv(fmt, N, K, M, planning_sms());
         return p.ok ? p.ws_total : bad;
     }
     case QG_OP_MOE_FFN: {
@@ -200,7 +233,8 @@ static int gemv_common(int fmt, const void *W, const float *x, const int8_t *xq,
     if (!x && (!xq || !xd || !xs)) return QG_EINVAL;
     if (!aligned(W, 16) || !aligned(y, 4) || (ws && !aligned(ws, 16))) return QG_EALIGN;
     if (x && !aligned(x, 4)) return QG_EALIGN;
-    if (!x && (!aligned(xq, 16) || !aligned(xd, 4) || !aligned(xs, 4))) return QG_EALIGN;
+    if (!x && (!aligned(xd, 4) || !aligned(xs, 4))) return QG_EALIGN;
+    if (!ws) return QG_EWORKSPACE;
     const int sms = current_sms();
     if (sms < 0) return sms;
     GemvCall c{};
@@ -322,7 +356,7 @@ int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]) {
 int qg_block_dots(int fmt, const void *W, const int8_t *xq, const int32_t *xs, int N, int K, int M, int32_t *dots,
                   int32_t *aux, void *stream) {
     if (!W || !xq || !xs || !dots || !aux || N < 1 || M < 1 || M > M_MAX || !shape_ok(fmt, K)) return QG_EINVAL;
-    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(xs, 4) || !aligned(dots, 4) || !aligned(aux, 4))
+    if (!aligned(W, 16) || !aligned(xs, 4) || !aligned(dots, 4) || !aligned(aux, 4))
         return QG_EALIGN;
     const int sms = current_sms();
     if (sms < 0) return sms;

@@ -10,16 +10,19 @@
 namespace qg {
 
 // ---------------------------------------------------------------------------------
-// Launch geometry of the streaming engine: NCW consumer warps + 1 producer warp.
-constexpr int NCW = 16;
-constexpr int NCONS = NCW * 32;
-constexpr int NTHREADS = NCONS + 32;
+// Launch geometry of the streaming engine: ncw_for(MT) consumer warps + 1 producer warp,
+// one CTA per SM.  Up to 4 tokens per lane the kernel fits 16 consumer warps in the
+// register file (4 per scheduler, to hide the latency of the decode chains); with 8 or 16
+// tokens the accumulators need more registers per thread and 8 warps run.
+__host__ __device__ constexpr int ncw_for(int MT) { return MT <= 4 ? 16 : 8; }
+__host__ __device__ constexpr int nthreads_for(int MT) { return ncw_for(MT) * 32 + 32; }
 constexpr int SMEM_MAX = 227 * 1024;       // opt-in dynamic shared memory per CTA (sm_100 family)
-constexpr int PART_SLOTS = 128;            // rows x tokens of one stage's partial-sum buffer
 constexpr int STAGE_SLACK = 64;            // bytes after each ring slot for over-reads
 
-// Device error word: bit 0 = a bounded wait gave up.
+// Device error word: bit 0 = a bounded wait gave up; bit 1 = a stage did not fit the
+// engine's piece table (its remaining tasks were skipped).
 constexpr unsigned int DEVERR_TIMEOUT = 1u;
+constexpr unsigned int DEVERR_PLAN = 2u;
 constexpr unsigned long long WAIT_NS = 2000000000ull;   // 2 s
 
 // ---------------------------------------------------------------------------------
@@ -77,6 +80,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// The bulk copies of a stage may complete before the producer posts their byte count: the
+// transaction count may go negative until then, and the phase cannot complete before the
+// producer's arrival.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
@@ -88,6 +94,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking test of the phase of parity `parity` (for polling several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -130,6 +148,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialization
+// attribute may start before the previous kernel in the stream has finished; it must call
+// griddep_wait() before reading anything that kernel writes.  The previous kernel calls
+// griddep_launch_dependents() to let it start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Barrier among the NCONS consumer threads only (the producer warp has returned).
+template <int NCONS>
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCONS) : "memory");
 }

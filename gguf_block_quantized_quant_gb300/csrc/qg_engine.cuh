@@ -1,247 +1,339 @@
 // qg_engine.cuh -- the weight-streaming engine behind every GEMV-shaped kernel of libqg.
 //
 // Decode GEMV is bound by HBM bandwidth: every weight byte is read once and used for
-// M <= 16 tokens.  The engine therefore spends its effort on keeping enough bytes in
-// flight per SM and on never touching a weight byte twice in HBM:
+// M <= 16 tokens.  The engine keeps enough bytes in flight per SM and spends as few
+// instructions per weight byte as it can.
 //
-//  * one CTA per SM (persistent), NCW consumer warps + 1 producer warp;
-//  * the producer's lane 0 copies contiguous runs of raw GGUF blocks from global memory
-//    into a ring of S shared-memory slots with 1-D bulk copies (cp.async.bulk, the TMA
-//    engine), completion tracked by one mbarrier per slot ("full"); runs that start or
-//    end off a 16-byte boundary are widened to it, and the few bytes past the end of a
-//    tensor that a widened copy may not read are fetched with byte loads;
-//  * consumers wait on "full", decode 32-element units in registers (qg_formats.cuh),
-//    multiply with the int8 activation codes by dp4a, apply the fp32 scales, reduce per
-//    row inside the warp, and release the slot through an "empty" mbarrier;
-//  * per-row partial sums of the warps go to a double-buffered shared array and are
-//    added in warp order by the job's epilogue, so every result is deterministic.
+// Work model.  A job is a sequence of OUTPUT ROWS, each the dot product of one weight-matrix
+// row (tpr tasks, see qg_formats.cuh) with an activation row.  Rows come in groups of grp
+// consecutive rows that are adjacent in memory (a whole matrix for a plain GEMV).
 //
-// A Job supplies the stage sequence (which rows of which tensor each slot receives), the
-// activation source, an optional prologue (e.g. quantizing x into shared memory) and the
-// epilogue (plain store, split-K partial, SwiGLU, weighted MoE sum).
+//  * one CTA per SM (persistent) with NCW consumer warps and one producer warp; the CTA
+//    owns a contiguous range of output rows (and, for split-K, a slice of every row);
+//  * the CTA's tasks are split into NCW contiguous ranges, one per consumer warp; a warp
+//    consumes its range in stages of tps tasks, lane l of step s taking task 32 s + l;
+//  * every warp owns D slots of the shared-memory ring: its j-th stage lands in slot
+//    (j mod D) * NCW + w, so each slot is used by one warp, in order, and no wait on a
+//    slot's mbarrier can be ahead of the slot's previous phase;
+//  * producer lane w feeds consumer warp w: it polls the "empty" mbarrier of the warp's
+//    next slot (non-blocking, so the lanes progress independently), then copies the
+//    stage's weight bytes -- one piece per run of adjacent rows -- with 1-D bulk copies
+//    (cp.async.bulk, the TMA engine), completion counted in bytes on the slot's "full"
+//    mbarrier; pieces that start or end off a 16-byte boundary are widened to it, and
+//    bytes past the end of a tensor that the widened copy may not read are loaded one by
+//    one;
+//  * activations arrive as a tile image written once per call by a preparation kernel; the
+//    producer issues the first stages, then waits for that kernel (programmatic dependent
+//    launch) and copies the image rows the CTA needs into shared memory;
+//  * a lane decodes its task in registers against the activation tiles; per step, a
+//    segmented shuffle reduction (rows are contiguous runs of lanes) leaves each row's
+//    sum at the row's first lane; a row that continues in the warp's next step is carried
+//    in registers; complete rows are stored by the job; rows shared with the neighbouring
+//    warp are combined after the last stage, in warp order, so every result is
+//    deterministic; the job may finish with a CTA-wide epilogue (MoE weighted sums).
 #pragma once
 
 #include "qg_formats.cuh"
 
 namespace qg {
 
-struct Stage {
-    const uint8_t *src[2];  // first byte of each segment (global)
-    const uint8_t *lim[2];  // end of the tensor holding segment k: bytes >= lim are never read
-    uint32_t bytes[2];      // bytes of each segment
-    int nseg;               // 1 or 2 segments
-    int R;                  // rows per segment
-    uint32_t rstride;       // bytes between consecutive rows of a segment
-    int nblk;               // blocks per row
-    int xb0;                // activation block of each row's first unit
-    int xm;                 // first activation row (token) used by this stage
-    int ntok;               // tokens per row (<= MT)
-    int tag0, tag1, tag2;   // job-defined
+constexpr int NPIECE_MAX = 8;      // weight pieces per stage
+constexpr int SCRATCH_INTS = 256;  // producer scratch (MoE top-k ids)
+constexpr int BND_FLOATS = 1 + 16; // boundary entry: row, then one sum per token
+
+// Unsigned division by a run-time constant (n < 2^31, d < 2^31): 32-bit reciprocal
+// estimate, corrected once.
+struct FastDiv {
+    uint32_t d, m;
+    __host__ __device__ static FastDiv make(uint32_t dv) {
+        FastDiv f;
+        f.d = dv;
+        f.m = dv <= 1 ? 0u : (uint32_t)((0x100000000ull + dv - 1) / dv);
+        return f;
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        if (d <= 1) return n;
+        uint32_t q = __umulhi(n, m);
+        if (q * d > n) --q;
+        return q;
+    }
 };
 
-// Shared memory carved by the engine (byte offsets from the dynamic smem base).
-struct EngineSmem {
-    uint32_t ring;   // S slots of slot_bytes (+ STAGE_SLACK each)
-    uint32_t part;   // 2 x PART_SLOTS x NCW floats
-    uint32_t job;    // job area
-    uint32_t bars;   // 2*S mbarriers, then 2*S u32 slot headers (data offsets of the segments)
+// Shared memory of the engine besides the ring, the activation tiles and the job area:
+// boundary sums (2 per warp), producer scratch, 2*S + 1 mbarriers, piece headers (per slot:
+// NPIECE_MAX piece addresses and the end of the tasks the pieces cover).
+__host__ __device__ constexpr uint32_t engine_fixed_smem(int S, int ncw) {
+    return (uint32_t)(ncw * 2 * BND_FLOATS * 4) + 4u * SCRATCH_INTS + 16u * (uint32_t)S + 8u +
+           4u * (NPIECE_MAX + 1) * (uint32_t)S + 16u;
+}
+
+// Byte offset of task tt within a row (tasks are whole or half blocks).
+template <class F>
+__host__ __device__ __forceinline__ uint32_t task_off(int tt) {
+    return (uint32_t)((tt / F::TPB) * F::BPT * F::BS);
+}
+
+// GEMV sink: per-token fp32 accumulators of one lane.
+template <int NT>
+struct AccSink {
+    static constexpr int MT = NT;
+    float acc[NT];
+    __device__ __forceinline__ void unit(int m, int, int, int, float contrib) { acc[m] += contrib; }
 };
 
-// Shared-memory bytes the engine needs besides the ring and the job area.
-__host__ __device__ constexpr uint32_t engine_fixed_smem(int S) {
-    return 2u * PART_SLOTS * NCW * 4u + 16u * (uint32_t)S + 8u * (uint32_t)S + 16u;
-}
-
-// Sum (in warp order) and clear the partials of stage row i, token m.
-template <int MT>
-__device__ __forceinline__ float part_take(float *part, int i, int m) {
-    float *p = part + (i * MT + m) * NCW;
-    float s = 0.0f;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) {
-        s += p[w];
-        p[w] = 0.0f;
-    }
-    return s;
-}
-
-template <int FMT, int MT, class Job>
-__device__ __forceinline__ void process_unit(const Job &job, const typename Job::XSrc &xs, const Stage &st,
-                                             uint32_t rowaddr, int u, float (&acc)[MT]) {
-    using F = Fmt<FMT>;
-    const int b = u / F::UPB, j = u - b * F::UPB;
-    WUnit w;
-    F::decode(rowaddr + (uint32_t)(b * F::BS), j, w);
-    const int xb = st.xb0 + u;
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        if (m < st.ntok) {
-            XUnit x;
-            xs.load(st.xm + m, xb, F::NEED_XS, x);
-            acc[m] = F::accum(acc[m], w, F::idot(w, x), x);
-        }
-    }
-}
-
-template <int FMT, int MT, class Job>
-__global__ void __launch_bounds__(NTHREADS, 1) engine_kernel(const Job job) {
-    using F = Fmt<FMT>;
+template <int FMT, int T, int MT, class Job>
+__global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job job) {
+    using F = FT<FMT, T>;
+    using TL = Tile<F::XGT>;
+    constexpr int NCW = ncw_for(MT), NCONS = NCW * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int S = job.nslots;
+    const int D = job.depth, S = NCW * D;
     const uint32_t slot_stride = job.slot_bytes + STAGE_SLACK;
 
-    EngineSmem L;
-    L.ring = smem_addr(smem);
-    L.part = L.ring + (uint32_t)S * slot_stride;
-    L.job = L.part + 2u * PART_SLOTS * NCW * 4u;
-    L.bars = L.job + job.job_smem_bytes;
-    float *part_base = reinterpret_cast<float *>(smem + (L.part - L.ring));
-    uint8_t *job_smem = smem + (L.job - L.ring);
-    auto full_bar = [&](int s) { return L.bars + 8u * (uint32_t)s; };
-    auto empty_bar = [&](int s) { return L.bars + 8u * (uint32_t)(S + s); };
-    auto slot_hdr = [&](int s) { return L.bars + 16u * (uint32_t)S + 8u * (uint32_t)s; };
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t xa = ring + (uint32_t)S * slot_stride;              // activation tiles
+    const uint32_t ja = xa + job.x_bytes;                              // job area
+    const uint32_t bnd = ja + job.j_bytes;                             // boundary sums
+    const uint32_t scr = bnd + (uint32_t)(NCW * 2 * BND_FLOATS * 4);   // producer scratch
+    const uint32_t bars = scr + 4u * SCRATCH_INTS;
+    const uint32_t xbar = bars + 16u * (uint32_t)S;
+    const uint32_t hdrs = xbar + 8u;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
+    auto hdr = [&](int s, int p) { return hdrs + 4u * (uint32_t)(s * (NPIECE_MAX + 1) + p); };
+    const uint32_t tok_stride = (uint32_t)(job.tpr_x * TL::STRIDE);
+    float *bsum = reinterpret_cast<float *>(smem + (bnd - ring));  // [NCW][2][BND_FLOATS]
+    int *scratch = reinterpret_cast<int *>(smem + (scr - ring));
+    float *jarea = reinterpret_cast<float *>(smem + (ja - ring));
+
+    // this CTA's tasks and the consumer warps' ranges (whole blocks)
+    int o0, o1, tpr, grp;
+    job.cta(o0, o1, tpr, grp);
+    const int ntask = (o1 - o0) * tpr;
+    const FastDiv tpr_div = FastDiv::make((uint32_t)tpr), grp_div = FastDiv::make((uint32_t)grp);
+    const int units = ntask / F::TPB;
+    auto wstart = [&](int w) { return (int)((long)units * w / NCW) * F::TPB; };
+    const int maxlen = (units + NCW - 1) / NCW * F::TPB;
+    const int nchunk = (maxlen + job.tps - 1) / job.tps;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), NCW);
+            mbar_init(empty_bar(s), 1);
         }
+        mbar_init(xbar, 1);
         fence_mbar_init();
     }
+    if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
+    job.init(jarea, tid);
     __syncthreads();
 
     if (warp == NCW) {
         // ------------------------------------------------------------------ producer
-        job.producer_prologue(job_smem, lane);
+        job.producer_prologue(lane, scratch);
+        __syncwarp();
+        const bool act = lane < NCW;  // lane w feeds consumer warp w
+        const int wa = act ? wstart(lane) : 0, wb = act ? wstart(lane + 1) : 0;
+        // Issues stage j of warp `lane` into its slot (the slot is known to be free).
+        auto issue = [&](int j) {
+            const int slot = (j % D) * NCW + lane;
+            const int fa = wa + j * job.tps, fb = min(wb, fa + job.tps);
+            const uint32_t sbase = ring + (uint32_t)slot * slot_stride;
+            const uint32_t fbar = full_bar(slot);
+            uint32_t off = 0, tx = 0;
+            int np = 0, f = fa;
+            for (; f < fb && np < NPIECE_MAX; ++np) {
+                const int o = (int)tpr_div.div((uint32_t)f), tt = f - o * tpr;
+                int fend = fb;
+                if (grp) {
+                    const int gend = ((int)grp_div.div((uint32_t)(o0 + o)) + 1) * grp - o0;  // next group's row
+                    fend = min(fb, gend * tpr);
+                }
+                const uint8_t *lim;
+                const uint8_t *src = job.seg_src(o0 + o, tt, lim, scratch);
+                const uint32_t bytes = task_off<F>(fend - f);
+                const uintptr_t s0 = (uintptr_t)src, a0 = s0 & ~(uintptr_t)15, e = s0 + bytes;
+                const uintptr_t a1 = (e + 15) & ~(uintptr_t)15, lim16 = (uintptr_t)lim & ~(uintptr_t)15;
+                uintptr_t a1c = a1 <= lim16 ? a1 : lim16;
+                if (a1c < a0) a1c = a0;
+                for (uintptr_t q = a1c; q < e; ++q)
+                    sts8(sbase + off + (uint32_t)(q - a0), *reinterpret_cast<const uint8_t *>(q));
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, np)), "r"(sbase + off + (uint32_t)(s0 & 15))
+                             : "memory");
+                const uint32_t nb = (uint32_t)(a1c - a0);
+                if (nb) bulk_g2s(sbase + off, reinterpret_cast<const void *>(a0), nb, fbar);
+                tx += nb;
+                off += (uint32_t)(a1 - a0);
+                f = fend;
+            }
+            // tasks [f, fb) did not fit the piece table (a planning error): the consumers
+            // skip them and the host sees DEVERR_PLAN
+            if (f < fb) atomicOr(&g_qg_dev_err, DEVERR_PLAN);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, NPIECE_MAX)), "r"(min(f, fb)) : "memory");
+            mbar_arrive_expect_tx(fbar, tx);
+        };
+        // the first D stages of every warp: the slots are free
+        const int jfirst = min(D, nchunk);
+        if (act)
+            for (int j = 0; j < jfirst; ++j) issue(j);
         __syncwarp();
         if (lane == 0) {
-            typename Job::Cursor c;
-            job.first(c);
-            for (int t = 0; c.valid; ++t, job.next(c)) {
-                Stage st;
-                job.stage(c, job_smem, true, st);
-                const int slot = t % S;
-                mbar_wait(empty_bar(slot), (uint32_t)((t / S) & 1) ^ 1u);
-                const uint32_t sbase = L.ring + (uint32_t)slot * slot_stride;
-                uint32_t off = 0, tx = 0;
-                uint32_t cdst[2], cbytes[2];
-                const uint8_t *csrc[2];
-                for (int k = 0; k < st.nseg; ++k) {
-                    const uintptr_t s0 = (uintptr_t)st.src[k];
-                    const uintptr_t a0 = s0 & ~(uintptr_t)15;
-                    const uintptr_t e = s0 + st.bytes[k];
-                    const uintptr_t a1 = (e + 15) & ~(uintptr_t)15;
-                    const uintptr_t lim16 = (uintptr_t)st.lim[k] & ~(uintptr_t)15;
-                    uintptr_t a1c = a1 <= lim16 ? a1 : lim16;
-                    if (a1c < a0) a1c = a0;
-                    cdst[k] = sbase + off;
-                    csrc[k] = reinterpret_cast<const uint8_t *>(a0);
-                    cbytes[k] = (uint32_t)(a1c - a0);
-                    tx += cbytes[k];
-                    // bytes the widened copy may not read: plain loads
-                    for (uintptr_t p = a1c; p < e; ++p)
-                        sts8(sbase + off + (uint32_t)(p - a0), *reinterpret_cast<const uint8_t *>(p));
-                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(slot_hdr(slot) + 4u * k),
-                                 "r"(sbase + off + (uint32_t)(s0 & 15)) : "memory");
-                    off += (uint32_t)(a1 - a0);
+            griddep_wait();
+            const int rows = ntask > 0 ? job.xrows() : 0;
+            uint32_t tx = 0;
+            for (int r = 0; r < rows; ++r) {
+                const uint32_t bytes = job.xrow_bytes(r);
+                if (bytes) bulk_g2s(xa + (uint32_t)r * tok_stride, job.xrow_src(r), bytes, xbar);
+                tx += bytes;
+            }
+            mbar_arrive_expect_tx(xbar, tx);
+        }
+        __syncwarp();
+        // then every lane refills its warp's slots as they are released
+        int j = jfirst;
+        unsigned long long t_idle = 0;
+        for (;;) {
+            const bool more = act && j < nchunk;
+            if (!__any_sync(0xffffffffu, more)) break;
+            const bool ready =
+                more && mbar_test_wait(empty_bar((j % D) * NCW + lane), (uint32_t)((j / D) & 1) ^ 1u);
+            if (ready) {
+                issue(j);
+                ++j;
+            }
+            if (__any_sync(0xffffffffu, ready)) {
+                t_idle = 0;
+            } else {
+                // no consumer warp has released a slot: back off; give up after WAIT_NS
+                if (*reinterpret_cast<volatile unsigned int *>(&g_qg_dev_err) & DEVERR_TIMEOUT) break;
+                const unsigned long long now = globaltimer_ns();
+                if (t_idle == 0) {
+                    t_idle = now;
+                } else if (now - t_idle > WAIT_NS) {
+                    if (lane == 0) atomicOr(&g_qg_dev_err, DEVERR_TIMEOUT);
+                    break;
                 }
-                mbar_arrive_expect_tx(full_bar(slot), tx);
-                for (int k = 0; k < st.nseg; ++k)
-                    if (cbytes[k]) bulk_g2s(cdst[k], csrc[k], cbytes[k], full_bar(slot));
+                __nanosleep(32);
             }
         }
         return;
     }
 
     // ---------------------------------------------------------------------- consumers
-    for (int i = tid; i < 2 * PART_SLOTS * NCW; i += NCONS) part_base[i] = 0.0f;
-    job.consumer_prologue(job_smem, tid);
-    consumer_sync();
+    const int a = wstart(warp), b = wstart(warp + 1);
+    const int ra = (int)tpr_div.div((uint32_t)a);
+    const bool a_mid = a < b && a != ra * tpr;
+    const int ntok = job.ntok;
+    mbar_wait(xbar, 0);
 
-    const typename Job::XSrc xsrc = job.xsrc(job_smem, L.job);
-    typename Job::Cursor c;
-    job.first(c);
-    int buf = 0;
-    for (int t = 0; c.valid; ++t, job.next(c)) {
-        Stage st;
-        job.stage(c, job_smem, false, st);
-        const int slot = t % S;
-        float *part = part_base + buf * PART_SLOTS * NCW;
-        const int U = st.nblk * F::UPB;
-        const int NR = st.nseg * st.R;
-
-        mbar_wait(full_bar(slot), (uint32_t)((t / S) & 1));
-        uint32_t data[2];
-        data[0] = lds32(slot_hdr(slot));
-        data[1] = lds32(slot_hdr(slot) + 4u);
-
-        if (U > 16) {
-            const int SPR = (U + 31) >> 5;
-            const int TS = NR * SPR;
-            const int s0 = warp * TS / NCW, s1 = (warp + 1) * TS / NCW;
-            float acc[MT];
+    float carry[MT];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
-            int cur = -1;
-            for (int s = s0; s < s1; ++s) {
-                const int i = s / SPR, k = s - i * SPR;
-                if (i != cur) {
-                    if (cur >= 0) {
+    for (int m = 0; m < MT; ++m) carry[m] = 0.0f;
+    int carry_o = -1;  // CTA-relative output row whose partial sum is in carry
+
+    for (int j = 0; j < nchunk; ++j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = a + j * job.tps;
+        mbar_wait(full_bar(slot), (uint32_t)((j / D) & 1));
+        const int fb = min(min(b, fa + job.tps), (int)lds32(hdr(slot, NPIECE_MAX)));
+        if (fa < fb) {
+            const int oa = (int)tpr_div.div((uint32_t)fa);
+            const int ga = grp ? (int)grp_div.div((uint32_t)(o0 + oa)) : 0;
+            for (int f0 = fa; f0 < fb; f0 += 32) {
+                const int f = f0 + lane;
+                const bool valid = f < fb;
+                int o = 0x7fffffff;
+                AccSink<MT> sink;
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const float v = warp_sum(acc[m]);
-                            if (lane == 0) part[(cur * MT + m) * NCW + warp] = v;
-                            acc[m] = 0.0f;
-                        }
+                for (int m = 0; m < MT; ++m) sink.acc[m] = 0.0f;
+                if (valid) {
+                    o = (int)tpr_div.div((uint32_t)f);
+                    const int tt = f - o * tpr;
+                    int piece = 0, fp = fa;
+                    if (grp) {
+                        const int g = (int)grp_div.div((uint32_t)(o0 + o));
+                        piece = g - ga;
+                        if (piece) fp = (g * grp - o0) * tpr;
                     }
-                    cur = i;
+                    const uint32_t addr = lds32(hdr(slot, piece)) + task_off<F>(f - fp);
+                    const XT xt{xa + job.xrow(o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE), tok_stride};
+                    F::run(addr, tt % F::TPB, xt, ntok, sink);
                 }
-                const int u = 32 * k + lane;
-                if (u < U) {
-                    const int sg = i >= st.R;
-                    const uint32_t rowaddr = data[sg] + (uint32_t)(i - sg * st.R) * st.rstride;
-                    process_unit<FMT, MT>(job, xsrc, st, rowaddr, u, acc);
-                }
-            }
-            if (cur >= 0) {
+                // segmented reduction: rows are contiguous runs of lanes
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const float v = warp_sum(acc[m]);
-                    if (lane == 0) part[(cur * MT + m) * NCW + warp] = v;
-                }
-            }
-        } else {
-            // short rows: 32/Up rows per warp step, Up = U rounded up to a power of two
-            int Up = 1;
-            while (Up < U) Up <<= 1;
-            const int P = 32 / Up;
-            const int TS = (NR + P - 1) / P;
-            const int s0 = warp * TS / NCW, s1 = (warp + 1) * TS / NCW;
-            for (int s = s0; s < s1; ++s) {
-                const int i = s * P + lane / Up, u = lane & (Up - 1);
-                float acc[MT];
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int o2 = __shfl_down_sync(0xffffffffu, o, d);
+                    const bool take = lane + d < 32 && o2 == o;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
-                if (u < U && i < NR) {
-                    const int sg = i >= st.R;
-                    const uint32_t rowaddr = data[sg] + (uint32_t)(i - sg * st.R) * st.rstride;
-                    process_unit<FMT, MT>(job, xsrc, st, rowaddr, u, acc);
+                    for (int m = 0; m < MT; ++m) {
+                        const float v = __shfl_down_sync(0xffffffffu, sink.acc[m], d);
+                        if (take) sink.acc[m] += v;
+                    }
                 }
+                const int oprev = __shfl_up_sync(0xffffffffu, o, 1);
+                const bool head = valid && (lane == 0 || oprev != o);
+                if (head && o == carry_o) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float v = acc[m];
-                    for (int o = Up >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (u == 0 && i < NR) part[(i * MT + m) * NCW + warp] = v;
+                    for (int m = 0; m < MT; ++m) sink.acc[m] += carry[m];
                 }
+                // the step's last row continues if it has tasks after this step
+                const int flast = min(fb, f0 + 32) - 1;
+                const int olast = __shfl_sync(0xffffffffu, o, flast - f0);
+                const bool cont = (olast + 1) * tpr > flast + 1;
+                if (head && !(o == olast && cont)) {
+                    if (a_mid && o == ra) {
+                        float *e = bsum + (warp * 2) * BND_FLOATS;  // shared with the previous warp
+                        e[0] = __int_as_float(o);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) e[1 + m] = sink.acc[m];
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < MT; ++m)
+                            if (m < ntok) job.store(o0 + o, m, sink.acc[m], jarea);
+                    }
+                }
+                // the continuing row's head broadcasts its sums as the next carry
+                const int hl = __reduce_min_sync(0xffffffffu, (valid && o == olast) ? lane : 31);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) carry[m] = __shfl_sync(0xffffffffu, sink.acc[m], hl);
+                carry_o = cont ? olast : -1;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(slot));
-        consumer_sync();
-        job.template epilogue<MT>(st, part, job_smem, tid);
-        buf ^= 1;
+    }
+    // a range that ended inside a row: its sum is shared with the next warp
+    if (carry_o >= 0 && lane == 0) {
+        float *e = bsum + (warp * 2 + ((a_mid && carry_o == ra) ? 0 : 1)) * BND_FLOATS;
+        e[0] = __int_as_float(carry_o);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) e[1 + m] = carry[m];
+    }
+    consumer_sync<NCONS>();
+    // rows shared by consecutive warps: their sums added in warp order
+    if (warp == 0) {
+        int cur = -1;
+        float acc = 0.0f;
+        for (int w = 0; w < NCW; ++w) {
+            for (int side = 0; side < 2; ++side) {
+                const float *e = bsum + (w * 2 + side) * BND_FLOATS;
+                const int r = __float_as_int(e[0]);
+                if (r < 0) continue;
+                if (r != cur) {
+                    if (cur >= 0 && lane < ntok) job.store(o0 + cur, lane, acc, jarea);
+                    cur = r;
+                    acc = 0.0f;
+                }
+                if (lane < ntok) acc += e[1 + lane];
+            }
+        }
+        if (cur >= 0 && lane < ntok) job.store(o0 + cur, lane, acc, jarea);
+    }
+    if (Job::HAS_FINISH) {
+        consumer_sync<NCONS>();
+        job.finish(jarea, tid, NCONS);
     }
 }
 

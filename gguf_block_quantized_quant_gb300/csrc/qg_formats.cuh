@@ -1,25 +1,29 @@
 // qg_formats.cuh -- register-resident decoders for the six GGUF block formats.
 //
 // The GEMV is computed on the raw blocks in place ("为什么专家缓存救不了稠密模型", Q&A
-// "如何让CUDA直接计算GGUF混合量化块而不展开为FP16？"): each 32-element unit of a block
-// is unpacked in registers into 8 words of four 8-bit codes, dotted with the int8
-// activation codes by dp4a, and the fp32 scale factors are applied to the exact int32 sum
-// (for K-quants together with the min "correction term"; for IQ4_XS after a register
+// "如何让CUDA直接计算GGUF混合量化块而不展开为FP16？"): weight codes are unpacked in
+// registers, multiplied with the int8 activation codes by dp4a into exact int32 sums per
+// 32-element unit (one activation block), and the fp32 scale factors are applied to those
+// sums (for K-quants together with the min "correction term"; for IQ4_XS after a register
 // lookup in the 16-entry codebook).  Byte layouts are the public GGUF block definitions
 // (the pages name the formats but do not print them):
 //
-//   Q8_0    34 B: fp16 d, int8 q[32]                          w = d*q
-//   Q4_0    18 B: fp16 d, qs[16]; e<16 low nibble of qs[e],   w = d*(nib-8)
+//   Q8_0    34 B: fp16 d, int8 q[32]                           w = d*q
+//   Q4_0    18 B: fp16 d, qs[16]; e<16 low nibble of qs[e],    w = d*(nib-8)
 //                 e>=16 high nibble of qs[e-16]
-//   Q4_K   144 B: fp16 d, fp16 dmin, sc12[12], qs[128]        w = d*S_j*code - dmin*M_j
-//   Q5_K   176 B: fp16 d, fp16 dmin, sc12[12], qh[32], qs[128] (code += 16*bit j of qh[l])
-//   Q6_K   210 B: ql[128], qh[64], int8 sc[16], fp16 d         w = d*sc[e/16]*(code-32)
-//   IQ4_XS 136 B: fp16 d, u16 scales_h, scales_l[4], qs[128]  w = d*(ls-32)*K[idx]
+//   Q4_K   144 B: fp16 d, fp16 dmin, sc12[12], qs[128]         w = d*S_j*code - dmin*M_j
+//   Q5_K   176 B: fp16 d, fp16 dmin, sc12[12], qh[32], qs[128] (code += 16 * bit j of qh[l])
+//   Q6_K   210 B: ql[128], qh[64], int8 sc[16], fp16 d          w = d*sc[e/16]*(code-32)
+//   IQ4_XS 136 B: fp16 d, u16 scales_h, scales_l[4], qs[128]   w = d*(ls-32)*K[idx]
 //
-// All weight reads are from shared memory (32-bit addresses).  Q8_0, Q4_0 and Q6_K blocks
-// may start on any even byte, so their fields are fetched as aligned words and realigned
-// with byte permutes; Q4_K/Q5_K blocks are 16-byte aligned and IQ4_XS blocks 8-byte aligned
-// in every staging layout used here.
+// Work is organised in TASKS, one per lane: four (or one) Q4_0/Q8_0 blocks, one Q4_K or
+// IQ4_XS superblock, half a Q5_K or Q6_K superblock.  A task's weights are read from
+// shared memory; its activations come from a per-task tile (codes, scales d, sums s and
+// packed 16-element half sums of each activation block), padded so that the 16-byte
+// loads of 8 consecutive lanes hit distinct banks.  Each format calls sink.unit(m, u, dot,
+// xs, contrib) once per token m and unit u with the exact integer dot product of the unit
+// and its fp32 contribution to y; the GEMV sink adds the contribution, the test-hook sink
+// stores the integers.
 #pragma once
 
 #include "qg_common.cuh"
@@ -28,181 +32,285 @@ namespace qg {
 
 enum : int { F_Q4_0 = 2, F_Q8_0 = 8, F_Q4_K = 12, F_Q5_K = 13, F_Q6_K = 14, F_IQ4_XS = 23 };
 
-// One decoded 32-element unit.
-struct WUnit {
-    uint32_t c[8];  // codes, 4 per word, element order (word k holds elements 4k..4k+3)
-    float fa;       // main scale of the unit
-    float fb;       // min factor (K-quants), else unused
-    int sA, sB;     // Q6_K sub-scales of elements 0..15 and 16..31
+// unsigned (weights) x signed (activations) 4-way byte dot product
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int r;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
+
+// ---------------------------------------------------------------------------------- tiles
+// Activation tile of XGT units: codes[32*XGT] | d[XGT] fp32 | s[XGT] int32 |
+// h[XGT] (sum of codes 0..15 in the low 16 bits, 16..31 in the high 16 bits), padded to an
+// odd number of 16-byte chunks.
+__host__ __device__ constexpr int tile_raw(int xgt) { return 44 * xgt; }
+__host__ __device__ constexpr int tile_stride(int xgt) {
+    return ((tile_raw(xgt) + 15) / 16) % 2 == 1 ? (tile_raw(xgt) + 15) / 16 * 16 : (tile_raw(xgt) + 15) / 16 * 16 + 16;
+}
+template <int XGT>
+struct Tile {
+    static constexpr int D = 32 * XGT, S = D + 4 * XGT, H = S + 4 * XGT, STRIDE = tile_stride(XGT);
 };
 
-// Activation operand of one unit for one token.
-struct XUnit {
-    uint32_t q[8];
-    float d;
-    int s;
-};
-
-// Realign 4 bytes starting at byte 2 (sel 0x5432) or byte 4 (sel 0x7654) of {w1:w0}.
-__device__ __forceinline__ uint32_t realign(uint32_t w0, uint32_t w1, uint32_t sel) { return prmt(w0, w1, sel); }
-
-template <int FMT>
-struct Fmt;
-
-// ------------------------------------------------------------------------------- Q8_0
-template <>
-struct Fmt<F_Q8_0> {
-    static constexpr int QK = 32, BS = 34, UPB = 1;
-    static constexpr bool NEED_XS = false;
-    __device__ __forceinline__ static void decode(uint32_t blk, int, WUnit &w) {
-        const uint32_t a = blk & 3u, base = blk - a;  // a is 0 or 2
-        uint32_t wd[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) wd[k] = lds32(base + 4 * k);
-        const uint32_t sel = a ? 0x7654u : 0x5432u;
-        w.fa = half_bits_to_float(a ? (wd[0] >> 16) : wd[0]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w.c[k] = realign(wd[k], wd[k + 1], sel);
-    }
-    __device__ __forceinline__ static int idot(const WUnit &w, const XUnit &x) {
-        int s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s = dp4a(w.c[k], x.q[k], s);
-        return s;
-    }
-    __device__ __forceinline__ static float accum(float acc, const WUnit &w, int dot, const XUnit &x) {
-        return fmaf(w.fa * x.d, (float)dot, acc);
-    }
-};
-
-// ------------------------------------------------------------------------------- Q4_0
-template <>
-struct Fmt<F_Q4_0> {
-    static constexpr int QK = 32, BS = 18, UPB = 1;
-    static constexpr bool NEED_XS = true;  // the -8 offset is folded in as -8*sum(q)
-    __device__ __forceinline__ static void decode(uint32_t blk, int, WUnit &w) {
-        const uint32_t a = blk & 3u, base = blk - a;
-        uint32_t wd[5];
-#pragma unroll
-        for (int k = 0; k < 5; ++k) wd[k] = lds32(base + 4 * k);
-        const uint32_t sel = a ? 0x7654u : 0x5432u;
-        w.fa = half_bits_to_float(a ? (wd[0] >> 16) : wd[0]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t q = realign(wd[k], wd[k + 1], sel);
-            w.c[k] = q & 0x0f0f0f0fu;             // elements 4k..4k+3
-            w.c[4 + k] = (q >> 4) & 0x0f0f0f0fu;  // elements 16+4k..
-        }
-    }
-    __device__ __forceinline__ static int idot(const WUnit &w, const XUnit &x) {
-        int s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s = dp4a(w.c[k], x.q[k], s);
-        return s - 8 * x.s;
-    }
-    __device__ __forceinline__ static float accum(float acc, const WUnit &w, int dot, const XUnit &x) {
-        return fmaf(w.fa * x.d, (float)dot, acc);
-    }
-};
-
-// ------------------------------------------------------------------------------- Q4_K / Q5_K
-// 6-bit scale S_j and min M_j of sub-block j from the 12 packed bytes (words h1..h3).
-__device__ __forceinline__ void kq_scale_min(uint32_t h1, uint32_t h2, uint32_t h3, int j, int &S, int &M) {
-    const int sh = 8 * (j & 3);
-    const int b0 = (h1 >> sh) & 255, b1 = (h2 >> sh) & 255, b2 = (h3 >> sh) & 255;
-    if (j < 4) {
-        S = b0 & 63;
-        M = b1 & 63;
-    } else {
-        S = (b2 & 15) | ((b0 >> 6) << 4);
-        M = (b2 >> 4) | ((b1 >> 6) << 4);
-    }
+__device__ __forceinline__ void ldx8(uint32_t a, uint32_t (&x)[8]) {
+    const uint4 p = lds128(a), q = lds128(a + 16);
+    x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
+    x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
 }
 
-template <int FMT>
-struct FmtKQ {
-    static constexpr int QK = 256, BS = (FMT == F_Q4_K ? 144 : 176), UPB = 8;
-    static constexpr bool NEED_XS = true;
-    __device__ __forceinline__ static void decode(uint32_t blk, int j, WUnit &w) {
-        const uint4 h = lds128(blk);
-        const uint32_t qs = blk + (FMT == F_Q4_K ? 16 : 48) + 32 * (j >> 1);
-        const uint4 q0 = lds128(qs), q1 = lds128(qs + 16);
-        int S, M;
-        kq_scale_min(h.y, h.z, h.w, j, S, M);
-        w.fa = half_bits_to_float(h.x) * (float)S;
-        w.fb = half_bits_to_float(h.x >> 16) * (float)M;
-        const int sh = 4 * (j & 1);
-        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w.c[k] = (qw[k] >> sh) & 0x0f0f0f0fu;
-        if (FMT == F_Q5_K) {
-            const uint4 h0 = lds128(blk + 16), h1 = lds128(blk + 32);
-            const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w.c[k] |= ((hw[k] >> j) & 0x01010101u) << 4;
-        }
-    }
-    __device__ __forceinline__ static int idot(const WUnit &w, const XUnit &x) {
-        int s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s = dp4a(w.c[k], x.q[k], s);
-        return s;
-    }
-    __device__ __forceinline__ static float accum(float acc, const WUnit &w, int dot, const XUnit &x) {
-        return fmaf(x.d, fmaf(w.fa, (float)dot, -w.fb * (float)x.s), acc);
-    }
-};
-template <>
-struct Fmt<F_Q4_K> : FmtKQ<F_Q4_K> {};
-template <>
-struct Fmt<F_Q5_K> : FmtKQ<F_Q5_K> {};
-
-// ------------------------------------------------------------------------------- Q6_K
-template <>
-struct Fmt<F_Q6_K> {
-    static constexpr int QK = 256, BS = 210, UPB = 8;
-    static constexpr bool NEED_XS = false;
-    // unit ut = activation block 4h+t of the superblock: elements 128h + 32t + l, l < 32
-    __device__ __forceinline__ static void decode(uint32_t blk, int ut, WUnit &w) {
-        const uint32_t a = blk & 3u, base = blk - a;
-        const int h = ut >> 2, t = ut & 3;
-        const uint32_t sel = a ? 0x7654u : 0x5432u;
-        const uint32_t lq = base + 64 * h + 32 * (t & 1);
-        const uint32_t hq = base + 128 + 32 * h;
-        uint32_t lw[9], hw[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-            lw[k] = lds32(lq + 4 * k);
-            hw[k] = lds32(hq + 4 * k);
-        }
-        const int sh = 4 * (t >> 1), hs = 2 * t;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t l = (realign(lw[k], lw[k + 1], sel) >> sh) & 0x0f0f0f0fu;
-            const uint32_t hi = (realign(hw[k], hw[k + 1], sel) >> hs) & 0x03030303u;
-            // per byte: (l | hi<<4) - 32, done without borrows between bytes
-            w.c[k] = ((l | (hi << 4)) + 0x60606060u) ^ 0x80808080u;
-        }
-        const uint32_t so = a + 192 + 8 * h + 2 * t;  // even
-        const uint32_t sw = lds32(base + (so & ~3u)) >> (8 * (so & 3u));
-        w.sA = (int)(int8_t)(sw & 255u);
-        w.sB = (int)(int8_t)((sw >> 8) & 255u);
-        w.fa = half_bits_to_float(lds32(base + 208) >> (8 * a));
-    }
-    __device__ __forceinline__ static int idot(const WUnit &w, const XUnit &x) {
-        int lo = 0, hi = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) lo = dp4a(w.c[k], x.q[k], lo);
-#pragma unroll
-        for (int k = 4; k < 8; ++k) hi = dp4a(w.c[k], x.q[k], hi);
-        return w.sA * lo + w.sB * hi;
-    }
-    __device__ __forceinline__ static float accum(float acc, const WUnit &w, int dot, const XUnit &x) {
-        return fmaf(w.fa * x.d, (float)dot, acc);
-    }
+// Activations of one task: tile address of token m is base + m * tok_stride.
+struct XT {
+    uint32_t base;
+    uint32_t tok_stride;
+    __device__ __forceinline__ uint32_t tile(int m) const { return base + (uint32_t)m * tok_stride; }
 };
 
-// ------------------------------------------------------------------------------- IQ4_XS
+// Byte offset OFF (even) into a run of words: realigned when OFF is 2 mod 4.
+template <int NW>
+__device__ __forceinline__ uint32_t word_at(const uint32_t (&w)[NW], int off) {
+    return (off & 3) ? prmt(w[off >> 2], w[(off >> 2) + 1], 0x5432u) : w[off >> 2];
+}
+
+// ================================================================================ Q8_0 / Q4_0
+// T blocks per task.  With T == 4 a task is 136 (Q8_0) or 72 (Q4_0) bytes and always starts
+// 8-byte aligned, so all field offsets are compile-time; with T == 1 the block may start on
+// any even byte and is realigned with run-time byte permutes.
+template <int FMT, int T>
+struct FmtLegacy {
+    static constexpr int QK = 32, BS = (FMT == F_Q8_0 ? 34 : 18), XGT = T, TPB = 1, BPT = T;
+    static constexpr int TASK_BYTES = T * BS;
+
+    template <class Sink>
+    __device__ __forceinline__ static void unit_from_words(const uint32_t (&c)[8], float d, int m, int u,
+                                                           uint32_t tile, Sink &sink) {
+        using TL = Tile<XGT>;
+        uint32_t x[8];
+        ldx8(tile + 32 * u, x);
+        const float xd = ldsf(tile + TL::D + 4 * u);
+        int dot = 0;
+        int xs = 0;
+        if (FMT == F_Q8_0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dot = dp4a(c[k], x[k], dot);
+        } else {
+            // c[0..3]: qs words; low nibbles = elements 0..15, high nibbles = 16..31
+            int lo = 0, hi = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                lo = dp4a(c[k] & 0x0f0f0f0fu, x[k], lo);
+                hi = dp4a_us(c[k] & 0xf0f0f0f0u, x[4 + k], hi);
+            }
+            xs = (int)lds32(tile + TL::S + 4 * u);
+            dot = lo + (hi >> 4) - 8 * xs;
+        }
+        sink.unit(m, u, dot, xs, d * xd * (float)dot);
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+        if constexpr (T == 4) {
+            constexpr int NW = TASK_BYTES / 4 + 2;
+            uint32_t w[NW];
+#pragma unroll
+            for (int i = 0; i < NW / 2; ++i) {
+                const uint2 v = lds64(addr + 8 * i);
+                w[2 * i] = v.x;
+                w[2 * i + 1] = v.y;
+            }
+#pragma unroll
+            for (int b = 0; b < T; ++b) {
+                const int off = BS * b;
+                const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                uint32_t c[8];
+#pragma unroll
+                for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
+#pragma unroll
+                for (int m = 0; m < Sink::MT; ++m)
+                    if (m < ntok) unit_from_words(c, d, m, b, xt.tile(m), sink);
+            }
+        } else {
+            const uint32_t a = addr & 3u, base = addr - a;  // a is 0 or 2
+            constexpr int NW = BS / 4 + 2;
+            uint32_t w[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) w[i] = lds32(base + 4 * i);
+            const uint32_t sel = a ? 0x7654u : 0x5432u;  // 4 bytes starting 2 past the block start
+            const float d = half_bits_to_float(a ? (w[0] >> 16) : w[0]);
+            uint32_t c[8];
+#pragma unroll
+            for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = prmt(w[k], w[k + 1], sel);
+#pragma unroll
+            for (int m = 0; m < Sink::MT; ++m)
+                if (m < ntok) unit_from_words(c, d, m, 0, xt.tile(m), sink);
+        }
+    }
+};
+
+// ================================================================================ Q4_K
+// One superblock per task.  The 8 six-bit scales and mins are unpacked four at a time into
+// bytes; sub-block 2p uses the low nibbles of qs[32p..32p+31], sub-block 2p+1 the high
+// nibbles, which are multiplied in place (16 * nibble) by an unsigned dp4a.
+struct FmtQ4K {
+    static constexpr int QK = 256, BS = 144, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 144;
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<8>;
+        const uint4 h = lds128(addr);
+        const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+        const uint32_t S03 = h.y & 0x3f3f3f3fu, M03 = h.z & 0x3f3f3f3fu;
+        const uint32_t S47 = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+        const uint32_t M47 = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            uint32_t q[8];
+            ldx8(addr + 16 + 32 * p, q);
+            const uint32_t Sw = p < 2 ? S03 : S47, Mw = p < 2 ? M03 : M47;
+            const int sh = 16 * (p & 1);
+            const float fa0 = d * (float)((Sw >> sh) & 255u), fa1 = d * (float)((Sw >> (sh + 8)) & 255u);
+            const float fb0 = dmin * (float)((Mw >> sh) & 255u), fb1 = dmin * (float)((Mw >> (sh + 8)) & 255u);
+#pragma unroll
+            for (int m = 0; m < Sink::MT; ++m) {
+                if (m < ntok) {
+                    const uint32_t t = xt.tile(m);
+                    uint32_t xa[8], xb[8];
+                    ldx8(t + 64 * p, xa);
+                    ldx8(t + 64 * p + 32, xb);
+                    const uint2 xd = lds64(t + TL::D + 8 * p), xs = lds64(t + TL::S + 8 * p);
+                    int da = 0, db = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da = dp4a(q[k] & 0x0f0f0f0fu, xa[k], da);
+                        db = dp4a_us(q[k] & 0xf0f0f0f0u, xb[k], db);
+                    }
+                    db >>= 4;
+                    const int s0 = (int)xs.x, s1 = (int)xs.y;
+                    sink.unit(m, 2 * p, da, s0, __uint_as_float(xd.x) * fmaf(fa0, (float)da, -fb0 * (float)s0));
+                    sink.unit(m, 2 * p + 1, db, s1, __uint_as_float(xd.y) * fmaf(fa1, (float)db, -fb1 * (float)s1));
+                }
+            }
+        }
+    }
+};
+
+// ================================================================================ Q5_K
+// Half a superblock per task (sub-blocks 4*hf .. 4*hf+3); the fifth bit of sub-block j is
+// bit j of each qh byte.
+struct FmtQ5K {
+    static constexpr int QK = 256, BS = 176, XGT = 4, TPB = 2, BPT = 1, TASK_BYTES = 88;
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<4>;
+        const uint4 h = lds128(addr);
+        const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+        const uint32_t Sw = hf ? ((h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u)) : (h.y & 0x3f3f3f3fu);
+        const uint32_t Mw = hf ? (((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u)) : (h.z & 0x3f3f3f3fu);
+        uint32_t qh[8];
+        ldx8(addr + 16, qh);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+            const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
+            uint32_t q[8];
+            ldx8(addr + 48 + 32 * (2 * hf + pp), q);
+            uint32_t c0[8], c1[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
+                c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
+            }
+            const float fa0 = d * (float)((Sw >> (16 * pp)) & 255u), fa1 = d * (float)((Sw >> (16 * pp + 8)) & 255u);
+            const float fb0 = dmin * (float)((Mw >> (16 * pp)) & 255u);
+            const float fb1 = dmin * (float)((Mw >> (16 * pp + 8)) & 255u);
+#pragma unroll
+            for (int m = 0; m < Sink::MT; ++m) {
+                if (m < ntok) {
+                    const uint32_t t = xt.tile(m);
+                    uint32_t xa[8], xb[8];
+                    ldx8(t + 64 * pp, xa);
+                    ldx8(t + 64 * pp + 32, xb);
+                    const uint2 xd = lds64(t + TL::D + 8 * pp), xs = lds64(t + TL::S + 8 * pp);
+                    int da = 0, db = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da = dp4a(c0[k], xa[k], da);
+                        db = dp4a(c1[k], xb[k], db);
+                    }
+                    const int s0 = (int)xs.x, s1 = (int)xs.y;
+                    sink.unit(m, 2 * pp, da, s0, __uint_as_float(xd.x) * fmaf(fa0, (float)da, -fb0 * (float)s0));
+                    sink.unit(m, 2 * pp + 1, db, s1, __uint_as_float(xd.y) * fmaf(fa1, (float)db, -fb1 * (float)s1));
+                }
+            }
+        }
+    }
+};
+
+// ================================================================================ Q6_K
+// Half a superblock per task (elements 128*hf .. +127, activation blocks t = 0..3): the low
+// four bits of element 32t + l come from byte l + 32*(t&1) of the half's 64 ql bytes (low
+// nibble for t < 2), the top two from bits 2t, 2t+1 of qh byte l.  Codes are used unsigned
+// (0..63) and the -32 offset is applied through the activation half sums.  Superblocks may
+// start on any even byte: words are realigned with run-time byte permutes.
+struct FmtQ6K {
+    static constexpr int QK = 256, BS = 210, XGT = 4, TPB = 2, BPT = 1, TASK_BYTES = 105;
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<4>;
+        const uint32_t a = addr & 3u, base = addr - a;
+        const uint32_t sel = a ? 0x5432u : 0x3210u;
+        uint32_t qh[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) qh[k] = lds32(base + 128 + 32 * hf + 4 * k);
+        uint32_t hw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hw[k] = prmt(qh[k], qh[k + 1], sel);
+        const uint32_t so = a + 192 + 8 * hf;  // 8 sub-scales of this half (even offset)
+        const uint32_t s0w = lds32(base + (so & ~3u)), s1w = lds32(base + (so & ~3u) + 4),
+                       s2w = lds32(base + (so & ~3u) + 8);
+        const uint32_t scA = prmt(s0w, s1w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+0..3]
+        const uint32_t scB = prmt(s1w, s2w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+4..7]
+        const float d = half_bits_to_float(lds32(base + 208) >> (8 * a));
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            uint32_t ql[9];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) ql[k] = lds32(base + 64 * hf + 32 * s + 4 * k);
+            uint32_t lw[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) lw[k] = prmt(ql[k], ql[k + 1], sel);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = s + 2 * tt;  // activation block within the half
+                uint32_t c[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    c[k] = ((lw[k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[k] >> (2 * t)) & 0x03030303u) << 4);
+                const uint32_t scw = t < 2 ? scA : scB;
+                const int sA = (int)(int8_t)((scw >> (16 * (t & 1))) & 255u);
+                const int sB = (int)(int8_t)((scw >> (16 * (t & 1) + 8)) & 255u);
+#pragma unroll
+                for (int m = 0; m < Sink::MT; ++m) {
+                    if (m < ntok) {
+                        const uint32_t tl = xt.tile(m);
+                        uint32_t x[8];
+                        ldx8(tl + 32 * t, x);
+                        const uint32_t xh = lds32(tl + TL::H + 4 * t);
+                        int lo = 0, hi = 0;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
+#pragma unroll
+                        for (int k = 4; k < 8; ++k) hi = dp4a(c[k], x[k], hi);
+                        const int hlo = (int)(int16_t)(xh & 0xffffu), hhi = (int)(int16_t)(xh >> 16);
+                        const int dot = sA * (lo - 32 * hlo) + sB * (hi - 32 * hhi);
+                        const float xd = ldsf(tl + TL::D + 4 * t);
+                        sink.unit(m, t, dot, 0, d * xd * (float)dot);
+                    }
+                }
+            }
+        }
+    }
+};
+
+// ================================================================================ IQ4_XS
 constexpr int8_t kIQ4Codebook[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                      1,    13,   25,  38,  53,  69,  89,  113};
 constexpr uint32_t cb_word(int i) {
@@ -210,74 +318,119 @@ constexpr uint32_t cb_word(int i) {
            ((uint32_t)(uint8_t)kIQ4Codebook[i + 2] << 16) | ((uint32_t)(uint8_t)kIQ4Codebook[i + 3] << 24);
 }
 
-// Codebook lookup of the four 4-bit indices in bits 15:0 of s (one per nibble): two byte
-// permutes over the table halves, then a third that keeps, per byte, the half chosen by the
-// index's bit 3.
-__device__ __forceinline__ uint32_t cb_lookup4(uint32_t s) {
-    const uint32_t lo = prmt(cb_word(0), cb_word(4), s & 0x7777u);
-    const uint32_t hi = prmt(cb_word(8), cb_word(12), s & 0x7777u);
-    return prmt(lo, hi, ((s >> 1) & 0x4444u) | 0x3210u);
+// Codebook values of the 8 indices in q (byte k: low nibble = element k of the unit's first
+// half, high nibble = element k of its second half): byte permutes over the two table
+// halves, then a permute that keeps, per byte, the half chosen by the index's bit 3.
+__device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &hi) {
+    const uint32_t i7 = q & 0x77777777u;
+    const uint32_t pick = ((q >> 1) & 0x44444444u) | 0x32103210u;
+    const uint32_t a0 = prmt(cb_word(0), cb_word(4), i7), b0 = prmt(cb_word(8), cb_word(12), i7);
+    const uint32_t a1 = prmt(cb_word(0), cb_word(4), i7 >> 16), b1 = prmt(cb_word(8), cb_word(12), i7 >> 16);
+    const uint32_t A = prmt(a0, b0, pick);        // values of nibbles (lo b0, hi b0, lo b1, hi b1)
+    const uint32_t B = prmt(a1, b1, pick >> 16);  // values of nibbles (lo b2, hi b2, lo b3, hi b3)
+    lo = prmt(A, B, 0x6420u);
+    hi = prmt(A, B, 0x7531u);
 }
 
-template <>
-struct Fmt<F_IQ4_XS> {
-    static constexpr int QK = 256, BS = 136, UPB = 8;
-    static constexpr bool NEED_XS = false;
-    __device__ __forceinline__ static void decode(uint32_t blk, int ib, WUnit &w) {
-        const uint2 hdr = lds64(blk);  // x: d | scales_h << 16, y: scales_l[0..3]
-        const uint2 qa = lds64(blk + 8 + 16 * ib), qb = lds64(blk + 16 + 16 * ib);
-        const int ls = ((hdr.y >> (4 * ib)) & 15) | (((hdr.x >> (16 + 2 * ib)) & 3) << 4);
-        w.fa = half_bits_to_float(hdr.x) * (float)(ls - 32);
-        const uint32_t qw[4] = {qa.x, qa.y, qb.x, qb.y};
+struct FmtIQ4XS {
+    static constexpr int QK = 256, BS = 136, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 136;
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<8>;
+        const uint2 hdr = lds64(addr);  // x: d | scales_h << 16, y: scales_l[0..3]
+        const float d = half_bits_to_float(hdr.x);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            // nibbles of bytes 0,1 then 2,3: (lo b0, hi b0, lo b1, hi b1)
-            const uint32_t A = cb_lookup4(qw[k]);
-            const uint32_t B = cb_lookup4(qw[k] >> 16);
-            w.c[k] = prmt(A, B, 0x6420u);      // elements 4k..4k+3 (low nibbles)
-            w.c[4 + k] = prmt(A, B, 0x7531u);  // elements 16+4k.. (high nibbles)
+        for (int ib = 0; ib < 8; ++ib) {
+            const uint2 qa = lds64(addr + 8 + 16 * ib), qb = lds64(addr + 16 + 16 * ib);
+            const int ls = (int)(((hdr.y >> (4 * ib)) & 15u) | (((hdr.x >> (16 + 2 * ib)) & 3u) << 4));
+            const float fa = d * (float)(ls - 32);
+            const uint32_t qw[4] = {qa.x, qa.y, qb.x, qb.y};
+            uint32_t c[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cb_lookup8(qw[k], c[k], c[4 + k]);
+#pragma unroll
+            for (int m = 0; m < Sink::MT; ++m) {
+                if (m < ntok) {
+                    const uint32_t t = xt.tile(m);
+                    uint32_t x[8];
+                    ldx8(t + 32 * ib, x);
+                    int dot = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dot = dp4a(c[k], x[k], dot);
+                    sink.unit(m, ib, dot, 0, fa * ldsf(t + TL::D + 4 * ib) * (float)dot);
+                }
+            }
         }
     }
-    __device__ __forceinline__ static int idot(const WUnit &w, const XUnit &x) {
-        int s = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s = dp4a(w.c[k], x.q[k], s);
-        return s;
-    }
-    __device__ __forceinline__ static float accum(float acc, const WUnit &w, int dot, const XUnit &x) {
-        return fmaf(w.fa * x.d, (float)dot, acc);
-    }
 };
 
-// ------------------------------------------------------------------------------- activations
-// Activation codes in shared memory: q at byte ldq*m + 32*xb, d/s at 4*(lds*m + xb).
-struct XSmem {
-    uint32_t q, d, s;
-    int ldq, lds;
-    __device__ __forceinline__ void load(int m, int xb, bool need_s, XUnit &x) const {
-        const uint32_t qa = q + (uint32_t)(m * ldq + 32 * xb);
-        const uint4 a = lds128(qa), b = lds128(qa + 16);
-        x.q[0] = a.x; x.q[1] = a.y; x.q[2] = a.z; x.q[3] = a.w;
-        x.q[4] = b.x; x.q[5] = b.y; x.q[6] = b.z; x.q[7] = b.w;
-        x.d = __uint_as_float(lds32(d + 4u * (uint32_t)(m * lds + xb)));
-        x.s = need_s ? (int)lds32(s + 4u * (uint32_t)(m * lds + xb)) : 0;
-    }
-};
+// ================================================================================ selection
+template <int FMT, int T>
+struct FmtSel;
+template <int T>
+struct FmtSel<F_Q8_0, T> { using type = FmtLegacy<F_Q8_0, T>; };
+template <int T>
+struct FmtSel<F_Q4_0, T> { using type = FmtLegacy<F_Q4_0, T>; };
+template <int T>
+struct FmtSel<F_Q4_K, T> { using type = FmtQ4K; };
+template <int T>
+struct FmtSel<F_Q5_K, T> { using type = FmtQ5K; };
+template <int T>
+struct FmtSel<F_Q6_K, T> { using type = FmtQ6K; };
+template <int T>
+struct FmtSel<F_IQ4_XS, T> { using type = FmtIQ4XS; };
+template <int FMT, int T>
+using FT = typename FmtSel<FMT, T>::type;
 
-// Activation codes in global memory (read-only for the kernel's lifetime).
-struct XGlob {
-    const int8_t *q;
-    const float *d;
-    const int32_t *s;
-    int ldq, lds;
-    __device__ __forceinline__ void load(int m, int xb, bool need_s, XUnit &x) const {
-        const int8_t *qa = q + (size_t)m * ldq + 32 * (size_t)xb;
-        const uint4 a = ldg128_nc(qa), b = ldg128_nc(qa + 16);
-        x.q[0] = a.x; x.q[1] = a.y; x.q[2] = a.z; x.q[3] = a.w;
-        x.q[4] = b.x; x.q[5] = b.y; x.q[6] = b.z; x.q[7] = b.w;
-        x.d = __ldg(d + (size_t)m * lds + xb);
-        x.s = need_s ? __ldg(s + (size_t)m * lds + xb) : 0;
+// ================================================================================ tile writer
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Activation rows -> task-tile image in global memory: tile (row r, task tt) at
+// img + (r * tpr + tt) * tile_stride(xgt).  One warp per activation block; lane i holds
+// element i.  src_f32 != nullptr: quantize fp32 rows (activation quantization rule) --
+// with u != nullptr the rows are h = silu(src_f32) * u (SwiGLU), also stored to h_out when
+// given -- else repack already-quantized rows (q: row pitch K; d/s: row pitch K/32).
+// mq/md/ms (nullable): the quantized rows in their plain layout as well.
+__device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const float *u, float *h_out, const int8_t *q,
+                                                const float *d, const int32_t *s, int rows, int K, int xgt_log2,
+                                                uint8_t *img, int8_t *mq, float *md, int32_t *ms, long wid,
+                                                long nwarps) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32, xgt = 1 << xgt_log2, tpr = nb >> xgt_log2, stride = tile_stride(xgt);
+    for (long w = wid; w < (long)rows * nb; w += nwarps) {
+        const int r = (int)(w / nb), b = (int)(w - (long)r * nb);
+        int qi, si;
+        float di;
+        if (src_f32) {
+            const long idx = (long)r * K + 32L * b + lane;
+            float v = src_f32[idx];
+            if (u) {
+                v = silu_mul(v, u[idx]);
+                if (h_out) h_out[idx] = v;
+            }
+            quant_block_warp(v, qi, di, si);
+        } else {
+            qi = q[(long)r * K + 32L * b + lane];
+            di = d[(long)r * nb + b];
+            si = s[(long)r * nb + b];
+        }
+        uint8_t *t = img + ((long)r * tpr + (b >> xgt_log2)) * stride;
+        const int u = b & (xgt - 1);
+        t[32 * u + lane] = (uint8_t)qi;
+        const int h16 = __reduce_add_sync(0xffffffffu, lane < 16 ? qi : 0);
+        if (lane == 0) {
+            reinterpret_cast<float *>(t + 32 * xgt)[u] = di;
+            reinterpret_cast<int32_t *>(t + 36 * xgt)[u] = si;
+            reinterpret_cast<uint32_t *>(t + 40 * xgt)[u] = ((uint32_t)h16 & 0xffffu) | ((uint32_t)(si - h16) << 16);
+        }
+        if (mq) {
+            mq[(long)r * K + 32L * b + lane] = (int8_t)qi;
+            if (lane == 0) {
+                md[(long)r * nb + b] = di;
+                ms[(long)r * nb + b] = si;
+            }
+        }
     }
-};
+}
 
 }  // namespace qg

@@ -1,352 +1,175 @@
-// qg_jobs.cuh -- stage sequences, activation sources, prologues and epilogues of the
-// four GEMV-shaped operations run by the streaming engine (qg_engine.cuh):
+// qg_jobs.cuh -- the four GEMV-shaped operations as output-row jobs for the streaming
+// engine (qg_engine.cuh):
 //
-//   GemvJob       y = W x (optionally one K-slice per CTA, partial sums to a buffer)
-//   FfnGateUpJob  g = Wg x, u = Wu x in one pass over both matrices, h = silu(g)*u
-//   MoeGateUpJob  the same for each token's routed experts and the shared expert, with
-//                 the softmax/top-k of the router computed by the producer warp
-//   MoeDownJob    o = Wd_e h for every slot, y = sum_routed w*o + o_shared (slot order)
+//   GemvJob        output row n = row n of W (optionally one K-slice per CTA: split-K,
+//                  partial sums to a buffer)
+//   FfnGateUpJob   output rows 0..I-1 = rows of Wg (g), I..2I-1 = rows of Wu (u)
+//   MoeGateUpJob   output rows of g and u for every (token, slot): the slot's routed expert
+//                  (from the router's top-k, computed by the producer warp) or the shared one
+//   MoeDownJob     per CTA, a range of hidden rows n: output rows (token, slot, n) of every
+//                  slot's down matrix, kept in shared memory; the epilogue forms
+//                  y[token][n] = sum over slots, in slot order, of weight * row (shared
+//                  expert: weight 1) -- the weighted aggregation of the expert outputs
+//
+// Engine interface: HAS_FINISH; fields depth, slot_bytes, x_bytes, j_bytes, tpr_x, tps,
+// ntok; cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store, init,
+// finish, producer_prologue.  Activation images (prep_tiles_warp) have one row of task
+// tiles per token (or per MoE slot), row pitch tpr * tile_stride(XGT).
 #pragma once
-
-#include <type_traits>
 
 #include "qg_engine.cuh"
 
 namespace qg {
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
-
-// Consumers quantize `rows` activation rows of `cols` fp32 values (cols a multiple of 32)
-// into shared memory: codes at q + r*ldq + c, scales/sums at d/s + 4*(r*lds + c/32).
-// Optionally mirror the result to global memory (gq/gd/gs, row pitch cols).
-__device__ __forceinline__ void quantize_rows_to_smem(const float *src, long src_ld, int rows, int cols,
-                                                      uint32_t q, uint32_t d, uint32_t s, int ldq, int lds,
-                                                      int tid, int8_t *gq, float *gd, int32_t *gs) {
-    const int warp = tid >> 5, lane = tid & 31;
-    const int nb = cols / 32;
-    for (int w = warp; w < rows * nb; w += NCW) {
-        const int r = w / nb, b = w - r * nb;
-        const float v = src[(long)r * src_ld + 32 * b + lane];
-        int qi, si;
-        float di;
-        quant_block_warp(v, qi, di, si);
-        sts8(q + (uint32_t)(r * ldq + 32 * b + lane), (uint32_t)qi & 255u);
-        if (gq) gq[(long)r * cols + 32 * b + lane] = (int8_t)qi;
-        if (lane == 0) {
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(d + 4u * (uint32_t)(r * lds + b)), "f"(di) : "memory");
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(s + 4u * (uint32_t)(r * lds + b)), "r"(si) : "memory");
-            if (gd) {
-                gd[(long)r * nb + b] = di;
-                gs[(long)r * nb + b] = si;
-            }
-        }
-    }
-}
-
-// Byte offsets of a quantized-activation area inside a job's shared memory.
-struct XArea {
-    uint32_t q, d, s, bytes;
-    int ldq, lds;
+struct EngineFields {
+    int depth;                          // ring slots per consumer warp
+    uint32_t slot_bytes, x_bytes, j_bytes;
+    int tpr_x, tps, ntok;
 };
-__host__ __device__ inline XArea make_xarea(uint32_t base, int rows, int cols) {
-    XArea a;
-    a.ldq = cols;
-    a.lds = cols / 32;
-    a.q = base;
-    a.d = base + (uint32_t)(((long)rows * cols + 15) / 16 * 16);
-    a.s = a.d + 4u * (uint32_t)(rows * a.lds);
-    a.bytes = a.s + 4u * (uint32_t)(rows * a.lds) - base;
-    return a;
-}
 
 // ===================================================================================== GEMV
-template <int FMT, bool XSM>
-struct GemvJob {
-    using F = Fmt<FMT>;
-    using XSrc = typename std::conditional<XSM, XSmem, XGlob>::type;
-    struct Cursor {
-        int row, blk, r0, r1, b0, b1, ks;
-        bool valid;
-    };
-    // engine
-    int nslots;
-    uint32_t slot_bytes, job_smem_bytes;
-    // problem
+template <int FMT, int T>
+struct GemvJob : EngineFields {
+    using F = FT<FMT, T>;
+    static constexpr bool HAS_FINISH = false;
     const uint8_t *W, *Wend;
-    int N, K, M, nbr, KS, groups, R, segb;  // segb == 0: whole rows per stage
+    int N, KS, groups, gpr;  // gpr: task groups (whole blocks) per row
     uint32_t rb;
-    const float *x;                         // XSM: fp32 activations (M x K)
-    const int8_t *xq;                       // !XSM: quantized activations
-    const float *xd;
-    const int32_t *xs;
-    float *out;                             // y (KS == 1) or partials [KS][M][N]
+    const uint8_t *ximg;
+    uint32_t ximg_pitch;
+    float *out;  // y (KS == 1) or partials [KS][M][N]
     long slice_stride;
-    uint32_t x_off;                         // XSM: offset of the x area in job smem
-    int kslice_max;                         // XSM: activation columns reserved per token
 
-    __device__ void first(Cursor &c) const {
-        c.ks = blockIdx.x % KS;
+    __device__ int ks() const { return blockIdx.x % KS; }
+    __device__ int t0() const { return (int)((long)ks() * gpr / KS) * F::TPB; }
+    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
         const int g = blockIdx.x / KS;
-        c.r0 = (int)((long)g * N / groups);
-        c.r1 = (int)((long)(g + 1) * N / groups);
-        c.b0 = (int)((long)c.ks * nbr / KS);
-        c.b1 = (int)((long)(c.ks + 1) * nbr / KS);
-        c.row = c.r0;
-        c.blk = c.b0;
-        c.valid = c.r0 < c.r1 && c.b0 < c.b1;
+        o0 = (int)((long)g * N / groups);
+        o1 = (int)((long)(g + 1) * N / groups);
+        tpr = (int)((long)(ks() + 1) * gpr / KS) * F::TPB - t0();
+        grp = KS == 1 ? 0 : 1;  // slices of consecutive rows are not adjacent
     }
-    __device__ void next(Cursor &c) const {
-        if (segb == 0) {
-            c.row += R;
-        } else {
-            c.blk += segb;
-            if (c.blk >= c.b1) {
-                c.blk = c.b0;
-                ++c.row;
-            }
-        }
-        c.valid = c.row < c.r1;
+    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
+        lim = Wend;
+        return W + (size_t)o * rb + task_off<F>(t0() + tt);
     }
-    __device__ void stage(const Cursor &c, uint8_t *, bool, Stage &st) const {
-        if (segb == 0) {
-            const int nr = min(R, c.r1 - c.row);
-            st.src[0] = W + (size_t)c.row * rb;
-            st.bytes[0] = (uint32_t)nr * rb;
-            st.R = nr;
-            st.nblk = nbr;
-            st.xb0 = 0;
-            st.tag1 = 1;
-        } else {
-            const int nb = min(segb, c.b1 - c.blk);
-            st.src[0] = W + (size_t)c.row * rb + (size_t)c.blk * F::BS;
-            st.bytes[0] = (uint32_t)(nb * F::BS);
-            st.R = 1;
-            st.nblk = nb;
-            st.xb0 = (XSM ? (c.blk - c.b0) : c.blk) * F::UPB;
-            st.tag1 = (c.blk + nb >= c.b1);
-        }
-        st.src[1] = st.src[0];
-        st.lim[0] = st.lim[1] = Wend;
-        st.bytes[1] = 0;
-        st.nseg = 1;
-        st.rstride = rb;
-        st.xm = 0;
-        st.ntok = M;
-        st.tag0 = c.row;
-        st.tag2 = c.ks;
+    __device__ int xrows() const { return ntok; }
+    __device__ const uint8_t *xrow_src(int r) const {
+        return ximg + (size_t)r * ximg_pitch + (size_t)t0() * tile_stride(F::XGT);
     }
-    __device__ XSrc xsrc(uint8_t *, uint32_t job_base) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(job_base + x_off, M, kslice_max);
-            return XSmem{a.q, a.d, a.s, a.ldq, a.lds};
-        } else {
-            return XGlob{xq, xd, xs, K, K / 32};
-        }
+    __device__ uint32_t xrow_bytes(int) const {
+        int o0, o1, tpr, grp;
+        cta(o0, o1, tpr, grp);
+        return (uint32_t)(tpr * tile_stride(F::XGT));
     }
-    __device__ void producer_prologue(uint8_t *, int) const {}
-    __device__ void consumer_prologue(uint8_t *js, int tid) const {
-        float *racc = reinterpret_cast<float *>(js);
-        if (tid < 16) racc[tid] = 0.0f;
-        if constexpr (XSM) {
-            Cursor c;
-            first(c);
-            if (!c.valid) return;
-            const int c0 = c.b0 * F::QK, cols = (c.b1 - c.b0) * F::QK;
-            const uint32_t base = smem_addr(js) + x_off;
-            const XArea a = make_xarea(base, M, kslice_max);
-            quantize_rows_to_smem(x + c0, K, M, cols, a.q, a.d, a.s, a.ldq, a.lds, tid, nullptr, nullptr,
-                                  nullptr);
-        }
+    __device__ uint32_t xrow(int, const FastDiv &) const { return 0; }
+    __device__ void store(int o, int m, float v, float *) const {
+        out[(long)ks() * slice_stride + (long)m * N + o] = v;
     }
-    template <int MT>
-    __device__ void epilogue(const Stage &st, float *part, uint8_t *js, int tid) const {
-        float *o = out + (long)st.tag2 * slice_stride;
-        if (segb == 0) {
-            for (int idx = tid; idx < st.R * M; idx += NCONS) {
-                const int i = idx / M, m = idx - i * M;
-                o[(long)m * N + st.tag0 + i] = part_take<MT>(part, i, m);
-            }
-        } else if (tid < M) {
-            float *racc = reinterpret_cast<float *>(js);
-            const float v = racc[tid] + part_take<MT>(part, 0, tid);
-            if (st.tag1) {
-                o[(long)tid * N + st.tag0] = v;
-                racc[tid] = 0.0f;
-            } else {
-                racc[tid] = v;
-            }
-        }
-    }
+    __device__ void init(float *, int) const {}
+    __device__ void finish(float *, int, int) const {}
+    __device__ void producer_prologue(int, int *) const {}
 };
 
 // ===================================================================================== FFN gate/up
-template <int FMT, bool XSM>
-struct FfnGateUpJob {
-    using F = Fmt<FMT>;
-    using XSrc = typename std::conditional<XSM, XSmem, XGlob>::type;
-    struct Cursor {
-        int row, r1;
-        bool valid;
-    };
-    int nslots;
-    uint32_t slot_bytes, job_smem_bytes;
+template <int FMT, int T>
+struct FfnGateUpJob : EngineFields {
+    using F = FT<FMT, T>;
+    static constexpr bool HAS_FINISH = false;
     const uint8_t *Wg, *Wu, *Wg_end, *Wu_end;
-    int H, I, M, nbr, R;
+    int I, m0;  // tokens [m0, m0 + ntok) of the batch
     uint32_t rb;
-    const float *x;
-    const int8_t *xq;
-    const float *xd;
-    const int32_t *xs;
-    float *g_out, *u_out, *h_out;  // M x I
-    uint32_t x_off;
+    const uint8_t *ximg;
+    uint32_t ximg_pitch;
+    float *g_out, *u_out;  // row pitch I, whole batch
 
-    __device__ void first(Cursor &c) const {
-        c.row = (int)((long)blockIdx.x * I / gridDim.x);
-        c.r1 = (int)((long)(blockIdx.x + 1) * I / gridDim.x);
-        c.valid = c.row < c.r1;
+    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
+        o0 = (int)((long)blockIdx.x * 2 * I / gridDim.x);
+        o1 = (int)((long)(blockIdx.x + 1) * 2 * I / gridDim.x);
+        tpr = tpr_x;
+        grp = I;
     }
-    __device__ void next(Cursor &c) const {
-        c.row += R;
-        c.valid = c.row < c.r1;
+    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
+        const bool up = o >= I;
+        lim = up ? Wu_end : Wg_end;
+        return (up ? Wu : Wg) + (size_t)(up ? o - I : o) * rb + task_off<F>(tt);
     }
-    __device__ void stage(const Cursor &c, uint8_t *, bool, Stage &st) const {
-        const int nr = min(R, c.r1 - c.row);
-        st.src[0] = Wg + (size_t)c.row * rb;
-        st.src[1] = Wu + (size_t)c.row * rb;
-        st.lim[0] = Wg_end;
-        st.lim[1] = Wu_end;
-        st.bytes[0] = st.bytes[1] = (uint32_t)nr * rb;
-        st.nseg = 2;
-        st.R = nr;
-        st.rstride = rb;
-        st.nblk = nbr;
-        st.xb0 = 0;
-        st.xm = 0;
-        st.ntok = M;
-        st.tag0 = c.row;
-        st.tag1 = st.tag2 = 0;
+    __device__ int xrows() const { return ntok; }
+    __device__ const uint8_t *xrow_src(int r) const { return ximg + (size_t)(m0 + r) * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(int, const FastDiv &) const { return 0; }
+    __device__ void store(int o, int m, float v, float *) const {
+        if (o < I)
+            g_out[(long)(m0 + m) * I + o] = v;
+        else
+            u_out[(long)(m0 + m) * I + o - I] = v;
     }
-    __device__ XSrc xsrc(uint8_t *, uint32_t job_base) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(job_base + x_off, M, H);
-            return XSmem{a.q, a.d, a.s, a.ldq, a.lds};
-        } else {
-            return XGlob{xq, xd, xs, H, H / 32};
-        }
-    }
-    __device__ void producer_prologue(uint8_t *, int) const {}
-    __device__ void consumer_prologue(uint8_t *js, int tid) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(smem_addr(js) + x_off, M, H);
-            quantize_rows_to_smem(x, H, M, H, a.q, a.d, a.s, a.ldq, a.lds, tid, nullptr, nullptr, nullptr);
-        }
-    }
-    template <int MT>
-    __device__ void epilogue(const Stage &st, float *part, uint8_t *, int tid) const {
-        for (int idx = tid; idx < st.R * M; idx += NCONS) {
-            const int i = idx / M, m = idx - i * M;
-            const float g = part_take<MT>(part, i, m);
-            const float u = part_take<MT>(part, st.R + i, m);
-            const long o = (long)m * I + st.tag0 + i;
-            g_out[o] = g;
-            u_out[o] = u;
-            h_out[o] = silu_mul(g, u);
-        }
-    }
+    __device__ void init(float *, int) const {}
+    __device__ void finish(float *, int, int) const {}
+    __device__ void producer_prologue(int, int *) const {}
 };
 
 // ===================================================================================== MoE gate/up
 constexpr int TOPK_MAX = 16;
 constexpr int E_MAX = 1024;
 
-template <int FMT, bool XSM>
-struct MoeGateUpJob {
-    using F = Fmt<FMT>;
-    using XSrc = typename std::conditional<XSM, XSmem, XGlob>::type;
-    struct Cursor {
-        long p, p1;
-        bool valid;
-    };
-    int nslots;
-    uint32_t slot_bytes, job_smem_bytes;
+template <int FMT, int T>
+struct MoeGateUpJob : EngineFields {
+    using F = FT<FMT, T>;
+    static constexpr bool HAS_FINISH = false;
     const uint8_t *Wg_exps, *Wu_exps, *Wg_sh, *Wu_sh;
     const uint8_t *Wg_exps_end, *Wu_exps_end, *Wg_sh_end, *Wu_sh_end;
-    int E, topk, H, I, M, nbr, R;
+    int E, topk, I, M;
+    FastDiv div_slots;           // by topk + 1
     uint32_t rb;
     size_t ebytes;               // bytes of one expert matrix
-    const float *logits;         // M x E
+    const float *logits;         // M x E (written by the previous kernel)
     int32_t *ids_ws;             // M x topk (always written)
     float *w_ws;
     int32_t *ids_out;            // nullable
     float *w_out;
-    const float *x;
-    const int8_t *xq;
-    const float *xd;
-    const int32_t *xs;
-    float *g_out, *u_out, *h_out;  // [M][topk+1][I]
-    uint32_t x_off;                // job smem: [ids M*topk int32][x area]
+    const uint8_t *ximg;
+    uint32_t ximg_pitch;
+    float *g_out, *u_out;        // [M][topk+1][I]
 
     __device__ int slots() const { return topk + 1; }
-    __device__ void first(Cursor &c) const {
-        const long P = (long)M * slots() * I;
-        c.p = P * blockIdx.x / gridDim.x;
-        c.p1 = P * (blockIdx.x + 1) / gridDim.x;
-        c.valid = c.p < c.p1;
+    // o = ((token * slots + slot) * 2 + up) * I + j; groups of I rows are one matrix
+    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
+        const long P = (long)M * slots() * 2 * I;
+        o0 = (int)(P * blockIdx.x / gridDim.x);
+        o1 = (int)(P * (blockIdx.x + 1) / gridDim.x);
+        tpr = tpr_x;
+        grp = I;
     }
-    __device__ int rows_of(const Cursor &c) const {
-        const int j = (int)(c.p % I);
-        return (int)min((long)R, min(c.p1 - c.p, (long)(I - j)));
-    }
-    __device__ void next(Cursor &c) const {
-        c.p += rows_of(c);
-        c.valid = c.p < c.p1;
-    }
-    __device__ void stage(const Cursor &c, uint8_t *js, bool producer, Stage &st) const {
-        const int gs = (int)(c.p / I), j = (int)(c.p % I);
-        const int nr = rows_of(c);
+    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *ids) const {
+        const int q = o / I, j = o - q * I, up = q & 1, gs = q >> 1;
         const int m = gs / slots(), s = gs - m * slots();
-        st.src[0] = st.src[1] = nullptr;
-        st.lim[0] = st.lim[1] = nullptr;
-        if (producer) {
-            const int32_t *ids = reinterpret_cast<const int32_t *>(js);
-            if (s < topk) {
-                const size_t e = (size_t)min(max(ids[m * topk + s], 0), E - 1);  // never leave the tensor
-                st.src[0] = Wg_exps + e * ebytes + (size_t)j * rb;
-                st.src[1] = Wu_exps + e * ebytes + (size_t)j * rb;
-                st.lim[0] = Wg_exps_end;
-                st.lim[1] = Wu_exps_end;
-            } else {
-                st.src[0] = Wg_sh + (size_t)j * rb;
-                st.src[1] = Wu_sh + (size_t)j * rb;
-                st.lim[0] = Wg_sh_end;
-                st.lim[1] = Wu_sh_end;
-            }
+        if (s < topk) {
+            const size_t e = (size_t)min(max(ids[m * topk + s], 0), E - 1);  // never leave the tensor
+            lim = up ? Wu_exps_end : Wg_exps_end;
+            return (up ? Wu_exps : Wg_exps) + e * ebytes + (size_t)j * rb + task_off<F>(tt);
         }
-        st.bytes[0] = st.bytes[1] = (uint32_t)nr * rb;
-        st.nseg = 2;
-        st.R = nr;
-        st.rstride = rb;
-        st.nblk = nbr;
-        st.xb0 = 0;
-        st.xm = m;
-        st.ntok = 1;
-        st.tag0 = gs;
-        st.tag1 = j;
-        st.tag2 = 0;
+        lim = up ? Wu_sh_end : Wg_sh_end;
+        return (up ? Wu_sh : Wg_sh) + (size_t)j * rb + task_off<F>(tt);
     }
-    __device__ XSrc xsrc(uint8_t *, uint32_t job_base) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(job_base + x_off, M, H);
-            return XSmem{a.q, a.d, a.s, a.ldq, a.lds};
-        } else {
-            return XGlob{xq, xd, xs, H, H / 32};
-        }
+    __device__ int xrows() const { return M; }
+    __device__ const uint8_t *xrow_src(int r) const { return ximg + (size_t)r * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(int o, const FastDiv &divI) const {
+        return div_slots.div(divI.div((uint32_t)o) >> 1);  // token
     }
-    // Router tail, one warp: softmax over E logits, the topk largest (ties: lower id),
-    // weights renormalized over the picks.  exp(l - max) / sum over the picks equals
-    // p / sum(p over the picks) for the softmax probabilities p.
-    __device__ void producer_prologue(uint8_t *js, int lane) const {
-        int32_t *ids = reinterpret_cast<int32_t *>(js);
+    __device__ void store(int o, int, float v, float *) const {
+        const int q = o / I, j = o - q * I;
+        ((q & 1) ? u_out : g_out)[(long)(q >> 1) * I + j] = v;
+    }
+    __device__ void init(float *, int) const {}
+    __device__ void finish(float *, int, int) const {}
+    // Router tail, one warp, after the logits kernel has finished: softmax over E logits,
+    // the topk largest (ties: lower id), weights renormalized over the picks.
+    // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax
+    // probabilities p.
+    __device__ void producer_prologue(int lane, int *ids) const {
+        griddep_wait();
         for (int m = 0; m < M; ++m) {
             float v[E_MAX / 32];
             float lmax = -INFINITY;
@@ -359,190 +182,115 @@ struct MoeGateUpJob {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
             uint32_t taken = 0;
-            int sel[TOPK_MAX];
-            float ev[TOPK_MAX];
             float esum = 0.0f;
+            int my_sel = 0;
+            float my_ev = 0.0f;
+            for (int r = 0; r < topk; ++r) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
 #pragma unroll
-            for (int r = 0; r < TOPK_MAX; ++r) {
-                sel[r] = 0;
-                ev[r] = 0.0f;
-                if (r < topk) {
-                    float bv = -INFINITY;
-                    int be = 0x7fffffff;
-#pragma unroll
-                    for (int i = 0; i < E_MAX / 32; ++i) {
-                        const int e = lane + 32 * i;
-                        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || be == 0x7fffffff)) {
-                            bv = v[i];
-                            be = e;
-                        }
+                for (int i = 0; i < E_MAX / 32; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !((taken >> i) & 1u) && (v[i] > bv || be == 0x7fffffff)) {
+                        bv = v[i];
+                        be = e;
                     }
+                }
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                        if (ov > bv || (ov == bv && oe < be)) {
-                            bv = ov;
-                            be = oe;
-                        }
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ov > bv || (ov == bv && oe < be)) {
+                        bv = ov;
+                        be = oe;
                     }
-                    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                    sel[r] = be;
-                    ev[r] = expf(bv - lmax);
-                    esum += ev[r];
+                }
+                if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                const float ev = expf(bv - lmax);
+                esum += ev;
+                if (lane == r) {
+                    my_sel = be;
+                    my_ev = ev;
                 }
             }
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < TOPK_MAX; ++r) {
-                    if (r < topk) {
-                        const float w = ev[r] / esum;
-                        ids[m * topk + r] = sel[r];
-                        if (blockIdx.x == 0) {
-                            ids_ws[m * topk + r] = sel[r];
-                            w_ws[m * topk + r] = w;
-                            if (ids_out) ids_out[m * topk + r] = sel[r];
-                            if (w_out) w_out[m * topk + r] = w;
-                        }
-                    }
+            if (lane < topk) {
+                const float w = my_ev / esum;
+                ids[m * topk + lane] = my_sel;
+                if (blockIdx.x == 0) {
+                    ids_ws[m * topk + lane] = my_sel;
+                    w_ws[m * topk + lane] = w;
+                    if (ids_out) ids_out[m * topk + lane] = my_sel;
+                    if (w_out) w_out[m * topk + lane] = w;
                 }
             }
             __syncwarp();
         }
     }
-    __device__ void consumer_prologue(uint8_t *js, int tid) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(smem_addr(js) + x_off, M, H);
-            quantize_rows_to_smem(x, H, M, H, a.q, a.d, a.s, a.ldq, a.lds, tid, nullptr, nullptr, nullptr);
-        }
-    }
-    template <int MT>
-    __device__ void epilogue(const Stage &st, float *part, uint8_t *, int tid) const {
-        for (int i = tid; i < st.R; i += NCONS) {
-            const float g = part_take<MT>(part, i, 0);
-            const float u = part_take<MT>(part, st.R + i, 0);
-            const long o = (long)st.tag0 * I + st.tag1 + i;
-            g_out[o] = g;
-            u_out[o] = u;
-            h_out[o] = silu_mul(g, u);
-        }
-    }
 };
 
 // ===================================================================================== MoE down
-template <int FMT, bool XSM>
-struct MoeDownJob {
-    using F = Fmt<FMT>;
-    using XSrc = typename std::conditional<XSM, XSmem, XGlob>::type;
-    struct Cursor {
-        int m, s, n, n0, n1;
-        bool valid;
-    };
-    int nslots;
-    uint32_t slot_bytes, job_smem_bytes;
+template <int FMT, int T>
+struct MoeDownJob : EngineFields {
+    using F = FT<FMT, T>;
+    static constexpr bool HAS_FINISH = true;
     const uint8_t *Wd_exps, *Wd_sh, *Wd_exps_end, *Wd_sh_end;
-    int E, topk, H, I, M, nbr, R, nloc_max;
+    int E, topk, H, M, m0;          // tokens [m0, m0 + M) of the batch
     uint32_t rb;
     size_t ebytes;
-    const int32_t *ids_ws;
+    const int32_t *ids_ws;          // [batch][topk] (written by the gate/up kernel)
     const float *w_ws;
-    const float *h;                 // [M][S][I] fp32 (XSM: quantized here)
-    const int8_t *hq;               // !XSM: requantized h in global memory
-    const float *hd;
-    const int32_t *hs;
-    int8_t *hq_ws;                  // XSM: CTA 0 mirrors its requantization here
-    float *hd_ws;
-    int32_t *hs_ws;
-    float *y;                       // M x H
-    uint32_t x_off;                 // job smem: [yacc M*nloc_max fp32][x area]
+    const uint8_t *ximg;            // requantized h: one image row per (token, slot)
+    uint32_t ximg_pitch;
+    float *y;                       // [batch][H]
 
     __device__ int slots() const { return topk + 1; }
-    __device__ void first(Cursor &c) const {
-        c.n0 = (int)((long)blockIdx.x * H / gridDim.x);
-        c.n1 = (int)((long)(blockIdx.x + 1) * H / gridDim.x);
-        c.m = 0;
-        c.s = 0;
-        c.n = c.n0;
-        c.valid = c.n0 < c.n1;
+    __device__ void nrange(int &n0, int &n1) const {
+        n0 = (int)((long)blockIdx.x * H / gridDim.x);
+        n1 = (int)((long)(blockIdx.x + 1) * H / gridDim.x);
     }
-    __device__ void next(Cursor &c) const {
-        c.n += R;
-        if (c.n >= c.n1) {
-            c.n = c.n0;
-            if (++c.s == slots()) {
-                c.s = 0;
-                ++c.m;
+    // CTA-local rows o = (token * slots + slot) * nloc + r, r < nloc = n1 - n0
+    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
+        int n0, n1;
+        nrange(n0, n1);
+        o0 = 0;
+        o1 = M * slots() * (n1 - n0);
+        tpr = tpr_x;
+        grp = n1 - n0;
+    }
+    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
+        int n0, n1;
+        nrange(n0, n1);
+        const int nloc = n1 - n0, q = o / nloc, r = o - q * nloc;
+        const int m = q / slots(), s = q - m * slots();
+        if (s < topk) {
+            const size_t e = (size_t)min(max(ids_ws[(m0 + m) * topk + s], 0), E - 1);
+            lim = Wd_exps_end;
+            return Wd_exps + e * ebytes + (size_t)(n0 + r) * rb + task_off<F>(tt);
+        }
+        lim = Wd_sh_end;
+        return Wd_sh + (size_t)(n0 + r) * rb + task_off<F>(tt);
+    }
+    __device__ int xrows() const { return M * slots(); }
+    __device__ const uint8_t *xrow_src(int r) const { return ximg + ((size_t)m0 * slots() + r) * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(int o, const FastDiv &divn) const { return divn.div((uint32_t)o); }  // token*slots+slot
+    __device__ void store(int o, int, float v, float *part) const { part[o] = v; }
+    __device__ void init(float *, int) const {}
+    __device__ void finish(float *part, int tid, int nthreads) const {
+        int n0, n1;
+        nrange(n0, n1);
+        const int nloc = n1 - n0;
+        for (int i = tid; i < M * nloc; i += nthreads) {
+            const int m = i / nloc, r = i - m * nloc;
+            float acc = 0.0f;
+            for (int s = 0; s < slots(); ++s) {
+                const float ws = s < topk ? w_ws[(m0 + m) * topk + s] : 1.0f;  // shared expert: weight 1
+                acc = fmaf(ws, part[(m * slots() + s) * nloc + r], acc);
             }
-        }
-        c.valid = c.m < M;
-    }
-    __device__ void stage(const Cursor &c, uint8_t *, bool producer, Stage &st) const {
-        const int nr = min(R, c.n1 - c.n);
-        st.src[0] = st.src[1] = nullptr;
-        st.lim[0] = st.lim[1] = nullptr;
-        if (producer) {
-            if (c.s < topk) {
-                const size_t e = (size_t)min(max(ids_ws[c.m * topk + c.s], 0), E - 1);
-                st.src[0] = Wd_exps + e * ebytes + (size_t)c.n * rb;
-                st.lim[0] = Wd_exps_end;
-            } else {
-                st.src[0] = Wd_sh + (size_t)c.n * rb;
-                st.lim[0] = Wd_sh_end;
-            }
-            st.src[1] = st.src[0];
-            st.lim[1] = st.lim[0];
-        }
-        st.bytes[0] = (uint32_t)nr * rb;
-        st.bytes[1] = 0;
-        st.nseg = 1;
-        st.R = nr;
-        st.rstride = rb;
-        st.nblk = nbr;
-        st.xb0 = 0;
-        st.xm = c.m * slots() + c.s;
-        st.ntok = 1;
-        st.tag0 = c.m;
-        st.tag1 = c.s;
-        st.tag2 = c.n - c.n0;
-    }
-    __device__ XSrc xsrc(uint8_t *, uint32_t job_base) const {
-        if constexpr (XSM) {
-            const XArea a = make_xarea(job_base + x_off, M * (topk + 1), I);
-            return XSmem{a.q, a.d, a.s, a.ldq, a.lds};
-        } else {
-            return XGlob{hq, hd, hs, I, I / 32};
+            y[(long)(m0 + m) * H + n0 + r] = acc;
         }
     }
-    __device__ void producer_prologue(uint8_t *, int) const {}
-    __device__ void consumer_prologue(uint8_t *js, int tid) const {
-        float *yacc = reinterpret_cast<float *>(js);
-        for (int i = tid; i < M * nloc_max; i += NCONS) yacc[i] = 0.0f;
-        if constexpr (XSM) {
-            const int rows = M * (topk + 1);
-            const XArea a = make_xarea(smem_addr(js) + x_off, rows, I);
-            const bool mirror = blockIdx.x == 0;
-            quantize_rows_to_smem(h, I, rows, I, a.q, a.d, a.s, a.ldq, a.lds, tid, mirror ? hq_ws : nullptr,
-                                  mirror ? hd_ws : nullptr, mirror ? hs_ws : nullptr);
-        }
-    }
-    template <int MT>
-    __device__ void epilogue(const Stage &st, float *part, uint8_t *js, int tid) const {
-        float *yacc = reinterpret_cast<float *>(js);
-        const int m = st.tag0, s = st.tag1;
-        const float wgt = s < topk ? w_ws[m * topk + s] : 1.0f;  // shared expert: weight 1
-        for (int i = tid; i < st.R; i += NCONS) {
-            const float o = part_take<MT>(part, i, 0);
-            float *a = yacc + m * nloc_max + st.tag2 + i;
-            const float v = fmaf(wgt, o, *a);
-            if (s == topk) {
-                Cursor c;
-                first(c);
-                y[(long)m * H + c.n0 + st.tag2 + i] = v;
-            } else {
-                *a = v;
-            }
-        }
-    }
+    __device__ void producer_prologue(int, int *) const {}
 };
 
 }  // namespace qg

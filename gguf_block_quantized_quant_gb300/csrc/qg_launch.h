@@ -14,6 +14,8 @@ struct GemvCall {
     const uint8_t *W;
     int N, K, M;
     const float *x;     // fp32 activations, or NULL when xq/xd/xs are given
+    const float *u;     // optional: the activations are silu(x) * u (written to h_out if set)
+    float *h_out;
     const int8_t *xq;
     const float *xd;
     const int32_t *xs;
@@ -75,6 +77,15 @@ int dev_err_take(unsigned int *err);  // read and clear the format's device erro
 int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *xd, int32_t *xs,
                      cudaStream_t s);
 int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStream_t s);
-int launch_router_logits(const float *x, int M, int H, const float *Wr, int E, float *logits, cudaStream_t s);
+// Activation tile image of `rows` rows of K elements (tiles of 2^xgt_log2 activation blocks),
+// from fp32 rows x (quantized here; with u != NULL the rows are silu(x) * u, also written to
+// h_out when given) or from xq/xd/xs; mq/md/ms optionally receive the quantized rows in
+// their plain layout.
+int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t *xq, const float *xd,
+                      const int32_t *xs, int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq, float *md,
+                      int32_t *ms, cudaStream_t s);
+// Router logits (fp32) and the activation tile image of x in one launch.
+int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,
+                       uint8_t *img, cudaStream_t s);
 
 }  // namespace qg

@@ -2,8 +2,7 @@
 //
 // Everything here is a pure function of the problem shape and the device's SM count, so
 // qg_workspace_size() and the launchers always agree.  The split-K factor depends on the
-// shape only (never on the device), which keeps the order of every floating-point sum
-// independent of the GPU the call runs on.
+// shape only (never on the device).
 #pragma once
 
 #include <stddef.h>
@@ -11,115 +10,142 @@
 
 #include <algorithm>
 
-#include "qg_common.cuh"
+#include "qg_engine.cuh"
 
 namespace qg {
 
 struct FmtInfo {
-    int qk, bs, upb;
+    int qk, bs;
 };
 
 inline bool fmt_info(int fmt, FmtInfo &f) {
     switch (fmt) {
-    case 2: f = {32, 18, 1}; return true;     // Q4_0
-    case 8: f = {32, 34, 1}; return true;     // Q8_0
-    case 12: f = {256, 144, 8}; return true;  // Q4_K
-    case 13: f = {256, 176, 8}; return true;  // Q5_K
-    case 14: f = {256, 210, 8}; return true;  // Q6_K
-    case 23: f = {256, 136, 8}; return true;  // IQ4_XS
+    case 2: f = {32, 18}; return true;     // Q4_0
+    case 8: f = {32, 34}; return true;     // Q8_0
+    case 12: f = {256, 144}; return true;  // Q4_K
+    case 13: f = {256, 176}; return true;  // Q5_K
+    case 14: f = {256, 210}; return true;  // Q6_K
+    case 23: f = {256, 136}; return true;  // IQ4_XS
     default: return false;
     }
 }
 
-constexpr int G_PLAN = 152;                    // split-K planning constant
-constexpr uint32_t XSMEM_CAP = 96 * 1024;      // activation codes kept in shared memory
-constexpr uint32_t STAGE_TARGET = 32 * 1024;   // bytes of weights per ring slot
-constexpr int MAX_SLOTS = 16;
+constexpr int G_PLAN = 152;               // split-K planning constant
+constexpr uint32_t XCAP = 140 * 1024;     // activation tiles held by one CTA
+constexpr int DMAX = 4;                   // ring slots per consumer warp
 constexpr int M_MAX = 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-// Must match make_xarea() in qg_jobs.cuh.
-inline uint32_t xarea_bytes(int rows, int cols) {
-    return (uint32_t)(align_up((size_t)rows * cols, 16) + 8ull * rows * (cols / 32));
-}
 inline int pick_mt(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+inline int log2i(int v) {
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
 
-// Ring of nslots slots of slot_bytes able to hold stages of up to `stage_bytes`.
-struct Ring {
-    uint32_t slot_bytes = 0;
-    int nslots = 0;
-    uint32_t smem_total = 0;
+// Task geometry of a row of K elements (must match the format traits in qg_formats.cuh).
+struct TaskGeo {
     bool ok = false;
+    int T = 1, TPB = 1, BPT = 1, XGT = 8, nbr = 0, gpr = 0, tpr = 0, stride = 0, bs = 0;
+    uint32_t rb = 0;
+    uint32_t bytes_of(int ntask) const { return (uint32_t)(((ntask + TPB - 1) / TPB) * BPT * bs); }
 };
-inline Ring plan_ring(uint32_t stage_bytes, uint32_t job_smem) {
+inline TaskGeo task_geo(int fmt, int K) {
+    TaskGeo g;
+    FmtInfo f;
+    if (!fmt_info(fmt, f) || K < f.qk || K % f.qk) return g;
+    g.bs = f.bs;
+    g.nbr = K / f.qk;
+    g.rb = (uint32_t)(g.nbr * f.bs);
+    if (f.qk == 32) {
+        g.T = g.nbr % 4 == 0 ? 4 : 1;
+        g.BPT = g.T;
+        g.XGT = g.T;
+        g.TPB = 1;
+        g.gpr = g.nbr / g.T;
+    } else {
+        g.T = 1;
+        g.BPT = 1;
+        g.TPB = (fmt == 13 || fmt == 14) ? 2 : 1;
+        g.XGT = 8 / g.TPB;
+        g.gpr = g.nbr;
+    }
+    g.tpr = g.gpr * g.TPB;
+    g.stride = tile_stride(g.XGT);
+    g.ok = true;
+    return g;
+}
+
+// Stage size and ring of one engine launch.
+struct Ring {
+    bool ok = false;
+    int tps = 0, depth = 0;
+    uint32_t slot_bytes = 0, x_bytes = 0, j_bytes = 0, smem_total = 0;
+};
+// run: the fewest tasks in one run of adjacent rows that any CTA of the launch sees (0: the
+// whole CTA range is one run); a stage of t tasks then spans at most t / run + 2 runs.
+// ncw: consumer warps of the launch (ncw_for(MT)).
+inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_bytes, int ncw) {
     Ring r;
-    r.slot_bytes = (uint32_t)align_up(stage_bytes + 32, 16);
-    const long avail = (long)SMEM_MAX - (long)engine_fixed_smem(MAX_SLOTS) - (long)job_smem;
-    if (avail <= 0) return r;
-    r.nslots = (int)std::min<long>(MAX_SLOTS, avail / (long)(r.slot_bytes + STAGE_SLACK));
-    if (r.nslots < 2) return r;
-    r.smem_total = (uint32_t)r.nslots * (r.slot_bytes + STAGE_SLACK) + engine_fixed_smem(r.nslots) + job_smem;
+    r.x_bytes = (uint32_t)align_up(x_bytes, 16);
+    r.j_bytes = (uint32_t)align_up(j_bytes, 16);
+    const double tb = (double)g.BPT * g.bs / g.TPB;  // bytes per task
+    const long avail = (long)SMEM_MAX - (long)engine_fixed_smem(ncw * DMAX, ncw) - (long)r.x_bytes - (long)r.j_bytes;
+    int tps = tb * 32 < 3000 ? 64 : 32;
+    for (; tps >= 2 * g.TPB; tps /= 2) {
+        int t = tps;
+        int pieces = 1;
+        if (run > 0) {
+            t = (int)std::min<long>(t, (long)(NPIECE_MAX - 2) * run);
+            t = std::max(2 * g.TPB, t / (2 * g.TPB) * (2 * g.TPB));
+            pieces = (int)std::min<long>(NPIECE_MAX, ((long)t + run - 1) / run + 1);
+            if ((long)t > (long)(NPIECE_MAX - 1) * run) return r;  // runs too short for the piece table
+        }
+        const uint32_t slot = (uint32_t)align_up(g.bytes_of(t) + 32u * pieces, 16);
+        const long d = avail / ((long)ncw * (slot + STAGE_SLACK));
+        if (d >= 2 || tps <= 2 * g.TPB) {
+            r.tps = t;
+            r.slot_bytes = slot;
+            r.depth = (int)std::min<long>(DMAX, d);
+            break;
+        }
+    }
+    if (r.depth < 1) return r;
+    const int S = ncw * r.depth;
+    r.smem_total = (uint32_t)S * (r.slot_bytes + STAGE_SLACK) + r.x_bytes + r.j_bytes + engine_fixed_smem(S, ncw);
     r.ok = r.smem_total <= (uint32_t)SMEM_MAX;
     return r;
-}
-// Per-slot byte budget that still leaves room for >= 4 slots.
-inline uint32_t stage_budget(uint32_t job_smem) {
-    const long avail = (long)SMEM_MAX - (long)engine_fixed_smem(MAX_SLOTS) - (long)job_smem;
-    long tb = std::min<long>(STAGE_TARGET, avail / 4 - STAGE_SLACK - 32);
-    return tb > 0 ? (uint32_t)(tb / 16 * 16) : 0;
 }
 
 // ----------------------------------------------------------------------------- GEMV
 struct GemvPlan {
     bool ok = false;
-    int nbr = 0, KS = 1, groups = 1, grid = 1, MT = 1, R = 0, segb = 0, kslice_max = 0;
-    uint32_t rb = 0, x_off = 64, job_smem = 0;
-    bool fused = false;      // activation quantization inside the GEMV kernel
-    bool quant_ws = false;   // activation quantization by a separate kernel into ws
+    TaskGeo geo;
+    int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0;
     Ring ring;
-    size_t ws_xq = 0, ws_xd = 0, ws_xs = 0, ws_part = 0, ws_total = 0;
+    size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
 
-// have_xq: the caller passes quantized activations (qg_gemv_q).
-inline GemvPlan plan_gemv(int fmt, int N, int K, int M, bool have_xq, int sms) {
+inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     GemvPlan p;
-    FmtInfo f;
-    if (!fmt_info(fmt, f) || N < 1 || K < f.qk || K % f.qk || M < 1 || M > M_MAX || sms < 1) return p;
-    p.nbr = K / f.qk;
-    p.rb = (uint32_t)(p.nbr * f.bs);
-    if (N < G_PLAN / 2) p.KS = std::min(p.nbr, (G_PLAN + N - 1) / N);
-    p.groups = p.KS == 1 ? std::min(N, sms) : N;
+    p.geo = task_geo(fmt, K);
+    const TaskGeo &g = p.geo;
+    if (!g.ok || N < 1 || M < 1 || M > M_MAX || sms < 1) return p;
+    p.KS = N < G_PLAN / 2 ? std::min(g.gpr, (G_PLAN + N - 1) / N) : 1;
+    auto xbytes = [&](int ks) { return (long)M * ((g.gpr + ks - 1) / ks) * g.TPB * g.stride; };
+    while (xbytes(p.KS) > (long)XCAP && p.KS < g.gpr) ++p.KS;
+    if (xbytes(p.KS) > (long)XCAP) return p;
+    p.groups = std::min(N, std::max(1, sms / p.KS));
     p.grid = p.groups * p.KS;
     p.MT = pick_mt(M);
-    p.kslice_max = (p.nbr + p.KS - 1) / p.KS * f.qk;
-    p.fused = !have_xq && xarea_bytes(M, p.kslice_max) + 64 <= XSMEM_CAP;
-    p.quant_ws = !have_xq && !p.fused;
-    p.job_smem = (uint32_t)align_up(64 + (p.fused ? xarea_bytes(M, p.kslice_max) : 0), 16);
-    const uint32_t tb = stage_budget(p.job_smem);
-    const int rows_per_cta = (N + p.groups - 1) / p.groups;
-    uint32_t stage_bytes;
-    if (p.KS == 1 && p.rb + 32 <= tb) {
-        p.R = std::min<long>(std::min<long>(PART_SLOTS / p.MT, (tb - 32) / p.rb), rows_per_cta);
-        p.segb = 0;
-        stage_bytes = (uint32_t)p.R * p.rb;
-    } else {
-        p.R = 1;
-        p.segb = std::max<int>(1, (int)((tb - 32) / (uint32_t)f.bs));
-        const int slice_blocks = (p.nbr + p.KS - 1) / p.KS;
-        stage_bytes = (uint32_t)(std::min(p.segb, slice_blocks) * f.bs);
-    }
-    p.ring = plan_ring(stage_bytes, p.job_smem);
+    p.tpr_x = (g.gpr + p.KS - 1) / p.KS * g.TPB;
+    // split-K: every row is its own run; the shortest slice has floor(gpr / KS) groups
+    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, ncw_for(p.MT));
     if (!p.ring.ok) return p;
     size_t o = 0;
-    if (p.quant_ws) {
-        p.ws_xq = o;
-        o = align_up(o + (size_t)M * K, 256);
-        p.ws_xd = o;
-        o = align_up(o + 4ull * M * (K / 32), 256);
-        p.ws_xs = o;
-        o = align_up(o + 4ull * M * (K / 32), 256);
-    }
+    p.ximg_pitch = (size_t)g.tpr * g.stride;
+    p.ws_ximg = o;
+    o = align_up(o + p.ximg_pitch * M, 256);
     if (p.KS > 1) {
         p.ws_part = o;
         o = align_up(o + 4ull * p.KS * M * N, 256);
@@ -132,43 +158,34 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, bool have_xq, int sms) {
 // ----------------------------------------------------------------------------- FFN sublayer
 struct FfnPlan {
     bool ok = false;
-    int nbr = 0, grid = 1, MT = 1, R = 0;
-    uint32_t rb = 0, x_off = 0, job_smem = 0;
-    bool fused = false;
+    TaskGeo geo;
+    int grid = 1, MT = 1, MC = 1, nchunk = 1;
     Ring ring;
-    GemvPlan down;  // y = Wd h, h (fp32) in ws
-    size_t ws_g = 0, ws_u = 0, ws_h = 0, ws_xq = 0, ws_xd = 0, ws_xs = 0, ws_down = 0, ws_total = 0;
+    GemvPlan down;  // y = Wd h; h = silu(g) * u is formed by its activation preparation
+    size_t ws_ximg = 0, ximg_pitch = 0, ws_g = 0, ws_u = 0, ws_h = 0, ws_down = 0, ws_total = 0;
 };
 
 inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     FfnPlan p;
-    FmtInfo f;
-    if (!fmt_info(fmt, f) || M < 1 || M > M_MAX || H < f.qk || H % f.qk || I < f.qk || I % f.qk || sms < 1)
-        return p;
-    p.nbr = H / f.qk;
-    p.rb = (uint32_t)(p.nbr * f.bs);
-    p.MT = pick_mt(M);
-    p.grid = std::min(I, sms);
-    p.fused = xarea_bytes(M, H) <= XSMEM_CAP;
-    p.job_smem = (uint32_t)align_up(p.fused ? xarea_bytes(M, H) : 16, 16);
-    uint32_t tb = stage_budget(p.job_smem);
-    if (2 * p.rb + 64 > tb) tb = (uint32_t)align_up(2 * p.rb + 64, 16);  // one pair per slot
-    const int rows_per_cta = (I + p.grid - 1) / p.grid;
-    p.R = (int)std::min<long>(std::min<long>(PART_SLOTS / (2 * p.MT), (tb - 64) / (2 * p.rb)), rows_per_cta);
-    if (p.R < 1) return p;
-    p.ring = plan_ring(2u * p.R * p.rb + 32, p.job_smem);
+    p.geo = task_geo(fmt, H);
+    const TaskGeo &g = p.geo;
+    if (!g.ok || !task_geo(fmt, I).ok || M < 1 || M > M_MAX || sms < 1) return p;
+    const long tiles = (long)g.tpr * g.stride;
+    p.MC = (int)std::min<long>(M, (long)XCAP / tiles);
+    if (p.MC < 1) return p;
+    p.nchunk = (M + p.MC - 1) / p.MC;
+    p.MT = pick_mt(p.MC);
+    p.grid = std::min(2 * I, sms);
+    p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, ncw_for(p.MT));
     if (!p.ring.ok) return p;
-    p.down = plan_gemv(fmt, H, I, M, false, sms);
+    p.down = plan_gemv(fmt, H, I, M, sms);
     if (!p.down.ok) return p;
     size_t o = 0;
+    p.ximg_pitch = (size_t)tiles;
+    p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);
     p.ws_g = o; o = align_up(o + 4ull * M * I, 256);
     p.ws_u = o; o = align_up(o + 4ull * M * I, 256);
     p.ws_h = o; o = align_up(o + 4ull * M * I, 256);
-    if (!p.fused) {
-        p.ws_xq = o; o = align_up(o + (size_t)M * H, 256);
-        p.ws_xd = o; o = align_up(o + 4ull * M * (H / 32), 256);
-        p.ws_xs = o; o = align_up(o + 4ull * M * (H / 32), 256);
-    }
     p.ws_down = o;
     o = align_up(o + p.down.ws_total, 256);
     p.ws_total = o;
@@ -179,77 +196,57 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
 // ----------------------------------------------------------------------------- MoE FFN
 struct MoePlan {
     bool ok = false;
-    int S = 0, nbr_h = 0, nbr_i = 0;
-    uint32_t rb_gu = 0, rb_d = 0;
-    // router
-    int router_grid = 0;
-    // gate/up
-    int gu_grid = 0, gu_R = 0;
-    bool gu_fused = false;
-    uint32_t gu_x_off = 0, gu_job = 0;
-    Ring gu_ring;
-    // down
-    int dn_grid = 0, dn_R = 0, dn_nloc = 0;
-    bool dn_fused = false;
-    uint32_t dn_x_off = 0, dn_job = 0;
-    Ring dn_ring;
+    int S = 0;
+    TaskGeo gh, gi;  // rows of H elements (gate/up) and of I elements (down)
+    int gu_grid = 0, dn_grid = 0, dn_MC = 1, dn_nchunk = 1;
+    Ring gu_ring, dn_ring;
     size_t ws_g = 0, ws_u = 0, ws_h = 0, ws_hq = 0, ws_hd = 0, ws_hs = 0, ws_logits = 0, ws_ids = 0, ws_w = 0,
-           ws_xq = 0, ws_xd = 0, ws_xs = 0, ws_total = 0;
+           ws_ximg = 0, ws_himg = 0, ximg_pitch = 0, himg_pitch = 0, ws_total = 0;
 };
 
 inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) {
     MoePlan p;
-    FmtInfo f;
-    if (!fmt_info(fmt, f) || M < 1 || M > M_MAX || H < f.qk || H % f.qk || I < f.qk || I % f.qk || E < 1 ||
-        E > 1024 || topk < 1 || topk > 16 || topk > E || sms < 1)
+    p.gh = task_geo(fmt, H);
+    p.gi = task_geo(fmt, I);
+    if (!p.gh.ok || !p.gi.ok || M < 1 || M > M_MAX || E < 1 || E > 1024 || topk < 1 || topk > 16 || topk > E ||
+        sms < 1 || M * topk > SCRATCH_INTS)
         return p;
     p.S = topk + 1;
-    p.nbr_h = H / f.qk;
-    p.nbr_i = I / f.qk;
-    p.rb_gu = (uint32_t)(p.nbr_h * f.bs);
-    p.rb_d = (uint32_t)(p.nbr_i * f.bs);
-    p.router_grid = (E + 7) / 8;
-    // gate/up
-    const long pairs = (long)M * p.S * I;
-    p.gu_grid = (int)std::min<long>(sms, pairs);
-    p.gu_x_off = (uint32_t)align_up(4ull * M * topk, 16);
-    p.gu_fused = p.gu_x_off + xarea_bytes(M, H) <= XSMEM_CAP;
-    p.gu_job = (uint32_t)align_up(p.gu_x_off + (p.gu_fused ? xarea_bytes(M, H) : 0), 16);
-    uint32_t tb = stage_budget(p.gu_job);
-    if (2 * p.rb_gu + 64 > tb) tb = (uint32_t)align_up(2 * p.rb_gu + 64, 16);
-    p.gu_R = (int)std::min<long>(PART_SLOTS / 2, (tb - 64) / (2 * p.rb_gu));
-    if (p.gu_R < 1) return p;
-    p.gu_ring = plan_ring(2u * p.gu_R * p.rb_gu + 32, p.gu_job);
+    // gate/up: output rows (token, slot, gate|up, row)
+    const long gu_rows = (long)M * p.S * 2 * I;
+    const long gu_x = (long)M * p.gh.tpr * p.gh.stride;
+    if (gu_x > (long)XCAP) return p;
+    p.gu_grid = (int)std::min<long>(sms, gu_rows);
+    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, ncw_for(1));
     if (!p.gu_ring.ok) return p;
-    // down
+    // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
+    const long tiles_tok = (long)p.S * p.gi.tpr * p.gi.stride;
     p.dn_grid = std::min(sms, H);
-    p.dn_nloc = (H + p.dn_grid - 1) / p.dn_grid;
-    p.dn_x_off = (uint32_t)align_up(4ull * M * p.dn_nloc, 16);
-    p.dn_fused = p.dn_x_off + xarea_bytes(M * p.S, I) <= XSMEM_CAP;
-    p.dn_job = (uint32_t)align_up(p.dn_x_off + (p.dn_fused ? xarea_bytes(M * p.S, I) : 0), 16);
-    uint32_t tbd = stage_budget(p.dn_job);
-    if (p.rb_d + 32 > tbd) tbd = (uint32_t)align_up(p.rb_d + 32, 16);
-    p.dn_R = (int)std::min<long>(std::min<long>(PART_SLOTS, (tbd - 32) / p.rb_d), p.dn_nloc);
-    if (p.dn_R < 1) return p;
-    p.dn_ring = plan_ring((uint32_t)p.dn_R * p.rb_d, p.dn_job);
+    const int nloc = (H + p.dn_grid - 1) / p.dn_grid;
+    const long part_tok = 4L * p.S * nloc;
+    p.dn_MC = (int)std::min<long>(M, (long)XCAP / (tiles_tok + part_tok));
+    if (p.dn_MC < 1) return p;
+    p.dn_nchunk = (M + p.dn_MC - 1) / p.dn_MC;
+    // CTAs own floor or ceil of H / dn_grid rows: runs are at least the floor long
+    p.dn_ring = plan_ring(p.gi, (long)(H / p.dn_grid) * p.gi.tpr, (uint32_t)(p.dn_MC * tiles_tok),
+                          (uint32_t)(p.dn_MC * part_tok), ncw_for(1));
     if (!p.dn_ring.ok) return p;
     // workspace
-    const size_t R = (size_t)M * p.S;
+    const size_t Rw = (size_t)M * p.S;
     size_t o = 0;
-    p.ws_g = o; o = align_up(o + 4 * R * I, 256);
-    p.ws_u = o; o = align_up(o + 4 * R * I, 256);
-    p.ws_h = o; o = align_up(o + 4 * R * I, 256);
-    p.ws_hq = o; o = align_up(o + R * I, 256);
-    p.ws_hd = o; o = align_up(o + 4 * R * (I / 32), 256);
-    p.ws_hs = o; o = align_up(o + 4 * R * (I / 32), 256);
+    p.ws_g = o; o = align_up(o + 4 * Rw * I, 256);
+    p.ws_u = o; o = align_up(o + 4 * Rw * I, 256);
+    p.ws_h = o; o = align_up(o + 4 * Rw * I, 256);
+    p.ws_hq = o; o = align_up(o + Rw * I, 256);
+    p.ws_hd = o; o = align_up(o + 4 * Rw * (I / 32), 256);
+    p.ws_hs = o; o = align_up(o + 4 * Rw * (I / 32), 256);
     p.ws_logits = o; o = align_up(o + 4ull * M * E, 256);
     p.ws_ids = o; o = align_up(o + 4ull * M * topk, 256);
     p.ws_w = o; o = align_up(o + 4ull * M * topk, 256);
-    if (!p.gu_fused) {
-        p.ws_xq = o; o = align_up(o + (size_t)M * H, 256);
-        p.ws_xd = o; o = align_up(o + 4ull * M * (H / 32), 256);
-        p.ws_xs = o; o = align_up(o + 4ull * M * (H / 32), 256);
-    }
+    p.ximg_pitch = (size_t)p.gh.tpr * p.gh.stride;
+    p.himg_pitch = (size_t)p.gi.tpr * p.gi.stride;
+    p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);
+    p.ws_himg = o; o = align_up(o + p.himg_pitch * Rw, 256);
     p.ws_total = o;
     p.ok = true;
     return p;

@@ -78,8 +78,8 @@ enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBL
 int qg_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs, void *stream);
 
 /* y = W x for M tokens [D27 Q&A; KES section 一]: x is quantized on the GPU as by
- * qg_quantize_act (inside the GEMV kernel when it fits in shared memory, else into ws),
- * then each 32-element unit contributes
+ * qg_quantize_act (once per call, into per-task activation tiles in ws), then each
+ * 32-element unit contributes
  *   Q8_0, Q4_0, Q6_K, IQ4_XS:  y += d_unit * xd * dot
  *   Q4_K, Q5_K:                y += xd * (d*S_j * dot - dmin*M_j * xs)
  * where dot is the exact int32 sum of weight codes times activation codes.
@@ -88,7 +88,7 @@ int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int 
             void *ws, size_t ws_bytes, void *stream);
 
 /* Same as qg_gemv with the activations already quantized (xq, xd, xs laid out as
- * produced by qg_quantize_act). */
+ * produced by qg_quantize_act).  Both GEMV calls need a workspace (ws != NULL). */
 int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, const int32_t *xs,
               float *y, int N, int K, int M, void *ws, size_t ws_bytes, void *stream);
 
@@ -146,7 +146,9 @@ int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]);
 int qg_block_dots(int fmt, const void *W_blocks, const int8_t *xq, const int32_t *xs,
                   int N, int K, int M, int32_t *dots, int32_t *aux, void *stream);
 
-/* Device-side error word (bit 1: a bounded wait in a kernel gave up), read and cleared.
+/* Device-side error word, read and cleared: value 1 = a bounded wait in a kernel gave up
+ * (results of that call are invalid); value 2 = a launch plan did not fit the engine's
+ * per-stage piece table and some rows were skipped (a library bug; results invalid).
  * Synchronizes the current device; for tests and diagnostics, not for the hot path. */
 int qg_device_error(unsigned int *err);
 

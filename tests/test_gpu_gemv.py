@@ -99,7 +99,7 @@ def test_gemv_q_prequantized_matches_oracle(qg, fmt):
 @pytest.mark.parametrize("fmt,N,K,M", [
     (synth.Q8_0, 20, 32768, 2),      # rows larger than a ring slot: K split into segments
     (synth.Q6_K, 50, 17408, 1),      # 14280-byte rows that start 8-byte aligned
-    (synth.Q4_K, 300, 8192, 16),     # activations too large for shared memory: quantized into ws
+    (synth.Q4_K, 300, 8192, 16),     # 16 tokens of activation tiles exceed one CTA: split along K
     (synth.IQ4_XS, 3, 65536, 4),     # split-K over many slices + segments
     (synth.Q4_0, 4099, 96, 1),       # tiny rows packed 8 per warp step, odd N
 ])
