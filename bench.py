@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Throughput of the quantized decode GEMV on raw GGUF blocks.
+
+Workload (one step): the dense-27B-like FFN shapes at M = 1 for Q4_0 and Q4_K -- gate/up
+K=5120 N=17408 and down K=17408 N=5120 -- i.e. four GEMV calls per step, each quantizing its
+activation row on the GPU and multiplying it against 50,135,040 bytes of raw blocks.  The
+headline value is the effective weight bandwidth (weight bytes / time, decimal GB/s) over
+the whole job; the roofline fraction is that bandwidth divided by the measured HBM copy
+bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+  * our arm: the step is captured once as a CUDA graph per weight copy set and replayed
+    K times between CUDA events on the launch stream; two copies of every matrix rotate,
+    so the 200 MB a step reads never comes from L2 (129 MB);
+  * e2e: the same K steps through the public Python API with host buffers: every step
+    copies its activation rows from pinned host memory and reads its results back;
+  * reference arm: the plain CPU oracle (the checker of the CUDA path) on the host cores,
+    each step a bounded sample of the same workload;
+  * N > 1 (torchrun): replicas only -- every rank runs the whole workload on its own GPU;
+    the value is the weight bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "effective weight GB/s per quant GEMV (fraction of HBM peak); MoE FFN tokens/s"
+WORKLOAD_NAME = "Q4_0 + Q4_K GEMV, M=1, dense-27B FFN shapes (17408x5120 gate/up, 5120x17408 down)"
+CONFIG_ID = 2  # seed id of this workload (synth.seed_for)
+MATRICES = [(synth.Q4_0, 17408, 5120), (synth.Q4_0, 5120, 17408), (synth.Q4_K, 17408, 5120), (synth.Q4_K, 5120, 17408)]
+M_TOKENS = 1
+ROTATE = 2                    # weight copies per matrix
+FALLBACK_HBM_GBS = 6800.0     # used only when no measured peak is available
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+# ----------------------------------------------------------------------------- helpers
+def weight_bytes_per_step() -> int:
+    return sum(synth.matrix_bytes(f, n, k) for f, n, k in MATRICES)
+
+
+def algorithmic_bytes_per_launch(fmt: int, N: int, K: int, M: int) -> int:
+    """Weight bytes + fp32 activations read + fp32 results written by one GEMV call."""
+    return synth.matrix_bytes(fmt, N, K) + 4 * M * K + 4 * M * N
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(ms: float, units: float, world: int):
+    """Slowest rank's time and the units of all ranks (replicas: no data exchange)."""
+    if world <= 1:
+        return ms, units
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError, TypeError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    csrc = os.path.join(ROOT, "gguf_block_quantized_quant_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic_per_launch():
+    """DRAM bytes (read + write) of one engine launch from the committed ncu summary, or
+    None when the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "engine_q4k_17408x5120_m1.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
+        kv = {k.strip(): v.strip() for k, v in kv.items()}
+        if kv.get("source_sha") != kernel_source_sha():
+            return None
+        return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while it runs."""
+
+    def __init__(self, uuid: str | None, period_ms: int = 100):
+        self.uuid, self.period_ms, self.proc, self.out = uuid, period_ms, None, ""
+
+    def __enter__(self):
+        q = "uuid,clocks.sm,clocks.max.sm,power.draw," + ",".join(f"clocks_event_reasons.{r}" for r in CLOCK_REASONS)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", str(self.period_ms)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    @staticmethod
+    def _norm(u: str) -> str:
+        u = u.strip().lower()
+        return (u[4:] if u.startswith("gpu-") else u).replace("-", "")
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        rows = [[x.strip() for x in line.split(",")] for line in self.out.splitlines()]
+        rows = [f for f in rows if len(f) >= 4 + len(CLOCK_REASONS)]
+        mine = [f for f in rows if self.uuid and self._norm(f[0]) == self._norm(self.uuid)]
+        if not mine and len({f[0] for f in rows}) == 1:
+            mine = rows  # one GPU visible: its samples are ours
+        for f in mine:
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for r, v in zip(CLOCK_REASONS, f[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(r)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(rows_per_matrix: int, seed_salt: int = 0):
+    """A bounded sample of the workload for the oracle: the first rows of every matrix."""
+    out = []
+    for i, (fmt, N, K) in enumerate(MATRICES):
+        g = synth.rng(CONFIG_ID, 10 + i + seed_salt)
+        r = min(rows_per_matrix, N)
+        out.append((fmt, r, K, synth.weights(fmt, r, K, g), synth.activations(M_TOKENS, K, g)))
+    return out
+
+
+def time_oracle(sample, min_seconds: float):
+    """Runs the oracle over the sample until min_seconds have passed; weight GB/s."""
+    import oracle
+    oracle.build()
+    nbytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for fmt, r, K, W, x in sample:
+            oracle.gemv(fmt, W, x, r, K)
+            nbytes += synth.matrix_bytes(fmt, r, K)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            return nbytes / el / 1e9, oracle.get_threads(), reps, el
+
+
+def cpu_baseline_block(seconds: float = 10.0):
+    rows = 256
+    sample = oracle_sample(rows)
+    gbs, cores, reps, el = time_oracle(sample, seconds)
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} rows of each of the 4 matrices ({sum(synth.matrix_bytes(f, r, k) for f, r, k, _, _ in sample)} "
+                      f"weight bytes), repeated {reps}x in {el:.1f} s, fp64 oracle with OpenMP over rows"}
+
+
+def run_reference(args, budget_s: float = 150.0):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    # rows per matrix per step: at most 64, fewer when K steps of 64 would exceed the budget
+    rows = 64
+    sample = oracle_sample(rows)
+    t0 = time.perf_counter()
+    for fmt, r, K, W, x in sample:
+        oracle.gemv(fmt, W, x, r, K)
+    t1 = time.perf_counter() - t0
+    if t1 * (args.steps + args.warmup) > budget_s:
+        rows = max(1, int(rows * budget_s / (t1 * (args.steps + args.warmup))))
+        sample = oracle_sample(rows)
+    for _ in range(args.warmup):
+        for fmt, r, K, W, x in sample:
+            oracle.gemv(fmt, W, x, r, K)
+    step_bytes = sum(synth.matrix_bytes(f, r, k) for f, r, k, _, _ in sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for fmt, r, K, W, x in sample:
+            oracle.gemv(fmt, W, x, r, K)
+    el = time.perf_counter() - t0
+    gbs = step_bytes * args.steps / el / 1e9
+    desc = (f"first {rows} rows of each of the 4 matrices per step ({step_bytes} weight bytes), "
+            f"fp64 oracle with OpenMP over rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; block codes/scales uniform, x ~ N(0,1))",
+        "config": {"workload": WORKLOAD_NAME, "M": M_TOKENS, "sample_rows_per_matrix": rows},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import gguf_block_quantized_quant_gb300 as qg
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "") or None
+
+    # inputs: seeded on the host, uploaded once; ROTATE copies of every matrix
+    mats = []
+    for i, (fmt, N, K) in enumerate(MATRICES):
+        g = synth.rng(CONFIG_ID, i)
+        W = torch.from_numpy(synth.weights(fmt, N, K, g)).to(dev)
+        x_host = torch.from_numpy(synth.activations(M_TOKENS, K, g)).pin_memory()
+        copies = [W] + [W.clone() for _ in range(ROTATE - 1)]
+        nws = qg.qg_workspace_size(qg.QG_OP_GEMV, fmt, M_TOKENS, N, K)
+        mats.append(dict(fmt=fmt, N=N, K=K, W=copies, x_host=x_host, x=x_host.to(dev),
+                         y=torch.empty((M_TOKENS, N), dtype=torch.float32, device=dev),
+                         y_host=torch.empty((M_TOKENS, N), dtype=torch.float32).pin_memory(),
+                         ws=torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)))
+    step_weight_bytes = weight_bytes_per_step()
+    launches_per_step = 2 * len(MATRICES)  # activation tile preparation + engine, per GEMV
+
+    s = torch.cuda.Stream(device=dev)
+
+    def step(c):
+        for m in mats:
+            qg.qg_gemv(m["fmt"], m["W"][c], m["x"], m["N"], y=m["y"], ws=m["ws"], stream=s)
+
+    with torch.cuda.stream(s):
+        for i in range(max(args.warmup, 1)):
+            step(i % ROTATE)
+        s.synchronize()
+        graphs = []
+        for c in range(ROTATE):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                step(c)
+            graphs.append(gr)
+        for i in range(args.warmup):
+            graphs[i % ROTATE].replay()
+        s.synchronize()
+    err = qg.qg_device_error()
+    if err:
+        raise SystemExit(f"bench.py: device error word {err:#x} after warm-up")
+
+    # ---- timed region: K graph replays
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(args.steps):
+                graphs[i % ROTATE].replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    ms, total_bytes = aggregate(ms_local, step_weight_bytes * args.steps, world)
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+
+    # ---- e2e: public API, host buffers, copies inside the timed region
+    h2d = sum(m["x_host"].numel() * 4 for m in mats)
+    d2h = sum(m["y_host"].numel() * 4 for m in mats)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        f0.record(s)
+        for i in range(args.steps):
+            c = i % ROTATE
+            for m in mats:
+                m["x"].copy_(m["x_host"], non_blocking=True)
+                qg.qg_gemv(m["fmt"], m["W"][c], m["x"], m["N"], y=m["y"], ws=m["ws"], stream=s)
+                m["y_host"].copy_(m["y"], non_blocking=True)
+        f1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_e2e, tb_e2e = aggregate(f0.elapsed_time(f1), step_weight_bytes * args.steps, world)
+    e2e_gbs = tb_e2e / (ms_e2e * 1e-3) / 1e9
+    err = qg.qg_device_error()
+    if err:
+        raise SystemExit(f"bench.py: device error word {err:#x} after the timed region")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (the GEMV engine; each call also runs its small
+    # activation preparation kernel, which the per-launch duration includes)
+    peak, peak_kind = measured_peak()
+    launch_ms = ms_local / (args.steps * len(MATRICES))
+    algo = sum(algorithmic_bytes_per_launch(f, n, k, M_TOKENS) for f, n, k in MATRICES) / len(MATRICES)
+    achieved = algo / (launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": dram_traffic_per_launch(), "peak_source": peak_kind,
+                "kernel": "engine_kernel (GEMV) + activation tile preparation, per call",
+                "algorithmic_bytes_per_launch": algo}
+
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded; block codes/scales uniform, fp16 scales from U[1e-3,2e-3], x ~ N(0,1))",
+        "config": {"workload": WORKLOAD_NAME, "M": M_TOKENS,
+                   "matrices": [f"{synth.FORMAT_NAMES[f]} {n}x{k}" for f, n, k in MATRICES],
+                   "weight_bytes_per_step": step_weight_bytes, "frac_of_hbm_peak": gbs / world / peak,
+                   "l2": f"inputs larger than L2: {ROTATE} rotating copies of every matrix, "
+                         f"{ROTATE * step_weight_bytes} weight bytes in rotation",
+                   "timing": "one CUDA graph per weight copy set, K replays between CUDA events on the launch stream",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": None,
+        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if world == 1:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_block(args.cpu_seconds)
+        if not args.no_secondary:
+            line["secondary"] = secondary(qg, torch, dev, s)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _graph_time_us(torch, s, fn, reps: int, warm: int = 3):
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            fn()
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            fn()
+        gr.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def secondary(qg, torch, dev, s):
+    """The other workloads, for context: format sweep, Q8_0 1024^2, MoE FFN tokens/s, FFN
+    sublayer.  Small matrices rotate through copies totalling > 4x L2 ("cold")."""
+    out = {}
+    l2 = 4 * torch.cuda.get_device_properties(dev).L2_cache_size
+    for fmt, N, K in [(synth.Q8_0, 1024, 1024), (synth.Q5_K, 4096, 4096), (synth.Q6_K, 4096, 4096),
+                      (synth.IQ4_XS, 4096, 4096)]:
+        g = synth.rng(3 if fmt != synth.Q8_0 else 1, 0)
+        nb = synth.matrix_bytes(fmt, N, K)
+        R = max(2, -(-l2 // nb))
+        base = torch.from_numpy(synth.weights(fmt, N, K, g)).to(dev)
+        Ws = [base] + [base.clone() for _ in range(R - 1)]
+        x = torch.from_numpy(synth.activations(1, K, g)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(qg.qg_workspace_size(qg.QG_OP_GEMV, fmt, 1, N, K), 16), dtype=torch.uint8, device=dev)
+
+        def fn():
+            for W in Ws:
+                qg.qg_gemv(fmt, W, x, N, y=y, ws=ws, stream=s)
+        us = _graph_time_us(torch, s, fn, 20) / R
+        out[f"{synth.FORMAT_NAMES[fmt]} {N}x{K} M=1 cold"] = {"us": us, "GB/s": nb / us / 1e3}
+        del Ws, base
+    # MoE FFN: Q4_K experts, H=2048, E=256 routed (I=512) + 1 shared, top-8
+    H, E, I, topk = 2048, 256, 512, 8
+    g = synth.rng(4, 0)
+    Wr = torch.from_numpy(synth.router_weights(E, H, g)).to(dev)
+    fq = synth.Q4_K
+    Wg = torch.from_numpy(synth.stacked_experts(fq, E, I, H, g)).to(dev)
+    Wu = torch.from_numpy(synth.stacked_experts(fq, E, I, H, g)).to(dev)
+    Wd = torch.from_numpy(synth.stacked_experts(fq, E, H, I, g)).to(dev)
+    Wgs = torch.from_numpy(synth.weights(fq, I, H, g)).to(dev)
+    Wus = torch.from_numpy(synth.weights(fq, I, H, g)).to(dev)
+    Wds = torch.from_numpy(synth.weights(fq, H, I, g)).to(dev)
+    for M in (1, 2, 4):
+        x = torch.from_numpy(synth.activations(M, H, g)).to(dev)
+        y = torch.empty((M, H), dtype=torch.float32, device=dev)
+        ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_MOE_FFN, fq, M, H, H, E, topk, I), dtype=torch.uint8,
+                         device=dev)
+        us = _graph_time_us(torch, s, lambda: qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y,
+                                                            ws=ws, stream=s), 200)
+        out[f"MoE FFN Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us, "tokens/s": M / (us * 1e-6)}
+    del Wg, Wu, Wd
+    # FFN sublayer: H=5120, I=17408 (150 / 219 MB of weights: larger than L2)
+    H, I = 5120, 17408
+    for fmt in (synth.Q4_K, synth.Q6_K):
+        g = synth.rng(5, fmt)
+        Wg = torch.from_numpy(synth.weights(fmt, I, H, g)).to(dev)
+        Wu = torch.from_numpy(synth.weights(fmt, I, H, g)).to(dev)
+        Wd = torch.from_numpy(synth.weights(fmt, H, I, g)).to(dev)
+        nb = 2 * synth.matrix_bytes(fmt, I, H) + synth.matrix_bytes(fmt, H, I)
+        for M in (1, 2, 4, 8, 16):
+            x = torch.from_numpy(synth.activations(M, H, g)).to(dev)
+            y = torch.empty((M, H), dtype=torch.float32, device=dev)
+            ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), dtype=torch.uint8,
+                             device=dev)
+            us = _graph_time_us(torch, s, lambda: qg.qg_ffn_sublayer(fmt, Wg, Wu, Wd, x, I, y=y, ws=ws, stream=s), 20)
+            out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {"us": us, "GB/s": nb / us / 1e3}
+        del Wg, Wu, Wd
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("bench.py: at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
