@@ -33,7 +33,8 @@ LIB_PATH = _build.LIB
 # every symbol declared in include/qg.h
 EXPORTS = ("qg_quantize_act", "qg_gemv", "qg_gemv_q", "qg_moe_ffn", "qg_ffn_sublayer", "qg_workspace_size",
            "qg_moe_ws_layout", "qg_ffn_ws_layout", "qg_block_dots", "qg_device_error", "qg_strerror",
-           "qg_version")
+           "qg_version", "qg_gemv_static_ws")
+QG_STATIC_WS_BYTES = 2097152  # include/qg.h
 
 
 class QGError(RuntimeError):
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.qg_quantize_act.argtypes = [P, I, I, P, P, P, P]
         L.qg_gemv.argtypes = [I, P, P, P, I, I, I, P, S, P]
         L.qg_gemv_q.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
+        L.qg_gemv_static_ws.argtypes = [I, P, P, P, I, I, I, P]
         L.qg_moe_ffn.argtypes = [I, P, I, I, P, I, I, P, P, P, P, P, P, I, P, P, P, P, S, P]
         L.qg_ffn_sublayer.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
         L.qg_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -134,6 +136,15 @@ def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
     ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), x.device)
     _check(lib().qg_gemv(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _ptr(ws), nws, _stream(stream)), "qg_gemv")
+    return y
+
+
+def qg_gemv_static_ws(fmt: int, W, x, N: int, y=None, stream=None):
+    """qg_gemv on the library's fixed device scratch (no workspace argument, no allocation
+    inside the call when y is given).  Calls that may overlap in time share the scratch."""
+    M, K = x.shape
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    _check(lib().qg_gemv_static_ws(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _stream(stream)), "qg_gemv_static_ws")
     return y
 
 

@@ -178,6 +178,31 @@ bool shape_ok(int fmt, int K) {
     return fmt_info(fmt, f) && K >= f.qk && K % f.qk == 0;
 }
 
+// Fixed scratch of qg_gemv_static_ws: one array per device, shared by every call.
+static __device__ __align__(256) uint8_t g_qg_static_ws[QG_STATIC_WS_BYTES];
+
+struct StaticWsCache {
+    std::mutex mu;
+    void *addr[64] = {};
+};
+StaticWsCache g_static_ws;
+
+// Device address of the scratch array on the current device (looked up once per device).
+void *static_ws_addr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_ws.mu);
+    if (!g_static_ws.addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_qg_static_ws) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_static_ws.addr[dev] = p;
+    }
+    return g_static_ws.addr[dev];
+}
+
 }  // namespace
 }  // namespace qg
 
@@ -257,6 +282,18 @@ int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int 
             void *stream) {
     if (!x) return QG_EINVAL;
     return gemv_common(fmt, W_blocks, x, nullptr, nullptr, nullptr, y, N, K, M, ws, ws_bytes, stream);
+}
+
+int qg_gemv_static_ws(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M, void *stream) {
+    if (!x || !W_blocks || !y || N < 1 || M < 1 || M > M_MAX || !shape_ok(fmt, K)) return QG_EINVAL;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    const GemvPlan p = plan_gemv(fmt, N, K, M, sms);
+    if (!p.ok) return QG_EINVAL;
+    if (p.ws_total > (size_t)QG_STATIC_WS_BYTES) return QG_EWORKSPACE;
+    void *ws = static_ws_addr();
+    if (!ws) return QG_ECUDA;
+    return gemv_common(fmt, W_blocks, x, nullptr, nullptr, nullptr, y, N, K, M, ws, QG_STATIC_WS_BYTES, stream);
 }
 
 int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, const int32_t *xs, float *y, int N,

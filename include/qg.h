@@ -92,6 +92,24 @@ int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int 
 int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, const int32_t *xs,
               float *y, int N, int K, int M, void *ws, size_t ws_bytes, void *stream);
 
+/* Bytes of the library's fixed device scratch array used by qg_gemv_static_ws. */
+#define QG_STATIC_WS_BYTES 2097152
+
+/* qg_gemv without a caller workspace: the scratch lives in one file-scope device array
+ * of QG_STATIC_WS_BYTES bytes inside the library (per device), so the call allocates
+ * nothing.  The pages have no counterpart to this entry point; it is a convenience for
+ * callers that cannot hand over a workspace.
+ *   Arguments, layouts and results as qg_gemv (y is bit-identical to qg_gemv's).
+ *   Limit: returns QG_EWORKSPACE, without launching, when qg_workspace_size(QG_OP_GEMV,
+ *   fmt, M, N, K, ...) exceeds QG_STATIC_WS_BYTES (e.g. very long rows at M = 16).
+ *   Races: every call on a device shares the one array.  Calls whose executions may
+ *   overlap (different streams without ordering, or several host threads) corrupt each
+ *   other's activations; order them on one stream.
+ *   The first call on each device looks up the array's address (cudaGetSymbolAddress);
+ *   make that first call outside any stream capture. */
+int qg_gemv_static_ws(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
+                      void *stream);
+
 /* MoE FFN for M tokens [KES section 四 ⑪; A3B section 1.1]:
  *   logits = Wr x (fp32); probabilities = softmax over the E experts; the topk largest
  *   (ties: lower expert id) are renormalized to weights w summing to 1;

@@ -78,6 +78,9 @@ def test_other_entry_points_reject_bad_arguments(L):
     P = _P
     assert L.qg_quantize_act(P(A16), 1, 33, P(A16), P(A16), P(A16), None) == -1
     assert L.qg_gemv_q(12, P(A16), None, P(A16), P(A16), P(A16), 4, 256, 1, None, 0, None) == -1
+    assert L.qg_gemv_static_ws(3, P(A16), P(A16), P(A16), 4, 256, 1, None) == -1    # unknown format
+    assert L.qg_gemv_static_ws(12, P(A16), None, P(A16), 4, 256, 1, None) == -1     # no activations
+    assert L.qg_gemv_static_ws(12, P(A16), P(A16), P(A16), 4, 256, 17, None) == -1  # batch above 16
     assert L.qg_block_dots(14, P(A16), P(A16), P(A16 + 2), 4, 256, 1, P(A16), P(A16), None) == -3
     args = [12, P(A16), 1, 2048, P(A16), 256, 8] + [P(A16)] * 6 + [512, P(A16), None, None]
     assert L.qg_moe_ffn(*args, None, 0, None) == -2                      # no workspace

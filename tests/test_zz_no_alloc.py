@@ -1,0 +1,53 @@
+"""qg_gemv_static_ws: the GEMV on the library's fixed device scratch array.  Its results
+must be bit-identical to qg_gemv with a caller workspace (same kernels, same plans); two
+calls in a row on one stream must not disturb each other; oversize problems are refused."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from qg_testlib import dev, qg_module
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qg():
+    return qg_module()
+
+CASES = [
+    (synth.Q4_K, 2048, 4096, 1),     # plain rows
+    (synth.Q6_K, 300, 5120, 4),      # several tokens
+    (synth.Q4_0, 5, 8192, 3),        # few rows: split-K partial sums live in the scratch too
+    (synth.IQ4_XS, 64, 17408, 16),   # long rows at the largest batch
+]
+
+
+@pytest.mark.parametrize("fmt,N,K,M", CASES, ids=[f"{synth.FORMAT_NAMES[c[0]]}-{c[1]}x{c[2]}-M{c[3]}" for c in CASES])
+def test_static_ws_two_calls_match_gemv(qg, fmt, N, K, M):
+    assert qg.qg_workspace_size(qg.QG_OP_GEMV, fmt, M, N, K) <= qg.QG_STATIC_WS_BYTES
+    g = np.random.default_rng(N * 7 + K + M)
+    W1, W2 = dev(synth.weights(fmt, N, K, g)), dev(synth.weights(fmt, N, K, g))
+    x1, x2 = dev(synth.activations(M, K, g)), dev(synth.activations(M, K, g))
+    s = torch.cuda.current_stream()
+    # two calls in a row on one stream, then the workspace entry point
+    y1 = qg.qg_gemv_static_ws(fmt, W1, x1, N, stream=s)
+    y2 = qg.qg_gemv_static_ws(fmt, W2, x2, N, stream=s)
+    r1 = qg.qg_gemv(fmt, W1, x1, N, stream=s)
+    r2 = qg.qg_gemv(fmt, W2, x2, N, stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, r1)
+    assert torch.equal(y2, r2)
+    assert not torch.equal(y1, y2)
+    assert qg.qg_device_error() == 0
+
+
+def test_static_ws_refuses_oversize(qg):
+    fmt, N, K, M = synth.Q8_0, 1, 131072, 16
+    need = qg.qg_workspace_size(qg.QG_OP_GEMV, fmt, M, N, K)
+    assert need > qg.QG_STATIC_WS_BYTES
+    W = torch.zeros((N, synth.row_bytes(fmt, K)), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.float32, device="cuda")
+    with pytest.raises(qg.QGError) as e:
+        qg.qg_gemv_static_ws(fmt, W, x, N)
+    assert e.value.status == qg.QG_EWORKSPACE
