@@ -23,6 +23,12 @@
  * layouts used here are the public GGUF block definitions.  Readings taken where
  * the pages are silent are stated next to the code that takes them.
  *
+ * Parity unpinned: the 16 values of the IQ4_NL codebook used by IQ4_XS.  The pages
+ * print no table (they only say the codebook is small and lives in registers); the
+ * values are the published IQ4_NL table, and a test can only restate them.  The
+ * decode of IQ4_XS around the table (indices, sub-scales, d) is pinned.  Agreement of
+ * the six byte layouts with real GGUF files is likewise unpinned: no file is at hand.
+ *
  * All floating point here is fp64 unless the method itself fixes fp32 (the
  * activation scale and the division that produces the activation codes).
  */
