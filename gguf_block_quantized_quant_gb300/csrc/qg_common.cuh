@@ -10,12 +10,13 @@
 namespace qg {
 
 // ---------------------------------------------------------------------------------
-// Launch geometry of the streaming engine: ncw_for(MT) consumer warps + 1 producer warp,
-// one CTA per SM.  Up to 4 tokens per lane the kernel fits 16 consumer warps in the
-// register file (4 per scheduler, to hide the latency of the decode chains); with 8 or 16
-// tokens the accumulators need more registers per thread and 8 warps run.
+// Launch geometry of the streaming engine: ncw_for(MT) warps, one CTA per SM.  Up to 4
+// tokens per lane the kernel fits 16 warps in the register file (4 per scheduler, to hide
+// the latency of the decode chains); with 8 or 16 tokens the accumulators need more
+// registers per thread and 8 warps run.
 __host__ __device__ constexpr int ncw_for(int MT) { return MT <= 4 ? 16 : 8; }
-__host__ __device__ constexpr int nthreads_for(int MT) { return ncw_for(MT) * 32 + 32; }
+__host__ __device__ constexpr int nthreads_for(int MT) { return ncw_for(MT) * 32; }
+
 constexpr int SMEM_MAX = 227 * 1024;       // opt-in dynamic shared memory per CTA (sm_100 family)
 constexpr int STAGE_SLACK = 64;            // bytes after each ring slot for over-reads
 
@@ -80,9 +81,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// The bulk copies of a stage may complete before the producer posts their byte count: the
+// The bulk copies of a stage may complete before the issuing lane posts their byte count: the
 // transaction count may go negative until then, and the phase cannot complete before the
-// producer's arrival.
+// issuing lane's arrival.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
@@ -155,7 +156,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Barrier among the NCONS consumer threads only (the producer warp has returned).
+// Barrier among the NCONS threads that reach it (every warp of the engine).
 template <int NCONS>
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NCONS) : "memory");

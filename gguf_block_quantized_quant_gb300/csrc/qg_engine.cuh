@@ -8,22 +8,20 @@
 // row (tpr tasks, see qg_formats.cuh) with an activation row.  Rows come in groups of grp
 // consecutive rows that are adjacent in memory (a whole matrix for a plain GEMV).
 //
-//  * one CTA per SM (persistent) with NCW consumer warps and one producer warp; the CTA
-//    owns a contiguous range of output rows (and, for split-K, a slice of every row);
-//  * the CTA's tasks are split into NCW contiguous ranges, one per consumer warp; a warp
-//    consumes its range in stages of tps tasks, lane l of step s taking task 32 s + l;
-//  * every warp owns D slots of the shared-memory ring: its j-th stage lands in slot
-//    (j mod D) * NCW + w, so each slot is used by one warp, in order, and no wait on a
-//    slot's mbarrier can be ahead of the slot's previous phase;
-//  * producer lane w feeds consumer warp w: it polls the "empty" mbarrier of the warp's
-//    next slot (non-blocking, so the lanes progress independently), then copies the
-//    stage's weight bytes -- one piece per run of adjacent rows -- with 1-D bulk copies
-//    (cp.async.bulk, the TMA engine), completion counted in bytes on the slot's "full"
-//    mbarrier; pieces that start or end off a 16-byte boundary are widened to it, and
+//  * one CTA per SM (persistent) with NCW warps; the CTA owns a contiguous range of output
+//    rows (and, for split-K, a slice of every row);
+//  * the CTA's tasks are split into NCW contiguous ranges, one per warp; a warp consumes
+//    its range in stages of tps tasks, lane l of step s taking task 32 s + l;
+//  * every warp feeds itself: it owns D slots of the shared-memory ring (its j-th stage
+//    lands in slot (j mod D) * NCW + w), issues its first D stages up front, and refills a
+//    slot with stage j + D as soon as it has consumed stage j.  A stage is copied with 1-D
+//    bulk copies (cp.async.bulk, the TMA engine), one per run of adjacent rows, issued by
+//    up to NPIECE_MAX lanes in parallel; completion is counted in bytes on the slot's
+//    mbarrier.  Pieces that start or end off a 16-byte boundary are widened to it, and
 //    bytes past the end of a tensor that the widened copy may not read are loaded one by
-//    one;
-//  * activations arrive as a tile image written once per call by a preparation kernel; the
-//    producer issues the first stages, then waits for that kernel (programmatic dependent
+//    one.  No warp ever waits for another warp's progress to get its data;
+//  * activations arrive as a tile image written once per call by a preparation kernel;
+//    warp 0 issues its first stages, then waits for that kernel (programmatic dependent
 //    launch) and copies the image rows the CTA needs into shared memory;
 //  * a lane decodes its task in registers against the activation tiles; per step, a
 //    segmented shuffle reduction (rows are contiguous runs of lanes) leaves each row's
@@ -38,7 +36,7 @@
 namespace qg {
 
 constexpr int NPIECE_MAX = 8;      // weight pieces per stage
-constexpr int SCRATCH_INTS = 256;  // producer scratch (MoE top-k ids)
+constexpr int SCRATCH_INTS = 256;  // prologue scratch (MoE top-k ids)
 constexpr int BND_FLOATS = 1 + 16; // boundary entry: row, then one sum per token
 
 // Unsigned division by a run-time constant (n < 2^31, d < 2^31): 32-bit reciprocal
@@ -60,10 +58,10 @@ struct FastDiv {
 };
 
 // Shared memory of the engine besides the ring, the activation tiles and the job area:
-// boundary sums (2 per warp), producer scratch, 2*S + 1 mbarriers, piece headers (per slot:
+// boundary sums (2 per warp), prologue scratch, S + 1 mbarriers, piece headers (per slot:
 // NPIECE_MAX piece addresses and the end of the tasks the pieces cover).
 __host__ __device__ constexpr uint32_t engine_fixed_smem(int S, int ncw) {
-    return (uint32_t)(ncw * 2 * BND_FLOATS * 4) + 4u * SCRATCH_INTS + 16u * (uint32_t)S + 8u +
+    return (uint32_t)(ncw * 2 * BND_FLOATS * 4) + 4u * SCRATCH_INTS + 8u * (uint32_t)S + 8u +
            4u * (NPIECE_MAX + 1) * (uint32_t)S + 16u;
 }
 
@@ -81,6 +79,12 @@ struct AccSink {
     __device__ __forceinline__ void unit(int m, int, int, int, float contrib) { acc[m] += contrib; }
 };
 
+// Orders this thread's earlier generic-proxy accesses of shared memory before its later
+// async-proxy (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <int FMT, int T, int MT, class Job>
 __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job job) {
     using F = FT<FMT, T>;
@@ -96,19 +100,31 @@ __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job j
     const uint32_t xa = ring + (uint32_t)S * slot_stride;              // activation tiles
     const uint32_t ja = xa + job.x_bytes;                              // job area
     const uint32_t bnd = ja + job.j_bytes;                             // boundary sums
-    const uint32_t scr = bnd + (uint32_t)(NCW * 2 * BND_FLOATS * 4);   // producer scratch
+    const uint32_t scr = bnd + (uint32_t)(NCW * 2 * BND_FLOATS * 4);   // prologue scratch
     const uint32_t bars = scr + 4u * SCRATCH_INTS;
-    const uint32_t xbar = bars + 16u * (uint32_t)S;
+    const uint32_t xbar = bars + 8u * (uint32_t)S;
     const uint32_t hdrs = xbar + 8u;
     auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(S + s); };
     auto hdr = [&](int s, int p) { return hdrs + 4u * (uint32_t)(s * (NPIECE_MAX + 1) + p); };
     const uint32_t tok_stride = (uint32_t)(job.tpr_x * TL::STRIDE);
     float *bsum = reinterpret_cast<float *>(smem + (bnd - ring));  // [NCW][2][BND_FLOATS]
     int *scratch = reinterpret_cast<int *>(smem + (scr - ring));
     float *jarea = reinterpret_cast<float *>(smem + (ja - ring));
 
-    // this CTA's tasks and the consumer warps' ranges (whole blocks)
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(full_bar(s), 1);
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+    }
+    if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
+    job.init(jarea, tid);
+    if constexpr (Job::HAS_PROLOGUE) {
+        __syncthreads();
+        if (warp == 0) job.prologue(lane, scratch);
+    }
+    __syncthreads();
+
+    // this CTA's tasks and this warp's range (whole blocks)
     int o0, o1, tpr, grp;
     job.cta(o0, o1, tpr, grp);
     const int ntask = (o1 - o0) * tpr;
@@ -117,68 +133,80 @@ __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job j
     auto wstart = [&](int w) { return (int)((long)units * w / NCW) * F::TPB; };
     const int maxlen = (units + NCW - 1) / NCW * F::TPB;
     const int nchunk = (maxlen + job.tps - 1) / job.tps;
+    const int a = wstart(warp), b = wstart(warp + 1);
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        mbar_init(xbar, 1);
-        fence_mbar_init();
-    }
-    if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
-    job.init(jarea, tid);
-    __syncthreads();
-
-    if (warp == NCW) {
-        // ------------------------------------------------------------------ producer
-        job.producer_prologue(lane, scratch);
-        __syncwarp();
-        const bool act = lane < NCW;  // lane w feeds consumer warp w
-        const int wa = act ? wstart(lane) : 0, wb = act ? wstart(lane + 1) : 0;
-        // Issues stage j of warp `lane` into its slot (the slot is known to be free).
-        auto issue = [&](int j) {
-            const int slot = (j % D) * NCW + lane;
-            const int fa = wa + j * job.tps, fb = min(wb, fa + job.tps);
-            const uint32_t sbase = ring + (uint32_t)slot * slot_stride;
-            const uint32_t fbar = full_bar(slot);
-            uint32_t off = 0, tx = 0;
-            int np = 0, f = fa;
-            for (; f < fb && np < NPIECE_MAX; ++np) {
-                const int o = (int)tpr_div.div((uint32_t)f), tt = f - o * tpr;
-                int fend = fb;
-                if (grp) {
-                    const int gend = ((int)grp_div.div((uint32_t)(o0 + o)) + 1) * grp - o0;  // next group's row
-                    fend = min(fb, gend * tpr);
+    // Copies stage j of this warp into its slot; all 32 lanes take part (lane p < NPIECE_MAX
+    // copies the stage's p-th run of adjacent rows).  The slot must be free.
+    auto issue = [&](int j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = a + j * job.tps, fb = min(b, fa + job.tps);
+        const uint32_t sbase = ring + (uint32_t)slot * slot_stride;
+        const uint32_t fbar = full_bar(slot);
+        int ps = fa, pe = fa;  // this lane's piece [ps, pe)
+        int covered = fb;
+        if (fa < fb) {
+            if (grp == 0) {
+                if (lane == 0) pe = fb;
+            } else {
+                const int oa = (int)tpr_div.div((uint32_t)fa);
+                const int ga = (int)grp_div.div((uint32_t)(o0 + oa));
+                const long g0 = (long)(ga + lane) * grp - o0;  // first CTA-relative row of group ga + lane
+                const long lo = g0 * tpr, hi = (g0 + grp) * tpr;
+                if (lane < NPIECE_MAX) {
+                    ps = (int)max((long)fa, lo);
+                    pe = (int)min((long)fb, hi);
                 }
-                const uint8_t *lim;
-                const uint8_t *src = job.seg_src(o0 + o, tt, lim, scratch);
-                const uint32_t bytes = task_off<F>(fend - f);
-                const uintptr_t s0 = (uintptr_t)src, a0 = s0 & ~(uintptr_t)15, e = s0 + bytes;
-                const uintptr_t a1 = (e + 15) & ~(uintptr_t)15, lim16 = (uintptr_t)lim & ~(uintptr_t)15;
-                uintptr_t a1c = a1 <= lim16 ? a1 : lim16;
-                if (a1c < a0) a1c = a0;
-                for (uintptr_t q = a1c; q < e; ++q)
-                    sts8(sbase + off + (uint32_t)(q - a0), *reinterpret_cast<const uint8_t *>(q));
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, np)), "r"(sbase + off + (uint32_t)(s0 & 15))
-                             : "memory");
-                const uint32_t nb = (uint32_t)(a1c - a0);
-                if (nb) bulk_g2s(sbase + off, reinterpret_cast<const void *>(a0), nb, fbar);
-                tx += nb;
-                off += (uint32_t)(a1 - a0);
-                f = fend;
+                const long cend = ((long)(ga + NPIECE_MAX) * grp - o0) * tpr;  // end of the last piece's group
+                if (cend < fb) {
+                    // the stage needs more pieces than the table holds (a planning error):
+                    // the rest of it is skipped and the host sees DEVERR_PLAN
+                    covered = (int)cend;
+                    if (lane == 0) atomicOr(&g_qg_dev_err, DEVERR_PLAN);
+                }
             }
-            // tasks [f, fb) did not fit the piece table (a planning error): the consumers
-            // skip them and the host sees DEVERR_PLAN
-            if (f < fb) atomicOr(&g_qg_dev_err, DEVERR_PLAN);
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, NPIECE_MAX)), "r"(min(f, fb)) : "memory");
-            mbar_arrive_expect_tx(fbar, tx);
-        };
-        // the first D stages of every warp: the slots are free
-        const int jfirst = min(D, nchunk);
-        if (act)
-            for (int j = 0; j < jfirst; ++j) issue(j);
+        }
+        const bool valid = ps < pe;
+        uintptr_t s0 = 0, a0 = 0, e = 0, a1 = 0, a1c = 0;
+        if (valid) {
+            const int o = (int)tpr_div.div((uint32_t)ps), tt = ps - o * tpr;
+            const uint8_t *lim;
+            const uint8_t *src = job.seg_src(o0 + o, tt, lim, scratch);
+            s0 = (uintptr_t)src;
+            a0 = s0 & ~(uintptr_t)15;
+            e = s0 + task_off<F>(pe - ps);
+            a1 = (e + 15) & ~(uintptr_t)15;
+            const uintptr_t lim16 = (uintptr_t)lim & ~(uintptr_t)15;
+            a1c = a1 <= lim16 ? a1 : lim16;
+            if (a1c < a0) a1c = a0;
+        }
+        // slot offsets: exclusive prefix sum of the widened piece sizes over the lanes
+        const uint32_t wsz = (uint32_t)(a1 - a0);
+        uint32_t incl = wsz;
+#pragma unroll
+        for (int d = 1; d < NPIECE_MAX; d <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        const uint32_t off = incl - wsz;
+        const uint32_t nb = (uint32_t)(a1c - a0);
+        if (valid) {
+            for (uintptr_t q = a1c; q < e; ++q)
+                sts8(sbase + off + (uint32_t)(q - a0), *reinterpret_cast<const uint8_t *>(q));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, lane)), "r"(sbase + off + (uint32_t)(s0 & 15))
+                         : "memory");
+            if (nb) bulk_g2s(sbase + off, reinterpret_cast<const void *>(a0), nb, fbar);
+        }
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, nb);
+        if (lane == 0)
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, NPIECE_MAX)), "r"(covered) : "memory");
         __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(fbar, tx);
+    };
+
+    // the first D stages: the slots are free
+    const int jfirst = min(D, nchunk);
+    for (int j = 0; j < jfirst; ++j) issue(j);
+    if (warp == 0) {
         if (lane == 0) {
             griddep_wait();
             const int rows = ntask > 0 ? job.xrows() : 0;
@@ -191,38 +219,9 @@ __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job j
             mbar_arrive_expect_tx(xbar, tx);
         }
         __syncwarp();
-        // then every lane refills its warp's slots as they are released
-        int j = jfirst;
-        unsigned long long t_idle = 0;
-        for (;;) {
-            const bool more = act && j < nchunk;
-            if (!__any_sync(0xffffffffu, more)) break;
-            const bool ready =
-                more && mbar_test_wait(empty_bar((j % D) * NCW + lane), (uint32_t)((j / D) & 1) ^ 1u);
-            if (ready) {
-                issue(j);
-                ++j;
-            }
-            if (__any_sync(0xffffffffu, ready)) {
-                t_idle = 0;
-            } else {
-                // no consumer warp has released a slot: back off; give up after WAIT_NS
-                if (*reinterpret_cast<volatile unsigned int *>(&g_qg_dev_err) & DEVERR_TIMEOUT) break;
-                const unsigned long long now = globaltimer_ns();
-                if (t_idle == 0) {
-                    t_idle = now;
-                } else if (now - t_idle > WAIT_NS) {
-                    if (lane == 0) atomicOr(&g_qg_dev_err, DEVERR_TIMEOUT);
-                    break;
-                }
-                __nanosleep(32);
-            }
-        }
-        return;
     }
 
-    // ---------------------------------------------------------------------- consumers
-    const int a = wstart(warp), b = wstart(warp + 1);
+    // ---------------------------------------------------------------------- consume
     const int ra = (int)tpr_div.div((uint32_t)a);
     const bool a_mid = a < b && a != ra * tpr;
     const int ntok = job.ntok;
@@ -301,8 +300,12 @@ __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job j
                 carry_o = cont ? olast : -1;
             }
         }
+        // refill the slot with stage j + D once every lane is done reading it
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(slot));
+        if (j + D < nchunk) {
+            fence_proxy_async_smem();
+            issue(j + D);
+        }
     }
     // a range that ended inside a row: its sum is shared with the next warp
     if (carry_o >= 0 && lane == 0) {

@@ -5,16 +5,17 @@
 //                  partial sums to a buffer)
 //   FfnGateUpJob   output rows 0..I-1 = rows of Wg (g), I..2I-1 = rows of Wu (u)
 //   MoeGateUpJob   output rows of g and u for every (token, slot): the slot's routed expert
-//                  (from the router's top-k, computed by the producer warp) or the shared one
+//                  (from the router's top-k, computed by warp 0 in the prologue) or the shared one
 //   MoeDownJob     per CTA, a range of hidden rows n: output rows (token, slot, n) of every
 //                  slot's down matrix, kept in shared memory; the epilogue forms
 //                  y[token][n] = sum over slots, in slot order, of weight * row (shared
 //                  expert: weight 1) -- the weighted aggregation of the expert outputs
 //
-// Engine interface: HAS_FINISH; fields depth, slot_bytes, x_bytes, j_bytes, tpr_x, tps,
-// ntok; cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store, init,
-// finish, producer_prologue.  Activation images (prep_tiles_warp) have one row of task
-// tiles per token (or per MoE slot), row pitch tpr * tile_stride(XGT).
+// Engine interface: HAS_FINISH, HAS_PROLOGUE; fields depth, slot_bytes, x_bytes, j_bytes,
+// tpr_x, tps, ntok; cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store,
+// init, finish, prologue (run by warp 0 before any weight copy, e.g. the MoE top-k).
+// Activation images (prep_tiles_warp) have one row of task tiles per token (or per MoE
+// slot), row pitch tpr * tile_stride(XGT).
 #pragma once
 
 #include "qg_engine.cuh"
@@ -31,7 +32,7 @@ struct EngineFields {
 template <int FMT, int T>
 struct GemvJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = false;
+    static constexpr bool HAS_FINISH = false, HAS_PROLOGUE = false;
     const uint8_t *W, *Wend;
     int N, KS, groups, gpr;  // gpr: task groups (whole blocks) per row
     uint32_t rb;
@@ -68,14 +69,14 @@ struct GemvJob : EngineFields {
     }
     __device__ void init(float *, int) const {}
     __device__ void finish(float *, int, int) const {}
-    __device__ void producer_prologue(int, int *) const {}
+    __device__ void prologue(int, int *) const {}
 };
 
 // ===================================================================================== FFN gate/up
 template <int FMT, int T>
 struct FfnGateUpJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = false;
+    static constexpr bool HAS_FINISH = false, HAS_PROLOGUE = false;
     const uint8_t *Wg, *Wu, *Wg_end, *Wu_end;
     int I, m0;  // tokens [m0, m0 + ntok) of the batch
     uint32_t rb;
@@ -106,7 +107,7 @@ struct FfnGateUpJob : EngineFields {
     }
     __device__ void init(float *, int) const {}
     __device__ void finish(float *, int, int) const {}
-    __device__ void producer_prologue(int, int *) const {}
+    __device__ void prologue(int, int *) const {}
 };
 
 // ===================================================================================== MoE gate/up
@@ -116,7 +117,7 @@ constexpr int E_MAX = 1024;
 template <int FMT, int T>
 struct MoeGateUpJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = false;
+    static constexpr bool HAS_FINISH = false, HAS_PROLOGUE = true;
     const uint8_t *Wg_exps, *Wu_exps, *Wg_sh, *Wu_sh;
     const uint8_t *Wg_exps_end, *Wu_exps_end, *Wg_sh_end, *Wu_sh_end;
     int E, topk, I, M;
@@ -164,11 +165,11 @@ struct MoeGateUpJob : EngineFields {
     }
     __device__ void init(float *, int) const {}
     __device__ void finish(float *, int, int) const {}
-    // Router tail, one warp, after the logits kernel has finished: softmax over E logits,
+    // Router tail, warp 0, after the logits kernel has finished: softmax over E logits,
     // the topk largest (ties: lower id), weights renormalized over the picks.
     // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax
     // probabilities p.
-    __device__ void producer_prologue(int lane, int *ids) const {
+    __device__ void prologue(int lane, int *ids) const {
         griddep_wait();
         for (int m = 0; m < M; ++m) {
             float v[E_MAX / 32];
@@ -232,7 +233,7 @@ struct MoeGateUpJob : EngineFields {
 template <int FMT, int T>
 struct MoeDownJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = true;
+    static constexpr bool HAS_FINISH = true, HAS_PROLOGUE = false;
     const uint8_t *Wd_exps, *Wd_sh, *Wd_exps_end, *Wd_sh_end;
     int E, topk, H, M, m0;          // tokens [m0, m0 + M) of the batch
     uint32_t rb;
@@ -290,7 +291,7 @@ struct MoeDownJob : EngineFields {
             y[(long)(m0 + m) * H + n0 + r] = acc;
         }
     }
-    __device__ void producer_prologue(int, int *) const {}
+    __device__ void prologue(int, int *) const {}
 };
 
 }  // namespace qg
