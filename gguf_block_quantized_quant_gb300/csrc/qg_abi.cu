@@ -6,6 +6,8 @@
 // mapping of a failure to "the caller runs the CPU path" is deliberately not reproduced:
 // a failure is returned as a negative status and nothing runs elsewhere.
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/qg.h"
 #include "qg_jobs.cuh"
@@ -44,22 +46,28 @@ __global__ void splitk_reduce_kernel(const float *part, int KS, long MN, float *
     }
 }
 
-// Activation tile image (see prep_tiles_warp); lets the dependent engine kernel start.
+// Activation tile image (see prep_tiles_warp).  Launched as a programmatic dependent of the
+// previous kernel in the stream: it lets its own dependent (the engine) start at once, then
+// waits for the previous kernel to finish before it reads any input or writes the
+// workspace.
 __global__ void __launch_bounds__(256) prep_tiles_kernel(const float *x, const float *u, float *h_out,
                                                          const int8_t *xq, const float *xd, const int32_t *xs,
                                                          int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq,
                                                          float *md, int32_t *ms) {
     griddep_launch_dependents();
+    griddep_wait();
     const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
     const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     prep_tiles_warp(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
 }
 
 // Blocks [0, ceil(E/8)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32, one warp per
-// expert row.  The remaining blocks write the activation tile image of x.
+// expert row.  The remaining blocks write the activation tile image of x.  Launched like
+// prep_tiles_kernel.
 __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M, int H, const float *Wr, int E,
                                                           float *logits, int xgt_log2, uint8_t *img) {
     griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int nrouter = (E + 7) / 8;
     if ((int)blockIdx.x >= nrouter) {
@@ -90,16 +98,54 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
     }
 }
 
+// The small kernels ask for the same L1 / shared-memory split as the engine (all shared),
+// so that an SM does not have to change its configuration between them and the engine and
+// they can run beside an engine CTA.  Set once per kernel and device.
+static bool prefer_shared(const void *kern) {
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kern, dev})) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return false;
+    done.insert({kern, dev});
+    return true;
+}
+
 int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *xd, int32_t *xs, cudaStream_t s) {
     const long blocks = (long)M * (K / 32);
     const int grid = (int)std::min<long>((blocks + 7) / 8, 4096);
+    if (!prefer_shared((const void *)quant_act_kernel)) return QG_ECUDA;
     quant_act_kernel<<<grid, 256, 0, s>>>(x, M, K, ldx, xq, xd, xs);
     return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
 }
 
 int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStream_t s) {
     const int grid = (int)std::min<long>((MN + 255) / 256, 1024);
+    if (!prefer_shared((const void *)splitk_reduce_kernel)) return QG_ECUDA;
     splitk_reduce_kernel<<<grid, 256, 0, s>>>(part, KS, MN, y);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream is still running (it must griddep_wait() before touching its data).
+template <class... KArgs, class... Args>
+static int launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t s, Args... args) {
+    if (!prefer_shared((const void *)kern)) return QG_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) != cudaSuccess) return QG_ECUDA;
     return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
 }
 
@@ -108,16 +154,14 @@ int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t
                       int32_t *ms, cudaStream_t s) {
     const long blocks = (long)rows * (K / 32);
     const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
-    prep_tiles_kernel<<<grid, 256, 0, s>>>(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
-    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+    return launch_pdl(prep_tiles_kernel, grid, 256, s, x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
 }
 
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,
                        uint8_t *img, cudaStream_t s) {
     const long blocks = (long)M * (H / 32);
     const int nprep = (int)std::min<long>((blocks + 7) / 8, 512);
-    router_prep_kernel<<<(E + 7) / 8 + nprep, 256, 0, s>>>(x, M, H, Wr, E, logits, xgt_log2, img);
-    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+    return launch_pdl(router_prep_kernel, (E + 7) / 8 + nprep, 256, s, x, M, H, Wr, E, logits, xgt_log2, img);
 }
 
 // ----------------------------------------------------------------------------- host helpers

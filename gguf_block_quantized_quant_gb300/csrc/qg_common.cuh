@@ -10,12 +10,14 @@
 namespace qg {
 
 // ---------------------------------------------------------------------------------
-// Launch geometry of the streaming engine: ncw_for(MT) warps, one CTA per SM.  Up to 4
-// tokens per lane the kernel fits 16 warps in the register file (4 per scheduler, to hide
-// the latency of the decode chains); with 8 or 16 tokens the accumulators need more
-// registers per thread and 8 warps run.
-__host__ __device__ constexpr int ncw_for(int MT) { return MT <= 4 ? 16 : 8; }
-__host__ __device__ constexpr int nthreads_for(int MT) { return ncw_for(MT) * 32; }
+// Launch geometry of the streaming engine: engine_ncw() warps, one CTA per SM.  Tasks of at
+// most 160 bytes with up to 4 tokens per lane run 16 warps (4 per scheduler, to hide the
+// latency of the decode chains, with two ring slots of 32 tasks per warp); larger tasks
+// (whose ring slots are twice the size and whose lanes carry two independent superblock
+// chains) and 8 or 16 tokens per lane (more accumulator registers) run 8 warps.
+__host__ __device__ constexpr int engine_ncw(int task_bytes, int MT) {
+    return (MT <= 4 && task_bytes <= 160) ? 16 : 8;
+}
 
 constexpr int SMEM_MAX = 227 * 1024;       // opt-in dynamic shared memory per CTA (sm_100 family)
 constexpr int STAGE_SLACK = 64;            // bytes after each ring slot for over-reads
@@ -25,6 +27,7 @@ constexpr int STAGE_SLACK = 64;            // bytes after each ring slot for ove
 constexpr unsigned int DEVERR_TIMEOUT = 1u;
 constexpr unsigned int DEVERR_PLAN = 2u;
 constexpr unsigned long long WAIT_NS = 2000000000ull;   // 2 s
+constexpr unsigned long long WAIT_CHECK_NS = 1000000ull; // 1 ms: look for an earlier timeout
 
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -90,14 +93,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Potentially blocking test: the thread may be suspended (up to about WAIT_HINT_NS) until
+// the phase completes, instead of spinning.
+constexpr uint32_t WAIT_HINT_NS = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(WAIT_HINT_NS)
         : "memory");
     return ok != 0;
 }
@@ -128,14 +134,22 @@ static __device__ unsigned int g_qg_dev_err;
 // ends.  The host reads the error word through qg_device_error().
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    // once any wait has given up, the data is invalid anyway: do not wait again
-    if (*reinterpret_cast<volatile unsigned int *>(&g_qg_dev_err) & DEVERR_TIMEOUT) return false;
-    unsigned long long t0 = globaltimer_ns();
+    const unsigned long long t0 = globaltimer_ns();
+    bool checked = false;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer_ns() - t0 > WAIT_NS) {
-            atomicOr(&g_qg_dev_err, DEVERR_TIMEOUT);
-            return false;
+        if ((it & 15u) == 0) {
+            const unsigned long long dt = globaltimer_ns() - t0;
+            // a wait this long is abnormal: if another wait already gave up, the data is
+            // invalid anyway, so do not wait again (read once; off the normal path)
+            if (!checked && dt > WAIT_CHECK_NS) {
+                checked = true;
+                if (*reinterpret_cast<volatile unsigned int *>(&g_qg_dev_err) & DEVERR_TIMEOUT) return false;
+            }
+            if (dt > WAIT_NS) {
+                atomicOr(&g_qg_dev_err, DEVERR_TIMEOUT);
+                return false;
+            }
         }
     }
 }

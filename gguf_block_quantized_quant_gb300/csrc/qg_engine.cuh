@@ -22,7 +22,9 @@
 //    one.  No warp ever waits for another warp's progress to get its data;
 //  * activations arrive as a tile image written once per call by a preparation kernel;
 //    warp 0 issues its first stages, then waits for that kernel (programmatic dependent
-//    launch) and copies the image rows the CTA needs into shared memory;
+//    launch) and copies the image rows the CTA needs into shared memory.  The engine in
+//    turn lets the next call's preparation launch early, so back-to-back calls overlap
+//    one call's tail with the next call's weight streaming;
 //  * a lane decodes its task in registers against the activation tiles; per step, a
 //    segmented shuffle reduction (rows are contiguous runs of lanes) leaves each row's
 //    sum at the row's first lane; a row that continues in the warp's next step is carried
@@ -65,7 +67,7 @@ __host__ __device__ constexpr uint32_t engine_fixed_smem(int S, int ncw) {
            4u * (NPIECE_MAX + 1) * (uint32_t)S + 16u;
 }
 
-// Byte offset of task tt within a row (tasks are whole or half blocks).
+// Byte offset of task tt within a row (tasks are whole blocks, or half a superblock).
 template <class F>
 __host__ __device__ __forceinline__ uint32_t task_off(int tt) {
     return (uint32_t)((tt / F::TPB) * F::BPT * F::BS);
@@ -75,8 +77,9 @@ __host__ __device__ __forceinline__ uint32_t task_off(int tt) {
 template <int NT>
 struct AccSink {
     static constexpr int MT = NT;
+    static constexpr bool DOTS = false;
     float acc[NT];
-    __device__ __forceinline__ void unit(int m, int, int, int, float contrib) { acc[m] += contrib; }
+    __device__ __forceinline__ void add(int m, float v) { acc[m] += v; }
 };
 
 // Orders this thread's earlier generic-proxy accesses of shared memory before its later
@@ -86,10 +89,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 template <int FMT, int T, int MT, class Job>
-__global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job job) {
+__global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1) engine_kernel(const Job job) {
     using F = FT<FMT, T>;
     using TL = Tile<F::XGT>;
-    constexpr int NCW = ncw_for(MT), NCONS = NCW * 32;
+    constexpr int NCW = engine_ncw(F::TASK_BYTES, MT), NCONS = NCW * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -118,6 +121,10 @@ __global__ void __launch_bounds__(nthreads_for(MT), 1) engine_kernel(const Job j
     }
     if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
     job.init(jarea, tid);
+    // the next kernel in the stream (the next call's activation preparation, launched as a
+    // programmatic dependent) may start now: it waits for this grid to finish before it
+    // touches any data, and its own dependent engine takes each SM this CTA leaves
+    griddep_launch_dependents();
     if constexpr (Job::HAS_PROLOGUE) {
         __syncthreads();
         if (warp == 0) job.prologue(lane, scratch);

@@ -18,7 +18,6 @@ namespace qg {
 
 namespace {
 
-constexpr bool kLegacy = QG_FMT == F_Q4_0 || QG_FMT == F_Q8_0;
 template <int V>
 using ic = std::integral_constant<int, V>;
 
@@ -34,14 +33,16 @@ int launch_engine(const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!ready[dev]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) != cudaSuccess)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) != cudaSuccess ||
+                cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 return -4;
             ready[dev] = true;
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(nthreads_for(MT));
+    cfg.blockDim = dim3(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -65,13 +66,22 @@ int launch_engine_mt(int MT, const Job &job, int grid, uint32_t smem, cudaStream
     }
 }
 
-// Runs fn(ic<T>) with the task size the plan chose (legacy formats: 4 blocks or 1).
+// Runs fn(ic<T>) with the task size the plan chose (see task_geo).
 template <class Fn>
 int with_t(const TaskGeo &g, Fn &&fn) {
-    if constexpr (kLegacy) {
+    if constexpr (QG_FMT == F_Q4_0) {
+        if (g.T == 8) return fn(ic<8>{});
         if (g.T == 4) return fn(ic<4>{});
+        return fn(ic<1>{});
+    } else if constexpr (QG_FMT == F_Q8_0) {
+        if (g.T == 4) return fn(ic<4>{});
+        return fn(ic<1>{});
+    } else if constexpr (QG_FMT == F_Q5_K || QG_FMT == F_Q6_K) {
+        return fn(ic<2>{});
+    } else {
+        if (g.T == 2) return fn(ic<2>{});
+        return fn(ic<1>{});
     }
-    return fn(ic<1>{});
 }
 
 template <class J>
@@ -263,16 +273,17 @@ int moe_run(const MoeCall &c, int sms) {
 // token's activation tile is built next to it.
 struct DotSink {
     static constexpr int MT = 1;
+    static constexpr bool DOTS = true;
     int32_t *dots, *aux;
     long base;  // index of unit 0 of this task for this token
     bool kquant;
-    __device__ __forceinline__ void unit(int, int u, int dot, int xs, float) {
+    __device__ __forceinline__ void unit(int, int u, int dot, int xs) {
         dots[base + u] = dot;
         aux[base + u] = kquant ? xs : 0;
     }
 };
 
-constexpr int HOOK_THREADS = 64, HOOK_WIN = 256, HOOK_TILE = 384;
+constexpr int HOOK_THREADS = 32, HOOK_WIN = 320, HOOK_TILE = 800;
 
 template <int FMT, int T>
 __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t *W, const int8_t *xq,
@@ -280,6 +291,7 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
                                                                   int32_t *dots, int32_t *aux) {
     using F = FT<FMT, T>;
     using TL = Tile<F::XGT>;
+    static_assert(F::BPT * F::BS + 15 <= HOOK_WIN && TL::STRIDE <= HOOK_TILE, "test-hook window too small");
     __shared__ __align__(16) uint8_t mem[HOOK_THREADS * (HOOK_WIN + HOOK_TILE)];
     const int nbr = K / F::QK, nu = K / 32;
     const int tpr = nbr / F::BPT * F::TPB;
@@ -305,6 +317,7 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
             reinterpret_cast<int32_t *>(tile + TL::S)[u] = xs[(long)m * nu + xb];
             reinterpret_cast<uint32_t *>(tile + TL::H)[u] =
                 ((uint32_t)hs & 0xffffu) | ((uint32_t)(sum - hs) << 16);
+            reinterpret_cast<float *>(tile + TL::Q)[u] = 0.0f;
         }
         DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K};
         F::run(smem_addr(blk), tt % F::TPB, XT{smem_addr(tile), 0}, 1, sink);

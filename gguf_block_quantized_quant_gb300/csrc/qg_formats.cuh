@@ -16,14 +16,14 @@
 //   Q6_K   210 B: ql[128], qh[64], int8 sc[16], fp16 d          w = d*sc[e/16]*(code-32)
 //   IQ4_XS 136 B: fp16 d, u16 scales_h, scales_l[4], qs[128]   w = d*(ls-32)*K[idx]
 //
-// Work is organised in TASKS, one per lane: four (or one) Q4_0/Q8_0 blocks, one Q4_K or
-// IQ4_XS superblock, half a Q5_K or Q6_K superblock.  A task's weights are read from
-// shared memory; its activations come from a per-task tile (codes, scales d, sums s and
-// packed 16-element half sums of each activation block), padded so that the 16-byte
-// loads of 8 consecutive lanes hit distinct banks.  Each format calls sink.unit(m, u, dot,
-// xs, contrib) once per token m and unit u with the exact integer dot product of the unit
-// and its fp32 contribution to y; the GEMV sink adds the contribution, the test-hook sink
-// stores the integers.
+// Work is organised in TASKS, one per lane: eight, four or one Q4_0 blocks, four or one
+// Q8_0 blocks, two or one Q4_K / IQ4_XS superblocks, a whole (or half a) Q5_K / Q6_K
+// superblock.  A task's weights are read from shared memory; its activations come from a
+// per-task tile (codes, scales d, sums s, packed 16-element half sums and d*s of each
+// activation block), padded so that the 16-byte loads of 8 consecutive lanes hit distinct
+// banks.  Every unit's dot product is an exact int32 sum; the test-hook sink receives
+// those integers (sink.unit), the GEMV sink the benchmark's fp32 contribution to y (sink.add),
+// formed with as few conversions and multiplies per unit as the format allows.
 #pragma once
 
 #include "qg_common.cuh"
@@ -42,15 +42,16 @@ __device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32
 
 // ---------------------------------------------------------------------------------- tiles
 // Activation tile of XGT units: codes[32*XGT] | d[XGT] fp32 | s[XGT] int32 |
-// h[XGT] (sum of codes 0..15 in the low 16 bits, 16..31 in the high 16 bits), padded to an
-// odd number of 16-byte chunks.
-__host__ __device__ constexpr int tile_raw(int xgt) { return 44 * xgt; }
+// h[XGT] (sum of codes 0..15 in the low 16 bits, 16..31 in the high 16 bits) |
+// ds[XGT] fp32 (d * s, the activation side of the K-quant min term), padded to an odd
+// number of 16-byte chunks.
+__host__ __device__ constexpr int tile_raw(int xgt) { return 48 * xgt; }
 __host__ __device__ constexpr int tile_stride(int xgt) {
     return ((tile_raw(xgt) + 15) / 16) % 2 == 1 ? (tile_raw(xgt) + 15) / 16 * 16 : (tile_raw(xgt) + 15) / 16 * 16 + 16;
 }
 template <int XGT>
 struct Tile {
-    static constexpr int D = 32 * XGT, S = D + 4 * XGT, H = S + 4 * XGT, STRIDE = tile_stride(XGT);
+    static constexpr int D = 32 * XGT, S = D + 4 * XGT, H = S + 4 * XGT, Q = H + 4 * XGT, STRIDE = tile_stride(XGT);
 };
 
 __device__ __forceinline__ void ldx8(uint32_t a, uint32_t (&x)[8]) {
@@ -72,10 +73,18 @@ __device__ __forceinline__ uint32_t word_at(const uint32_t (&w)[NW], int off) {
     return (off & 3) ? prmt(w[off >> 2], w[(off >> 2) + 1], 0x5432u) : w[off >> 2];
 }
 
+// Byte k of w, zero-extended.
+__device__ __forceinline__ int byte_of(uint32_t w, int k) { return (int)((w >> (8 * k)) & 255u); }
+
+// Sinks.  A format calls, per token m:
+//   DOTS sinks:   unit(m, u, dot, xs) with the exact int32 dot of unit u and the
+//                 activation sum xs (the integer contract of the test hook);
+//   value sinks:  add(m, v) with the benchmark's fp32 contribution to y.
+
 // ================================================================================ Q8_0 / Q4_0
-// T blocks per task.  With T == 4 a task is 136 (Q8_0) or 72 (Q4_0) bytes and always starts
-// 8-byte aligned, so all field offsets are compile-time; with T == 1 the block may start on
-// any even byte and is realigned with run-time byte permutes.
+// T blocks per task.  With T == 4 or 8 a task is T*34 (Q8_0) or T*18 (Q4_0) bytes; every
+// group of 4 blocks starts 8-byte aligned, so all field offsets are compile-time; with
+// T == 1 the block may start on any even byte and is realigned with run-time byte permutes.
 template <int FMT, int T>
 struct FmtLegacy {
     static constexpr int QK = 32, BS = (FMT == F_Q8_0 ? 34 : 18), XGT = T, TPB = 1, BPT = T;
@@ -87,7 +96,6 @@ struct FmtLegacy {
         using TL = Tile<XGT>;
         uint32_t x[8];
         ldx8(tile + 32 * u, x);
-        const float xd = ldsf(tile + TL::D + 4 * u);
         int dot = 0;
         int xs = 0;
         if (FMT == F_Q8_0) {
@@ -104,30 +112,37 @@ struct FmtLegacy {
             xs = (int)lds32(tile + TL::S + 4 * u);
             dot = lo + (hi >> 4) - 8 * xs;
         }
-        sink.unit(m, u, dot, xs, d * xd * (float)dot);
+        if constexpr (Sink::DOTS) {
+            sink.unit(m, u, dot, xs);
+        } else {
+            sink.add(m, d * ldsf(tile + TL::D + 4 * u) * (float)dot);
+        }
     }
 
     template <class Sink>
     __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
-        if constexpr (T == 4) {
-            constexpr int NW = TASK_BYTES / 4 + 2;
-            uint32_t w[NW];
+        if constexpr (T >= 4) {
+            constexpr int NW = 4 * BS / 4 + 2;
 #pragma unroll
-            for (int i = 0; i < NW / 2; ++i) {
-                const uint2 v = lds64(addr + 8 * i);
-                w[2 * i] = v.x;
-                w[2 * i + 1] = v.y;
-            }
+            for (int g = 0; g < T / 4; ++g) {
+                uint32_t w[NW];
 #pragma unroll
-            for (int b = 0; b < T; ++b) {
-                const int off = BS * b;
-                const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
-                uint32_t c[8];
+                for (int i = 0; i < NW / 2; ++i) {
+                    const uint2 v = lds64(addr + 4 * BS * g + 8 * i);
+                    w[2 * i] = v.x;
+                    w[2 * i + 1] = v.y;
+                }
 #pragma unroll
-                for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
+                for (int b = 0; b < 4; ++b) {
+                    const int off = BS * b;
+                    const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                    uint32_t c[8];
 #pragma unroll
-                for (int m = 0; m < Sink::MT; ++m)
-                    if (m < ntok) unit_from_words(c, d, m, b, xt.tile(m), sink);
+                    for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
+#pragma unroll
+                    for (int m = 0; m < Sink::MT; ++m)
+                        if (m < ntok) unit_from_words(c, d, m, 4 * g + b, xt.tile(m), sink);
+                }
             }
         } else {
             const uint32_t a = addr & 3u, base = addr - a;  // a is 0 or 2
@@ -148,35 +163,42 @@ struct FmtLegacy {
 };
 
 // ================================================================================ Q4_K
-// One superblock per task.  The 8 six-bit scales and mins are unpacked four at a time into
+// T superblocks per task.  The 8 six-bit scales and mins are unpacked four at a time into
 // bytes; sub-block 2p uses the low nibbles of qs[32p..32p+31], sub-block 2p+1 the high
-// nibbles, which are multiplied in place (16 * nibble) by an unsigned dp4a.
+// nibbles, which are multiplied in place (16 * nibble) by an unsigned dp4a.  Value path:
+// per token, A = sum_j xd_j * (S_j * dot_j) and B = sum_j (xd_j * s_j) * M_j are
+// accumulated, and the superblock's d and dmin are applied once: y += d * A - dmin * B.
+template <int T>
 struct FmtQ4K {
-    static constexpr int QK = 256, BS = 144, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 144;
+    static constexpr int QK = 256, BS = 144, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 144 * T;
+
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
-        using TL = Tile<8>;
+    __device__ __forceinline__ static void superblock(uint32_t addr, int u0, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
         const uint4 h = lds128(addr);
-        const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
         const uint32_t S03 = h.y & 0x3f3f3f3fu, M03 = h.z & 0x3f3f3f3fu;
         const uint32_t S47 = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
         const uint32_t M47 = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+        float A[MT], B[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             uint32_t q[8];
             ldx8(addr + 16 + 32 * p, q);
             const uint32_t Sw = p < 2 ? S03 : S47, Mw = p < 2 ? M03 : M47;
-            const int sh = 16 * (p & 1);
-            const float fa0 = d * (float)((Sw >> sh) & 255u), fa1 = d * (float)((Sw >> (sh + 8)) & 255u);
-            const float fb0 = dmin * (float)((Mw >> sh) & 255u), fb1 = dmin * (float)((Mw >> (sh + 8)) & 255u);
+            const int k0 = 2 * (p & 1);
+            const int sc0 = byte_of(Sw, k0), sc1 = byte_of(Sw, k0 + 1);
+            const float mn0 = (float)byte_of(Mw, k0), mn1 = (float)byte_of(Mw, k0 + 1);
+            const int u = u0 + 2 * p;
 #pragma unroll
-            for (int m = 0; m < Sink::MT; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 if (m < ntok) {
                     const uint32_t t = xt.tile(m);
                     uint32_t xa[8], xb[8];
-                    ldx8(t + 64 * p, xa);
-                    ldx8(t + 64 * p + 32, xb);
-                    const uint2 xd = lds64(t + TL::D + 8 * p), xs = lds64(t + TL::S + 8 * p);
+                    ldx8(t + 32 * u, xa);
+                    ldx8(t + 32 * u + 32, xb);
                     int da = 0, db = 0;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -184,128 +206,189 @@ struct FmtQ4K {
                         db = dp4a_us(q[k] & 0xf0f0f0f0u, xb[k], db);
                     }
                     db >>= 4;
-                    const int s0 = (int)xs.x, s1 = (int)xs.y;
-                    sink.unit(m, 2 * p, da, s0, __uint_as_float(xd.x) * fmaf(fa0, (float)da, -fb0 * (float)s0));
-                    sink.unit(m, 2 * p + 1, db, s1, __uint_as_float(xd.y) * fmaf(fa1, (float)db, -fb1 * (float)s1));
+                    if constexpr (Sink::DOTS) {
+                        const uint2 xs = lds64(t + TL::S + 4 * u);
+                        sink.unit(m, u, da, (int)xs.x);
+                        sink.unit(m, u + 1, db, (int)xs.y);
+                    } else {
+                        const uint2 xd = lds64(t + TL::D + 4 * u), xq = lds64(t + TL::Q + 4 * u);
+                        A[m] = fmaf(__uint_as_float(xd.x), (float)(sc0 * da), A[m]);
+                        A[m] = fmaf(__uint_as_float(xd.y), (float)(sc1 * db), A[m]);
+                        B[m] = fmaf(__uint_as_float(xq.x), mn0, B[m]);
+                        B[m] = fmaf(__uint_as_float(xq.y), mn1, B[m]);
+                    }
                 }
             }
         }
+        if constexpr (!Sink::DOTS) {
+            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
+        }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) superblock(addr + BS * t, 8 * t, xt, ntok, sink);
     }
 };
 
 // ================================================================================ Q5_K
-// Half a superblock per task (sub-blocks 4*hf .. 4*hf+3); the fifth bit of sub-block j is
-// bit j of each qh byte.
+// T == 2: a whole superblock per task; T == 1: half a superblock (sub-blocks 4*hf ..
+// 4*hf+3).  The fifth bit of sub-block j is bit j of each qh byte.  Combine as Q4_K.
+template <int T>
 struct FmtQ5K {
-    static constexpr int QK = 256, BS = 176, XGT = 4, TPB = 2, BPT = 1, TASK_BYTES = 88;
+    static constexpr int QK = 256, BS = 176, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 88 * T;
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int hf, const XT &xt, int ntok, Sink &sink) {
-        using TL = Tile<4>;
+    __device__ __forceinline__ static void run(uint32_t addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
         const uint4 h = lds128(addr);
-        const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
-        const uint32_t Sw = hf ? ((h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u)) : (h.y & 0x3f3f3f3fu);
-        const uint32_t Mw = hf ? (((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u)) : (h.z & 0x3f3f3f3fu);
         uint32_t qh[8];
         ldx8(addr + 16, qh);
+        float A[MT], B[MT];
 #pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-            const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
-            uint32_t q[8];
-            ldx8(addr + 48 + 32 * (2 * hf + pp), q);
-            uint32_t c0[8], c1[8];
+        for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
-                c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
-            }
-            const float fa0 = d * (float)((Sw >> (16 * pp)) & 255u), fa1 = d * (float)((Sw >> (16 * pp + 8)) & 255u);
-            const float fb0 = dmin * (float)((Mw >> (16 * pp)) & 255u);
-            const float fb1 = dmin * (float)((Mw >> (16 * pp + 8)) & 255u);
+        for (int i = 0; i < T; ++i) {
+            const int hf = T == 2 ? i : hf_arg;
+            const uint32_t Sw = hf ? ((h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u)) : (h.y & 0x3f3f3f3fu);
+            const uint32_t Mw = hf ? (((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u)) : (h.z & 0x3f3f3f3fu);
 #pragma unroll
-            for (int m = 0; m < Sink::MT; ++m) {
-                if (m < ntok) {
-                    const uint32_t t = xt.tile(m);
-                    uint32_t xa[8], xb[8];
-                    ldx8(t + 64 * pp, xa);
-                    ldx8(t + 64 * pp + 32, xb);
-                    const uint2 xd = lds64(t + TL::D + 8 * pp), xs = lds64(t + TL::S + 8 * pp);
-                    int da = 0, db = 0;
+            for (int pp = 0; pp < 2; ++pp) {
+                const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
+                const int u = 4 * i + 2 * pp;    // their units in the task tile
+                uint32_t q[8];
+                ldx8(addr + 48 + 32 * (2 * hf + pp), q);
+                uint32_t c0[8], c1[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        da = dp4a(c0[k], xa[k], da);
-                        db = dp4a(c1[k], xb[k], db);
+                for (int k = 0; k < 8; ++k) {
+                    c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
+                    c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
+                }
+                const int sc0 = byte_of(Sw, 2 * pp), sc1 = byte_of(Sw, 2 * pp + 1);
+                const float mn0 = (float)byte_of(Mw, 2 * pp), mn1 = (float)byte_of(Mw, 2 * pp + 1);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < ntok) {
+                        const uint32_t t = xt.tile(m);
+                        uint32_t xa[8], xb[8];
+                        ldx8(t + 32 * u, xa);
+                        ldx8(t + 32 * u + 32, xb);
+                        int da = 0, db = 0;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            da = dp4a(c0[k], xa[k], da);
+                            db = dp4a(c1[k], xb[k], db);
+                        }
+                        if constexpr (Sink::DOTS) {
+                            const uint2 xs = lds64(t + TL::S + 4 * u);
+                            sink.unit(m, u, da, (int)xs.x);
+                            sink.unit(m, u + 1, db, (int)xs.y);
+                        } else {
+                            const uint2 xd = lds64(t + TL::D + 4 * u), xq = lds64(t + TL::Q + 4 * u);
+                            A[m] = fmaf(__uint_as_float(xd.x), (float)(sc0 * da), A[m]);
+                            A[m] = fmaf(__uint_as_float(xd.y), (float)(sc1 * db), A[m]);
+                            B[m] = fmaf(__uint_as_float(xq.x), mn0, B[m]);
+                            B[m] = fmaf(__uint_as_float(xq.y), mn1, B[m]);
+                        }
                     }
-                    const int s0 = (int)xs.x, s1 = (int)xs.y;
-                    sink.unit(m, 2 * pp, da, s0, __uint_as_float(xd.x) * fmaf(fa0, (float)da, -fb0 * (float)s0));
-                    sink.unit(m, 2 * pp + 1, db, s1, __uint_as_float(xd.y) * fmaf(fa1, (float)db, -fb1 * (float)s1));
                 }
             }
+        }
+        if constexpr (!Sink::DOTS) {
+            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
         }
     }
 };
 
 // ================================================================================ Q6_K
-// Half a superblock per task (elements 128*hf .. +127, activation blocks t = 0..3): the low
-// four bits of element 32t + l come from byte l + 32*(t&1) of the half's 64 ql bytes (low
-// nibble for t < 2), the top two from bits 2t, 2t+1 of qh byte l.  Codes are used unsigned
-// (0..63) and the -32 offset is applied through the activation half sums.  Superblocks may
-// start on any even byte: words are realigned with run-time byte permutes.
+// T == 2: a whole superblock per task; T == 1: half a superblock (elements 128*hf ..
+// +127).  Within a half, activation block t = 0..3: the low four bits of element 32t + l
+// come from byte l + 32*(t&1) of the half's 64 ql bytes (low nibble for t < 2), the top two
+// from bits 2t, 2t+1 of qh byte l.  Codes are used unsigned (0..63) and the -32 offset is
+// applied through the activation half sums.  Superblocks may start on any even byte: words
+// are realigned with run-time byte permutes.  Value path: sum_t xd_t * dot_t per token,
+// times d once.
+template <int T>
 struct FmtQ6K {
-    static constexpr int QK = 256, BS = 210, XGT = 4, TPB = 2, BPT = 1, TASK_BYTES = 105;
+    static constexpr int QK = 256, BS = 210, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 105 * T;
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int hf, const XT &xt, int ntok, Sink &sink) {
-        using TL = Tile<4>;
+    __device__ __forceinline__ static void run(uint32_t addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
         const uint32_t a = addr & 3u, base = addr - a;
         const uint32_t sel = a ? 0x5432u : 0x3210u;
-        uint32_t qh[9];
+        float A[MT];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) qh[k] = lds32(base + 128 + 32 * hf + 4 * k);
-        uint32_t hw[8];
+        for (int m = 0; m < MT; ++m) A[m] = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) hw[k] = prmt(qh[k], qh[k + 1], sel);
-        const uint32_t so = a + 192 + 8 * hf;  // 8 sub-scales of this half (even offset)
-        const uint32_t s0w = lds32(base + (so & ~3u)), s1w = lds32(base + (so & ~3u) + 4),
-                       s2w = lds32(base + (so & ~3u) + 8);
-        const uint32_t scA = prmt(s0w, s1w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+0..3]
-        const uint32_t scB = prmt(s1w, s2w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+4..7]
-        const float d = half_bits_to_float(lds32(base + 208) >> (8 * a));
+        for (int i = 0; i < T; ++i) {
+            const int hf = T == 2 ? i : hf_arg;
+            uint32_t qh[9];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            uint32_t ql[9];
+            for (int k = 0; k < 9; ++k) qh[k] = lds32(base + 128 + 32 * hf + 4 * k);
+            uint32_t hw[8];
 #pragma unroll
-            for (int k = 0; k < 9; ++k) ql[k] = lds32(base + 64 * hf + 32 * s + 4 * k);
-            uint32_t lw[8];
+            for (int k = 0; k < 8; ++k) hw[k] = prmt(qh[k], qh[k + 1], sel);
+            const uint32_t so = a + 192 + 8 * hf;  // 8 sub-scales of this half (even offset)
+            const uint32_t s0w = lds32(base + (so & ~3u)), s1w = lds32(base + (so & ~3u) + 4),
+                           s2w = lds32(base + (so & ~3u) + 8);
+            const uint32_t scA = prmt(s0w, s1w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+0..3]
+            const uint32_t scB = prmt(s1w, s2w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+4..7]
 #pragma unroll
-            for (int k = 0; k < 8; ++k) lw[k] = prmt(ql[k], ql[k + 1], sel);
+            for (int s = 0; s < 2; ++s) {
+                uint32_t ql[9];
 #pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int t = s + 2 * tt;  // activation block within the half
-                uint32_t c[8];
+                for (int k = 0; k < 9; ++k) ql[k] = lds32(base + 64 * hf + 32 * s + 4 * k);
+                uint32_t lw[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    c[k] = ((lw[k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[k] >> (2 * t)) & 0x03030303u) << 4);
-                const uint32_t scw = t < 2 ? scA : scB;
-                const int sA = (int)(int8_t)((scw >> (16 * (t & 1))) & 255u);
-                const int sB = (int)(int8_t)((scw >> (16 * (t & 1) + 8)) & 255u);
+                for (int k = 0; k < 8; ++k) lw[k] = prmt(ql[k], ql[k + 1], sel);
 #pragma unroll
-                for (int m = 0; m < Sink::MT; ++m) {
-                    if (m < ntok) {
-                        const uint32_t tl = xt.tile(m);
-                        uint32_t x[8];
-                        ldx8(tl + 32 * t, x);
-                        const uint32_t xh = lds32(tl + TL::H + 4 * t);
-                        int lo = 0, hi = 0;
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = s + 2 * tt;  // activation block within the half
+                    const int u = 4 * i + t;   // its unit in the task tile
+                    uint32_t c[8];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
+                    for (int k = 0; k < 8; ++k)
+                        c[k] = ((lw[k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[k] >> (2 * t)) & 0x03030303u) << 4);
+                    const uint32_t scw = t < 2 ? scA : scB;
+                    const int sA = (int)(int8_t)((scw >> (16 * (t & 1))) & 255u);
+                    const int sB = (int)(int8_t)((scw >> (16 * (t & 1) + 8)) & 255u);
 #pragma unroll
-                        for (int k = 4; k < 8; ++k) hi = dp4a(c[k], x[k], hi);
-                        const int hlo = (int)(int16_t)(xh & 0xffffu), hhi = (int)(int16_t)(xh >> 16);
-                        const int dot = sA * (lo - 32 * hlo) + sB * (hi - 32 * hhi);
-                        const float xd = ldsf(tl + TL::D + 4 * t);
-                        sink.unit(m, t, dot, 0, d * xd * (float)dot);
+                    for (int m = 0; m < MT; ++m) {
+                        if (m < ntok) {
+                            const uint32_t tl = xt.tile(m);
+                            uint32_t x[8];
+                            ldx8(tl + 32 * u, x);
+                            const uint32_t xh = lds32(tl + TL::H + 4 * u);
+                            int lo = 0, hi = 0;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
+#pragma unroll
+                            for (int k = 4; k < 8; ++k) hi = dp4a(c[k], x[k], hi);
+                            const int hlo = (int)(int16_t)(xh & 0xffffu), hhi = (int)(int16_t)(xh >> 16);
+                            const int dot = sA * (lo - 32 * hlo) + sB * (hi - 32 * hhi);
+                            if constexpr (Sink::DOTS) {
+                                sink.unit(m, u, dot, 0);
+                            } else {
+                                A[m] = fmaf(ldsf(tl + TL::D + 4 * u), (float)dot, A[m]);
+                            }
+                        }
                     }
                 }
             }
+        }
+        if constexpr (!Sink::DOTS) {
+            const float d = half_bits_to_float(lds32(base + 208) >> (8 * a));
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(m, d * A[m]);
         }
     }
 };
@@ -332,35 +415,58 @@ __device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &h
     hi = prmt(A, B, 0x7531u);
 }
 
+// T superblocks per task (136 bytes each, 8-byte aligned).  Value path: per token,
+// sum_ib xd_ib * ((ls_ib - 32) * dot_ib), times d once per superblock.
+template <int T>
 struct FmtIQ4XS {
-    static constexpr int QK = 256, BS = 136, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 136;
+    static constexpr int QK = 256, BS = 136, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 136 * T;
+
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
-        using TL = Tile<8>;
+    __device__ __forceinline__ static void superblock(uint32_t addr, int u0, const XT &xt, int ntok, Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
         const uint2 hdr = lds64(addr);  // x: d | scales_h << 16, y: scales_l[0..3]
-        const float d = half_bits_to_float(hdr.x);
+        float A[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) A[m] = 0.0f;
 #pragma unroll
         for (int ib = 0; ib < 8; ++ib) {
             const uint2 qa = lds64(addr + 8 + 16 * ib), qb = lds64(addr + 16 + 16 * ib);
             const int ls = (int)(((hdr.y >> (4 * ib)) & 15u) | (((hdr.x >> (16 + 2 * ib)) & 3u) << 4));
-            const float fa = d * (float)(ls - 32);
             const uint32_t qw[4] = {qa.x, qa.y, qb.x, qb.y};
             uint32_t c[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cb_lookup8(qw[k], c[k], c[4 + k]);
+            const int u = u0 + ib;
 #pragma unroll
-            for (int m = 0; m < Sink::MT; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 if (m < ntok) {
                     const uint32_t t = xt.tile(m);
                     uint32_t x[8];
-                    ldx8(t + 32 * ib, x);
+                    ldx8(t + 32 * u, x);
                     int dot = 0;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) dot = dp4a(c[k], x[k], dot);
-                    sink.unit(m, ib, dot, 0, fa * ldsf(t + TL::D + 4 * ib) * (float)dot);
+                    if constexpr (Sink::DOTS) {
+                        sink.unit(m, u, dot, 0);
+                    } else {
+                        A[m] = fmaf(ldsf(t + TL::D + 4 * u), (float)((ls - 32) * dot), A[m]);
+                    }
                 }
             }
         }
+        if constexpr (!Sink::DOTS) {
+            const float d = half_bits_to_float(hdr.x);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(m, d * A[m]);
+        }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) superblock(addr + BS * t, 8 * t, xt, ntok, sink);
     }
 };
 
@@ -372,13 +478,13 @@ struct FmtSel<F_Q8_0, T> { using type = FmtLegacy<F_Q8_0, T>; };
 template <int T>
 struct FmtSel<F_Q4_0, T> { using type = FmtLegacy<F_Q4_0, T>; };
 template <int T>
-struct FmtSel<F_Q4_K, T> { using type = FmtQ4K; };
+struct FmtSel<F_Q4_K, T> { using type = FmtQ4K<T>; };
 template <int T>
-struct FmtSel<F_Q5_K, T> { using type = FmtQ5K; };
+struct FmtSel<F_Q5_K, T> { using type = FmtQ5K<T>; };
 template <int T>
-struct FmtSel<F_Q6_K, T> { using type = FmtQ6K; };
+struct FmtSel<F_Q6_K, T> { using type = FmtQ6K<T>; };
 template <int T>
-struct FmtSel<F_IQ4_XS, T> { using type = FmtIQ4XS; };
+struct FmtSel<F_IQ4_XS, T> { using type = FmtIQ4XS<T>; };
 template <int FMT, int T>
 using FT = typename FmtSel<FMT, T>::type;
 
@@ -422,6 +528,7 @@ __device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const floa
             reinterpret_cast<float *>(t + 32 * xgt)[u] = di;
             reinterpret_cast<int32_t *>(t + 36 * xgt)[u] = si;
             reinterpret_cast<uint32_t *>(t + 40 * xgt)[u] = ((uint32_t)h16 & 0xffffu) | ((uint32_t)(si - h16) << 16);
+            reinterpret_cast<float *>(t + 44 * xgt)[u] = di * (float)si;
         }
         if (mq) {
             mq[(long)r * K + 32L * b + lane] = (int8_t)qi;

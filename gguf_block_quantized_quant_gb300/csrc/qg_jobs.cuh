@@ -14,6 +14,9 @@
 // Engine interface: HAS_FINISH, HAS_PROLOGUE; fields depth, slot_bytes, x_bytes, j_bytes,
 // tpr_x, tps, ntok; cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store,
 // init, finish, prologue (run by warp 0 before any weight copy, e.g. the MoE top-k).
+// The engine may start before the previous kernel in the stream has finished (programmatic
+// dependent launch): seg_src may only read data no earlier kernel writes (the weights),
+// unless the job's prologue first waits for the previous kernel (griddep_wait).
 // Activation images (prep_tiles_warp) have one row of task tiles per token (or per MoE
 // slot), row pitch tpr * tile_stride(XGT).
 #pragma once
@@ -233,7 +236,7 @@ struct MoeGateUpJob : EngineFields {
 template <int FMT, int T>
 struct MoeDownJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = true, HAS_PROLOGUE = false;
+    static constexpr bool HAS_FINISH = true, HAS_PROLOGUE = true;
     const uint8_t *Wd_exps, *Wd_sh, *Wd_exps_end, *Wd_sh_end;
     int E, topk, H, M, m0;          // tokens [m0, m0 + M) of the batch
     uint32_t rb;
@@ -291,7 +294,9 @@ struct MoeDownJob : EngineFields {
             y[(long)(m0 + m) * H + n0 + r] = acc;
         }
     }
-    __device__ void prologue(int, int *) const {}
+    // The weight copies need the routed expert ids, written two kernels earlier: wait for
+    // the previous kernel (and so for everything before it) before any copy is issued.
+    __device__ void prologue(int, int *) const { griddep_wait(); }
 };
 
 }  // namespace qg

@@ -43,12 +43,15 @@ inline int log2i(int v) {
     return l;
 }
 
-// Task geometry of a row of K elements (must match the format traits in qg_formats.cuh).
+// Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
+//   Q4_0: 8, 4 or 1 blocks per task; Q8_0: 4 or 1; Q4_K, IQ4_XS: 2 or 1 superblocks (the
+//   largest that divides the row); Q5_K, Q6_K: one whole superblock (T = 2 halves).
 struct TaskGeo {
     bool ok = false;
     int T = 1, TPB = 1, BPT = 1, XGT = 8, nbr = 0, gpr = 0, tpr = 0, stride = 0, bs = 0;
     uint32_t rb = 0;
     uint32_t bytes_of(int ntask) const { return (uint32_t)(((ntask + TPB - 1) / TPB) * BPT * bs); }
+    int task_bytes() const { return BPT * bs / TPB; }
 };
 inline TaskGeo task_geo(int fmt, int K) {
     TaskGeo g;
@@ -58,23 +61,30 @@ inline TaskGeo task_geo(int fmt, int K) {
     g.nbr = K / f.qk;
     g.rb = (uint32_t)(g.nbr * f.bs);
     if (f.qk == 32) {
-        g.T = g.nbr % 4 == 0 ? 4 : 1;
+        g.T = (fmt == 2 && g.nbr % 8 == 0) ? 8 : g.nbr % 4 == 0 ? 4 : 1;
         g.BPT = g.T;
         g.XGT = g.T;
         g.TPB = 1;
         g.gpr = g.nbr / g.T;
-    } else {
-        g.T = 1;
+    } else if (fmt == 13 || fmt == 14) {
+        g.T = 2;
         g.BPT = 1;
-        g.TPB = (fmt == 13 || fmt == 14) ? 2 : 1;
-        g.XGT = 8 / g.TPB;
+        g.TPB = 1;
+        g.XGT = 8;
         g.gpr = g.nbr;
+    } else {
+        g.T = g.nbr % 2 == 0 ? 2 : 1;
+        g.BPT = g.T;
+        g.TPB = 1;
+        g.XGT = 8 * g.T;
+        g.gpr = g.nbr / g.T;
     }
     g.tpr = g.gpr * g.TPB;
     g.stride = tile_stride(g.XGT);
     g.ok = true;
     return g;
 }
+inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
 
 // Stage size and ring of one engine launch.
 struct Ring {
@@ -84,7 +94,7 @@ struct Ring {
 };
 // run: the fewest tasks in one run of adjacent rows that any CTA of the launch sees (0: the
 // whole CTA range is one run); a stage of t tasks then spans at most t / run + 2 runs.
-// ncw: consumer warps of the launch (ncw_for(MT)).
+// ncw: warps of the launch (geo_ncw).
 inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_bytes, int ncw) {
     Ring r;
     r.x_bytes = (uint32_t)align_up(x_bytes, 16);
@@ -140,7 +150,7 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     p.MT = pick_mt(M);
     p.tpr_x = (g.gpr + p.KS - 1) / p.KS * g.TPB;
     // split-K: every row is its own run; the shortest slice has floor(gpr / KS) groups
-    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, ncw_for(p.MT));
+    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, geo_ncw(g, p.MT));
     if (!p.ring.ok) return p;
     size_t o = 0;
     p.ximg_pitch = (size_t)g.tpr * g.stride;
@@ -176,7 +186,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     p.nchunk = (M + p.MC - 1) / p.MC;
     p.MT = pick_mt(p.MC);
     p.grid = std::min(2 * I, sms);
-    p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, ncw_for(p.MT));
+    p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, geo_ncw(g, p.MT));
     if (!p.ring.ok) return p;
     p.down = plan_gemv(fmt, H, I, M, sms);
     if (!p.down.ok) return p;
@@ -217,7 +227,7 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     const long gu_x = (long)M * p.gh.tpr * p.gh.stride;
     if (gu_x > (long)XCAP) return p;
     p.gu_grid = (int)std::min<long>(sms, gu_rows);
-    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, ncw_for(1));
+    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, geo_ncw(p.gh, 1));
     if (!p.gu_ring.ok) return p;
     // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
     const long tiles_tok = (long)p.S * p.gi.tpr * p.gi.stride;
@@ -229,7 +239,7 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     p.dn_nchunk = (M + p.dn_MC - 1) / p.dn_MC;
     // CTAs own floor or ceil of H / dn_grid rows: runs are at least the floor long
     p.dn_ring = plan_ring(p.gi, (long)(H / p.dn_grid) * p.gi.tpr, (uint32_t)(p.dn_MC * tiles_tok),
-                          (uint32_t)(p.dn_MC * part_tok), ncw_for(1));
+                          (uint32_t)(p.dn_MC * part_tok), geo_ncw(p.gi, 1));
     if (!p.dn_ring.ok) return p;
     // workspace
     const size_t Rw = (size_t)M * p.S;
