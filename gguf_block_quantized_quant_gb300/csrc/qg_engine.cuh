@@ -132,8 +132,9 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
     __syncthreads();
 
     // this CTA's tasks and this warp's range (whole blocks)
+    const typename Job::Ctx cx = job.ctx();
     int o0, o1, tpr, grp;
-    job.cta(o0, o1, tpr, grp);
+    job.cta(cx, o0, o1, tpr, grp);
     const int ntask = (o1 - o0) * tpr;
     const FastDiv tpr_div = FastDiv::make((uint32_t)tpr), grp_div = FastDiv::make((uint32_t)grp);
     const int units = ntask / F::TPB;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
         if (valid) {
             const int o = (int)tpr_div.div((uint32_t)ps), tt = ps - o * tpr;
             const uint8_t *lim;
-            const uint8_t *src = job.seg_src(o0 + o, tt, lim, scratch);
+            const uint8_t *src = job.seg_src(cx, o0 + o, tt, lim, scratch);
             s0 = (uintptr_t)src;
             a0 = s0 & ~(uintptr_t)15;
             e = s0 + task_off<F>(pe - ps);
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
             const int rows = ntask > 0 ? job.xrows() : 0;
             uint32_t tx = 0;
             for (int r = 0; r < rows; ++r) {
-                const uint32_t bytes = job.xrow_bytes(r);
-                if (bytes) bulk_g2s(xa + (uint32_t)r * tok_stride, job.xrow_src(r), bytes, xbar);
+                const uint32_t bytes = job.xrow_bytes(cx, r);
+                if (bytes) bulk_g2s(xa + (uint32_t)r * tok_stride, job.xrow_src(cx, r), bytes, xbar);
                 tx += bytes;
             }
             mbar_arrive_expect_tx(xbar, tx);
@@ -263,8 +264,9 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
                         piece = g - ga;
                         if (piece) fp = (g * grp - o0) * tpr;
                     }
-                    const uint32_t addr = lds32(hdr(slot, piece)) + task_off<F>(f - fp);
-                    const XT xt{xa + job.xrow(o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE), tok_stride};
+                    const SAddr addr = smem + (lds32(hdr(slot, piece)) - ring) + task_off<F>(f - fp);
+                    const XT xt{smem + (xa - ring) + job.xrow(cx, o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE),
+                                tok_stride};
                     F::run(addr, tt % F::TPB, xt, ntok, sink);
                 }
                 // segmented reduction: rows are contiguous runs of lanes
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
                     } else {
 #pragma unroll
                         for (int m = 0; m < MT; ++m)
-                            if (m < ntok) job.store(o0 + o, m, sink.acc[m], jarea);
+                            if (m < ntok) job.store(cx, o0 + o, m, sink.acc[m], jarea);
                     }
                 }
                 // the continuing row's head broadcasts its sums as the next carry
@@ -332,18 +334,18 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
                 const int r = __float_as_int(e[0]);
                 if (r < 0) continue;
                 if (r != cur) {
-                    if (cur >= 0 && lane < ntok) job.store(o0 + cur, lane, acc, jarea);
+                    if (cur >= 0 && lane < ntok) job.store(cx, o0 + cur, lane, acc, jarea);
                     cur = r;
                     acc = 0.0f;
                 }
                 if (lane < ntok) acc += e[1 + lane];
             }
         }
-        if (cur >= 0 && lane < ntok) job.store(o0 + cur, lane, acc, jarea);
+        if (cur >= 0 && lane < ntok) job.store(cx, o0 + cur, lane, acc, jarea);
     }
     if (Job::HAS_FINISH) {
         consumer_sync<NCONS>();
-        job.finish(jarea, tid, NCONS);
+        job.finish(cx, jarea, tid, NCONS);
     }
 }
 

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
             reinterpret_cast<float *>(tile + TL::Q)[u] = 0.0f;
         }
         DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K};
-        F::run(smem_addr(blk), tt % F::TPB, XT{smem_addr(tile), 0}, 1, sink);
+        F::run(blk, tt % F::TPB, XT{tile, 0}, 1, sink);
     }
 }
 

@@ -40,6 +40,15 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 }
 __device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
 
+// Shared-memory operands of the decoders are plain pointers derived from the kernel's
+// extern __shared__ array: the compiler emits shared loads with immediate offsets and
+// schedules them freely between the barrier waits (whose "memory" clobbers order them).
+using SAddr = const uint8_t *;
+__device__ __forceinline__ uint32_t lds32(SAddr p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ uint2 lds64(SAddr p) { return *reinterpret_cast<const uint2 *>(p); }
+__device__ __forceinline__ uint4 lds128(SAddr p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ float ldsf(SAddr p) { return *reinterpret_cast<const float *>(p); }
+
 // ---------------------------------------------------------------------------------- tiles
 // Activation tile of XGT units: codes[32*XGT] | d[XGT] fp32 | s[XGT] int32 |
 // h[XGT] (sum of codes 0..15 in the low 16 bits, 16..31 in the high 16 bits) |
@@ -54,7 +63,7 @@ struct Tile {
     static constexpr int D = 32 * XGT, S = D + 4 * XGT, H = S + 4 * XGT, Q = H + 4 * XGT, STRIDE = tile_stride(XGT);
 };
 
-__device__ __forceinline__ void ldx8(uint32_t a, uint32_t (&x)[8]) {
+__device__ __forceinline__ void ldx8(SAddr a, uint32_t (&x)[8]) {
     const uint4 p = lds128(a), q = lds128(a + 16);
     x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
     x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
@@ -62,9 +71,9 @@ __device__ __forceinline__ void ldx8(uint32_t a, uint32_t (&x)[8]) {
 
 // Activations of one task: tile address of token m is base + m * tok_stride.
 struct XT {
-    uint32_t base;
+    SAddr base;
     uint32_t tok_stride;
-    __device__ __forceinline__ uint32_t tile(int m) const { return base + (uint32_t)m * tok_stride; }
+    __device__ __forceinline__ SAddr tile(int m) const { return base + (uint32_t)m * tok_stride; }
 };
 
 // Byte offset OFF (even) into a run of words: realigned when OFF is 2 mod 4.
@@ -92,7 +101,7 @@ struct FmtLegacy {
 
     template <class Sink>
     __device__ __forceinline__ static void unit_from_words(const uint32_t (&c)[8], float d, int m, int u,
-                                                           uint32_t tile, Sink &sink) {
+                                                           SAddr tile, Sink &sink) {
         using TL = Tile<XGT>;
         uint32_t x[8];
         ldx8(tile + 32 * u, x);
@@ -120,11 +129,16 @@ struct FmtLegacy {
     }
 
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
         if constexpr (T >= 4) {
             constexpr int NW = 4 * BS / 4 + 2;
+            // eight Q4_0 blocks make 144-byte tasks: with 8-byte loads lanes l and l + 8
+            // would share banks, so lanes with bit 3 set take the two groups of four in the
+            // opposite order (a 72-byte shift that makes each half-warp conflict-free)
+            const int sw = T == 8 ? (int)((threadIdx.x >> 3) & 1) : 0;
 #pragma unroll
-            for (int g = 0; g < T / 4; ++g) {
+            for (int gi = 0; gi < T / 4; ++gi) {
+                const int g = gi ^ sw;
                 uint32_t w[NW];
 #pragma unroll
                 for (int i = 0; i < NW / 2; ++i) {
@@ -145,7 +159,8 @@ struct FmtLegacy {
                 }
             }
         } else {
-            const uint32_t a = addr & 3u, base = addr - a;  // a is 0 or 2
+            const uint32_t a = (uint32_t)((uintptr_t)addr & 3u);  // 0 or 2
+            const SAddr base = addr - a;
             constexpr int NW = BS / 4 + 2;
             uint32_t w[NW];
 #pragma unroll
@@ -173,7 +188,7 @@ struct FmtQ4K {
     static constexpr int QK = 256, BS = 144, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 144 * T;
 
     template <class Sink>
-    __device__ __forceinline__ static void superblock(uint32_t addr, int u0, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void superblock(SAddr addr, int u0, const XT &xt, int ntok, Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
         const uint4 h = lds128(addr);
@@ -195,7 +210,7 @@ struct FmtQ4K {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m < ntok) {
-                    const uint32_t t = xt.tile(m);
+                    const SAddr t = xt.tile(m);
                     uint32_t xa[8], xb[8];
                     ldx8(t + 32 * u, xa);
                     ldx8(t + 32 * u + 32, xb);
@@ -228,10 +243,18 @@ struct FmtQ4K {
         }
     }
 
+    // With two superblocks per task the tasks of consecutive lanes are 288 bytes (18 chunks
+    // of 16 bytes) apart, so lanes l and l + 4 would hit the same banks on every 16-byte
+    // load; lanes with bit 2 set take their superblocks in the opposite order, which
+    // shifts them by 9 chunks and makes each quarter-warp's loads conflict-free.
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
+        const int sw = T == 2 ? (int)((threadIdx.x >> 2) & 1) : 0;
 #pragma unroll
-        for (int t = 0; t < T; ++t) superblock(addr + BS * t, 8 * t, xt, ntok, sink);
+        for (int i = 0; i < T; ++i) {
+            const int t = i ^ sw;
+            superblock(addr + BS * t, 8 * t, xt, ntok, sink);
+        }
     }
 };
 
@@ -242,7 +265,7 @@ template <int T>
 struct FmtQ5K {
     static constexpr int QK = 256, BS = 176, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 88 * T;
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void run(SAddr addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
         const uint4 h = lds128(addr);
@@ -273,7 +296,7 @@ struct FmtQ5K {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     if (m < ntok) {
-                        const uint32_t t = xt.tile(m);
+                        const SAddr t = xt.tile(m);
                         uint32_t xa[8], xb[8];
                         ldx8(t + 32 * u, xa);
                         ldx8(t + 32 * u + 32, xb);
@@ -319,10 +342,11 @@ template <int T>
 struct FmtQ6K {
     static constexpr int QK = 256, BS = 210, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 105 * T;
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void run(SAddr addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
-        const uint32_t a = addr & 3u, base = addr - a;
+        const uint32_t a = (uint32_t)((uintptr_t)addr & 3u);
+        const SAddr base = addr - a;
         const uint32_t sel = a ? 0x5432u : 0x3210u;
         float A[MT];
 #pragma unroll
@@ -363,7 +387,7 @@ struct FmtQ6K {
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         if (m < ntok) {
-                            const uint32_t tl = xt.tile(m);
+                            const SAddr tl = xt.tile(m);
                             uint32_t x[8];
                             ldx8(tl + 32 * u, x);
                             const uint32_t xh = lds32(tl + TL::H + 4 * u);
@@ -422,7 +446,7 @@ struct FmtIQ4XS {
     static constexpr int QK = 256, BS = 136, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 136 * T;
 
     template <class Sink>
-    __device__ __forceinline__ static void superblock(uint32_t addr, int u0, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void superblock(SAddr addr, int u0, const XT &xt, int ntok, Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
         const uint2 hdr = lds64(addr);  // x: d | scales_h << 16, y: scales_l[0..3]
@@ -441,7 +465,7 @@ struct FmtIQ4XS {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m < ntok) {
-                    const uint32_t t = xt.tile(m);
+                    const SAddr t = xt.tile(m);
                     uint32_t x[8];
                     ldx8(t + 32 * u, x);
                     int dot = 0;
@@ -463,10 +487,17 @@ struct FmtIQ4XS {
         }
     }
 
+    // Tasks of two superblocks are 272 bytes apart: with 8-byte loads (half-warps) lanes l
+    // and l + 8 would share banks; lanes with bit 3 set take the superblocks in the
+    // opposite order (a 136-byte shift) so each half-warp's loads are conflict-free.
     template <class Sink>
-    __device__ __forceinline__ static void run(uint32_t addr, int, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
+        const int sw = T == 2 ? (int)((threadIdx.x >> 3) & 1) : 0;
 #pragma unroll
-        for (int t = 0; t < T; ++t) superblock(addr + BS * t, 8 * t, xt, ntok, sink);
+        for (int i = 0; i < T; ++i) {
+            const int t = i ^ sw;
+            superblock(addr + BS * t, 8 * t, xt, ntok, sink);
+        }
     }
 };
 

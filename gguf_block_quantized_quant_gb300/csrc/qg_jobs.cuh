@@ -12,8 +12,9 @@
 //                  expert: weight 1) -- the weighted aggregation of the expert outputs
 //
 // Engine interface: HAS_FINISH, HAS_PROLOGUE; fields depth, slot_bytes, x_bytes, j_bytes,
-// tpr_x, tps, ntok; cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store,
-// init, finish, prologue (run by warp 0 before any weight copy, e.g. the MoE top-k).
+// tpr_x, tps, ntok; Ctx ctx() (per-CTA constants, computed once and passed to the calls
+// below); cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store, init,
+// finish, prologue (run by warp 0 before any weight copy, e.g. the MoE top-k).
 // The engine may start before the previous kernel in the stream has finished (programmatic
 // dependent launch): seg_src may only read data no earlier kernel writes (the weights),
 // unless the job's prologue first waits for the previous kernel (griddep_wait).
@@ -44,34 +45,41 @@ struct GemvJob : EngineFields {
     float *out;  // y (KS == 1) or partials [KS][M][N]
     long slice_stride;
 
-    __device__ int ks() const { return blockIdx.x % KS; }
-    __device__ int t0() const { return (int)((long)ks() * gpr / KS) * F::TPB; }
-    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
-        const int g = blockIdx.x / KS;
-        o0 = (int)((long)g * N / groups);
-        o1 = (int)((long)(g + 1) * N / groups);
-        tpr = (int)((long)(ks() + 1) * gpr / KS) * F::TPB - t0();
+    // per-CTA constants: K-slice, its first task, its tasks per row, the output slice
+    struct Ctx {
+        int ks, t0, tpr, o0, o1;
+        float *out;
+    };
+    __device__ Ctx ctx() const {
+        Ctx c;
+        const int g = KS == 1 ? (int)blockIdx.x : (int)blockIdx.x / KS;
+        c.ks = KS == 1 ? 0 : (int)blockIdx.x - g * KS;
+        c.t0 = (int)((long)c.ks * gpr / KS) * F::TPB;
+        c.tpr = (int)((long)(c.ks + 1) * gpr / KS) * F::TPB - c.t0;
+        c.o0 = (int)((long)g * N / groups);
+        c.o1 = (int)((long)(g + 1) * N / groups);
+        c.out = out + (long)c.ks * slice_stride;
+        return c;
+    }
+    __device__ void cta(const Ctx &c, int &o0, int &o1, int &tpr, int &grp) const {
+        o0 = c.o0;
+        o1 = c.o1;
+        tpr = c.tpr;
         grp = KS == 1 ? 0 : 1;  // slices of consecutive rows are not adjacent
     }
-    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
+    __device__ const uint8_t *seg_src(const Ctx &c, int o, int tt, const uint8_t *&lim, const int *) const {
         lim = Wend;
-        return W + (size_t)o * rb + task_off<F>(t0() + tt);
+        return W + (size_t)o * rb + task_off<F>(c.t0 + tt);
     }
     __device__ int xrows() const { return ntok; }
-    __device__ const uint8_t *xrow_src(int r) const {
-        return ximg + (size_t)r * ximg_pitch + (size_t)t0() * tile_stride(F::XGT);
+    __device__ const uint8_t *xrow_src(const Ctx &c, int r) const {
+        return ximg + (size_t)r * ximg_pitch + (size_t)c.t0 * tile_stride(F::XGT);
     }
-    __device__ uint32_t xrow_bytes(int) const {
-        int o0, o1, tpr, grp;
-        cta(o0, o1, tpr, grp);
-        return (uint32_t)(tpr * tile_stride(F::XGT));
-    }
-    __device__ uint32_t xrow(int, const FastDiv &) const { return 0; }
-    __device__ void store(int o, int m, float v, float *) const {
-        out[(long)ks() * slice_stride + (long)m * N + o] = v;
-    }
+    __device__ uint32_t xrow_bytes(const Ctx &c, int) const { return (uint32_t)(c.tpr * tile_stride(F::XGT)); }
+    __device__ uint32_t xrow(const Ctx &, int, const FastDiv &) const { return 0; }
+    __device__ void store(const Ctx &c, int o, int m, float v, float *) const { c.out[(long)m * N + o] = v; }
     __device__ void init(float *, int) const {}
-    __device__ void finish(float *, int, int) const {}
+    __device__ void finish(const Ctx &, float *, int, int) const {}
     __device__ void prologue(int, int *) const {}
 };
 
@@ -87,29 +95,31 @@ struct FfnGateUpJob : EngineFields {
     uint32_t ximg_pitch;
     float *g_out, *u_out;  // row pitch I, whole batch
 
-    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
+    struct Ctx {};
+    __device__ Ctx ctx() const { return {}; }
+    __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
         o0 = (int)((long)blockIdx.x * 2 * I / gridDim.x);
         o1 = (int)((long)(blockIdx.x + 1) * 2 * I / gridDim.x);
         tpr = tpr_x;
         grp = I;
     }
-    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
+    __device__ const uint8_t *seg_src(const Ctx &, int o, int tt, const uint8_t *&lim, const int *) const {
         const bool up = o >= I;
         lim = up ? Wu_end : Wg_end;
         return (up ? Wu : Wg) + (size_t)(up ? o - I : o) * rb + task_off<F>(tt);
     }
     __device__ int xrows() const { return ntok; }
-    __device__ const uint8_t *xrow_src(int r) const { return ximg + (size_t)(m0 + r) * ximg_pitch; }
-    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
-    __device__ uint32_t xrow(int, const FastDiv &) const { return 0; }
-    __device__ void store(int o, int m, float v, float *) const {
+    __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + (size_t)(m0 + r) * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(const Ctx &, int, const FastDiv &) const { return 0; }
+    __device__ void store(const Ctx &, int o, int m, float v, float *) const {
         if (o < I)
             g_out[(long)(m0 + m) * I + o] = v;
         else
             u_out[(long)(m0 + m) * I + o - I] = v;
     }
     __device__ void init(float *, int) const {}
-    __device__ void finish(float *, int, int) const {}
+    __device__ void finish(const Ctx &, float *, int, int) const {}
     __device__ void prologue(int, int *) const {}
 };
 
@@ -138,14 +148,16 @@ struct MoeGateUpJob : EngineFields {
 
     __device__ int slots() const { return topk + 1; }
     // o = ((token * slots + slot) * 2 + up) * I + j; groups of I rows are one matrix
-    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
+    struct Ctx {};
+    __device__ Ctx ctx() const { return {}; }
+    __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
         const long P = (long)M * slots() * 2 * I;
         o0 = (int)(P * blockIdx.x / gridDim.x);
         o1 = (int)(P * (blockIdx.x + 1) / gridDim.x);
         tpr = tpr_x;
         grp = I;
     }
-    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *ids) const {
+    __device__ const uint8_t *seg_src(const Ctx &, int o, int tt, const uint8_t *&lim, const int *ids) const {
         const int q = o / I, j = o - q * I, up = q & 1, gs = q >> 1;
         const int m = gs / slots(), s = gs - m * slots();
         if (s < topk) {
@@ -157,17 +169,17 @@ struct MoeGateUpJob : EngineFields {
         return (up ? Wu_sh : Wg_sh) + (size_t)j * rb + task_off<F>(tt);
     }
     __device__ int xrows() const { return M; }
-    __device__ const uint8_t *xrow_src(int r) const { return ximg + (size_t)r * ximg_pitch; }
-    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
-    __device__ uint32_t xrow(int o, const FastDiv &divI) const {
+    __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + (size_t)r * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divI) const {
         return div_slots.div(divI.div((uint32_t)o) >> 1);  // token
     }
-    __device__ void store(int o, int, float v, float *) const {
+    __device__ void store(const Ctx &, int o, int, float v, float *) const {
         const int q = o / I, j = o - q * I;
         ((q & 1) ? u_out : g_out)[(long)(q >> 1) * I + j] = v;
     }
     __device__ void init(float *, int) const {}
-    __device__ void finish(float *, int, int) const {}
+    __device__ void finish(const Ctx &, float *, int, int) const {}
     // Router tail, warp 0, after the logits kernel has finished: softmax over E logits,
     // the topk largest (ties: lower id), weights renormalized over the picks.
     // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax
@@ -248,42 +260,45 @@ struct MoeDownJob : EngineFields {
     float *y;                       // [batch][H]
 
     __device__ int slots() const { return topk + 1; }
-    __device__ void nrange(int &n0, int &n1) const {
-        n0 = (int)((long)blockIdx.x * H / gridDim.x);
-        n1 = (int)((long)(blockIdx.x + 1) * H / gridDim.x);
+    // per-CTA constants: this CTA's hidden rows [n0, n0 + nloc) and the row decomposition
+    struct Ctx {
+        int n0, nloc;
+        FastDiv dnloc, dslots;
+    };
+    __device__ Ctx ctx() const {
+        Ctx c;
+        c.n0 = (int)((long)blockIdx.x * H / gridDim.x);
+        c.nloc = (int)((long)(blockIdx.x + 1) * H / gridDim.x) - c.n0;
+        c.dnloc = FastDiv::make((uint32_t)c.nloc);
+        c.dslots = FastDiv::make((uint32_t)slots());
+        return c;
     }
-    // CTA-local rows o = (token * slots + slot) * nloc + r, r < nloc = n1 - n0
-    __device__ void cta(int &o0, int &o1, int &tpr, int &grp) const {
-        int n0, n1;
-        nrange(n0, n1);
+    // CTA-local rows o = (token * slots + slot) * nloc + r, r < nloc
+    __device__ void cta(const Ctx &c, int &o0, int &o1, int &tpr, int &grp) const {
         o0 = 0;
-        o1 = M * slots() * (n1 - n0);
+        o1 = M * slots() * c.nloc;
         tpr = tpr_x;
-        grp = n1 - n0;
+        grp = c.nloc;
     }
-    __device__ const uint8_t *seg_src(int o, int tt, const uint8_t *&lim, const int *) const {
-        int n0, n1;
-        nrange(n0, n1);
-        const int nloc = n1 - n0, q = o / nloc, r = o - q * nloc;
-        const int m = q / slots(), s = q - m * slots();
+    __device__ const uint8_t *seg_src(const Ctx &c, int o, int tt, const uint8_t *&lim, const int *) const {
+        const int q = (int)c.dnloc.div((uint32_t)o), r = o - q * c.nloc;
+        const int m = (int)c.dslots.div((uint32_t)q), s = q - m * slots();
         if (s < topk) {
             const size_t e = (size_t)min(max(ids_ws[(m0 + m) * topk + s], 0), E - 1);
             lim = Wd_exps_end;
-            return Wd_exps + e * ebytes + (size_t)(n0 + r) * rb + task_off<F>(tt);
+            return Wd_exps + e * ebytes + (size_t)(c.n0 + r) * rb + task_off<F>(tt);
         }
         lim = Wd_sh_end;
-        return Wd_sh + (size_t)(n0 + r) * rb + task_off<F>(tt);
+        return Wd_sh + (size_t)(c.n0 + r) * rb + task_off<F>(tt);
     }
     __device__ int xrows() const { return M * slots(); }
-    __device__ const uint8_t *xrow_src(int r) const { return ximg + ((size_t)m0 * slots() + r) * ximg_pitch; }
-    __device__ uint32_t xrow_bytes(int) const { return ximg_pitch; }
-    __device__ uint32_t xrow(int o, const FastDiv &divn) const { return divn.div((uint32_t)o); }  // token*slots+slot
-    __device__ void store(int o, int, float v, float *part) const { part[o] = v; }
+    __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + ((size_t)m0 * slots() + r) * ximg_pitch; }
+    __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
+    __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divn) const { return divn.div((uint32_t)o); }  // token*slots+slot
+    __device__ void store(const Ctx &, int o, int, float v, float *part) const { part[o] = v; }
     __device__ void init(float *, int) const {}
-    __device__ void finish(float *part, int tid, int nthreads) const {
-        int n0, n1;
-        nrange(n0, n1);
-        const int nloc = n1 - n0;
+    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads) const {
+        const int nloc = c.nloc;
         for (int i = tid; i < M * nloc; i += nthreads) {
             const int m = i / nloc, r = i - m * nloc;
             float acc = 0.0f;
@@ -291,7 +306,7 @@ struct MoeDownJob : EngineFields {
                 const float ws = s < topk ? w_ws[(m0 + m) * topk + s] : 1.0f;  // shared expert: weight 1
                 acc = fmaf(ws, part[(m * slots() + s) * nloc + r], acc);
             }
-            y[(long)(m0 + m) * H + n0 + r] = acc;
+            y[(long)(m0 + m) * H + c.n0 + r] = acc;
         }
     }
     // The weight copies need the routed expert ids, written two kernels earlier: wait for
