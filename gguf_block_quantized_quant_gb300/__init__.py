@@ -140,8 +140,12 @@ def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
 
 
 def qg_gemv_static_ws(fmt: int, W, x, N: int, y=None, stream=None):
-    """qg_gemv on the library's fixed device scratch (no workspace argument, no allocation
-    inside the call when y is given).  Calls that may overlap in time share the scratch."""
+    """qg_gemv on the library's fixed device scratch, for callers that cannot allocate
+    device memory where they call (a plugin inside a framework whose allocator owns the
+    device memory, or a path that cannot afford cudaMalloc's synchronization).  Nothing is
+    allocated inside the call when y is given.  Every call on a device shares the scratch:
+    calls that may overlap on the GPU must be ordered on one stream.  The first call on a
+    device looks up the scratch address and should come before any stream capture."""
     M, K = x.shape
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
     _check(lib().qg_gemv_static_ws(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _stream(stream)), "qg_gemv_static_ws")

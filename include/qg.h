@@ -95,18 +95,26 @@ int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, 
 /* Bytes of the library's fixed device scratch array used by qg_gemv_static_ws. */
 #define QG_STATIC_WS_BYTES 2097152
 
-/* qg_gemv without a caller workspace: the scratch lives in one file-scope device array
- * of QG_STATIC_WS_BYTES bytes inside the library (per device), so the call allocates
- * nothing.  The pages have no counterpart to this entry point; it is a convenience for
- * callers that cannot hand over a workspace.
+/* qg_gemv without a caller workspace.  The pages have no counterpart to this entry point.
+ * It is for callers that cannot allocate device memory at the point where they call the
+ * GEMV: code running inside a host framework whose allocator owns all device memory (a
+ * plugin must not call cudaMalloc behind its back), code on a latency-critical path where
+ * cudaMalloc's implicit device synchronization is not acceptable, or a plain C host
+ * program that links only this library and has no device allocator of its own.  Such a
+ * caller passes only its inputs and outputs; the scratch lives in one file-scope device
+ * array of QG_STATIC_WS_BYTES bytes inside the library, held by every GPU that loads the
+ * library until the process exits.  The call itself allocates nothing.
  *   Arguments, layouts and results as qg_gemv (y is bit-identical to qg_gemv's).
  *   Limit: returns QG_EWORKSPACE, without launching, when qg_workspace_size(QG_OP_GEMV,
  *   fmt, M, N, K, ...) exceeds QG_STATIC_WS_BYTES (e.g. very long rows at M = 16).
+ *   Contents: the array keeps whatever the last call left in it; every call writes all
+ *   of the scratch it reads before reading it, so nothing needs to start at zero.
  *   Races: every call on a device shares the one array.  Calls whose executions may
- *   overlap (different streams without ordering, or several host threads) corrupt each
- *   other's activations; order them on one stream.
- *   The first call on each device looks up the array's address (cudaGetSymbolAddress);
- *   make that first call outside any stream capture. */
+ *   overlap on the GPU (different streams without ordering, or several host threads)
+ *   corrupt each other's activations; order them on one stream.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call before any
+ *   stream capture. */
 int qg_gemv_static_ws(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
                       void *stream);
 

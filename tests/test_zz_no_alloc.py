@@ -1,6 +1,9 @@
-"""qg_gemv_static_ws: the GEMV on the library's fixed device scratch array.  Its results
-must be bit-identical to qg_gemv with a caller workspace (same kernels, same plans); two
-calls in a row on one stream must not disturb each other; oversize problems are refused."""
+"""qg_gemv_static_ws: the GEMV for callers that cannot allocate device memory where they
+call it (for example a plugin whose host framework owns every device allocation), which
+runs on the library's fixed device scratch array instead of a caller workspace.  Its
+results must be bit-identical to qg_gemv with a workspace (same kernels, same plans); two
+calls in a row on one stream share the array and must not disturb each other; problems
+whose workspace would exceed the array are refused.  This file is collected last."""
 import numpy as np
 import pytest
 import torch
