@@ -10,11 +10,12 @@
 namespace qg {
 
 // ---------------------------------------------------------------------------------
-// Launch geometry of the streaming engine: engine_ncw() warps, one CTA per SM.  Tasks of at
-// most 160 bytes with up to 4 tokens per lane run 16 warps (4 per scheduler, to hide the
-// latency of the decode chains, with two ring slots of 32 tasks per warp); larger tasks
-// (whose ring slots are twice the size and whose lanes carry two independent superblock
-// chains) and 8 or 16 tokens per lane (more accumulator registers) run 8 warps.
+// Launch geometry of the streaming engine: engine_ncw() warps, one CTA per SM.  A lane
+// copies its task from the ring into registers before decoding it, so a ring slot is busy
+// only until then.  Tasks of at most 160 bytes with up to 4 tokens per lane run 16 warps
+// (4 per scheduler, to hide the latency of the decode chains); larger tasks hold up to 72
+// words per lane and run 8 warps with the room of two ring slots each, as do 8 or 16
+// tokens per lane (more accumulator registers).
 __host__ __device__ constexpr int engine_ncw(int task_bytes, int MT) {
     return (MT <= 4 && task_bytes <= 160) ? 16 : 8;
 }

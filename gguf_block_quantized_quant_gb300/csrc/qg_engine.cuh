@@ -242,78 +242,80 @@ __global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1
 
     for (int j = 0; j < nchunk; ++j) {
         const int slot = (j % D) * NCW + warp;
-        const int fa = a + j * job.tps;
+        const int fa = a + j * job.tps;  // a stage is at most 32 tasks: one per lane
         mbar_wait(full_bar(slot), (uint32_t)((j / D) & 1));
         const int fb = min(min(b, fa + job.tps), (int)lds32(hdr(slot, NPIECE_MAX)));
-        if (fa < fb) {
-            const int oa = (int)tpr_div.div((uint32_t)fa);
-            const int ga = grp ? (int)grp_div.div((uint32_t)(o0 + oa)) : 0;
-            for (int f0 = fa; f0 < fb; f0 += 32) {
-                const int f = f0 + lane;
-                const bool valid = f < fb;
-                int o = 0x7fffffff;
-                AccSink<MT> sink;
-#pragma unroll
-                for (int m = 0; m < MT; ++m) sink.acc[m] = 0.0f;
-                if (valid) {
-                    o = (int)tpr_div.div((uint32_t)f);
-                    const int tt = f - o * tpr;
-                    int piece = 0, fp = fa;
-                    if (grp) {
-                        const int g = (int)grp_div.div((uint32_t)(o0 + o));
-                        piece = g - ga;
-                        if (piece) fp = (g * grp - o0) * tpr;
-                    }
-                    const SAddr addr = smem + (lds32(hdr(slot, piece)) - ring) + task_off<F>(f - fp);
-                    const XT xt{smem + (xa - ring) + job.xrow(cx, o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE),
-                                tok_stride};
-                    F::run(addr, tt % F::TPB, xt, ntok, sink);
-                }
-                // segmented reduction: rows are contiguous runs of lanes
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int o2 = __shfl_down_sync(0xffffffffu, o, d);
-                    const bool take = lane + d < 32 && o2 == o;
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const float v = __shfl_down_sync(0xffffffffu, sink.acc[m], d);
-                        if (take) sink.acc[m] += v;
-                    }
-                }
-                const int oprev = __shfl_up_sync(0xffffffffu, o, 1);
-                const bool head = valid && (lane == 0 || oprev != o);
-                if (head && o == carry_o) {
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) sink.acc[m] += carry[m];
-                }
-                // the step's last row continues if it has tasks after this step
-                const int flast = min(fb, f0 + 32) - 1;
-                const int olast = __shfl_sync(0xffffffffu, o, flast - f0);
-                const bool cont = (olast + 1) * tpr > flast + 1;
-                if (head && !(o == olast && cont)) {
-                    if (a_mid && o == ra) {
-                        float *e = bsum + (warp * 2) * BND_FLOATS;  // shared with the previous warp
-                        e[0] = __int_as_float(o);
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) e[1 + m] = sink.acc[m];
-                    } else {
-#pragma unroll
-                        for (int m = 0; m < MT; ++m)
-                            if (m < ntok) job.store(cx, o0 + o, m, sink.acc[m], jarea);
-                    }
-                }
-                // the continuing row's head broadcasts its sums as the next carry
-                const int hl = __reduce_min_sync(0xffffffffu, (valid && o == olast) ? lane : 31);
-#pragma unroll
-                for (int m = 0; m < MT; ++m) carry[m] = __shfl_sync(0xffffffffu, sink.acc[m], hl);
-                carry_o = cont ? olast : -1;
+        const int f = fa + lane;
+        const bool valid = f < fb;
+        int o = 0x7fffffff, tt = 0;
+        uint32_t w[F::WW];
+        uint32_t aoff = 0;
+        SAddr xbase = smem;
+        if (valid) {
+            o = (int)tpr_div.div((uint32_t)f);
+            tt = f - o * tpr;
+            int piece = 0, fp = fa;
+            if (grp) {
+                const int ga = (int)grp_div.div((uint32_t)(o0 + (int)tpr_div.div((uint32_t)fa)));
+                const int g = (int)grp_div.div((uint32_t)(o0 + o));
+                piece = g - ga;
+                if (piece) fp = (g * grp - o0) * tpr;
             }
+            const SAddr addr = smem + (lds32(hdr(slot, piece)) - ring) + task_off<F>(f - fp);
+            F::load(addr, w);
+            aoff = (uint32_t)((uintptr_t)addr & 3u);
+            xbase = smem + (xa - ring) + job.xrow(cx, o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE);
         }
-        // refill the slot with stage j + D once every lane is done reading it
+        // the stage is in registers: refill the slot with stage j + D while decoding
         __syncwarp();
         if (j + D < nchunk) {
             fence_proxy_async_smem();
             issue(j + D);
+        }
+        if (fa < fb) {
+            const int f0 = fa;
+            AccSink<MT> sink;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) sink.acc[m] = 0.0f;
+            if (valid) F::compute(w, aoff, tt % F::TPB, XT{xbase, tok_stride}, ntok, sink);
+            // segmented reduction: rows are contiguous runs of lanes
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o2 = __shfl_down_sync(0xffffffffu, o, d);
+                const bool take = lane + d < 32 && o2 == o;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float v = __shfl_down_sync(0xffffffffu, sink.acc[m], d);
+                    if (take) sink.acc[m] += v;
+                }
+            }
+            const int oprev = __shfl_up_sync(0xffffffffu, o, 1);
+            const bool head = valid && (lane == 0 || oprev != o);
+            if (head && o == carry_o) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) sink.acc[m] += carry[m];
+            }
+            // the step's last row continues if it has tasks after this step
+            const int flast = min(fb, f0 + 32) - 1;
+            const int olast = __shfl_sync(0xffffffffu, o, flast - f0);
+            const bool cont = (olast + 1) * tpr > flast + 1;
+            if (head && !(o == olast && cont)) {
+                if (a_mid && o == ra) {
+                    float *e = bsum + (warp * 2) * BND_FLOATS;  // shared with the previous warp
+                    e[0] = __int_as_float(o);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) e[1 + m] = sink.acc[m];
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < ntok) job.store(cx, o0 + o, m, sink.acc[m], jarea);
+                }
+            }
+            // the continuing row's head broadcasts its sums as the next carry
+            const int hl = __reduce_min_sync(0xffffffffu, (valid && o == olast) ? lane : 31);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) carry[m] = __shfl_sync(0xffffffffu, sink.acc[m], hl);
+            carry_o = cont ? olast : -1;
         }
     }
     // a range that ended inside a row: its sum is shared with the next warp

@@ -91,13 +91,43 @@ __device__ __forceinline__ int byte_of(uint32_t w, int k) { return (int)((w >> (
 //   value sinks:  add(m, v) with the benchmark's fp32 contribution to y.
 
 // ================================================================================ Q8_0 / Q4_0
-// T blocks per task.  With T == 4 or 8 a task is T*34 (Q8_0) or T*18 (Q4_0) bytes; every
-// group of 4 blocks starts 8-byte aligned, so all field offsets are compile-time; with
-// T == 1 the block may start on any even byte and is realigned with run-time byte permutes.
+// T blocks per task.  With T == 4 or 8 a task is T*34 (Q8_0) or T*18 (Q4_0) bytes and starts
+// 8-byte (T == 8: 16-byte) aligned, so all field offsets are compile-time; with T == 1 the
+// block may start on any even byte and is realigned with run-time byte permutes.
+// Every decoder works in two phases: load() copies the task's bytes from shared memory
+// into registers (so that the engine can refill the ring slot at once), compute() decodes
+// them against the activation tiles.
 template <int FMT, int T>
 struct FmtLegacy {
     static constexpr int QK = 32, BS = (FMT == F_Q8_0 ? 34 : 18), XGT = T, TPB = 1, BPT = T;
     static constexpr int TASK_BYTES = T * BS;
+    // T >= 4: the task's words plus two (the last block's realignment reads past its end);
+    // T == 1: the words that cover the block from its 4-byte-aligned start
+    static constexpr int WW = T >= 4 ? TASK_BYTES / 4 + 2 : BS / 4 + 2;
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        if constexpr (T == 8) {
+#pragma unroll
+            for (int i = 0; i < TASK_BYTES / 16; ++i) {
+                const uint4 v = lds128(addr + 16 * i);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+            const uint2 v = lds64(addr + TASK_BYTES);
+            w[WW - 2] = v.x;
+            w[WW - 1] = v.y;
+        } else if constexpr (T == 4) {
+#pragma unroll
+            for (int i = 0; i < WW / 2; ++i) {
+                const uint2 v = lds64(addr + 8 * i);
+                w[2 * i] = v.x;
+                w[2 * i + 1] = v.y;
+            }
+        } else {
+            const SAddr base = addr - ((uintptr_t)addr & 3u);
+#pragma unroll
+            for (int i = 0; i < WW; ++i) w[i] = lds32(base + 4 * i);
+        }
+    }
 
     template <class Sink>
     __device__ __forceinline__ static void unit_from_words(const uint32_t (&c)[8], float d, int m, int u,
@@ -129,42 +159,21 @@ struct FmtLegacy {
     }
 
     template <class Sink>
-    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t a, int, const XT &xt,
+                                                   int ntok, Sink &sink) {
         if constexpr (T >= 4) {
-            constexpr int NW = 4 * BS / 4 + 2;
-            // eight Q4_0 blocks make 144-byte tasks: with 8-byte loads lanes l and l + 8
-            // would share banks, so lanes with bit 3 set take the two groups of four in the
-            // opposite order (a 72-byte shift that makes each half-warp conflict-free)
-            const int sw = T == 8 ? (int)((threadIdx.x >> 3) & 1) : 0;
 #pragma unroll
-            for (int gi = 0; gi < T / 4; ++gi) {
-                const int g = gi ^ sw;
-                uint32_t w[NW];
+            for (int b = 0; b < T; ++b) {
+                const int off = BS * b;
+                const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                uint32_t c[8];
 #pragma unroll
-                for (int i = 0; i < NW / 2; ++i) {
-                    const uint2 v = lds64(addr + 4 * BS * g + 8 * i);
-                    w[2 * i] = v.x;
-                    w[2 * i + 1] = v.y;
-                }
+                for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int off = BS * b;
-                    const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
-                    uint32_t c[8];
-#pragma unroll
-                    for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
-#pragma unroll
-                    for (int m = 0; m < Sink::MT; ++m)
-                        if (m < ntok) unit_from_words(c, d, m, 4 * g + b, xt.tile(m), sink);
-                }
+                for (int m = 0; m < Sink::MT; ++m)
+                    if (m < ntok) unit_from_words(c, d, m, b, xt.tile(m), sink);
             }
         } else {
-            const uint32_t a = (uint32_t)((uintptr_t)addr & 3u);  // 0 or 2
-            const SAddr base = addr - a;
-            constexpr int NW = BS / 4 + 2;
-            uint32_t w[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i) w[i] = lds32(base + 4 * i);
             const uint32_t sel = a ? 0x7654u : 0x5432u;  // 4 bytes starting 2 past the block start
             const float d = half_bits_to_float(a ? (w[0] >> 16) : w[0]);
             uint32_t c[8];
@@ -175,33 +184,60 @@ struct FmtLegacy {
                 if (m < ntok) unit_from_words(c, d, m, 0, xt.tile(m), sink);
         }
     }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, (uint32_t)((uintptr_t)addr & 3u), hf, xt, ntok, sink);
+    }
 };
 
 // ================================================================================ Q4_K
-// T superblocks per task.  The 8 six-bit scales and mins are unpacked four at a time into
-// bytes; sub-block 2p uses the low nibbles of qs[32p..32p+31], sub-block 2p+1 the high
-// nibbles, which are multiplied in place (16 * nibble) by an unsigned dp4a.  Value path:
-// per token, A = sum_j xd_j * (S_j * dot_j) and B = sum_j (xd_j * s_j) * M_j are
+// T superblocks per task (16-byte aligned).  The 8 six-bit scales and mins are unpacked four
+// at a time into bytes; sub-block 2p uses the low nibbles of qs[32p..32p+31], sub-block 2p+1
+// the high nibbles, which are multiplied in place (16 * nibble) by an unsigned dp4a.  Value
+// path: per token, A = sum_j xd_j * (S_j * dot_j) and B = sum_j (xd_j * s_j) * M_j are
 // accumulated, and the superblock's d and dmin are applied once: y += d * A - dmin * B.
 template <int T>
 struct FmtQ4K {
     static constexpr int QK = 256, BS = 144, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 144 * T;
+    static constexpr int WW = 36 * T;
+
+    // With two superblocks per task the tasks of consecutive lanes are 288 bytes (18 chunks
+    // of 16 bytes) apart, so lanes l and l + 4 would hit the same banks on every 16-byte
+    // load; lanes with bit 2 set load their second superblock first (a 9-chunk shift), so
+    // w[0..35] holds superblock swap() and w[36..71] the other one.
+    __device__ __forceinline__ static int swap() { return T == 2 ? (int)((threadIdx.x >> 2) & 1) : 0; }
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        const int sw = swap();
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+            const SAddr sb = addr + BS * (i ^ sw);
+#pragma unroll
+            for (int c = 0; c < 9; ++c) {
+                const uint4 v = lds128(sb + 16 * c);
+                w[36 * i + 4 * c] = v.x; w[36 * i + 4 * c + 1] = v.y;
+                w[36 * i + 4 * c + 2] = v.z; w[36 * i + 4 * c + 3] = v.w;
+            }
+        }
+    }
 
     template <class Sink>
-    __device__ __forceinline__ static void superblock(SAddr addr, int u0, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void superblock(const uint32_t *w, int u0, const XT &xt, int ntok,
+                                                      Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
-        const uint4 h = lds128(addr);
-        const uint32_t S03 = h.y & 0x3f3f3f3fu, M03 = h.z & 0x3f3f3f3fu;
-        const uint32_t S47 = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
-        const uint32_t M47 = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+        const uint32_t S03 = w[1] & 0x3f3f3f3fu, M03 = w[2] & 0x3f3f3f3fu;
+        const uint32_t S47 = (w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u);
+        const uint32_t M47 = ((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u);
         float A[MT], B[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            uint32_t q[8];
-            ldx8(addr + 16 + 32 * p, q);
+            const uint32_t *q = w + 4 + 8 * p;
             const uint32_t Sw = p < 2 ? S03 : S47, Mw = p < 2 ? M03 : M47;
             const int k0 = 2 * (p & 1);
             const int sc0 = byte_of(Sw, k0), sc1 = byte_of(Sw, k0 + 1);
@@ -236,55 +272,63 @@ struct FmtQ4K {
             }
         }
         if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+            const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
         }
     }
 
-    // With two superblocks per task the tasks of consecutive lanes are 288 bytes (18 chunks
-    // of 16 bytes) apart, so lanes l and l + 4 would hit the same banks on every 16-byte
-    // load; lanes with bit 2 set take their superblocks in the opposite order, which
-    // shifts them by 9 chunks and makes each quarter-warp's loads conflict-free.
     template <class Sink>
-    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
-        const int sw = T == 2 ? (int)((threadIdx.x >> 2) & 1) : 0;
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
+        const int sw = swap();
 #pragma unroll
-        for (int i = 0; i < T; ++i) {
-            const int t = i ^ sw;
-            superblock(addr + BS * t, 8 * t, xt, ntok, sink);
-        }
+        for (int i = 0; i < T; ++i) superblock(w + 36 * i, 8 * (i ^ sw), xt, ntok, sink);
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, 0, hf, xt, ntok, sink);
     }
 };
 
 // ================================================================================ Q5_K
-// T == 2: a whole superblock per task; T == 1: half a superblock (sub-blocks 4*hf ..
-// 4*hf+3).  The fifth bit of sub-block j is bit j of each qh byte.  Combine as Q4_K.
+// One whole superblock per task (16-byte aligned).  The fifth bit of sub-block j is bit j
+// of each qh byte.  Combine as Q4_K.
 template <int T>
 struct FmtQ5K {
-    static constexpr int QK = 256, BS = 176, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 88 * T;
+    static_assert(T == 2, "Q5_K tasks are whole superblocks");
+    static constexpr int QK = 256, BS = 176, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 176;
+    static constexpr int WW = 44;
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+#pragma unroll
+        for (int c = 0; c < 11; ++c) {
+            const uint4 v = lds128(addr + 16 * c);
+            w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+    }
+
     template <class Sink>
-    __device__ __forceinline__ static void run(SAddr addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
-        const uint4 h = lds128(addr);
-        uint32_t qh[8];
-        ldx8(addr + 16, qh);
+        const uint32_t *qh = w + 4;
         float A[MT], B[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < T; ++i) {
-            const int hf = T == 2 ? i : hf_arg;
-            const uint32_t Sw = hf ? ((h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u)) : (h.y & 0x3f3f3f3fu);
-            const uint32_t Mw = hf ? (((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u)) : (h.z & 0x3f3f3f3fu);
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t Sw = hf ? ((w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u)) : (w[1] & 0x3f3f3f3fu);
+            const uint32_t Mw = hf ? (((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u)) : (w[2] & 0x3f3f3f3fu);
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
                 const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
-                const int u = 4 * i + 2 * pp;    // their units in the task tile
-                uint32_t q[8];
-                ldx8(addr + 48 + 32 * (2 * hf + pp), q);
+                const uint32_t *q = w + 12 + 8 * (2 * hf + pp);
                 uint32_t c0[8], c1[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -298,8 +342,8 @@ struct FmtQ5K {
                     if (m < ntok) {
                         const SAddr t = xt.tile(m);
                         uint32_t xa[8], xb[8];
-                        ldx8(t + 32 * u, xa);
-                        ldx8(t + 32 * u + 32, xb);
+                        ldx8(t + 32 * j0, xa);
+                        ldx8(t + 32 * j0 + 32, xb);
                         int da = 0, db = 0;
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
@@ -307,11 +351,11 @@ struct FmtQ5K {
                             db = dp4a(c1[k], xb[k], db);
                         }
                         if constexpr (Sink::DOTS) {
-                            const uint2 xs = lds64(t + TL::S + 4 * u);
-                            sink.unit(m, u, da, (int)xs.x);
-                            sink.unit(m, u + 1, db, (int)xs.y);
+                            const uint2 xs = lds64(t + TL::S + 4 * j0);
+                            sink.unit(m, j0, da, (int)xs.x);
+                            sink.unit(m, j0 + 1, db, (int)xs.y);
                         } else {
-                            const uint2 xd = lds64(t + TL::D + 4 * u), xq = lds64(t + TL::Q + 4 * u);
+                            const uint2 xd = lds64(t + TL::D + 4 * j0), xq = lds64(t + TL::Q + 4 * j0);
                             A[m] = fmaf(__uint_as_float(xd.x), (float)(sc0 * da), A[m]);
                             A[m] = fmaf(__uint_as_float(xd.y), (float)(sc1 * db), A[m]);
                             B[m] = fmaf(__uint_as_float(xq.x), mn0, B[m]);
@@ -322,61 +366,66 @@ struct FmtQ5K {
             }
         }
         if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+            const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
         }
     }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, 0, hf, xt, ntok, sink);
+    }
 };
 
 // ================================================================================ Q6_K
-// T == 2: a whole superblock per task; T == 1: half a superblock (elements 128*hf ..
-// +127).  Within a half, activation block t = 0..3: the low four bits of element 32t + l
-// come from byte l + 32*(t&1) of the half's 64 ql bytes (low nibble for t < 2), the top two
-// from bits 2t, 2t+1 of qh byte l.  Codes are used unsigned (0..63) and the -32 offset is
-// applied through the activation half sums.  Superblocks may start on any even byte: words
-// are realigned with run-time byte permutes.  Value path: sum_t xd_t * dot_t per token,
-// times d once.
+// One whole superblock per task.  Within half hf, activation block t = 0..3: the low four
+// bits of element 32t + l come from byte l + 32*(t&1) of the half's 64 ql bytes (low nibble
+// for t < 2), the top two from bits 2t, 2t+1 of qh byte l.  Codes are used unsigned (0..63)
+// and the -32 offset is applied through the activation half sums.  Superblocks start on any
+// even byte: the words from the 4-byte-aligned start are loaded and realigned with byte
+// permutes.  Value path: sum_t xd_t * dot_t per token, times d once.
 template <int T>
 struct FmtQ6K {
-    static constexpr int QK = 256, BS = 210, XGT = 4 * T, TPB = 2 / T, BPT = 1, TASK_BYTES = 105 * T;
+    static_assert(T == 2, "Q6_K tasks are whole superblocks");
+    static constexpr int QK = 256, BS = 210, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 210;
+    static constexpr int WW = 54;  // 216 bytes from the aligned start cover the block
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        const SAddr base = addr - ((uintptr_t)addr & 3u);
+#pragma unroll
+        for (int i = 0; i < WW; ++i) w[i] = lds32(base + 4 * i);
+    }
+
     template <class Sink>
-    __device__ __forceinline__ static void run(SAddr addr, int hf_arg, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t a, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
-        const uint32_t a = (uint32_t)((uintptr_t)addr & 3u);
-        const SAddr base = addr - a;
         const uint32_t sel = a ? 0x5432u : 0x3210u;
         float A[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) A[m] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < T; ++i) {
-            const int hf = T == 2 ? i : hf_arg;
-            uint32_t qh[9];
-#pragma unroll
-            for (int k = 0; k < 9; ++k) qh[k] = lds32(base + 128 + 32 * hf + 4 * k);
+        for (int hf = 0; hf < 2; ++hf) {
             uint32_t hw[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) hw[k] = prmt(qh[k], qh[k + 1], sel);
-            const uint32_t so = a + 192 + 8 * hf;  // 8 sub-scales of this half (even offset)
-            const uint32_t s0w = lds32(base + (so & ~3u)), s1w = lds32(base + (so & ~3u) + 4),
-                           s2w = lds32(base + (so & ~3u) + 8);
-            const uint32_t scA = prmt(s0w, s1w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+0..3]
-            const uint32_t scB = prmt(s1w, s2w, (so & 2) ? 0x5432u : 0x3210u);  // sc[8hf+4..7]
+            for (int k = 0; k < 8; ++k) hw[k] = prmt(w[32 + 8 * hf + k], w[33 + 8 * hf + k], sel);
+            // sub-scales 8hf..8hf+7 start at byte 192 + 8hf of the block
+            const uint32_t scA = prmt(w[48 + 2 * hf], w[49 + 2 * hf], sel);  // sc[8hf+0..3]
+            const uint32_t scB = prmt(w[49 + 2 * hf], w[50 + 2 * hf], sel);  // sc[8hf+4..7]
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-                uint32_t ql[9];
-#pragma unroll
-                for (int k = 0; k < 9; ++k) ql[k] = lds32(base + 64 * hf + 32 * s + 4 * k);
                 uint32_t lw[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) lw[k] = prmt(ql[k], ql[k + 1], sel);
+                for (int k = 0; k < 8; ++k) lw[k] = prmt(w[16 * hf + 8 * s + k], w[16 * hf + 8 * s + k + 1], sel);
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const int t = s + 2 * tt;  // activation block within the half
-                    const int u = 4 * i + t;   // its unit in the task tile
+                    const int u = 4 * hf + t;  // its unit in the task tile
                     uint32_t c[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
@@ -409,11 +458,18 @@ struct FmtQ6K {
             }
         }
         if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(lds32(base + 208) >> (8 * a));
+            const float d = half_bits_to_float(w[52] >> (8 * a));
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < ntok) sink.add(m, d * A[m]);
         }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, (uint32_t)((uintptr_t)addr & 3u), hf, xt, ntok, sink);
     }
 };
 
@@ -439,28 +495,46 @@ __device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &h
     hi = prmt(A, B, 0x7531u);
 }
 
-// T superblocks per task (136 bytes each, 8-byte aligned).  Value path: per token,
-// sum_ib xd_ib * ((ls_ib - 32) * dot_ib), times d once per superblock.
+// T superblocks per task (136 bytes each; a two-superblock task is 16-byte aligned, a
+// single one 8-byte aligned).  Value path: per token, sum_ib xd_ib * ((ls_ib - 32) *
+// dot_ib), times d once per superblock.
 template <int T>
 struct FmtIQ4XS {
     static constexpr int QK = 256, BS = 136, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 136 * T;
+    static constexpr int WW = 34 * T;
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        if constexpr (T == 2) {
+#pragma unroll
+            for (int c = 0; c < WW / 4; ++c) {
+                const uint4 v = lds128(addr + 16 * c);
+                w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < WW / 2; ++c) {
+                const uint2 v = lds64(addr + 8 * c);
+                w[2 * c] = v.x;
+                w[2 * c + 1] = v.y;
+            }
+        }
+    }
 
     template <class Sink>
-    __device__ __forceinline__ static void superblock(SAddr addr, int u0, const XT &xt, int ntok, Sink &sink) {
+    __device__ __forceinline__ static void superblock(const uint32_t *w, int u0, const XT &xt, int ntok,
+                                                      Sink &sink) {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
-        const uint2 hdr = lds64(addr);  // x: d | scales_h << 16, y: scales_l[0..3]
+        const uint32_t h0 = w[0], h1 = w[1];  // h0: d | scales_h << 16, h1: scales_l[0..3]
         float A[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) A[m] = 0.0f;
 #pragma unroll
         for (int ib = 0; ib < 8; ++ib) {
-            const uint2 qa = lds64(addr + 8 + 16 * ib), qb = lds64(addr + 16 + 16 * ib);
-            const int ls = (int)(((hdr.y >> (4 * ib)) & 15u) | (((hdr.x >> (16 + 2 * ib)) & 3u) << 4));
-            const uint32_t qw[4] = {qa.x, qa.y, qb.x, qb.y};
+            const int ls = (int)(((h1 >> (4 * ib)) & 15u) | (((h0 >> (16 + 2 * ib)) & 3u) << 4));
             uint32_t c[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cb_lookup8(qw[k], c[k], c[4 + k]);
+            for (int k = 0; k < 4; ++k) cb_lookup8(w[2 + 4 * ib + k], c[k], c[4 + k]);
             const int u = u0 + ib;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
@@ -480,24 +554,25 @@ struct FmtIQ4XS {
             }
         }
         if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(hdr.x);
+            const float d = half_bits_to_float(h0);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < ntok) sink.add(m, d * A[m]);
         }
     }
 
-    // Tasks of two superblocks are 272 bytes apart: with 8-byte loads (half-warps) lanes l
-    // and l + 8 would share banks; lanes with bit 3 set take the superblocks in the
-    // opposite order (a 136-byte shift) so each half-warp's loads are conflict-free.
     template <class Sink>
-    __device__ __forceinline__ static void run(SAddr addr, int, const XT &xt, int ntok, Sink &sink) {
-        const int sw = T == 2 ? (int)((threadIdx.x >> 3) & 1) : 0;
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
 #pragma unroll
-        for (int i = 0; i < T; ++i) {
-            const int t = i ^ sw;
-            superblock(addr + BS * t, 8 * t, xt, ntok, sink);
-        }
+        for (int t = 0; t < T; ++t) superblock(w + 34 * t, 8 * t, xt, ntok, sink);
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, 0, hf, xt, ntok, sink);
     }
 };
 

@@ -99,21 +99,20 @@ inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_b
     Ring r;
     r.x_bytes = (uint32_t)align_up(x_bytes, 16);
     r.j_bytes = (uint32_t)align_up(j_bytes, 16);
-    const double tb = (double)g.BPT * g.bs / g.TPB;  // bytes per task
     const long avail = (long)SMEM_MAX - (long)engine_fixed_smem(ncw * DMAX, ncw) - (long)r.x_bytes - (long)r.j_bytes;
-    int tps = tb * 32 < 3000 ? 64 : 32;
-    for (; tps >= 2 * g.TPB; tps /= 2) {
+    // a stage is one task per lane (fewer only when not even one slot per warp would fit)
+    for (int tps = 32; tps >= 2; tps /= 2) {
         int t = tps;
         int pieces = 1;
         if (run > 0) {
             t = (int)std::min<long>(t, (long)(NPIECE_MAX - 2) * run);
-            t = std::max(2 * g.TPB, t / (2 * g.TPB) * (2 * g.TPB));
+            t = std::max(2, t / 2 * 2);
             pieces = (int)std::min<long>(NPIECE_MAX, ((long)t + run - 1) / run + 1);
             if ((long)t > (long)(NPIECE_MAX - 1) * run) return r;  // runs too short for the piece table
         }
         const uint32_t slot = (uint32_t)align_up(g.bytes_of(t) + 32u * pieces, 16);
         const long d = avail / ((long)ncw * (slot + STAGE_SLACK));
-        if (d >= 2 || tps <= 2 * g.TPB) {
+        if (d >= 1) {
             r.tps = t;
             r.slot_bytes = slot;
             r.depth = (int)std::min<long>(DMAX, d);
