@@ -29,7 +29,7 @@ int or_get_threads(void) {
 
 int or_block_elems(int fmt) {
     switch (fmt) {
-    case OR_Q4_0: case OR_Q8_0: return 32;
+    case OR_Q4_0: case OR_Q4_1: case OR_Q5_0: case OR_Q5_1: case OR_Q8_0: case OR_IQ4_NL: return 32;
     case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: case OR_IQ4_XS: return 256;
     default: return 0;
     }
@@ -38,6 +38,10 @@ int or_block_elems(int fmt) {
 int or_block_bytes(int fmt) {
     switch (fmt) {
     case OR_Q4_0: return 18;    /* fp16 d + 16 bytes of nibbles              */
+    case OR_Q4_1: return 20;    /* fp16 d, fp16 m + 16 bytes of nibbles      */
+    case OR_Q5_0: return 22;    /* fp16 d, 32 fifth bits, 16 B of nibbles     */
+    case OR_Q5_1: return 24;    /* fp16 d, fp16 m, 32 fifth bits, nibbles     */
+    case OR_IQ4_NL: return 18;  /* fp16 d + 16 bytes of codebook indices      */
     case OR_Q8_0: return 34;    /* fp16 d + 32 int8                          */
     case OR_Q4_K: return 144;   /* d, dmin, 12 B scales/mins, 128 B nibbles   */
     case OR_Q5_K: return 176;   /* Q4_K fields + 32 B of fifth bits           */
@@ -98,6 +102,34 @@ void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double 
             a = rd_half(blk);
             int nib = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);
             code = nib - 8;
+            break;
+        }
+        case OR_Q4_1: {
+            /* fp16 d, fp16 m, nibbles as Q4_0; w = d * nibble + m */
+            a = rd_half(blk);
+            b = -rd_half(blk + 2);
+            code = e < 16 ? (blk[4 + e] & 15) : (blk[4 + e - 16] >> 4);
+            break;
+        }
+        case OR_Q5_0:
+        case OR_Q5_1: {
+            /* fp16 d, [fp16 m,] 32-bit little-endian qh (bit e = fifth bit of element e),
+             * nibbles as Q4_0; Q5_0: w = d * (code - 16), Q5_1: w = d * code + m */
+            const int one = fmt == OR_Q5_1;
+            a = rd_half(blk);
+            const uint8_t *qh = blk + (one ? 4 : 2), *qs = blk + (one ? 8 : 6);
+            int nib = e < 16 ? (qs[e] & 15) : (qs[e - 16] >> 4);
+            int hb = (qh[e / 8] >> (e % 8)) & 1;
+            code = nib | (hb << 4);
+            if (one) b = -rd_half(blk + 2);
+            else code -= 16;
+            break;
+        }
+        case OR_IQ4_NL: {
+            /* fp16 d, 16 bytes of 4-bit codebook indices laid out as Q4_0 nibbles */
+            a = rd_half(blk);
+            int idx = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);
+            code = kIQ4NL[idx];
             break;
         }
         case OR_Q4_K:
@@ -193,7 +225,9 @@ void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_
     }
 }
 
-static int has_min_term(int fmt) { return fmt == OR_Q4_K || fmt == OR_Q5_K; }
+static int has_min_term(int fmt) {
+    return fmt == OR_Q4_K || fmt == OR_Q5_K || fmt == OR_Q4_1 || fmt == OR_Q5_1;
+}
 
 void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *xs,
                    int N, int K, int M, int32_t *dots, int32_t *aux) {

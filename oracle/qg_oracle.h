@@ -43,7 +43,10 @@ extern "C" {
 #endif
 
 /* GGUF type ids for the six block formats. */
-enum { OR_Q4_0 = 2, OR_Q8_0 = 8, OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_IQ4_XS = 23 };
+enum {
+    OR_Q4_0 = 2, OR_Q4_1 = 3, OR_Q5_0 = 6, OR_Q5_1 = 7, OR_Q8_0 = 8,
+    OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_IQ4_NL = 20, OR_IQ4_XS = 23
+};
 
 /* Elements per block (32 or 256) and bytes per block; 0 for an unknown format. */
 int or_block_elems(int fmt);
@@ -53,8 +56,9 @@ int or_block_bytes(int fmt);
 double or_half_to_double(uint16_t h);
 
 /* Decode one block.  w[QK]: the dequantized weights (fp64).  c[QK]: the integer
- * codes of the per-32 dot-product contract (Q8_0: q; Q4_0: nibble-8;
- * Q4_K/Q5_K: unsigned code; Q6_K: sc[e/16]*(code-32); IQ4_XS: codebook value).
+ * codes of the per-32 dot-product contract (Q8_0: q; Q4_0: nibble-8; Q4_1: nibble;
+ * Q5_0: 5-bit code - 16; Q5_1: 5-bit code; Q4_K/Q5_K: unsigned code;
+ * Q6_K: sc[e/16]*(code-32); IQ4_XS, IQ4_NL: codebook value).
  * A[QK/32], B[QK/32]: per 32-element unit, the factors with
  *   w_e = A_u * c_e - B_u        (Q6_K: w_e = A_u * c_e, the sub-scale is in c_e)
  * Any output pointer may be NULL. */

@@ -11,6 +11,10 @@ Field offsets follow the public GGUF block definitions:
 
   Q8_0   34 B: fp16 d @0, int8 q[32] @2            d ~ U[1e-3,2e-3], q ~ U{-127..127}
   Q4_0   18 B: fp16 d @0, nibbles @2                d ~ U[1e-3,2e-3], nibble bytes uniform
+  Q4_1   20 B: fp16 d @0, fp16 m @2, nibbles @4     d as Q4_0, m ~ U[-1e-3,1e-3]
+  Q5_0   22 B: fp16 d @0, qh @2, nibbles @6         d as Q4_0, qh and nibble bytes uniform
+  Q5_1   24 B: fp16 d @0, fp16 m @2, qh @4, nib @8  d, m as Q4_1
+  IQ4_NL 18 B: fp16 d @0, indices @2                d as Q4_0, index bytes uniform
   Q4_K  144 B: fp16 d @0, fp16 dmin @2, rest bytes  d ~ U[1e-3,2e-3], dmin ~ U[0,1e-3]
   Q5_K  176 B: as Q4_K (the qh bytes are uniform too)
   Q6_K  210 B: ql/qh @0..191 uniform, int8 sc[16] @192 ~ U{-127..127}, fp16 d @208
@@ -20,11 +24,14 @@ from __future__ import annotations
 
 import numpy as np
 
-Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_XS = 2, 8, 12, 13, 14, 23
-FORMATS = {"Q4_0": Q4_0, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "IQ4_XS": IQ4_XS}
+Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_NL, IQ4_XS = 2, 3, 6, 7, 8, 12, 13, 14, 20, 23
+FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K,
+           "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
 FORMAT_NAMES = {v: k for k, v in FORMATS.items()}
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_XS: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_XS: 136}
+BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_NL: 32,
+               IQ4_XS: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_NL: 18,
+               IQ4_XS: 136}
 
 BASE_SEED = 0x51472026
 
@@ -62,8 +69,11 @@ def weights(fmt: int, N: int, K: int, g: np.random.Generator) -> np.ndarray:
     if fmt == Q8_0:
         _put_half(blocks, 0, d)
         blocks[:, 2:34] = g.integers(-127, 128, size=(nblk, 32), dtype=np.int16).astype(np.int8).view(np.uint8)
-    elif fmt in (Q4_0, IQ4_XS):
+    elif fmt in (Q4_0, IQ4_XS, IQ4_NL, Q5_0):
         _put_half(blocks, 0, d)
+    elif fmt in (Q4_1, Q5_1):
+        _put_half(blocks, 0, d)
+        _put_half(blocks, 2, g.uniform(-1e-3, 1e-3, size=nblk).astype(np.float32))
     elif fmt in (Q4_K, Q5_K):
         _put_half(blocks, 0, d)
         _put_half(blocks, 2, g.uniform(0.0, 1e-3, size=nblk).astype(np.float32))

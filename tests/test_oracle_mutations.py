@@ -37,6 +37,12 @@ MUTATIONS = [
     ("shared expert weighted", "double ws = s < topk ? w[(size_t)m * topk + s] : 1.0;",
      "double ws = s < topk ? w[(size_t)m * topk + s] : 0.5;"),
     ("fp16 exponent bias", "expo - 25", "expo - 24"),
+    ("q4_1 min sign", "b = -rd_half(blk + 2);\n            code = e < 16", "b = rd_half(blk + 2);\n            code = e < 16"),
+    ("q5 fifth bit index", "int hb = (qh[e / 8] >> (e % 8)) & 1;", "int hb = (qh[e / 8] >> (e % 4)) & 1;"),
+    ("q5_0 offset dropped", "else code -= 16;", "else code -= 0;"),
+    ("q5_1 min from wrong field", "if (one) b = -rd_half(blk + 2);", "if (one) b = -rd_half(blk + 4);"),
+    ("iq4_nl nibble order", "int idx = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);",
+     "int idx = e < 16 ? (blk[2 + e] >> 4) : (blk[2 + e - 16] & 15);"),
 ]
 
 PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]

@@ -20,7 +20,8 @@ import pytest
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "blocks.txt")
-FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.IQ4_XS]
+FMTS = [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q4_K, synth.Q5_K, synth.Q6_K,
+        synth.IQ4_NL, synth.IQ4_XS]
 IQ4NL = [-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113]
 
 
@@ -81,6 +82,39 @@ def _enc_q4_0(d, nib):
     b[0:2] = _h(d)
     for i in range(16):
         b[2 + i] = nib[i] | (nib[16 + i] << 4)
+    return b
+
+
+def _enc_q4_1(d, m, nib):
+    b = np.zeros(20, np.uint8)
+    b[0:2] = _h(d)
+    b[2:4] = _h(m)
+    for i in range(16):
+        b[4 + i] = nib[i] | (nib[16 + i] << 4)
+    return b
+
+
+def _enc_q5(fmt, d, m, code):
+    """code[32] in 0..31 (stored): Q5_0 without m, Q5_1 with m."""
+    one = fmt == synth.Q5_1
+    b = np.zeros(24 if one else 22, np.uint8)
+    b[0:2] = _h(d)
+    if one:
+        b[2:4] = _h(m)
+    qh = sum(((int(code[e]) >> 4) & 1) << e for e in range(32))
+    qo = 4 if one else 2
+    b[qo:qo + 4] = np.array([qh & 255, (qh >> 8) & 255, (qh >> 16) & 255, qh >> 24], np.uint8)
+    so = qo + 4
+    for i in range(16):
+        b[so + i] = (code[i] & 15) | ((code[16 + i] & 15) << 4)
+    return b
+
+
+def _enc_iq4_nl(d, idx):
+    b = np.zeros(18, np.uint8)
+    b[0:2] = _h(d)
+    for i in range(16):
+        b[2 + i] = idx[i] | (idx[16 + i] << 4)
     return b
 
 
@@ -152,6 +186,18 @@ def test_roundtrip_encode_decode(orc, fmt):
         elif fmt == synth.Q4_0:
             nib = g.integers(0, 16, 32)
             blk, expect = _enc_q4_0(d, nib), d * (nib - 8)
+        elif fmt == synth.Q4_1:
+            m = float(np.float16(g.uniform(-1, 1)))
+            nib = g.integers(0, 16, 32)
+            blk, expect = _enc_q4_1(d, m, nib), d * nib + m
+        elif fmt in (synth.Q5_0, synth.Q5_1):
+            m = float(np.float16(g.uniform(-1, 1)))
+            code = g.integers(0, 32, 32)
+            blk = _enc_q5(fmt, d, m, code)
+            expect = d * (code - 16) if fmt == synth.Q5_0 else d * code + m
+        elif fmt == synth.IQ4_NL:
+            idx = g.integers(0, 16, 32)
+            blk, expect = _enc_iq4_nl(d, idx), d * np.array(IQ4NL)[idx]
         elif fmt in (synth.Q4_K, synth.Q5_K):
             dmin = float(np.float16(g.uniform(0, 1)))
             S, M = g.integers(0, 64, 8), g.integers(0, 64, 8)
@@ -300,7 +346,7 @@ def test_int_path_equals_fp64_bruteforce(orc, fmt):
         want = np.einsum("nuk,muk->mnu", codes.reshape(N, K // 32, 32).astype(np.int64),
                          xq.reshape(M, K // 32, 32).astype(np.int64))
         np.testing.assert_array_equal(dots, want)
-        if fmt in (synth.Q4_K, synth.Q5_K):
+        if fmt in (synth.Q4_K, synth.Q5_K, synth.Q4_1, synth.Q5_1):  # formats with a min term
             np.testing.assert_array_equal(aux, np.broadcast_to(xs[:, None, :], aux.shape))
         else:
             assert not aux.any()
