@@ -69,11 +69,11 @@ int launch_engine_mt(int MT, const Job &job, int grid, uint32_t smem, cudaStream
 // Runs fn(ic<T>) with the task size the plan chose (see task_geo).
 template <class Fn>
 int with_t(const TaskGeo &g, Fn &&fn) {
-    if constexpr (QG_FMT == F_Q4_0) {
+    if constexpr (QG_FMT == F_Q4_0 || QG_FMT == F_IQ4_NL) {
         if (g.T == 8) return fn(ic<8>{});
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
-    } else if constexpr (QG_FMT == F_Q8_0) {
+    } else if constexpr (QG_FMT == F_Q8_0 || QG_FMT == F_Q4_1 || QG_FMT == F_Q5_0 || QG_FMT == F_Q5_1) {
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
     } else if constexpr (QG_FMT == F_Q5_K || QG_FMT == F_Q6_K) {
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
                 ((uint32_t)hs & 0xffffu) | ((uint32_t)(sum - hs) << 16);
             reinterpret_cast<float *>(tile + TL::Q)[u] = 0.0f;
         }
-        DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K};
+        DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K || FMT == F_Q4_1 || FMT == F_Q5_1};
         F::run(blk, tt % F::TPB, XT{tile, 0}, 1, sink);
     }
 }

@@ -1,4 +1,4 @@
-// qg_formats.cuh -- register-resident decoders for the six GGUF block formats.
+// qg_formats.cuh -- register-resident decoders for the GGUF block formats.
 //
 // The GEMV is computed on the raw blocks in place ("为什么专家缓存救不了稠密模型", Q&A
 // "如何让CUDA直接计算GGUF混合量化块而不展开为FP16？"): weight codes are unpacked in
@@ -11,14 +11,18 @@
 //   Q8_0    34 B: fp16 d, int8 q[32]                           w = d*q
 //   Q4_0    18 B: fp16 d, qs[16]; e<16 low nibble of qs[e],    w = d*(nib-8)
 //                 e>=16 high nibble of qs[e-16]
+//   Q4_1    20 B: fp16 d, fp16 m, qs[16]                       w = d*nib + m
+//   Q5_0    22 B: fp16 d, u32 qh, qs[16] (bit e of qh = 5th)   w = d*(code-16)
+//   Q5_1    24 B: fp16 d, fp16 m, u32 qh, qs[16]               w = d*code + m
+//   IQ4_NL  18 B: fp16 d, qs[16] codebook indices              w = d*K[idx]
 //   Q4_K   144 B: fp16 d, fp16 dmin, sc12[12], qs[128]         w = d*S_j*code - dmin*M_j
 //   Q5_K   176 B: fp16 d, fp16 dmin, sc12[12], qh[32], qs[128] (code += 16 * bit j of qh[l])
 //   Q6_K   210 B: ql[128], qh[64], int8 sc[16], fp16 d          w = d*sc[e/16]*(code-32)
 //   IQ4_XS 136 B: fp16 d, u16 scales_h, scales_l[4], qs[128]   w = d*(ls-32)*K[idx]
 //
-// Work is organised in TASKS, one per lane: eight, four or one Q4_0 blocks, four or one
-// Q8_0 blocks, two or one Q4_K / IQ4_XS superblocks, a whole (or half a) Q5_K / Q6_K
-// superblock.  A task's weights are read from shared memory; its activations come from a
+// Work is organised in TASKS, one per lane: eight, four or one Q4_0 / IQ4_NL blocks, four
+// or one Q8_0 / Q4_1 / Q5_0 / Q5_1 blocks, two or one Q4_K / IQ4_XS superblocks, a whole
+// Q5_K / Q6_K superblock.  A task's weights are read from shared memory; its activations come from a
 // per-task tile (codes, scales d, sums s, packed 16-element half sums and d*s of each
 // activation block), padded so that the 16-byte loads of 8 consecutive lanes hit distinct
 // banks.  Every unit's dot product is an exact int32 sum; the test-hook sink receives
@@ -30,7 +34,10 @@
 
 namespace qg {
 
-enum : int { F_Q4_0 = 2, F_Q8_0 = 8, F_Q4_K = 12, F_Q5_K = 13, F_Q6_K = 14, F_IQ4_XS = 23 };
+enum : int {
+    F_Q4_0 = 2, F_Q4_1 = 3, F_Q5_0 = 6, F_Q5_1 = 7, F_Q8_0 = 8,
+    F_Q4_K = 12, F_Q5_K = 13, F_Q6_K = 14, F_IQ4_NL = 20, F_IQ4_XS = 23
+};
 
 // unsigned (weights) x signed (activations) 4-way byte dot product
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -90,16 +97,57 @@ __device__ __forceinline__ int byte_of(uint32_t w, int k) { return (int)((w >> (
 //                 activation sum xs (the integer contract of the test hook);
 //   value sinks:  add(m, v) with the benchmark's fp32 contribution to y.
 
-// ================================================================================ Q8_0 / Q4_0
-// T blocks per task.  With T == 4 or 8 a task is T*34 (Q8_0) or T*18 (Q4_0) bytes and starts
-// 8-byte (T == 8: 16-byte) aligned, so all field offsets are compile-time; with T == 1 the
-// block may start on any even byte and is realigned with run-time byte permutes.
-// Every decoder works in two phases: load() copies the task's bytes from shared memory
-// into registers (so that the engine can refill the ring slot at once), compute() decodes
-// them against the activation tiles.
+// ================================================================================ IQ4 codebook
+constexpr int8_t kIQ4Codebook[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
+                                     1,    13,   25,  38,  53,  69,  89,  113};
+constexpr uint32_t cb_word(int i) {
+    return (uint32_t)(uint8_t)kIQ4Codebook[i] | ((uint32_t)(uint8_t)kIQ4Codebook[i + 1] << 8) |
+           ((uint32_t)(uint8_t)kIQ4Codebook[i + 2] << 16) | ((uint32_t)(uint8_t)kIQ4Codebook[i + 3] << 24);
+}
+
+// Codebook values of the 8 indices in q (byte k: low nibble = element k of the unit's first
+// half, high nibble = element k of its second half): byte permutes over the two table
+// halves, then a permute that keeps, per byte, the half chosen by the index's bit 3.
+__device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &hi) {
+    const uint32_t i7 = q & 0x77777777u;
+    const uint32_t pick = ((q >> 1) & 0x44444444u) | 0x32103210u;
+    const uint32_t a0 = prmt(cb_word(0), cb_word(4), i7), b0 = prmt(cb_word(8), cb_word(12), i7);
+    const uint32_t a1 = prmt(cb_word(0), cb_word(4), i7 >> 16), b1 = prmt(cb_word(8), cb_word(12), i7 >> 16);
+    const uint32_t A = prmt(a0, b0, pick);        // values of nibbles (lo b0, hi b0, lo b1, hi b1)
+    const uint32_t B = prmt(a1, b1, pick >> 16);  // values of nibbles (lo b2, hi b2, lo b3, hi b3)
+    lo = prmt(A, B, 0x6420u);
+    hi = prmt(A, B, 0x7531u);
+}
+
+// ====================================================================== 32-element blocks
+// Q8_0, Q4_0, Q4_1, Q5_0, Q5_1 and IQ4_NL: T blocks per task.  With T == 4 or 8 every
+// block's field offsets are compile-time (a task starts 8-byte, with T == 8 16-byte,
+// aligned); with T == 1 a block may start on any even byte and its fields are realigned
+// with run-time byte permutes.  Every decoder works in two phases: load() copies the
+// task's bytes from shared memory into registers (so that the engine can refill the ring
+// slot at once), compute() decodes them against the activation tiles.
+//
+//   Q8_0    34 B: d, q[32]                      dot = sum q*x
+//   Q4_0    18 B: d, qs[16]                     dot = sum (nib-8)*x
+//   Q4_1    20 B: d, m, qs[16]                  y += d*xd*sum(nib*x) + m*(xd*s)
+//   Q5_0    22 B: d, qh[4], qs[16]              dot = sum ((nib|bit<<4)-16)*x
+//   Q5_1    24 B: d, m, qh[4], qs[16]           y += d*xd*sum((nib|bit<<4)*x) + m*(xd*s)
+//   IQ4_NL  18 B: d, qs[16] (codebook indices)  dot = sum K[idx]*x
+// Element e < 16 uses the low nibble of qs[e], e >= 16 the high nibble of qs[e-16]; the
+// fifth bit of element e is bit e of the little-endian 32-bit qh.
+
+// Bit i of t (i < 4) moved to bit 4 of byte i.
+__device__ __forceinline__ uint32_t spread4_bit4(uint32_t t) { return ((t * 0x00204081u) & 0x01010101u) << 4; }
+
 template <int FMT, int T>
 struct FmtLegacy {
-    static constexpr int QK = 32, BS = (FMT == F_Q8_0 ? 34 : 18), XGT = T, TPB = 1, BPT = T;
+    static constexpr int QK = 32, XGT = T, TPB = 1, BPT = T;
+    static constexpr int BS = FMT == F_Q8_0 ? 34 : FMT == F_Q4_1 ? 20 : FMT == F_Q5_0 ? 22 : FMT == F_Q5_1 ? 24 : 18;
+    static constexpr bool HAS_M = FMT == F_Q4_1 || FMT == F_Q5_1;
+    static constexpr bool HAS_QH = FMT == F_Q5_0 || FMT == F_Q5_1;
+    static constexpr int QH_OFF = FMT == F_Q5_1 ? 4 : 2;
+    static constexpr int QS_OFF = FMT == F_Q4_1 ? 4 : FMT == F_Q5_0 ? 6 : FMT == F_Q5_1 ? 8 : 2;
+    static constexpr int NQW = FMT == F_Q8_0 ? 8 : 4;  // code words per block
     static constexpr int TASK_BYTES = T * BS;
     // T >= 4: the task's words plus two (the last block's realignment reads past its end);
     // T == 1: the words that cover the block from its 4-byte-aligned start
@@ -129,32 +177,62 @@ struct FmtLegacy {
         }
     }
 
+    // The 4 bytes at byte offset o (even, compile-time) of a block that starts a (0 or 2)
+    // bytes into w[0]: pair (w[o/4], w[o/4+1]) starting at byte a + o%4 of the pair.
+    __device__ __forceinline__ static uint32_t rword(const uint32_t (&w)[WW], uint32_t a, int o) {
+        return prmt(w[o >> 2], w[(o >> 2) + 1], 0x3210u + 0x2222u * ((a + (uint32_t)(o & 3)) >> 1));
+    }
+
     template <class Sink>
-    __device__ __forceinline__ static void unit_from_words(const uint32_t (&c)[8], float d, int m, int u,
-                                                           SAddr tile, Sink &sink) {
+    __device__ __forceinline__ static void unit(const uint32_t (&c)[8], uint32_t qh, float d, float mv, int m, int u,
+                                                SAddr tile, Sink &sink) {
         using TL = Tile<XGT>;
         uint32_t x[8];
         ldx8(tile + 32 * u, x);
-        int dot = 0;
-        int xs = 0;
-        if (FMT == F_Q8_0) {
+        int dot = 0, xs = 0;
+        if constexpr (FMT == F_Q8_0) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) dot = dp4a(c[k], x[k], dot);
-        } else {
-            // c[0..3]: qs words; low nibbles = elements 0..15, high nibbles = 16..31
+        } else if constexpr (FMT == F_Q4_0 || FMT == F_Q4_1) {
             int lo = 0, hi = 0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 lo = dp4a(c[k] & 0x0f0f0f0fu, x[k], lo);
                 hi = dp4a_us(c[k] & 0xf0f0f0f0u, x[4 + k], hi);
             }
-            xs = (int)lds32(tile + TL::S + 4 * u);
-            dot = lo + (hi >> 4) - 8 * xs;
+            dot = lo + (hi >> 4);
+            if constexpr (FMT == F_Q4_0) {
+                xs = (int)lds32(tile + TL::S + 4 * u);
+                dot -= 8 * xs;
+            }
+        } else if constexpr (HAS_QH) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t lo = (c[k] & 0x0f0f0f0fu) | spread4_bit4((qh >> (4 * k)) & 15u);
+                const uint32_t hi = ((c[k] >> 4) & 0x0f0f0f0fu) | spread4_bit4((qh >> (16 + 4 * k)) & 15u);
+                dot = dp4a(lo, x[k], dot);
+                dot = dp4a(hi, x[4 + k], dot);
+            }
+            if constexpr (FMT == F_Q5_0) {
+                xs = (int)lds32(tile + TL::S + 4 * u);
+                dot -= 16 * xs;
+            }
+        } else {  // IQ4_NL
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t lo, hi;
+                cb_lookup8(c[k], lo, hi);
+                dot = dp4a(lo, x[k], dot);
+                dot = dp4a(hi, x[4 + k], dot);
+            }
         }
         if constexpr (Sink::DOTS) {
+            if constexpr (HAS_M) xs = (int)lds32(tile + TL::S + 4 * u);
             sink.unit(m, u, dot, xs);
         } else {
-            sink.add(m, d * ldsf(tile + TL::D + 4 * u) * (float)dot);
+            float v = d * ldsf(tile + TL::D + 4 * u) * (float)dot;
+            if constexpr (HAS_M) v = fmaf(mv, ldsf(tile + TL::Q + 4 * u), v);
+            sink.add(m, v);
         }
     }
 
@@ -166,22 +244,25 @@ struct FmtLegacy {
             for (int b = 0; b < T; ++b) {
                 const int off = BS * b;
                 const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                const float mv = HAS_M ? half_bits_to_float(word_at(w, off + 2)) : 0.0f;
+                const uint32_t qh = HAS_QH ? word_at(w, off + QH_OFF) : 0u;
                 uint32_t c[8];
 #pragma unroll
-                for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = word_at(w, off + 2 + 4 * k);
+                for (int k = 0; k < NQW; ++k) c[k] = word_at(w, off + QS_OFF + 4 * k);
 #pragma unroll
                 for (int m = 0; m < Sink::MT; ++m)
-                    if (m < ntok) unit_from_words(c, d, m, b, xt.tile(m), sink);
+                    if (m < ntok) unit(c, qh, d, mv, m, b, xt.tile(m), sink);
             }
         } else {
-            const uint32_t sel = a ? 0x7654u : 0x5432u;  // 4 bytes starting 2 past the block start
-            const float d = half_bits_to_float(a ? (w[0] >> 16) : w[0]);
+            const float d = half_bits_to_float(rword(w, a, 0));
+            const float mv = HAS_M ? half_bits_to_float(rword(w, a, 2)) : 0.0f;
+            const uint32_t qh = HAS_QH ? rword(w, a, QH_OFF) : 0u;
             uint32_t c[8];
 #pragma unroll
-            for (int k = 0; k < (FMT == F_Q8_0 ? 8 : 4); ++k) c[k] = prmt(w[k], w[k + 1], sel);
+            for (int k = 0; k < NQW; ++k) c[k] = rword(w, a, QS_OFF + 4 * k);
 #pragma unroll
             for (int m = 0; m < Sink::MT; ++m)
-                if (m < ntok) unit_from_words(c, d, m, 0, xt.tile(m), sink);
+                if (m < ntok) unit(c, qh, d, mv, m, 0, xt.tile(m), sink);
         }
     }
 
@@ -474,27 +555,6 @@ struct FmtQ6K {
 };
 
 // ================================================================================ IQ4_XS
-constexpr int8_t kIQ4Codebook[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
-                                     1,    13,   25,  38,  53,  69,  89,  113};
-constexpr uint32_t cb_word(int i) {
-    return (uint32_t)(uint8_t)kIQ4Codebook[i] | ((uint32_t)(uint8_t)kIQ4Codebook[i + 1] << 8) |
-           ((uint32_t)(uint8_t)kIQ4Codebook[i + 2] << 16) | ((uint32_t)(uint8_t)kIQ4Codebook[i + 3] << 24);
-}
-
-// Codebook values of the 8 indices in q (byte k: low nibble = element k of the unit's first
-// half, high nibble = element k of its second half): byte permutes over the two table
-// halves, then a permute that keeps, per byte, the half chosen by the index's bit 3.
-__device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &hi) {
-    const uint32_t i7 = q & 0x77777777u;
-    const uint32_t pick = ((q >> 1) & 0x44444444u) | 0x32103210u;
-    const uint32_t a0 = prmt(cb_word(0), cb_word(4), i7), b0 = prmt(cb_word(8), cb_word(12), i7);
-    const uint32_t a1 = prmt(cb_word(0), cb_word(4), i7 >> 16), b1 = prmt(cb_word(8), cb_word(12), i7 >> 16);
-    const uint32_t A = prmt(a0, b0, pick);        // values of nibbles (lo b0, hi b0, lo b1, hi b1)
-    const uint32_t B = prmt(a1, b1, pick >> 16);  // values of nibbles (lo b2, hi b2, lo b3, hi b3)
-    lo = prmt(A, B, 0x6420u);
-    hi = prmt(A, B, 0x7531u);
-}
-
 // T superblocks per task (136 bytes each; a two-superblock task is 16-byte aligned, a
 // single one 8-byte aligned).  Value path: per token, sum_ib xd_ib * ((ls_ib - 32) *
 // dot_ib), times d once per superblock.
@@ -583,6 +643,14 @@ template <int T>
 struct FmtSel<F_Q8_0, T> { using type = FmtLegacy<F_Q8_0, T>; };
 template <int T>
 struct FmtSel<F_Q4_0, T> { using type = FmtLegacy<F_Q4_0, T>; };
+template <int T>
+struct FmtSel<F_Q4_1, T> { using type = FmtLegacy<F_Q4_1, T>; };
+template <int T>
+struct FmtSel<F_Q5_0, T> { using type = FmtLegacy<F_Q5_0, T>; };
+template <int T>
+struct FmtSel<F_Q5_1, T> { using type = FmtLegacy<F_Q5_1, T>; };
+template <int T>
+struct FmtSel<F_IQ4_NL, T> { using type = FmtLegacy<F_IQ4_NL, T>; };
 template <int T>
 struct FmtSel<F_Q4_K, T> { using type = FmtQ4K<T>; };
 template <int T>

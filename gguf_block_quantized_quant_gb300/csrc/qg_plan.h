@@ -21,6 +21,10 @@ struct FmtInfo {
 inline bool fmt_info(int fmt, FmtInfo &f) {
     switch (fmt) {
     case 2: f = {32, 18}; return true;     // Q4_0
+    case 3: f = {32, 20}; return true;     // Q4_1
+    case 6: f = {32, 22}; return true;     // Q5_0
+    case 7: f = {32, 24}; return true;     // Q5_1
+    case 20: f = {32, 18}; return true;    // IQ4_NL
     case 8: f = {32, 34}; return true;     // Q8_0
     case 12: f = {256, 144}; return true;  // Q4_K
     case 13: f = {256, 176}; return true;  // Q5_K
@@ -44,8 +48,8 @@ inline int log2i(int v) {
 }
 
 // Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
-//   Q4_0: 8, 4 or 1 blocks per task; Q8_0: 4 or 1; Q4_K, IQ4_XS: 2 or 1 superblocks (the
-//   largest that divides the row); Q5_K, Q6_K: one whole superblock (T = 2 halves).
+//   Q4_0, IQ4_NL: 8, 4 or 1 blocks per task; Q8_0, Q4_1, Q5_0, Q5_1: 4 or 1; Q4_K, IQ4_XS:
+//   2 or 1 superblocks (the largest that divides the row); Q5_K, Q6_K: one whole superblock.
 struct TaskGeo {
     bool ok = false;
     int T = 1, TPB = 1, BPT = 1, XGT = 8, nbr = 0, gpr = 0, tpr = 0, stride = 0, bs = 0;
@@ -61,7 +65,7 @@ inline TaskGeo task_geo(int fmt, int K) {
     g.nbr = K / f.qk;
     g.rb = (uint32_t)(g.nbr * f.bs);
     if (f.qk == 32) {
-        g.T = (fmt == 2 && g.nbr % 8 == 0) ? 8 : g.nbr % 4 == 0 ? 4 : 1;
+        g.T = ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0) ? 8 : g.nbr % 4 == 0 ? 4 : 1;
         g.BPT = g.T;
         g.XGT = g.T;
         g.TPB = 1;

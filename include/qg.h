@@ -49,10 +49,14 @@ extern "C" {
 /* Block formats, numbered by their GGUF type ids. */
 enum qg_format {
     QG_Q4_0 = 2,    /* 32 elements, 18 B: fp16 d, 16 B of 4-bit codes; w = d*(c-8)           */
+    QG_Q4_1 = 3,    /* 32 elements, 20 B: fp16 d, fp16 m, 4-bit codes; w = d*c + m           */
+    QG_Q5_0 = 6,    /* 32 elements, 22 B: fp16 d, 32 fifth bits, 4-bit codes; w = d*(c-16)   */
+    QG_Q5_1 = 7,    /* 32 elements, 24 B: fp16 d, fp16 m, fifth bits, codes; w = d*c + m     */
     QG_Q8_0 = 8,    /* 32 elements, 34 B: fp16 d, 32 int8 codes; w = d*q                     */
     QG_Q4_K = 12,   /* 256 elements, 144 B: fp16 d, dmin, 8 x 6-bit scale/min, 4-bit codes   */
     QG_Q5_K = 13,   /* 256 elements, 176 B: as Q4_K plus one high bit per code              */
     QG_Q6_K = 14,   /* 256 elements, 210 B: 6-bit codes, 16 int8 sub-scales, fp16 d          */
+    QG_IQ4_NL = 20, /* 32 elements, 18 B: fp16 d, 4-bit indices into the 16-entry codebook   */
     QG_IQ4_XS = 23  /* 256 elements, 136 B: fp16 d, 6-bit sub-scales, 4-bit codebook indices */
 };
 

@@ -61,7 +61,7 @@ def test_gemv_rejects_bad_arguments(L):
         a = dict(ok, **kw)
         return L_.qg_gemv(a["fmt"], _P(a["W"]), _P(a["x"]), _P(a["y"]), a["N"], a["K"], a["M"], None, 0, None)
 
-    assert call(fmt=3) == -1          # unknown format
+    assert call(fmt=5) == -1          # unknown format (type id 5 is unused)
     assert call(K=255) == -1          # not a multiple of the block size
     assert call(K=0) == -1
     assert call(M=0) == -1
@@ -78,7 +78,7 @@ def test_other_entry_points_reject_bad_arguments(L):
     P = _P
     assert L.qg_quantize_act(P(A16), 1, 33, P(A16), P(A16), P(A16), None) == -1
     assert L.qg_gemv_q(12, P(A16), None, P(A16), P(A16), P(A16), 4, 256, 1, None, 0, None) == -1
-    assert L.qg_gemv_static_ws(3, P(A16), P(A16), P(A16), 4, 256, 1, None) == -1    # unknown format
+    assert L.qg_gemv_static_ws(5, P(A16), P(A16), P(A16), 4, 256, 1, None) == -1    # unknown format
     assert L.qg_gemv_static_ws(12, P(A16), None, P(A16), 4, 256, 1, None) == -1     # no activations
     assert L.qg_gemv_static_ws(12, P(A16), P(A16), P(A16), 4, 256, 17, None) == -1  # batch above 16
     assert L.qg_block_dots(14, P(A16), P(A16), P(A16 + 2), 4, 256, 1, P(A16), P(A16), None) == -3

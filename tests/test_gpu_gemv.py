@@ -120,6 +120,7 @@ FULL = [
     (synth.Q4_K, 17408, 5120), (synth.Q4_K, 5120, 17408),
     (synth.Q5_K, 4096, 4096), (synth.Q6_K, 4096, 4096), (synth.IQ4_XS, 4096, 4096),
     (synth.Q6_K, 17408, 5120), (synth.Q6_K, 5120, 17408),
+    (synth.Q4_1, 4096, 4096), (synth.Q5_0, 4096, 4096), (synth.Q5_1, 4096, 4096), (synth.IQ4_NL, 4096, 4096),
 ]
 
 
