@@ -61,40 +61,70 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(const float *x, const f
     prep_tiles_warp(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
 }
 
-// Blocks [0, ceil(E/8)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32, one warp per
-// expert row.  The remaining blocks write the activation tile image of x.  Launched like
-// prep_tiles_kernel.
+// Blocks [0, ceil(E/2)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32.  Each block takes
+// two experts, four warps per expert, each warp a quarter of the row with 16-byte loads so
+// that a lane's loads are all in flight at once; the quarters are added in order.  The
+// remaining blocks write the activation tile image of x.  Launched like prep_tiles_kernel.
+constexpr int ROUTER_SPLIT = 4;  // warps per expert row
 __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M, int H, const float *Wr, int E,
                                                           float *logits, int xgt_log2, uint8_t *img) {
     griddep_launch_dependents();
     griddep_wait();
-    const int lane = threadIdx.x & 31;
-    const int nrouter = (E + 7) / 8;
+    __shared__ float part[8][M_MAX];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int epb = 8 / ROUTER_SPLIT;  // experts per block
+    const int nrouter = (E + epb - 1) / epb;
     if ((int)blockIdx.x >= nrouter) {
         const long nwarps = (long)(gridDim.x - nrouter) * (blockDim.x >> 5);
-        const long wid = (long)(blockIdx.x - nrouter) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const long wid = (long)(blockIdx.x - nrouter) * (blockDim.x >> 5) + warp;
         prep_tiles_warp(x, nullptr, nullptr, nullptr, nullptr, nullptr, M, H, xgt_log2, img, nullptr, nullptr, nullptr,
                         wid, nwarps);
         return;
     }
-    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (e >= E) return;
+    const int e = blockIdx.x * epb + warp / ROUTER_SPLIT, q = warp % ROUTER_SPLIT;
     float acc[M_MAX];
 #pragma unroll
     for (int m = 0; m < M_MAX; ++m) acc[m] = 0.0f;
-    const float *wr = Wr + (long)e * H;
-    for (int k = lane; k < H; k += 32) {
-        const float wv = __ldg(wr + k);
+    if (e < E) {
+        const float *wr = Wr + (long)e * H;
+        const int k0 = (int)((long)q * H / ROUTER_SPLIT), k1 = (int)((long)(q + 1) * H / ROUTER_SPLIT);
+        if ((((uintptr_t)wr | (uintptr_t)x) & 15u) == 0 && ((k0 | k1) & 3) == 0) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(wr);
+#pragma unroll 4
+            for (int k = (k0 >> 2) + lane; k < (k1 >> 2); k += 32) {
+                const float4 wv = __ldg(w4 + k);
 #pragma unroll
-        for (int m = 0; m < M_MAX; ++m)
-            if (m < M) acc[m] = fmaf(wv, __ldg(x + (long)m * H + k), acc[m]);
+                for (int m = 0; m < M_MAX; ++m) {
+                    if (m < M) {
+                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (long)m * H) + k);
+                        acc[m] = fmaf(wv.x, xv.x, acc[m]);
+                        acc[m] = fmaf(wv.y, xv.y, acc[m]);
+                        acc[m] = fmaf(wv.z, xv.z, acc[m]);
+                        acc[m] = fmaf(wv.w, xv.w, acc[m]);
+                    }
+                }
+            }
+        } else {
+            for (int k = k0 + lane; k < k1; k += 32) {
+                const float wv = __ldg(wr + k);
+#pragma unroll
+                for (int m = 0; m < M_MAX; ++m)
+                    if (m < M) acc[m] = fmaf(wv, __ldg(x + (long)m * H + k), acc[m]);
+            }
+        }
     }
 #pragma unroll
     for (int m = 0; m < M_MAX; ++m) {
         if (m < M) {
             const float v = warp_sum(acc[m]);
-            if (lane == 0) logits[(long)m * E + e] = v;
+            if (lane == 0) part[warp][m] = v;
         }
+    }
+    __syncthreads();
+    if (e < E && q == 0 && lane < M) {
+        float v = part[warp][lane];
+        for (int r = 1; r < ROUTER_SPLIT; ++r) v += part[warp + r][lane];
+        logits[(long)lane * E + e] = v;
     }
 }
 
@@ -161,7 +191,8 @@ int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, flo
                        uint8_t *img, cudaStream_t s) {
     const long blocks = (long)M * (H / 32);
     const int nprep = (int)std::min<long>((blocks + 7) / 8, 512);
-    return launch_pdl(router_prep_kernel, (E + 7) / 8 + nprep, 256, s, x, M, H, Wr, E, logits, xgt_log2, img);
+    const int epb = 8 / ROUTER_SPLIT;
+    return launch_pdl(router_prep_kernel, (E + epb - 1) / epb + nprep, 256, s, x, M, H, Wr, E, logits, xgt_log2, img);
 }
 
 // ----------------------------------------------------------------------------- host helpers

@@ -19,6 +19,10 @@ namespace qg {
 __host__ __device__ constexpr int engine_ncw(int task_bytes, int MT) {
     return (MT <= 4 && task_bytes <= 160) ? 16 : 8;
 }
+// One-token launches with tasks over 160 bytes may run 12 warps (3 per scheduler) with one
+// ring slot each when every CTA has enough tasks for two stages per warp.
+constexpr int NCW_WIDE = 12;
+__host__ __device__ constexpr bool ncw_wide_allowed(int task_bytes, int MT) { return MT == 1 && task_bytes > 160; }
 
 constexpr int SMEM_MAX = 227 * 1024;       // opt-in dynamic shared memory per CTA (sm_100 family)
 constexpr int STAGE_SLACK = 64;            // bytes after each ring slot for over-reads

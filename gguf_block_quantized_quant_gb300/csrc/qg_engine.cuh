@@ -88,11 +88,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int FMT, int T, int MT, class Job>
-__global__ void __launch_bounds__(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32, 1) engine_kernel(const Job job) {
+// NCW: warps of the CTA (engine_ncw(), or 12 for large one-token launches, see plan_ncw).
+template <int FMT, int T, int MT, int NCW, class Job>
+__global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
     using F = FT<FMT, T>;
     using TL = Tile<F::XGT>;
-    constexpr int NCW = engine_ncw(F::TASK_BYTES, MT), NCONS = NCW * 32;
+    constexpr int NCONS = NCW * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;

@@ -23,11 +23,11 @@ using ic = std::integral_constant<int, V>;
 
 // Each kernel instantiation opts in to the full shared memory once per device; launches
 // use programmatic stream serialization (see griddep_wait in qg_common.cuh).
-template <int FMT, int T, int MT, class Job>
+template <int FMT, int T, int MT, int NCW, class Job>
 int launch_engine(const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     static std::mutex mu;
     static bool ready[64] = {};
-    auto kern = engine_kernel<FMT, T, MT, Job>;
+    auto kern = engine_kernel<FMT, T, MT, NCW, Job>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
     {
@@ -42,7 +42,7 @@ int launch_engine(const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(engine_ncw(FT<FMT, T>::TASK_BYTES, MT) * 32);
+    cfg.blockDim = dim3(NCW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -54,14 +54,26 @@ int launch_engine(const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// The launch with MT tokens per lane and ncw warps (the default engine_ncw(), or NCW_WIDE
+// where ncw_wide_allowed()).
+template <int FMT, int T, int MT, class Job>
+int launch_engine_ncw(int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
+    constexpr int TB = FT<FMT, T>::TASK_BYTES;
+    if constexpr (ncw_wide_allowed(TB, MT)) {
+        if (ncw == NCW_WIDE) return launch_engine<FMT, T, MT, NCW_WIDE>(job, grid, smem, s);
+    }
+    if (ncw != engine_ncw(TB, MT)) return -1;
+    return launch_engine<FMT, T, MT, engine_ncw(TB, MT)>(job, grid, smem, s);
+}
+
 template <int FMT, int T, class Job>
-int launch_engine_mt(int MT, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
+int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     switch (MT) {
-    case 1: return launch_engine<FMT, T, 1>(job, grid, smem, s);
-    case 2: return launch_engine<FMT, T, 2>(job, grid, smem, s);
-    case 4: return launch_engine<FMT, T, 4>(job, grid, smem, s);
-    case 8: return launch_engine<FMT, T, 8>(job, grid, smem, s);
-    case 16: return launch_engine<FMT, T, 16>(job, grid, smem, s);
+    case 1: return launch_engine_ncw<FMT, T, 1>(ncw, job, grid, smem, s);
+    case 2: return launch_engine_ncw<FMT, T, 2>(ncw, job, grid, smem, s);
+    case 4: return launch_engine_ncw<FMT, T, 4>(ncw, job, grid, smem, s);
+    case 8: return launch_engine_ncw<FMT, T, 8>(ncw, job, grid, smem, s);
+    case 16: return launch_engine_ncw<FMT, T, 16>(ncw, job, grid, smem, s);
     default: return -1;
     }
 }
@@ -120,7 +132,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.out = out;
         j.slice_stride = (long)c.M * c.N;
-        return launch_engine_mt<FMT, T>(p.MT, j, p.grid, p.ring.smem_total, c.stream);
+        return launch_engine_mt<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
     });
     if (rc) return rc;
     if (p.KS > 1) return launch_splitk_reduce(out, p.KS, (long)c.M * c.N, c.y, c.stream);
@@ -163,7 +175,7 @@ int ffn_run(const FfnCall &c, int sms) {
             j.ximg_pitch = (uint32_t)p.ximg_pitch;
             j.g_out = g;
             j.u_out = u;
-            return launch_engine_mt<FMT, T>(p.MT, j, p.grid, p.ring.smem_total, c.stream);
+            return launch_engine_mt<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
         });
         if (rc) return rc;
     }
@@ -229,7 +241,7 @@ int moe_run(const MoeCall &c, int sms) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.g_out = g;
         j.u_out = u;
-        return launch_engine<FMT, T, 1>(j, p.gu_grid, p.gu_ring.smem_total, c.stream);
+        return launch_engine_ncw<FMT, T, 1>(p.gu_ncw, j, p.gu_grid, p.gu_ring.smem_total, c.stream);
     });
     if (rc) return rc;
     // h = silu(g) * u, requantized: one image row per token and slot; the plain h and its
@@ -259,7 +271,7 @@ int moe_run(const MoeCall &c, int sms) {
             j.ximg = himg;
             j.ximg_pitch = (uint32_t)p.himg_pitch;
             j.y = c.y;
-            return launch_engine<FMT, T, 1>(j, p.dn_grid, p.dn_ring.smem_total, c.stream);
+            return launch_engine_ncw<FMT, T, 1>(p.dn_ncw, j, p.dn_grid, p.dn_ring.smem_total, c.stream);
         });
         if (rc) return rc;
     }

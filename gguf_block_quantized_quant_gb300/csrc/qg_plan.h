@@ -89,6 +89,11 @@ inline TaskGeo task_geo(int fmt, int K) {
     return g;
 }
 inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
+// Warps of a launch whose CTAs hold up to tasks_per_cta tasks.
+inline int plan_ncw(const TaskGeo &g, int MT, long tasks_per_cta) {
+    if (ncw_wide_allowed(g.task_bytes(), MT) && tasks_per_cta >= (long)NCW_WIDE * 32 * 2) return NCW_WIDE;
+    return geo_ncw(g, MT);
+}
 
 // Stage size and ring of one engine launch.
 struct Ring {
@@ -134,7 +139,7 @@ inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_b
 struct GemvPlan {
     bool ok = false;
     TaskGeo geo;
-    int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0;
+    int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0, ncw = 8;
     Ring ring;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
@@ -153,7 +158,8 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     p.MT = pick_mt(M);
     p.tpr_x = (g.gpr + p.KS - 1) / p.KS * g.TPB;
     // split-K: every row is its own run; the shortest slice has floor(gpr / KS) groups
-    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, geo_ncw(g, p.MT));
+    p.ncw = plan_ncw(g, p.MT, (long)((N + p.groups - 1) / p.groups) * p.tpr_x);
+    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, p.ncw);
     if (!p.ring.ok) return p;
     size_t o = 0;
     p.ximg_pitch = (size_t)g.tpr * g.stride;
@@ -172,7 +178,7 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
 struct FfnPlan {
     bool ok = false;
     TaskGeo geo;
-    int grid = 1, MT = 1, MC = 1, nchunk = 1;
+    int grid = 1, MT = 1, MC = 1, nchunk = 1, ncw = 8;
     Ring ring;
     GemvPlan down;  // y = Wd h; h = silu(g) * u is formed by its activation preparation
     size_t ws_ximg = 0, ximg_pitch = 0, ws_g = 0, ws_u = 0, ws_h = 0, ws_down = 0, ws_total = 0;
@@ -189,7 +195,8 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     p.nchunk = (M + p.MC - 1) / p.MC;
     p.MT = pick_mt(p.MC);
     p.grid = std::min(2 * I, sms);
-    p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, geo_ncw(g, p.MT));
+    p.ncw = plan_ncw(g, p.MT, (long)((2L * I + p.grid - 1) / p.grid) * g.tpr);
+    p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, p.ncw);
     if (!p.ring.ok) return p;
     p.down = plan_gemv(fmt, H, I, M, sms);
     if (!p.down.ok) return p;
@@ -209,7 +216,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
 // ----------------------------------------------------------------------------- MoE FFN
 struct MoePlan {
     bool ok = false;
-    int S = 0;
+    int S = 0, gu_ncw = 8, dn_ncw = 8;
     TaskGeo gh, gi;  // rows of H elements (gate/up) and of I elements (down)
     int gu_grid = 0, dn_grid = 0, dn_MC = 1, dn_nchunk = 1;
     Ring gu_ring, dn_ring;
@@ -230,7 +237,8 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     const long gu_x = (long)M * p.gh.tpr * p.gh.stride;
     if (gu_x > (long)XCAP) return p;
     p.gu_grid = (int)std::min<long>(sms, gu_rows);
-    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, geo_ncw(p.gh, 1));
+    p.gu_ncw = plan_ncw(p.gh, 1, (gu_rows + p.gu_grid - 1) / p.gu_grid * p.gh.tpr);
+    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, p.gu_ncw);
     if (!p.gu_ring.ok) return p;
     // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
     const long tiles_tok = (long)p.S * p.gi.tpr * p.gi.stride;
@@ -242,7 +250,7 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     p.dn_nchunk = (M + p.dn_MC - 1) / p.dn_MC;
     // CTAs own floor or ceil of H / dn_grid rows: runs are at least the floor long
     p.dn_ring = plan_ring(p.gi, (long)(H / p.dn_grid) * p.gi.tpr, (uint32_t)(p.dn_MC * tiles_tok),
-                          (uint32_t)(p.dn_MC * part_tok), geo_ncw(p.gi, 1));
+                          (uint32_t)(p.dn_MC * part_tok), p.dn_ncw = geo_ncw(p.gi, 1));
     if (!p.dn_ring.ok) return p;
     // workspace
     const size_t Rw = (size_t)M * p.S;
