@@ -18,7 +18,9 @@ bandwidth.
   * reference arm: the plain CPU oracle (the checker of the CUDA path) on the host cores,
     each step a bounded sample of the same workload;
   * N > 1 (torchrun): replicas only -- every rank runs the whole workload on its own GPU;
-    the value is the weight bytes of all ranks over the slowest rank's time.
+    the value is the weight bytes of all ranks over the slowest rank's time;
+  * --one FMT:NxK:M (e.g. Q4_K:17408x5120:1): three untimed GEMV calls of one shape on
+    seeded synthetic input and nothing else -- the small case a profiler captures.
 """
 from __future__ import annotations
 
@@ -483,6 +485,25 @@ def secondary(qg, torch, dev, s):
     return out
 
 
+def run_one(spec: str):
+    """Three qg_gemv calls of one shape (format name:NxK:M), for a profiler to capture."""
+    import torch
+
+    import gguf_block_quantized_quant_gb300 as qg
+
+    name, shape, m = spec.split(":")
+    N, K = (int(v) for v in shape.lower().split("x"))
+    fmt = synth.FORMATS[name]
+    g = np.random.default_rng(synth.seed_for(CONFIG_ID, fmt))
+    W = torch.from_numpy(synth.weights(fmt, N, K, g)).cuda()
+    x = torch.from_numpy(synth.activations(int(m), K, g)).cuda()
+    for _ in range(3):
+        y = qg.qg_gemv(fmt, W, x, N)
+    torch.cuda.synchronize()
+    print(json.dumps({"one": spec, "weight_bytes": int(W.numel()), "y_abs_sum": float(y.abs().sum())}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,7 +513,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--one", metavar="FMT:NxK:M", help="three untimed GEMV calls of one shape, then exit")
     args = ap.parse_args(argv)
+    if args.one:
+        return run_one(args.one)
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps")
     if args.impl == "reference":

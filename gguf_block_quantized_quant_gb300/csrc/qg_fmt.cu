@@ -68,6 +68,9 @@ int launch_engine_ncw(int ncw, const Job &job, int grid, uint32_t smem, cudaStre
 
 template <int FMT, int T, class Job>
 int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
+    if constexpr (T == 16) {  // 16-block tasks are planned for one token per lane only
+        return MT == 1 ? launch_engine_ncw<FMT, T, 1>(ncw, job, grid, smem, s) : -1;
+    }
     switch (MT) {
     case 1: return launch_engine_ncw<FMT, T, 1>(ncw, job, grid, smem, s);
     case 2: return launch_engine_ncw<FMT, T, 2>(ncw, job, grid, smem, s);
@@ -78,10 +81,15 @@ int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, c
     }
 }
 
-// Runs fn(ic<T>) with the task size the plan chose (see task_geo).
-template <class Fn>
+// Runs fn(ic<T>) with the task size the plan chose (see task_geo); LONG: the plan may have
+// asked for long tasks.
+template <bool LONG, class Fn>
 int with_t(const TaskGeo &g, Fn &&fn) {
     if constexpr (QG_FMT == F_Q4_0 || QG_FMT == F_IQ4_NL) {
+        if constexpr (LONG && QG_FMT == F_Q4_0) {
+            if (g.T == 16) return fn(ic<16>{});
+        }
+        if (g.T == 16) return -1;
         if (g.T == 8) return fn(ic<8>{});
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
@@ -117,7 +125,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
                                nullptr, nullptr, c.stream);
     if (rc) return rc;
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
-    rc = with_t(p.geo, [&](auto Tc) {
+    rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
         GemvJob<FMT, T> j;
         set_engine(j, p.ring, p.tpr_x, c.M);
@@ -160,7 +168,7 @@ int ffn_run(const FfnCall &c, int sms) {
     if (rc) return rc;
     for (int ch = 0; ch < p.nchunk; ++ch) {
         const int m0 = ch * p.MC, mc = std::min(p.MC, c.M - m0);
-        rc = with_t(p.geo, [&](auto Tc) {
+        rc = with_t<true>(p.geo, [&](auto Tc) {
             constexpr int T = decltype(Tc)::value;
             FfnGateUpJob<FMT, T> j;
             set_engine(j, p.ring, p.geo.tpr, mc);
@@ -213,7 +221,7 @@ int moe_run(const MoeCall &c, int sms) {
     int rc = launch_router_prep(c.x, c.M, c.H, c.Wr, c.E, logits, log2i(p.gh.XGT), ximg, c.stream);
     if (rc) return rc;
     const size_t eb_gu = (size_t)c.I * p.gh.rb, eb_d = (size_t)c.H * p.gi.rb;
-    rc = with_t(p.gh, [&](auto Tc) {
+    rc = with_t<false>(p.gh, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
         MoeGateUpJob<FMT, T> j;
         set_engine(j, p.gu_ring, p.gh.tpr, 1);
@@ -251,7 +259,7 @@ int moe_run(const MoeCall &c, int sms) {
     if (rc) return rc;
     for (int ch = 0; ch < p.dn_nchunk; ++ch) {
         const int m0 = ch * p.dn_MC, mc = std::min(p.dn_MC, c.M - m0);
-        rc = with_t(p.gi, [&](auto Tc) {
+        rc = with_t<false>(p.gi, [&](auto Tc) {
             constexpr int T = decltype(Tc)::value;
             MoeDownJob<FMT, T> j;
             set_engine(j, p.dn_ring, p.gi.tpr, 1);
@@ -338,11 +346,11 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
 
 template <int FMT>
 int dots_run(const DotsCall &c) {
-    const TaskGeo g = task_geo(FMT, c.K);
+    const TaskGeo g = task_geo(FMT, c.K, c.M == 1);
     if (!g.ok) return -1;
     const long ntask = (long)c.N * g.tpr;
     const int grid = (int)((ntask + HOOK_THREADS - 1) / HOOK_THREADS);
-    with_t(g, [&](auto Tc) {
+    with_t<true>(g, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
         block_dots_kernel<FMT, T><<<grid, HOOK_THREADS, 0, c.stream>>>(c.W, c.xq, c.xs, c.N, c.K, c.M, c.dots,
                                                                        c.aux);

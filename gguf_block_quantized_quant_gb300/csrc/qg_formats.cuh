@@ -120,10 +120,10 @@ __device__ __forceinline__ void cb_lookup8(uint32_t q, uint32_t &lo, uint32_t &h
 }
 
 // ====================================================================== 32-element blocks
-// Q8_0, Q4_0, Q4_1, Q5_0, Q5_1 and IQ4_NL: T blocks per task.  With T == 4 or 8 every
-// block's field offsets are compile-time (a task starts 8-byte, with T == 8 16-byte,
+// Q8_0, Q4_0, Q4_1, Q5_0, Q5_1 and IQ4_NL: T blocks per task.  With T == 4, 8 or 16 every
+// block's field offsets are compile-time (a task starts 8-byte, with T >= 8 16-byte,
 // aligned); with T == 1 a block may start on any even byte and its fields are realigned
-// with run-time byte permutes.  Every decoder works in two phases: load() copies the
+// with run-time byte permutes.  A 16-block (Q4_0) task is held as two halves of 8 blocks.  Every decoder works in two phases: load() copies the
 // task's bytes from shared memory into registers (so that the engine can refill the ring
 // slot at once), compute() decodes them against the activation tiles.
 //
@@ -149,12 +149,36 @@ struct FmtLegacy {
     static constexpr int QS_OFF = FMT == F_Q4_1 ? 4 : FMT == F_Q5_0 ? 6 : FMT == F_Q5_1 ? 8 : 2;
     static constexpr int NQW = FMT == F_Q8_0 ? 8 : 4;  // code words per block
     static constexpr int TASK_BYTES = T * BS;
-    // T >= 4: the task's words plus two (the last block's realignment reads past its end);
-    // T == 1: the words that cover the block from its 4-byte-aligned start
-    static constexpr int WW = T >= 4 ? TASK_BYTES / 4 + 2 : BS / 4 + 2;
+    static_assert(T != 16 || FMT == F_Q4_0, "16-block tasks are Q4_0 only");
+    // T >= 4: per half, its words plus two (the last block's realignment reads past its
+    // end); T == 1: the words that cover the block from its 4-byte-aligned start
+    static constexpr int NH = T == 16 ? 2 : 1, HB = T / NH;
+    static constexpr int HW = HB * BS / 4 + 2;
+    static constexpr int WW = T >= 4 ? NH * HW : BS / 4 + 2;
+
+    // With 16 blocks per task the tasks of consecutive lanes are 288 bytes (18 chunks of 16
+    // bytes) apart, so lanes l and l + 4 would hit the same banks on every 16-byte load;
+    // lanes with bit 2 set load their second half first (a 9-chunk shift), so w[0..HW-1]
+    // holds half swap() and w[HW..] the other one.
+    __device__ __forceinline__ static int swap() { return T == 16 ? (int)((threadIdx.x >> 2) & 1) : 0; }
 
     __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
-        if constexpr (T == 8) {
+        if constexpr (T == 16) {
+            const int sw = swap();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const SAddr hb = addr + (HB * BS) * (h ^ sw);
+#pragma unroll
+                for (int i = 0; i < HB * BS / 16; ++i) {
+                    const uint4 v = lds128(hb + 16 * i);
+                    w[HW * h + 4 * i] = v.x; w[HW * h + 4 * i + 1] = v.y;
+                    w[HW * h + 4 * i + 2] = v.z; w[HW * h + 4 * i + 3] = v.w;
+                }
+                const uint2 v = lds64(hb + HB * BS);
+                w[HW * h + HW - 2] = v.x;
+                w[HW * h + HW - 1] = v.y;
+            }
+        } else if constexpr (T == 8) {
 #pragma unroll
             for (int i = 0; i < TASK_BYTES / 16; ++i) {
                 const uint4 v = lds128(addr + 16 * i);
@@ -240,9 +264,10 @@ struct FmtLegacy {
     __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t a, int, const XT &xt,
                                                    int ntok, Sink &sink) {
         if constexpr (T >= 4) {
+            const int sw = swap();
 #pragma unroll
             for (int b = 0; b < T; ++b) {
-                const int off = BS * b;
+                const int h = b / HB, off = 4 * HW * h + BS * (b % HB);
                 const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
                 const float mv = HAS_M ? half_bits_to_float(word_at(w, off + 2)) : 0.0f;
                 const uint32_t qh = HAS_QH ? word_at(w, off + QH_OFF) : 0u;
@@ -251,7 +276,7 @@ struct FmtLegacy {
                 for (int k = 0; k < NQW; ++k) c[k] = word_at(w, off + QS_OFF + 4 * k);
 #pragma unroll
                 for (int m = 0; m < Sink::MT; ++m)
-                    if (m < ntok) unit(c, qh, d, mv, m, b, xt.tile(m), sink);
+                    if (m < ntok) unit(c, qh, d, mv, m, HB * (h ^ sw) + b % HB, xt.tile(m), sink);
             }
         } else {
             const float d = half_bits_to_float(rword(w, a, 0));

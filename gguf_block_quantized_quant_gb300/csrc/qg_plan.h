@@ -48,8 +48,12 @@ inline int log2i(int v) {
 }
 
 // Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
-//   Q4_0, IQ4_NL: 8, 4 or 1 blocks per task; Q8_0, Q4_1, Q5_0, Q5_1: 4 or 1; Q4_K, IQ4_XS:
-//   2 or 1 superblocks (the largest that divides the row); Q5_K, Q6_K: one whole superblock.
+//   Q4_0: 16 (only with long_tasks), 8, 4 or 1 blocks per task; IQ4_NL: 8, 4 or 1; Q8_0,
+//   Q4_1, Q5_0, Q5_1: 4 or 1; Q4_K, IQ4_XS: 2 or 1 superblocks (the largest that divides the
+//   row); Q5_K, Q6_K: one whole superblock.
+// long_tasks asks for 16-block Q4_0 tasks (288 bytes, the size of two Q4_K superblocks): with
+// one token per lane they leave the lane's decode fewer, longer loads and let the 12-warp
+// engine run; with several tokens per lane the 8-block tasks on 16 warps were faster.
 struct TaskGeo {
     bool ok = false;
     int T = 1, TPB = 1, BPT = 1, XGT = 8, nbr = 0, gpr = 0, tpr = 0, stride = 0, bs = 0;
@@ -57,7 +61,7 @@ struct TaskGeo {
     uint32_t bytes_of(int ntask) const { return (uint32_t)(((ntask + TPB - 1) / TPB) * BPT * bs); }
     int task_bytes() const { return BPT * bs / TPB; }
 };
-inline TaskGeo task_geo(int fmt, int K) {
+inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     TaskGeo g;
     FmtInfo f;
     if (!fmt_info(fmt, f) || K < f.qk || K % f.qk) return g;
@@ -65,7 +69,10 @@ inline TaskGeo task_geo(int fmt, int K) {
     g.nbr = K / f.qk;
     g.rb = (uint32_t)(g.nbr * f.bs);
     if (f.qk == 32) {
-        g.T = ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0) ? 8 : g.nbr % 4 == 0 ? 4 : 1;
+        g.T = (long_tasks && fmt == 2 && g.nbr % 16 == 0)           ? 16
+              : ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0) ? 8
+              : g.nbr % 4 == 0                              ? 4
+                                                            : 1;
         g.BPT = g.T;
         g.XGT = g.T;
         g.TPB = 1;
@@ -146,7 +153,7 @@ struct GemvPlan {
 
 inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     GemvPlan p;
-    p.geo = task_geo(fmt, K);
+    p.geo = task_geo(fmt, K, pick_mt(M) == 1);
     const TaskGeo &g = p.geo;
     if (!g.ok || N < 1 || M < 1 || M > M_MAX || sms < 1) return p;
     p.KS = N < G_PLAN / 2 ? std::min(g.gpr, (G_PLAN + N - 1) / N) : 1;
@@ -186,9 +193,9 @@ struct FfnPlan {
 
 inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     FfnPlan p;
-    p.geo = task_geo(fmt, H);
+    p.geo = task_geo(fmt, H, M == 1);
     const TaskGeo &g = p.geo;
-    if (!g.ok || !task_geo(fmt, I).ok || M < 1 || M > M_MAX || sms < 1) return p;
+    if (!g.ok || !task_geo(fmt, I, false).ok || M < 1 || M > M_MAX || sms < 1) return p;
     const long tiles = (long)g.tpr * g.stride;
     p.MC = (int)std::min<long>(M, (long)XCAP / tiles);
     if (p.MC < 1) return p;
@@ -226,8 +233,8 @@ struct MoePlan {
 
 inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) {
     MoePlan p;
-    p.gh = task_geo(fmt, H);
-    p.gi = task_geo(fmt, I);
+    p.gh = task_geo(fmt, H, false);
+    p.gi = task_geo(fmt, I, false);
     if (!p.gh.ok || !p.gi.ok || M < 1 || M > M_MAX || E < 1 || E > 1024 || topk < 1 || topk > 16 || topk > E ||
         sms < 1 || M * topk > SCRATCH_INTS)
         return p;

@@ -102,6 +102,9 @@ def test_gemv_q_prequantized_matches_oracle(qg, fmt):
     (synth.Q4_K, 300, 8192, 16),     # 16 tokens of activation tiles exceed one CTA: split along K
     (synth.IQ4_XS, 3, 65536, 4),     # split-K over many slices + segments
     (synth.Q4_0, 4099, 96, 1),       # tiny rows packed 8 per warp step, odd N
+    (synth.Q4_0, 1037, 512, 1),      # one token: one 16-block task per row (two swapped halves)
+    (synth.Q4_0, 333, 2560, 1),      # one token: 5 tasks of 16 blocks per row, rows wrap in a step
+    (synth.Q4_0, 333, 2560, 2),      # two tokens on the same rows: 8-block tasks
 ])
 def test_gemv_layout_paths(qg, fmt, N, K, M):
     g = np.random.default_rng(N + K + M)
