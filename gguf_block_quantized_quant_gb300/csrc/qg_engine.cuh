@@ -42,13 +42,15 @@ constexpr int SCRATCH_INTS = 256;  // prologue scratch (MoE top-k ids)
 constexpr int BND_FLOATS = 1 + 16; // boundary entry: row, then one sum per token
 
 // Unsigned division by a run-time constant (n < 2^31, d < 2^31): 32-bit reciprocal
-// estimate, corrected once.
+// estimate m = ceil(2^32 / d) (any m in [2^32 / d, 2^32 / d + 2) gives a quotient that is
+// exact or one too large for n < 2^31), corrected once.  m comes from a 32-bit division:
+// (2^32 - 1) / d + 1 equals ceil(2^32 / d) for every d > 1.
 struct FastDiv {
     uint32_t d, m;
     __host__ __device__ static FastDiv make(uint32_t dv) {
         FastDiv f;
         f.d = dv;
-        f.m = dv <= 1 ? 0u : (uint32_t)((0x100000000ull + dv - 1) / dv);
+        f.m = dv <= 1 ? 0u : 0xffffffffu / dv + 1u;
         return f;
     }
     __device__ __forceinline__ uint32_t div(uint32_t n) const {

@@ -70,6 +70,15 @@ struct Tile {
     static constexpr int D = 32 * XGT, S = D + 4 * XGT, H = S + 4 * XGT, Q = H + 4 * XGT, STRIDE = tile_stride(XGT);
 };
 
+// Four consecutive 32-bit fields of a tile (d, s, h or ds of units u..u+3, u a multiple
+// of 4): one 16-byte load, which keeps the lanes of a quarter-warp on distinct banks (the
+// tile stride is an odd number of 16-byte chunks) where 32-bit loads of lanes 8 tiles
+// apart would share a bank.
+__device__ __forceinline__ void ld4(SAddr a, uint32_t *v) {
+    const uint4 p = lds128(a);
+    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+}
+
 __device__ __forceinline__ void ldx8(SAddr a, uint32_t (&x)[8]) {
     const uint4 p = lds128(a), q = lds128(a + 16);
     x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
@@ -207,13 +216,18 @@ struct FmtLegacy {
         return prmt(w[o >> 2], w[(o >> 2) + 1], 0x3210u + 0x2222u * ((a + (uint32_t)(o & 3)) >> 1));
     }
 
+    // Whether a unit needs the activation sum s: the code offset of Q4_0 and Q5_0 is
+    // applied through it, and the test hook reports it for the additive-min formats.
+    template <class Sink>
+    static constexpr bool needs_s() { return FMT == F_Q4_0 || FMT == F_Q5_0 || (Sink::DOTS && HAS_M); }
+
+    // One block against token m's tile, unit u; xd, xs, xq: the unit's activation d, s, ds.
     template <class Sink>
     __device__ __forceinline__ static void unit(const uint32_t (&c)[8], uint32_t qh, float d, float mv, int m, int u,
-                                                SAddr tile, Sink &sink) {
-        using TL = Tile<XGT>;
+                                                SAddr tile, float xd, int xs, float xq, Sink &sink) {
         uint32_t x[8];
         ldx8(tile + 32 * u, x);
-        int dot = 0, xs = 0;
+        int dot = 0;
         if constexpr (FMT == F_Q8_0) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) dot = dp4a(c[k], x[k], dot);
@@ -225,10 +239,7 @@ struct FmtLegacy {
                 hi = dp4a_us(c[k] & 0xf0f0f0f0u, x[4 + k], hi);
             }
             dot = lo + (hi >> 4);
-            if constexpr (FMT == F_Q4_0) {
-                xs = (int)lds32(tile + TL::S + 4 * u);
-                dot -= 8 * xs;
-            }
+            if constexpr (FMT == F_Q4_0) dot -= 8 * xs;
         } else if constexpr (HAS_QH) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -237,10 +248,7 @@ struct FmtLegacy {
                 dot = dp4a(lo, x[k], dot);
                 dot = dp4a(hi, x[4 + k], dot);
             }
-            if constexpr (FMT == F_Q5_0) {
-                xs = (int)lds32(tile + TL::S + 4 * u);
-                dot -= 16 * xs;
-            }
+            if constexpr (FMT == F_Q5_0) dot -= 16 * xs;
         } else {  // IQ4_NL
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -251,11 +259,10 @@ struct FmtLegacy {
             }
         }
         if constexpr (Sink::DOTS) {
-            if constexpr (HAS_M) xs = (int)lds32(tile + TL::S + 4 * u);
             sink.unit(m, u, dot, xs);
         } else {
-            float v = d * ldsf(tile + TL::D + 4 * u) * (float)dot;
-            if constexpr (HAS_M) v = fmaf(mv, ldsf(tile + TL::Q + 4 * u), v);
+            float v = d * xd * (float)dot;
+            if constexpr (HAS_M) v = fmaf(mv, xq, v);
             sink.add(m, v);
         }
     }
@@ -263,20 +270,39 @@ struct FmtLegacy {
     template <class Sink>
     __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t a, int, const XT &xt,
                                                    int ntok, Sink &sink) {
+        using TL = Tile<XGT>;
         if constexpr (T >= 4) {
             const int sw = swap();
+            // groups of 4 blocks (units u0..u0+3 of one half): their activation d, s and ds
+            // come in one 16-byte load each per token
 #pragma unroll
-            for (int b = 0; b < T; ++b) {
-                const int h = b / HB, off = 4 * HW * h + BS * (b % HB);
-                const float d = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
-                const float mv = HAS_M ? half_bits_to_float(word_at(w, off + 2)) : 0.0f;
-                const uint32_t qh = HAS_QH ? word_at(w, off + QH_OFF) : 0u;
-                uint32_t c[8];
+            for (int g = 0; g < T / 4; ++g) {
+                float d[4], mv[4];
+                uint32_t qh[4], c[4][8];
 #pragma unroll
-                for (int k = 0; k < NQW; ++k) c[k] = word_at(w, off + QS_OFF + 4 * k);
+                for (int i = 0; i < 4; ++i) {
+                    const int b = 4 * g + i, off = 4 * HW * (b / HB) + BS * (b % HB);
+                    d[i] = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                    mv[i] = HAS_M ? half_bits_to_float(word_at(w, off + 2)) : 0.0f;
+                    qh[i] = HAS_QH ? word_at(w, off + QH_OFF) : 0u;
 #pragma unroll
-                for (int m = 0; m < Sink::MT; ++m)
-                    if (m < ntok) unit(c, qh, d, mv, m, HB * (h ^ sw) + b % HB, xt.tile(m), sink);
+                    for (int k = 0; k < NQW; ++k) c[i][k] = word_at(w, off + QS_OFF + 4 * k);
+                }
+                const int u0 = HB * ((4 * g / HB) ^ sw) + (4 * g) % HB;
+#pragma unroll
+                for (int m = 0; m < Sink::MT; ++m) {
+                    if (m < ntok) {
+                        const SAddr tl = xt.tile(m);
+                        uint32_t xd[4], xs[4] = {0u, 0u, 0u, 0u}, xq[4] = {0u, 0u, 0u, 0u};
+                        ld4(tl + TL::D + 4 * u0, xd);
+                        if constexpr (needs_s<Sink>()) ld4(tl + TL::S + 4 * u0, xs);
+                        if constexpr (HAS_M && !Sink::DOTS) ld4(tl + TL::Q + 4 * u0, xq);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            unit(c[i], qh[i], d[i], mv[i], m, u0 + i, tl, __uint_as_float(xd[i]), (int)xs[i],
+                                 __uint_as_float(xq[i]), sink);
+                    }
+                }
             }
         } else {
             const float d = half_bits_to_float(rword(w, a, 0));
@@ -286,8 +312,14 @@ struct FmtLegacy {
 #pragma unroll
             for (int k = 0; k < NQW; ++k) c[k] = rword(w, a, QS_OFF + 4 * k);
 #pragma unroll
-            for (int m = 0; m < Sink::MT; ++m)
-                if (m < ntok) unit(c, qh, d, mv, m, 0, xt.tile(m), sink);
+            for (int m = 0; m < Sink::MT; ++m) {
+                if (m < ntok) {
+                    const SAddr tl = xt.tile(m);
+                    const int xs = needs_s<Sink>() ? (int)lds32(tl + TL::S) : 0;
+                    const float xq = HAS_M && !Sink::DOTS ? ldsf(tl + TL::Q) : 0.0f;
+                    unit(c, qh, d, mv, m, 0, tl, ldsf(tl + TL::D), xs, xq, sink);
+                }
+            }
         }
     }
 
@@ -338,21 +370,29 @@ struct FmtQ4K {
         const uint32_t S03 = w[1] & 0x3f3f3f3fu, M03 = w[2] & 0x3f3f3f3fu;
         const uint32_t S47 = (w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u);
         const uint32_t M47 = ((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u);
-        float A[MT], B[MT];
+        const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
 #pragma unroll
-        for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            // the 8 units' activation d and ds: 16-byte loads
+            uint32_t xd[8], xq[8];
+            if constexpr (!Sink::DOTS) {
+                ld4(t + TL::D + 4 * u0, xd);
+                ld4(t + TL::D + 4 * u0 + 16, xd + 4);
+                ld4(t + TL::Q + 4 * u0, xq);
+                ld4(t + TL::Q + 4 * u0 + 16, xq + 4);
+            }
+            float A = 0.0f, B = 0.0f;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const uint32_t *q = w + 4 + 8 * p;
-            const uint32_t Sw = p < 2 ? S03 : S47, Mw = p < 2 ? M03 : M47;
-            const int k0 = 2 * (p & 1);
-            const int sc0 = byte_of(Sw, k0), sc1 = byte_of(Sw, k0 + 1);
-            const float mn0 = (float)byte_of(Mw, k0), mn1 = (float)byte_of(Mw, k0 + 1);
-            const int u = u0 + 2 * p;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < ntok) {
-                    const SAddr t = xt.tile(m);
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t *q = w + 4 + 8 * p;
+                const uint32_t Sw = p < 2 ? S03 : S47, Mw = p < 2 ? M03 : M47;
+                const int k0 = 2 * (p & 1);
+                const int sc0 = byte_of(Sw, k0), sc1 = byte_of(Sw, k0 + 1);
+                const float mn0 = (float)byte_of(Mw, k0), mn1 = (float)byte_of(Mw, k0 + 1);
+                const int u = u0 + 2 * p;
+                {
                     uint32_t xa[8], xb[8];
                     ldx8(t + 32 * u, xa);
                     ldx8(t + 32 * u + 32, xb);
@@ -368,20 +408,14 @@ struct FmtQ4K {
                         sink.unit(m, u, da, (int)xs.x);
                         sink.unit(m, u + 1, db, (int)xs.y);
                     } else {
-                        const uint2 xd = lds64(t + TL::D + 4 * u), xq = lds64(t + TL::Q + 4 * u);
-                        A[m] = fmaf(__uint_as_float(xd.x), (float)(sc0 * da), A[m]);
-                        A[m] = fmaf(__uint_as_float(xd.y), (float)(sc1 * db), A[m]);
-                        B[m] = fmaf(__uint_as_float(xq.x), mn0, B[m]);
-                        B[m] = fmaf(__uint_as_float(xq.y), mn1, B[m]);
+                        A = fmaf(__uint_as_float(xd[2 * p]), (float)(sc0 * da), A);
+                        A = fmaf(__uint_as_float(xd[2 * p + 1]), (float)(sc1 * db), A);
+                        B = fmaf(__uint_as_float(xq[2 * p]), mn0, B);
+                        B = fmaf(__uint_as_float(xq[2 * p + 1]), mn1, B);
                     }
                 }
             }
-        }
-        if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
+            if constexpr (!Sink::DOTS) sink.add(m, fmaf(d, A, -dmin * B));
         }
     }
 
@@ -424,58 +458,59 @@ struct FmtQ5K {
         using TL = Tile<XGT>;
         constexpr int MT = Sink::MT;
         const uint32_t *qh = w + 4;
-        float A[MT], B[MT];
+        const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
 #pragma unroll
-        for (int m = 0; m < MT; ++m) A[m] = B[m] = 0.0f;
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            // the 8 units' activation d and ds: 16-byte loads
+            uint32_t xd[8], xq[8];
+            if constexpr (!Sink::DOTS) {
+                ld4(t + TL::D, xd);
+                ld4(t + TL::D + 16, xd + 4);
+                ld4(t + TL::Q, xq);
+                ld4(t + TL::Q + 16, xq + 4);
+            }
+            float A = 0.0f, B = 0.0f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const uint32_t Sw = hf ? ((w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u)) : (w[1] & 0x3f3f3f3fu);
-            const uint32_t Mw = hf ? (((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u)) : (w[2] & 0x3f3f3f3fu);
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t Sw = hf ? ((w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u)) : (w[1] & 0x3f3f3f3fu);
+                const uint32_t Mw =
+                    hf ? (((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u)) : (w[2] & 0x3f3f3f3fu);
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-                const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
-                const uint32_t *q = w + 12 + 8 * (2 * hf + pp);
-                uint32_t c0[8], c1[8];
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
+                    const uint32_t *q = w + 12 + 8 * (2 * hf + pp);
+                    uint32_t c0[8], c1[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
-                    c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
-                }
-                const int sc0 = byte_of(Sw, 2 * pp), sc1 = byte_of(Sw, 2 * pp + 1);
-                const float mn0 = (float)byte_of(Mw, 2 * pp), mn1 = (float)byte_of(Mw, 2 * pp + 1);
+                    for (int k = 0; k < 8; ++k) {
+                        c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
+                        c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
+                    }
+                    const int sc0 = byte_of(Sw, 2 * pp), sc1 = byte_of(Sw, 2 * pp + 1);
+                    const float mn0 = (float)byte_of(Mw, 2 * pp), mn1 = (float)byte_of(Mw, 2 * pp + 1);
+                    uint32_t xa[8], xb[8];
+                    ldx8(t + 32 * j0, xa);
+                    ldx8(t + 32 * j0 + 32, xb);
+                    int da = 0, db = 0;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (m < ntok) {
-                        const SAddr t = xt.tile(m);
-                        uint32_t xa[8], xb[8];
-                        ldx8(t + 32 * j0, xa);
-                        ldx8(t + 32 * j0 + 32, xb);
-                        int da = 0, db = 0;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            da = dp4a(c0[k], xa[k], da);
-                            db = dp4a(c1[k], xb[k], db);
-                        }
-                        if constexpr (Sink::DOTS) {
-                            const uint2 xs = lds64(t + TL::S + 4 * j0);
-                            sink.unit(m, j0, da, (int)xs.x);
-                            sink.unit(m, j0 + 1, db, (int)xs.y);
-                        } else {
-                            const uint2 xd = lds64(t + TL::D + 4 * j0), xq = lds64(t + TL::Q + 4 * j0);
-                            A[m] = fmaf(__uint_as_float(xd.x), (float)(sc0 * da), A[m]);
-                            A[m] = fmaf(__uint_as_float(xd.y), (float)(sc1 * db), A[m]);
-                            B[m] = fmaf(__uint_as_float(xq.x), mn0, B[m]);
-                            B[m] = fmaf(__uint_as_float(xq.y), mn1, B[m]);
-                        }
+                    for (int k = 0; k < 8; ++k) {
+                        da = dp4a(c0[k], xa[k], da);
+                        db = dp4a(c1[k], xb[k], db);
+                    }
+                    if constexpr (Sink::DOTS) {
+                        const uint2 xs = lds64(t + TL::S + 4 * j0);
+                        sink.unit(m, j0, da, (int)xs.x);
+                        sink.unit(m, j0 + 1, db, (int)xs.y);
+                    } else {
+                        A = fmaf(__uint_as_float(xd[j0]), (float)(sc0 * da), A);
+                        A = fmaf(__uint_as_float(xd[j0 + 1]), (float)(sc1 * db), A);
+                        B = fmaf(__uint_as_float(xq[j0]), mn0, B);
+                        B = fmaf(__uint_as_float(xq[j0 + 1]), mn1, B);
                     }
                 }
             }
-        }
-        if constexpr (!Sink::DOTS) {
-            const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < ntok) sink.add(m, fmaf(d, A[m], -dmin * B[m]));
+            if constexpr (!Sink::DOTS) sink.add(m, fmaf(d, A, -dmin * B));
         }
     }
 
@@ -523,6 +558,19 @@ struct FmtQ6K {
             // sub-scales 8hf..8hf+7 start at byte 192 + 8hf of the block
             const uint32_t scA = prmt(w[48 + 2 * hf], w[49 + 2 * hf], sel);  // sc[8hf+0..3]
             const uint32_t scB = prmt(w[49 + 2 * hf], w[50 + 2 * hf], sel);  // sc[8hf+4..7]
+            // up to 4 tokens: the half's activation d and h of every token in two 16-byte
+            // loads (more tokens: one 32-bit load per unit, to spare registers)
+            constexpr bool VEC = MT <= 4;
+            uint32_t xdv[VEC ? MT : 1][4], xhv[VEC ? MT : 1][4];
+            if constexpr (VEC && !Sink::DOTS) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < ntok) {
+                        ld4(xt.tile(m) + TL::D + 16 * hf, xdv[m]);
+                        ld4(xt.tile(m) + TL::H + 16 * hf, xhv[m]);
+                    }
+                }
+            }
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
                 uint32_t lw[8];
@@ -545,7 +593,7 @@ struct FmtQ6K {
                             const SAddr tl = xt.tile(m);
                             uint32_t x[8];
                             ldx8(tl + 32 * u, x);
-                            const uint32_t xh = lds32(tl + TL::H + 4 * u);
+                            const uint32_t xh = VEC && !Sink::DOTS ? xhv[VEC ? m : 0][t] : lds32(tl + TL::H + 4 * u);
                             int lo = 0, hi = 0;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
@@ -556,7 +604,8 @@ struct FmtQ6K {
                             if constexpr (Sink::DOTS) {
                                 sink.unit(m, u, dot, 0);
                             } else {
-                                A[m] = fmaf(ldsf(tl + TL::D + 4 * u), (float)dot, A[m]);
+                                const float xd = VEC ? __uint_as_float(xdv[VEC ? m : 0][t]) : ldsf(tl + TL::D + 4 * u);
+                                A[m] = fmaf(xd, (float)dot, A[m]);
                             }
                         }
                     }
@@ -614,6 +663,19 @@ struct FmtIQ4XS {
         float A[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) A[m] = 0.0f;
+        // up to 4 tokens: the 8 units' activation d of every token in two 16-byte loads
+        // (more tokens: one 32-bit load per unit, to spare registers)
+        constexpr bool VEC = MT <= 4;
+        uint32_t xdv[VEC ? MT : 1][8];
+        if constexpr (VEC && !Sink::DOTS) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < ntok) {
+                    ld4(xt.tile(m) + TL::D + 4 * u0, xdv[m]);
+                    ld4(xt.tile(m) + TL::D + 4 * u0 + 16, xdv[m] + 4);
+                }
+            }
+        }
 #pragma unroll
         for (int ib = 0; ib < 8; ++ib) {
             const int ls = (int)(((h1 >> (4 * ib)) & 15u) | (((h0 >> (16 + 2 * ib)) & 3u) << 4));
@@ -633,7 +695,8 @@ struct FmtIQ4XS {
                     if constexpr (Sink::DOTS) {
                         sink.unit(m, u, dot, 0);
                     } else {
-                        A[m] = fmaf(ldsf(t + TL::D + 4 * u), (float)((ls - 32) * dot), A[m]);
+                        const float xd = VEC ? __uint_as_float(xdv[VEC ? m : 0][ib]) : ldsf(t + TL::D + 4 * u);
+                        A[m] = fmaf(xd, (float)((ls - 32) * dot), A[m]);
                     }
                 }
             }
