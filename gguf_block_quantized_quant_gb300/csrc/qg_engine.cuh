@@ -61,6 +61,16 @@ struct FastDiv {
     }
 };
 
+// floor(n * i / parts) for 0 <= i <= parts (the start of part i when n items are split into
+// parts nearly equal parts): 32-bit arithmetic whenever n * parts < 2^32, which holds for
+// every planned shape (a 64-bit division is a long call on the GPU, and every thread of a
+// CTA computes its range before its first copy).
+__device__ __forceinline__ int split_point(long n, int i, int parts) {
+    if ((unsigned long long)n * (unsigned long long)parts < (1ull << 32))
+        return (int)((uint32_t)n * (uint32_t)i / (uint32_t)parts);
+    return (int)(n * i / parts);
+}
+
 // Shared memory of the engine besides the ring, the activation tiles and the job area:
 // boundary sums (2 per warp), prologue scratch, S + 1 mbarriers, piece headers (per slot:
 // NPIECE_MAX piece addresses and the end of the tasks the pieces cover).
@@ -117,22 +127,18 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
     int *scratch = reinterpret_cast<int *>(smem + (scr - ring));
     float *jarea = reinterpret_cast<float *>(smem + (ja - ring));
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(full_bar(s), 1);
-        mbar_init(xbar, 1);
-        fence_mbar_init();
-    }
-    if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
-    job.init(jarea, tid);
     // the next kernel in the stream (the next call's activation preparation, launched as a
     // programmatic dependent) may start now: it waits for this grid to finish before it
     // touches any data, and its own dependent engine takes each SM this CTA leaves
     griddep_launch_dependents();
-    if constexpr (Job::HAS_PROLOGUE) {
-        __syncthreads();
-        if (warp == 0) job.prologue(lane, scratch);
+    // every warp initialises the barriers of its own ring slots (so that it can issue its
+    // first copies before the CTA-wide barrier), warp 0 also the activation barrier
+    if (lane == 0) {
+        for (int j = 0; j < D; ++j) mbar_init(full_bar(j * NCW + warp), 1);
+        if (warp == 0) mbar_init(xbar, 1);
+        fence_mbar_init();
     }
-    __syncthreads();
+    __syncwarp();
 
     // this CTA's tasks and this warp's range (whole blocks)
     const typename Job::Ctx cx = job.ctx();
@@ -214,9 +220,20 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
         if (lane == 0) mbar_arrive_expect_tx(fbar, tx);
     };
 
-    // the first D stages: the slots are free
+    // the first D stages: the slots are free.  A job with a prologue (whose copies depend
+    // on it) issues them after the CTA-wide set-up, any other job before it.
     const int jfirst = min(D, nchunk);
-    for (int j = 0; j < jfirst; ++j) issue(j);
+    if constexpr (!Job::HAS_PROLOGUE)
+        for (int j = 0; j < jfirst; ++j) issue(j);
+    if (tid < NCW * 2) bsum[tid * BND_FLOATS] = __int_as_float(-1);
+    job.init(jarea, tid);
+    if constexpr (Job::HAS_PROLOGUE) {
+        __syncthreads();
+        if (warp == 0) job.prologue(lane, scratch);
+    }
+    __syncthreads();
+    if constexpr (Job::HAS_PROLOGUE)
+        for (int j = 0; j < jfirst; ++j) issue(j);
     if (warp == 0) {
         if (lane == 0) {
             griddep_wait();

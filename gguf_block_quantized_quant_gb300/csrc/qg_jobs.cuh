@@ -54,10 +54,10 @@ struct GemvJob : EngineFields {
         Ctx c;
         const int g = KS == 1 ? (int)blockIdx.x : (int)blockIdx.x / KS;
         c.ks = KS == 1 ? 0 : (int)blockIdx.x - g * KS;
-        c.t0 = (int)((long)c.ks * gpr / KS) * F::TPB;
-        c.tpr = (int)((long)(c.ks + 1) * gpr / KS) * F::TPB - c.t0;
-        c.o0 = (int)((long)g * N / groups);
-        c.o1 = (int)((long)(g + 1) * N / groups);
+        c.t0 = split_point(gpr, c.ks, KS) * F::TPB;
+        c.tpr = split_point(gpr, c.ks + 1, KS) * F::TPB - c.t0;
+        c.o0 = split_point(N, g, groups);
+        c.o1 = split_point(N, g + 1, groups);
         c.out = out + (long)c.ks * slice_stride;
         return c;
     }
@@ -98,8 +98,8 @@ struct FfnGateUpJob : EngineFields {
     struct Ctx {};
     __device__ Ctx ctx() const { return {}; }
     __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
-        o0 = (int)((long)blockIdx.x * 2 * I / gridDim.x);
-        o1 = (int)((long)(blockIdx.x + 1) * 2 * I / gridDim.x);
+        o0 = split_point(2L * I, (int)blockIdx.x, (int)gridDim.x);
+        o1 = split_point(2L * I, (int)blockIdx.x + 1, (int)gridDim.x);
         tpr = tpr_x;
         grp = I;
     }
@@ -152,8 +152,8 @@ struct MoeGateUpJob : EngineFields {
     __device__ Ctx ctx() const { return {}; }
     __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
         const long P = (long)M * slots() * 2 * I;
-        o0 = (int)(P * blockIdx.x / gridDim.x);
-        o1 = (int)(P * (blockIdx.x + 1) / gridDim.x);
+        o0 = split_point(P, (int)blockIdx.x, (int)gridDim.x);
+        o1 = split_point(P, (int)blockIdx.x + 1, (int)gridDim.x);
         tpr = tpr_x;
         grp = I;
     }
@@ -267,8 +267,8 @@ struct MoeDownJob : EngineFields {
     };
     __device__ Ctx ctx() const {
         Ctx c;
-        c.n0 = (int)((long)blockIdx.x * H / gridDim.x);
-        c.nloc = (int)((long)(blockIdx.x + 1) * H / gridDim.x) - c.n0;
+        c.n0 = split_point(H, (int)blockIdx.x, (int)gridDim.x);
+        c.nloc = split_point(H, (int)blockIdx.x + 1, (int)gridDim.x) - c.n0;
         c.dnloc = FastDiv::make((uint32_t)c.nloc);
         c.dslots = FastDiv::make((uint32_t)slots());
         return c;
