@@ -23,10 +23,13 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_NL, IQ4_XS = 2, 3, 6, 7, 8, 12, 13, 14, 20, 23
-FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K,
-           "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
-_QK = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_NL: 32, IQ4_XS: 256}
-_BS = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_NL: 18, IQ4_XS: 136}
+Q2_K, Q3_K = 10, 11
+FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q2_K": Q2_K, "Q3_K": Q3_K,
+           "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
+_QK = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K: 256, Q4_K: 256, Q5_K: 256, Q6_K: 256,
+       IQ4_NL: 32, IQ4_XS: 256}
+_BS = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176, Q6_K: 210,
+       IQ4_NL: 18, IQ4_XS: 136}
 
 _lib = None
 
@@ -52,6 +55,7 @@ def _configure(L):
     L.or_half_to_double.argtypes = [ctypes.c_uint16]
     L.or_half_to_double.restype = ctypes.c_double
     L.or_decode_block.argtypes = [i, P, P, P, P, P]
+    L.or_decode_block_mc.argtypes = [i, P, P, P, P, P, P]
     L.or_dequant_matrix.argtypes = [i, P, i, i, P]
     L.or_quantize_act.argtypes = [P, i, i, P, P, P]
     L.or_block_dots.argtypes = [i, P, P, P, i, i, i, P, P]
@@ -154,17 +158,19 @@ def half_to_double(bits: int) -> float:
     return float(lib().or_half_to_double(int(bits)))
 
 
-def decode_block(fmt, blk):
-    """Returns (w fp64[QK], codes int32[QK], A fp64[QK/32], B fp64[QK/32])."""
+def decode_block(fmt, blk, with_mc: bool = False):
+    """Returns (w fp64[QK], codes int32[QK], A fp64[QK/32], B fp64[QK/32]), and the min
+    codes int32[QK] as a fifth item when with_mc."""
     blk = _u8(blk)
     assert blk.size == _BS[fmt]
     qk = _QK[fmt]
     w = np.zeros(qk, np.float64)
     c = np.zeros(qk, np.int32)
+    mc = np.zeros(qk, np.int32)
     A = np.zeros(qk // 32, np.float64)
     B = np.zeros(qk // 32, np.float64)
-    lib().or_decode_block(fmt, _p(blk), _p(w), _p(c), _p(A), _p(B))
-    return w, c, A, B
+    lib().or_decode_block_mc(fmt, _p(blk), _p(w), _p(c), _p(mc), _p(A), _p(B))
+    return (w, c, A, B, mc) if with_mc else (w, c, A, B)
 
 
 def dequant_matrix(fmt, W, N, K):

@@ -30,7 +30,7 @@ int or_get_threads(void) {
 int or_block_elems(int fmt) {
     switch (fmt) {
     case OR_Q4_0: case OR_Q4_1: case OR_Q5_0: case OR_Q5_1: case OR_Q8_0: case OR_IQ4_NL: return 32;
-    case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: case OR_IQ4_XS: return 256;
+    case OR_Q2_K: case OR_Q3_K: case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: case OR_IQ4_XS: return 256;
     default: return 0;
     }
 }
@@ -43,6 +43,8 @@ int or_block_bytes(int fmt) {
     case OR_Q5_1: return 24;    /* fp16 d, fp16 m, 32 fifth bits, nibbles     */
     case OR_IQ4_NL: return 18;  /* fp16 d + 16 bytes of codebook indices      */
     case OR_Q8_0: return 34;    /* fp16 d + 32 int8                          */
+    case OR_Q2_K: return 84;    /* 16 B 4-bit scale|min, 64 B 2-bit codes, d, dmin */
+    case OR_Q3_K: return 110;   /* 32 B high bits, 64 B 2-bit codes, 12 B scales, d */
     case OR_Q4_K: return 144;   /* d, dmin, 12 B scales/mins, 128 B nibbles   */
     case OR_Q5_K: return 176;   /* Q4_K fields + 32 B of fifth bits           */
     case OR_Q6_K: return 210;   /* 128 B ql, 64 B qh, 16 int8 scales, fp16 d  */
@@ -86,12 +88,26 @@ static void kquant_scale_min(const uint8_t *sc12, int j, int *S, int *M) {
     }
 }
 
+/* Q3_K: the signed 6-bit scale of 16-element sub-block i (0..15), packed in 12 bytes:
+ * its low 4 bits are the low nibble of byte i (i < 8) or the high nibble of byte i-8,
+ * its high 2 bits are bits 2*(i/4), 2*(i/4)+1 of byte 8 + i%4; the value is that - 32. */
+static int q3k_scale(const uint8_t *sc12, int i) {
+    int low4 = i < 8 ? (sc12[i] & 15) : (sc12[i - 8] >> 4);
+    int high2 = (sc12[8 + i % 4] >> (2 * (i / 4))) & 3;
+    return (low4 | (high2 << 4)) - 32;
+}
+
 void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double *A, double *B) {
+    or_decode_block_mc(fmt, blk, w, c, NULL, A, B);
+}
+
+void or_decode_block_mc(int fmt, const uint8_t *blk, double *w, int32_t *c, int32_t *mc, double *A, double *B) {
     int QK = or_block_elems(fmt);
     for (int e = 0; e < QK; ++e) {
         int u = e / 32;        /* 32-element unit (= one activation block) */
         int code = 0;          /* contract code c_e                        */
-        double a = 0, b = 0;   /* w_e = a * c_e - b                        */
+        int mcode = 1;         /* min code mc_e                            */
+        double a = 0, b = 0;   /* w_e = a * c_e - b * mc_e                 */
         switch (fmt) {
         case OR_Q8_0: {
             a = rd_half(blk);
@@ -148,6 +164,30 @@ void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double 
             b = dmin * M;
             break;
         }
+        case OR_Q2_K:
+        case OR_Q3_K: {
+            /* Element e = 128h + 32j + l: its 2-bit code is bits 2j, 2j+1 of qs[32h + l];
+             * it belongs to 16-element sub-block e/16.
+             * Q2_K: scales[16] @0 (low nibble: scale, high nibble: min), qs @16, fp16 d @80,
+             *       fp16 dmin @82; w = d * scale * code - dmin * min.
+             * Q3_K: hmask[32] @0, qs @32, 12 B packed scales @96, fp16 d @108; the third bit of
+             *       the code is bit 4h + j of hmask[l], and a clear bit subtracts 4:
+             *       w = d * (scale - 32) * (code - 4 * (1 - bit)). */
+            int h = e / 128, r = e % 128, j = r / 32, l = r % 32, sb = e / 16;
+            if (fmt == OR_Q2_K) {
+                int q2 = (blk[16 + 32 * h + l] >> (2 * j)) & 3;
+                code = (blk[sb] & 15) * q2;
+                mcode = blk[sb] >> 4;
+                a = rd_half(blk + 80);
+                b = rd_half(blk + 82);
+            } else {
+                int q2 = (blk[32 + 32 * h + l] >> (2 * j)) & 3;
+                int hb = (blk[l] >> (4 * h + j)) & 1;
+                code = q3k_scale(blk + 96, sb) * (q2 - (hb ? 0 : 4));
+                a = rd_half(blk + 108);
+            }
+            break;
+        }
         case OR_Q6_K: {
             const uint8_t *ql = blk, *qh = blk + 128;
             const int8_t *sc = (const int8_t *)(blk + 192);
@@ -176,8 +216,9 @@ void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double 
         default:
             return;
         }
-        if (w) w[e] = a * code - b;
+        if (w) w[e] = a * code - b * mcode;
         if (c) c[e] = code;
+        if (mc) mc[e] = mcode;
         if (e % 32 == 0) {
             if (A) A[u] = a;
             if (B) B[u] = b;
@@ -226,7 +267,7 @@ void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_
 }
 
 static int has_min_term(int fmt) {
-    return fmt == OR_Q4_K || fmt == OR_Q5_K || fmt == OR_Q4_1 || fmt == OR_Q5_1;
+    return fmt == OR_Q4_K || fmt == OR_Q5_K || fmt == OR_Q4_1 || fmt == OR_Q5_1 || fmt == OR_Q2_K;
 }
 
 void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *xs,
@@ -235,18 +276,26 @@ void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *x
     int upb = QK / 32;
 #pragma omp parallel for schedule(static) num_threads(or_get_threads())
     for (int n = 0; n < N; ++n) {
-        int32_t c[256];
+        int32_t c[256], mc[256];
         for (int b = 0; b < nb; ++b) {
-            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, NULL, NULL);
+            or_decode_block_mc(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, mc, NULL, NULL);
             for (int ub = 0; ub < upb; ++ub) {
                 int u = b * upb + ub;
                 for (int m = 0; m < M; ++m) {
                     const int8_t *q = xq + (size_t)m * K + (size_t)u * 32;
-                    int32_t dot = 0;
-                    for (int i = 0; i < 32; ++i) dot += c[ub * 32 + i] * (int32_t)q[i];
+                    int32_t dot = 0, msum = 0;
+                    for (int i = 0; i < 32; ++i) {
+                        dot += c[ub * 32 + i] * (int32_t)q[i];
+                        msum += mc[ub * 32 + i] * (int32_t)q[i];
+                    }
                     size_t o = ((size_t)m * N + n) * nu + u;
                     dots[o] = dot;
-                    if (aux) aux[o] = has_min_term(fmt) ? xs[(size_t)m * nu + u] : 0;
+                    if (aux) {
+                        /* the per-16 mins of Q2_K enter through their own sum; for the
+                         * other formats mc = 1 and the sum is the activation sum xs */
+                        int32_t a = fmt == OR_Q2_K ? msum : xs[(size_t)m * nu + u];
+                        aux[o] = has_min_term(fmt) ? a : 0;
+                    }
                 }
             }
         }
@@ -259,19 +308,22 @@ void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, con
     int upb = QK / 32;
 #pragma omp parallel for schedule(static) num_threads(or_get_threads())
     for (int n = 0; n < N; ++n) {
-        int32_t c[256];
+        int32_t c[256], mc[256];
         double A[8], B[8];
         for (int m = 0; m < M; ++m) y[(size_t)m * N + n] = 0.0;
         for (int b = 0; b < nb; ++b) {
-            or_decode_block(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, A, B);
+            or_decode_block_mc(fmt, W + ((size_t)n * nb + b) * BS, NULL, c, mc, A, B);
             for (int ub = 0; ub < upb; ++ub) {
                 int u = b * upb + ub;
                 for (int m = 0; m < M; ++m) {
                     const int8_t *q = xq + (size_t)m * K + (size_t)u * 32;
-                    int32_t dot = 0;
-                    for (int i = 0; i < 32; ++i) dot += c[ub * 32 + i] * (int32_t)q[i];
+                    int32_t dot = 0, msum = 0;
+                    for (int i = 0; i < 32; ++i) {
+                        dot += c[ub * 32 + i] * (int32_t)q[i];
+                        msum += mc[ub * 32 + i] * (int32_t)q[i];
+                    }
                     double d_x = xd[(size_t)m * nu + u];
-                    double s_x = xs[(size_t)m * nu + u];
+                    double s_x = fmt == OR_Q2_K ? (double)msum : (double)xs[(size_t)m * nu + u];
                     y[(size_t)m * N + n] += d_x * (A[ub] * (double)dot - B[ub] * s_x);
                 }
             }

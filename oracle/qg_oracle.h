@@ -27,7 +27,7 @@
  * print no table (they only say the codebook is small and lives in registers); the
  * values are the published IQ4_NL table, and a test can only restate them.  The
  * decode of IQ4_XS around the table (indices, sub-scales, d) is pinned.  Agreement of
- * the six byte layouts with real GGUF files is likewise unpinned: no file is at hand.
+ * the twelve byte layouts with real GGUF files is likewise unpinned: no file is at hand.
  *
  * All floating point here is fp64 unless the method itself fixes fp32 (the
  * activation scale and the division that produces the activation codes).
@@ -42,10 +42,10 @@
 extern "C" {
 #endif
 
-/* GGUF type ids for the six block formats. */
+/* GGUF type ids of the block formats. */
 enum {
     OR_Q4_0 = 2, OR_Q4_1 = 3, OR_Q5_0 = 6, OR_Q5_1 = 7, OR_Q8_0 = 8,
-    OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_IQ4_NL = 20, OR_IQ4_XS = 23
+    OR_Q2_K = 10, OR_Q3_K = 11, OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_IQ4_NL = 20, OR_IQ4_XS = 23
 };
 
 /* Elements per block (32 or 256) and bytes per block; 0 for an unknown format. */
@@ -58,11 +58,14 @@ double or_half_to_double(uint16_t h);
 /* Decode one block.  w[QK]: the dequantized weights (fp64).  c[QK]: the integer
  * codes of the per-32 dot-product contract (Q8_0: q; Q4_0: nibble-8; Q4_1: nibble;
  * Q5_0: 5-bit code - 16; Q5_1: 5-bit code; Q4_K/Q5_K: unsigned code;
- * Q6_K: sc[e/16]*(code-32); IQ4_XS, IQ4_NL: codebook value).
+ * Q6_K: sc[e/16]*(code-32); Q2_K: sc[e/16]*code; Q3_K: (scale-32)*(code-4 or code);
+ * IQ4_XS, IQ4_NL: codebook value).  mc[QK]: the integer min codes (Q2_K: the 4-bit
+ * min of the element's 16-element sub-block; 1 for every other format).
  * A[QK/32], B[QK/32]: per 32-element unit, the factors with
- *   w_e = A_u * c_e - B_u        (Q6_K: w_e = A_u * c_e, the sub-scale is in c_e)
+ *   w_e = A_u * c_e - B_u * mc_e  (Q6_K, Q3_K: B_u = 0, the sub-scale is in c_e)
  * Any output pointer may be NULL. */
 void or_decode_block(int fmt, const uint8_t *blk, double *w, int32_t *c, double *A, double *B);
+void or_decode_block_mc(int fmt, const uint8_t *blk, double *w, int32_t *c, int32_t *mc, double *A, double *B);
 
 /* Dequantize a whole N x K matrix to fp64 (row-major). */
 void or_dequant_matrix(int fmt, const uint8_t *W, int N, int K, double *out);
@@ -73,12 +76,14 @@ void or_dequant_matrix(int fmt, const uint8_t *W, int N, int K, double *out);
 void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs);
 
 /* Per-32 integer dot products: dots[m][n][u] = sum_i c_i * xq[m][32u+i];
- * aux[m][n][u] = xs[m][u] for Q4_K/Q5_K, else 0.  Layout M x N x (K/32). */
+ * aux[m][n][u] = sum_i mc_i * xq[m][32u+i] (= xs[m][u] where mc = 1) for the formats
+ * with a min term (Q4_1, Q5_1, Q2_K, Q4_K, Q5_K), else 0.  Layout M x N x (K/32). */
 void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *xs,
                    int N, int K, int M, int32_t *dots, int32_t *aux);
 
-/* y[m][n] = sum_u xd[m][u] * (A_u * dot - B_u * xs[m][u]) in fp64 from the
- * integer sums (the exact result the GPU path reaches up to rounding order). */
+/* y[m][n] = sum_u xd[m][u] * (A_u * dot - B_u * aux) in fp64 from the integer sums,
+ * aux = xs[m][u] (Q2_K: the sum over the unit of mc_i * xq, with its per-16 mins)
+ * (the exact result the GPU path reaches up to rounding order). */
 void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, const int32_t *xs,
                int N, int K, int M, double *y);
 

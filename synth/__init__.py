@@ -18,6 +18,9 @@ Field offsets follow the public GGUF block definitions:
   Q4_K  144 B: fp16 d @0, fp16 dmin @2, rest bytes  d ~ U[1e-3,2e-3], dmin ~ U[0,1e-3]
   Q5_K  176 B: as Q4_K (the qh bytes are uniform too)
   Q6_K  210 B: ql/qh @0..191 uniform, int8 sc[16] @192 ~ U{-127..127}, fp16 d @208
+  Q2_K   84 B: scale|min bytes @0..15 and codes @16..79 uniform, fp16 d @80, fp16 dmin @82
+               (d, dmin as Q4_K)
+  Q3_K  110 B: hmask, codes and packed scales @0..107 uniform, fp16 d @108 ~ U[1e-3,2e-3]
   IQ4_XS 136 B: fp16 d @0, scales and indices uniform bytes
 """
 from __future__ import annotations
@@ -25,13 +28,14 @@ from __future__ import annotations
 import numpy as np
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_NL, IQ4_XS = 2, 3, 6, 7, 8, 12, 13, 14, 20, 23
-FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K,
-           "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
+Q2_K, Q3_K = 10, 11
+FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q2_K": Q2_K, "Q3_K": Q3_K,
+           "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
 FORMAT_NAMES = {v: k for k, v in FORMATS.items()}
-BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_NL: 32,
-               IQ4_XS: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_NL: 18,
-               IQ4_XS: 136}
+BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K: 256, Q4_K: 256, Q5_K: 256,
+               Q6_K: 256, IQ4_NL: 32, IQ4_XS: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
+               Q6_K: 210, IQ4_NL: 18, IQ4_XS: 136}
 
 BASE_SEED = 0x51472026
 
@@ -77,6 +81,11 @@ def weights(fmt: int, N: int, K: int, g: np.random.Generator) -> np.ndarray:
     elif fmt in (Q4_K, Q5_K):
         _put_half(blocks, 0, d)
         _put_half(blocks, 2, g.uniform(0.0, 1e-3, size=nblk).astype(np.float32))
+    elif fmt == Q2_K:
+        _put_half(blocks, 80, d)
+        _put_half(blocks, 82, g.uniform(0.0, 1e-3, size=nblk).astype(np.float32))
+    elif fmt == Q3_K:
+        _put_half(blocks, 108, d)
     elif fmt == Q6_K:
         blocks[:, 192:208] = g.integers(-127, 128, size=(nblk, 16), dtype=np.int16).astype(np.int8).view(np.uint8)
         _put_half(blocks, 208, d)

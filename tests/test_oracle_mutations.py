@@ -43,6 +43,18 @@ MUTATIONS = [
     ("q5_1 min from wrong field", "if (one) b = -rd_half(blk + 2);", "if (one) b = -rd_half(blk + 4);"),
     ("iq4_nl nibble order", "int idx = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);",
      "int idx = e < 16 ? (blk[2 + e] >> 4) : (blk[2 + e - 16] & 15);"),
+    ("q2_k scale and min nibbles swapped", "code = (blk[sb] & 15) * q2;\n                mcode = blk[sb] >> 4;",
+     "code = (blk[sb] >> 4) * q2;\n                mcode = blk[sb] & 15;"),
+    ("q2_k dmin field", "b = rd_half(blk + 82);", "b = rd_half(blk + 80);"),
+    ("q2_k code shift", "int q2 = (blk[16 + 32 * h + l] >> (2 * j)) & 3;", "int q2 = (blk[16 + 32 * h + l] >> j) & 3;"),
+    ("q2_k dots aux from the plain sum", "int32_t a = fmt == OR_Q2_K ? msum", "int32_t a = fmt == OR_Q3_K ? msum"),
+    ("q2_k gemv min from the plain sum", "double s_x = fmt == OR_Q2_K ? (double)msum",
+     "double s_x = fmt == OR_Q3_K ? (double)msum"),
+    ("q3_k high-bit index transposed", "int hb = (blk[l] >> (4 * h + j)) & 1;", "int hb = (blk[l] >> (4 * j + h)) & 1;"),
+    ("q3_k offset on the wrong bit value", "(q2 - (hb ? 0 : 4))", "(q2 - (hb ? 4 : 0))"),
+    ("q3_k scale high bits transposed", "int high2 = (sc12[8 + i % 4] >> (2 * (i / 4))) & 3;",
+     "int high2 = (sc12[8 + i / 4] >> (2 * (i % 4))) & 3;"),
+    ("q3_k scale offset", "return (low4 | (high2 << 4)) - 32;", "return (low4 | (high2 << 4)) - 31;"),
 ]
 
 PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]

@@ -20,8 +20,9 @@ import pytest
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "blocks.txt")
-FMTS = [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q4_K, synth.Q5_K, synth.Q6_K,
-        synth.IQ4_NL, synth.IQ4_XS]
+FMTS = [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q2_K, synth.Q3_K, synth.Q4_K,
+        synth.Q5_K, synth.Q6_K, synth.IQ4_NL, synth.IQ4_XS]
+MIN_FMTS = (synth.Q4_K, synth.Q5_K, synth.Q4_1, synth.Q5_1, synth.Q2_K)  # formats with a min term
 IQ4NL = [-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113]
 
 
@@ -159,6 +160,41 @@ def _enc_q6_k(d, sc, code):
     return b
 
 
+def _enc_q2_k(d, dmin, S, M, code):
+    """S[16], M[16] in 0..15 (per 16-element sub-block), code[256] in 0..3."""
+    b = np.zeros(84, np.uint8)
+    for s in range(16):
+        b[s] = S[s] | (M[s] << 4)
+    for e in range(256):
+        h, r = divmod(e, 128)
+        j, l = divmod(r, 32)
+        b[16 + 32 * h + l] |= code[e] << (2 * j)
+    b[80:82] = _h(d)
+    b[82:84] = _h(dmin)
+    return b
+
+
+def _enc_q3_k(d, sc, q3):
+    """sc[16] in -32..31 (per 16-element sub-block), q3[256] in -4..3."""
+    b = np.zeros(110, np.uint8)
+    for i in range(16):
+        v = int(sc[i]) + 32
+        if i < 8:
+            b[96 + i] |= v & 15
+        else:
+            b[96 + i - 8] |= (v & 15) << 4
+        b[104 + i % 4] |= (v >> 4) << (2 * (i // 4))
+    for e in range(256):
+        h, r = divmod(e, 128)
+        j, l = divmod(r, 32)
+        q = int(q3[e])
+        b[32 + 32 * h + l] |= (q & 3) << (2 * j)
+        if q >= 0:
+            b[l] |= 1 << (4 * h + j)
+    b[108:110] = _h(d)
+    return b
+
+
 def _enc_iq4_xs(d, ls, idx):
     b = np.zeros(136, np.uint8)
     b[0:2] = _h(d)
@@ -210,16 +246,55 @@ def test_roundtrip_encode_decode(orc, fmt):
             code = g.integers(0, 64, 256)
             blk = _enc_q6_k(d, sc, code)
             expect = d * sc[np.arange(256) // 16] * (code - 32)
+        elif fmt == synth.Q2_K:
+            dmin = float(np.float16(g.uniform(0, 1)))
+            S, M = g.integers(0, 16, 16), g.integers(0, 16, 16)
+            code = g.integers(0, 4, 256)
+            blk = _enc_q2_k(d, dmin, S, M, code)
+            s = np.arange(256) // 16
+            expect = d * S[s] * code - dmin * M[s]
+        elif fmt == synth.Q3_K:
+            sc = g.integers(-32, 32, 16)
+            q3 = g.integers(-4, 4, 256)
+            blk = _enc_q3_k(d, sc, q3)
+            expect = d * sc[np.arange(256) // 16] * q3
         else:
             ls = g.integers(0, 64, 8)
             idx = g.integers(0, 16, 256)
             blk = _enc_iq4_xs(d, ls, idx)
             expect = d * (ls[np.arange(256) // 32] - 32) * np.array(IQ4NL)[idx]
-        w, c, A, B = orc.decode_block(fmt, blk)
+        w, c, A, B, mc = orc.decode_block(fmt, blk, with_mc=True)
         np.testing.assert_array_equal(w, expect)
         # the integer decomposition rebuilds the same weights
         u = np.arange(len(w)) // 32
-        np.testing.assert_allclose(A[u] * c - B[u], w, rtol=0, atol=1e-12 * (1 + np.abs(w).max()))
+        np.testing.assert_allclose(A[u] * c - B[u] * mc, w, rtol=0, atol=1e-12 * (1 + np.abs(w).max()))
+
+
+def test_q3k_each_scale_alone(orc):
+    """Each of the 16 packed 6-bit scales (both nibble paths, all four high-bit pairs)
+    selects exactly its own 16 elements."""
+    for i in range(16):
+        for v in (-32, -31, -17, 1, 15, 31):
+            sc = [0] * 16
+            sc[i] = v
+            w, _, _, _ = orc.decode_block(synth.Q3_K, _enc_q3_k(1.0, sc, [3] * 256))
+            nz = np.flatnonzero(w)
+            if v:
+                np.testing.assert_array_equal(nz, np.arange(16 * i, 16 * i + 16))
+                assert np.all(w[nz] == 3 * v)
+            else:
+                assert nz.size == 0
+
+
+def test_q2k_scale_and_min_nibbles(orc):
+    """Q2_K: the low nibble scales the code, the high nibble is the min, per 16 elements."""
+    for s in range(16):
+        S, M = [0] * 16, [0] * 16
+        S[s], M[s] = 5, 3
+        w, _, _, _ = orc.decode_block(synth.Q2_K, _enc_q2_k(1.0, 1.0, S, M, [2] * 256))
+        nz = np.flatnonzero(w)
+        np.testing.assert_array_equal(nz, np.arange(16 * s, 16 * s + 16))
+        assert np.all(w[nz] == 5 * 2 - 3)
 
 
 def test_iq4_codebook_recovered(orc):
@@ -346,7 +421,13 @@ def test_int_path_equals_fp64_bruteforce(orc, fmt):
         want = np.einsum("nuk,muk->mnu", codes.reshape(N, K // 32, 32).astype(np.int64),
                          xq.reshape(M, K // 32, 32).astype(np.int64))
         np.testing.assert_array_equal(dots, want)
-        if fmt in (synth.Q4_K, synth.Q5_K, synth.Q4_1, synth.Q5_1):  # formats with a min term
+        if fmt == synth.Q2_K:  # per-16 mins: aux is the unit's sum of min code * activation code
+            mcs = np.stack([np.concatenate([orc.decode_block(fmt, W[n, b * 84:(b + 1) * 84], with_mc=True)[4]
+                                            for b in range(K // qk)]) for n in range(N)])
+            want_a = np.einsum("nuk,muk->mnu", mcs.reshape(N, K // 32, 32).astype(np.int64),
+                               xq.reshape(M, K // 32, 32).astype(np.int64))
+            np.testing.assert_array_equal(aux, want_a)
+        elif fmt in MIN_FMTS:
             np.testing.assert_array_equal(aux, np.broadcast_to(xs[:, None, :], aux.shape))
         else:
             assert not aux.any()
