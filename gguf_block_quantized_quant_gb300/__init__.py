@@ -6,8 +6,8 @@ pointers and the current CUDA stream, and raises ``QGError`` on a non-zero statu
 arithmetic runs in the library's CUDA kernels; PyTorch only provides device memory and
 streams.  If ``libqg.so`` has not been built, every call raises: there is no fallback.
 
-Block formats (GGUF type ids): Q4_0=2, Q4_1=3, Q5_0=6, Q5_1=7, Q8_0=8, Q4_K=12, Q5_K=13,
-Q6_K=14, IQ4_NL=20, IQ4_XS=23.
+Block formats (GGUF type ids): Q4_0=2, Q4_1=3, Q5_0=6, Q5_1=7, Q8_0=8, Q2_K=10, Q3_K=11,
+Q4_K=12, Q5_K=13, Q6_K=14, IQ4_NL=20, IQ4_XS=23.
 A weight matrix of N rows and K columns is passed as a uint8 CUDA tensor holding the N
 rows of raw blocks back to back (``row_bytes(fmt, K)`` bytes per row).
 """
@@ -21,12 +21,13 @@ import torch
 from . import build as _build
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_NL, IQ4_XS = 2, 3, 6, 7, 8, 12, 13, 14, 20, 23
-FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q4_K": Q4_K, "Q5_K": Q5_K,
-           "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
-BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256, IQ4_NL: 32,
-               IQ4_XS: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_NL: 18,
-               IQ4_XS: 136}
+Q2_K, Q3_K = 10, 11
+FORMATS = {"Q4_0": Q4_0, "Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1, "Q8_0": Q8_0, "Q2_K": Q2_K, "Q3_K": Q3_K,
+           "Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "IQ4_NL": IQ4_NL, "IQ4_XS": IQ4_XS}
+BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K: 256, Q4_K: 256, Q5_K: 256,
+               Q6_K: 256, IQ4_NL: 32, IQ4_XS: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
+               Q6_K: 210, IQ4_NL: 18, IQ4_XS: 136}
 
 QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER = 1, 2, 3, 4
 QG_OK, QG_EINVAL, QG_EWORKSPACE, QG_EALIGN, QG_ECUDA, QG_EDEVICE = 0, -1, -2, -3, -4, -5

@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libqg.so")
 
-FORMATS = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8, "q4_k": 12, "q5_k": 13, "q6_k": 14,
-           "iq4_nl": 20, "iq4_xs": 23}
+FORMATS = {"q4_0": 2, "q4_1": 3, "q5_0": 6, "q5_1": 7, "q8_0": 8, "q2_k": 10, "q3_k": 11, "q4_k": 12, "q5_k": 13,
+           "q6_k": 14, "iq4_nl": 20, "iq4_xs": 23}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

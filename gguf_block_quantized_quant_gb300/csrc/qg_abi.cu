@@ -244,6 +244,8 @@ int by_format(int fmt, Fn &&fn) {
     case QG_Q5_1: return fn(std::integral_constant<int, QG_Q5_1>{});
     case QG_IQ4_NL: return fn(std::integral_constant<int, QG_IQ4_NL>{});
     case QG_Q8_0: return fn(std::integral_constant<int, QG_Q8_0>{});
+    case QG_Q2_K: return fn(std::integral_constant<int, QG_Q2_K>{});
+    case QG_Q3_K: return fn(std::integral_constant<int, QG_Q3_K>{});
     case QG_Q4_K: return fn(std::integral_constant<int, QG_Q4_K>{});
     case QG_Q5_K: return fn(std::integral_constant<int, QG_Q5_K>{});
     case QG_Q6_K: return fn(std::integral_constant<int, QG_Q6_K>{});
@@ -486,7 +488,8 @@ int qg_device_error(unsigned int *err) {
     if (cudaMemcpyFromSymbol(&v, g_qg_dev_err, sizeof(v)) != cudaSuccess) return QG_ECUDA;
     if (cudaMemcpyToSymbol(g_qg_dev_err, &zero, sizeof(zero)) != cudaSuccess) return QG_ECUDA;
     all |= v;
-    const int fmts[] = {QG_Q4_0, QG_Q4_1, QG_Q5_0, QG_Q5_1, QG_Q8_0, QG_Q4_K, QG_Q5_K, QG_Q6_K, QG_IQ4_NL, QG_IQ4_XS};
+    const int fmts[] = {QG_Q4_0, QG_Q4_1, QG_Q5_0, QG_Q5_1, QG_Q8_0, QG_Q2_K, QG_Q3_K,
+                        QG_Q4_K, QG_Q5_K, QG_Q6_K, QG_IQ4_NL, QG_IQ4_XS};
     for (int f : fmts) {
         const int rc = by_format(f, [&](auto F) { return dev_err_take<decltype(F)::value>(&v); });
         if (rc) return rc;

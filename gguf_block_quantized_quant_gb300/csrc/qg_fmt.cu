@@ -96,7 +96,7 @@ int with_t(const TaskGeo &g, Fn &&fn) {
     } else if constexpr (QG_FMT == F_Q8_0 || QG_FMT == F_Q4_1 || QG_FMT == F_Q5_0 || QG_FMT == F_Q5_1) {
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
-    } else if constexpr (QG_FMT == F_Q5_K || QG_FMT == F_Q6_K) {
+    } else if constexpr (QG_FMT == F_Q3_K || QG_FMT == F_Q5_K || QG_FMT == F_Q6_K) {
         return fn(ic<2>{});
     } else {
         if (g.T == 2) return fn(ic<2>{});
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(HOOK_THREADS) block_dots_kernel(const uint8_t 
                 ((uint32_t)hs & 0xffffu) | ((uint32_t)(sum - hs) << 16);
             reinterpret_cast<float *>(tile + TL::Q)[u] = 0.0f;
         }
-        DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K || FMT == F_Q4_1 || FMT == F_Q5_1};
+        DotSink sink{dots, aux, ((long)m * N + n) * nu + (long)tt * F::XGT, FMT == F_Q4_K || FMT == F_Q5_K || FMT == F_Q4_1 || FMT == F_Q5_1 || FMT == F_Q2_K};
         F::run(blk, tt % F::TPB, XT{tile, 0}, 1, sink);
     }
 }

@@ -36,7 +36,7 @@ namespace qg {
 
 enum : int {
     F_Q4_0 = 2, F_Q4_1 = 3, F_Q5_0 = 6, F_Q5_1 = 7, F_Q8_0 = 8,
-    F_Q4_K = 12, F_Q5_K = 13, F_Q6_K = 14, F_IQ4_NL = 20, F_IQ4_XS = 23
+    F_Q2_K = 10, F_Q3_K = 11, F_Q4_K = 12, F_Q5_K = 13, F_Q6_K = 14, F_IQ4_NL = 20, F_IQ4_XS = 23
 };
 
 // unsigned (weights) x signed (activations) 4-way byte dot product
@@ -320,6 +320,179 @@ struct FmtLegacy {
                     unit(c, qh, d, mv, m, 0, tl, ldsf(tl + TL::D), xs, xq, sink);
                 }
             }
+        }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, (uint32_t)((uintptr_t)addr & 3u), hf, xt, ntok, sink);
+    }
+};
+
+// ================================================================================ Q2_K
+// T superblocks per task (84 bytes each: 4-byte aligned; a two-superblock task starts
+// 8-byte aligned).  Words: 0..3 the 16 scale|min bytes (low nibble: scale, high nibble:
+// min of a 16-element sub-block), 4..19 the 2-bit codes, 20 d | dmin << 16.  Activation
+// unit u = 4h + j takes bits 2j, 2j+1 of code words 4 + 8h .. 4 + 8h + 7; its first 16
+// elements are sub-block 2u, the last 16 sub-block 2u + 1.  Per unit the exact integers
+// are D = S_2u * dot(first 16) + S_2u+1 * dot(last 16) and the min sum
+// Mn = M_2u * h_lo + M_2u+1 * h_hi (h: the activation half sums of the tile); per token
+// A = sum xd * D and B = sum xd * Mn, and y += d * A - dmin * B once per superblock.
+template <int T>
+struct FmtQ2K {
+    static constexpr int QK = 256, BS = 84, XGT = 8 * T, TPB = 1, BPT = T, TASK_BYTES = 84 * T;
+    static constexpr int WW = 21 * T;
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        if constexpr (T == 2) {
+#pragma unroll
+            for (int i = 0; i < WW / 2; ++i) {
+                const uint2 v = lds64(addr + 8 * i);
+                w[2 * i] = v.x;
+                w[2 * i + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < WW; ++i) w[i] = lds32(addr + 4 * i);
+        }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void superblock(const uint32_t *w, int u0, const XT &xt, int ntok,
+                                                      Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
+        const float d = half_bits_to_float(w[20]), dmin = half_bits_to_float(w[20] >> 16);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            uint32_t xd[8], xh[8];
+            ld4(t + TL::H + 4 * u0, xh);
+            ld4(t + TL::H + 4 * u0 + 16, xh + 4);
+            if constexpr (!Sink::DOTS) {
+                ld4(t + TL::D + 4 * u0, xd);
+                ld4(t + TL::D + 4 * u0 + 16, xd + 4);
+            }
+            float A = 0.0f, B = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int h = u >> 2, j = u & 3;
+                const uint32_t sm = (w[u >> 1] >> (16 * (u & 1))) & 0xffffu;  // bytes 2u, 2u+1
+                const int sa = (int)(sm & 15u), ma = (int)((sm >> 4) & 15u);
+                const int sb = (int)((sm >> 8) & 15u), mb = (int)(sm >> 12);
+                uint32_t x[8];
+                ldx8(t + 32 * (u0 + u), x);
+                int lo = 0, hi = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    lo = dp4a((w[4 + 8 * h + k] >> (2 * j)) & 0x03030303u, x[k], lo);
+                    hi = dp4a((w[8 + 8 * h + k] >> (2 * j)) & 0x03030303u, x[4 + k], hi);
+                }
+                const int hlo = (int)(int16_t)(xh[u] & 0xffffu), hhi = (int)(int16_t)(xh[u] >> 16);
+                const int D = sa * lo + sb * hi, Mn = ma * hlo + mb * hhi;
+                if constexpr (Sink::DOTS) {
+                    sink.unit(m, u0 + u, D, Mn);
+                } else {
+                    A = fmaf(__uint_as_float(xd[u]), (float)D, A);
+                    B = fmaf(__uint_as_float(xd[u]), (float)Mn, B);
+                }
+            }
+            if constexpr (!Sink::DOTS) sink.add(m, fmaf(d, A, -dmin * B));
+        }
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
+#pragma unroll
+        for (int i = 0; i < T; ++i) superblock(w + 21 * i, 8 * i, xt, ntok, sink);
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
+        uint32_t w[WW];
+        load(addr, w);
+        compute(w, 0, hf, xt, ntok, sink);
+    }
+};
+
+// ================================================================================ Q3_K
+// One whole superblock per task (110 bytes, starting on any even byte: the 28 words from
+// the 4-byte-aligned start are loaded and realigned with byte permutes).  Block words:
+// 0..7 the third code bits (bit 4h + j of byte l for element 128h + 32j + l), 8..23 the
+// low 2-bit codes (as Q2_K), 24..26 the sixteen packed 6-bit scales, 27 d.  Codes are used
+// unsigned (0..7) and the -4 offset is applied through the activation half sums, so that
+// per unit D = sc_2u * (dot_lo - 4 h_lo) + sc_2u+1 * (dot_hi - 4 h_hi) is exact; per token
+// A = sum xd * D, y += d * A.
+template <int T>
+struct FmtQ3K {
+    static_assert(T == 2, "Q3_K tasks are whole superblocks");
+    static constexpr int QK = 256, BS = 110, XGT = 8, TPB = 1, BPT = 1, TASK_BYTES = 110;
+    static constexpr int WW = 28;
+
+    __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
+        const SAddr base = addr - ((uintptr_t)addr & 3u);
+#pragma unroll
+        for (int i = 0; i < WW; ++i) w[i] = lds32(base + 4 * i);
+    }
+
+    template <class Sink>
+    __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t a, int, const XT &xt, int ntok,
+                                                   Sink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = Sink::MT;
+        const uint32_t sel = a ? 0x5432u : 0x3210u;
+        auto word = [&](int i) { return prmt(w[i], w[i + 1], sel); };  // block word i (i < 27)
+        // the sixteen scales as bytes 0..63 (scale + 32): low nibbles from block bytes 96..103,
+        // high 2 bits from bytes 104..107
+        const uint32_t s0 = word(24), s1 = word(25), s2 = word(26);
+        uint32_t sc[4];
+        sc[0] = (s0 & 0x0f0f0f0fu) | ((s2 & 0x03030303u) << 4);
+        sc[1] = (s1 & 0x0f0f0f0fu) | (((s2 >> 2) & 0x03030303u) << 4);
+        sc[2] = ((s0 >> 4) & 0x0f0f0f0fu) | (((s2 >> 4) & 0x03030303u) << 4);
+        sc[3] = ((s1 >> 4) & 0x0f0f0f0fu) | (((s2 >> 6) & 0x03030303u) << 4);
+        const float d = half_bits_to_float(a ? (w[27] >> 16) : w[27]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            uint32_t xd[8], xh[8];
+            ld4(t + TL::H, xh);
+            ld4(t + TL::H + 16, xh + 4);
+            if constexpr (!Sink::DOTS) {
+                ld4(t + TL::D, xd);
+                ld4(t + TL::D + 16, xd + 4);
+            }
+            float A = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int h = u >> 2, j = u & 3;
+                uint32_t x[8];
+                ldx8(t + 32 * u, x);
+                int lo = 0, hi = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t cl = ((word(8 + 8 * h + k) >> (2 * j)) & 0x03030303u) |
+                                        (((word(k) >> u) & 0x01010101u) << 2);
+                    const uint32_t ch = ((word(12 + 8 * h + k) >> (2 * j)) & 0x03030303u) |
+                                        (((word(4 + k) >> u) & 0x01010101u) << 2);
+                    lo = dp4a(cl, x[k], lo);
+                    hi = dp4a(ch, x[4 + k], hi);
+                }
+                const int hlo = (int)(int16_t)(xh[u] & 0xffffu), hhi = (int)(int16_t)(xh[u] >> 16);
+                const int sa = (int)((sc[u >> 1] >> (16 * (u & 1))) & 255u) - 32;
+                const int sb = (int)((sc[u >> 1] >> (16 * (u & 1) + 8)) & 255u) - 32;
+                const int D = sa * (lo - 4 * hlo) + sb * (hi - 4 * hhi);
+                if constexpr (Sink::DOTS) {
+                    sink.unit(m, u, D, 0);
+                } else {
+                    A = fmaf(__uint_as_float(xd[u]), (float)D, A);
+                }
+            }
+            if constexpr (!Sink::DOTS) sink.add(m, d * A);
         }
     }
 
@@ -739,6 +912,10 @@ template <int T>
 struct FmtSel<F_Q5_1, T> { using type = FmtLegacy<F_Q5_1, T>; };
 template <int T>
 struct FmtSel<F_IQ4_NL, T> { using type = FmtLegacy<F_IQ4_NL, T>; };
+template <int T>
+struct FmtSel<F_Q2_K, T> { using type = FmtQ2K<T>; };
+template <int T>
+struct FmtSel<F_Q3_K, T> { using type = FmtQ3K<T>; };
 template <int T>
 struct FmtSel<F_Q4_K, T> { using type = FmtQ4K<T>; };
 template <int T>

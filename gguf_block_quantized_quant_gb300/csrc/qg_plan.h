@@ -26,6 +26,8 @@ inline bool fmt_info(int fmt, FmtInfo &f) {
     case 7: f = {32, 24}; return true;     // Q5_1
     case 20: f = {32, 18}; return true;    // IQ4_NL
     case 8: f = {32, 34}; return true;     // Q8_0
+    case 10: f = {256, 84}; return true;   // Q2_K
+    case 11: f = {256, 110}; return true;  // Q3_K
     case 12: f = {256, 144}; return true;  // Q4_K
     case 13: f = {256, 176}; return true;  // Q5_K
     case 14: f = {256, 210}; return true;  // Q6_K
@@ -49,8 +51,8 @@ inline int log2i(int v) {
 
 // Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
 //   Q4_0: 16 (only with long_tasks), 8, 4 or 1 blocks per task; IQ4_NL: 8, 4 or 1; Q8_0,
-//   Q4_1, Q5_0, Q5_1: 4 or 1; Q4_K, IQ4_XS: 2 or 1 superblocks (the largest that divides the
-//   row); Q5_K, Q6_K: one whole superblock.
+//   Q4_1, Q5_0, Q5_1: 4 or 1; Q2_K, Q4_K, IQ4_XS: 2 or 1 superblocks (the largest that divides
+//   the row); Q3_K, Q5_K, Q6_K: one whole superblock.
 // long_tasks asks for 16-block Q4_0 tasks (288 bytes, the size of two Q4_K superblocks): with
 // one token per lane they leave the lane's decode fewer, longer loads and let the 12-warp
 // engine run; with several tokens per lane the 8-block tasks on 16 warps were faster.
@@ -77,7 +79,7 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
         g.XGT = g.T;
         g.TPB = 1;
         g.gpr = g.nbr / g.T;
-    } else if (fmt == 13 || fmt == 14) {
+    } else if (fmt == 11 || fmt == 13 || fmt == 14) {
         g.T = 2;
         g.BPT = 1;
         g.TPB = 1;

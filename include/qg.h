@@ -53,6 +53,8 @@ enum qg_format {
     QG_Q5_0 = 6,    /* 32 elements, 22 B: fp16 d, 32 fifth bits, 4-bit codes; w = d*(c-16)   */
     QG_Q5_1 = 7,    /* 32 elements, 24 B: fp16 d, fp16 m, fifth bits, codes; w = d*c + m     */
     QG_Q8_0 = 8,    /* 32 elements, 34 B: fp16 d, 32 int8 codes; w = d*q                     */
+    QG_Q2_K = 10,   /* 256 elements, 84 B: 16 x (4-bit scale, 4-bit min), 2-bit codes, d, dmin */
+    QG_Q3_K = 11,   /* 256 elements, 110 B: 3-bit codes (2 low + 1 high), 16 6-bit scales, d */
     QG_Q4_K = 12,   /* 256 elements, 144 B: fp16 d, dmin, 8 x 6-bit scale/min, 4-bit codes   */
     QG_Q5_K = 13,   /* 256 elements, 176 B: as Q4_K plus one high bit per code              */
     QG_Q6_K = 14,   /* 256 elements, 210 B: 6-bit codes, 16 int8 sub-scales, fp16 d          */
@@ -170,9 +172,12 @@ int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]);
 
 /* Test hook, exact integer contract: dots[m][n][u] = sum over the 32 elements of unit
  * u of (weight code) * xq, where the weight code is q (Q8_0), nibble-8 (Q4_0), the
- * unsigned code (Q4_K, Q5_K), sub-scale*(code-32) (Q6_K) or the codebook value
- * (IQ4_XS); aux[m][n][u] = xs[m][u] for Q4_K/Q5_K, else 0.  dots, aux: M x N x K/32
- * int32.  Uses the same block decoders as the GEMV kernels. */
+ * unsigned code (Q4_1, Q5_1, Q4_K, Q5_K), 5-bit code-16 (Q5_0), sub-scale*code (Q2_K),
+ * (scale-32)*(signed 3-bit code) (Q3_K), sub-scale*(code-32) (Q6_K) or the codebook
+ * value (IQ4_NL, IQ4_XS); aux[m][n][u] = the unit's min sum for the formats with a min
+ * term: xs[m][u] for Q4_1, Q5_1, Q4_K, Q5_K, and sum of (16-element sub-block min) * xq
+ * for Q2_K; else 0.  dots, aux: M x N x K/32 int32.  Uses the same block decoders as the
+ * GEMV kernels. */
 int qg_block_dots(int fmt, const void *W_blocks, const int8_t *xq, const int32_t *xs,
                   int N, int K, int M, int32_t *dots, int32_t *aux, void *stream);
 

@@ -4,8 +4,8 @@ import pytest
 
 import synth
 
-FMTS = [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q4_K, synth.Q5_K, synth.Q6_K,
-        synth.IQ4_NL, synth.IQ4_XS]
+FMTS = [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q2_K, synth.Q3_K, synth.Q4_K, synth.Q5_K,
+        synth.Q6_K, synth.IQ4_NL, synth.IQ4_XS]
 FMT_IDS = [synth.FORMAT_NAMES[f] for f in FMTS]
 
 # Per-element bound on the final fp32 outputs against the fp64 oracle:

@@ -105,6 +105,9 @@ def test_gemv_q_prequantized_matches_oracle(qg, fmt):
     (synth.Q4_0, 1037, 512, 1),      # one token: one 16-block task per row (two swapped halves)
     (synth.Q4_0, 333, 2560, 1),      # one token: 5 tasks of 16 blocks per row, rows wrap in a step
     (synth.Q4_0, 333, 2560, 2),      # two tokens on the same rows: 8-block tasks
+    (synth.Q2_K, 77, 768, 1),        # odd superblocks per row: one-superblock tasks, 4-byte aligned
+    (synth.Q3_K, 301, 2304, 3),      # 110-byte superblocks that start 2-byte aligned
+    (synth.Q2_K, 5, 65536, 16),      # split-K with 16 tokens
 ])
 def test_gemv_layout_paths(qg, fmt, N, K, M):
     g = np.random.default_rng(N + K + M)
@@ -124,6 +127,7 @@ FULL = [
     (synth.Q5_K, 4096, 4096), (synth.Q6_K, 4096, 4096), (synth.IQ4_XS, 4096, 4096),
     (synth.Q6_K, 17408, 5120), (synth.Q6_K, 5120, 17408),
     (synth.Q4_1, 4096, 4096), (synth.Q5_0, 4096, 4096), (synth.Q5_1, 4096, 4096), (synth.IQ4_NL, 4096, 4096),
+    (synth.Q2_K, 4096, 4096), (synth.Q3_K, 4096, 4096), (synth.Q2_K, 17408, 5120), (synth.Q3_K, 5120, 17408),
 ]
 
 

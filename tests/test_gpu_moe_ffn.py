@@ -121,8 +121,8 @@ def test_moe_config_shape(qg, M):
     _check_moe(fmt, inp, out, M, H, E, topk, I)
 
 
-@pytest.mark.parametrize("fmt", [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q5_K, synth.Q6_K,
-                                 synth.IQ4_NL, synth.IQ4_XS])
+@pytest.mark.parametrize("fmt", [synth.Q4_0, synth.Q4_1, synth.Q5_0, synth.Q5_1, synth.Q8_0, synth.Q2_K, synth.Q3_K,
+                                 synth.Q5_K, synth.Q6_K, synth.IQ4_NL, synth.IQ4_XS])
 def test_moe_other_formats_small(qg, fmt):
     M, H, E, topk, I = 3, 512, 40, 4, 256
     inp, out = _moe_case(qg, fmt, M, H, E, topk, I, seed=500 + fmt)
@@ -166,7 +166,7 @@ def _ffn_case(qg, fmt, M, H, I, seed, sample_rows=None):
 
 
 @pytest.mark.parametrize("fmt", [synth.Q4_K, synth.Q6_K, synth.Q8_0, synth.IQ4_XS, synth.Q4_0, synth.Q5_K, synth.Q4_1,
-                                 synth.Q5_0, synth.Q5_1, synth.IQ4_NL])
+                                 synth.Q5_0, synth.Q5_1, synth.IQ4_NL, synth.Q2_K, synth.Q3_K])
 @pytest.mark.parametrize("M", [1, 3, 16])
 def test_ffn_small(qg, fmt, M):
     _ffn_case(qg, fmt, M, 1024, 2816, seed=fmt * 31 + M)
