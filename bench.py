@@ -430,7 +430,9 @@ def secondary(qg, torch, dev, s):
     out = {}
     l2 = 4 * torch.cuda.get_device_properties(dev).L2_cache_size
     for fmt, N, K in [(synth.Q8_0, 1024, 1024), (synth.Q5_K, 4096, 4096), (synth.Q6_K, 4096, 4096),
-                      (synth.IQ4_XS, 4096, 4096)]:
+                      (synth.IQ4_XS, 4096, 4096), (synth.Q2_K, 4096, 4096), (synth.Q3_K, 4096, 4096),
+                      (synth.Q4_1, 4096, 4096), (synth.Q5_0, 4096, 4096), (synth.Q5_1, 4096, 4096),
+                      (synth.IQ4_NL, 4096, 4096)]:
         g = synth.rng(3 if fmt != synth.Q8_0 else 1, 0)
         nb = synth.matrix_bytes(fmt, N, K)
         R = max(2, -(-l2 // nb))
