@@ -371,4 +371,282 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
     }
 }
 
+
+// ===================================================================================
+// Row-pair engine (plain GEMV with whole rows per CTA).  A task is the same column block
+// of two adjacent rows (one superblock or 4 / 8 blocks of each), so every activation-tile
+// load of a lane serves both rows: half the tile traffic of one-row tasks of the same
+// size, and tasks 144 bytes apart (an odd number of 16-byte chunks) load without bank
+// conflicts.  The CTA owns row pairs [p0, p1); tasks are ordered pair by pair, column by
+// column.  A stage's bytes are at most three runs of the row-major matrix: the first
+// pair's first row from the stage's first column, everything from that pair's second row
+// (same column) through the last pair's first row, and the last pair's second row up to
+// the stage's last column.  Ring, barriers, refill, carries and the combine of pairs
+// shared by two warps work as in engine_kernel, with two sums per token.
+constexpr int PAIR_BND = 1 + 2 * 16;  // boundary entry: pair, then row-0 and row-1 sums
+constexpr int PAIR_RUNS = 3;
+__host__ __device__ constexpr uint32_t pair_fixed_smem(int S, int ncw) {
+    return (uint32_t)(ncw * 2 * PAIR_BND * 4) + 8u * (uint32_t)S + 8u + 4u * PAIR_RUNS * (uint32_t)S + 16u;
+}
+
+template <int NT>
+struct PairSink {
+    static constexpr int MT = NT;
+    float acc[2][NT];
+    __device__ __forceinline__ void add(int r, int m, float v) { acc[r][m] += v; }
+};
+
+template <int FMT, int T, int MT, int NCW, class Job>
+__global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job) {
+    using F = FT<FMT, T>;
+    using TL = Tile<F::XGT>;
+    constexpr int NCONS = NCW * 32;
+    constexpr uint32_t TB = F::TASK_BYTES;  // one row's part of a task
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int D = job.depth, S = NCW * D;
+    const uint32_t slot_stride = job.slot_bytes + STAGE_SLACK;
+
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t xa = ring + (uint32_t)S * slot_stride;             // activation tiles
+    const uint32_t bnd = xa + job.x_bytes;                            // boundary sums
+    const uint32_t bars = bnd + (uint32_t)(NCW * 2 * PAIR_BND * 4);
+    const uint32_t xbar = bars + 8u * (uint32_t)S;
+    const uint32_t hdrs = xbar + 8u;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto hdr = [&](int s, int k) { return hdrs + 4u * (uint32_t)(s * PAIR_RUNS + k); };
+    const uint32_t tok_stride = (uint32_t)(job.tpr_x * TL::STRIDE);
+    float *bsum = reinterpret_cast<float *>(smem + (bnd - ring));  // [NCW][2][PAIR_BND]
+
+    griddep_launch_dependents();
+    if (lane == 0) {
+        for (int j = 0; j < D; ++j) mbar_init(full_bar(j * NCW + warp), 1);
+        if (warp == 0) mbar_init(xbar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int N = job.N, tpr = job.tpr_x;
+    const int P = (N + 1) >> 1;
+    const int p0 = split_point(P, (int)blockIdx.x, (int)gridDim.x);
+    const int p1 = split_point(P, (int)blockIdx.x + 1, (int)gridDim.x);
+    const int ntask = (p1 - p0) * tpr;
+    const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
+    const int a = (int)((long)ntask * warp / NCW), b = (int)((long)ntask * (warp + 1) / NCW);
+    const int maxlen = (ntask + NCW - 1) / NCW;
+    const int nchunk = (maxlen + job.tps - 1) / job.tps;
+
+    // Copies stage j of this warp into its slot (which must be free); lane k < 3 copies run k.
+    auto issue = [&](int j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = a + j * job.tps, fb = min(b, fa + job.tps);
+        const uint32_t sbase = ring + (uint32_t)slot * slot_stride;
+        const uint32_t fbar = full_bar(slot);
+        bool valid = false;
+        uintptr_t s0 = 0, a0 = 0, e = 0, a1c = 0;
+        if (fa < fb && lane < PAIR_RUNS) {
+            const int pa = (int)tpr_div.div((uint32_t)fa), ca = fa - pa * tpr;
+            const int pb = (int)tpr_div.div((uint32_t)(fb - 1)), cb = fb - 1 - pb * tpr;
+            const int ra = 2 * (p0 + pa), rz = 2 * (p0 + pb);
+            int row = 0, col = 0, n = 0;
+            if (lane == 0) {
+                row = ra, col = ca, n = pa == pb ? cb - ca + 1 : tpr - ca;
+            } else if (lane == 1) {
+                row = ra + 1, col = ca;
+                n = pa == pb ? cb - ca + 1 : (tpr - ca) + (rz - ra - 2) * tpr + cb + 1;
+            } else if (pb > pa) {
+                row = rz + 1, col = 0, n = cb + 1;
+            }
+            valid = n > 0 && row < N;
+            if (valid) {
+                s0 = (uintptr_t)(job.W + (size_t)row * job.rb + (size_t)col * TB);
+                a0 = s0 & ~(uintptr_t)15;
+                e = s0 + (uintptr_t)n * TB;
+                const uintptr_t lim16 = (uintptr_t)job.Wend & ~(uintptr_t)15;
+                a1c = (e + 15) & ~(uintptr_t)15;
+                if (a1c > lim16) a1c = lim16 > a0 ? lim16 : a0;
+            }
+        }
+        // slot offsets: exclusive prefix sum of the widened run sizes over lanes 0..2
+        const uint32_t wsz = valid ? (uint32_t)(((e + 15) & ~(uintptr_t)15) - a0) : 0u;
+        uint32_t incl = wsz;
+#pragma unroll
+        for (int d = 1; d < PAIR_RUNS; d <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        const uint32_t off = incl - wsz;
+        const uint32_t nb = valid ? (uint32_t)(a1c - a0) : 0u;
+        if (valid) {
+            for (uintptr_t q = a1c; q < e; ++q)
+                sts8(sbase + off + (uint32_t)(q - a0), *reinterpret_cast<const uint8_t *>(q));
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hdr(slot, lane)), "r"(sbase + off + (uint32_t)(s0 & 15))
+                         : "memory");
+            if (nb) bulk_g2s(sbase + off, reinterpret_cast<const void *>(a0), nb, fbar);
+        }
+        const uint32_t tx = __reduce_add_sync(0xffffffffu, nb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(fbar, tx);
+    };
+
+    const int jfirst = min(D, nchunk);
+    for (int j = 0; j < jfirst; ++j) issue(j);
+    if (tid < NCW * 2) bsum[tid * PAIR_BND] = __int_as_float(-1);
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) {
+            griddep_wait();
+            const int rows = ntask > 0 ? job.ntok : 0;
+            const uint32_t bytes = (uint32_t)(tpr * TL::STRIDE);
+            for (int r = 0; r < rows; ++r)
+                bulk_g2s(xa + (uint32_t)r * tok_stride, job.ximg + (size_t)r * job.ximg_pitch, bytes, xbar);
+            mbar_arrive_expect_tx(xbar, bytes * (uint32_t)rows);
+        }
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------------- consume
+    const int pa0 = (int)tpr_div.div((uint32_t)a);
+    const bool a_mid = a < b && a != pa0 * tpr;
+    const int ntok = job.ntok;
+    mbar_wait(xbar, 0);
+
+    auto store_pair = [&](int p, int m, float v0, float v1) {
+        const int r0 = 2 * (p0 + p);
+        job.out[(long)m * N + r0] = v0;
+        if (r0 + 1 < N) job.out[(long)m * N + r0 + 1] = v1;
+    };
+
+    float carry[2][MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) carry[0][m] = carry[1][m] = 0.0f;
+    int carry_p = -1;
+
+    for (int j = 0; j < nchunk; ++j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = a + j * job.tps;
+        mbar_wait(full_bar(slot), (uint32_t)((j / D) & 1));
+        const int fb = min(b, fa + job.tps);
+        const int f = fa + lane;
+        const bool valid = f < fb;
+        int p = 0x7fffffff, c = 0;
+        uint32_t w0[F::WW], w1[F::WW];
+        SAddr xbase = smem;
+        if (valid) {
+            const int pa = (int)tpr_div.div((uint32_t)fa), ca = fa - pa * tpr;
+            const int pb = (int)tpr_div.div((uint32_t)(fb - 1));
+            p = (int)tpr_div.div((uint32_t)f);
+            c = f - p * tpr;
+            const SAddr h0 = smem + (lds32(hdr(slot, 0)) - ring);
+            const SAddr h1 = smem + (lds32(hdr(slot, 1)) - ring);
+            const int ra = 2 * pa, r0 = 2 * p;  // CTA-relative rows
+            const SAddr addr0 = p == pa ? h0 + (uint32_t)(c - ca) * TB
+                                        : h1 + (uint32_t)((r0 - ra - 1) * tpr + c - ca) * TB;
+            SAddr addr1;
+            if (2 * (p0 + p) + 1 >= N)
+                addr1 = addr0;  // the last row of an odd N has no partner
+            else if (pb > pa && p == pb)
+                addr1 = smem + (lds32(hdr(slot, 2)) - ring) + (uint32_t)c * TB;
+            else
+                addr1 = h1 + (uint32_t)((r0 - ra) * tpr + c - ca) * TB;
+            F::load(addr0, w0);
+            F::load(addr1, w1);
+            xbase = smem + (xa - ring) + (uint32_t)(c * TL::STRIDE);
+        }
+        __syncwarp();
+        if (j + D < nchunk) {
+            fence_proxy_async_smem();
+            issue(j + D);
+        }
+        if (fa < fb) {
+            PairSink<MT> sink;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) sink.acc[0][m] = sink.acc[1][m] = 0.0f;
+            if (valid) F::compute_pair(w0, w1, XT{xbase, tok_stride}, ntok, sink);
+            // segmented reduction: pairs are contiguous runs of lanes
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int p2 = __shfl_down_sync(0xffffffffu, p, d);
+                const bool take = lane + d < 32 && p2 == p;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float v = __shfl_down_sync(0xffffffffu, sink.acc[r][m], d);
+                        if (take) sink.acc[r][m] += v;
+                    }
+                }
+            }
+            const int pprev = __shfl_up_sync(0xffffffffu, p, 1);
+            const bool head = valid && (lane == 0 || pprev != p);
+            if (head && p == carry_p) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    sink.acc[0][m] += carry[0][m];
+                    sink.acc[1][m] += carry[1][m];
+                }
+            }
+            const int flast = min(fb, fa + 32) - 1;
+            const int plast = __shfl_sync(0xffffffffu, p, flast - fa);
+            const bool cont = (plast + 1) * tpr > flast + 1;
+            if (head && !(p == plast && cont)) {
+                if (a_mid && p == pa0) {
+                    float *e = bsum + (warp * 2) * PAIR_BND;  // shared with the previous warp
+                    e[0] = __int_as_float(p);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        e[1 + m] = sink.acc[0][m];
+                        e[17 + m] = sink.acc[1][m];
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < ntok) store_pair(p, m, sink.acc[0][m], sink.acc[1][m]);
+                }
+            }
+            const int hl = __reduce_min_sync(0xffffffffu, (valid && p == plast) ? lane : 31);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                carry[0][m] = __shfl_sync(0xffffffffu, sink.acc[0][m], hl);
+                carry[1][m] = __shfl_sync(0xffffffffu, sink.acc[1][m], hl);
+            }
+            carry_p = cont ? plast : -1;
+        }
+    }
+    // a range that ended inside a pair: its sums are shared with the next warp
+    if (carry_p >= 0 && lane == 0) {
+        float *e = bsum + (warp * 2 + ((a_mid && carry_p == pa0) ? 0 : 1)) * PAIR_BND;
+        e[0] = __int_as_float(carry_p);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            e[1 + m] = carry[0][m];
+            e[17 + m] = carry[1][m];
+        }
+    }
+    consumer_sync<NCONS>();
+    // pairs shared by consecutive warps: their sums added in warp order (lane m: token m)
+    if (warp == 0) {
+        int cur = -1;
+        float acc0 = 0.0f, acc1 = 0.0f;
+        for (int w = 0; w < NCW; ++w) {
+            for (int side = 0; side < 2; ++side) {
+                const float *e = bsum + (w * 2 + side) * PAIR_BND;
+                const int r = __float_as_int(e[0]);
+                if (r < 0) continue;
+                if (r != cur) {
+                    if (cur >= 0 && lane < ntok) store_pair(cur, lane, acc0, acc1);
+                    cur = r;
+                    acc0 = acc1 = 0.0f;
+                }
+                if (lane < ntok) {
+                    acc0 += e[1 + lane];
+                    acc1 += e[17 + lane];
+                }
+            }
+        }
+        if (cur >= 0 && lane < ntok) store_pair(cur, lane, acc0, acc1);
+    }
+}
+
 }  // namespace qg

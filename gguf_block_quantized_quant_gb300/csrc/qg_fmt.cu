@@ -23,11 +23,16 @@ using ic = std::integral_constant<int, V>;
 
 // Each kernel instantiation opts in to the full shared memory once per device; launches
 // use programmatic stream serialization (see griddep_wait in qg_common.cuh).
-template <int FMT, int T, int MT, int NCW, class Job>
+template <int FMT, int T, int MT, int NCW, class Job, bool PAIR = false>
 int launch_engine(const Job &job, int grid, uint32_t smem, cudaStream_t s) {
     static std::mutex mu;
     static bool ready[64] = {};
-    auto kern = engine_kernel<FMT, T, MT, NCW, Job>;
+    auto kern = [] {
+        if constexpr (PAIR)
+            return engine_pair_kernel<FMT, T, MT, NCW, Job>;
+        else
+            return engine_kernel<FMT, T, MT, NCW, Job>;
+    }();
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
     {
@@ -78,6 +83,30 @@ int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, c
     case 8: return launch_engine_ncw<FMT, T, 8>(ncw, job, grid, smem, s);
     case 16: return launch_engine_ncw<FMT, T, 16>(ncw, job, grid, smem, s);
     default: return -1;
+    }
+}
+
+// The row-pair engine (engine_pair_kernel) for plain GEMV: Q4_K one-superblock and Q4_0
+// 8-block tasks of two rows; ncw is 8 or 12 (see plan_gemv).
+template <int FMT, int T, class Job>
+int launch_pair(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
+    if constexpr ((FMT == F_Q4_K && T == 1) || (FMT == F_Q4_0 && T == 8)) {
+        auto go = [&](auto MTc) {
+            constexpr int M = decltype(MTc)::value;
+            if (M == 1 && ncw == NCW_WIDE) return launch_engine<FMT, T, M, NCW_WIDE, Job, true>(job, grid, smem, s);
+            if (ncw != 8) return -1;
+            return launch_engine<FMT, T, M, 8, Job, true>(job, grid, smem, s);
+        };
+        switch (MT) {
+        case 1: return go(ic<1>{});
+        case 2: return go(ic<2>{});
+        case 4: return go(ic<4>{});
+        case 8: return go(ic<8>{});
+        case 16: return go(ic<16>{});
+        default: return -1;
+        }
+    } else {
+        return -1;
     }
 }
 
@@ -140,6 +169,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.out = out;
         j.slice_stride = (long)c.M * c.N;
+        if (p.pair) return launch_pair<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
         return launch_engine_mt<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
     });
     if (rc) return rc;

@@ -227,6 +227,20 @@ struct FmtLegacy {
                                                 SAddr tile, float xd, int xs, float xq, Sink &sink) {
         uint32_t x[8];
         ldx8(tile + 32 * u, x);
+        const int dot = unit_dot(c, qh, x, xs);
+        if constexpr (Sink::DOTS) {
+            sink.unit(m, u, dot, xs);
+        } else {
+            float v = d * xd * (float)dot;
+            if constexpr (HAS_M) v = fmaf(mv, xq, v);
+            sink.add(m, v);
+        }
+    }
+
+    // The exact integer dot of one block (codes c, fifth bits qh) with activation codes x
+    // (sum xs), the format's code offset included.
+    __device__ __forceinline__ static int unit_dot(const uint32_t (&c)[8], uint32_t qh, const uint32_t (&x)[8],
+                                                   int xs) {
         int dot = 0;
         if constexpr (FMT == F_Q8_0) {
 #pragma unroll
@@ -258,12 +272,57 @@ struct FmtLegacy {
                 dot = dp4a(hi, x[4 + k], dot);
             }
         }
-        if constexpr (Sink::DOTS) {
-            sink.unit(m, u, dot, xs);
-        } else {
-            float v = d * xd * (float)dot;
-            if constexpr (HAS_M) v = fmaf(mv, xq, v);
-            sink.add(m, v);
+        return dot;
+    }
+
+    // Two rows' tasks of the same columns (w0: row 0, w1: row 1; T = 4 or 8 blocks each)
+    // against the same activation tiles: every activation load serves both rows.  Per row
+    // the arithmetic and its order are compute()'s.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], const uint32_t (&w1)[WW],
+                                                        const XT &xt, int ntok, PSink &sink) {
+        static_assert(T == 4 || T == 8, "row pairs take 4- or 8-block tasks");
+        using TL = Tile<XGT>;
+#pragma unroll
+        for (int g = 0; g < T / 4; ++g) {
+            float d[2][4], mv[2][4];
+            uint32_t qh[2][4], c[2][4][8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int off = BS * (4 * g + i);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t(&w)[WW] = r ? w1 : w0;
+                    d[r][i] = half_bits_to_float((off & 3) ? (w[off >> 2] >> 16) : w[off >> 2]);
+                    mv[r][i] = HAS_M ? half_bits_to_float(word_at(w, off + 2)) : 0.0f;
+                    qh[r][i] = HAS_QH ? word_at(w, off + QH_OFF) : 0u;
+#pragma unroll
+                    for (int k = 0; k < NQW; ++k) c[r][i][k] = word_at(w, off + QS_OFF + 4 * k);
+                }
+            }
+            const int u0 = 4 * g;
+#pragma unroll
+            for (int m = 0; m < PSink::MT; ++m) {
+                if (m < ntok) {
+                    const SAddr tl = xt.tile(m);
+                    uint32_t xd[4], xs[4] = {0u, 0u, 0u, 0u}, xq[4] = {0u, 0u, 0u, 0u};
+                    ld4(tl + TL::D + 4 * u0, xd);
+                    if constexpr (FMT == F_Q4_0 || FMT == F_Q5_0) ld4(tl + TL::S + 4 * u0, xs);
+                    if constexpr (HAS_M) ld4(tl + TL::Q + 4 * u0, xq);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t x[8];
+                        ldx8(tl + 32 * (u0 + i), x);
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const int dot = unit_dot(c[r][i], qh[r][i], x, (int)xs[i]);
+                            float v = d[r][i] * __uint_as_float(xd[i]) * (float)dot;
+                            if constexpr (HAS_M) v = fmaf(mv[r][i], __uint_as_float(xq[i]), v);
+                            sink.add(r, m, v);
+                        }
+                    }
+                }
+            }
         }
     }
 
@@ -598,6 +657,66 @@ struct FmtQ4K {
         const int sw = swap();
 #pragma unroll
         for (int i = 0; i < T; ++i) superblock(w + 36 * i, 8 * (i ^ sw), xt, ntok, sink);
+    }
+
+    // Two rows' superblocks of the same column (T == 1) against the same activation tile:
+    // every activation load serves both rows.  Per row the arithmetic and its order are
+    // superblock()'s.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], const uint32_t (&w1)[WW],
+                                                        const XT &xt, int ntok, PSink &sink) {
+        static_assert(T == 1, "row pairs take one-superblock tasks");
+        using TL = Tile<XGT>;
+        constexpr int MT = PSink::MT;
+        uint32_t S03[2], M03[2], S47[2], M47[2];
+        float d[2], dmin[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint32_t(&w)[WW] = r ? w1 : w0;
+            S03[r] = w[1] & 0x3f3f3f3fu;
+            M03[r] = w[2] & 0x3f3f3f3fu;
+            S47[r] = (w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u);
+            M47[r] = ((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u);
+            d[r] = half_bits_to_float(w[0]);
+            dmin[r] = half_bits_to_float(w[0] >> 16);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            uint32_t xd[8], xq[8];
+            ld4(t + TL::D, xd);
+            ld4(t + TL::D + 16, xd + 4);
+            ld4(t + TL::Q, xq);
+            ld4(t + TL::Q + 16, xq + 4);
+            float A[2] = {0.0f, 0.0f}, B[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t xa[8], xb[8];
+                ldx8(t + 64 * p, xa);
+                ldx8(t + 64 * p + 32, xb);
+                const int k0 = 2 * (p & 1);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t(&w)[WW] = r ? w1 : w0;
+                    const uint32_t *q = w + 4 + 8 * p;
+                    const uint32_t Sw = p < 2 ? S03[r] : S47[r], Mw = p < 2 ? M03[r] : M47[r];
+                    int da = 0, db = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da = dp4a(q[k] & 0x0f0f0f0fu, xa[k], da);
+                        db = dp4a_us(q[k] & 0xf0f0f0f0u, xb[k], db);
+                    }
+                    db >>= 4;
+                    A[r] = fmaf(__uint_as_float(xd[2 * p]), (float)(byte_of(Sw, k0) * da), A[r]);
+                    A[r] = fmaf(__uint_as_float(xd[2 * p + 1]), (float)(byte_of(Sw, k0 + 1) * db), A[r]);
+                    B[r] = fmaf(__uint_as_float(xq[2 * p]), (float)byte_of(Mw, k0), B[r]);
+                    B[r] = fmaf(__uint_as_float(xq[2 * p + 1]), (float)byte_of(Mw, k0 + 1), B[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) sink.add(r, m, fmaf(d[r], A[r], -dmin[r] * B[r]));
+        }
     }
 
     template <class Sink>

@@ -62,6 +62,9 @@ struct TaskGeo {
     uint32_t rb = 0;
     uint32_t bytes_of(int ntask) const { return (uint32_t)(((ntask + TPB - 1) / TPB) * BPT * bs); }
     int task_bytes() const { return BPT * bs / TPB; }
+    // every task of every row starts 16-byte aligned (rows start at multiples of rb from a
+    // 16-byte-aligned tensor): runs need no widening
+    bool aligned16() const { return task_bytes() % 16 == 0 && rb % 16 == 0; }
 };
 inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     TaskGeo g;
@@ -98,6 +101,24 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     return g;
 }
 inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
+
+// Geometry of one row's part of a row-pair task (engine_pair_kernel): Q4_K one superblock,
+// Q4_0 eight blocks (rows whose block count is a multiple of 8); not ok for other formats.
+inline TaskGeo pair_geo(int fmt, int K) {
+    TaskGeo g = task_geo(fmt, K, false);
+    if (!g.ok) return g;
+    if (fmt == 12) {
+        g.T = 1, g.BPT = 1, g.XGT = 8, g.gpr = g.nbr;
+    } else if (fmt == 2 && g.nbr % 8 == 0) {
+        g.T = 8, g.BPT = 8, g.XGT = 8, g.gpr = g.nbr / 8;
+    } else {
+        g.ok = false;
+        return g;
+    }
+    g.tpr = g.gpr;
+    g.stride = tile_stride(g.XGT);
+    return g;
+}
 // Warps of a launch whose CTAs hold up to tasks_per_cta tasks.
 inline int plan_ncw(const TaskGeo &g, int MT, long tasks_per_cta) {
     if (ncw_wide_allowed(g.task_bytes(), MT) && tasks_per_cta >= (long)NCW_WIDE * 32 * 2) return NCW_WIDE;
@@ -144,11 +165,30 @@ inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_b
     return r;
 }
 
+// Ring of a row-pair launch: stages of 32 two-row tasks, at most PAIR_RUNS runs each.
+inline Ring plan_ring_pair(const TaskGeo &g, uint32_t x_bytes, int ncw) {
+    Ring r;
+    r.x_bytes = (uint32_t)align_up(x_bytes, 16);
+    const long avail = (long)SMEM_MAX - (long)pair_fixed_smem(ncw * DMAX, ncw) - (long)r.x_bytes;
+    const uint32_t slot =
+        (uint32_t)align_up(2u * g.bytes_of(32) + (g.aligned16() ? 0u : 32u * PAIR_RUNS), 16);
+    const long d = avail / ((long)ncw * (slot + STAGE_SLACK));
+    if (d < 1) return r;
+    r.tps = 32;
+    r.slot_bytes = slot;
+    r.depth = (int)std::min<long>(DMAX, d);
+    const int S = ncw * r.depth;
+    r.smem_total = (uint32_t)S * (r.slot_bytes + STAGE_SLACK) + r.x_bytes + pair_fixed_smem(S, ncw);
+    r.ok = r.smem_total <= (uint32_t)SMEM_MAX;
+    return r;
+}
+
 // ----------------------------------------------------------------------------- GEMV
 struct GemvPlan {
     bool ok = false;
     TaskGeo geo;
     int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0, ncw = 8;
+    bool pair = false;  // row-pair engine: tasks of two rows (engine_pair_kernel)
     Ring ring;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
@@ -170,6 +210,28 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     p.ncw = plan_ncw(g, p.MT, (long)((N + p.groups - 1) / p.groups) * p.tpr_x);
     p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, p.ncw);
     if (!p.ring.ok) return p;
+    // row pairs: an un-split GEMV of Q4_K or Q4_0 (8-block tasks) with at least two rows
+    // and two tokens (with one token the one-row tasks measured faster)
+    if (p.KS == 1 && N >= 2 && p.MT >= 2) {
+        const TaskGeo pg = pair_geo(fmt, K);
+        const long px = (long)M * pg.tpr * pg.stride;
+        if (pg.ok && px <= (long)XCAP) {
+            const int P = (N + 1) / 2, pgroups = std::min(P, sms);
+            const int tb2 = 2 * pg.task_bytes();
+            const long tasks_cta = (long)((P + pgroups - 1) / pgroups) * pg.tpr;
+            const int pncw = ncw_wide_allowed(tb2, p.MT) && tasks_cta >= (long)NCW_WIDE * 32 * 2 ? NCW_WIDE
+                                                                                               : engine_ncw(tb2, p.MT);
+            const Ring pr = plan_ring_pair(pg, (uint32_t)px, pncw);
+            if (pr.ok) {
+                p.pair = true;
+                p.geo = pg;
+                p.groups = p.grid = pgroups;
+                p.tpr_x = pg.tpr;
+                p.ncw = pncw;
+                p.ring = pr;
+            }
+        }
+    }
     size_t o = 0;
     p.ximg_pitch = (size_t)g.tpr * g.stride;
     p.ws_ximg = o;
