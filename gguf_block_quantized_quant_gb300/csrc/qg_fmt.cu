@@ -146,6 +146,30 @@ void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
 
 }  // namespace
 
+// A row-pair GEMV plan (p.pair) of N rows against an activation tile image that is already
+// written (ximg, per-token pitch ximg_pitch, tiles of p.geo.XGT units): out = W x.
+template <int FMT>
+int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8_t *ximg, size_t ximg_pitch,
+                  float *out, cudaStream_t stream) {
+    return with_t<false>(p.geo, [&](auto Tc) {
+        constexpr int T = decltype(Tc)::value;
+        GemvJob<FMT, T> j;
+        set_engine(j, p.ring, p.tpr_x, M);
+        j.W = W;
+        j.Wend = W + (size_t)N * p.geo.rb;
+        j.N = N;
+        j.KS = 1;
+        j.groups = p.groups;
+        j.gpr = p.geo.gpr;
+        j.rb = p.geo.rb;
+        j.ximg = ximg;
+        j.ximg_pitch = (uint32_t)ximg_pitch;
+        j.out = out;
+        j.slice_stride = (long)M * N;
+        return launch_pair<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, stream);
+    });
+}
+
 template <int FMT>
 int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
@@ -193,10 +217,18 @@ int ffn_run(const FfnCall &c, int sms) {
     float *g = reinterpret_cast<float *>(c.ws + p.ws_g);
     float *u = reinterpret_cast<float *>(c.ws + p.ws_u);
     float *h = reinterpret_cast<float *>(c.ws + p.ws_h);
-    int rc = launch_prep_tiles(c.x, nullptr, nullptr, nullptr, nullptr, nullptr, c.M, c.H, log2i(p.geo.XGT), ximg,
-                               nullptr, nullptr, nullptr, c.stream);
+    const int xgt = p.gate.pair ? p.gate.geo.XGT : p.geo.XGT;
+    int rc = launch_prep_tiles(c.x, nullptr, nullptr, nullptr, nullptr, nullptr, c.M, c.H, log2i(xgt), ximg, nullptr,
+                               nullptr, nullptr, c.stream);
     if (rc) return rc;
-    for (int ch = 0; ch < p.nchunk; ++ch) {
+    if (p.gate.pair) {
+        // several tokens: gate and up as two row-pair launches on the same tile image
+        rc = gemv_pair_run<FMT>(p.gate, c.Wg, c.I, c.M, ximg, p.ximg_pitch, g, c.stream);
+        if (rc) return rc;
+        rc = gemv_pair_run<FMT>(p.gate, c.Wu, c.I, c.M, ximg, p.ximg_pitch, u, c.stream);
+        if (rc) return rc;
+    }
+    for (int ch = 0; ch < (p.gate.pair ? 0 : p.nchunk); ++ch) {
         const int m0 = ch * p.MC, mc = std::min(p.MC, c.M - m0);
         rc = with_t<true>(p.geo, [&](auto Tc) {
             constexpr int T = decltype(Tc)::value;

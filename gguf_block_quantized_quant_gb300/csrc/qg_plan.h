@@ -251,6 +251,7 @@ struct FfnPlan {
     TaskGeo geo;
     int grid = 1, MT = 1, MC = 1, nchunk = 1, ncw = 8;
     Ring ring;
+    GemvPlan gate;  // several tokens: gate and up as two row-pair GEMV launches (gate.pair)
     GemvPlan down;  // y = Wd h; h = silu(g) * u is formed by its activation preparation
     size_t ws_ximg = 0, ximg_pitch = 0, ws_g = 0, ws_u = 0, ws_h = 0, ws_down = 0, ws_total = 0;
 };
@@ -271,8 +272,9 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     if (!p.ring.ok) return p;
     p.down = plan_gemv(fmt, H, I, M, sms);
     if (!p.down.ok) return p;
+    if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
     size_t o = 0;
-    p.ximg_pitch = (size_t)tiles;
+    p.ximg_pitch = (size_t)(p.gate.pair ? p.gate.ximg_pitch : tiles);
     p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);
     p.ws_g = o; o = align_up(o + 4ull * M * I, 256);
     p.ws_u = o; o = align_up(o + 4ull * M * I, 256);
