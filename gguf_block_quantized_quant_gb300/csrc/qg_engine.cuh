@@ -374,10 +374,10 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
 
 // ===================================================================================
 // Row-pair engine (plain GEMV with whole rows per CTA).  A task is the same column block
-// of two adjacent rows (one superblock or 4 / 8 blocks of each), so every activation-tile
+// of two adjacent rows (one superblock, or 8 Q4_0 blocks, of each), so every activation-tile
 // load of a lane serves both rows: half the tile traffic of one-row tasks of the same
-// size, and tasks 144 bytes apart (an odd number of 16-byte chunks) load without bank
-// conflicts.  The CTA owns row pairs [p0, p1); tasks are ordered pair by pair, column by
+// size (and Q4_K / Q4_0 tasks 144 bytes apart, an odd number of 16-byte chunks, load
+// without bank conflicts).  The CTA owns row pairs [p0, p1); tasks are ordered pair by pair, column by
 // column.  A stage's bytes are at most three runs of the row-major matrix: the first
 // pair's first row from the stage's first column, everything from that pair's second row
 // (same column) through the last pair's first row, and the last pair's second row up to
@@ -532,6 +532,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
         const bool valid = f < fb;
         int p = 0x7fffffff, c = 0;
         uint32_t w0[F::WW], w1[F::WW];
+        uint32_t al0 = 0, al1 = 0;
         SAddr xbase = smem;
         if (valid) {
             const int pa = (int)tpr_div.div((uint32_t)fa), ca = fa - pa * tpr;
@@ -552,6 +553,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
                 addr1 = h1 + (uint32_t)((r0 - ra) * tpr + c - ca) * TB;
             F::load(addr0, w0);
             F::load(addr1, w1);
+            al0 = (uint32_t)((uintptr_t)addr0 & 3u);
+            al1 = (uint32_t)((uintptr_t)addr1 & 3u);
             xbase = smem + (xa - ring) + (uint32_t)(c * TL::STRIDE);
         }
         __syncwarp();
@@ -563,7 +566,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
             PairSink<MT> sink;
 #pragma unroll
             for (int m = 0; m < MT; ++m) sink.acc[0][m] = sink.acc[1][m] = 0.0f;
-            if (valid) F::compute_pair(w0, w1, XT{xbase, tok_stride}, ntok, sink);
+            if (valid) F::compute_pair(w0, al0, w1, al1, XT{xbase, tok_stride}, ntok, sink);
             // segmented reduction: pairs are contiguous runs of lanes
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {

@@ -86,23 +86,21 @@ int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, c
     }
 }
 
-// The row-pair engine (engine_pair_kernel) for plain GEMV: Q4_K one-superblock and Q4_0
-// 8-block tasks of two rows; ncw is 8 or 12 (see plan_gemv).
+// The row-pair engine (engine_pair_kernel) for plain GEMV with two or more tokens: Q4_K,
+// Q5_K and Q6_K one-superblock and Q4_0 8-block tasks of two rows, on 8 warps.
 template <int FMT, int T, class Job>
 int launch_pair(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
-    if constexpr ((FMT == F_Q4_K && T == 1) || (FMT == F_Q4_0 && T == 8)) {
-        auto go = [&](auto MTc) {
-            constexpr int M = decltype(MTc)::value;
-            if (M == 1 && ncw == NCW_WIDE) return launch_engine<FMT, T, M, NCW_WIDE, Job, true>(job, grid, smem, s);
-            if (ncw != 8) return -1;
-            return launch_engine<FMT, T, M, 8, Job, true>(job, grid, smem, s);
-        };
+    if constexpr ((FMT == F_Q4_K && T == 1) || (FMT == F_Q4_0 && T == 8) || FMT == F_Q5_K || FMT == F_Q6_K) {
+        if (ncw != 8) return -1;
         switch (MT) {
-        case 1: return go(ic<1>{});
-        case 2: return go(ic<2>{});
-        case 4: return go(ic<4>{});
-        case 8: return go(ic<8>{});
-        case 16: return go(ic<16>{});
+        case 2: return launch_engine<FMT, T, 2, 8, Job, true>(job, grid, smem, s);
+        case 4: return launch_engine<FMT, T, 4, 8, Job, true>(job, grid, smem, s);
+        case 8: return launch_engine<FMT, T, 8, 8, Job, true>(job, grid, smem, s);
+        case 16:
+            if constexpr (FMT == F_Q5_K || FMT == F_Q6_K)
+                return -1;  // not planned: see plan_gemv
+            else
+                return launch_engine<FMT, T, 16, 8, Job, true>(job, grid, smem, s);
         default: return -1;
         }
     } else {

@@ -279,8 +279,8 @@ struct FmtLegacy {
     // against the same activation tiles: every activation load serves both rows.  Per row
     // the arithmetic and its order are compute()'s.
     template <class PSink>
-    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], const uint32_t (&w1)[WW],
-                                                        const XT &xt, int ntok, PSink &sink) {
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], uint32_t, const uint32_t (&w1)[WW],
+                                                        uint32_t, const XT &xt, int ntok, PSink &sink) {
         static_assert(T == 4 || T == 8, "row pairs take 4- or 8-block tasks");
         using TL = Tile<XGT>;
 #pragma unroll
@@ -663,8 +663,8 @@ struct FmtQ4K {
     // every activation load serves both rows.  Per row the arithmetic and its order are
     // superblock()'s.
     template <class PSink>
-    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], const uint32_t (&w1)[WW],
-                                                        const XT &xt, int ntok, PSink &sink) {
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], uint32_t, const uint32_t (&w1)[WW],
+                                                        uint32_t, const XT &xt, int ntok, PSink &sink) {
         static_assert(T == 1, "row pairs take one-superblock tasks");
         using TL = Tile<XGT>;
         constexpr int MT = PSink::MT;
@@ -806,6 +806,62 @@ struct FmtQ5K {
         }
     }
 
+    // Two rows' superblocks of the same column against the same activation tile (every
+    // activation load serves both rows); per row the arithmetic and its order are compute()'s.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], uint32_t, const uint32_t (&w1)[WW],
+                                                        uint32_t, const XT &xt, int ntok, PSink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = PSink::MT;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m >= ntok) continue;
+            const SAddr t = xt.tile(m);
+            uint32_t xd[8], xq[8];
+            ld4(t + TL::D, xd);
+            ld4(t + TL::D + 16, xd + 4);
+            ld4(t + TL::Q, xq);
+            ld4(t + TL::Q + 16, xq + 4);
+            float A[2] = {0.0f, 0.0f}, B[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int j0 = 4 * hf + 2 * pp;
+                    uint32_t xa[8], xb[8];
+                    ldx8(t + 32 * j0, xa);
+                    ldx8(t + 32 * j0 + 32, xb);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const uint32_t(&w)[WW] = r ? w1 : w0;
+                        const uint32_t *qh = w + 4;
+                        const uint32_t Sw =
+                            hf ? ((w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u)) : (w[1] & 0x3f3f3f3fu);
+                        const uint32_t Mw =
+                            hf ? (((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u)) : (w[2] & 0x3f3f3f3fu);
+                        const uint32_t *q = w + 12 + 8 * (2 * hf + pp);
+                        int da = 0, db = 0;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            da = dp4a((q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4), xa[k], da);
+                            db = dp4a(((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4), xb[k],
+                                      db);
+                        }
+                        A[r] = fmaf(__uint_as_float(xd[j0]), (float)(byte_of(Sw, 2 * pp) * da), A[r]);
+                        A[r] = fmaf(__uint_as_float(xd[j0 + 1]), (float)(byte_of(Sw, 2 * pp + 1) * db), A[r]);
+                        B[r] = fmaf(__uint_as_float(xq[j0]), (float)byte_of(Mw, 2 * pp), B[r]);
+                        B[r] = fmaf(__uint_as_float(xq[j0 + 1]), (float)byte_of(Mw, 2 * pp + 1), B[r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t(&w)[WW] = r ? w1 : w0;
+                sink.add(r, m, fmaf(half_bits_to_float(w[0]), A[r], -half_bits_to_float(w[0] >> 16) * B[r]));
+            }
+        }
+    }
+
     template <class Sink>
     __device__ __forceinline__ static void run(SAddr addr, int hf, const XT &xt, int ntok, Sink &sink) {
         uint32_t w[WW];
@@ -909,6 +965,98 @@ struct FmtQ6K {
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < ntok) sink.add(m, d * A[m]);
+        }
+    }
+
+    // Two rows' superblocks of the same column (each with its own 2-byte alignment a0, a1)
+    // against the same activation tile; per row the arithmetic and its order are compute()'s.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], uint32_t a0,
+                                                        const uint32_t (&w1)[WW], uint32_t a1, const XT &xt, int ntok,
+                                                        PSink &sink) {
+        using TL = Tile<XGT>;
+        constexpr int MT = PSink::MT;
+        const uint32_t sel[2] = {a0 ? 0x5432u : 0x3210u, a1 ? 0x5432u : 0x3210u};
+        float A[2][MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) A[0][m] = A[1][m] = 0.0f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t hw[2][8], scA[2], scB[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t(&w)[WW] = r ? w1 : w0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hw[r][k] = prmt(w[32 + 8 * hf + k], w[33 + 8 * hf + k], sel[r]);
+                scA[r] = prmt(w[48 + 2 * hf], w[49 + 2 * hf], sel[r]);
+                scB[r] = prmt(w[49 + 2 * hf], w[50 + 2 * hf], sel[r]);
+            }
+            constexpr bool VEC = MT <= 4;
+            uint32_t xdv[VEC ? MT : 1][4], xhv[VEC ? MT : 1][4];
+            if constexpr (VEC) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < ntok) {
+                        ld4(xt.tile(m) + TL::D + 16 * hf, xdv[m]);
+                        ld4(xt.tile(m) + TL::H + 16 * hf, xhv[m]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                uint32_t lw[2][8];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t(&w)[WW] = r ? w1 : w0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        lw[r][k] = prmt(w[16 * hf + 8 * s + k], w[16 * hf + 8 * s + k + 1], sel[r]);
+                }
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = s + 2 * tt, u = 4 * hf + t;
+                    uint32_t c[2][8];
+                    int sA[2], sB[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            c[r][k] = ((lw[r][k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[r][k] >> (2 * t)) & 0x03030303u) << 4);
+                        const uint32_t scw = t < 2 ? scA[r] : scB[r];
+                        sA[r] = (int)(int8_t)((scw >> (16 * (t & 1))) & 255u);
+                        sB[r] = (int)(int8_t)((scw >> (16 * (t & 1) + 8)) & 255u);
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (m < ntok) {
+                            const SAddr tl = xt.tile(m);
+                            uint32_t x[8];
+                            ldx8(tl + 32 * u, x);
+                            const uint32_t xh = VEC ? xhv[VEC ? m : 0][t] : lds32(tl + TL::H + 4 * u);
+                            const float xd = VEC ? __uint_as_float(xdv[VEC ? m : 0][t]) : ldsf(tl + TL::D + 4 * u);
+                            const int hlo = (int)(int16_t)(xh & 0xffffu), hhi = (int)(int16_t)(xh >> 16);
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                int lo = 0, hi = 0;
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) lo = dp4a(c[r][k], x[k], lo);
+#pragma unroll
+                                for (int k = 4; k < 8; ++k) hi = dp4a(c[r][k], x[k], hi);
+                                const int dot = sA[r] * (lo - 32 * hlo) + sB[r] * (hi - 32 * hhi);
+                                A[r][m] = fmaf(xd, (float)dot, A[r][m]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint32_t(&w)[WW] = r ? w1 : w0;
+            const float d = half_bits_to_float(w[52] >> (8 * (r ? a1 : a0)));
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(r, m, d * A[r][m]);
         }
     }
 

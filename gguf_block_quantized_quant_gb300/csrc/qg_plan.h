@@ -102,13 +102,16 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
 }
 inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
 
-// Geometry of one row's part of a row-pair task (engine_pair_kernel): Q4_K one superblock,
-// Q4_0 eight blocks (rows whose block count is a multiple of 8); not ok for other formats.
+// Geometry of one row's part of a row-pair task (engine_pair_kernel): one Q4_K, Q5_K or
+// Q6_K superblock, or eight Q4_0 blocks (rows whose block count is a multiple of 8); not
+// ok for other formats.
 inline TaskGeo pair_geo(int fmt, int K) {
     TaskGeo g = task_geo(fmt, K, false);
     if (!g.ok) return g;
     if (fmt == 12) {
         g.T = 1, g.BPT = 1, g.XGT = 8, g.gpr = g.nbr;
+    } else if (fmt == 13 || fmt == 14) {
+        g.T = 2, g.BPT = 1, g.XGT = 8, g.gpr = g.nbr;  // the whole-superblock task of these formats
     } else if (fmt == 2 && g.nbr % 8 == 0) {
         g.T = 8, g.BPT = 8, g.XGT = 8, g.gpr = g.nbr / 8;
     } else {
@@ -215,12 +218,12 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     if (p.KS == 1 && N >= 2 && p.MT >= 2) {
         const TaskGeo pg = pair_geo(fmt, K);
         const long px = (long)M * pg.tpr * pg.stride;
-        if (pg.ok && px <= (long)XCAP) {
+        // Q5_K / Q6_K pairs hold 88 / 108 words of weights: at 16 tokens per lane they ran
+        // out of registers and were slower than one-row tasks
+        const bool regs_ok = p.MT <= 8 || (fmt != 13 && fmt != 14);
+        if (pg.ok && px <= (long)XCAP && regs_ok) {
             const int P = (N + 1) / 2, pgroups = std::min(P, sms);
-            const int tb2 = 2 * pg.task_bytes();
-            const long tasks_cta = (long)((P + pgroups - 1) / pgroups) * pg.tpr;
-            const int pncw = ncw_wide_allowed(tb2, p.MT) && tasks_cta >= (long)NCW_WIDE * 32 * 2 ? NCW_WIDE
-                                                                                               : engine_ncw(tb2, p.MT);
+            const int pncw = 8;  // two-row tasks of 288 to 420 bytes and two or more tokens per lane
             const Ring pr = plan_ring_pair(pg, (uint32_t)px, pncw);
             if (pr.ok) {
                 p.pair = true;
