@@ -374,15 +374,16 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
 
 // ===================================================================================
 // Row-pair engine (plain GEMV with whole rows per CTA).  A task is the same column block
-// of two adjacent rows (one superblock, or 8 Q4_0 blocks, of each), so every activation-tile
-// load of a lane serves both rows: half the tile traffic of one-row tasks of the same
-// size (and Q4_K / Q4_0 tasks 144 bytes apart, an odd number of 16-byte chunks, load
-// without bank conflicts).  The CTA owns row pairs [p0, p1); tasks are ordered pair by pair, column by
-// column.  A stage's bytes are at most three runs of the row-major matrix: the first
-// pair's first row from the stage's first column, everything from that pair's second row
-// (same column) through the last pair's first row, and the last pair's second row up to
-// the stage's last column.  Ring, barriers, refill, carries and the combine of pairs
-// shared by two warps work as in engine_kernel, with two sums per token.
+// of two adjacent rows (one superblock, or 4 or 8 32-element blocks, of each), so every
+// activation-tile load of a lane serves both rows: half the tile traffic of one-row tasks
+// of the same size (and Q4_K / Q4_0 tasks 144 bytes apart, an odd number of 16-byte
+// chunks, load without bank conflicts).  The CTA owns row pairs [p0, p1); tasks are
+// ordered pair by pair, column by column.  A stage's bytes are at most three runs of the
+// row-major matrix: the first pair's first row from the stage's first column, everything
+// from that pair's second row (same column) through the last pair's first row, and the
+// last pair's second row up to the stage's last column.  Ring, barriers, refill, carries
+// and the combine of pairs shared by two warps work as in engine_kernel, with two sums
+// per token.
 constexpr int PAIR_BND = 1 + 2 * 16;  // boundary entry: pair, then row-0 and row-1 sums
 constexpr int PAIR_RUNS = 3;
 __host__ __device__ constexpr uint32_t pair_fixed_smem(int S, int ncw) {
