@@ -87,11 +87,11 @@ int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, c
 }
 
 // The row-pair engine (engine_pair_kernel) for plain GEMV with two or more tokens: Q4_K,
-// Q5_K and Q6_K one-superblock, Q4_0 / IQ4_NL 8-block and Q8_0 / Q4_1 / Q5_0 / Q5_1
-// 4-block tasks of two rows, on 8 warps.
+// Q5_K, Q6_K and IQ4_XS one-superblock, Q4_0 / IQ4_NL 8-block and Q8_0 / Q4_1 / Q5_0 /
+// Q5_1 4-block tasks of two rows, on 8 warps.
 template <int FMT, int T, class Job>
 int launch_pair(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
-    if constexpr ((FMT == F_Q4_K && T == 1) || ((FMT == F_Q4_0 || FMT == F_IQ4_NL) && T == 8) ||
+    if constexpr (((FMT == F_Q4_K || FMT == F_IQ4_XS) && T == 1) || ((FMT == F_Q4_0 || FMT == F_IQ4_NL) && T == 8) ||
                   ((FMT == F_Q8_0 || FMT == F_Q4_1 || FMT == F_Q5_0 || FMT == F_Q5_1) && T == 4) || FMT == F_Q5_K ||
                   FMT == F_Q6_K) {
         if (ncw != 8) return -1;

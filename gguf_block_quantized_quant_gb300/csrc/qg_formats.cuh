@@ -1149,6 +1149,65 @@ struct FmtIQ4XS {
         }
     }
 
+    // Two rows' superblocks of the same column (T == 1) against the same activation tile;
+    // per row the arithmetic and its order are superblock()'s.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair(const uint32_t (&w0)[WW], uint32_t, const uint32_t (&w1)[WW],
+                                                        uint32_t, const XT &xt, int ntok, PSink &sink) {
+        static_assert(T == 1, "row pairs take one-superblock tasks");
+        using TL = Tile<XGT>;
+        constexpr int MT = PSink::MT;
+        float A[2][MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) A[0][m] = A[1][m] = 0.0f;
+        constexpr bool VEC = MT <= 4;
+        uint32_t xdv[VEC ? MT : 1][8];
+        if constexpr (VEC) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < ntok) {
+                    ld4(xt.tile(m) + TL::D, xdv[m]);
+                    ld4(xt.tile(m) + TL::D + 16, xdv[m] + 4);
+                }
+            }
+        }
+#pragma unroll
+        for (int ib = 0; ib < 8; ++ib) {
+            int ls[2];
+            uint32_t c[2][8];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t(&w)[WW] = r ? w1 : w0;
+                ls[r] = (int)(((w[1] >> (4 * ib)) & 15u) | (((w[0] >> (16 + 2 * ib)) & 3u) << 4));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cb_lookup8(w[2 + 4 * ib + k], c[r][k], c[r][4 + k]);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < ntok) {
+                    const SAddr t = xt.tile(m);
+                    uint32_t x[8];
+                    ldx8(t + 32 * ib, x);
+                    const float xd = VEC ? __uint_as_float(xdv[VEC ? m : 0][ib]) : ldsf(t + TL::D + 4 * ib);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        int dot = 0;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) dot = dp4a(c[r][k], x[k], dot);
+                        A[r][m] = fmaf(xd, (float)((ls[r] - 32) * dot), A[r][m]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float d = half_bits_to_float((r ? w1 : w0)[0]);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < ntok) sink.add(r, m, d * A[r][m]);
+        }
+    }
+
     template <class Sink>
     __device__ __forceinline__ static void compute(const uint32_t (&w)[WW], uint32_t, int, const XT &xt, int ntok,
                                                    Sink &sink) {

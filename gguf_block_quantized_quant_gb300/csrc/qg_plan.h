@@ -102,15 +102,16 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
 }
 inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
 
-// Geometry of one row's part of a row-pair task (engine_pair_kernel): one Q4_K, Q5_K or
-// Q6_K superblock, eight Q4_0 or IQ4_NL blocks, or four Q8_0 / Q4_1 / Q5_0 / Q5_1 blocks
-// (rows whose block count is a multiple of that); not ok for other formats.
+// Geometry of one row's part of a row-pair task (engine_pair_kernel): one Q4_K, Q5_K, Q6_K
+// or IQ4_XS superblock, eight Q4_0 or IQ4_NL blocks, or four Q8_0 / Q4_1 / Q5_0 / Q5_1
+// blocks (rows whose block count is a multiple of that); not ok otherwise (Q2_K and Q3_K,
+// whose decode outweighs their activation traffic, measured no gain from pairs).
 inline TaskGeo pair_geo(int fmt, int K) {
     TaskGeo g = task_geo(fmt, K, false);
     if (!g.ok) return g;
-    if (fmt == 12) {
+    if (fmt == 12 || fmt == 23) {  // Q4_K, IQ4_XS
         g.T = 1, g.BPT = 1, g.XGT = 8, g.gpr = g.nbr;
-    } else if (fmt == 13 || fmt == 14) {
+    } else if (fmt == 13 || fmt == 14) {  // Q5_K, Q6_K
         g.T = 2, g.BPT = 1, g.XGT = 8, g.gpr = g.nbr;  // the whole-superblock task of these formats
     } else if ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0) {
         g.T = 8, g.BPT = 8, g.XGT = 8, g.gpr = g.nbr / 8;
