@@ -119,6 +119,28 @@ def test_gemv_layout_paths(qg, fmt, N, K, M):
                   f"{synth.FORMAT_NAMES[fmt]} N={N} K={K} M={M}")
 
 
+# ----------------------------------------------------------------------------- row pairs
+# Two or more tokens on an un-split GEMV take the row-pair engine (two rows per task) for
+# Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, IQ4_NL, Q4_K, Q5_K, Q6_K and IQ4_XS: odd row counts (the
+# last pair has one row), stages that start and end inside a pair, and 2..16 tokens.
+PAIR_CASES = [(fmt, N, K, M)
+              for fmt, K in [(synth.Q4_K, 1280), (synth.Q4_0, 768), (synth.Q8_0, 384), (synth.Q5_1, 640),
+                             (synth.Q6_K, 2304), (synth.Q5_K, 512), (synth.IQ4_XS, 1024), (synth.IQ4_NL, 1536)]
+              for N, M in [(77, 2), (153, 3), (1001, 5), (2, 16)]]
+
+
+@pytest.mark.parametrize("fmt,N,K,M", PAIR_CASES,
+                         ids=[f"{synth.FORMAT_NAMES[f]}-{n}x{k}-M{m}" for f, n, k, m in PAIR_CASES])
+def test_gemv_row_pairs(qg, fmt, N, K, M):
+    g = np.random.default_rng(7000 + N + K + M + fmt)
+    W = synth.weights(fmt, N, K, g)
+    x = synth.activations(M, K, g)
+    y = host(qg.qg_gemv(fmt, dev(W), dev(x), N))
+    oq, od, os_ = oracle.quantize_act(x)
+    assert_within(y, oracle.gemv_q(fmt, W, oq, od, os_, N, K), oracle.absdot(fmt, W, oq, od, N, K),
+                  f"{synth.FORMAT_NAMES[fmt]} pairs N={N} K={K} M={M}")
+
+
 # ----------------------------------------------------------------------------- full sizes, sampled rows
 FULL = [
     (synth.Q8_0, 1024, 1024),
