@@ -405,23 +405,42 @@ def run_ours(args):
     return 0
 
 
-def _graph_time_us(torch, s, fn, reps: int, warm: int = 3):
+def _eager_time_us(torch, s, fn, reps: int, warm: int = 3):
+    """Mean µs of fn() launched from the host each time (no graph) on stream s."""
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            fn()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            fn()
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def _graph_time_us(torch, s, fn, reps: int, warm: int = 3, per_graph: int = 8):
+    """Mean µs of fn() from CUDA graphs of per_graph calls each (consecutive calls inside a
+    graph overlap through programmatic dependent launch; a graph boundary does not)."""
     with torch.cuda.stream(s):
         for _ in range(warm):
             fn()
         s.synchronize()
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=s):
-            fn()
+            for _ in range(per_graph):
+                fn()
         gr.replay()
         s.synchronize()
+        n = max(1, reps // per_graph)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        for _ in range(reps):
+        for _ in range(n):
             gr.replay()
         e1.record(s)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / reps
+    return e0.elapsed_time(e1) * 1e3 / (n * per_graph)
 
 
 def secondary(qg, torch, dev, s):
@@ -464,9 +483,12 @@ def secondary(qg, torch, dev, s):
         y = torch.empty((M, H), dtype=torch.float32, device=dev)
         ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_MOE_FFN, fq, M, H, H, E, topk, I), dtype=torch.uint8,
                          device=dev)
-        us = _graph_time_us(torch, s, lambda: qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y,
-                                                            ws=ws, stream=s), 200)
-        out[f"MoE FFN Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us, "tokens/s": M / (us * 1e-6)}
+        call = lambda: qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y, ws=ws, stream=s)  # noqa
+        us = _graph_time_us(torch, s, call, 200)
+        # the same chain launched from the host call by call: the launch gaps a graph removes
+        ue = _eager_time_us(torch, s, call, 200)
+        out[f"MoE FFN Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us, "tokens/s": M / (us * 1e-6),
+                                                                  "us_eager": ue}
     del Wg, Wu, Wd
     # FFN sublayer: H=5120, I=17408 (150 / 219 MB of weights: larger than L2)
     H, I = 5120, 17408
@@ -481,8 +503,11 @@ def secondary(qg, torch, dev, s):
             y = torch.empty((M, H), dtype=torch.float32, device=dev)
             ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), dtype=torch.uint8,
                              device=dev)
-            us = _graph_time_us(torch, s, lambda: qg.qg_ffn_sublayer(fmt, Wg, Wu, Wd, x, I, y=y, ws=ws, stream=s), 20)
-            out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {"us": us, "GB/s": nb / us / 1e3}
+            call = lambda: qg.qg_ffn_sublayer(fmt, Wg, Wu, Wd, x, I, y=y, ws=ws, stream=s)  # noqa: E731
+            us = _graph_time_us(torch, s, call, 20)
+            ue = _eager_time_us(torch, s, call, 20)
+            out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {"us": us, "GB/s": nb / us / 1e3,
+                                                                                 "us_eager": ue}
         del Wg, Wu, Wd
     return out
 
