@@ -1,0 +1,219 @@
+// plan_model.cu -- a host model of the streaming engines' stage layout, checked against the
+// planner for a sweep of shapes (GEMV, FFN sublayer, MoE FFN; every block format; 1..16
+// tokens).  For every CTA, warp and stage of every planned launch it rebuilds, the way the
+// kernels do, the runs of weight bytes a stage copies and the address every lane decodes,
+// and checks: runs stay inside their tensor, the widened runs fit the ring slot, a run's
+// tasks are adjacent in memory, every task is covered once, row-pair lanes find both rows'
+// tasks, and no lane reads past its slot and its slack.  Test infrastructure: compiled and
+// run by tests/test_plan_model.py on the CPU; prints "fails 0" when every check holds.
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <vector>
+#include "qg_plan.h"
+using namespace qg;
+static int fails = 0;
+#define CHECK(c, ...) do { if (!(c)) { ++fails; if (fails < 20) { printf("FAIL %d: ", __LINE__); printf(__VA_ARGS__); printf("\n"); } } } while (0)
+struct Cta { int o0, o1, tpr, grp; };
+static uint32_t toff(const TaskGeo &g, int tt) { return (uint32_t)((tt / g.TPB) * g.BPT * g.bs); }
+
+void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, std::function<Cta(int)> cta,
+         std::function<uintptr_t(int, int, uintptr_t &)> seg) {
+    CHECK(r.ok, "%s ring not ok", name);
+    CHECK(r.smem_total <= (uint32_t)SMEM_MAX, "%s smem %u", name, r.smem_total);
+    for (int b = 0; b < grid; ++b) {
+        Cta c = cta(b);
+        const int ntask = (c.o1 - c.o0) * c.tpr, units = ntask / g.TPB;
+        auto wstart = [&](int w) { return (int)((long)units * w / NCW) * g.TPB; };
+        const int maxlen = (units + NCW - 1) / NCW * g.TPB, nchunk = (maxlen + r.tps - 1) / r.tps;
+        for (int w = 0; w < NCW; ++w)
+            for (int j = 0; j < nchunk; ++j) {
+                const int fa = wstart(w) + j * r.tps, fb = std::min(wstart(w + 1), fa + r.tps);
+                if (fa >= fb) continue;
+                // pieces as the engine forms them: lane p takes group ga + p
+                std::vector<std::pair<int, int>> pcs;
+                if (c.grp == 0) pcs.push_back({fa, fb});
+                else {
+                    const int ga = (c.o0 + fa / c.tpr) / c.grp;
+                    for (int p = 0; p < NPIECE_MAX; ++p) {
+                        const long g0 = (long)(ga + p) * c.grp - c.o0;
+                        const int ps = (int)std::max((long)fa, g0 * c.tpr), pe = (int)std::min((long)fb, (g0 + c.grp) * c.tpr);
+                        if (ps < pe) pcs.push_back({ps, pe});
+                    }
+                    const long cend = ((long)(ga + NPIECE_MAX) * c.grp - c.o0) * c.tpr;
+                    CHECK(cend >= fb, "%s b%d w%d j%d: stage needs more than %d pieces", name, b, w, j, NPIECE_MAX);
+                }
+                uint32_t off = 0;
+                int covered = fa;
+                for (auto &pc : pcs) {
+                    CHECK(pc.first == covered, "%s gap in pieces", name);
+                    CHECK((pc.second - pc.first) % g.TPB == 0, "%s piece not whole blocks", name);
+                    const int o = pc.first / c.tpr, tt = pc.first - o * c.tpr;
+                    uintptr_t lim;
+                    const uintptr_t s0 = seg(c.o0 + o, tt, lim), e = s0 + toff(g, pc.second - pc.first);
+                    CHECK(e <= lim, "%s piece past tensor end", name);
+                    off += (uint32_t)(((e + 15) & ~(uintptr_t)15) - (s0 & ~(uintptr_t)15));
+                    covered = pc.second;
+                }
+                CHECK(covered == fb, "%s stage not covered", name);
+                CHECK(off <= r.slot_bytes, "%s slot overflow %u > %u", name, off, r.slot_bytes);
+            }
+    }
+}
+
+
+// mirrors engine_pair_kernel: runs per stage, slot use, and every lane's two task addresses
+void sim_pair(const char *name, const GemvPlan &p, int N) {
+    const TaskGeo &g = p.geo;
+    const Ring &r = p.ring;
+    CHECK(r.ok, "%s pair ring", name);
+    const int P = (N + 1) / 2, tpr = p.tpr_x, NCW = p.ncw;
+    const long TB = g.task_bytes();
+    for (int cta = 0; cta < p.grid; ++cta) {
+        const int p0 = (int)((long)P * cta / p.grid), p1 = (int)((long)P * (cta + 1) / p.grid);
+        const int ntask = (p1 - p0) * tpr;
+        const int maxlen = (ntask + NCW - 1) / NCW, nchunk = (maxlen + r.tps - 1) / r.tps;
+        for (int w = 0; w < NCW; ++w) {
+            const int a = (int)((long)ntask * w / NCW), b = (int)((long)ntask * (w + 1) / NCW);
+            for (int j = 0; j < nchunk; ++j) {
+                const int fa = a + j * r.tps, fb = std::min(b, fa + r.tps);
+                if (fa >= fb) continue;
+                const int pa = fa / tpr, ca = fa - pa * tpr, pb = (fb - 1) / tpr, cb = fb - 1 - pb * tpr;
+                const int ra = 2 * (p0 + pa), rz = 2 * (p0 + pb);
+                long runrow[3], runcol[3], runn[3];
+                bool valid[3];
+                for (int k = 0; k < 3; ++k) {
+                    int row = 0, col = 0, n = 0;
+                    if (k == 0) { row = ra; col = ca; n = pa == pb ? cb - ca + 1 : tpr - ca; }
+                    else if (k == 1) { row = ra + 1; col = ca; n = pa == pb ? cb - ca + 1 : (tpr - ca) + (rz - ra - 2) * tpr + cb + 1; }
+                    else if (pb > pa) { row = rz + 1; col = 0; n = cb + 1; }
+                    valid[k] = n > 0 && row < N;
+                    runrow[k] = row; runcol[k] = col; runn[k] = n;
+                    if (valid[k]) CHECK((long)row * tpr + col + n <= (long)N * tpr, "%s run past end", name);
+                }
+                // slot offsets (aligned formats: no widening)
+                long off[3], tot = 0;
+                for (int k = 0; k < 3; ++k) {
+                    off[k] = tot;
+                    if (valid[k]) {
+                        const long s0 = (long)runrow[k] * g.rb + runcol[k] * TB;
+                        const long e = s0 + runn[k] * TB;
+                        tot += ((e + 15) & ~15L) - (s0 & ~15L);
+                        off[k] += s0 & 15;
+                    }
+                }
+                CHECK(tot <= (long)r.slot_bytes, "%s slot %ld > %u", name, tot, r.slot_bytes);
+                // every run's tasks in row-major order; find the slot address of (row, col)
+                auto where = [&](long row, long col) -> long {
+                    for (int k = 0; k < 3; ++k) {
+                        if (!valid[k]) continue;
+                        const long idx = (row * tpr + col) - (runrow[k] * tpr + runcol[k]);
+                        if (idx >= 0 && idx < runn[k]) return off[k] + idx * TB;
+                    }
+                    return -1;
+                };
+                for (int l = 0; l < fb - fa; ++l) {
+                    const int f = fa + l, pp = f / tpr, c = f - pp * tpr;
+                    const int r0 = 2 * pp;  // CTA-relative
+                    const long want0 = where(2L * (p0 + pp), c);
+                    CHECK(want0 >= 0, "%s row0 not copied", name);
+                    const long got0 = pp == pa ? off[0] + (long)(c - ca) * TB : off[1] + (long)((r0 - 2 * pa - 1) * tpr + c - ca) * TB;
+                    CHECK(got0 == want0, "%s addr0 %ld != %ld (f %d pa %d pb %d)", name, got0, want0, f, pa, pb);
+                    long got1;
+                    if (2 * (p0 + pp) + 1 >= N) got1 = got0;
+                    else {
+                        got1 = (pb > pa && pp == pb) ? off[2] + (long)c * TB : off[1] + (long)((r0 - 2 * pa) * tpr + c - ca) * TB;
+                        const long want1 = where(2L * (p0 + pp) + 1, c);
+                        CHECK(want1 >= 0 && got1 == want1, "%s addr1 %ld != %ld", name, got1, want1);
+                    }
+                    CHECK(got0 + TB + 8 <= (long)r.slot_bytes + STAGE_SLACK && got1 + TB + 8 <= (long)r.slot_bytes + STAGE_SLACK,
+                          "%s consumer read past slot", name);
+                }
+            }
+        }
+    }
+}
+
+int main() {
+    const int sms = 152;
+    const uintptr_t BASE = 0x7f0000000000ull;
+    int fmts[] = {2, 3, 6, 7, 8, 10, 11, 12, 13, 14, 20, 23};
+    int Ks[] = {32, 96, 256, 512, 544, 768, 1056, 2048, 4096, 5120, 17408, 7168, 14336, 2816};
+    int Ns[] = {1, 2, 3, 5, 37, 64, 75, 76, 151, 152, 153, 300, 1024, 2048, 4096, 5120, 17408};
+    int Ms[] = {1, 2, 3, 4, 5, 8, 16};
+    int nplans = 0, npair = 0;
+    char nm[160];
+    for (int fmt : fmts) for (int K : Ks) for (int N : Ns) for (int M : Ms) {
+        if (!task_geo(fmt, K, true).ok) continue;
+        GemvPlan p = plan_gemv(fmt, N, K, M, sms);
+        if (!p.ok) { CHECK(false, "gemv plan failed fmt %d N %d K %d M %d", fmt, N, K, M); continue; }
+        ++nplans;
+        const TaskGeo &g = p.geo;
+        if (p.pair) {
+            snprintf(nm, sizeof nm, "pair f%d N%d K%d M%d", fmt, N, K, M);
+            sim_pair(nm, p, N);
+            ++npair;
+            continue;
+        }
+        snprintf(nm, sizeof nm, "gemv f%d N%d K%d M%d KS%d", fmt, N, K, M, p.KS);
+        CHECK(p.ring.x_bytes >= (uint32_t)(M * p.tpr_x * g.stride), "%s x bytes", nm);
+        const int KS = p.KS, groups = p.groups, gpr = g.gpr, TPB = g.TPB;
+        sim(nm, g, p.ring, p.grid, p.ncw,
+            [&](int b) { const int gg = b / KS, ks = b % KS; Cta c; c.o0 = (int)((long)gg * N / groups);
+                         c.o1 = (int)((long)(gg + 1) * N / groups); const int t0 = (int)((long)ks * gpr / KS) * TPB;
+                         c.tpr = (int)((long)(ks + 1) * gpr / KS) * TPB - t0; c.grp = KS == 1 ? 0 : 1;
+                         CHECK(c.tpr <= p.tpr_x, "slice tpr"); return c; },
+            [&](int o, int tt, uintptr_t &lim) { lim = BASE + (uintptr_t)N * g.rb; return BASE + (uintptr_t)o * g.rb + toff(g, tt); });
+    }
+    printf("gemv plans %d (row pairs %d)\n", nplans, npair);
+    int Hs[] = {512, 1024, 2048, 4096, 5120, 7168}, Is[] = {256, 512, 1536, 2048, 14336, 17408};
+    for (int fmt : fmts) for (int H : Hs) for (int I : Is) for (int M : Ms) {
+        if (!task_geo(fmt, H, false).ok || !task_geo(fmt, I, false).ok) continue;
+        FfnPlan p = plan_ffn(fmt, M, H, I, sms);
+        if (!p.ok) { CHECK(false, "ffn plan failed fmt %d H %d I %d M %d", fmt, H, I, M); continue; }
+        snprintf(nm, sizeof nm, "ffn f%d H%d I%d M%d", fmt, H, I, M);
+        if (p.gate.pair) {
+            CHECK(p.ximg_pitch >= (size_t)p.gate.tpr_x * p.gate.geo.stride, "%s gate pitch", nm);
+            sim_pair(nm, p.gate, I);
+            ++npair;
+        }
+        const TaskGeo &g = p.geo;
+        sim(nm, g, p.ring, p.grid, p.ncw,
+            [&](int b) { Cta c; c.o0 = (int)((long)b * 2 * I / p.grid); c.o1 = (int)((long)(b + 1) * 2 * I / p.grid);
+                         c.tpr = g.tpr; c.grp = I; return c; },
+            [&](int o, int tt, uintptr_t &lim) { const bool up = o >= I; const uintptr_t base = up ? BASE + (1ull << 36) : BASE;
+                                                 lim = base + (uintptr_t)I * g.rb; return base + (uintptr_t)(up ? o - I : o) * g.rb + toff(g, tt); });
+    }
+    int Es[] = {16, 64, 256}, topks[] = {1, 4, 8}, mH[] = {512, 2048, 4096, 7168}, mI[] = {256, 512, 768, 1536};
+    for (int fmt : fmts) for (int E : Es) for (int topk : topks) for (int H : mH) for (int I : mI) for (int M : Ms) {
+        if (topk > E || !task_geo(fmt, H, false).ok || !task_geo(fmt, I, false).ok) continue;
+        MoePlan p = plan_moe(fmt, M, H, E, topk, I, sms);
+        if (!p.ok) {
+            if ((long)M * task_geo(fmt, H, false).tpr * task_geo(fmt, H, false).stride <= (long)XCAP)
+                CHECK(false, "moe plan failed f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+            continue;
+        }
+        const int S = p.S;
+        snprintf(nm, sizeof nm, "moe-gu f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+        const size_t eb = (size_t)I * p.gh.rb;
+        sim(nm, p.gh, p.gu_ring, p.gu_grid, p.gu_ncw,
+            [&](int b) { const long P = (long)M * S * 2 * I; Cta c; c.o0 = (int)(P * b / p.gu_grid); c.o1 = (int)(P * (b + 1) / p.gu_grid);
+                         c.tpr = p.gh.tpr; c.grp = I; return c; },
+            [&](int o, int tt, uintptr_t &lim) { const int q = o / I, jj = o - q * I, up = q & 1, s = (q >> 1) % S;
+                uintptr_t base; if (s < topk) { base = (up ? BASE + (1ull << 38) : BASE) + (uintptr_t)((s * 37 + 5) % E) * eb; lim = (up ? BASE + (1ull << 38) : BASE) + eb * E; }
+                else { base = up ? BASE + (3ull << 38) : BASE + (2ull << 38); lim = base + eb; }
+                return base + (uintptr_t)jj * p.gh.rb + toff(p.gh, tt); });
+        snprintf(nm, sizeof nm, "moe-dn f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+        for (int ch = 0; ch < p.dn_nchunk; ++ch) {
+            const int mc = std::min(p.dn_MC, M - ch * p.dn_MC);
+            sim(nm, p.gi, p.dn_ring, p.dn_grid, p.dn_ncw,
+                [&](int b) { const int n0 = (int)((long)b * H / p.dn_grid), n1 = (int)((long)(b + 1) * H / p.dn_grid); Cta c;
+                             c.o0 = 0; c.o1 = mc * S * (n1 - n0); c.tpr = p.gi.tpr; c.grp = n1 - n0;
+                             CHECK((uint32_t)(4 * c.o1) <= p.dn_ring.j_bytes, "moe dn jarea");
+                             CHECK((uint32_t)(mc * S * p.gi.tpr * p.gi.stride) <= p.dn_ring.x_bytes, "moe dn x"); return c; },
+                [&](int o, int tt, uintptr_t &lim) { lim = BASE + (uintptr_t)H * p.gi.rb * (E + 1) * 32; return BASE + (uintptr_t)o * p.gi.rb + toff(p.gi, tt); });
+        }
+    }
+    printf("fails %d\n", fails);
+    return fails != 0;
+}
