@@ -444,12 +444,17 @@ struct FmtQ2K {
                 const int sb = (int)((sm >> 8) & 15u), mb = (int)(sm >> 12);
                 uint32_t x[8];
                 ldx8(t + 32 * (u0 + u), x);
+                // codes masked in place (bytes 4^j * code, unsigned) and the sums shifted
+                // back once: exact, every term is a multiple of 4^j
+                const uint32_t msk = 0x03030303u << (2 * j);
                 int lo = 0, hi = 0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    lo = dp4a((w[4 + 8 * h + k] >> (2 * j)) & 0x03030303u, x[k], lo);
-                    hi = dp4a((w[8 + 8 * h + k] >> (2 * j)) & 0x03030303u, x[4 + k], hi);
+                    lo = dp4a_us(w[4 + 8 * h + k] & msk, x[k], lo);
+                    hi = dp4a_us(w[8 + 8 * h + k] & msk, x[4 + k], hi);
                 }
+                lo >>= 2 * j;
+                hi >>= 2 * j;
                 const int hlo = (int)(int16_t)(xh[u] & 0xffffu), hhi = (int)(int16_t)(xh[u] >> 16);
                 const int D = sa * lo + sb * hi, Mn = ma * hlo + mb * hhi;
                 if constexpr (Sink::DOTS) {
@@ -531,16 +536,19 @@ struct FmtQ3K {
                 const int h = u >> 2, j = u & 3;
                 uint32_t x[8];
                 ldx8(t + 32 * u, x);
-                int lo = 0, hi = 0;
+                // low 2 bits and third bit each masked in place (bytes 4^j * bits and
+                // 2^u * bit, unsigned), their sums shifted back once: exact
+                const uint32_t ml = 0x03030303u << (2 * j), mh = 0x01010101u << u;
+                int lo = 0, hi = 0, lb = 0, hb = 0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint32_t cl = ((word(8 + 8 * h + k) >> (2 * j)) & 0x03030303u) |
-                                        (((word(k) >> u) & 0x01010101u) << 2);
-                    const uint32_t ch = ((word(12 + 8 * h + k) >> (2 * j)) & 0x03030303u) |
-                                        (((word(4 + k) >> u) & 0x01010101u) << 2);
-                    lo = dp4a(cl, x[k], lo);
-                    hi = dp4a(ch, x[4 + k], hi);
+                    lo = dp4a_us(word(8 + 8 * h + k) & ml, x[k], lo);
+                    hi = dp4a_us(word(12 + 8 * h + k) & ml, x[4 + k], hi);
+                    lb = dp4a_us(word(k) & mh, x[k], lb);
+                    hb = dp4a_us(word(4 + k) & mh, x[4 + k], hb);
                 }
+                lo = (lo >> (2 * j)) + 4 * (lb >> u);
+                hi = (hi >> (2 * j)) + 4 * (hb >> u);
                 const int hlo = (int)(int16_t)(xh[u] & 0xffffu), hhi = (int)(int16_t)(xh[u] >> 16);
                 const int sa = (int)((sc[u >> 1] >> (16 * (u & 1))) & 255u) - 32;
                 const int sb = (int)((sc[u >> 1] >> (16 * (u & 1) + 8)) & 255u) - 32;
