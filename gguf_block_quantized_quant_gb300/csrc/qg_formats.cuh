@@ -781,23 +781,23 @@ struct FmtQ5K {
                 for (int pp = 0; pp < 2; ++pp) {
                     const int j0 = 4 * hf + 2 * pp;  // sub-blocks j0 (low nibbles) and j0+1 (high nibbles)
                     const uint32_t *q = w + 12 + 8 * (2 * hf + pp);
-                    uint32_t c0[8], c1[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        c0[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> j0) & 0x01010101u) << 4);
-                        c1[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (j0 + 1)) & 0x01010101u) << 4);
-                    }
                     const int sc0 = byte_of(Sw, 2 * pp), sc1 = byte_of(Sw, 2 * pp + 1);
                     const float mn0 = (float)byte_of(Mw, 2 * pp), mn1 = (float)byte_of(Mw, 2 * pp + 1);
                     uint32_t xa[8], xb[8];
                     ldx8(t + 32 * j0, xa);
                     ldx8(t + 32 * j0 + 32, xb);
-                    int da = 0, db = 0;
+                    // nibbles and fifth bits masked where they sit (unsigned bytes), each sum
+                    // shifted back once: exact, every term is a multiple of the bit weight
+                    const uint32_t ma = 0x01010101u << j0, mb = 0x01010101u << (j0 + 1);
+                    int la = 0, lb = 0, ha = 0, hb = 0;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        da = dp4a(c0[k], xa[k], da);
-                        db = dp4a(c1[k], xb[k], db);
+                        la = dp4a_us(q[k] & 0x0f0f0f0fu, xa[k], la);
+                        lb = dp4a_us(q[k] & 0xf0f0f0f0u, xb[k], lb);
+                        ha = dp4a_us(qh[k] & ma, xa[k], ha);
+                        hb = dp4a_us(qh[k] & mb, xb[k], hb);
                     }
+                    const int da = la + 16 * (ha >> j0), db = (lb >> 4) + 16 * (hb >> (j0 + 1));
                     if constexpr (Sink::DOTS) {
                         const uint2 xs = lds64(t + TL::S + 4 * j0);
                         sink.unit(m, j0, da, (int)xs.x);
@@ -936,10 +936,15 @@ struct FmtQ6K {
                 for (int tt = 0; tt < 2; ++tt) {
                     const int t = s + 2 * tt;  // activation block within the half
                     const int u = 4 * hf + t;  // its unit in the task tile
+                    // up to 2 tokens: the low 4 and high 2 code bits masked where they sit
+                    // (unsigned bytes) and each sum shifted back once (exact), two dots per
+                    // word; more tokens: the 6-bit codes assembled once and one dot per word
+                    constexpr bool SPLIT = MT <= 2;
                     uint32_t c[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        c[k] = ((lw[k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[k] >> (2 * t)) & 0x03030303u) << 4);
+                        c[k] = SPLIT ? 0u
+                                     : ((lw[k] >> (4 * tt)) & 0x0f0f0f0fu) | (((hw[k] >> (2 * t)) & 0x03030303u) << 4);
                     const uint32_t scw = t < 2 ? scA : scB;
                     const int sA = (int)(int8_t)((scw >> (16 * (t & 1))) & 255u);
                     const int sB = (int)(int8_t)((scw >> (16 * (t & 1) + 8)) & 255u);
@@ -951,10 +956,24 @@ struct FmtQ6K {
                             ldx8(tl + 32 * u, x);
                             const uint32_t xh = VEC && !Sink::DOTS ? xhv[VEC ? m : 0][t] : lds32(tl + TL::H + 4 * u);
                             int lo = 0, hi = 0;
+                            if constexpr (SPLIT) {
+                                const uint32_t ml = 0x0f0f0f0fu << (4 * tt), mh = 0x03030303u << (2 * t);
+                                int l0 = 0, l1 = 0, h0 = 0, h1 = 0;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
+                                for (int k = 0; k < 4; ++k) {
+                                    l0 = dp4a_us(lw[k] & ml, x[k], l0);
+                                    h0 = dp4a_us(hw[k] & mh, x[k], h0);
+                                    l1 = dp4a_us(lw[4 + k] & ml, x[4 + k], l1);
+                                    h1 = dp4a_us(hw[4 + k] & mh, x[4 + k], h1);
+                                }
+                                lo = (l0 >> (4 * tt)) + 16 * (h0 >> (2 * t));
+                                hi = (l1 >> (4 * tt)) + 16 * (h1 >> (2 * t));
+                            } else {
 #pragma unroll
-                            for (int k = 4; k < 8; ++k) hi = dp4a(c[k], x[k], hi);
+                                for (int k = 0; k < 4; ++k) lo = dp4a(c[k], x[k], lo);
+#pragma unroll
+                                for (int k = 4; k < 8; ++k) hi = dp4a(c[k], x[k], hi);
+                            }
                             const int hlo = (int)(int16_t)(xh & 0xffffu), hhi = (int)(int16_t)(xh >> 16);
                             const int dot = sA * (lo - 32 * hlo) + sB * (hi - 32 * hhi);
                             if constexpr (Sink::DOTS) {
