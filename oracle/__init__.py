@@ -71,6 +71,13 @@ def _configure(L):
     L.or_moe_down.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
     L.or_moe_ffn.argtypes = [i, P, i, i, P, i, i, P, P, P, P, P, P, i, P, P, P]
     L.or_ffn_sublayer.argtypes = [i, P, P, P, P, i, i, i, P, P, P, P]
+    L.or_quantize_act16.argtypes = [P, i, i, P, P, P]
+    L.or_gemv_q16.argtypes = [i, P, P, P, P, i, i, i, P]
+    L.or_absdot16.argtypes = [i, P, P, P, i, i, i, P]
+    L.or_moe_gateup16.argtypes = [i, P, i, i, i, i, i, P, P, P, P, P, P, P, P]
+    L.or_requant16.argtypes = [P, i, i, P, P, P]
+    L.or_moe_down16.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
+    L.or_moe_ffn16.argtypes = [i, P, i, i, P, i, i, P, P, P, P, P, P, i, P, P, P]
     L.or_set_threads.argtypes = [i]
     L.or_get_threads.restype = i
     return L
@@ -320,3 +327,87 @@ def ffn_sublayer(fmt, Wg, Wu, Wd, x, I):
     lib().or_ffn_sublayer(fmt, _p(_u8(Wg)), _p(_u8(Wu)), _p(_u8(Wd)), _p(x), M, H, I,
                           _p(y), _p(g), _p(u), _p(h))
     return y, g, u, h
+
+
+# ----------------------------------------------------------------------------- s16 activations
+def quantize_act16(x):
+    x = _f32(x)
+    M, K = x.shape
+    xq = np.zeros((M, K), np.int16)
+    xd = np.zeros((M, K // 32), np.float32)
+    xs = np.zeros((M, K // 32), np.int32)
+    lib().or_quantize_act16(_p(x), M, K, _p(xq), _p(xd), _p(xs))
+    return xq, xd, xs
+
+
+def gemv_q16(fmt, W, xq, xd, xs, N, K):
+    W = _u8(W)
+    xq = np.ascontiguousarray(xq, np.int16)
+    xd = _f32(xd)
+    xs = np.ascontiguousarray(xs, np.int32)
+    M = xq.shape[0]
+    y = np.zeros((M, N), np.float64)
+    lib().or_gemv_q16(fmt, _p(W), _p(xq), _p(xd), _p(xs), N, K, M, _p(y))
+    return y
+
+
+def absdot16(fmt, W, xq, xd, N, K):
+    W = _u8(W)
+    xq = np.ascontiguousarray(xq, np.int16)
+    xd = _f32(xd)
+    M = xq.shape[0]
+    s = np.zeros((M, N), np.float64)
+    lib().or_absdot16(fmt, _p(W), _p(xq), _p(xd), N, K, M, _p(s))
+    return s
+
+
+def moe_gateup16(fmt, x, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh):
+    x = _f32(x)
+    M, H = x.shape
+    ids = np.ascontiguousarray(ids, np.int32)
+    S = topk + 1
+    g = np.zeros((M, S, I), np.float64)
+    u = np.zeros((M, S, I), np.float64)
+    h = np.zeros((M, S, I), np.float64)
+    lib().or_moe_gateup16(fmt, _p(x), M, H, E, topk, I, _p(ids), _p(_u8(Wg_exps)), _p(_u8(Wu_exps)),
+                          _p(_u8(Wg_sh)), _p(_u8(Wu_sh)), _p(g), _p(u), _p(h))
+    return g, u, h
+
+
+def requant16(h):
+    h = np.ascontiguousarray(h, np.float64)
+    R, I = h.shape
+    hq = np.zeros((R, I), np.int16)
+    hd = np.zeros((R, I // 32), np.float32)
+    hs = np.zeros((R, I // 32), np.int32)
+    lib().or_requant16(_p(h), R, I, _p(hq), _p(hd), _p(hs))
+    return hq, hd, hs
+
+
+def moe_down16(fmt, M, H, E, topk, I, ids, w, hq, hd, hs, Wd_exps, Wd_sh, want_o=False):
+    S = topk + 1
+    ids = np.ascontiguousarray(ids, np.int32)
+    w = np.ascontiguousarray(w, np.float64)
+    hq = np.ascontiguousarray(hq, np.int16).reshape(M * S, I)
+    hd = _f32(hd).reshape(M * S, I // 32)
+    hs = np.ascontiguousarray(hs, np.int32).reshape(M * S, I // 32)
+    y = np.zeros((M, H), np.float64)
+    yabs = np.zeros((M, H), np.float64)
+    o = np.zeros((M, S, H), np.float64) if want_o else None
+    lib().or_moe_down16(fmt, M, H, E, topk, I, _p(ids), _p(w), _p(hq), _p(hd), _p(hs),
+                        _p(_u8(Wd_exps)), _p(_u8(Wd_sh)), _p(y), _p(o), _p(yabs))
+    return (y, yabs, o) if want_o else (y, yabs)
+
+
+def moe_ffn16(fmt, x, Wr, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I):
+    x = _f32(x)
+    Wr = _f32(Wr)
+    M, H = x.shape
+    E = Wr.shape[0]
+    y = np.zeros((M, H), np.float64)
+    ids = np.zeros((M, topk), np.int32)
+    w = np.zeros((M, topk), np.float64)
+    lib().or_moe_ffn16(fmt, _p(x), M, H, _p(Wr), E, topk, _p(_u8(Wg_exps)), _p(_u8(Wu_exps)),
+                       _p(_u8(Wd_exps)), _p(_u8(Wg_sh)), _p(_u8(Wu_sh)), _p(_u8(Wd_sh)), I,
+                       _p(y), _p(ids), _p(w))
+    return y, ids, w

@@ -234,11 +234,21 @@ void or_dequant_matrix(int fmt, const uint8_t *W, int N, int K, double *out) {
                             NULL, NULL, NULL);
 }
 
-/* Activation quantization, one 32-element block at a time.  The page names the
- * activation format "Q8_F32S" only; the per-32 block, the fp32 scale, round half
- * away from zero and true division are the readings taken here. */
-void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs) {
-    int nb = K / 32;
+/* Activation codes of either width: exactly one of q8, q16 is non-NULL. */
+typedef struct {
+    const int8_t *q8;
+    const int16_t *q16;
+} or_codes;
+
+static int32_t code_at(or_codes a, size_t i) { return a.q8 ? (int32_t)a.q8[i] : (int32_t)a.q16[i]; }
+
+/* Activation quantization, one 32-element block at a time, to codes in [-qmax, qmax]
+ * with d = amax / qmax.  The page names the int8 activation format "Q8_F32S" only; the
+ * per-32 block, the fp32 scale, round half away from zero and true division are the
+ * readings taken here.  q8 or q16 receives the codes. */
+static void quantize_rows(const float *x, int M, int K, float qmax, int8_t *q8, int16_t *q16, float *xd,
+                          int32_t *xs) {
+    int nb = K / 32, lim = (int)qmax;
     for (int m = 0; m < M; ++m) {
         for (int b = 0; b < nb; ++b) {
             const float *xb = x + (size_t)m * K + (size_t)b * 32;
@@ -247,23 +257,37 @@ void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_
                 float a = fabsf(xb[i]);
                 if (a > amax) amax = a;
             }
-            float d = amax / 127.0f;                /* fp32, round to nearest even */
+            float d = amax / qmax;                  /* fp32, round to nearest even */
             int32_t s = 0;
             for (int i = 0; i < 32; ++i) {
                 int q = 0;
                 if (d != 0.0f) {
                     float v = xb[i] / d;            /* fp32 IEEE division */
                     q = (int)roundf(v);             /* half away from zero */
-                    if (q > 127) q = 127;
-                    if (q < -127) q = -127;
+                    if (q > lim) q = lim;
+                    if (q < -lim) q = -lim;
                 }
-                xq[(size_t)m * K + (size_t)b * 32 + i] = (int8_t)q;
+                size_t o = (size_t)m * K + (size_t)b * 32 + i;
+                if (q8) q8[o] = (int8_t)q;
+                else q16[o] = (int16_t)q;
                 s += q;
             }
             xd[(size_t)m * nb + b] = d;
             xs[(size_t)m * nb + b] = s;
         }
     }
+}
+
+void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs) {
+    quantize_rows(x, M, K, 127.0f, xq, NULL, xd, xs);
+}
+
+/* s16 activations ([KES] section 四, issue ⑫: the MoE FFN moved from int8 to s16
+ * activations, the quantization step 256 times finer).  Reading: the step is the int8
+ * step divided by 256, d = amax / (127 * 256) = amax / 32512 (in fp32 the same as
+ * (amax / 127) / 256: a power-of-two scaling), and the codes lie in [-32512, 32512]. */
+void or_quantize_act16(const float *x, int M, int K, int16_t *xq, float *xd, int32_t *xs) {
+    quantize_rows(x, M, K, 32512.0f, NULL, xq, xd, xs);
 }
 
 static int has_min_term(int fmt) {
@@ -302,8 +326,8 @@ void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *x
     }
 }
 
-void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, const int32_t *xs,
-               int N, int K, int M, double *y) {
+static void gemv_codes(int fmt, const uint8_t *W, or_codes xq, const float *xd, const int32_t *xs,
+                       int N, int K, int M, double *y) {
     int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
     int upb = QK / 32;
 #pragma omp parallel for schedule(static) num_threads(or_get_threads())
@@ -316,11 +340,11 @@ void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, con
             for (int ub = 0; ub < upb; ++ub) {
                 int u = b * upb + ub;
                 for (int m = 0; m < M; ++m) {
-                    const int8_t *q = xq + (size_t)m * K + (size_t)u * 32;
+                    size_t q0 = (size_t)m * K + (size_t)u * 32;
                     int32_t dot = 0, msum = 0;
                     for (int i = 0; i < 32; ++i) {
-                        dot += c[ub * 32 + i] * (int32_t)q[i];
-                        msum += mc[ub * 32 + i] * (int32_t)q[i];
+                        dot += c[ub * 32 + i] * code_at(xq, q0 + i);
+                        msum += mc[ub * 32 + i] * code_at(xq, q0 + i);
                     }
                     double d_x = xd[(size_t)m * nu + u];
                     double s_x = fmt == OR_Q2_K ? (double)msum : (double)xs[(size_t)m * nu + u];
@@ -329,6 +353,18 @@ void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, con
             }
         }
     }
+}
+
+void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, const int32_t *xs,
+               int N, int K, int M, double *y) {
+    or_codes a = {xq, NULL};
+    gemv_codes(fmt, W, a, xd, xs, N, K, M, y);
+}
+
+void or_gemv_q16(int fmt, const uint8_t *W, const int16_t *xq, const float *xd, const int32_t *xs,
+                 int N, int K, int M, double *y) {
+    or_codes a = {NULL, xq};
+    gemv_codes(fmt, W, a, xd, xs, N, K, M, y);
 }
 
 void or_gemv_deq(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
@@ -351,8 +387,8 @@ void or_gemv_deq(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
     }
 }
 
-void or_absdot(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
-               int N, int K, int M, double *sabs) {
+static void absdot_codes(int fmt, const uint8_t *W, or_codes xq, const float *xd,
+                         int N, int K, int M, double *sabs) {
     int QK = or_block_elems(fmt), BS = or_block_bytes(fmt), nb = K / QK, nu = K / 32;
 #pragma omp parallel for schedule(static) num_threads(or_get_threads())
     for (int n = 0; n < N; ++n) {
@@ -363,12 +399,24 @@ void or_absdot(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
             for (int e = 0; e < QK; ++e) {
                 int k = b * QK + e;
                 for (int m = 0; m < M; ++m) {
-                    double xhat = (double)xq[(size_t)m * K + k] * (double)xd[(size_t)m * nu + k / 32];
+                    double xhat = (double)code_at(xq, (size_t)m * K + k) * (double)xd[(size_t)m * nu + k / 32];
                     sabs[(size_t)m * N + n] += fabs(w[e] * xhat);
                 }
             }
         }
     }
+}
+
+void or_absdot(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
+               int N, int K, int M, double *sabs) {
+    or_codes a = {xq, NULL};
+    absdot_codes(fmt, W, a, xd, N, K, M, sabs);
+}
+
+void or_absdot16(int fmt, const uint8_t *W, const int16_t *xq, const float *xd,
+                 int N, int K, int M, double *sabs) {
+    or_codes a = {NULL, xq};
+    absdot_codes(fmt, W, a, xd, N, K, M, sabs);
 }
 
 void or_gemv(int fmt, const uint8_t *W, const float *x, int N, int K, int M, double *y) {
@@ -426,25 +474,30 @@ static size_t matrix_bytes(int fmt, int rows, int cols) {
     return (size_t)rows * (size_t)(cols / or_block_elems(fmt)) * (size_t)or_block_bytes(fmt);
 }
 
-void or_moe_gateup(int fmt, const float *x, int M, int H, int E, int topk, int I,
-                   const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
-                   const uint8_t *Wg_sh, const uint8_t *Wu_sh,
-                   double *g, double *u, double *h) {
+/* The MoE stages take the activation width as a parameter: bits = 8 (the int8 rule) or
+ * 16 (the s16 rule); codes of the other width are never formed. */
+static void moe_gateup_bits(int bits, int fmt, const float *x, int M, int H, int E, int topk, int I,
+                            const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
+                            const uint8_t *Wg_sh, const uint8_t *Wu_sh,
+                            double *g, double *u, double *h) {
     (void)E;
     int S = topk + 1;
     size_t eb = matrix_bytes(fmt, I, H);
-    int8_t *xq = (int8_t *)malloc((size_t)H);
+    int8_t *q8 = bits == 8 ? (int8_t *)malloc((size_t)H) : NULL;
+    int16_t *q16 = bits == 16 ? (int16_t *)malloc(sizeof(int16_t) * (size_t)H) : NULL;
+    or_codes xq = {q8, q16};
     float *xd = (float *)malloc(sizeof(float) * (H / 32));
     int32_t *xs = (int32_t *)malloc(sizeof(int32_t) * (H / 32));
     double *gg = (double *)malloc(sizeof(double) * I);
     double *uu = (double *)malloc(sizeof(double) * I);
     for (int m = 0; m < M; ++m) {
-        or_quantize_act(x + (size_t)m * H, 1, H, xq, xd, xs);   /* x quantized once per token */
+        /* x quantized once per token */
+        quantize_rows(x + (size_t)m * H, 1, H, bits == 8 ? 127.0f : 32512.0f, q8, q16, xd, xs);
         for (int s = 0; s < S; ++s) {
             const uint8_t *Wg = s < topk ? Wg_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wg_sh;
             const uint8_t *Wu = s < topk ? Wu_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wu_sh;
-            or_gemv_q(fmt, Wg, xq, xd, xs, I, H, 1, gg);
-            or_gemv_q(fmt, Wu, xq, xd, xs, I, H, 1, uu);
+            gemv_codes(fmt, Wg, xq, xd, xs, I, H, 1, gg);
+            gemv_codes(fmt, Wu, xq, xd, xs, I, H, 1, uu);
             for (int j = 0; j < I; ++j) {
                 size_t o = ((size_t)m * S + s) * I + j;
                 if (g) g[o] = gg[j];
@@ -453,21 +506,46 @@ void or_moe_gateup(int fmt, const float *x, int M, int H, int E, int topk, int I
             }
         }
     }
-    free(xq); free(xd); free(xs); free(gg); free(uu);
+    free(q8); free(q16); free(xd); free(xs); free(gg); free(uu);
+}
+
+void or_moe_gateup(int fmt, const float *x, int M, int H, int E, int topk, int I,
+                   const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
+                   const uint8_t *Wg_sh, const uint8_t *Wu_sh,
+                   double *g, double *u, double *h) {
+    moe_gateup_bits(8, fmt, x, M, H, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh, g, u, h);
+}
+
+void or_moe_gateup16(int fmt, const float *x, int M, int H, int E, int topk, int I,
+                     const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
+                     const uint8_t *Wg_sh, const uint8_t *Wu_sh,
+                     double *g, double *u, double *h) {
+    moe_gateup_bits(16, fmt, x, M, H, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh, g, u, h);
+}
+
+static float *h_to_fp32(const double *h, size_t n) {
+    float *hf = (float *)malloc(sizeof(float) * n);
+    for (size_t i = 0; i < n; ++i) hf[i] = (float)h[i];   /* round to nearest fp32 */
+    return hf;
 }
 
 void or_requant(const double *h, int R, int I, int8_t *hq, float *hd, int32_t *hs) {
-    float *hf = (float *)malloc(sizeof(float) * (size_t)R * I);
-    for (size_t i = 0; i < (size_t)R * I; ++i) hf[i] = (float)h[i];   /* round to nearest fp32 */
+    float *hf = h_to_fp32(h, (size_t)R * I);
     or_quantize_act(hf, R, I, hq, hd, hs);
     free(hf);
 }
 
-void or_moe_down(int fmt, int M, int H, int E, int topk, int I,
-                 const int32_t *ids, const double *w,
-                 const int8_t *hq, const float *hd, const int32_t *hs,
-                 const uint8_t *Wd_exps, const uint8_t *Wd_sh,
-                 double *y, double *o, double *yabs) {
+void or_requant16(const double *h, int R, int I, int16_t *hq, float *hd, int32_t *hs) {
+    float *hf = h_to_fp32(h, (size_t)R * I);
+    or_quantize_act16(hf, R, I, hq, hd, hs);
+    free(hf);
+}
+
+static void moe_down_codes(int fmt, int M, int H, int E, int topk, int I,
+                           const int32_t *ids, const double *w,
+                           or_codes hq, const float *hd, const int32_t *hs,
+                           const uint8_t *Wd_exps, const uint8_t *Wd_sh,
+                           double *y, double *o, double *yabs) {
     (void)E;
     int S = topk + 1, nu = I / 32;
     size_t eb = matrix_bytes(fmt, H, I);
@@ -482,8 +560,9 @@ void or_moe_down(int fmt, int M, int H, int E, int topk, int I,
             const uint8_t *Wd = s < topk ? Wd_exps + eb * (size_t)ids[(size_t)m * topk + s] : Wd_sh;
             double ws = s < topk ? w[(size_t)m * topk + s] : 1.0;     /* shared expert: weight 1 */
             size_t r = (size_t)m * S + s;
-            or_gemv_q(fmt, Wd, hq + r * I, hd + r * nu, hs + r * nu, H, I, 1, oo);
-            if (yabs) or_absdot(fmt, Wd, hq + r * I, hd + r * nu, H, I, 1, aa);
+            or_codes hr = {hq.q8 ? hq.q8 + r * I : NULL, hq.q16 ? hq.q16 + r * I : NULL};
+            gemv_codes(fmt, Wd, hr, hd + r * nu, hs + r * nu, H, I, 1, oo);
+            if (yabs) absdot_codes(fmt, Wd, hr, hd + r * nu, H, I, 1, aa);
             for (int n = 0; n < H; ++n) {
                 y[(size_t)m * H + n] += ws * oo[n];
                 if (o) o[r * H + n] = oo[n];
@@ -495,20 +574,56 @@ void or_moe_down(int fmt, int M, int H, int E, int topk, int I,
     free(aa);
 }
 
+void or_moe_down(int fmt, int M, int H, int E, int topk, int I,
+                 const int32_t *ids, const double *w,
+                 const int8_t *hq, const float *hd, const int32_t *hs,
+                 const uint8_t *Wd_exps, const uint8_t *Wd_sh,
+                 double *y, double *o, double *yabs) {
+    or_codes a = {hq, NULL};
+    moe_down_codes(fmt, M, H, E, topk, I, ids, w, a, hd, hs, Wd_exps, Wd_sh, y, o, yabs);
+}
+
+void or_moe_down16(int fmt, int M, int H, int E, int topk, int I,
+                   const int32_t *ids, const double *w,
+                   const int16_t *hq, const float *hd, const int32_t *hs,
+                   const uint8_t *Wd_exps, const uint8_t *Wd_sh,
+                   double *y, double *o, double *yabs) {
+    or_codes a = {NULL, hq};
+    moe_down_codes(fmt, M, H, E, topk, I, ids, w, a, hd, hs, Wd_exps, Wd_sh, y, o, yabs);
+}
+
+static void moe_ffn_bits(int bits, int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
+                         const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
+                         const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
+                         double *y, int32_t *ids, double *w) {
+    int S = topk + 1;
+    size_t R = (size_t)M * S;
+    or_router(x, M, H, Wr, E, topk, NULL, NULL, ids, w);
+    double *h = (double *)malloc(sizeof(double) * R * I);
+    int8_t *q8 = bits == 8 ? (int8_t *)malloc(R * I) : NULL;
+    int16_t *q16 = bits == 16 ? (int16_t *)malloc(sizeof(int16_t) * R * I) : NULL;
+    or_codes hq = {q8, q16};
+    float *hd = (float *)malloc(sizeof(float) * R * (I / 32));
+    int32_t *hs = (int32_t *)malloc(sizeof(int32_t) * R * (I / 32));
+    moe_gateup_bits(bits, fmt, x, M, H, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh, NULL, NULL, h);
+    float *hf = h_to_fp32(h, R * I);
+    quantize_rows(hf, (int)R, I, bits == 8 ? 127.0f : 32512.0f, q8, q16, hd, hs);
+    moe_down_codes(fmt, M, H, E, topk, I, ids, w, hq, hd, hs, Wd_exps, Wd_sh, y, NULL, NULL);
+    free(h); free(hf); free(q8); free(q16); free(hd); free(hs);
+}
+
 void or_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
                 const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
                 const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
                 double *y, int32_t *ids, double *w) {
-    int S = topk + 1;
-    or_router(x, M, H, Wr, E, topk, NULL, NULL, ids, w);
-    double *h = (double *)malloc(sizeof(double) * (size_t)M * S * I);
-    int8_t *hq = (int8_t *)malloc((size_t)M * S * I);
-    float *hd = (float *)malloc(sizeof(float) * (size_t)M * S * (I / 32));
-    int32_t *hs = (int32_t *)malloc(sizeof(int32_t) * (size_t)M * S * (I / 32));
-    or_moe_gateup(fmt, x, M, H, E, topk, I, ids, Wg_exps, Wu_exps, Wg_sh, Wu_sh, NULL, NULL, h);
-    or_requant(h, M * S, I, hq, hd, hs);
-    or_moe_down(fmt, M, H, E, topk, I, ids, w, hq, hd, hs, Wd_exps, Wd_sh, y, NULL, NULL);
-    free(h); free(hq); free(hd); free(hs);
+    moe_ffn_bits(8, fmt, x, M, H, Wr, E, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I, y, ids, w);
+}
+
+void or_moe_ffn16(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
+                  const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
+                  const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
+                  double *y, int32_t *ids, double *w) {
+    moe_ffn_bits(16, fmt, x, M, H, Wr, E, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I, y, ids, w);
 }
 
 void or_ffn_sublayer(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint8_t *Wd,

@@ -75,6 +75,11 @@ void or_dequant_matrix(int fmt, const uint8_t *W, int N, int K, double *out);
  * x: M x K fp32.  xq: M x K int8.  xd, xs: M x K/32.  K must be a multiple of 32. */
 void or_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs);
 
+/* s16 activations ([KES] section 四, issue ⑫): the same rule with a step 256 times finer,
+ * d = amax/32512 (fp32 division; equal to (amax/127)/256), q = clamp(roundf(x/d),
+ * -32512, 32512), s = sum q.  xq: M x K int16. */
+void or_quantize_act16(const float *x, int M, int K, int16_t *xq, float *xd, int32_t *xs);
+
 /* Per-32 integer dot products: dots[m][n][u] = sum_i c_i * xq[m][32u+i];
  * aux[m][n][u] = sum_i mc_i * xq[m][32u+i] (= xs[m][u] where mc = 1) for the formats
  * with a min term (Q4_1, Q5_1, Q2_K, Q4_K, Q5_K), else 0.  Layout M x N x (K/32). */
@@ -86,6 +91,9 @@ void or_block_dots(int fmt, const uint8_t *W, const int8_t *xq, const int32_t *x
  * (the exact result the GPU path reaches up to rounding order). */
 void or_gemv_q(int fmt, const uint8_t *W, const int8_t *xq, const float *xd, const int32_t *xs,
                int N, int K, int M, double *y);
+/* The same with s16 activation codes. */
+void or_gemv_q16(int fmt, const uint8_t *W, const int16_t *xq, const float *xd, const int32_t *xs,
+                 int N, int K, int M, double *y);
 
 /* Same y by brute force: fp64 dequantize-then-dot against xhat = q*d. */
 void or_gemv_deq(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
@@ -94,6 +102,8 @@ void or_gemv_deq(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
 /* sabs[m][n] = sum_k |w_k * xhat_k|, the scale of the per-element tolerance. */
 void or_absdot(int fmt, const uint8_t *W, const int8_t *xq, const float *xd,
                int N, int K, int M, double *sabs);
+void or_absdot16(int fmt, const uint8_t *W, const int16_t *xq, const float *xd,
+                 int N, int K, int M, double *sabs);
 
 /* Full GEMV: quantize x, then or_gemv_q.  y: M x N. */
 void or_gemv(int fmt, const uint8_t *W, const float *x, int N, int K, int M, double *y);
@@ -137,6 +147,23 @@ void or_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, i
                 const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
                 const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
                 double *y, int32_t *ids, double *w);
+
+/* The MoE FFN and its stages with s16 activations ([KES] section 四, issue ⑫): x and
+ * the requantized h both follow or_quantize_act16; the router is unchanged (fp32 x). */
+void or_moe_gateup16(int fmt, const float *x, int M, int H, int E, int topk, int I,
+                     const int32_t *ids, const uint8_t *Wg_exps, const uint8_t *Wu_exps,
+                     const uint8_t *Wg_sh, const uint8_t *Wu_sh,
+                     double *g, double *u, double *h);
+void or_requant16(const double *h, int R, int I, int16_t *hq, float *hd, int32_t *hs);
+void or_moe_down16(int fmt, int M, int H, int E, int topk, int I,
+                   const int32_t *ids, const double *w,
+                   const int16_t *hq, const float *hd, const int32_t *hs,
+                   const uint8_t *Wd_exps, const uint8_t *Wd_sh,
+                   double *y, double *o, double *yabs);
+void or_moe_ffn16(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
+                  const uint8_t *Wg_exps, const uint8_t *Wu_exps, const uint8_t *Wd_exps,
+                  const uint8_t *Wg_sh, const uint8_t *Wu_sh, const uint8_t *Wd_sh, int I,
+                  double *y, int32_t *ids, double *w);
 
 /* FFN sublayer: quantize x, g = Wg x, u = Wu x (Wg, Wu: I x H), h = silu(g)*u,
  * requantize h, y = Wd h (Wd: H x I).  g, u, h (nullable): M x I. */

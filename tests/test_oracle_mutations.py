@@ -55,6 +55,14 @@ MUTATIONS = [
     ("q3_k scale high bits transposed", "int high2 = (sc12[8 + i % 4] >> (2 * (i / 4))) & 3;",
      "int high2 = (sc12[8 + i / 4] >> (2 * (i % 4))) & 3;"),
     ("q3_k scale offset", "return (low4 | (high2 << 4)) - 32;", "return (low4 | (high2 << 4)) - 31;"),
+    ("s16 step", "quantize_rows(x, M, K, 32512.0f, NULL, xq, xd, xs);",
+     "quantize_rows(x, M, K, 32767.0f, NULL, xq, xd, xs);"),
+    ("s16 codes narrowed to a byte", "return a.q8 ? (int32_t)a.q8[i] : (int32_t)a.q16[i];",
+     "return a.q8 ? (int32_t)a.q8[i] : (int32_t)(int8_t)a.q16[i];"),
+    ("moe s16 gate/up input at the int8 step", "bits == 8 ? 127.0f : 32512.0f, q8, q16, xd, xs);",
+     "127.0f, q8, q16, xd, xs);"),
+    ("moe s16 h requantized at the int8 step", "quantize_rows(hf, (int)R, I, bits == 8 ? 127.0f : 32512.0f,",
+     "quantize_rows(hf, (int)R, I, 127.0f,"),
 ]
 
 PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]

@@ -9,7 +9,10 @@
 * closed forms (all-ones Q8_0 weights reduce the GEMV to a plain sum);
 * the router's top-k against a full stable sort, softmax invariants;
 * SwiGLU identities (silu(g) - silu(-g) = g, silu(ln 3) = 0.75 ln 3);
-* MoE special cases that reduce to the FFN sublayer.
+* MoE special cases that reduce to the FFN sublayer;
+* s16 activations: an exact grid (step 2^-20) with its ties, the step equal to the int8
+  step / 256 bit for bit, the integer path against fp64 brute force, and an end-to-end
+  MoE much closer than the int8 one to the unquantized fp64 MoE.
 """
 import math
 import os
@@ -561,3 +564,115 @@ def test_moe_stages_compose(orc):
     ref = orc.gemv_q(fmt, Wg[e], xq[1:2], xd[1:2], xs[1:2], I, H)[0]
     np.testing.assert_array_equal(gg[1, 2], ref)
     assert np.all(yabs >= np.abs(y) * (1 - 1e-12))
+
+
+# ----------------------------------------------------------------------------- s16 activations
+def test_quant16_exact_grid(orc):
+    """amax = 32512 * 2^-20 makes the s16 step d = 2^-20 exactly: elements on the grid
+    j * 2^-20 quantize to j, exact half steps round away from zero."""
+    step = 2.0 ** -20
+    j = [32512, -12345, 0, 1, -1, 255, 256, -257, 20000, -32511]
+    ties = [2.5, -2.5, 0.5, -0.5, 32511.5, -100.5]
+    want_t = [3, -3, 1, -1, 32512, -101]
+    x = np.zeros((1, 32), np.float32)
+    x[0, :len(j)] = np.array(j, np.float64) * step
+    x[0, len(j):len(j) + len(ties)] = np.array(ties, np.float64) * step
+    xq, xd, xs = orc.quantize_act16(x)
+    assert xd[0, 0] == np.float32(step)
+    want = j + want_t + [0] * (32 - len(j) - len(ties))
+    assert list(xq[0]) == want
+    assert xs[0, 0] == sum(want)
+
+
+def test_quant16_step_is_int8_step_over_256(orc):
+    """The s16 step is the int8 step divided by 256, bit for bit."""
+    g = np.random.default_rng(8)
+    x = (g.standard_normal((4, 1024)) * np.exp(g.uniform(-20, 20, (4, 1)))).astype(np.float32)
+    _, d8, _ = orc.quantize_act(x)
+    _, d16, _ = orc.quantize_act16(x)
+    np.testing.assert_array_equal(d16, (d8 / np.float32(256)).astype(np.float32))
+
+
+def test_quant16_properties(orc):
+    g = np.random.default_rng(9)
+    x = (g.standard_normal((5, 512)) * np.exp(g.uniform(-20, 20, (5, 1)))).astype(np.float32)
+    x[1, 32:64] = 0.0
+    xq, xd, xs = orc.quantize_act16(x)
+    xb = x.reshape(5, 16, 32).astype(np.float64)
+    qb = xq.reshape(5, 16, 32).astype(np.int64)
+    amax = np.abs(x.reshape(5, 16, 32)).max(-1)
+    np.testing.assert_array_equal(xd, (amax / np.float32(32512)).astype(np.float32))
+    nz = amax > 0
+    assert np.all(np.abs(qb).max(-1)[nz] == 32512) and not qb[~nz].any()
+    # x/d is rounded to fp32 before the code is taken: up to 32512 * 2^-24 of a step off
+    bound = (0.5 + 32512 * 2.0 ** -23) * xd[..., None].astype(np.float64)
+    assert np.all(np.abs(xb - qb * xd[..., None].astype(np.float64)) <= bound)
+    np.testing.assert_array_equal(xs, qb.sum(-1))
+
+
+def test_requant16_is_quant16_of_fp32(orc):
+    g = np.random.default_rng(10)
+    h = g.standard_normal((3, 64)) * 3
+    for u, v in zip(orc.requant16(h), orc.quantize_act16(h.astype(np.float32))):
+        np.testing.assert_array_equal(u, v)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_int16_path_equals_fp64_bruteforce(orc, fmt):
+    """s16 codes through the integer-sum path equal fp64 dequantize-then-dot, and the
+    s16 result is far closer to the unquantized product than the int8 one."""
+    g = np.random.default_rng(199 + fmt)
+    qk = synth.BLOCK_ELEMS[fmt]
+    N, K, M = 6, 512 if qk == 256 else 128, 2
+    W = synth.weights(fmt, N, K, g)
+    x = synth.activations(M, K, g)
+    xq, xd, xs = orc.quantize_act16(x)
+    Wd = orc.dequant_matrix(fmt, W, N, K)
+    xhat = xq.astype(np.float64) * np.repeat(xd.astype(np.float64), 32, axis=1)
+    y16 = orc.gemv_q16(fmt, W, xq, xd, xs, N, K)
+    sabs = orc.absdot16(fmt, W, xq, xd, N, K)
+    np.testing.assert_allclose(sabs, (np.abs(xhat)[:, None, :] * np.abs(Wd)[None]).sum(-1), rtol=1e-12)
+    assert np.all(np.abs(y16 - xhat @ Wd.T) <= 1e-12 * sabs + 1e-300)
+    y_exact = x.astype(np.float64) @ Wd.T
+    y8 = orc.gemv(fmt, W, x, N, K)
+    assert np.abs(y16 - y_exact).max() * 50 < np.abs(y8 - y_exact).max()
+
+
+def _moe_exact(orc, fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I):
+    """fp64 MoE FFN with unquantized activations, from the dequantized matrices."""
+    M, H = x.shape
+    _, _, ids, w = orc.router(x, Wr, k)
+    deq = lambda W, n, kk: orc.dequant_matrix(fmt, W, n, kk)  # noqa: E731
+    y = np.zeros((M, H))
+    for m in range(M):
+        xm = x[m].astype(np.float64)
+        for s in range(k + 1):
+            Wg_s, Wu_s, Wd_s = (Wg[ids[m, s]], Wu[ids[m, s]], Wd[ids[m, s]]) if s < k else (sg, su, sd)
+            gg, uu = deq(Wg_s, I, H) @ xm, deq(Wu_s, I, H) @ xm
+            h = gg * uu / (1 + np.exp(-gg))
+            y[m] += (w[m, s] if s < k else 1.0) * (deq(Wd_s, H, I) @ h)
+    return y
+
+
+def test_moe16_stages_compose_and_beat_int8(orc):
+    g = np.random.default_rng(24)
+    fmt, E, H, I, M, k = synth.Q4_K, 8, 512, 256, 2, 3
+    Wg, Wu, Wd, (sg, su, sd) = _moe_small(g, fmt, E, H, I)
+    Wr = synth.router_weights(E, H, g)
+    x = synth.activations(M, H, g)
+    y, ids, w = orc.moe_ffn16(fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I)
+    _, _, ids2, w2 = orc.router(x, Wr, k)
+    gg, uu, hh = orc.moe_gateup16(fmt, x, E, k, I, ids2, Wg, Wu, sg, su)
+    hq, hd, hs = orc.requant16(hh.reshape(M * (k + 1), I))
+    y2, yabs = orc.moe_down16(fmt, M, H, E, k, I, ids2, w2, hq, hd, hs, Wd, sd)
+    np.testing.assert_array_equal(ids, ids2)
+    np.testing.assert_array_equal(y, y2)
+    xq, xd, xs = orc.quantize_act16(x)
+    e = ids[1, 2]
+    np.testing.assert_array_equal(gg[1, 2], orc.gemv_q16(fmt, Wg[e], xq[1:2], xd[1:2], xs[1:2], I, H)[0])
+    np.testing.assert_array_equal(uu[0, k], orc.gemv_q16(fmt, su, xq[0:1], xd[0:1], xs[0:1], I, H)[0])
+    assert np.all(yabs >= np.abs(y) * (1 - 1e-12))
+    # the finer step shows end to end: the s16 MoE is much closer to the unquantized one
+    y_exact = _moe_exact(orc, fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I)
+    y8 = orc.moe_ffn(fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I)[0]
+    assert np.abs(y - y_exact).max() * 50 < np.abs(y8 - y_exact).max()
