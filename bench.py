@@ -509,6 +509,12 @@ def secondary(qg, torch, dev, s):
         ue = _eager_time_us(torch, s, call, 200)
         out[f"MoE FFN Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us, "tokens/s": M / (us * 1e-6),
                                                                   "us_eager": ue}
+        # the same with s16 activations (two int8 planes per activation row)
+        ws16 = torch.empty(qg.qg_workspace_size(qg.QG_OP_MOE_FFN_S16, fq, M, H, H, E, topk, I), dtype=torch.uint8,
+                           device=dev)
+        call16 = lambda: qg.qg_moe_ffn_s16(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y, ws=ws16, stream=s)  # noqa
+        us16 = _graph_time_us(torch, s, call16, 200)
+        out[f"MoE FFN s16 Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us16, "tokens/s": M / (us16 * 1e-6)}
     del Wg, Wu, Wd
     # FFN sublayer: H=5120, I=17408 (150 / 219 MB of weights: larger than L2)
     H, I = 5120, 17408

@@ -29,7 +29,7 @@ BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K
 BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
                Q6_K: 210, IQ4_NL: 18, IQ4_XS: 136}
 
-QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER = 1, 2, 3, 4
+QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER, QG_OP_MOE_FFN_S16 = 1, 2, 3, 4, 5
 QG_OK, QG_EINVAL, QG_EWORKSPACE, QG_EALIGN, QG_ECUDA, QG_EDEVICE = 0, -1, -2, -3, -4, -5
 WS_INVALID = ctypes.c_size_t(-1).value
 
@@ -38,7 +38,7 @@ LIB_PATH = _build.LIB
 # every symbol declared in include/qg.h
 EXPORTS = ("qg_quantize_act", "qg_gemv", "qg_gemv_q", "qg_moe_ffn", "qg_ffn_sublayer", "qg_workspace_size",
            "qg_moe_ws_layout", "qg_ffn_ws_layout", "qg_block_dots", "qg_device_error", "qg_strerror",
-           "qg_version", "qg_gemv_static_ws")
+           "qg_version", "qg_gemv_static_ws", "qg_quantize_act_s16", "qg_moe_ffn_s16", "qg_moe_s16_ws_layout")
 QG_STATIC_WS_BYTES = 2097152  # include/qg.h
 
 
@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.qg_gemv_q.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
         L.qg_gemv_static_ws.argtypes = [I, P, P, P, I, I, I, P]
         L.qg_moe_ffn.argtypes = [I, P, I, I, P, I, I, P, P, P, P, P, P, I, P, P, P, P, S, P]
+        L.qg_moe_ffn_s16.argtypes = [I, P, I, I, P, I, I, P, P, P, P, P, P, I, P, P, P, P, S, P]
+        L.qg_quantize_act_s16.argtypes = [P, I, I, P, P, P, P]
+        L.qg_moe_s16_ws_layout.argtypes = [I, I, I, I, I, ctypes.POINTER(S)]
         L.qg_ffn_sublayer.argtypes = [I, P, P, P, P, P, I, I, I, P, S, P]
         L.qg_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         L.qg_workspace_size.restype = S
@@ -136,6 +139,16 @@ def qg_quantize_act(x, xq=None, xd=None, xs=None, stream=None):
     return xq, xd, xs
 
 
+def qg_quantize_act_s16(x, xq=None, xd=None, xs=None, stream=None):
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int16, device=x.device) if xq is None else xq
+    xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device) if xd is None else xd
+    xs = torch.empty((M, K // 32), dtype=torch.int32, device=x.device) if xs is None else xs
+    _check(lib().qg_quantize_act_s16(_ptr(x), M, K, _ptr(xq), _ptr(xd), _ptr(xs), _stream(stream)),
+           "qg_quantize_act_s16")
+    return xq, xd, xs
+
+
 def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
     M, K = x.shape
     y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
@@ -178,6 +191,18 @@ def qg_moe_ffn(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_
     return y
 
 
+def qg_moe_ffn_s16(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I: int,
+                   y=None, topk_ids=None, topk_w=None, ws=None, stream=None):
+    M, H = x.shape
+    E = Wr.shape[0]
+    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN_S16, fmt, M, H, H, E, topk, I), x.device)
+    _check(lib().qg_moe_ffn_s16(fmt, _ptr(x), M, H, _ptr(Wr), E, topk, _ptr(Wg_exps), _ptr(Wu_exps),
+                                _ptr(Wd_exps), _ptr(Wg_sh), _ptr(Wu_sh), _ptr(Wd_sh), I, _ptr(y), _ptr(topk_ids),
+                                _ptr(topk_w), _ptr(ws), nws, _stream(stream)), "qg_moe_ffn_s16")
+    return y
+
+
 def qg_ffn_sublayer(fmt: int, Wg, Wu, Wd, x, I: int, y=None, ws=None, stream=None):
     M, H = x.shape
     y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
@@ -190,6 +215,12 @@ def qg_ffn_sublayer(fmt: int, Wg, Wu, Wd, x, I: int, y=None, ws=None, stream=Non
 def qg_moe_ws_layout(M: int, H: int, E: int, topk: int, I: int):
     off = (ctypes.c_size_t * 7)()
     _check(lib().qg_moe_ws_layout(M, H, E, topk, I, off), "qg_moe_ws_layout")
+    return list(off)
+
+
+def qg_moe_s16_ws_layout(M: int, H: int, E: int, topk: int, I: int):
+    off = (ctypes.c_size_t * 7)()
+    _check(lib().qg_moe_s16_ws_layout(M, H, E, topk, I, off), "qg_moe_s16_ws_layout")
     return list(off)
 
 

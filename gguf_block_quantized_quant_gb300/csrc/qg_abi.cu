@@ -37,6 +37,26 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const float *x, int M, i
     }
 }
 
+// s16 activation quantization in the plain layout (qg_quantize_act_s16).
+__global__ void __launch_bounds__(256) quant_act_s16_kernel(const float *x, int M, int K, int16_t *xq, float *xd,
+                                                            int32_t *xs) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32;
+    const long total = (long)M * nb;
+    const long wpg = (long)gridDim.x * (blockDim.x >> 5);
+    for (long w = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += wpg) {
+        const int m = (int)(w / nb), b = (int)(w % nb);
+        int q, s;
+        float d;
+        quant_block_warp16(x[(long)m * K + 32 * b + lane], q, d, s);
+        xq[(long)m * K + 32 * b + lane] = (int16_t)q;
+        if (lane == 0) {
+            xd[(long)m * nb + b] = d;
+            xs[(long)m * nb + b] = s;
+        }
+    }
+}
+
 // y[i] = sum over the K-slices in slice order.
 __global__ void splitk_reduce_kernel(const float *part, int KS, long MN, float *y) {
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < MN; i += (long)gridDim.x * blockDim.x) {
@@ -61,13 +81,26 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(const float *x, const f
     prep_tiles_warp(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
 }
 
+// The s16 tile image of two int8 planes per row (see prep_tiles_s16_warp); launched like
+// prep_tiles_kernel.
+__global__ void __launch_bounds__(256) prep_tiles_s16_kernel(const float *x, const float *u, int in_planes,
+                                                             float *h_out, int rows, int K, int xgt_log2,
+                                                             uint8_t *img, int16_t *mq, float *md, int32_t *ms) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+    const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    prep_tiles_s16_warp(x, u, in_planes, h_out, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
+}
+
 // Blocks [0, ceil(E/2)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32.  Each block takes
 // two experts, four warps per expert, each warp a quarter of the row with 16-byte loads so
 // that a lane's loads are all in flight at once; the quarters are added in order.  The
-// remaining blocks write the activation tile image of x.  Launched like prep_tiles_kernel.
+// remaining blocks write the activation tile image of x (int8 rows, or with s16 == true
+// the two int8 planes of each s16 row).  Launched like prep_tiles_kernel.
 constexpr int ROUTER_SPLIT = 4;  // warps per expert row
 __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M, int H, const float *Wr, int E,
-                                                          float *logits, int xgt_log2, uint8_t *img) {
+                                                          float *logits, int xgt_log2, uint8_t *img, bool s16) {
     griddep_launch_dependents();
     griddep_wait();
     __shared__ float part[8][M_MAX];
@@ -77,8 +110,11 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
     if ((int)blockIdx.x >= nrouter) {
         const long nwarps = (long)(gridDim.x - nrouter) * (blockDim.x >> 5);
         const long wid = (long)(blockIdx.x - nrouter) * (blockDim.x >> 5) + warp;
-        prep_tiles_warp(x, nullptr, nullptr, nullptr, nullptr, nullptr, M, H, xgt_log2, img, nullptr, nullptr, nullptr,
-                        wid, nwarps);
+        if (s16)
+            prep_tiles_s16_warp(x, nullptr, 1, nullptr, M, H, xgt_log2, img, nullptr, nullptr, nullptr, wid, nwarps);
+        else
+            prep_tiles_warp(x, nullptr, nullptr, nullptr, nullptr, nullptr, M, H, xgt_log2, img, nullptr, nullptr,
+                            nullptr, wid, nwarps);
         return;
     }
     const int e = blockIdx.x * epb + warp / ROUTER_SPLIT, q = warp % ROUTER_SPLIT;
@@ -153,6 +189,14 @@ int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *
     return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
 }
 
+static int launch_quant_act_s16(const float *x, int M, int K, int16_t *xq, float *xd, int32_t *xs, cudaStream_t s) {
+    const long blocks = (long)M * (K / 32);
+    const int grid = (int)std::min<long>((blocks + 7) / 8, 4096);
+    if (!prefer_shared((const void *)quant_act_s16_kernel)) return QG_ECUDA;
+    quant_act_s16_kernel<<<grid, 256, 0, s>>>(x, M, K, xq, xd, xs);
+    return cudaGetLastError() == cudaSuccess ? 0 : QG_ECUDA;
+}
+
 int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStream_t s) {
     const int grid = (int)std::min<long>((MN + 255) / 256, 1024);
     if (!prefer_shared((const void *)splitk_reduce_kernel)) return QG_ECUDA;
@@ -187,12 +231,20 @@ int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t
     return launch_pdl(prep_tiles_kernel, grid, 256, s, x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
 }
 
+int launch_prep_tiles_s16(const float *x, const float *u, int in_planes, float *h_out, int rows, int K, int xgt_log2,
+                          uint8_t *img, int16_t *mq, float *md, int32_t *ms, cudaStream_t s) {
+    const long blocks = (long)rows * (K / 32);
+    const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
+    return launch_pdl(prep_tiles_s16_kernel, grid, 256, s, x, u, in_planes, h_out, rows, K, xgt_log2, img, mq, md, ms);
+}
+
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,
-                       uint8_t *img, cudaStream_t s) {
+                       uint8_t *img, bool s16, cudaStream_t s) {
     const long blocks = (long)M * (H / 32);
     const int nprep = (int)std::min<long>((blocks + 7) / 8, 512);
     const int epb = 8 / ROUTER_SPLIT;
-    return launch_pdl(router_prep_kernel, (E + epb - 1) / epb + nprep, 256, s, x, M, H, Wr, E, logits, xgt_log2, img);
+    return launch_pdl(router_prep_kernel, (E + epb - 1) / epb + nprep, 256, s, x, M, H, Wr, E, logits, xgt_log2, img,
+                      s16);
 }
 
 // ----------------------------------------------------------------------------- host helpers
@@ -313,6 +365,14 @@ int qg_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t
     return launch_quant_act(x, M, K, K, xq, xd, xs, (cudaStream_t)stream);
 }
 
+int qg_quantize_act_s16(const float *x, int M, int K, int16_t *xq, float *xd, int32_t *xs, void *stream) {
+    if (!x || !xq || !xd || !xs || M < 1 || K < 32 || K % 32) return QG_EINVAL;
+    if (!aligned(x, 4) || !aligned(xq, 2) || !aligned(xd, 4) || !aligned(xs, 4)) return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    return launch_quant_act_s16(x, M, K, xq, xd, xs, (cudaStream_t)stream);
+}
+
 size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, int I) {
     const size_t bad = (size_t)-1;
     switch (op) {
@@ -321,8 +381,9 @@ size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, 
         const GemvPlan p = plan_gemv(fmt, N, K, M, planning_sms());
         return p.ok ? p.ws_total : bad;
     }
-    case QG_OP_MOE_FFN: {
-        const MoePlan p = plan_moe(fmt, M, K, E, topk, I, planning_sms());
+    case QG_OP_MOE_FFN:
+    case QG_OP_MOE_FFN_S16: {
+        const MoePlan p = plan_moe(fmt, M, K, E, topk, I, planning_sms(), op == QG_OP_MOE_FFN_S16);
         return p.ok ? p.ws_total : bad;
     }
     case QG_OP_FFN_SUBLAYER: {
@@ -408,9 +469,10 @@ int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd, con
     return by_format(fmt, [&](auto F) { return ffn_run<decltype(F)::value>(c, sms); });
 }
 
-int qg_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk, const void *Wg_exps,
-               const void *Wu_exps, const void *Wd_exps, const void *Wg_sh, const void *Wu_sh, const void *Wd_sh,
-               int I, float *y, int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+static int moe_common(bool s16, int fmt, const float *x, int M, int H, const float *Wr, int E, int topk,
+                      const void *Wg_exps, const void *Wu_exps, const void *Wd_exps, const void *Wg_sh,
+                      const void *Wu_sh, const void *Wd_sh, int I, float *y, int32_t *topk_ids, float *topk_w,
+                      void *ws, size_t ws_bytes, void *stream) {
     if (!x || !Wr || !Wg_exps || !Wu_exps || !Wd_exps || !Wg_sh || !Wu_sh || !Wd_sh || !y) return QG_EINVAL;
     if (M < 1 || M > M_MAX || E < 1 || E > E_MAX || topk < 1 || topk > TOPK_MAX || topk > E) return QG_EINVAL;
     if (!shape_ok(fmt, H) || !shape_ok(fmt, I)) return QG_EINVAL;
@@ -440,16 +502,31 @@ int qg_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, in
     c.y = y;
     c.ids_out = topk_ids;
     c.w_out = topk_w;
+    c.s16 = s16;
     c.ws = static_cast<uint8_t *>(ws);
     c.ws_bytes = ws_bytes;
     c.stream = (cudaStream_t)stream;
     return by_format(fmt, [&](auto F) { return moe_run<decltype(F)::value>(c, sms); });
 }
 
-int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]) {
+int qg_moe_ffn(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk, const void *Wg_exps,
+               const void *Wu_exps, const void *Wd_exps, const void *Wg_sh, const void *Wu_sh, const void *Wd_sh,
+               int I, float *y, int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+    return moe_common(false, fmt, x, M, H, Wr, E, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I, y,
+                      topk_ids, topk_w, ws, ws_bytes, stream);
+}
+
+int qg_moe_ffn_s16(int fmt, const float *x, int M, int H, const float *Wr, int E, int topk, const void *Wg_exps,
+                   const void *Wu_exps, const void *Wd_exps, const void *Wg_sh, const void *Wu_sh, const void *Wd_sh,
+                   int I, float *y, int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream) {
+    return moe_common(true, fmt, x, M, H, Wr, E, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, I, y,
+                      topk_ids, topk_w, ws, ws_bytes, stream);
+}
+
+static int moe_layout(bool s16, int M, int H, int E, int topk, int I, size_t off[7]) {
     if (!off) return QG_EINVAL;
     // the layout does not depend on the block format or the SM count
-    const MoePlan p = plan_moe(QG_Q8_0, M, H, E, topk, I, G_PLAN);
+    const MoePlan p = plan_moe(QG_Q8_0, M, H, E, topk, I, G_PLAN, s16);
     if (!p.ok) return QG_EINVAL;
     off[0] = p.ws_g;
     off[1] = p.ws_u;
@@ -459,6 +536,14 @@ int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]) {
     off[5] = p.ws_hs;
     off[6] = p.ws_logits;
     return QG_OK;
+}
+
+int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]) {
+    return moe_layout(false, M, H, E, topk, I, off);
+}
+
+int qg_moe_s16_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]) {
+    return moe_layout(true, M, H, E, topk, I, off);
 }
 
 int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]) {

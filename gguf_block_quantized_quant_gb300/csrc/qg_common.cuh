@@ -203,4 +203,21 @@ __device__ __forceinline__ void quant_block_warp(float v, int &q, float &d, int 
     s = __reduce_add_sync(0xffffffffu, q);
 }
 
+// s16 activation quantization of one 32-element block, one element per lane: the same
+// rule with a step 256 times finer, d = amax / 32512 (= (amax / 127) / 256) and codes in
+// [-32512, 32512].
+constexpr int S16_QMAX = 127 * 256;
+__device__ __forceinline__ void quant_block_warp16(float v, int &q, float &d, int &s) {
+    float a = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    d = __fdiv_rn(a, (float)S16_QMAX);
+    q = 0;
+    if (d != 0.0f) {
+        q = (int)roundf(__fdiv_rn(v, d));
+        q = q > S16_QMAX ? S16_QMAX : (q < -S16_QMAX ? -S16_QMAX : q);
+    }
+    s = __reduce_add_sync(0xffffffffu, q);
+}
+
 }  // namespace qg

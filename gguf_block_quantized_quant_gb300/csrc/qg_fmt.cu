@@ -265,11 +265,9 @@ int ffn_run(const FfnCall &c, int sms) {
     return gemv_run_planned<FMT>(p.down, d);
 }
 
-template <int FMT>
-int moe_run(const MoeCall &c, int sms) {
-    const MoePlan p = plan_moe(FMT, c.M, c.H, c.E, c.topk, c.I, sms);
-    if (!p.ok) return -1;
-    if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
+// P activation rows per token: 1 (int8) or 2 (the two int8 planes of s16 activations).
+template <int FMT, int P>
+int moe_run_p(const MoeCall &c, const MoePlan &p) {
     float *logits = reinterpret_cast<float *>(c.ws + p.ws_logits);
     int32_t *ids = reinterpret_cast<int32_t *>(c.ws + p.ws_ids);
     float *w = reinterpret_cast<float *>(c.ws + p.ws_w);
@@ -281,13 +279,13 @@ int moe_run(const MoeCall &c, int sms) {
     int32_t *hs = reinterpret_cast<int32_t *>(c.ws + p.ws_hs);
     uint8_t *ximg = c.ws + p.ws_ximg, *himg = c.ws + p.ws_himg;
 
-    int rc = launch_router_prep(c.x, c.M, c.H, c.Wr, c.E, logits, log2i(p.gh.XGT), ximg, c.stream);
+    int rc = launch_router_prep(c.x, c.M, c.H, c.Wr, c.E, logits, log2i(p.gh.XGT), ximg, P == 2, c.stream);
     if (rc) return rc;
     const size_t eb_gu = (size_t)c.I * p.gh.rb, eb_d = (size_t)c.H * p.gi.rb;
     rc = with_t<false>(p.gh, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
-        MoeGateUpJob<FMT, T> j;
-        set_engine(j, p.gu_ring, p.gh.tpr, 1);
+        MoeGateUpJob<FMT, T, P> j;
+        set_engine(j, p.gu_ring, p.gh.tpr, P);
         j.Wg_exps = c.Wg_exps;
         j.Wu_exps = c.Wu_exps;
         j.Wg_sh = c.Wg_sh;
@@ -312,20 +310,24 @@ int moe_run(const MoeCall &c, int sms) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.g_out = g;
         j.u_out = u;
-        return launch_engine_ncw<FMT, T, 1>(p.gu_ncw, j, p.gu_grid, p.gu_ring.smem_total, c.stream);
+        return launch_engine_ncw<FMT, T, P>(p.gu_ncw, j, p.gu_grid, p.gu_ring.smem_total, c.stream);
     });
     if (rc) return rc;
-    // h = silu(g) * u, requantized: one image row per token and slot; the plain h and its
+    // h = silu(g) * u, requantized: P image rows per token and slot; the plain h and its
     // codes are kept in the workspace for callers
-    rc = launch_prep_tiles(g, u, h, nullptr, nullptr, nullptr, c.M * p.S, c.I, log2i(p.gi.XGT), himg, hq, hd, hs,
-                           c.stream);
+    if constexpr (P == 2)
+        rc = launch_prep_tiles_s16(g, u, 2, h, c.M * p.S, c.I, log2i(p.gi.XGT), himg,
+                                   reinterpret_cast<int16_t *>(hq), hd, hs, c.stream);
+    else
+        rc = launch_prep_tiles(g, u, h, nullptr, nullptr, nullptr, c.M * p.S, c.I, log2i(p.gi.XGT), himg, hq, hd,
+                               hs, c.stream);
     if (rc) return rc;
     for (int ch = 0; ch < p.dn_nchunk; ++ch) {
         const int m0 = ch * p.dn_MC, mc = std::min(p.dn_MC, c.M - m0);
         rc = with_t<false>(p.gi, [&](auto Tc) {
             constexpr int T = decltype(Tc)::value;
-            MoeDownJob<FMT, T> j;
-            set_engine(j, p.dn_ring, p.gi.tpr, 1);
+            MoeDownJob<FMT, T, P> j;
+            set_engine(j, p.dn_ring, p.gi.tpr, P);
             j.Wd_exps = c.Wd_exps;
             j.Wd_sh = c.Wd_sh;
             j.Wd_exps_end = c.Wd_exps + eb_d * c.E;
@@ -342,11 +344,19 @@ int moe_run(const MoeCall &c, int sms) {
             j.ximg = himg;
             j.ximg_pitch = (uint32_t)p.himg_pitch;
             j.y = c.y;
-            return launch_engine_ncw<FMT, T, 1>(p.dn_ncw, j, p.dn_grid, p.dn_ring.smem_total, c.stream);
+            return launch_engine_ncw<FMT, T, P>(p.dn_ncw, j, p.dn_grid, p.dn_ring.smem_total, c.stream);
         });
         if (rc) return rc;
     }
     return 0;
+}
+
+template <int FMT>
+int moe_run(const MoeCall &c, int sms) {
+    const MoePlan p = plan_moe(FMT, c.M, c.H, c.E, c.topk, c.I, sms, c.s16);
+    if (!p.ok) return -1;
+    if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
+    return c.s16 ? moe_run_p<FMT, 2>(c, p) : moe_run_p<FMT, 1>(c, p);
 }
 
 // ----------------------------------------------------------------------------- test hook

@@ -1283,6 +1283,19 @@ using FT = typename FmtSel<FMT, T>::type;
 // ================================================================================ tile writer
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// One activation block (lane i holds code i) into unit u of a task tile of xgt units:
+// codes, then per unit d, s, the two 16-element half sums packed in 16 bits each, d * s.
+__device__ __forceinline__ void put_tile_unit(uint8_t *t, int u, int xgt, int lane, int qi, float di, int si) {
+    t[32 * u + lane] = (uint8_t)qi;
+    const int h16 = __reduce_add_sync(0xffffffffu, lane < 16 ? qi : 0);
+    if (lane == 0) {
+        reinterpret_cast<float *>(t + 32 * xgt)[u] = di;
+        reinterpret_cast<int32_t *>(t + 36 * xgt)[u] = si;
+        reinterpret_cast<uint32_t *>(t + 40 * xgt)[u] = ((uint32_t)h16 & 0xffffu) | ((uint32_t)(si - h16) << 16);
+        reinterpret_cast<float *>(t + 44 * xgt)[u] = di * (float)si;
+    }
+}
+
 // Activation rows -> task-tile image in global memory: tile (row r, task tt) at
 // img + (r * tpr + tt) * tile_stride(xgt).  One warp per activation block; lane i holds
 // element i.  src_f32 != nullptr: quantize fp32 rows (activation quantization rule) --
@@ -1312,21 +1325,64 @@ __device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const floa
             di = d[(long)r * nb + b];
             si = s[(long)r * nb + b];
         }
-        uint8_t *t = img + ((long)r * tpr + (b >> xgt_log2)) * stride;
-        const int u = b & (xgt - 1);
-        t[32 * u + lane] = (uint8_t)qi;
-        const int h16 = __reduce_add_sync(0xffffffffu, lane < 16 ? qi : 0);
-        if (lane == 0) {
-            reinterpret_cast<float *>(t + 32 * xgt)[u] = di;
-            reinterpret_cast<int32_t *>(t + 36 * xgt)[u] = si;
-            reinterpret_cast<uint32_t *>(t + 40 * xgt)[u] = ((uint32_t)h16 & 0xffffu) | ((uint32_t)(si - h16) << 16);
-            reinterpret_cast<float *>(t + 44 * xgt)[u] = di * (float)si;
-        }
+        put_tile_unit(img + ((long)r * tpr + (b >> xgt_log2)) * stride, b & (xgt - 1), xgt, lane, qi, di, si);
         if (mq) {
             mq[(long)r * K + 32L * b + lane] = (int8_t)qi;
             if (lane == 0) {
                 md[(long)r * nb + b] = di;
                 ms[(long)r * nb + b] = si;
+            }
+        }
+    }
+}
+
+// s16 activation rows -> task-tile image of two int8 planes per row.  An s16 code q is
+// split as q = 256 * hi + lo with hi = (q + 128) >> 8 in [-127, 127] and lo in [-128, 127];
+// image row 2r holds the hi plane with scale 256 * d (exact: a power-of-two scaling), row
+// 2r + 1 the lo plane with scale d, each in the int8 tile layout.  Every per-unit term the
+// engines form from a row (d * dot, d * s, the min-code sums) is linear in the codes, so
+// the two planes' results add up to the s16 result with the exact integer sums.
+// src_f32: fp32 rows; with u != nullptr the rows are h = silu(g) * u (also stored to h_out
+// when given), where in_planes == 2 means g and u hold two partial rows per row (the two
+// planes' results of the previous step) that are added first.  mq/md/ms (nullable): the
+// s16 codes, steps and code sums in their plain layout.
+__device__ __forceinline__ void prep_tiles_s16_warp(const float *src_f32, const float *u, int in_planes, float *h_out,
+                                                    int rows, int K, int xgt_log2, uint8_t *img, int16_t *mq,
+                                                    float *md, int32_t *ms, long wid, long nwarps) {
+    const int lane = threadIdx.x & 31;
+    const int nb = K / 32, xgt = 1 << xgt_log2, tpr = nb >> xgt_log2, stride = tile_stride(xgt);
+    for (long w = wid; w < (long)rows * nb; w += nwarps) {
+        const int r = (int)(w / nb), b = (int)(w - (long)r * nb);
+        const long idx = (long)r * K + 32L * b + lane;
+        float v;
+        if (u) {
+            float gv, uv;
+            if (in_planes == 2) {
+                const long i0 = 2L * r * K + 32L * b + lane;
+                gv = src_f32[i0] + src_f32[i0 + K];
+                uv = u[i0] + u[i0 + K];
+            } else {
+                gv = src_f32[idx];
+                uv = u[idx];
+            }
+            v = silu_mul(gv, uv);
+            if (h_out) h_out[idx] = v;
+        } else {
+            v = src_f32[idx];
+        }
+        int q, s;
+        float d;
+        quant_block_warp16(v, q, d, s);
+        const int hi = (q + 128) >> 8, lo = q - 256 * hi;
+        const int shi = __reduce_add_sync(0xffffffffu, hi);
+        const long tt = b >> xgt_log2;
+        put_tile_unit(img + ((2L * r) * tpr + tt) * stride, b & (xgt - 1), xgt, lane, hi, 256.0f * d, shi);
+        put_tile_unit(img + ((2L * r + 1) * tpr + tt) * stride, b & (xgt - 1), xgt, lane, lo, d, s - 256 * shi);
+        if (mq) {
+            mq[idx] = (int16_t)q;
+            if (lane == 0) {
+                md[(long)r * nb + b] = d;
+                ms[(long)r * nb + b] = s;
             }
         }
     }

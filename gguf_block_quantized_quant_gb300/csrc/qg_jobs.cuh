@@ -19,7 +19,10 @@
 // dependent launch): seg_src may only read data no earlier kernel writes (the weights),
 // unless the job's prologue first waits for the previous kernel (griddep_wait).
 // Activation images (prep_tiles_warp) have one row of task tiles per token (or per MoE
-// slot), row pitch tpr * tile_stride(XGT).
+// slot), row pitch tpr * tile_stride(XGT).  The MoE jobs take P activation rows per token
+// (or slot): P = 2 for s16 activations held as two int8 planes (prep_tiles_s16_warp); the
+// engine then runs P tokens per lane over one row's planes, and the P results of an output
+// row are kept apart for the next step to add.
 #pragma once
 
 #include "qg_engine.cuh"
@@ -127,7 +130,7 @@ struct FfnGateUpJob : EngineFields {
 constexpr int TOPK_MAX = 16;
 constexpr int E_MAX = 1024;
 
-template <int FMT, int T>
+template <int FMT, int T, int P = 1>
 struct MoeGateUpJob : EngineFields {
     using F = FT<FMT, T>;
     static constexpr bool HAS_FINISH = false, HAS_PROLOGUE = true;
@@ -142,18 +145,18 @@ struct MoeGateUpJob : EngineFields {
     float *w_ws;
     int32_t *ids_out;            // nullable
     float *w_out;
-    const uint8_t *ximg;
+    const uint8_t *ximg;         // P rows per token
     uint32_t ximg_pitch;
-    float *g_out, *u_out;        // [M][topk+1][I]
+    float *g_out, *u_out;        // [M][topk+1][P][I]
 
     __device__ int slots() const { return topk + 1; }
     // o = ((token * slots + slot) * 2 + up) * I + j; groups of I rows are one matrix
     struct Ctx {};
     __device__ Ctx ctx() const { return {}; }
     __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
-        const long P = (long)M * slots() * 2 * I;
-        o0 = split_point(P, (int)blockIdx.x, (int)gridDim.x);
-        o1 = split_point(P, (int)blockIdx.x + 1, (int)gridDim.x);
+        const long rows = (long)M * slots() * 2 * I;
+        o0 = split_point(rows, (int)blockIdx.x, (int)gridDim.x);
+        o1 = split_point(rows, (int)blockIdx.x + 1, (int)gridDim.x);
         tpr = tpr_x;
         grp = I;
     }
@@ -168,15 +171,15 @@ struct MoeGateUpJob : EngineFields {
         lim = up ? Wu_sh_end : Wg_sh_end;
         return (up ? Wu_sh : Wg_sh) + (size_t)j * rb + task_off<F>(tt);
     }
-    __device__ int xrows() const { return M; }
+    __device__ int xrows() const { return M * P; }
     __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + (size_t)r * ximg_pitch; }
     __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
     __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divI) const {
-        return div_slots.div(divI.div((uint32_t)o) >> 1);  // token
+        return P * div_slots.div(divI.div((uint32_t)o) >> 1);  // the token's first row
     }
-    __device__ void store(const Ctx &, int o, int, float v, float *) const {
+    __device__ void store(const Ctx &, int o, int m, float v, float *) const {
         const int q = o / I, j = o - q * I;
-        ((q & 1) ? u_out : g_out)[(long)(q >> 1) * I + j] = v;
+        ((q & 1) ? u_out : g_out)[((long)(q >> 1) * P + m) * I + j] = v;
     }
     __device__ void init(float *, int) const {}
     __device__ void finish(const Ctx &, float *, int, int) const {}
@@ -245,7 +248,7 @@ struct MoeGateUpJob : EngineFields {
 };
 
 // ===================================================================================== MoE down
-template <int FMT, int T>
+template <int FMT, int T, int P = 1>
 struct MoeDownJob : EngineFields {
     using F = FT<FMT, T>;
     static constexpr bool HAS_FINISH = true, HAS_PROLOGUE = true;
@@ -255,7 +258,7 @@ struct MoeDownJob : EngineFields {
     size_t ebytes;
     const int32_t *ids_ws;          // [batch][topk] (written by the gate/up kernel)
     const float *w_ws;
-    const uint8_t *ximg;            // requantized h: one image row per (token, slot)
+    const uint8_t *ximg;            // requantized h: P image rows per (token, slot)
     uint32_t ximg_pitch;
     float *y;                       // [batch][H]
 
@@ -291,11 +294,15 @@ struct MoeDownJob : EngineFields {
         lim = Wd_sh_end;
         return Wd_sh + (size_t)(c.n0 + r) * rb + task_off<F>(tt);
     }
-    __device__ int xrows() const { return M * slots(); }
-    __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + ((size_t)m0 * slots() + r) * ximg_pitch; }
+    __device__ int xrows() const { return M * slots() * P; }
+    __device__ const uint8_t *xrow_src(const Ctx &, int r) const {
+        return ximg + ((size_t)m0 * slots() * P + r) * ximg_pitch;
+    }
     __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
-    __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divn) const { return divn.div((uint32_t)o); }  // token*slots+slot
-    __device__ void store(const Ctx &, int o, int, float v, float *part) const { part[o] = v; }
+    __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divn) const {
+        return P * divn.div((uint32_t)o);  // first row of (token * slots + slot)
+    }
+    __device__ void store(const Ctx &, int o, int m, float v, float *part) const { part[o * P + m] = v; }
     __device__ void init(float *, int) const {}
     __device__ void finish(const Ctx &c, float *part, int tid, int nthreads) const {
         const int nloc = c.nloc;
@@ -304,7 +311,11 @@ struct MoeDownJob : EngineFields {
             float acc = 0.0f;
             for (int s = 0; s < slots(); ++s) {
                 const float ws = s < topk ? w_ws[(m0 + m) * topk + s] : 1.0f;  // shared expert: weight 1
-                acc = fmaf(ws, part[(m * slots() + s) * nloc + r], acc);
+                const float *o = part + ((m * slots() + s) * nloc + r) * P;
+                float v = o[0];
+#pragma unroll
+                for (int p = 1; p < P; ++p) v += o[p];
+                acc = fmaf(ws, v, acc);
             }
             y[(long)(m0 + m) * H + c.n0 + r] = acc;
         }

@@ -295,7 +295,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
 // ----------------------------------------------------------------------------- MoE FFN
 struct MoePlan {
     bool ok = false;
-    int S = 0, gu_ncw = 8, dn_ncw = 8;
+    int S = 0, P = 1, gu_ncw = 8, dn_ncw = 8;  // P: activation rows per token (s16: 2 planes)
     TaskGeo gh, gi;  // rows of H elements (gate/up) and of I elements (down)
     int gu_grid = 0, dn_grid = 0, dn_MC = 1, dn_nchunk = 1;
     Ring gu_ring, dn_ring;
@@ -303,8 +303,9 @@ struct MoePlan {
            ws_ximg = 0, ws_himg = 0, ximg_pitch = 0, himg_pitch = 0, ws_total = 0;
 };
 
-inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) {
+inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, bool s16 = false) {
     MoePlan p;
+    p.P = s16 ? 2 : 1;
     p.gh = task_geo(fmt, H, false);
     p.gi = task_geo(fmt, I, false);
     if (!p.gh.ok || !p.gi.ok || M < 1 || M > M_MAX || E < 1 || E > 1024 || topk < 1 || topk > 16 || topk > E ||
@@ -313,31 +314,31 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     p.S = topk + 1;
     // gate/up: output rows (token, slot, gate|up, row)
     const long gu_rows = (long)M * p.S * 2 * I;
-    const long gu_x = (long)M * p.gh.tpr * p.gh.stride;
+    const long gu_x = (long)M * p.P * p.gh.tpr * p.gh.stride;
     if (gu_x > (long)XCAP) return p;
     p.gu_grid = (int)std::min<long>(sms, gu_rows);
-    p.gu_ncw = plan_ncw(p.gh, 1, (gu_rows + p.gu_grid - 1) / p.gu_grid * p.gh.tpr);
+    p.gu_ncw = plan_ncw(p.gh, p.P, (gu_rows + p.gu_grid - 1) / p.gu_grid * p.gh.tpr);
     p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, p.gu_ncw);
     if (!p.gu_ring.ok) return p;
     // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
-    const long tiles_tok = (long)p.S * p.gi.tpr * p.gi.stride;
+    const long tiles_tok = (long)p.S * p.P * p.gi.tpr * p.gi.stride;
     p.dn_grid = std::min(sms, H);
     const int nloc = (H + p.dn_grid - 1) / p.dn_grid;
-    const long part_tok = 4L * p.S * nloc;
+    const long part_tok = 4L * p.S * p.P * nloc;
     p.dn_MC = (int)std::min<long>(M, (long)XCAP / (tiles_tok + part_tok));
     if (p.dn_MC < 1) return p;
     p.dn_nchunk = (M + p.dn_MC - 1) / p.dn_MC;
     // CTAs own floor or ceil of H / dn_grid rows: runs are at least the floor long
     p.dn_ring = plan_ring(p.gi, (long)(H / p.dn_grid) * p.gi.tpr, (uint32_t)(p.dn_MC * tiles_tok),
-                          (uint32_t)(p.dn_MC * part_tok), p.dn_ncw = geo_ncw(p.gi, 1));
+                          (uint32_t)(p.dn_MC * part_tok), p.dn_ncw = geo_ncw(p.gi, p.P));
     if (!p.dn_ring.ok) return p;
     // workspace
     const size_t Rw = (size_t)M * p.S;
     size_t o = 0;
-    p.ws_g = o; o = align_up(o + 4 * Rw * I, 256);
-    p.ws_u = o; o = align_up(o + 4 * Rw * I, 256);
+    p.ws_g = o; o = align_up(o + 4 * Rw * p.P * I, 256);   // [token][slot][plane][I]
+    p.ws_u = o; o = align_up(o + 4 * Rw * p.P * I, 256);
     p.ws_h = o; o = align_up(o + 4 * Rw * I, 256);
-    p.ws_hq = o; o = align_up(o + Rw * I, 256);
+    p.ws_hq = o; o = align_up(o + Rw * p.P * I, 256);        // int8, or int16 codes for s16
     p.ws_hd = o; o = align_up(o + 4 * Rw * (I / 32), 256);
     p.ws_hs = o; o = align_up(o + 4 * Rw * (I / 32), 256);
     p.ws_logits = o; o = align_up(o + 4ull * M * E, 256);
@@ -345,8 +346,8 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms) 
     p.ws_w = o; o = align_up(o + 4ull * M * topk, 256);
     p.ximg_pitch = (size_t)p.gh.tpr * p.gh.stride;
     p.himg_pitch = (size_t)p.gi.tpr * p.gi.stride;
-    p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);
-    p.ws_himg = o; o = align_up(o + p.himg_pitch * Rw, 256);
+    p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M * p.P, 256);
+    p.ws_himg = o; o = align_up(o + p.himg_pitch * Rw * p.P, 256);
     p.ws_total = o;
     p.ok = true;
     return p;

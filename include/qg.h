@@ -73,7 +73,7 @@ enum qg_status {
 };
 
 /* Operations for qg_workspace_size(). */
-enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBLAYER = 4 };
+enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBLAYER = 4, QG_OP_MOE_FFN_S16 = 5 };
 
 /* Activation quantization "Q8_F32S" [D27 Q&A]: for each token m and each 32-element
  * block b of K, d = amax|x| / 127 (fp32, IEEE division), q = clamp(roundf(x / d),
@@ -82,6 +82,16 @@ enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBL
  *   x:  M x K fp32.   xq: M x K int8.   xd: M x K/32 fp32.   xs: M x K/32 int32.
  * K must be a multiple of 32. */
 int qg_quantize_act(const float *x, int M, int K, int8_t *xq, float *xd, int32_t *xs, void *stream);
+
+/* s16 activation quantization [KES section 四, issue ⑫: int8 activation error compounds
+ * over many MoE layers; the MoE FFN moved to s16 activations with a step 256 times finer]:
+ * the rule of qg_quantize_act with d = amax|x| / 32512 (= (amax / 127) / 256, fp32 IEEE
+ * division) and q = clamp(roundf(x / d), -32512, 32512).
+ *   x: M x K fp32.   xq: M x K int16 (2-byte aligned).   xd: M x K/32 fp32.
+ *   xs: M x K/32 int32 (sum of the 32 codes).  K must be a multiple of 32.
+ * The MoE's s16 path (qg_moe_ffn_s16) computes the same codes on the fly; this call is
+ * the plain-layout form, for callers and tests. */
+int qg_quantize_act_s16(const float *x, int M, int K, int16_t *xq, float *xd, int32_t *xs, void *stream);
 
 /* y = W x for M tokens [D27 Q&A; KES section 一]: x is quantized on the GPU as by
  * qg_quantize_act (once per call, into per-task activation tiles in ws), then each
@@ -143,6 +153,20 @@ int qg_moe_ffn(int fmt, const float *x, int M, int H,
                float *y, int32_t *topk_ids, float *topk_w,
                void *ws, size_t ws_bytes, void *stream);
 
+/* The MoE FFN with s16 activations [KES section 四, issue ⑫]: as qg_moe_ffn, with x and
+ * the requantized h quantized by the qg_quantize_act_s16 rule instead of the int8 one (the
+ * router still reads fp32 x).  Arguments, layouts, limits and errors as qg_moe_ffn; the
+ * workspace is qg_workspace_size(QG_OP_MOE_FFN_S16, ...) and its intermediates are at
+ * qg_moe_s16_ws_layout().  On the GPU an s16 code q is held as two int8 planes,
+ * q = 256 * hi + lo, whose exact integer dots are combined in fp32: twice the dot work
+ * and activation traffic of the int8 path over the same weight bytes. */
+int qg_moe_ffn_s16(int fmt, const float *x, int M, int H,
+                   const float *Wr, int E, int topk,
+                   const void *Wg_exps, const void *Wu_exps, const void *Wd_exps,
+                   const void *Wg_sh, const void *Wu_sh, const void *Wd_sh, int I,
+                   float *y, int32_t *topk_ids, float *topk_w,
+                   void *ws, size_t ws_bytes, void *stream);
+
 /* FFN sublayer on one stream with a reused workspace [D27 section
  * "原位量化计算与单流融合的实际收益"]: x quantized once, g = Wg x and u = Wu x in one
  * launch, h = silu(g) * u, h requantized, y = Wd h.
@@ -155,7 +179,7 @@ int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd,
  * NULL); (size_t)-1 means the arguments are invalid.  The size depends on the shape and
  * on the current device's SM count (152 is assumed when no device is usable).
  *   QG_OP_GEMV / QG_OP_GEMV_Q: (fmt, M, N, K)            E, topk, I ignored
- *   QG_OP_MOE_FFN:             (fmt, M, N=H, K=H, E, topk, I)
+ *   QG_OP_MOE_FFN, QG_OP_MOE_FFN_S16: (fmt, M, N=H, K=H, E, topk, I)
  *   QG_OP_FFN_SUBLAYER:        (fmt, M, N=H, K=H, I)      E, topk ignored */
 size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, int I);
 
@@ -166,6 +190,15 @@ size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, 
  *   off[6] logits: fp32 M x E
  * Returns QG_OK or QG_EINVAL. */
 int qg_moe_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]);
+
+/* The same offsets for qg_moe_ffn_s16, whose intermediates are:
+ *   off[0] g, off[1] u : fp32, M x (topk+1) x 2 x I -- per row the two planes' partial
+ *          results, whose fp32 sum is g (u)
+ *   off[2] h : fp32, M x (topk+1) x I
+ *   off[3] hq (int16), off[4] hd (fp32), off[5] hs (int32): h requantized by the s16 rule,
+ *          M x (topk+1) x I  and  M x (topk+1) x I/32
+ *   off[6] logits: fp32 M x E */
+int qg_moe_s16_ws_layout(int M, int H, int E, int topk, int I, size_t off[7]);
 
 /* Offsets of the FFN sublayer intermediates: off[0] g, off[1] u, off[2] h (fp32 M x I). */
 int qg_ffn_ws_layout(int fmt, int M, int H, int I, size_t off[3]);

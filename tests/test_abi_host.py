@@ -87,6 +87,10 @@ def test_other_entry_points_reject_bad_arguments(L):
     bad_topk = list(args)
     bad_topk[6] = 17
     assert L.qg_moe_ffn(*bad_topk, P(A16), 1 << 30, None) == -1
+    assert L.qg_moe_ffn_s16(*args, None, 0, None) == -2                  # no workspace
+    assert L.qg_moe_ffn_s16(*bad_topk, P(A16), 1 << 30, None) == -1
+    assert L.qg_quantize_act_s16(P(A16), 1, 33, P(A16), P(A16), P(A16), None) == -1
+    assert L.qg_quantize_act_s16(P(A16), 1, 64, P(A16 + 1), P(A16), P(A16), None) == -3  # int16 codes misaligned
     assert L.qg_ffn_sublayer(12, P(A16), P(A16), P(A16), P(A16), P(A16), 1, 5120, 17408, None, 0, None) == -2
     assert L.qg_ffn_sublayer(12, P(A16), P(A16), P(A16), P(A16), P(A16), 1, 5000, 17408, P(A16), 1 << 30,
                              None) == -1
@@ -104,6 +108,15 @@ def test_workspace_sizes(L):
     assert moe != bad and moe > 3 * 4 * 4 * 9 * 512
     off = qg.qg_moe_ws_layout(4, 2048, 256, 8, 512)
     assert off == sorted(off) and off[-1] < moe
+    # s16: two planes of g and u per row, int16 codes of h, two image rows per activation row
+    moe16 = qg.qg_workspace_size(qg.QG_OP_MOE_FFN_S16, 12, 4, 2048, 2048, 256, 8, 512)
+    assert moe16 != bad and moe16 > moe
+    off16 = qg.qg_moe_s16_ws_layout(4, 2048, 256, 8, 512)
+    R, I = 4 * 9, 512
+    assert off16 == sorted(off16) and off16[-1] < moe16
+    assert off16[1] - off16[0] >= 4 * R * 2 * I and off16[3] - off16[2] >= 4 * R * I
+    assert off16[4] - off16[3] >= 2 * R * I
+    assert qg.qg_workspace_size(qg.QG_OP_MOE_FFN_S16, 12, 17, 2048, 2048, 256, 8, 512) == bad
     ffn = qg.qg_workspace_size(qg.QG_OP_FFN_SUBLAYER, 14, 16, 5120, 5120, 0, 0, 17408)
     assert ffn != bad and ffn >= 3 * 4 * 16 * 17408
     assert qg.qg_ffn_ws_layout(14, 16, 5120, 17408)[2] < ffn

@@ -1,6 +1,7 @@
 """The calls capture into CUDA graphs: every op of the path (GEMV with one and with several
-tokens, FFN sublayer, MoE FFN) is recorded once on a capture stream, its inputs are then
-overwritten in place and the graph replayed, and each replay equals a direct call on the
+tokens, FFN sublayer, MoE FFN with int8 and with s16 activations) is recorded once on a
+capture stream, its inputs are then overwritten in place and the graph replayed, and each
+replay equals a direct call on the
 same inputs bit for bit (the kernels are deterministic and allocate nothing, so a captured
 chain of preparation and engine launches, with their programmatic dependent launches,
 replays exactly)."""
@@ -72,8 +73,9 @@ def test_ffn_graph_replay(qg, M):
                           [y])
 
 
+@pytest.mark.parametrize("s16", [False, True], ids=["int8", "s16"])
 @pytest.mark.parametrize("M", [1, 3])
-def test_moe_graph_replay(qg, M):
+def test_moe_graph_replay(qg, M, s16):
     import torch
     fmt, H, E, topk, I = synth.Q4_K, 512, 16, 4, 256
     g = np.random.default_rng(31 + M)
@@ -86,9 +88,10 @@ def test_moe_graph_replay(qg, M):
     y = torch.empty((M, H), dtype=torch.float32, device="cuda")
     ids = torch.empty((M, topk), dtype=torch.int32, device="cuda")
     wts = torch.empty((M, topk), dtype=torch.float32, device="cuda")
-    nws = qg.qg_workspace_size(qg.QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I)
+    op, call = (qg.QG_OP_MOE_FFN_S16, qg.qg_moe_ffn_s16) if s16 else (qg.QG_OP_MOE_FFN, qg.qg_moe_ffn)
+    nws = qg.qg_workspace_size(op, fmt, M, H, H, E, topk, I)
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
     fresh = [[synth.activations(M, H, g)] for _ in range(2)]
     _replays_equal_direct(
-        lambda s: qg.qg_moe_ffn(fmt, x, Wr, topk, Wg, Wu, Wd, sg, su, sd, I, y=y, topk_ids=ids, topk_w=wts, ws=ws,
-                                stream=s), [x], fresh, [y, ids, wts])
+        lambda s: call(fmt, x, Wr, topk, Wg, Wu, Wd, sg, su, sd, I, y=y, topk_ids=ids, topk_w=wts, ws=ws, stream=s),
+        [x], fresh, [y, ids, wts])
