@@ -81,18 +81,6 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(const float *x, const f
     prep_tiles_warp(x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
 }
 
-// The s16 tile image of two int8 planes per row (see prep_tiles_s16_warp); launched like
-// prep_tiles_kernel.
-__global__ void __launch_bounds__(256) prep_tiles_s16_kernel(const float *x, const float *u, int in_planes,
-                                                             float *h_out, int rows, int K, int xgt_log2,
-                                                             uint8_t *img, int16_t *mq, float *md, int32_t *ms) {
-    griddep_launch_dependents();
-    griddep_wait();
-    const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
-    const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    prep_tiles_s16_warp(x, u, in_planes, h_out, rows, K, xgt_log2, img, mq, md, ms, wid, nwarps);
-}
-
 // Blocks [0, ceil(E/2)): logits[m][e] = sum_k Wr[e][k] * x[m][k] in fp32.  Each block takes
 // two experts, four warps per expert, each warp a quarter of the row with 16-byte loads so
 // that a lane's loads are all in flight at once; the quarters are added in order.  The
@@ -111,7 +99,7 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
         const long nwarps = (long)(gridDim.x - nrouter) * (blockDim.x >> 5);
         const long wid = (long)(blockIdx.x - nrouter) * (blockDim.x >> 5) + warp;
         if (s16)
-            prep_tiles_s16_warp(x, nullptr, 1, nullptr, M, H, xgt_log2, img, nullptr, nullptr, nullptr, wid, nwarps);
+            prep_tiles_s16_warp(x, M, H, xgt_log2, img, wid, nwarps);
         else
             prep_tiles_warp(x, nullptr, nullptr, nullptr, nullptr, nullptr, M, H, xgt_log2, img, nullptr, nullptr,
                             nullptr, wid, nwarps);
@@ -229,13 +217,6 @@ int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t
     const long blocks = (long)rows * (K / 32);
     const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
     return launch_pdl(prep_tiles_kernel, grid, 256, s, x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
-}
-
-int launch_prep_tiles_s16(const float *x, const float *u, int in_planes, float *h_out, int rows, int K, int xgt_log2,
-                          uint8_t *img, int16_t *mq, float *md, int32_t *ms, cudaStream_t s) {
-    const long blocks = (long)rows * (K / 32);
-    const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
-    return launch_pdl(prep_tiles_s16_kernel, grid, 256, s, x, u, in_planes, h_out, rows, K, xgt_log2, img, mq, md, ms);
 }
 
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,

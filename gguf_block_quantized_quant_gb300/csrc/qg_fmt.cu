@@ -298,7 +298,9 @@ int moe_run_p(const MoeCall &c, const MoePlan &p) {
         j.topk = c.topk;
         j.I = c.I;
         j.M = c.M;
+        j.nunits = c.M * p.S * (c.I / 32);
         j.div_slots = FastDiv::make((uint32_t)p.S);
+        j.div_ub = FastDiv::make((uint32_t)(c.I / 32));
         j.rb = p.gh.rb;
         j.ebytes = eb_gu;
         j.logits = logits;
@@ -310,17 +312,17 @@ int moe_run_p(const MoeCall &c, const MoePlan &p) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.g_out = g;
         j.u_out = u;
+        // the epilogue writes h requantized (P image rows per token and slot) for the down
+        // projection, and the plain h and its codes for callers
+        j.himg = himg;
+        j.himg_tpr = p.gi.tpr;
+        j.himg_xgt_log2 = log2i(p.gi.XGT);
+        j.h_out = h;
+        j.hq = hq;
+        j.hd = hd;
+        j.hs = hs;
         return launch_engine_ncw<FMT, T, P>(p.gu_ncw, j, p.gu_grid, p.gu_ring.smem_total, c.stream);
     });
-    if (rc) return rc;
-    // h = silu(g) * u, requantized: P image rows per token and slot; the plain h and its
-    // codes are kept in the workspace for callers
-    if constexpr (P == 2)
-        rc = launch_prep_tiles_s16(g, u, 2, h, c.M * p.S, c.I, log2i(p.gi.XGT), himg,
-                                   reinterpret_cast<int16_t *>(hq), hd, hs, c.stream);
-    else
-        rc = launch_prep_tiles(g, u, h, nullptr, nullptr, nullptr, c.M * p.S, c.I, log2i(p.gi.XGT), himg, hq, hd,
-                               hs, c.stream);
     if (rc) return rc;
     for (int ch = 0; ch < p.dn_nchunk; ++ch) {
         const int m0 = ch * p.dn_MC, mc = std::min(p.dn_MC, c.M - m0);

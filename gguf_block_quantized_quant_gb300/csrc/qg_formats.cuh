@@ -1296,6 +1296,24 @@ __device__ __forceinline__ void put_tile_unit(uint8_t *t, int u, int xgt, int la
     }
 }
 
+// Quantized activation block b (32 codes, one per lane) of image row r, in an image of tpr
+// tasks per row of 2^xgt_log2 blocks each.
+__device__ __forceinline__ void put_block(uint8_t *img, long r, int tpr, int b, int xgt_log2, int lane, int q,
+                                          float d, int s) {
+    const int xgt = 1 << xgt_log2;
+    put_tile_unit(img + (r * tpr + (b >> xgt_log2)) * tile_stride(xgt), b & (xgt - 1), xgt, lane, q, d, s);
+}
+
+// An s16 block of activation row r as its two int8 planes (see prep_tiles_s16_warp): image
+// rows 2r (hi, step 256 d) and 2r + 1 (lo, step d).
+__device__ __forceinline__ void put_block_s16(uint8_t *img, long r, int tpr, int b, int xgt_log2, int lane, int q,
+                                              float d, int s) {
+    const int hi = (q + 128) >> 8, lo = q - 256 * hi;
+    const int shi = __reduce_add_sync(0xffffffffu, hi);
+    put_block(img, 2 * r, tpr, b, xgt_log2, lane, hi, 256.0f * d, shi);
+    put_block(img, 2 * r + 1, tpr, b, xgt_log2, lane, lo, d, s - 256 * shi);
+}
+
 // Activation rows -> task-tile image in global memory: tile (row r, task tt) at
 // img + (r * tpr + tt) * tile_stride(xgt).  One warp per activation block; lane i holds
 // element i.  src_f32 != nullptr: quantize fp32 rows (activation quantization rule) --
@@ -1307,7 +1325,7 @@ __device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const floa
                                                 uint8_t *img, int8_t *mq, float *md, int32_t *ms, long wid,
                                                 long nwarps) {
     const int lane = threadIdx.x & 31;
-    const int nb = K / 32, xgt = 1 << xgt_log2, tpr = nb >> xgt_log2, stride = tile_stride(xgt);
+    const int nb = K / 32, tpr = nb >> xgt_log2;
     for (long w = wid; w < (long)rows * nb; w += nwarps) {
         const int r = (int)(w / nb), b = (int)(w - (long)r * nb);
         int qi, si;
@@ -1325,7 +1343,7 @@ __device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const floa
             di = d[(long)r * nb + b];
             si = s[(long)r * nb + b];
         }
-        put_tile_unit(img + ((long)r * tpr + (b >> xgt_log2)) * stride, b & (xgt - 1), xgt, lane, qi, di, si);
+        put_block(img, r, tpr, b, xgt_log2, lane, qi, di, si);
         if (mq) {
             mq[(long)r * K + 32L * b + lane] = (int8_t)qi;
             if (lane == 0) {
@@ -1338,53 +1356,21 @@ __device__ __forceinline__ void prep_tiles_warp(const float *src_f32, const floa
 
 // s16 activation rows -> task-tile image of two int8 planes per row.  An s16 code q is
 // split as q = 256 * hi + lo with hi = (q + 128) >> 8 in [-127, 127] and lo in [-128, 127];
-// image row 2r holds the hi plane with scale 256 * d (exact: a power-of-two scaling), row
-// 2r + 1 the lo plane with scale d, each in the int8 tile layout.  Every per-unit term the
-// engines form from a row (d * dot, d * s, the min-code sums) is linear in the codes, so
-// the two planes' results add up to the s16 result with the exact integer sums.
-// src_f32: fp32 rows; with u != nullptr the rows are h = silu(g) * u (also stored to h_out
-// when given), where in_planes == 2 means g and u hold two partial rows per row (the two
-// planes' results of the previous step) that are added first.  mq/md/ms (nullable): the
-// s16 codes, steps and code sums in their plain layout.
-__device__ __forceinline__ void prep_tiles_s16_warp(const float *src_f32, const float *u, int in_planes, float *h_out,
-                                                    int rows, int K, int xgt_log2, uint8_t *img, int16_t *mq,
-                                                    float *md, int32_t *ms, long wid, long nwarps) {
+// image row 2r holds the hi plane with step 256 * d (exact: a power-of-two scaling), row
+// 2r + 1 the lo plane with step d, each in the int8 tile layout (put_block_s16).  Every
+// per-unit term the engines form from a row (d * dot, d * s, the min-code sums) is linear
+// in the codes, so the two planes' results add up to the s16 result with the exact integer
+// sums.  One warp per activation block of the fp32 rows x.
+__device__ __forceinline__ void prep_tiles_s16_warp(const float *x, int rows, int K, int xgt_log2, uint8_t *img,
+                                                    long wid, long nwarps) {
     const int lane = threadIdx.x & 31;
-    const int nb = K / 32, xgt = 1 << xgt_log2, tpr = nb >> xgt_log2, stride = tile_stride(xgt);
+    const int nb = K / 32, tpr = nb >> xgt_log2;
     for (long w = wid; w < (long)rows * nb; w += nwarps) {
         const int r = (int)(w / nb), b = (int)(w - (long)r * nb);
-        const long idx = (long)r * K + 32L * b + lane;
-        float v;
-        if (u) {
-            float gv, uv;
-            if (in_planes == 2) {
-                const long i0 = 2L * r * K + 32L * b + lane;
-                gv = src_f32[i0] + src_f32[i0 + K];
-                uv = u[i0] + u[i0 + K];
-            } else {
-                gv = src_f32[idx];
-                uv = u[idx];
-            }
-            v = silu_mul(gv, uv);
-            if (h_out) h_out[idx] = v;
-        } else {
-            v = src_f32[idx];
-        }
         int q, s;
         float d;
-        quant_block_warp16(v, q, d, s);
-        const int hi = (q + 128) >> 8, lo = q - 256 * hi;
-        const int shi = __reduce_add_sync(0xffffffffu, hi);
-        const long tt = b >> xgt_log2;
-        put_tile_unit(img + ((2L * r) * tpr + tt) * stride, b & (xgt - 1), xgt, lane, hi, 256.0f * d, shi);
-        put_tile_unit(img + ((2L * r + 1) * tpr + tt) * stride, b & (xgt - 1), xgt, lane, lo, d, s - 256 * shi);
-        if (mq) {
-            mq[idx] = (int16_t)q;
-            if (lane == 0) {
-                md[(long)r * nb + b] = d;
-                ms[(long)r * nb + b] = s;
-            }
-        }
+        quant_block_warp16(x[(long)r * K + 32L * b + lane], q, d, s);
+        put_block_s16(img, r, tpr, b, xgt_log2, lane, q, d, s);
     }
 }
 

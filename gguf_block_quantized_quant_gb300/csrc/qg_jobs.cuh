@@ -5,7 +5,9 @@
 //                  partial sums to a buffer)
 //   FfnGateUpJob   output rows 0..I-1 = rows of Wg (g), I..2I-1 = rows of Wu (u)
 //   MoeGateUpJob   output rows of g and u for every (token, slot): the slot's routed expert
-//                  (from the router's top-k, computed by warp 0 in the prologue) or the shared one
+//                  (from the router's top-k, computed by warp 0 in the prologue) or the shared one;
+//                  each CTA owns whole 32-blocks of positions and its epilogue requantizes
+//                  h = silu(g) * u into the down projection's activation tiles
 //   MoeDownJob     per CTA, a range of hidden rows n: output rows (token, slot, n) of every
 //                  slot's down matrix, kept in shared memory; the epilogue forms
 //                  y[token][n] = sum over slots, in slot order, of weight * row (shared
@@ -133,11 +135,13 @@ constexpr int E_MAX = 1024;
 template <int FMT, int T, int P = 1>
 struct MoeGateUpJob : EngineFields {
     using F = FT<FMT, T>;
-    static constexpr bool HAS_FINISH = false, HAS_PROLOGUE = true;
+    static constexpr bool HAS_FINISH = true, HAS_PROLOGUE = true;
     const uint8_t *Wg_exps, *Wu_exps, *Wg_sh, *Wu_sh;
     const uint8_t *Wg_exps_end, *Wu_exps_end, *Wg_sh_end, *Wu_sh_end;
     int E, topk, I, M;
+    int nunits;                  // M * (topk + 1) * I / 32 units of 32 positions j
     FastDiv div_slots;           // by topk + 1
+    FastDiv div_ub;              // by I / 32
     uint32_t rb;
     size_t ebytes;               // bytes of one expert matrix
     const float *logits;         // M x E (written by the previous kernel)
@@ -148,21 +152,47 @@ struct MoeGateUpJob : EngineFields {
     const uint8_t *ximg;         // P rows per token
     uint32_t ximg_pitch;
     float *g_out, *u_out;        // [M][topk+1][P][I]
+    // h = silu(g) * u requantized (int8, or s16 as two planes): the down projection's
+    // activation tile image (P rows per (token, slot), tiles of 2^himg_xgt_log2 blocks,
+    // himg_tpr tasks per row), and the plain h, codes (int8 or int16), steps and code sums
+    uint8_t *himg;
+    int himg_tpr, himg_xgt_log2;
+    float *h_out;
+    void *hq;
+    float *hd;
+    int32_t *hs;
 
     __device__ int slots() const { return topk + 1; }
-    // o = ((token * slots + slot) * 2 + up) * I + j; groups of I rows are one matrix
-    struct Ctx {};
-    __device__ Ctx ctx() const { return {}; }
-    __device__ void cta(const Ctx &, int &o0, int &o1, int &tpr, int &grp) const {
-        const long rows = (long)M * slots() * 2 * I;
-        o0 = split_point(rows, (int)blockIdx.x, (int)gridDim.x);
-        o1 = split_point(rows, (int)blockIdx.x + 1, (int)gridDim.x);
-        tpr = tpr_x;
-        grp = I;
+    // The CTA owns units [u0, u0 + nu); unit (token * slots + slot) * I/32 + jb holds the
+    // gate and up rows j = 32 jb .. 32 jb + 31 of that slot's expert, so that the CTA can
+    // requantize whole 32-blocks of h when its rows are done.  CTA-local rows:
+    // o = 64 * (unit - u0) + 32 * up + (j & 31); runs of 32 adjacent rows.
+    struct Ctx {
+        int u0, nu;
+    };
+    __device__ Ctx ctx() const {
+        Ctx c;
+        c.u0 = split_point(nunits, (int)blockIdx.x, (int)gridDim.x);
+        c.nu = split_point(nunits, (int)blockIdx.x + 1, (int)gridDim.x) - c.u0;
+        return c;
     }
-    __device__ const uint8_t *seg_src(const Ctx &, int o, int tt, const uint8_t *&lim, const int *ids) const {
-        const int q = o / I, j = o - q * I, up = q & 1, gs = q >> 1;
-        const int m = gs / slots(), s = gs - m * slots();
+    __device__ void cta(const Ctx &c, int &o0, int &o1, int &tpr, int &grp) const {
+        o0 = 0;
+        o1 = 64 * c.nu;
+        tpr = tpr_x;
+        grp = 32;
+    }
+    // (token * slots + slot, jb) of CTA-local row o
+    __device__ __forceinline__ int unit_gs(const Ctx &c, int o, int &jb) const {
+        const int un = c.u0 + (o >> 6);
+        const int gs = (int)div_ub.div((uint32_t)un);
+        jb = un - gs * (I >> 5);
+        return gs;
+    }
+    __device__ const uint8_t *seg_src(const Ctx &c, int o, int tt, const uint8_t *&lim, const int *ids) const {
+        int jb;
+        const int gs = unit_gs(c, o, jb), up = (o >> 5) & 1, j = 32 * jb + (o & 31);
+        const int m = (int)div_slots.div((uint32_t)gs), s = gs - m * slots();
         if (s < topk) {
             const size_t e = (size_t)min(max(ids[m * topk + s], 0), E - 1);  // never leave the tensor
             lim = up ? Wu_exps_end : Wg_exps_end;
@@ -174,15 +204,53 @@ struct MoeGateUpJob : EngineFields {
     __device__ int xrows() const { return M * P; }
     __device__ const uint8_t *xrow_src(const Ctx &, int r) const { return ximg + (size_t)r * ximg_pitch; }
     __device__ uint32_t xrow_bytes(const Ctx &, int) const { return ximg_pitch; }
-    __device__ uint32_t xrow(const Ctx &, int o, const FastDiv &divI) const {
-        return P * div_slots.div(divI.div((uint32_t)o) >> 1);  // the token's first row
+    __device__ uint32_t xrow(const Ctx &c, int o, const FastDiv &) const {
+        int jb;
+        return P * div_slots.div((uint32_t)unit_gs(c, o, jb));  // the token's first row
     }
-    __device__ void store(const Ctx &, int o, int m, float v, float *) const {
-        const int q = o / I, j = o - q * I;
-        ((q & 1) ? u_out : g_out)[((long)(q >> 1) * P + m) * I + j] = v;
+    // g or u of plane m to the workspace and to the CTA's job area (64 * nu * P floats)
+    __device__ void store(const Ctx &c, int o, int m, float v, float *part) const {
+        int jb;
+        const int gs = unit_gs(c, o, jb), j = 32 * jb + (o & 31);
+        (((o >> 5) & 1) ? u_out : g_out)[((long)gs * P + m) * I + j] = v;
+        part[o * P + m] = v;
     }
     __device__ void init(float *, int) const {}
-    __device__ void finish(const Ctx &, float *, int, int) const {}
+    // One warp per unit: h = silu(g) * u for its 32 positions (g, u: the planes' partial
+    // rows added in plane order), quantized by the activation rule of the call and written
+    // into the down projection's tile image and the workspace.
+    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads) const {
+        const int lane = tid & 31;
+        for (int i = tid >> 5; i < c.nu; i += nthreads >> 5) {
+            int jb;
+            const int gs = unit_gs(c, 64 * i, jb);
+            const float *pg = part + (64 * i + lane) * P, *pu = part + (64 * i + 32 + lane) * P;
+            float g = pg[0], u = pu[0];
+#pragma unroll
+            for (int p = 1; p < P; ++p) {
+                g += pg[p];
+                u += pu[p];
+            }
+            const float h = silu_mul(g, u);
+            const long e = (long)gs * I + 32 * jb + lane, eb = (long)gs * (I >> 5) + jb;
+            h_out[e] = h;
+            int q, sum;
+            float d;
+            if constexpr (P == 2) {
+                quant_block_warp16(h, q, d, sum);
+                put_block_s16(himg, gs, himg_tpr, jb, himg_xgt_log2, lane, q, d, sum);
+                static_cast<int16_t *>(hq)[e] = (int16_t)q;
+            } else {
+                quant_block_warp(h, q, d, sum);
+                put_block(himg, gs, himg_tpr, jb, himg_xgt_log2, lane, q, d, sum);
+                static_cast<int8_t *>(hq)[e] = (int8_t)q;
+            }
+            if (lane == 0) {
+                hd[eb] = d;
+                hs[eb] = sum;
+            }
+        }
+    }
     // Router tail, warp 0, after the logits kernel has finished: softmax over E logits,
     // the topk largest (ties: lower id), weights renormalized over the picks.
     // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax

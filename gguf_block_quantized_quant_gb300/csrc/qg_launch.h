@@ -85,12 +85,6 @@ int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStrea
 int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t *xq, const float *xd,
                       const int32_t *xs, int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq, float *md,
                       int32_t *ms, cudaStream_t s);
-// The s16 tile image (two int8 planes per row) of `rows` rows: from fp32 rows x, or with
-// u != NULL from h = silu(g) * u where g = x and u hold in_planes partial rows per row
-// (added first); h_out and mq/md/ms (s16 codes, steps, code sums) optionally receive h and
-// the quantized rows in their plain layout.
-int launch_prep_tiles_s16(const float *x, const float *u, int in_planes, float *h_out, int rows, int K, int xgt_log2,
-                          uint8_t *img, int16_t *mq, float *md, int32_t *ms, cudaStream_t s);
 // Router logits (fp32) and the activation tile image of x (s16: two planes per row) in one
 // launch.
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,

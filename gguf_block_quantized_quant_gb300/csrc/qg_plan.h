@@ -312,13 +312,15 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, 
         sms < 1 || M * topk > SCRATCH_INTS)
         return p;
     p.S = topk + 1;
-    // gate/up: output rows (token, slot, gate|up, row)
-    const long gu_rows = (long)M * p.S * 2 * I;
+    // gate/up: units of 32 positions j of one (token, slot), each its 32 gate and 32 up rows;
+    // a CTA holds the g and u of its units (P planes each) for the requantization of h
+    const long gu_units = (long)M * p.S * (I / 32);
     const long gu_x = (long)M * p.P * p.gh.tpr * p.gh.stride;
     if (gu_x > (long)XCAP) return p;
-    p.gu_grid = (int)std::min<long>(sms, gu_rows);
-    p.gu_ncw = plan_ncw(p.gh, p.P, (gu_rows + p.gu_grid - 1) / p.gu_grid * p.gh.tpr);
-    p.gu_ring = plan_ring(p.gh, (long)I * p.gh.tpr, (uint32_t)gu_x, 0, p.gu_ncw);
+    p.gu_grid = (int)std::min<long>(sms, gu_units);
+    const long upc = (gu_units + p.gu_grid - 1) / p.gu_grid;  // most units of one CTA
+    p.gu_ncw = plan_ncw(p.gh, p.P, upc * 64 * p.gh.tpr);
+    p.gu_ring = plan_ring(p.gh, 32L * p.gh.tpr, (uint32_t)gu_x, (uint32_t)(upc * 64 * p.P * 4), p.gu_ncw);
     if (!p.gu_ring.ok) return p;
     // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
     const long tiles_tok = (long)p.S * p.P * p.gi.tpr * p.gi.stride;

@@ -14,11 +14,11 @@
 using namespace qg;
 static int fails = 0;
 #define CHECK(c, ...) do { if (!(c)) { ++fails; if (fails < 20) { printf("FAIL %d: ", __LINE__); printf(__VA_ARGS__); printf("\n"); } } } while (0)
-struct Cta { int o0, o1, tpr, grp; };
+struct Cta { int o0, o1, tpr, grp, base = 0; };  // base: job-specific CTA origin (MoE gate/up: first unit)
 static uint32_t toff(const TaskGeo &g, int tt) { return (uint32_t)((tt / g.TPB) * g.BPT * g.bs); }
 
-void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, std::function<Cta(int)> cta,
-         std::function<uintptr_t(int, int, uintptr_t &)> seg) {
+void sim_c(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, std::function<Cta(int)> cta,
+           std::function<uintptr_t(const Cta &, int, int, uintptr_t &)> seg) {
     CHECK(r.ok, "%s ring not ok", name);
     CHECK(r.smem_total <= (uint32_t)SMEM_MAX, "%s smem %u", name, r.smem_total);
     for (int b = 0; b < grid; ++b) {
@@ -50,7 +50,7 @@ void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, s
                     CHECK((pc.second - pc.first) % g.TPB == 0, "%s piece not whole blocks", name);
                     const int o = pc.first / c.tpr, tt = pc.first - o * c.tpr;
                     uintptr_t lim;
-                    const uintptr_t s0 = seg(c.o0 + o, tt, lim), e = s0 + toff(g, pc.second - pc.first);
+                    const uintptr_t s0 = seg(c, c.o0 + o, tt, lim), e = s0 + toff(g, pc.second - pc.first);
                     CHECK(e <= lim, "%s piece past tensor end", name);
                     off += (uint32_t)(((e + 15) & ~(uintptr_t)15) - (s0 & ~(uintptr_t)15));
                     covered = pc.second;
@@ -61,6 +61,10 @@ void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, s
     }
 }
 
+void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, std::function<Cta(int)> cta,
+         std::function<uintptr_t(int, int, uintptr_t &)> seg) {
+    sim_c(name, g, r, grid, NCW, cta, [&](const Cta &, int o, int tt, uintptr_t &lim) { return seg(o, tt, lim); });
+}
 
 // mirrors engine_pair_kernel: runs per stage, slot use, and every lane's two task addresses
 void sim_pair(const char *name, const GemvPlan &p, int N) {
@@ -187,32 +191,41 @@ int main() {
     int Es[] = {16, 64, 256}, topks[] = {1, 4, 8}, mH[] = {512, 2048, 4096, 7168}, mI[] = {256, 512, 768, 1536};
     for (int fmt : fmts) for (int E : Es) for (int topk : topks) for (int H : mH) for (int I : mI) for (int M : Ms) {
         if (topk > E || !task_geo(fmt, H, false).ok || !task_geo(fmt, I, false).ok) continue;
-        MoePlan p = plan_moe(fmt, M, H, E, topk, I, sms);
+      for (int P = 1; P <= 2; ++P) {
+        MoePlan p = plan_moe(fmt, M, H, E, topk, I, sms, P == 2);
         if (!p.ok) {
-            if ((long)M * task_geo(fmt, H, false).tpr * task_geo(fmt, H, false).stride <= (long)XCAP)
-                CHECK(false, "moe plan failed f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+            if ((long)M * P * task_geo(fmt, H, false).tpr * task_geo(fmt, H, false).stride <= (long)XCAP)
+                CHECK(false, "moe plan failed f%d E%d k%d H%d I%d M%d P%d", fmt, E, topk, H, I, M, P);
             continue;
         }
         const int S = p.S;
-        snprintf(nm, sizeof nm, "moe-gu f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+        CHECK(p.P == P, "moe planes");
+        snprintf(nm, sizeof nm, "moe-gu f%d E%d k%d H%d I%d M%d P%d", fmt, E, topk, H, I, M, P);
         const size_t eb = (size_t)I * p.gh.rb;
-        sim(nm, p.gh, p.gu_ring, p.gu_grid, p.gu_ncw,
-            [&](int b) { const long P = (long)M * S * 2 * I; Cta c; c.o0 = (int)(P * b / p.gu_grid); c.o1 = (int)(P * (b + 1) / p.gu_grid);
-                         c.tpr = p.gh.tpr; c.grp = I; return c; },
-            [&](int o, int tt, uintptr_t &lim) { const int q = o / I, jj = o - q * I, up = q & 1, s = (q >> 1) % S;
+        const long units = (long)M * S * (I / 32);
+        // units of 32 positions: CTA-local rows 64 * unit + 32 * up + (j & 31)
+        sim_c(nm, p.gh, p.gu_ring, p.gu_grid, p.gu_ncw,
+            [&](int b) { const int u0 = (int)(units * b / p.gu_grid), u1 = (int)(units * (b + 1) / p.gu_grid); Cta c;
+                         c.o0 = 0; c.o1 = 64 * (u1 - u0); c.tpr = p.gh.tpr; c.grp = 32; c.base = u0;
+                         CHECK((uint32_t)(4 * c.o1 * P) <= p.gu_ring.j_bytes, "moe gu jarea");
+                         CHECK((uint32_t)(M * P * p.gh.tpr * p.gh.stride) <= p.gu_ring.x_bytes, "moe gu x"); return c; },
+            [&](const Cta &c, int o, int tt, uintptr_t &lim) {
+                const int un = c.base + (o >> 6), up = (o >> 5) & 1, gs = un / (I / 32), jj = 32 * (un % (I / 32)) + (o & 31);
+                const int s = gs % S;
                 uintptr_t base; if (s < topk) { base = (up ? BASE + (1ull << 38) : BASE) + (uintptr_t)((s * 37 + 5) % E) * eb; lim = (up ? BASE + (1ull << 38) : BASE) + eb * E; }
                 else { base = up ? BASE + (3ull << 38) : BASE + (2ull << 38); lim = base + eb; }
                 return base + (uintptr_t)jj * p.gh.rb + toff(p.gh, tt); });
-        snprintf(nm, sizeof nm, "moe-dn f%d E%d k%d H%d I%d M%d", fmt, E, topk, H, I, M);
+        snprintf(nm, sizeof nm, "moe-dn f%d E%d k%d H%d I%d M%d P%d", fmt, E, topk, H, I, M, P);
         for (int ch = 0; ch < p.dn_nchunk; ++ch) {
             const int mc = std::min(p.dn_MC, M - ch * p.dn_MC);
             sim(nm, p.gi, p.dn_ring, p.dn_grid, p.dn_ncw,
                 [&](int b) { const int n0 = (int)((long)b * H / p.dn_grid), n1 = (int)((long)(b + 1) * H / p.dn_grid); Cta c;
                              c.o0 = 0; c.o1 = mc * S * (n1 - n0); c.tpr = p.gi.tpr; c.grp = n1 - n0;
-                             CHECK((uint32_t)(4 * c.o1) <= p.dn_ring.j_bytes, "moe dn jarea");
-                             CHECK((uint32_t)(mc * S * p.gi.tpr * p.gi.stride) <= p.dn_ring.x_bytes, "moe dn x"); return c; },
+                             CHECK((uint32_t)(4 * c.o1 * P) <= p.dn_ring.j_bytes, "moe dn jarea");
+                             CHECK((uint32_t)(mc * S * P * p.gi.tpr * p.gi.stride) <= p.dn_ring.x_bytes, "moe dn x"); return c; },
                 [&](int o, int tt, uintptr_t &lim) { lim = BASE + (uintptr_t)H * p.gi.rb * (E + 1) * 32; return BASE + (uintptr_t)o * p.gi.rb + toff(p.gi, tt); });
         }
+      }
     }
     printf("fails %d\n", fails);
     return fails != 0;
