@@ -96,14 +96,28 @@ def row_bytes(fmt: int, K: int) -> int:
     return (K // BLOCK_ELEMS[fmt]) * BLOCK_BYTES[fmt]
 
 
-def _ptr(t):
+def _ptr(t, host_ok=True):
+    """Device address of a tensor: a CUDA tensor, or (where the C API allows host memory:
+    activations and outputs) a page-locked host tensor, which the kernels address directly."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("libqg takes CUDA tensors only")
+    if not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError("libqg takes CUDA tensors" + (" or page-locked (pinned) host tensors" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError("libqg takes contiguous tensors only")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t):
+    """The CUDA device of a call whose activations are t (the current device for host t)."""
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
+def _out(shape, dtype, like):
+    """An output next to the activations: on their device, or page-locked host memory."""
+    if like.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
 
 
 def _stream(stream):
@@ -131,9 +145,9 @@ def qg_workspace_size(op: int, fmt: int, M: int, N: int, K: int, E: int = 0, top
 
 def qg_quantize_act(x, xq=None, xd=None, xs=None, stream=None):
     M, K = x.shape
-    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
-    xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device) if xd is None else xd
-    xs = torch.empty((M, K // 32), dtype=torch.int32, device=x.device) if xs is None else xs
+    xq = _out((M, K), torch.int8, x) if xq is None else xq
+    xd = _out((M, K // 32), torch.float32, x) if xd is None else xd
+    xs = _out((M, K // 32), torch.int32, x) if xs is None else xs
     _check(lib().qg_quantize_act(_ptr(x), M, K, _ptr(xq), _ptr(xd), _ptr(xs), _stream(stream)),
            "qg_quantize_act")
     return xq, xd, xs
@@ -141,9 +155,9 @@ def qg_quantize_act(x, xq=None, xd=None, xs=None, stream=None):
 
 def qg_quantize_act_s16(x, xq=None, xd=None, xs=None, stream=None):
     M, K = x.shape
-    xq = torch.empty((M, K), dtype=torch.int16, device=x.device) if xq is None else xq
-    xd = torch.empty((M, K // 32), dtype=torch.float32, device=x.device) if xd is None else xd
-    xs = torch.empty((M, K // 32), dtype=torch.int32, device=x.device) if xs is None else xs
+    xq = _out((M, K), torch.int16, x) if xq is None else xq
+    xd = _out((M, K // 32), torch.float32, x) if xd is None else xd
+    xs = _out((M, K // 32), torch.int32, x) if xs is None else xs
     _check(lib().qg_quantize_act_s16(_ptr(x), M, K, _ptr(xq), _ptr(xd), _ptr(xs), _stream(stream)),
            "qg_quantize_act_s16")
     return xq, xd, xs
@@ -151,9 +165,9 @@ def qg_quantize_act_s16(x, xq=None, xd=None, xs=None, stream=None):
 
 def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
     M, K = x.shape
-    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
-    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), x.device)
-    _check(lib().qg_gemv(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _ptr(ws), nws, _stream(stream)), "qg_gemv")
+    y = _out((M, N), torch.float32, x) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), _dev(x))
+    _check(lib().qg_gemv(fmt, _ptr(W, False), _ptr(x), _ptr(y), N, K, M, _ptr(ws, False), nws, _stream(stream)), "qg_gemv")
     return y
 
 
@@ -165,16 +179,16 @@ def qg_gemv_static_ws(fmt: int, W, x, N: int, y=None, stream=None):
     calls that may overlap on the GPU must be ordered on one stream.  The first call on a
     device looks up the scratch address and should come before any stream capture."""
     M, K = x.shape
-    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
-    _check(lib().qg_gemv_static_ws(fmt, _ptr(W), _ptr(x), _ptr(y), N, K, M, _stream(stream)), "qg_gemv_static_ws")
+    y = _out((M, N), torch.float32, x) if y is None else y
+    _check(lib().qg_gemv_static_ws(fmt, _ptr(W, False), _ptr(x), _ptr(y), N, K, M, _stream(stream)), "qg_gemv_static_ws")
     return y
 
 
 def qg_gemv_q(fmt: int, W, xq, xd, xs, N: int, y=None, ws=None, stream=None):
     M, K = xq.shape
-    y = torch.empty((M, N), dtype=torch.float32, device=xq.device) if y is None else y
-    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV_Q, fmt, M, N, K), xq.device)
-    _check(lib().qg_gemv_q(fmt, _ptr(W), _ptr(xq), _ptr(xd), _ptr(xs), _ptr(y), N, K, M, _ptr(ws), nws,
+    y = _out((M, N), torch.float32, xq) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_GEMV_Q, fmt, M, N, K), _dev(xq))
+    _check(lib().qg_gemv_q(fmt, _ptr(W, False), _ptr(xq), _ptr(xd), _ptr(xs), _ptr(y), N, K, M, _ptr(ws, False), nws,
                            _stream(stream)), "qg_gemv_q")
     return y
 
@@ -183,11 +197,11 @@ def qg_moe_ffn(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_
                y=None, topk_ids=None, topk_w=None, ws=None, stream=None):
     M, H = x.shape
     E = Wr.shape[0]
-    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
-    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), x.device)
-    _check(lib().qg_moe_ffn(fmt, _ptr(x), M, H, _ptr(Wr), E, topk, _ptr(Wg_exps), _ptr(Wu_exps), _ptr(Wd_exps),
-                            _ptr(Wg_sh), _ptr(Wu_sh), _ptr(Wd_sh), I, _ptr(y), _ptr(topk_ids), _ptr(topk_w),
-                            _ptr(ws), nws, _stream(stream)), "qg_moe_ffn")
+    y = _out((M, H), torch.float32, x) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), _dev(x))
+    _check(lib().qg_moe_ffn(fmt, _ptr(x), M, H, _ptr(Wr, False), E, topk, _ptr(Wg_exps, False), _ptr(Wu_exps, False), _ptr(Wd_exps, False),
+                            _ptr(Wg_sh, False), _ptr(Wu_sh, False), _ptr(Wd_sh, False), I, _ptr(y), _ptr(topk_ids), _ptr(topk_w),
+                            _ptr(ws, False), nws, _stream(stream)), "qg_moe_ffn")
     return y
 
 
@@ -195,19 +209,19 @@ def qg_moe_ffn_s16(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh,
                    y=None, topk_ids=None, topk_w=None, ws=None, stream=None):
     M, H = x.shape
     E = Wr.shape[0]
-    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
-    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN_S16, fmt, M, H, H, E, topk, I), x.device)
-    _check(lib().qg_moe_ffn_s16(fmt, _ptr(x), M, H, _ptr(Wr), E, topk, _ptr(Wg_exps), _ptr(Wu_exps),
-                                _ptr(Wd_exps), _ptr(Wg_sh), _ptr(Wu_sh), _ptr(Wd_sh), I, _ptr(y), _ptr(topk_ids),
-                                _ptr(topk_w), _ptr(ws), nws, _stream(stream)), "qg_moe_ffn_s16")
+    y = _out((M, H), torch.float32, x) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_MOE_FFN_S16, fmt, M, H, H, E, topk, I), _dev(x))
+    _check(lib().qg_moe_ffn_s16(fmt, _ptr(x), M, H, _ptr(Wr, False), E, topk, _ptr(Wg_exps, False), _ptr(Wu_exps, False),
+                                _ptr(Wd_exps, False), _ptr(Wg_sh, False), _ptr(Wu_sh, False), _ptr(Wd_sh, False), I, _ptr(y), _ptr(topk_ids),
+                                _ptr(topk_w), _ptr(ws, False), nws, _stream(stream)), "qg_moe_ffn_s16")
     return y
 
 
 def qg_ffn_sublayer(fmt: int, Wg, Wu, Wd, x, I: int, y=None, ws=None, stream=None):
     M, H = x.shape
-    y = torch.empty((M, H), dtype=torch.float32, device=x.device) if y is None else y
-    ws, nws = _ws(ws, qg_workspace_size(QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), x.device)
-    _check(lib().qg_ffn_sublayer(fmt, _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(x), _ptr(y), M, H, I, _ptr(ws), nws,
+    y = _out((M, H), torch.float32, x) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), _dev(x))
+    _check(lib().qg_ffn_sublayer(fmt, _ptr(Wg, False), _ptr(Wu, False), _ptr(Wd, False), _ptr(x), _ptr(y), M, H, I, _ptr(ws, False), nws,
                                  _stream(stream)), "qg_ffn_sublayer")
     return y
 
@@ -232,9 +246,9 @@ def qg_ffn_ws_layout(fmt: int, M: int, H: int, I: int):
 
 def qg_block_dots(fmt: int, W, xq, xs, N: int, stream=None):
     M, K = xq.shape
-    dots = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
-    aux = torch.empty((M, N, K // 32), dtype=torch.int32, device=xq.device)
-    _check(lib().qg_block_dots(fmt, _ptr(W), _ptr(xq), _ptr(xs), N, K, M, _ptr(dots), _ptr(aux), _stream(stream)),
+    dots = _out((M, N, K // 32), torch.int32, xq)
+    aux = _out((M, N, K // 32), torch.int32, xq)
+    _check(lib().qg_block_dots(fmt, _ptr(W, False), _ptr(xq), _ptr(xs), N, K, M, _ptr(dots), _ptr(aux), _stream(stream)),
            "qg_block_dots")
     return dots, aux
 

@@ -18,10 +18,15 @@
  *        top-k -> expert gate/up -> swiglu -> down, weighted aggregation).
  *
  * Conventions for every call below:
- *  - All tensor pointers are DEVICE pointers owned by the caller.  The library never
- *    allocates, frees or synchronizes; each call only validates its arguments on the
- *    host and enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
- *    stream).  Results are ready when the stream reaches them.
+ *  - All tensor pointers are owned by the caller.  Weights (W, the expert tensors, Wr)
+ *    and the workspace ws must be device memory.  Activations and outputs (x, y, xq, xd,
+ *    xs, topk_ids, topk_w, dots, aux) may be device memory or page-locked host memory
+ *    that the device addresses directly (cudaHostAlloc / cudaHostRegister under unified
+ *    addressing): the kernels then read and write them over the host link (NVLink-C2C on
+ *    Grace systems) with no staging copy; results in host memory are complete when the
+ *    stream reaches the point after the call.  The library never allocates, frees or
+ *    synchronizes; each call only validates its arguments on the host and enqueues
+ *    kernels on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - Return value: QG_OK (0) or a negative QG_E* status.  Every argument check happens
  *    on the host before any launch, so a failed call has enqueued nothing.  There is no
  *    CPU fallback: a GPU problem is reported, never silently computed elsewhere.
