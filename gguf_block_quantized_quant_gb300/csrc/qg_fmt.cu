@@ -150,25 +150,30 @@ void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
 // A row-pair GEMV plan (p.pair) of N rows against an activation tile image that is already
 // written (ximg, per-token pitch ximg_pitch, tiles of p.geo.XGT units): out = W x.
 template <int FMT>
+// The tokens go in chunks of p.MC (one launch each; every launch streams the weights).
 int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8_t *ximg, size_t ximg_pitch,
                   float *out, cudaStream_t stream) {
-    return with_t<false>(p.geo, [&](auto Tc) {
-        constexpr int T = decltype(Tc)::value;
-        GemvJob<FMT, T> j;
-        set_engine(j, p.ring, p.tpr_x, M);
-        j.W = W;
-        j.Wend = W + (size_t)N * p.geo.rb;
-        j.N = N;
-        j.KS = 1;
-        j.groups = p.groups;
-        j.gpr = p.geo.gpr;
-        j.rb = p.geo.rb;
-        j.ximg = ximg;
-        j.ximg_pitch = (uint32_t)ximg_pitch;
-        j.out = out;
-        j.slice_stride = (long)M * N;
-        return launch_pair<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, stream);
-    });
+    for (int m0 = 0; m0 < M; m0 += p.MC) {
+        const int rc = with_t<false>(p.geo, [&](auto Tc) {
+            constexpr int T = decltype(Tc)::value;
+            GemvJob<FMT, T> j;
+            set_engine(j, p.ring, p.tpr_x, std::min(p.MC, M - m0));
+            j.W = W;
+            j.Wend = W + (size_t)N * p.geo.rb;
+            j.N = N;
+            j.KS = 1;
+            j.groups = p.groups;
+            j.gpr = p.geo.gpr;
+            j.rb = p.geo.rb;
+            j.ximg = ximg + (size_t)m0 * ximg_pitch;
+            j.ximg_pitch = (uint32_t)ximg_pitch;
+            j.out = out + (size_t)m0 * N;
+            j.slice_stride = (long)M * N;
+            return launch_pair<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, stream);
+        });
+        if (rc) return rc;
+    }
+    return 0;
 }
 
 template <int FMT>
@@ -178,6 +183,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     int rc = launch_prep_tiles(c.x, c.u, c.h_out, c.xq, c.xd, c.xs, c.M, c.K, log2i(p.geo.XGT), ximg, nullptr,
                                nullptr, nullptr, c.stream);
     if (rc) return rc;
+    if (p.pair) return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y, c.stream);
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
@@ -194,7 +200,6 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
         j.ximg_pitch = (uint32_t)p.ximg_pitch;
         j.out = out;
         j.slice_stride = (long)c.M * c.N;
-        if (p.pair) return launch_pair<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
         return launch_engine_mt<FMT, T>(p.MT, p.ncw, j, p.grid, p.ring.smem_total, c.stream);
     });
     if (rc) return rc;

@@ -676,6 +676,10 @@ struct FmtQ4K {
         static_assert(T == 1, "row pairs take one-superblock tasks");
         using TL = Tile<XGT>;
         constexpr int MT = PSink::MT;
+        if constexpr (MT >= 16) {
+            compute_pair_tokens_inner(w0, 0u, w1, 0u, xt, ntok, sink);
+            return;
+        }
         uint32_t S03[2], M03[2], S47[2], M47[2];
         float d[2], dmin[2];
 #pragma unroll
@@ -724,6 +728,67 @@ struct FmtQ4K {
             }
 #pragma unroll
             for (int r = 0; r < 2; ++r) sink.add(r, m, fmaf(d[r], A[r], -dmin[r] * B[r]));
+        }
+    }
+
+    // compute_pair with the loop over unit pairs outside and tokens inside (16 tokens per
+    // lane): a unit's masked code words and its scales folded with d and dmin (fp32) are
+    // formed once for all tokens, and per token and row a unit pair costs its 16 dp4a, two
+    // conversions and four FMAs into the row's sum.  Measured 17 % faster than the
+    // token-outer order at 16 tokens, equal at 8 and slower at 2 and 4.
+    template <class PSink>
+    __device__ __forceinline__ static void compute_pair_tokens_inner(const uint32_t (&w0)[WW], uint32_t, const uint32_t (&w1)[WW],
+                                                        uint32_t, const XT &xt, int ntok, PSink &sink) {
+        static_assert(T == 1, "row pairs take one-superblock tasks");
+        using TL = Tile<XGT>;
+        constexpr int MT = PSink::MT;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int k0 = 2 * (p & 1);
+            uint32_t lo[2][8], hi[2][8];
+            float dsc[2][2], dmn[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t(&w)[WW] = r ? w1 : w0;
+                const uint32_t Sw = p < 2 ? (w[1] & 0x3f3f3f3fu) : ((w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u));
+                const uint32_t Mw =
+                    p < 2 ? (w[2] & 0x3f3f3f3fu) : (((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u));
+                const float d = half_bits_to_float(w[0]), dmin = half_bits_to_float(w[0] >> 16);
+                dsc[r][0] = d * (float)byte_of(Sw, k0);
+                dsc[r][1] = d * (float)byte_of(Sw, k0 + 1);
+                dmn[r][0] = dmin * (float)byte_of(Mw, k0);
+                dmn[r][1] = dmin * (float)byte_of(Mw, k0 + 1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    lo[r][k] = w[4 + 8 * p + k] & 0x0f0f0f0fu;
+                    hi[r][k] = w[4 + 8 * p + k] & 0xf0f0f0f0u;
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m >= ntok) continue;
+                const SAddr t = xt.tile(m);
+                uint32_t xa[8], xb[8];
+                ldx8(t + 64 * p, xa);
+                ldx8(t + 64 * p + 32, xb);
+                const uint2 xd = lds64(t + TL::D + 8 * p), xq = lds64(t + TL::Q + 8 * p);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    int da = 0, db = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        da = dp4a(lo[r][k], xa[k], da);
+                        db = dp4a_us(hi[r][k], xb[k], db);
+                    }
+                    db >>= 4;
+                    float v = sink.acc[r][m];
+                    v = fmaf((float)da, __uint_as_float(xd.x) * dsc[r][0], v);
+                    v = fmaf((float)db, __uint_as_float(xd.y) * dsc[r][1], v);
+                    v = fmaf(-__uint_as_float(xq.x), dmn[r][0], v);
+                    v = fmaf(-__uint_as_float(xq.y), dmn[r][1], v);
+                    sink.acc[r][m] = v;
+                }
+            }
         }
     }
 

@@ -195,6 +195,7 @@ struct GemvPlan {
     TaskGeo geo;
     int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0, ncw = 8;
     bool pair = false;  // row-pair engine: tasks of two rows (engine_pair_kernel)
+    int MC = 0;         // row pairs: tokens per launch (launches over token chunks of MC)
     Ring ring;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
@@ -205,6 +206,7 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     const TaskGeo &g = p.geo;
     if (!g.ok || N < 1 || M < 1 || M > M_MAX || sms < 1) return p;
     p.KS = N < G_PLAN / 2 ? std::min(g.gpr, (G_PLAN + N - 1) / N) : 1;
+    const bool split_for_n = p.KS > 1;
     auto xbytes = [&](int ks) { return (long)M * ((g.gpr + ks - 1) / ks) * g.TPB * g.stride; };
     while (xbytes(p.KS) > (long)XCAP && p.KS < g.gpr) ++p.KS;
     if (xbytes(p.KS) > (long)XCAP) return p;
@@ -216,14 +218,20 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     p.ncw = plan_ncw(g, p.MT, (long)((N + p.groups - 1) / p.groups) * p.tpr_x);
     p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, p.ncw);
     if (!p.ring.ok) return p;
-    // row pairs: an un-split GEMV of Q4_K or Q4_0 (8-block tasks) with at least two rows
-    // and two tokens (with one token the one-row tasks measured faster)
-    if (p.KS == 1 && N >= 2 && p.MT >= 2) {
+    // row pairs: a GEMV of whole rows (not split for lack of rows) with at least two rows
+    // and two tokens (with one token the one-row tasks measured faster).  When the tiles of
+    // all tokens do not fit, the tokens go in chunks of MC, the largest power of two whose
+    // tiles do (each chunk streams the weights again: measured faster than the split-K
+    // one-row launch at 8 and 16 tokens on rows of 17408).
+    if (!split_for_n && N >= 2 && p.MT >= 2) {
         const TaskGeo pg = pair_geo(fmt, K);
-        const long px = (long)M * pg.tpr * pg.stride;
+        int mc = M;
+        while (mc > 2 && (long)mc * pg.tpr * pg.stride > (long)XCAP) mc = pick_mt(mc) / 2;
+        const long px = (long)mc * pg.tpr * pg.stride;
+        const int mt = pick_mt(mc) < 2 ? 2 : pick_mt(mc);
         // Q5_K / Q6_K pairs hold 88 / 108 words of weights: at 16 tokens per lane they ran
         // out of registers and were slower than one-row tasks
-        const bool regs_ok = p.MT <= 8 || (fmt != 13 && fmt != 14);
+        const bool regs_ok = mt <= 8 || (fmt != 13 && fmt != 14);
         if (pg.ok && px <= (long)XCAP && regs_ok) {
             const int P = (N + 1) / 2, pgroups = std::min(P, sms);
             const int pncw = 8;  // two-row tasks of 288 to 420 bytes and two or more tokens per lane
@@ -231,6 +239,9 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
             if (pr.ok) {
                 p.pair = true;
                 p.geo = pg;
+                p.KS = 1;
+                p.MT = mt;
+                p.MC = mc;
                 p.groups = p.grid = pgroups;
                 p.tpr_x = pg.tpr;
                 p.ncw = pncw;

@@ -155,6 +155,10 @@ int main() {
         const TaskGeo &g = p.geo;
         if (p.pair) {
             snprintf(nm, sizeof nm, "pair f%d N%d K%d M%d", fmt, N, K, M);
+            // token chunks: MC tokens per launch, their tiles within the launch's x area
+            CHECK(p.MC >= 1 && p.MC <= M && p.MC <= p.MT && p.MT >= 2, "%s chunk %d of %d (MT %d)", nm, p.MC, M, p.MT);
+            CHECK((long)p.MC * g.tpr * g.stride <= (long)p.ring.x_bytes, "%s chunk tiles", nm);
+            CHECK(p.KS == 1, "%s pairs split", nm);
             sim_pair(nm, p, N);
             ++npair;
             continue;

@@ -127,6 +127,10 @@ PAIR_CASES = [(fmt, N, K, M)
               for fmt, K in [(synth.Q4_K, 1280), (synth.Q4_0, 768), (synth.Q8_0, 384), (synth.Q5_1, 640),
                              (synth.Q6_K, 2304), (synth.Q5_K, 512), (synth.IQ4_XS, 1024), (synth.IQ4_NL, 1536)]
               for N, M in [(77, 2), (153, 3), (1001, 5), (2, 16)]]
+# rows too long for the tiles of every token: row pairs over token chunks (the last chunk
+# ragged), and 16 tokens per lane with the unit-outer Q4_K decode
+PAIR_CASES += [(synth.Q4_K, 301, 17408, 8), (synth.Q4_K, 300, 17408, 15), (synth.Q4_0, 77, 17408, 6),
+               (synth.Q6_K, 200, 17408, 16), (synth.Q8_0, 100, 8192, 16), (synth.Q4_K, 999, 2048, 16)]
 
 
 @pytest.mark.parametrize("fmt,N,K,M", PAIR_CASES,
