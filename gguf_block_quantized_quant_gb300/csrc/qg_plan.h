@@ -225,14 +225,14 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     // one-row launch at 8 and 16 tokens on rows of 17408).
     if (!split_for_n && N >= 2 && p.MT >= 2) {
         const TaskGeo pg = pair_geo(fmt, K);
-        int mc = M;
+        // Q5_K / Q6_K pairs hold 88 / 108 words of weights: at 16 tokens per lane they ran
+        // out of registers, so they take at most 8 tokens per launch (two launches of 8
+        // measured faster than one one-row launch of 16)
+        int mc = (fmt == 13 || fmt == 14) ? std::min(M, 8) : M;
         while (mc > 2 && (long)mc * pg.tpr * pg.stride > (long)XCAP) mc = pick_mt(mc) / 2;
         const long px = (long)mc * pg.tpr * pg.stride;
         const int mt = pick_mt(mc) < 2 ? 2 : pick_mt(mc);
-        // Q5_K / Q6_K pairs hold 88 / 108 words of weights: at 16 tokens per lane they ran
-        // out of registers and were slower than one-row tasks
-        const bool regs_ok = mt <= 8 || (fmt != 13 && fmt != 14);
-        if (pg.ok && px <= (long)XCAP && regs_ok) {
+        if (pg.ok && px <= (long)XCAP) {
             const int P = (N + 1) / 2, pgroups = std::min(P, sms);
             const int pncw = 8;  // two-row tasks of 288 to 420 bytes and two or more tokens per lane
             const Ring pr = plan_ring_pair(pg, (uint32_t)px, pncw);
