@@ -385,9 +385,11 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
 // and the combine of pairs shared by two warps work as in engine_kernel, with two sums
 // per token.
 constexpr int PAIR_BND = 1 + 2 * 16;  // boundary entry: pair, then row-0 and row-1 sums
-constexpr int PAIR_RUNS = 3;
+constexpr int PAIR_RUNS = 3;        // runs of a stage over whole rows
+constexpr int PAIR_RUNS_SPLIT = 8;  // over K-slices: one run per row of up to 4 pairs
+constexpr int PAIR_SPLIT_MIN_TPR = 11;  // slice tasks that keep a 32-task stage within 4 pairs
 __host__ __device__ constexpr uint32_t pair_fixed_smem(int S, int ncw) {
-    return (uint32_t)(ncw * 2 * PAIR_BND * 4) + 8u * (uint32_t)S + 8u + 4u * PAIR_RUNS * (uint32_t)S + 16u;
+    return (uint32_t)(ncw * 2 * PAIR_BND * 4) + 8u * (uint32_t)S + 8u + 4u * PAIR_RUNS_SPLIT * (uint32_t)S + 16u;
 }
 
 template <int NT>
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
     const uint32_t xbar = bars + 8u * (uint32_t)S;
     const uint32_t hdrs = xbar + 8u;
     auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
-    auto hdr = [&](int s, int k) { return hdrs + 4u * (uint32_t)(s * PAIR_RUNS + k); };
+    auto hdr = [&](int s, int k) { return hdrs + 4u * (uint32_t)(s * PAIR_RUNS_SPLIT + k); };
     const uint32_t tok_stride = (uint32_t)(job.tpr_x * TL::STRIDE);
     float *bsum = reinterpret_cast<float *>(smem + (bnd - ring));  // [NCW][2][PAIR_BND]
 
@@ -428,17 +430,26 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
     }
     __syncwarp();
 
-    const int N = job.N, tpr = job.tpr_x;
+    // CTA = (group of row pairs, K-slice): with KS > 1 the CTA takes tasks [t0, t0 + tpr)
+    // of every row of its pairs and writes partial sums to slice ks of job.out
+    const int N = job.N, KS = job.KS;
+    const bool split = KS > 1;
+    const int grp = (int)blockIdx.x / KS, ks = (int)blockIdx.x - grp * KS, ngroups = (int)gridDim.x / KS;
+    const int t0 = split_point(job.gpr, ks, KS) * F::TPB;
+    const int tpr = split_point(job.gpr, ks + 1, KS) * F::TPB - t0;
+    float *const out = job.out + (long)ks * job.slice_stride;
     const int P = (N + 1) >> 1;
-    const int p0 = split_point(P, (int)blockIdx.x, (int)gridDim.x);
-    const int p1 = split_point(P, (int)blockIdx.x + 1, (int)gridDim.x);
+    const int p0 = split_point(P, grp, ngroups);
+    const int p1 = split_point(P, grp + 1, ngroups);
     const int ntask = (p1 - p0) * tpr;
     const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
     const int a = (int)((long)ntask * warp / NCW), b = (int)((long)ntask * (warp + 1) / NCW);
     const int maxlen = (ntask + NCW - 1) / NCW;
     const int nchunk = (maxlen + job.tps - 1) / job.tps;
 
-    // Copies stage j of this warp into its slot (which must be free); lane k < 3 copies run k.
+    // Copies stage j of this warp into its slot (which must be free).  Whole rows: lane
+    // k < 3 copies run k (see above).  K-slices: lane k < 8 copies the slice part of row
+    // k & 1 of the stage's (k >> 1)-th pair.
     auto issue = [&](int j) {
         const int slot = (j % D) * NCW + warp;
         const int fa = a + j * job.tps, fb = min(b, fa + job.tps);
@@ -446,12 +457,21 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
         const uint32_t fbar = full_bar(slot);
         bool valid = false;
         uintptr_t s0 = 0, a0 = 0, e = 0, a1c = 0;
-        if (fa < fb && lane < PAIR_RUNS) {
+        if (fa < fb && lane < (split ? PAIR_RUNS_SPLIT : PAIR_RUNS)) {
             const int pa = (int)tpr_div.div((uint32_t)fa), ca = fa - pa * tpr;
             const int pb = (int)tpr_div.div((uint32_t)(fb - 1)), cb = fb - 1 - pb * tpr;
             const int ra = 2 * (p0 + pa), rz = 2 * (p0 + pb);
             int row = 0, col = 0, n = 0;
-            if (lane == 0) {
+            if (split) {
+                const int pp = pa + (lane >> 1);
+                if (pp <= pb) {
+                    row = 2 * (p0 + pp) + (lane & 1);
+                    col = pp == pa ? ca : 0;
+                    n = (pp == pb ? cb + 1 : tpr) - col;
+                }
+                // a stage over more than 4 pairs (a planning error) is skipped past them
+                if (lane == 0 && pb - pa >= PAIR_RUNS_SPLIT / 2) atomicOr(&g_qg_dev_err, DEVERR_PLAN);
+            } else if (lane == 0) {
                 row = ra, col = ca, n = pa == pb ? cb - ca + 1 : tpr - ca;
             } else if (lane == 1) {
                 row = ra + 1, col = ca;
@@ -461,7 +481,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
             }
             valid = n > 0 && row < N;
             if (valid) {
-                s0 = (uintptr_t)(job.W + (size_t)row * job.rb + (size_t)col * TB);
+                s0 = (uintptr_t)(job.W + (size_t)row * job.rb + (size_t)(t0 + col) * TB);
                 a0 = s0 & ~(uintptr_t)15;
                 e = s0 + (uintptr_t)n * TB;
                 const uintptr_t lim16 = (uintptr_t)job.Wend & ~(uintptr_t)15;
@@ -473,7 +493,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
         const uint32_t wsz = valid ? (uint32_t)(((e + 15) & ~(uintptr_t)15) - a0) : 0u;
         uint32_t incl = wsz;
 #pragma unroll
-        for (int d = 1; d < PAIR_RUNS; d <<= 1) {
+        for (int d = 1; d < PAIR_RUNS_SPLIT; d <<= 1) {
             const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
             if (lane >= d) incl += v;
         }
@@ -501,7 +521,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
             const int rows = ntask > 0 ? job.ntok : 0;
             const uint32_t bytes = (uint32_t)(tpr * TL::STRIDE);
             for (int r = 0; r < rows; ++r)
-                bulk_g2s(xa + (uint32_t)r * tok_stride, job.ximg + (size_t)r * job.ximg_pitch, bytes, xbar);
+                bulk_g2s(xa + (uint32_t)r * tok_stride,
+                         job.ximg + (size_t)r * job.ximg_pitch + (size_t)t0 * TL::STRIDE, bytes, xbar);
             mbar_arrive_expect_tx(xbar, bytes * (uint32_t)rows);
         }
         __syncwarp();
@@ -515,8 +536,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
 
     auto store_pair = [&](int p, int m, float v0, float v1) {
         const int r0 = 2 * (p0 + p);
-        job.out[(long)m * N + r0] = v0;
-        if (r0 + 1 < N) job.out[(long)m * N + r0 + 1] = v1;
+        out[(long)m * N + r0] = v0;
+        if (r0 + 1 < N) out[(long)m * N + r0 + 1] = v1;
     };
 
     float carry[2][MT];
@@ -540,18 +561,26 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
             const int pb = (int)tpr_div.div((uint32_t)(fb - 1));
             p = (int)tpr_div.div((uint32_t)f);
             c = f - p * tpr;
-            const SAddr h0 = smem + (lds32(hdr(slot, 0)) - ring);
-            const SAddr h1 = smem + (lds32(hdr(slot, 1)) - ring);
-            const int ra = 2 * pa, r0 = 2 * p;  // CTA-relative rows
-            const SAddr addr0 = p == pa ? h0 + (uint32_t)(c - ca) * TB
-                                        : h1 + (uint32_t)((r0 - ra - 1) * tpr + c - ca) * TB;
-            SAddr addr1;
-            if (2 * (p0 + p) + 1 >= N)
-                addr1 = addr0;  // the last row of an odd N has no partner
-            else if (pb > pa && p == pb)
-                addr1 = smem + (lds32(hdr(slot, 2)) - ring) + (uint32_t)c * TB;
-            else
-                addr1 = h1 + (uint32_t)((r0 - ra) * tpr + c - ca) * TB;
+            SAddr addr0, addr1;
+            if (split) {
+                // (a stage over more than 4 pairs was flagged when it was issued; its extra
+                // lanes read the last run, inside the slot)
+                const int k = min(2 * (p - pa), PAIR_RUNS_SPLIT - 2);
+                const uint32_t cofs = (uint32_t)(c - (p == pa ? ca : 0)) * TB;
+                addr0 = smem + (lds32(hdr(slot, k)) - ring) + cofs;
+                addr1 = 2 * (p0 + p) + 1 >= N ? addr0 : smem + (lds32(hdr(slot, k + 1)) - ring) + cofs;
+            } else {
+                const SAddr h0 = smem + (lds32(hdr(slot, 0)) - ring);
+                const SAddr h1 = smem + (lds32(hdr(slot, 1)) - ring);
+                const int ra = 2 * pa, r0 = 2 * p;  // CTA-relative rows
+                addr0 = p == pa ? h0 + (uint32_t)(c - ca) * TB : h1 + (uint32_t)((r0 - ra - 1) * tpr + c - ca) * TB;
+                if (2 * (p0 + p) + 1 >= N)
+                    addr1 = addr0;  // the last row of an odd N has no partner
+                else if (pb > pa && p == pb)
+                    addr1 = smem + (lds32(hdr(slot, 2)) - ring) + (uint32_t)c * TB;
+                else
+                    addr1 = h1 + (uint32_t)((r0 - ra) * tpr + c - ca) * TB;
+            }
             F::load(addr0, w0);
             F::load(addr1, w1);
             al0 = (uint32_t)((uintptr_t)addr0 & 3u);

@@ -151,8 +151,12 @@ void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
 // written (ximg, per-token pitch ximg_pitch, tiles of p.geo.XGT units): out = W x.
 template <int FMT>
 // The tokens go in chunks of p.MC (one launch each; every launch streams the weights).
+// With p.KS > 1 every launch writes partial sums of its K-slices to part ([KS][M][N]),
+// added into y by one reduction at the end.
 int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8_t *ximg, size_t ximg_pitch,
-                  float *out, cudaStream_t stream) {
+                  float *y, float *part, cudaStream_t stream) {
+    if (p.KS > 1 && part == nullptr) return -1;
+    float *out = p.KS > 1 ? part : y;
     for (int m0 = 0; m0 < M; m0 += p.MC) {
         const int rc = with_t<false>(p.geo, [&](auto Tc) {
             constexpr int T = decltype(Tc)::value;
@@ -161,7 +165,7 @@ int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8
             j.W = W;
             j.Wend = W + (size_t)N * p.geo.rb;
             j.N = N;
-            j.KS = 1;
+            j.KS = p.KS;
             j.groups = p.groups;
             j.gpr = p.geo.gpr;
             j.rb = p.geo.rb;
@@ -173,6 +177,7 @@ int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8
         });
         if (rc) return rc;
     }
+    if (p.KS > 1) return launch_splitk_reduce(part, p.KS, (long)M * N, y, stream);
     return 0;
 }
 
@@ -183,7 +188,9 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     int rc = launch_prep_tiles(c.x, c.u, c.h_out, c.xq, c.xd, c.xs, c.M, c.K, log2i(p.geo.XGT), ximg, nullptr,
                                nullptr, nullptr, c.stream);
     if (rc) return rc;
-    if (p.pair) return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y, c.stream);
+    if (p.pair)
+        return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y,
+                                  p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : nullptr, c.stream);
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
@@ -229,9 +236,9 @@ int ffn_run(const FfnCall &c, int sms) {
     if (rc) return rc;
     if (p.gate.pair) {
         // several tokens: gate and up as two row-pair launches on the same tile image
-        rc = gemv_pair_run<FMT>(p.gate, c.Wg, c.I, c.M, ximg, p.ximg_pitch, g, c.stream);
+        rc = gemv_pair_run<FMT>(p.gate, c.Wg, c.I, c.M, ximg, p.ximg_pitch, g, nullptr, c.stream);
         if (rc) return rc;
-        rc = gemv_pair_run<FMT>(p.gate, c.Wu, c.I, c.M, ximg, p.ximg_pitch, u, c.stream);
+        rc = gemv_pair_run<FMT>(p.gate, c.Wu, c.I, c.M, ximg, p.ximg_pitch, u, nullptr, c.stream);
         if (rc) return rc;
     }
     for (int ch = 0; ch < (p.gate.pair ? 0 : p.nchunk); ++ch) {

@@ -171,13 +171,14 @@ inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_b
     return r;
 }
 
-// Ring of a row-pair launch: stages of 32 two-row tasks, at most PAIR_RUNS runs each.
-inline Ring plan_ring_pair(const TaskGeo &g, uint32_t x_bytes, int ncw) {
+// Ring of a row-pair launch: stages of 32 two-row tasks, at most PAIR_RUNS runs each (whole
+// rows) or PAIR_RUNS_SPLIT (K-slices).
+inline Ring plan_ring_pair(const TaskGeo &g, uint32_t x_bytes, int ncw, bool split = false) {
     Ring r;
     r.x_bytes = (uint32_t)align_up(x_bytes, 16);
     const long avail = (long)SMEM_MAX - (long)pair_fixed_smem(ncw * DMAX, ncw) - (long)r.x_bytes;
-    const uint32_t slot =
-        (uint32_t)align_up(2u * g.bytes_of(32) + (g.aligned16() ? 0u : 32u * PAIR_RUNS), 16);
+    const uint32_t slot = (uint32_t)align_up(
+        2u * g.bytes_of(32) + (g.aligned16() ? 0u : 32u * (split ? PAIR_RUNS_SPLIT : PAIR_RUNS)), 16);
     const long d = avail / ((long)ncw * (slot + STAGE_SLACK));
     if (d < 1) return r;
     r.tps = 32;
@@ -229,21 +230,31 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
         // out of registers, so they take at most 8 tokens per launch (two launches of 8
         // measured faster than one one-row launch of 16)
         int mc = (fmt == 13 || fmt == 14) ? std::min(M, 8) : M;
-        while (mc > 2 && (long)mc * pg.tpr * pg.stride > (long)XCAP) mc = pick_mt(mc) / 2;
-        const long px = (long)mc * pg.tpr * pg.stride;
+        // tiles of mc tokens over a 1/ks slice of the row; slices keep at least
+        // PAIR_SPLIT_MIN_TPR tasks and every slice group at least 16 CTAs
+        auto slice_x = [&](int m, int ks) { return (long)m * ((pg.gpr + ks - 1) / ks) * pg.stride; };
+        auto ks_ok = [&](int ks) { return ks == 1 || (pg.gpr / ks >= PAIR_SPLIT_MIN_TPR && sms / ks >= 16); };
+        int ks = 1;
+        while (pg.ok && mc >= 2) {
+            ks = 1;
+            while (slice_x(mc, ks) > (long)XCAP && ks_ok(ks + 1)) ++ks;
+            if (slice_x(mc, ks) <= (long)XCAP) break;
+            mc = pick_mt(mc) / 2;  // tokens in chunks instead
+        }
         const int mt = pick_mt(mc) < 2 ? 2 : pick_mt(mc);
-        if (pg.ok && px <= (long)XCAP) {
-            const int P = (N + 1) / 2, pgroups = std::min(P, sms);
+        if (pg.ok && mc >= 1 && slice_x(mc, ks) <= (long)XCAP) {
+            const int P = (N + 1) / 2, pgroups = std::min(P, sms / ks);
             const int pncw = 8;  // two-row tasks of 288 to 420 bytes and two or more tokens per lane
-            const Ring pr = plan_ring_pair(pg, (uint32_t)px, pncw);
+            const Ring pr = plan_ring_pair(pg, (uint32_t)slice_x(mc, ks), pncw, ks > 1);
             if (pr.ok) {
                 p.pair = true;
                 p.geo = pg;
-                p.KS = 1;
+                p.KS = ks;
                 p.MT = mt;
                 p.MC = mc;
-                p.groups = p.grid = pgroups;
-                p.tpr_x = pg.tpr;
+                p.groups = pgroups;
+                p.grid = pgroups * ks;
+                p.tpr_x = (pg.gpr + ks - 1) / ks;
                 p.ncw = pncw;
                 p.ring = pr;
             }
@@ -290,6 +301,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     p.down = plan_gemv(fmt, H, I, M, sms);
     if (!p.down.ok) return p;
     if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
+    if (p.gate.pair && p.gate.KS > 1) p.gate.pair = false;  // its partial sums have no workspace here
     size_t o = 0;
     p.ximg_pitch = (size_t)(p.gate.pair ? p.gate.ximg_pitch : tiles);
     p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);

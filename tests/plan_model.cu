@@ -67,14 +67,21 @@ void sim(const char *name, const TaskGeo &g, const Ring &r, int grid, int NCW, s
 }
 
 // mirrors engine_pair_kernel: runs per stage, slot use, and every lane's two task addresses
+// (whole rows: at most 3 runs that may span rows; K-slices: one run per row of each pair)
 void sim_pair(const char *name, const GemvPlan &p, int N) {
     const TaskGeo &g = p.geo;
     const Ring &r = p.ring;
     CHECK(r.ok, "%s pair ring", name);
-    const int P = (N + 1) / 2, tpr = p.tpr_x, NCW = p.ncw;
+    const int P = (N + 1) / 2, NCW = p.ncw, KS = p.KS, ngroups = p.grid / KS;
+    const bool split = KS > 1;
+    CHECK(p.grid % KS == 0, "%s grid %d not a multiple of KS %d", name, p.grid, KS);
     const long TB = g.task_bytes();
     for (int cta = 0; cta < p.grid; ++cta) {
-        const int p0 = (int)((long)P * cta / p.grid), p1 = (int)((long)P * (cta + 1) / p.grid);
+        const int grp = cta / KS, ks = cta % KS;
+        const int t0 = (int)((long)g.gpr * ks / KS), tpr = (int)((long)g.gpr * (ks + 1) / KS) - t0;
+        CHECK(tpr <= p.tpr_x, "%s slice of %d tasks past the tile area (%d)", name, tpr, p.tpr_x);
+        if (split) CHECK(tpr >= PAIR_SPLIT_MIN_TPR, "%s slice of %d tasks", name, tpr);
+        const int p0 = (int)((long)P * grp / ngroups), p1 = (int)((long)P * (grp + 1) / ngroups);
         const int ntask = (p1 - p0) * tpr;
         const int maxlen = (ntask + NCW - 1) / NCW, nchunk = (maxlen + r.tps - 1) / r.tps;
         for (int w = 0; w < NCW; ++w) {
@@ -84,33 +91,46 @@ void sim_pair(const char *name, const GemvPlan &p, int N) {
                 if (fa >= fb) continue;
                 const int pa = fa / tpr, ca = fa - pa * tpr, pb = (fb - 1) / tpr, cb = fb - 1 - pb * tpr;
                 const int ra = 2 * (p0 + pa), rz = 2 * (p0 + pb);
-                long runrow[3], runcol[3], runn[3];
-                bool valid[3];
-                for (int k = 0; k < 3; ++k) {
+                const int nruns = split ? PAIR_RUNS_SPLIT : PAIR_RUNS;
+                if (split) CHECK(pb - pa < PAIR_RUNS_SPLIT / 2, "%s stage over %d pairs", name, pb - pa + 1);
+                long runrow[PAIR_RUNS_SPLIT], runcol[PAIR_RUNS_SPLIT], runn[PAIR_RUNS_SPLIT];
+                bool valid[PAIR_RUNS_SPLIT];
+                for (int k = 0; k < nruns; ++k) {
                     int row = 0, col = 0, n = 0;
-                    if (k == 0) { row = ra; col = ca; n = pa == pb ? cb - ca + 1 : tpr - ca; }
+                    if (split) {
+                        const int pp = pa + k / 2;
+                        if (pp <= pb) { row = 2 * (p0 + pp) + (k & 1); col = pp == pa ? ca : 0; n = (pp == pb ? cb + 1 : tpr) - col; }
+                    } else if (k == 0) { row = ra; col = ca; n = pa == pb ? cb - ca + 1 : tpr - ca; }
                     else if (k == 1) { row = ra + 1; col = ca; n = pa == pb ? cb - ca + 1 : (tpr - ca) + (rz - ra - 2) * tpr + cb + 1; }
                     else if (pb > pa) { row = rz + 1; col = 0; n = cb + 1; }
                     valid[k] = n > 0 && row < N;
                     runrow[k] = row; runcol[k] = col; runn[k] = n;
-                    if (valid[k]) CHECK((long)row * tpr + col + n <= (long)N * tpr, "%s run past end", name);
+                    if (valid[k]) {
+                        if (split) CHECK(col + n <= tpr, "%s split run past its slice", name);
+                        else CHECK((long)row * tpr + col + n <= (long)N * tpr, "%s run past end", name);
+                    }
                 }
-                // slot offsets (aligned formats: no widening)
-                long off[3], tot = 0;
-                for (int k = 0; k < 3; ++k) {
+                // slot offsets (the real byte addresses: slices start at t0 within the row)
+                long off[PAIR_RUNS_SPLIT], tot = 0;
+                for (int k = 0; k < nruns; ++k) {
                     off[k] = tot;
                     if (valid[k]) {
-                        const long s0 = (long)runrow[k] * g.rb + runcol[k] * TB;
+                        const long s0 = (long)runrow[k] * g.rb + (t0 + runcol[k]) * TB;
                         const long e = s0 + runn[k] * TB;
+                        CHECK(e <= (long)N * g.rb, "%s run past the tensor", name);
                         tot += ((e + 15) & ~15L) - (s0 & ~15L);
                         off[k] += s0 & 15;
                     }
                 }
                 CHECK(tot <= (long)r.slot_bytes, "%s slot %ld > %u", name, tot, r.slot_bytes);
-                // every run's tasks in row-major order; find the slot address of (row, col)
+                // slot address of task (row, col): runs are row-major within the slice
                 auto where = [&](long row, long col) -> long {
-                    for (int k = 0; k < 3; ++k) {
+                    for (int k = 0; k < nruns; ++k) {
                         if (!valid[k]) continue;
+                        if (split) {
+                            if (row == runrow[k] && col >= runcol[k] && col < runcol[k] + runn[k]) return off[k] + (col - runcol[k]) * TB;
+                            continue;
+                        }
                         const long idx = (row * tpr + col) - (runrow[k] * tpr + runcol[k]);
                         if (idx >= 0 && idx < runn[k]) return off[k] + idx * TB;
                     }
@@ -121,12 +141,19 @@ void sim_pair(const char *name, const GemvPlan &p, int N) {
                     const int r0 = 2 * pp;  // CTA-relative
                     const long want0 = where(2L * (p0 + pp), c);
                     CHECK(want0 >= 0, "%s row0 not copied", name);
-                    const long got0 = pp == pa ? off[0] + (long)(c - ca) * TB : off[1] + (long)((r0 - 2 * pa - 1) * tpr + c - ca) * TB;
+                    long got0, got1;
+                    if (split) {
+                        const int k = std::min(2 * (pp - pa), PAIR_RUNS_SPLIT - 2);
+                        const long cofs = (long)(c - (pp == pa ? ca : 0)) * TB;
+                        got0 = off[k] + cofs;
+                        got1 = 2 * (p0 + pp) + 1 >= N ? got0 : off[k + 1] + cofs;
+                    } else {
+                        got0 = pp == pa ? off[0] + (long)(c - ca) * TB : off[1] + (long)((r0 - 2 * pa - 1) * tpr + c - ca) * TB;
+                        got1 = 2 * (p0 + pp) + 1 >= N ? got0
+                             : (pb > pa && pp == pb) ? off[2] + (long)c * TB : off[1] + (long)((r0 - 2 * pa) * tpr + c - ca) * TB;
+                    }
                     CHECK(got0 == want0, "%s addr0 %ld != %ld (f %d pa %d pb %d)", name, got0, want0, f, pa, pb);
-                    long got1;
-                    if (2 * (p0 + pp) + 1 >= N) got1 = got0;
-                    else {
-                        got1 = (pb > pa && pp == pb) ? off[2] + (long)c * TB : off[1] + (long)((r0 - 2 * pa) * tpr + c - ca) * TB;
+                    if (2 * (p0 + pp) + 1 < N) {
                         const long want1 = where(2L * (p0 + pp) + 1, c);
                         CHECK(want1 >= 0 && got1 == want1, "%s addr1 %ld != %ld", name, got1, want1);
                     }
@@ -157,8 +184,9 @@ int main() {
             snprintf(nm, sizeof nm, "pair f%d N%d K%d M%d", fmt, N, K, M);
             // token chunks: MC tokens per launch, their tiles within the launch's x area
             CHECK(p.MC >= 1 && p.MC <= M && p.MC <= p.MT && p.MT >= 2, "%s chunk %d of %d (MT %d)", nm, p.MC, M, p.MT);
-            CHECK((long)p.MC * g.tpr * g.stride <= (long)p.ring.x_bytes, "%s chunk tiles", nm);
-            CHECK(p.KS == 1, "%s pairs split", nm);
+
+            CHECK((long)p.MC * p.tpr_x * g.stride <= (long)p.ring.x_bytes, "%s slice tiles", nm);
+            if (p.KS > 1) CHECK(p.ws_part > 0 && p.ws_total >= p.ws_part + 4ull * p.KS * M * N, "%s partials", nm);
             sim_pair(nm, p, N);
             ++npair;
             continue;
