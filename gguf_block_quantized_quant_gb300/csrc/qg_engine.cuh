@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
     const uint32_t hdrs = xbar + 8u;
     auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
     auto hdr = [&](int s, int p) { return hdrs + 4u * (uint32_t)(s * (NPIECE_MAX + 1) + p); };
-    const uint32_t tok_stride = (uint32_t)(job.tpr_x * TL::STRIDE);
+    const uint32_t tok_stride = (uint32_t)((job.tpr_x + job.xrep) * TL::STRIDE);
     float *bsum = reinterpret_cast<float *>(smem + (bnd - ring));  // [NCW][2][BND_FLOATS]
     int *scratch = reinterpret_cast<int *>(smem + (scr - ring));
     float *jarea = reinterpret_cast<float *>(smem + (ja - ring));
@@ -243,6 +243,13 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
                 const uint32_t bytes = job.xrow_bytes(cx, r);
                 if (bytes) bulk_g2s(xa + (uint32_t)r * tok_stride, job.xrow_src(cx, r), bytes, xbar);
                 tx += bytes;
+                // the row's first job.xrep tiles again after it (the row holds tpr tiles)
+                for (int v = tpr; v < tpr + job.xrep; v += tpr) {
+                    const uint32_t rb2 = (uint32_t)(min(tpr, tpr + job.xrep - v) * TL::STRIDE);
+                    bulk_g2s(xa + (uint32_t)r * tok_stride + (uint32_t)(v * TL::STRIDE), job.xrow_src(cx, r), rb2,
+                             xbar);
+                    tx += rb2;
+                }
             }
             mbar_arrive_expect_tx(xbar, tx);
         }
@@ -284,7 +291,10 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
             const SAddr addr = smem + (lds32(hdr(slot, piece)) - ring) + task_off<F>(f - fp);
             F::load(addr, w);
             aoff = (uint32_t)((uintptr_t)addr & 3u);
-            xbase = smem + (xa - ring) + job.xrow(cx, o0 + o, grp_div) * tok_stride + (uint32_t)(tt * TL::STRIDE);
+            // with repeated tiles a lane reads virtual column (column of the stage's first
+            // task) + lane, past the row's end where the stage wraps
+            const int xc = job.xrep ? fa - (int)tpr_div.div((uint32_t)fa) * tpr + lane : tt;
+            xbase = smem + (xa - ring) + job.xrow(cx, o0 + o, grp_div) * tok_stride + (uint32_t)(xc * TL::STRIDE);
         }
         // the stage is in registers: refill the slot with stage j + D while decoding
         __syncwarp();

@@ -143,6 +143,7 @@ void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
     j.tpr_x = tpr_x;
     j.tps = r.tps;
     j.ntok = ntok;
+    j.xrep = 0;
 }
 
 }  // namespace
@@ -196,6 +197,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
         constexpr int T = decltype(Tc)::value;
         GemvJob<FMT, T> j;
         set_engine(j, p.ring, p.tpr_x, c.M);
+        j.xrep = p.xrep;
         j.W = c.W;
         j.Wend = c.W + (size_t)c.N * p.geo.rb;
         j.N = c.N;

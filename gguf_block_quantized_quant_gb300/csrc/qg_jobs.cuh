@@ -35,6 +35,7 @@ struct EngineFields {
     int depth;                          // ring slots per consumer warp
     uint32_t slot_bytes, x_bytes, j_bytes;
     int tpr_x, tps, ntok;
+    int xrep;  // activation tiles repeated past a row's end (virtual columns), 0 = none
 };
 
 // ===================================================================================== GEMV

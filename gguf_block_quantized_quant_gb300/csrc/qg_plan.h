@@ -40,6 +40,7 @@ constexpr int G_PLAN = 152;               // split-K planning constant
 constexpr uint32_t XCAP = 140 * 1024;     // activation tiles held by one CTA
 constexpr int DMAX = 4;                   // ring slots per consumer warp
 constexpr int M_MAX = 16;
+constexpr int XREP = 31;  // repeated activation tiles past a row's end (a stage's 32 lanes)
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int pick_mt(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -197,6 +198,7 @@ struct GemvPlan {
     int KS = 1, groups = 1, grid = 1, MT = 1, tpr_x = 0, ncw = 8;
     bool pair = false;  // row-pair engine: tasks of two rows (engine_pair_kernel)
     int MC = 0;         // row pairs: tokens per launch (launches over token chunks of MC)
+    int xrep = 0;       // one-row engine: activation tiles repeated past a row's end
     Ring ring;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
@@ -217,7 +219,13 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     p.tpr_x = (g.gpr + p.KS - 1) / p.KS * g.TPB;
     // split-K: every row is its own run; the shortest slice has floor(gpr / KS) groups
     p.ncw = plan_ncw(g, p.MT, (long)((N + p.groups - 1) / p.groups) * p.tpr_x);
-    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB, (uint32_t)xbytes(p.KS), 0, p.ncw);
+    // one token: every row's tiles are followed by copies of its first XREP tiles, so that
+    // the 32 lanes of a stage read consecutive tiles even where the stage wraps to the next
+    // row (no bank conflicts between a row's last tiles and the next row's first)
+    const long xrep_bytes = (long)M * (p.tpr_x + XREP) * g.stride;
+    p.xrep = (p.MT == 1 && xrep_bytes <= (long)XCAP) ? XREP : 0;
+    p.ring = plan_ring(g, p.KS == 1 ? 0 : (long)(g.gpr / p.KS) * g.TPB,
+                       (uint32_t)((long)M * (p.tpr_x + p.xrep) * g.stride), 0, p.ncw);
     if (!p.ring.ok) return p;
     // row pairs: a GEMV of whole rows (not split for lack of rows) with at least two rows
     // and two tokens (with one token the one-row tasks measured faster).  When the tiles of

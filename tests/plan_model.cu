@@ -192,7 +192,9 @@ int main() {
             continue;
         }
         snprintf(nm, sizeof nm, "gemv f%d N%d K%d M%d KS%d", fmt, N, K, M, p.KS);
-        CHECK(p.ring.x_bytes >= (uint32_t)(M * p.tpr_x * g.stride), "%s x bytes", nm);
+        CHECK(p.ring.x_bytes >= (uint32_t)(M * (p.tpr_x + p.xrep) * g.stride), "%s x bytes", nm);
+        // repeated tiles: a stage's last lane reads virtual column (tpr - 1) + 31 at most
+        CHECK(p.xrep == 0 || (p.xrep >= 31 && M == 1), "%s xrep %d", nm, p.xrep);
         const int KS = p.KS, groups = p.groups, gpr = g.gpr, TPB = g.TPB;
         sim(nm, g, p.ring, p.grid, p.ncw,
             [&](int b) { const int gg = b / KS, ks = b % KS; Cta c; c.o0 = (int)((long)gg * N / groups);
