@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
     job.init(jarea, tid);
     if constexpr (Job::HAS_PROLOGUE) {
         __syncthreads();
-        if (warp == 0) job.prologue(lane, scratch);
+        job.prologue(warp, NCW, lane, scratch);
     }
     __syncthreads();
     if constexpr (Job::HAS_PROLOGUE)

@@ -5,7 +5,7 @@
 //                  partial sums to a buffer)
 //   FfnGateUpJob   output rows 0..I-1 = rows of Wg (g), I..2I-1 = rows of Wu (u)
 //   MoeGateUpJob   output rows of g and u for every (token, slot): the slot's routed expert
-//                  (from the router's top-k, computed by warp 0 in the prologue) or the shared one;
+//                  (from the router's top-k, computed in the prologue) or the shared one;
 //                  each CTA owns whole 32-blocks of positions and its epilogue requantizes
 //                  h = silu(g) * u into the down projection's activation tiles
 //   MoeDownJob     per CTA, a range of hidden rows n: output rows (token, slot, n) of every
@@ -16,7 +16,7 @@
 // Engine interface: HAS_FINISH, HAS_PROLOGUE; fields depth, slot_bytes, x_bytes, j_bytes,
 // tpr_x, tps, ntok; Ctx ctx() (per-CTA constants, computed once and passed to the calls
 // below); cta(o0, o1, tpr, grp), seg_src, xrows/xrow_src/xrow_bytes, xrow, store, init,
-// finish, prologue (run by warp 0 before any weight copy, e.g. the MoE top-k).
+// finish, prologue (run by every warp before any weight copy, e.g. the MoE top-k).
 // The engine may start before the previous kernel in the stream has finished (programmatic
 // dependent launch): seg_src may only read data no earlier kernel writes (the weights),
 // unless the job's prologue first waits for the previous kernel (griddep_wait).
@@ -86,7 +86,7 @@ struct GemvJob : EngineFields {
     __device__ void store(const Ctx &c, int o, int m, float v, float *) const { c.out[(long)m * N + o] = v; }
     __device__ void init(float *, int) const {}
     __device__ void finish(const Ctx &, float *, int, int) const {}
-    __device__ void prologue(int, int *) const {}
+    __device__ void prologue(int, int, int, int *) const {}
 };
 
 // ===================================================================================== FFN gate/up
@@ -126,7 +126,7 @@ struct FfnGateUpJob : EngineFields {
     }
     __device__ void init(float *, int) const {}
     __device__ void finish(const Ctx &, float *, int, int) const {}
-    __device__ void prologue(int, int *) const {}
+    __device__ void prologue(int, int, int, int *) const {}
 };
 
 // ===================================================================================== MoE gate/up
@@ -252,19 +252,20 @@ struct MoeGateUpJob : EngineFields {
             }
         }
     }
-    // Router tail, warp 0, after the logits kernel has finished: softmax over E logits,
-    // the topk largest (ties: lower id), weights renormalized over the picks.
+    // Router tail, after the logits kernel has finished: softmax over E logits, the topk
+    // largest (ties: lower id), weights renormalized over the picks; one warp per token.
     // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax
-    // probabilities p.
-    __device__ void prologue(int lane, int *ids) const {
+    // probabilities p.  A round of the selection is two warp reductions: the largest logit
+    // (as an order-preserving integer key), then the lowest expert id holding it.
+    __device__ void prologue(int warp, int nwarps, int lane, int *ids) const {
         griddep_wait();
-        for (int m = 0; m < M; ++m) {
+        for (int m = warp; m < M; m += nwarps) {
             float v[E_MAX / 32];
             float lmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < E_MAX / 32; ++i) {
                 const int e = lane + 32 * i;
-                v[i] = e < E ? logits[(long)m * E + e] : -INFINITY;
+                v[i] = e < E ? logits[(long)m * E + e] + 0.0f : -INFINITY;  // + 0: -0 as +0
                 lmax = fmaxf(lmax, v[i]);
             }
 #pragma unroll
@@ -274,6 +275,7 @@ struct MoeGateUpJob : EngineFields {
             int my_sel = 0;
             float my_ev = 0.0f;
             for (int r = 0; r < topk; ++r) {
+                // this lane's largest remaining logit (its lowest id on ties)
                 float bv = -INFINITY;
                 int be = 0x7fffffff;
 #pragma unroll
@@ -284,15 +286,11 @@ struct MoeGateUpJob : EngineFields {
                         be = e;
                     }
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
+                const int bits = __float_as_int(bv);
+                const int key = be == 0x7fffffff ? (int)0x80000000 : (bits >= 0 ? bits : bits ^ 0x7fffffff);
+                const int kmax = __reduce_max_sync(0xffffffffu, key);
+                be = __reduce_min_sync(0xffffffffu, key == kmax ? be : 0x7fffffff);
+                bv = __int_as_float(kmax >= 0 ? kmax : kmax ^ 0x7fffffff);
                 if ((be & 31) == lane) taken |= 1u << (be >> 5);
                 const float ev = expf(bv - lmax);
                 esum += ev;
@@ -391,7 +389,7 @@ struct MoeDownJob : EngineFields {
     }
     // The weight copies need the routed expert ids, written two kernels earlier: wait for
     // the previous kernel (and so for everything before it) before any copy is issued.
-    __device__ void prologue(int, int *) const { griddep_wait(); }
+    __device__ void prologue(int, int, int, int *) const { griddep_wait(); }
 };
 
 }  // namespace qg
