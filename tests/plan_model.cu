@@ -261,6 +261,26 @@ int main() {
         }
       }
     }
+    // the launch shapes chosen for the decode FFN of hidden 5120 / inter 17408 (measured
+    // choices; a change here changes the timings the documentation reports)
+    {
+        const GemvPlan a = plan_gemv(12, 17408, 5120, 1, sms), b = plan_gemv(12, 5120, 17408, 1, sms);
+        CHECK(!a.pair && a.KS == 1 && a.ncw == 12 && a.xrep == XREP && a.geo.T == 2, "Q4_K 17408x5120 M1 plan");
+        CHECK(!b.pair && b.KS == 1 && b.ncw == 12 && b.xrep == XREP, "Q4_K 5120x17408 M1 plan");
+        const GemvPlan c = plan_gemv(2, 17408, 5120, 1, sms);
+        CHECK(!c.pair && c.geo.T == 16 && c.xrep == XREP, "Q4_0 17408x5120 M1 plan");
+        const GemvPlan d = plan_gemv(12, 17408, 5120, 4, sms);
+        CHECK(d.pair && d.KS == 1 && d.MT == 4 && d.MC == 4, "Q4_K 17408x5120 M4 plan");
+        const GemvPlan e = plan_gemv(12, 5120, 17408, 16, sms), f = plan_gemv(12, 5120, 17408, 8, sms);
+        CHECK(e.pair && e.KS == 4 && e.MT == 16 && e.MC == 16 && e.grid == 152, "Q4_K 5120x17408 M16 plan: K-sliced pairs");
+        CHECK(f.pair && f.KS == 2 && f.MT == 8, "Q4_K 5120x17408 M8 plan");
+        const GemvPlan g6 = plan_gemv(14, 17408, 5120, 16, sms);
+        CHECK(g6.pair && g6.MT == 8 && g6.MC == 8, "Q6_K 17408x5120 M16 plan: two launches of 8");
+        const FfnPlan h = plan_ffn(12, 16, 5120, 17408, sms);
+        CHECK(h.ok && h.gate.pair && h.gate.KS == 1 && h.down.pair && h.down.KS == 4, "FFN Q4_K M16 plan");
+        const MoePlan m1 = plan_moe(12, 1, 2048, 256, 8, 512, sms), m2 = plan_moe(12, 1, 2048, 256, 8, 512, sms, true);
+        CHECK(m1.ok && m1.P == 1 && m1.gu_grid == 144 && m2.ok && m2.P == 2, "MoE plans");
+    }
     printf("fails %d\n", fails);
     return fails != 0;
 }
