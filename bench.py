@@ -22,7 +22,8 @@ bandwidth.
   * N > 1 (torchrun): replicas only -- every rank runs the whole workload on its own GPU;
     the value is the weight bytes of all ranks over the slowest rank's time;
   * --one FMT:NxK:M (e.g. Q4_K:17408x5120:1): three untimed GEMV calls of one shape on
-    seeded synthetic input and nothing else -- the small case a profiler captures.
+    seeded synthetic input and nothing else -- the small case a profiler captures;
+    --one-moe M does the same for the MoE FFN of M tokens.
 """
 from __future__ import annotations
 
@@ -580,6 +581,30 @@ def run_one(spec: str):
     return 0
 
 
+def run_one_moe(m: int):
+    """Three qg_moe_ffn calls (Q4_K experts, H=2048, 256 routed + 1 shared, I=512, top-8) of
+    m tokens, for a profiler to capture."""
+    import torch
+
+    import gguf_block_quantized_quant_gb300 as qg
+
+    H, E, I, topk, fq = 2048, 256, 512, 8, synth.Q4_K
+    g = synth.rng(4, 0)
+    Wr = torch.from_numpy(synth.router_weights(E, H, g)).cuda()
+    Wg = torch.from_numpy(synth.stacked_experts(fq, E, I, H, g)).cuda()
+    Wu = torch.from_numpy(synth.stacked_experts(fq, E, I, H, g)).cuda()
+    Wd = torch.from_numpy(synth.stacked_experts(fq, E, H, I, g)).cuda()
+    sg = torch.from_numpy(synth.weights(fq, I, H, g)).cuda()
+    su = torch.from_numpy(synth.weights(fq, I, H, g)).cuda()
+    sd = torch.from_numpy(synth.weights(fq, H, I, g)).cuda()
+    x = torch.from_numpy(synth.activations(m, H, g)).cuda()
+    for _ in range(3):
+        y = qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, sg, su, sd, I)
+    torch.cuda.synchronize()
+    print(json.dumps({"one_moe": m, "y_abs_sum": float(y.abs().sum())}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -590,9 +615,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--one", metavar="FMT:NxK:M", help="three untimed GEMV calls of one shape, then exit")
+    ap.add_argument("--one-moe", type=int, metavar="M", help="three untimed MoE FFN calls of M tokens, then exit")
     args = ap.parse_args(argv)
     if args.one:
         return run_one(args.one)
+    if args.one_moe:
+        return run_one_moe(args.one_moe)
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps")
     if args.impl == "reference":
