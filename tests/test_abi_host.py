@@ -120,3 +120,18 @@ def test_workspace_sizes(L):
     ffn = qg.qg_workspace_size(qg.QG_OP_FFN_SUBLAYER, 14, 16, 5120, 5120, 0, 0, 17408)
     assert ffn != bad and ffn >= 3 * 4 * 16 * 17408
     assert qg.qg_ffn_ws_layout(14, 16, 5120, 17408)[2] < ffn
+
+
+def test_binding_takes_device_or_page_locked_tensors_only():
+    """Activations may be page-locked host tensors (the kernels address them directly);
+    plain pageable host tensors, and host tensors for weights or workspaces, are refused
+    before any call reaches the library."""
+    import torch
+
+    import gguf_block_quantized_quant_gb300 as qg
+    t = torch.zeros(16, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        qg._ptr(t)                 # pageable host memory
+    with pytest.raises(ValueError):
+        qg._ptr(t, False)          # weights / workspace must be device memory
+    assert qg._ptr(None) is None
