@@ -149,7 +149,11 @@ int qg_gemv_static_ws(int fmt, const void *W_blocks, const float *x, float *y, i
  *   x: M x H fp32.  Wr: E x H fp32.  Wg_exps, Wu_exps: E stacked I x H matrices;
  *   Wd_exps: E stacked H x I matrices.  Wg_sh, Wu_sh: I x H; Wd_sh: H x I.
  *   y: M x H fp32.  topk_ids (int32) / topk_w (fp32): M x topk, may be NULL.
- *   Limits: 1 <= topk <= 16, topk <= E <= 1024, H and I multiples of the block size.
+ *   Limits: 1 <= topk <= 16, topk <= E <= 1024, H and I multiples of the block size, and
+ *   the activation tiles of all M tokens over H within one CTA's 140 KB tile area (about
+ *   1.5 bytes per element and token: every M up to 16 for H <= 4096; M <= 13 for H = 7168
+ *   with Q4_K); QG_EINVAL otherwise, before any launch (qg_workspace_size returns
+ *   (size_t)-1 for such a shape).
  * The intermediates stay in ws; qg_moe_ws_layout() gives their offsets. */
 int qg_moe_ffn(int fmt, const float *x, int M, int H,
                const float *Wr, int E, int topk,
@@ -160,7 +164,8 @@ int qg_moe_ffn(int fmt, const float *x, int M, int H,
 
 /* The MoE FFN with s16 activations [KES section 四, issue ⑫]: as qg_moe_ffn, with x and
  * the requantized h quantized by the qg_quantize_act_s16 rule instead of the int8 one (the
- * router still reads fp32 x).  Arguments, layouts, limits and errors as qg_moe_ffn; the
+ * router still reads fp32 x).  Arguments, layouts, limits and errors as qg_moe_ffn (the
+ * tile-area limit counts two planes per token: every M up to 16 for H <= 2048); the
  * workspace is qg_workspace_size(QG_OP_MOE_FFN_S16, ...) and its intermediates are at
  * qg_moe_s16_ws_layout().  On the GPU an s16 code q is held as two int8 planes,
  * q = 256 * hi + lo, whose exact integer dots are combined in fp32: twice the dot work
