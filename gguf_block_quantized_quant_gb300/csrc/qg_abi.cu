@@ -5,6 +5,8 @@
 // whose device call reports one status (0 = done on the GPU).  The page's host-side
 // mapping of a failure to "the caller runs the CPU path" is deliberately not reproduced:
 // a failure is returned as a negative status and nothing runs elsewhere.
+#include <cuda.h>
+
 #include <mutex>
 #include <set>
 #include <utility>
@@ -295,26 +297,70 @@ bool shape_ok(int fmt, int K) {
 // Fixed scratch of qg_gemv_static_ws: one array per device, shared by every call.
 static __device__ __align__(256) uint8_t g_qg_static_ws[QG_STATIC_WS_BYTES];
 
+// The array's address belongs to the context that loaded the module: after a device reset
+// (or a host framework that releases and re-creates the primary context) the old address
+// is dangling.  The cache is therefore keyed on the current context's unique id, read
+// through the driver entry points cuCtxGetCurrent / cuCtxGetId (the runtime API has no
+// context id).
+typedef CUresult (*PFN_ctx_get_current)(CUcontext *);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long *);
+
 struct StaticWsCache {
     std::mutex mu;
+    bool fns_tried = false;
+    PFN_ctx_get_current get_current = nullptr;
+    PFN_ctx_get_id get_id = nullptr;
     void *addr[64] = {};
+    unsigned long long ctx_id[64] = {};
 };
 StaticWsCache g_static_ws;
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Unique id of the current context, or false if it cannot be read.
+bool current_ctx_id(unsigned long long &id) {
+    if (!g_static_ws.fns_tried) {
+        g_static_ws.fns_tried = true;
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+                cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+            g_static_ws.get_current = reinterpret_cast<PFN_ctx_get_current>(f1);
+            g_static_ws.get_id = reinterpret_cast<PFN_ctx_get_id>(f2);
+        }
+        cudaGetLastError();
+    }
+    if (!g_static_ws.get_current || !g_static_ws.get_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_static_ws.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_static_ws.get_id(ctx, &id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context: looked up (cudaGetSymbolAddress)
+// on the first call in each context of each device, and again whenever the current context
+// of that device has changed since.  Where the context id cannot be read, the address is
+// looked up on every call.
 void *static_ws_addr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(g_static_ws.mu);
-    if (!g_static_ws.addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_qg_static_ws) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        g_static_ws.addr[dev] = p;
+    unsigned long long id = 0;
+    // before the runtime's first use of the device no context is current yet: the lookup
+    // below binds the device's primary context, and its id is read after it
+    const bool known = current_ctx_id(id);
+    if (known && g_static_ws.addr[dev] && g_static_ws.ctx_id[dev] == id) return g_static_ws.addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qg_static_ws) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
     }
-    return g_static_ws.addr[dev];
+    if (current_ctx_id(id)) {
+        g_static_ws.addr[dev] = p;
+        g_static_ws.ctx_id[dev] = id;
+    } else {
+        g_static_ws.addr[dev] = nullptr;
+    }
+    return p;
 }
 
 }  // namespace

@@ -32,8 +32,9 @@
  *    CPU fallback: a GPU problem is reported, never silently computed elsewhere.
  *  - Layouts: x is M x K fp32 row-major; y is M x N fp32 row-major.  A weight matrix
  *    W with N rows and K columns is N rows of K/QK blocks each, rows contiguous, no
- *    padding, raw GGUF byte order (QK = 32 for Q4_0/Q8_0, 256 for the others).  Expert
- *    tensors are E such matrices stacked contiguously.
+ *    padding, raw GGUF byte order.  QK = 32 elements for Q4_0, Q4_1, Q5_0, Q5_1, Q8_0
+ *    and IQ4_NL; QK = 256 for Q2_K, Q3_K, Q4_K, Q5_K, Q6_K and IQ4_XS.  Expert tensors
+ *    are E such matrices stacked contiguously.
  *  - Alignment: W and ws must be 16-byte aligned (QG_EALIGN otherwise); x, y and the
  *    quantized-activation arrays must be 4-byte aligned.
  *  - Limits: 1 <= M <= 16 tokens; K a positive multiple of the block size; N >= 1.
@@ -100,10 +101,17 @@ int qg_quantize_act_s16(const float *x, int M, int K, int16_t *xq, float *xd, in
 
 /* y = W x for M tokens [D27 Q&A; KES section 一]: x is quantized on the GPU as by
  * qg_quantize_act (once per call, into per-task activation tiles in ws), then each
- * 32-element unit contributes
- *   Q8_0, Q4_0, Q6_K, IQ4_XS:  y += d_unit * xd * dot
+ * 32-element unit u (activation step xd, code sum xs) contributes
+ *   Q8_0, Q4_0, Q5_0, IQ4_NL:  y += d * xd * dot
+ *   Q6_K, Q3_K:                y += d * xd * dot   (the 16-element sub-scales are in dot)
+ *   IQ4_XS:                    y += d*(ls_u - 32) * xd * dot
+ *   Q4_1, Q5_1:                y += xd * (d * dot + m * xs)
  *   Q4_K, Q5_K:                y += xd * (d*S_j * dot - dmin*M_j * xs)
- * where dot is the exact int32 sum of weight codes times activation codes.
+ *   Q2_K:                      y += xd * (d * dot - dmin * mins)
+ * where dot is the exact int32 sum of weight codes times activation codes, with the
+ * codes of qg_block_dots below (its offsets included: nibble-8, code-16, code-32, the
+ * codebook value), and mins is the exact sum of each 16-element sub-block's 4-bit min
+ * times its activation codes.
  *   fmt: qg_format.  W: N x K blocks.  x: M x K fp32.  y: M x N fp32 (overwritten). */
 int qg_gemv(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
             void *ws, size_t ws_bytes, void *stream);
@@ -133,9 +141,11 @@ int qg_gemv_q(int fmt, const void *W_blocks, const int8_t *xq, const float *xd, 
  *   Races: every call on a device shares the one array.  Calls whose executions may
  *   overlap on the GPU (different streams without ordering, or several host threads)
  *   corrupt each other's activations; order them on one stream.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call before any
- *   stream capture. */
+ *   Set-up: the first call in each CUDA context of a device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current); make that first call before
+ *   any stream capture.  The address is cached per device together with the context's id
+ *   and looked up again when the device's context has changed (after cudaDeviceReset, or
+ *   when a host framework re-creates the primary context). */
 int qg_gemv_static_ws(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
                       void *stream);
 
