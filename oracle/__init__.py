@@ -78,6 +78,11 @@ def _configure(L):
     L.or_requant16.argtypes = [P, i, i, P, P, P]
     L.or_moe_down16.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
     L.or_moe_ffn16.argtypes = [i, P, i, i, P, i, i, P, P, P, P, P, P, i, P, P, P]
+    L.or_float_to_half.argtypes = [ctypes.c_float]
+    L.or_float_to_half.restype = ctypes.c_uint16
+    L.or_float_to_half_array.argtypes = [P, ctypes.c_size_t, P]
+    L.or_dequant_f16.argtypes = [i, P, i, i, P]
+    L.or_prefill_gemm.argtypes = [i, P, P, i, i, i, P, P]
     L.or_set_threads.argtypes = [i]
     L.or_get_threads.restype = i
     return L
@@ -411,3 +416,31 @@ def moe_ffn16(fmt, x, Wr, topk, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_sh, Wd_sh, 
                        _p(_u8(Wd_exps)), _p(_u8(Wg_sh)), _p(_u8(Wu_sh)), _p(_u8(Wd_sh)), I,
                        _p(y), _p(ids), _p(w))
     return y, ids, w
+
+
+# ----------------------------------------------------------------------------- prefill (fp16 operands)
+def float_to_half(x):
+    """fp32 -> fp16 bit patterns (uint16), round to nearest, ties to even."""
+    x = _f32(x)
+    out = np.zeros(x.shape, np.uint16)
+    lib().or_float_to_half_array(_p(x), x.size, _p(out))
+    return out
+
+
+def dequant_f16(fmt, W, N, K):
+    """The fp16 weights (bit patterns, N x K uint16) of the prefill reading."""
+    W = _u8(W)
+    out = np.zeros((N, K), np.uint16)
+    lib().or_dequant_f16(fmt, _p(W), N, K, _p(out))
+    return out
+
+
+def prefill_gemm(fmt, W, x, N, K):
+    """y[m][n] = sum_k w16[n][k] * x16[m][k] in fp64; returns (y, sabs), both M x N."""
+    x = _f32(x)
+    M = x.shape[0]
+    assert x.shape[1] == K
+    y = np.zeros((M, N), np.float64)
+    sabs = np.zeros((M, N), np.float64)
+    lib().or_prefill_gemm(fmt, _p(_u8(W)), _p(x), N, K, M, _p(y), _p(sabs))
+    return y, sabs

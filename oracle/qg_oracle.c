@@ -649,3 +649,90 @@ void or_ffn_sublayer(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint8_
     if (h) memcpy(h, hh, sizeof(double) * (size_t)M * I);
     free(gg); free(uu); free(hh); free(xq); free(xd); free(xs); free(hq); free(hd); free(hs);
 }
+
+/* ------------------------------------------------------------------------------------
+ * Prefill GEMM on fp16 operands (readings in qg_oracle.h). */
+
+/* From the definition of binary16: a finite nonzero value is r * 2^(e-10) with e the
+ * exponent (clamped below at -14, where the spacing stops shrinking: gradual underflow)
+ * and r an integer; r in [1024, 2048) is a normal number (exponent field e + 15,
+ * fraction r - 1024), r < 1024 a subnormal one (exponent field 0, fraction r).  The
+ * magnitude is scaled to units of 2^(e-10) exactly (a power-of-two scaling in fp64) and
+ * rounded to the nearest integer, ties to the even one. */
+uint16_t or_float_to_half(float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof(bits));
+    uint16_t sign = (uint16_t)((bits >> 31) << 15);
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00u);
+    double a = fabs((double)f);
+    if (isinf(f)) return (uint16_t)(sign | 0x7c00u);
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);          /* a = m * 2^E with m in [0.5, 1): a in [2^(E-1), 2^E) */
+    int e = E - 1;
+    if (e < -14) e = -14;
+    double scaled = ldexp(a, 10 - e);
+    double r = floor(scaled);
+    double frac = scaled - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) == 1.0)) r += 1.0;
+    if (r >= 2048.0) {     /* rounding carried into the next binade */
+        r = 1024.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7c00u);  /* beyond 65504: infinity */
+    if (r < 1024.0) return (uint16_t)(sign | (uint16_t)r);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(r - 1024.0));
+}
+
+void or_float_to_half_array(const float *x, size_t n, uint16_t *out) {
+    for (size_t i = 0; i < n; ++i) out[i] = or_float_to_half(x[i]);
+}
+
+/* The fp16 weights of one row (K elements) by the reading: w32 = A*c - B*mc in fp32. */
+static void dequant_row_f16(int fmt, const uint8_t *row, int K, uint16_t *out) {
+    int QK = or_block_elems(fmt), BS = or_block_bytes(fmt);
+    int32_t c[256], mc[256];
+    double A[8], B[8];
+    for (int b = 0; b < K / QK; ++b) {
+        or_decode_block_mc(fmt, row + (size_t)b * BS, NULL, c, mc, A, B);
+        for (int e = 0; e < QK; ++e) {
+            float a32 = (float)A[e / 32], b32 = (float)B[e / 32];
+            float p1 = a32 * (float)c[e];
+            float p2 = b32 * (float)mc[e];
+            float w32 = p1 - p2;
+            out[(size_t)b * QK + e] = or_float_to_half(w32);
+        }
+    }
+}
+
+void or_dequant_f16(int fmt, const uint8_t *W, int N, int K, uint16_t *out) {
+    size_t rb = (size_t)(K / or_block_elems(fmt)) * or_block_bytes(fmt);
+    for (int n = 0; n < N; ++n) dequant_row_f16(fmt, W + (size_t)n * rb, K, out + (size_t)n * K);
+}
+
+void or_prefill_gemm(int fmt, const uint8_t *W, const float *x, int N, int K, int M, double *y, double *sabs) {
+    size_t rb = (size_t)(K / or_block_elems(fmt)) * or_block_bytes(fmt);
+    double *x16 = (double *)malloc(sizeof(double) * (size_t)M * K);
+    for (size_t i = 0; i < (size_t)M * K; ++i) x16[i] = or_half_to_double(or_float_to_half(x[i]));
+#pragma omp parallel for schedule(dynamic, 4) num_threads(or_get_threads())
+    for (int n = 0; n < N; ++n) {
+        uint16_t *w16 = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)K);
+        double *wv = (double *)malloc(sizeof(double) * (size_t)K);
+        dequant_row_f16(fmt, W + (size_t)n * rb, K, w16);
+        for (int k = 0; k < K; ++k) wv[k] = or_half_to_double(w16[k]);
+        for (int m = 0; m < M; ++m) {
+            const double *xm = x16 + (size_t)m * K;
+            double acc = 0.0, aabs = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double p = wv[k] * xm[k];
+                acc += p;
+                aabs += fabs(p);
+            }
+            y[(size_t)m * N + n] = acc;
+            if (sabs) sabs[(size_t)m * N + n] = aabs;
+        }
+        free(w16);
+        free(wv);
+    }
+    free(x16);
+}

@@ -171,6 +171,32 @@ void or_ffn_sublayer(int fmt, const uint8_t *Wg, const uint8_t *Wu, const uint8_
                      const float *x, int M, int H, int I,
                      double *y, double *g, double *u, double *h);
 
+/* ---------------------------------------------------------------------------------
+ * Prefill GEMM on fp16 operands ([KES] section 九: the prefill matrix products moved to
+ * the tensor cores with the weights dequantized to fp16 inside the kernel, prefill of 512
+ * tokens 372 -> 902 tokens/s; section 四, issue ⑮: prefill takes float activations, not
+ * int8 ones, because int8 activations cost ten times the perplexity there).  Readings:
+ *  - each weight is formed in fp32 from its block, w32 = A_u * c_e - B_u * mc_e with the
+ *    factors of or_decode_block_mc (both products are exact in fp32 for every format
+ *    here; the subtraction rounds once), then rounded to the nearest fp16, ties to even;
+ *  - each activation is its fp32 value rounded to the nearest fp16, ties to even;
+ *  - y[m][n] = sum_k w16[n][k] * x16[m][k]; the oracle sums the exact products in fp64
+ *    (the GPU accumulates in fp32).
+ * Parity of these readings against the page's own kernel is unpinned: the page prints
+ * neither its rounding nor its dequantization order. */
+
+/* IEEE binary32 -> binary16, round to nearest, ties to even (overflow to infinity,
+ * gradual underflow, NaN kept as a quiet NaN).  Returns the binary16 bit pattern. */
+uint16_t or_float_to_half(float f);
+void or_float_to_half_array(const float *x, size_t n, uint16_t *out);
+
+/* fp16 weights of an N x K matrix (bit patterns, row-major), by the reading above. */
+void or_dequant_f16(int fmt, const uint8_t *W, int N, int K, uint16_t *out);
+
+/* y[m][n] = sum_k w16[n][k] * x16[m][k] in fp64 (x: M x K fp32; y: M x N).
+ * sabs (nullable): sum_k |w16 * x16|, the scale of the per-element tolerance. */
+void or_prefill_gemm(int fmt, const uint8_t *W, const float *x, int N, int K, int M, double *y, double *sabs);
+
 /* Threads used by the OpenMP loops over output rows (1 = single-threaded). */
 void or_set_threads(int n);
 int or_get_threads(void);

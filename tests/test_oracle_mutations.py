@@ -63,6 +63,16 @@ MUTATIONS = [
      "127.0f, q8, q16, xd, xs);"),
     ("moe s16 h requantized at the int8 step", "quantize_rows(hf, (int)R, I, bits == 8 ? 127.0f : 32512.0f,",
      "quantize_rows(hf, (int)R, I, 127.0f,"),
+    ("fp16 ties away from zero", "if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) == 1.0)) r += 1.0;",
+     "if (frac >= 0.5) r += 1.0;"),
+    ("fp16 no gradual underflow", "if (e < -14) e = -14;", "if (e < -15) e = -15;"),
+    ("fp16 overflow threshold", "if (e > 15) return (uint16_t)(sign | 0x7c00u);",
+     "if (e > 16) return (uint16_t)(sign | 0x7c00u);"),
+    ("prefill weight min term dropped", "float w32 = p1 - p2;", "float w32 = p1;"),
+    ("prefill activation not rounded to fp16", "x16[i] = or_half_to_double(or_float_to_half(x[i]));",
+     "x16[i] = (double)x[i];"),
+    ("prefill rows reversed", "dequant_row_f16(fmt, W + (size_t)n * rb, K, w16);",
+     "dequant_row_f16(fmt, W + (size_t)(N - 1 - n) * rb, K, w16);"),
 ]
 
 PIN_TESTS = [name for name in dir(pins) if name.startswith("test_")]

@@ -676,3 +676,75 @@ def test_moe16_stages_compose_and_beat_int8(orc):
     y_exact = _moe_exact(orc, fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I)
     y8 = orc.moe_ffn(fmt, x, Wr, k, Wg, Wu, Wd, sg, su, sd, I)[0]
     assert np.abs(y - y_exact).max() * 50 < np.abs(y8 - y_exact).max()
+
+
+# ----------------------------------------------------------------------------- prefill, fp16 operands
+def _f16_probe_values():
+    """fp32 inputs for the fp32 -> fp16 rounding: every finite fp16 value, every midpoint
+    between neighbouring finite fp16 values (exact ties in fp32), the fp32 neighbours of
+    those midpoints, the overflow boundary and values spread over 60 binades."""
+    h = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)  # +0 .. 65504
+    mids = (h[:-1] + h[1:]) / 2
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)                            # exact ties
+    up = np.nextafter(mids32, np.float32(np.inf))
+    down = np.nextafter(mids32, np.float32(0))
+    edge = np.array([65504, 65519.99, 65520, 65536, 1e6, 2.0 ** -24, 2.0 ** -25, 1.5 * 2.0 ** -25, 2.0 ** -26,
+                     2.0 ** -14, 2.0 ** -14 - 2.0 ** -25], np.float32)
+    g = np.random.default_rng(1616)
+    spread = (g.standard_normal(20000) * 2.0 ** g.integers(-40, 18, 20000)).astype(np.float32)
+    v = np.concatenate([h.astype(np.float32), mids32, up, down, edge, spread])
+    return np.concatenate([v, -v])
+
+
+def test_float_to_half_matches_numpy(orc):
+    x = _f16_probe_values()
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = orc.float_to_half(x)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first x={x[bad[0]]!r}: {got[bad[0]]:#06x} vs {ref[bad[0]]:#06x}"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequant_f16_is_rounded_fp32_weight(orc, fmt):
+    # every product A*c and B*mc is exact in fp32 and their fp64 difference is exact, so
+    # the reading's fp16 weight is numpy's fp64 -> fp32 -> fp16 rounding of the fp64 weight
+    qk = synth.BLOCK_ELEMS[fmt]
+    N, K = 7, 4 * qk
+    W = synth.weights(fmt, N, K, np.random.default_rng(900 + fmt))
+    w64 = orc.dequant_matrix(fmt, W, N, K)
+    ref = w64.astype(np.float32).astype(np.float16).view(np.uint16)
+    got = orc.dequant_f16(fmt, W, N, K)
+    np.testing.assert_array_equal(got, ref)
+    if fmt not in MIN_FMTS:  # one product only: w64 is exact in fp32, the fp16 rounding is direct
+        np.testing.assert_array_equal(got, w64.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_prefill_gemm_equals_fp64_matmul(orc, fmt):
+    qk = synth.BLOCK_ELEMS[fmt]
+    N, K, M = 9, 2 * max(qk, 128), 5
+    g = np.random.default_rng(300 + fmt)
+    W = synth.weights(fmt, N, K, g)
+    x = synth.activations(M, K, g) * np.float32(3.0)
+    w16 = orc.dequant_f16(fmt, W, N, K).view(np.float16).astype(np.float64)
+    x16 = x.astype(np.float16).astype(np.float64)
+    y, sabs = orc.prefill_gemm(fmt, W, x, N, K)
+    np.testing.assert_allclose(y, x16 @ w16.T, rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(sabs, np.abs(x16) @ np.abs(w16).T, rtol=1e-12, atol=1e-300)
+
+
+def test_prefill_q8_integer_closed_form(orc):
+    # Q8_0 with d = 1 (fp16 0x3c00): the fp16 weights are the int8 codes themselves, and
+    # integer activations below 2048 are exact in fp16, so y is the integer dot product
+    K, N, M = 64, 3, 2
+    g = np.random.default_rng(5)
+    codes = g.integers(-127, 128, (N, K)).astype(np.int8)
+    W = np.zeros((N, K // 32, 34), np.uint8)
+    W[:, :, 0], W[:, :, 1] = 0x00, 0x3c
+    W[:, :, 2:] = codes.reshape(N, K // 32, 32).view(np.uint8)
+    x = g.integers(-2047, 2048, (M, K)).astype(np.float32)
+    y, _ = orc.prefill_gemm(synth.Q8_0, W.reshape(N, -1), x, N, K)
+    want = x.astype(np.int64) @ codes.astype(np.int64).T
+    np.testing.assert_array_equal(y, want.astype(np.float64))
