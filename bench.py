@@ -23,7 +23,8 @@ bandwidth.
     the value is the weight bytes of all ranks over the slowest rank's time;
   * --one FMT:NxK:M (e.g. Q4_K:17408x5120:1): three untimed GEMV calls of one shape on
     seeded synthetic input and nothing else -- the small case a profiler captures;
-    --one-moe M does the same for the MoE FFN of M tokens.
+    --one-moe M does the same for the MoE FFN of M tokens, --one-prefill FMT:NxK:M for the
+    prefill GEMM on the tensor cores (qg_prefill_gemm).
 """
 from __future__ import annotations
 
@@ -98,6 +99,18 @@ def measured_peak():
         return v, "measured"
     except (OSError, KeyError, ValueError, TypeError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor-core peak (TFLOP/s) measured on this machine: burst (a kernel timed
+    alone) and sustained (inside a long loop); fp16 runs at the bf16 rate.  Fallback 1900."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError, TypeError):
+        return 1900.0, 1700.0, "fallback"
 
 
 def kernel_source_sha() -> str:
@@ -509,7 +522,10 @@ def secondary(qg, torch, dev, s):
             for W in Ws:
                 qg.qg_gemv(fmt, W, x, N, y=y, ws=ws, stream=s)
         us = _graph_time_us(torch, s, fn, 20) / R
-        out[f"{synth.FORMAT_NAMES[fmt]} {N}x{K} M=1 cold"] = {"us": us, "GB/s": nb / us / 1e3}
+        peak, _ = measured_peak()
+        out[f"{synth.FORMAT_NAMES[fmt]} {N}x{K} M=1 cold"] = {"us": us, "GB/s": nb / us / 1e3,
+                                                            "GiB/s": nb / us * 1e6 / 2 ** 30,
+                                                            "frac_of_hbm": nb / us / 1e3 / peak}
         del Ws, base
     # MoE FFN: Q4_K experts, H=2048, E=256 routed (I=512) + 1 shared, top-8
     H, E, I, topk = 2048, 256, 512, 8
@@ -559,7 +575,58 @@ def secondary(qg, torch, dev, s):
             out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {"us": us, "GB/s": nb / us / 1e3,
                                                                                  "us_eager": ue}
         del Wg, Wu, Wd
+    out.update(prefill_secondary(qg, torch, dev, s))
     return out
+
+
+PREFILL_M = 512
+PREFILL_MATRICES = [(synth.Q4_K, 17408, 5120), (synth.Q4_K, 5120, 17408), (synth.Q4_0, 17408, 5120),
+                    (synth.Q4_0, 5120, 17408)]
+
+
+def prefill_secondary(qg, torch, dev, s):
+    """Prefill GEMM on the tensor cores (qg_prefill_gemm), 512 tokens, dense-27B FFN shapes:
+    TFLOP/s = 2 M N K / call time, against the measured dense bf16 peak (fp16 runs at the
+    same rate), burst figure (each call is timed inside a short graph of calls)."""
+    out = {}
+    burst, _, kind = measured_tensor_peak()
+    M = PREFILL_M
+    for fmt, N, K in PREFILL_MATRICES:
+        g = synth.rng(6, fmt * 7 + (N > K))
+        W = torch.from_numpy(synth.weights(fmt, N, K, g)).to(dev)
+        x = torch.from_numpy(synth.activations(M, K, g)).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_PREFILL, fmt, M, N, K), dtype=torch.uint8, device=dev)
+        call = lambda: qg.qg_prefill_gemm(fmt, W, x, N, y=y, ws=ws, stream=s)  # noqa: E731
+        us = _graph_time_us(torch, s, call, 40, per_graph=4)
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        out[f"prefill {synth.FORMAT_NAMES[fmt]} {N}x{K} M={M}"] = {
+            "us": us, "TFLOP/s": tf, "frac_of_tensor_peak": tf / burst,
+            "peak": {"value": burst, "unit": "TFLOP/s", "source": kind, "which": "dense bf16 burst"},
+            "tokens/s": M / (us * 1e-6)}
+        del W, x, y, ws
+    return out
+
+
+def run_one_prefill(spec: str):
+    """Three qg_prefill_gemm calls of one shape (format name:NxK:M), for a profiler."""
+    import torch
+
+    import gguf_block_quantized_quant_gb300 as qg
+
+    name, shape, m = spec.split(":")
+    N, K = (int(v) for v in shape.lower().split("x"))
+    fmt = synth.FORMATS[name]
+    g = np.random.default_rng(synth.seed_for(6, fmt))
+    W = torch.from_numpy(synth.weights(fmt, N, K, g)).cuda()
+    x = torch.from_numpy(synth.activations(int(m), K, g)).cuda()
+    for _ in range(3):
+        y = qg.qg_prefill_gemm(fmt, W, x, N)
+    torch.cuda.synchronize()
+    if qg.qg_device_error():
+        raise SystemExit("bench.py: device error word set by the prefill calls")
+    print(json.dumps({"one_prefill": spec, "y_abs_sum": float(y.abs().sum())}))
+    return 0
 
 
 def run_one(spec: str):
@@ -616,9 +683,20 @@ def main(argv=None):
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--one", metavar="FMT:NxK:M", help="three untimed GEMV calls of one shape, then exit")
     ap.add_argument("--one-moe", type=int, metavar="M", help="three untimed MoE FFN calls of M tokens, then exit")
+    ap.add_argument("--one-prefill", metavar="FMT:NxK:M", help="three untimed prefill GEMM calls, then exit")
+    ap.add_argument("--prefill-only", action="store_true", help="print the prefill secondary entries only")
     args = ap.parse_args(argv)
     if args.one:
         return run_one(args.one)
+    if args.one_prefill:
+        return run_one_prefill(args.one_prefill)
+    if args.prefill_only:
+        import torch
+
+        import gguf_block_quantized_quant_gb300 as qg
+        s = torch.cuda.Stream()
+        print(json.dumps(prefill_secondary(qg, torch, torch.device("cuda", 0), s)), flush=True)
+        return 0
     if args.one_moe:
         return run_one_moe(args.one_moe)
     if args.warmup < 3:

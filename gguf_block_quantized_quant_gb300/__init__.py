@@ -29,7 +29,7 @@ BLOCK_ELEMS = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K
 BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
                Q6_K: 210, IQ4_NL: 18, IQ4_XS: 136}
 
-QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER, QG_OP_MOE_FFN_S16 = 1, 2, 3, 4, 5
+QG_OP_GEMV, QG_OP_GEMV_Q, QG_OP_MOE_FFN, QG_OP_FFN_SUBLAYER, QG_OP_MOE_FFN_S16, QG_OP_PREFILL = 1, 2, 3, 4, 5, 6
 QG_OK, QG_EINVAL, QG_EWORKSPACE, QG_EALIGN, QG_ECUDA, QG_EDEVICE = 0, -1, -2, -3, -4, -5
 WS_INVALID = ctypes.c_size_t(-1).value
 
@@ -38,7 +38,8 @@ LIB_PATH = _build.LIB
 # every symbol declared in include/qg.h
 EXPORTS = ("qg_quantize_act", "qg_gemv", "qg_gemv_q", "qg_moe_ffn", "qg_ffn_sublayer", "qg_workspace_size",
            "qg_moe_ws_layout", "qg_ffn_ws_layout", "qg_block_dots", "qg_device_error", "qg_strerror",
-           "qg_version", "qg_gemv_static_ws", "qg_quantize_act_s16", "qg_moe_ffn_s16", "qg_moe_s16_ws_layout")
+           "qg_version", "qg_gemv_static_ws", "qg_quantize_act_s16", "qg_moe_ffn_s16", "qg_moe_s16_ws_layout",
+           "qg_prefill_gemm", "qg_dequant_f16", "qg_test_wait_expiry")
 QG_STATIC_WS_BYTES = 2097152  # include/qg.h
 
 
@@ -75,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.qg_moe_ws_layout.argtypes = [I, I, I, I, I, ctypes.POINTER(S)]
         L.qg_ffn_ws_layout.argtypes = [I, I, I, I, ctypes.POINTER(S)]
         L.qg_block_dots.argtypes = [I, P, P, P, I, I, I, P, P, P]
+        L.qg_prefill_gemm.argtypes = [I, P, P, P, I, I, I, P, S, P]
+        L.qg_dequant_f16.argtypes = [I, P, I, I, P, P]
+        L.qg_test_wait_expiry.argtypes = [ctypes.c_ulonglong, P]
         L.qg_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.qg_strerror.argtypes = [I]
         L.qg_strerror.restype = ctypes.c_char_p
@@ -251,6 +255,29 @@ def qg_block_dots(fmt: int, W, xq, xs, N: int, stream=None):
     _check(lib().qg_block_dots(fmt, _ptr(W, False), _ptr(xq), _ptr(xs), N, K, M, _ptr(dots), _ptr(aux), _stream(stream)),
            "qg_block_dots")
     return dots, aux
+
+
+def qg_prefill_gemm(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
+    """Prefill GEMM on the tensor cores: y = fp16(W) fp16(x)^T in fp32, for M >> 16 tokens."""
+    M, K = x.shape
+    y = _out((M, N), torch.float32, x) if y is None else y
+    ws, nws = _ws(ws, qg_workspace_size(QG_OP_PREFILL, fmt, M, N, K), _dev(x))
+    _check(lib().qg_prefill_gemm(fmt, _ptr(W, False), _ptr(x), _ptr(y), N, K, M, _ptr(ws, False), nws,
+                                 _stream(stream)), "qg_prefill_gemm")
+    return y
+
+
+def qg_dequant_f16(fmt: int, W, N: int, K: int, stream=None):
+    """Test hook: the fp16 weights (uint16 bit patterns, N x K) the prefill GEMM multiplies."""
+    out = torch.empty((N, K), dtype=torch.int16, device=W.device)
+    _check(lib().qg_dequant_f16(fmt, _ptr(W, False), N, K, _ptr(out), _stream(stream)), "qg_dequant_f16")
+    return out
+
+
+def qg_test_wait_expiry(limit_ns: int, stream=None):
+    """Test hook: a bounded wait that nothing satisfies gives up after limit_ns and sets the
+    device error word (read it with qg_device_error)."""
+    _check(lib().qg_test_wait_expiry(int(limit_ns), _stream(stream)), "qg_test_wait_expiry")
 
 
 def qg_device_error() -> int:

@@ -154,6 +154,45 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
     }
 }
 
+// fp16 activation image of the prefill GEMM (see launch_prefill_x16): one thread per 16-byte
+// chunk of the image, in image order (coalesced stores).  Chunk position p of row r of a
+// tile holds the 8 elements of logical chunk p ^ (r & 7) (the 128-byte swizzle).  Launched
+// like prep_tiles_kernel.
+__global__ void __launch_bounds__(256) prefill_x16_kernel(const float *x, int M, int K, int BT, int nkt, long chunks,
+                                                          uint4 *img) {
+    griddep_launch_dependents();
+    griddep_wait();
+    for (long c = (long)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += (long)gridDim.x * blockDim.x) {
+        const long tile = c / (BT * 8);
+        const int within = (int)(c - tile * (BT * 8));
+        const int r = within >> 3, pos = within & 7;
+        const int tt = (int)(tile / nkt), kt = (int)(tile - (long)tt * nkt);
+        const int m = tt * BT + r, k0 = kt * 64 + 8 * (pos ^ (r & 7));
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (m < M && k0 + i < K) ? x[(long)m * K + k0 + i] : 0.0f;
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            h[i] = *reinterpret_cast<const uint32_t *>(&p);
+        }
+        img[c] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Test hook of the failure detector: one thread waits, through the kernels' bounded wait
+// routine, for the first phase of an mbarrier that nothing ever arrives at; after limit_ns
+// the wait gives up, sets DEVERR_TIMEOUT in the error word and the kernel returns.
+__global__ void wait_expiry_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait_limit(b, 0, limit_ns);
+}
+
 // The small kernels ask for the same L1 / shared-memory split as the engine (all shared),
 // so that an SM does not have to change its configuration between them and the engine and
 // they can run beside an engine CTA.  Set once per kernel and device.
@@ -219,6 +258,12 @@ int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t
     const long blocks = (long)rows * (K / 32);
     const int grid = (int)std::min<long>((blocks + 7) / 8, 2048);
     return launch_pdl(prep_tiles_kernel, grid, 256, s, x, u, h_out, xq, xd, xs, rows, K, xgt_log2, img, mq, md, ms);
+}
+
+int launch_prefill_x16(const float *x, int M, int K, int BT, int ntt, int nkt, uint8_t *img, cudaStream_t s) {
+    const long chunks = (long)ntt * nkt * BT * 8;
+    const int grid = (int)std::min<long>((chunks + 255) / 256, 4096);
+    return launch_pdl(prefill_x16_kernel, grid, 256, s, x, M, K, BT, nkt, chunks, reinterpret_cast<uint4 *>(img));
 }
 
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,
@@ -417,6 +462,10 @@ size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, 
         const FfnPlan p = plan_ffn(fmt, M, K, I, planning_sms());
         return p.ok ? p.ws_total : bad;
     }
+    case QG_OP_PREFILL: {
+        const PrefillPlan p = plan_prefill(fmt, N, K, M, planning_sms());
+        return p.ok ? p.ws_total : bad;
+    }
     default: return bad;
     }
 }
@@ -592,6 +641,40 @@ int qg_block_dots(int fmt, const void *W, const int8_t *xq, const int32_t *xs, i
     if (sms < 0) return sms;
     DotsCall c{static_cast<const uint8_t *>(W), xq, xs, N, K, M, dots, aux, (cudaStream_t)stream};
     return by_format(fmt, [&](auto F) { return dots_run<decltype(F)::value>(c); });
+}
+
+int qg_prefill_gemm(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M, void *ws,
+                    size_t ws_bytes, void *stream) {
+    if (!W_blocks || !x || !y || N < 1 || M < 1 || M > PF_M_MAX || !shape_ok(fmt, K)) return QG_EINVAL;
+    if (!aligned(W_blocks, 16) || !aligned(x, 4) || !aligned(y, 4) || (ws && !aligned(ws, 16))) return QG_EALIGN;
+    if (!ws) return QG_EWORKSPACE;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    const PrefillPlan p = plan_prefill(fmt, N, K, M, sms);
+    if (!p.ok) return QG_EINVAL;
+    if (ws_bytes < p.ws_total) return QG_EWORKSPACE;
+    PrefillCall c{static_cast<const uint8_t *>(W_blocks), x, y, N, K, M, static_cast<uint8_t *>(ws), ws_bytes,
+                  (cudaStream_t)stream};
+    return by_format(fmt, [&](auto F) { return prefill_run<decltype(F)::value>(c, sms); });
+}
+
+int qg_dequant_f16(int fmt, const void *W_blocks, int N, int K, uint16_t *out, void *stream) {
+    if (!W_blocks || !out || N < 1 || !shape_ok(fmt, K)) return QG_EINVAL;
+    if (!aligned(W_blocks, 16) || !aligned(out, 4)) return QG_EALIGN;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    return by_format(fmt, [&](auto F) {
+        return dequant_f16_run<decltype(F)::value>(static_cast<const uint8_t *>(W_blocks), N, K, out,
+                                                   (cudaStream_t)stream);
+    });
+}
+
+int qg_test_wait_expiry(unsigned long long limit_ns, void *stream) {
+    if (limit_ns < 1000ull || limit_ns > 1000000000ull) return QG_EINVAL;
+    const int sms = current_sms();
+    if (sms < 0) return sms;
+    wait_expiry_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
 int qg_device_error(unsigned int *err) {

@@ -133,11 +133,11 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 // One error word per translation unit (no relocatable device code); the host ORs them.
 static __device__ unsigned int g_qg_dev_err;
 
-// Waits for the phase of parity `parity` to complete.  Gives up after WAIT_NS, records
+// Waits for the phase of parity `parity` to complete.  Gives up after limit_ns, records
 // DEVERR_TIMEOUT in the device error word and returns false; the caller then carries on
 // (with invalid data) so that every thread still reaches every barrier and the kernel
 // ends.  The host reads the error word through qg_device_error().
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     bool checked = false;
@@ -151,13 +151,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
                 checked = true;
                 if (*reinterpret_cast<volatile unsigned int *>(&g_qg_dev_err) & DEVERR_TIMEOUT) return false;
             }
-            if (dt > WAIT_NS) {
+            if (dt > limit_ns) {
                 atomicOr(&g_qg_dev_err, DEVERR_TIMEOUT);
                 return false;
             }
         }
     }
 }
+// The kernels' wait: limit WAIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_limit(bar, parity, WAIT_NS); }
+
+// Waits for the phase of parity `parity` of `bar` for at most limit_ns, without looking at
+// the device error word.  For the end of a kernel: after an earlier wait gave up, bulk copies
+// (or tensor-core operations) still in flight must land before the shared or tensor memory
+// they target is released.  On the normal path the phase is complete and this returns at
+// once.  Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+constexpr unsigned long long DRAIN_NS = 100000000ull;  // 100 ms
 
 // 1-D bulk copy global -> shared (this CTA), completion counted on `bar` in bytes.
 // dst, src and bytes must all be multiples of 16.

@@ -348,6 +348,13 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
             carry_o = cont ? olast : -1;
         }
     }
+    // every stage was consumed on the normal path; after a wait gave up, this warp's bulk
+    // copies still in flight land (bounded) before the CTA can exit
+    if (lane == 0) {
+        for (int d = 0; d < D && d < nchunk; ++d)
+            mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nchunk - 1 - d) / D)) / D) & 1), DRAIN_NS);
+        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
+    }
     // a range that ended inside a row: its sum is shared with the next warp
     if (carry_o >= 0 && lane == 0) {
         float *e = bsum + (warp * 2 + ((a_mid && carry_o == ra) ? 0 : 1)) * BND_FLOATS;
@@ -656,6 +663,12 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_pair_kernel(const Job job)
             }
             carry_p = cont ? plast : -1;
         }
+    }
+    // as in engine_kernel: this warp's copies still in flight land before the CTA exits
+    if (lane == 0) {
+        for (int d = 0; d < D && d < nchunk; ++d)
+            mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nchunk - 1 - d) / D)) / D) & 1), DRAIN_NS);
+        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
     }
     // a range that ended inside a pair: its sums are shared with the next warp
     if (carry_p >= 0 && lane == 0) {

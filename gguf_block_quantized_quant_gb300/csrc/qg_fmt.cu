@@ -9,6 +9,7 @@
 
 #include "qg_jobs.cuh"
 #include "qg_launch.h"
+#include "qg_prefill.cuh"
 
 #ifndef QG_FMT
 #error "QG_FMT must be defined"
@@ -456,11 +457,77 @@ int dev_err_take(unsigned int *err) {
     return 0;
 }
 
+// ----------------------------------------------------------------------------- prefill GEMM
+// The fp16 activation image (normal launch), then the tensor-core GEMM (programmatic
+// dependent launch: its set-up overlaps the image), then the split-K reduction if any.
+template <int FMT>
+int prefill_run(const PrefillCall &c, int sms) {
+    const PrefillPlan p = plan_prefill(FMT, c.N, c.K, c.M, sms);
+    if (!p.ok) return -1;
+    if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
+    uint8_t *ximg = c.ws + p.ws_ximg;
+    int rc = launch_prefill_x16(c.x, c.M, c.K, p.BT, p.ntt, p.nkt, ximg, c.stream);
+    if (rc) return rc;
+    static std::mutex mu;
+    static bool ready[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev]) {
+            if (cudaFuncSetAttribute(prefill_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) !=
+                cudaSuccess)
+                return -4;
+            ready[dev] = true;
+        }
+    }
+    PrefillArgs a{};
+    a.W = c.W;
+    a.rb = p.rb;
+    a.N = c.N;
+    a.K = c.K;
+    a.M = c.M;
+    a.BT = p.BT;
+    a.nkt = p.nkt;
+    a.ktps = p.ktps;
+    a.stages = p.stages;
+    a.tmem_cols = p.tmem_cols;
+    a.idesc = p.idesc;
+    a.ximg = ximg;
+    a.out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.nn, (unsigned)p.ntt, (unsigned)p.KS);
+    cfg.blockDim = dim3(PF_THREADS);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, prefill_kernel<FMT>, a) != cudaSuccess) return -4;
+    if (cudaGetLastError() != cudaSuccess) return -4;
+    if (p.KS > 1) return launch_splitk_reduce(a.out, p.KS, (long)c.M * c.N, c.y, c.stream);
+    return 0;
+}
+
+template <int FMT>
+int dequant_f16_run(const uint8_t *W, int N, int K, uint16_t *out, cudaStream_t s) {
+    FmtInfo f;
+    if (!fmt_info(FMT, f)) return -1;
+    const long total = (long)N * (K / 32);
+    const int grid = (int)std::min<long>((total + 255) / 256, 8192);
+    dequant_f16_kernel<FMT><<<grid, 256, 0, s>>>(W, (uint32_t)((K / f.qk) * f.bs), N, K, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 template int gemv_run<QG_FMT>(const GemvCall &, int);
 template int gemv_run_planned<QG_FMT>(const GemvPlan &, const GemvCall &);
 template int ffn_run<QG_FMT>(const FfnCall &, int);
 template int moe_run<QG_FMT>(const MoeCall &, int);
 template int dots_run<QG_FMT>(const DotsCall &);
 template int dev_err_take<QG_FMT>(unsigned int *);
+template int prefill_run<QG_FMT>(const PrefillCall &, int);
+template int dequant_f16_run<QG_FMT>(const uint8_t *, int, int, uint16_t *, cudaStream_t);
 
 }  // namespace qg

@@ -60,6 +60,16 @@ struct DotsCall {
     cudaStream_t stream;
 };
 
+struct PrefillCall {
+    const uint8_t *W;
+    const float *x;     // M x K fp32
+    float *y;           // M x N fp32
+    int N, K, M;
+    uint8_t *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
 // Per-format launchers (status codes as in qg.h).
 template <int FMT>
 int gemv_run(const GemvCall &c, int sms);
@@ -73,6 +83,10 @@ template <int FMT>
 int dots_run(const DotsCall &c);
 template <int FMT>
 int dev_err_take(unsigned int *err);  // read and clear the format's device error word
+template <int FMT>
+int prefill_run(const PrefillCall &c, int sms);
+template <int FMT>
+int dequant_f16_run(const uint8_t *W, int N, int K, uint16_t *out, cudaStream_t s);
 
 // Format-independent kernels (qg_abi.cu).
 int launch_quant_act(const float *x, int M, int K, long ldx, int8_t *xq, float *xd, int32_t *xs,
@@ -85,6 +99,10 @@ int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStrea
 int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t *xq, const float *xd,
                       const int32_t *xs, int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq, float *md,
                       int32_t *ms, cudaStream_t s);
+// fp16 activation image of the prefill GEMM: M x K fp32 rows -> ntt tiles of BT tokens x nkt
+// tiles of 64 elements, each BT x 128 bytes in the tensor cores' K-major 128-byte-swizzled
+// layout (rows past M and elements past K are zero).
+int launch_prefill_x16(const float *x, int M, int K, int BT, int ntt, int nkt, uint8_t *img, cudaStream_t s);
 // Router logits (fp32) and the activation tile image of x (s16: two planes per row) in one
 // launch.
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,

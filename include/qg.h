@@ -79,7 +79,14 @@ enum qg_status {
 };
 
 /* Operations for qg_workspace_size(). */
-enum qg_op { QG_OP_GEMV = 1, QG_OP_GEMV_Q = 2, QG_OP_MOE_FFN = 3, QG_OP_FFN_SUBLAYER = 4, QG_OP_MOE_FFN_S16 = 5 };
+enum qg_op {
+    QG_OP_GEMV = 1,
+    QG_OP_GEMV_Q = 2,
+    QG_OP_MOE_FFN = 3,
+    QG_OP_FFN_SUBLAYER = 4,
+    QG_OP_MOE_FFN_S16 = 5,
+    QG_OP_PREFILL = 6
+};
 
 /* Activation quantization "Q8_F32S" [D27 Q&A]: for each token m and each 32-element
  * block b of K, d = amax|x| / 127 (fp32, IEEE division), q = clamp(roundf(x / d),
@@ -195,12 +202,36 @@ int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd,
                     const float *x, float *y, int M, int H, int I,
                     void *ws, size_t ws_bytes, void *stream);
 
+/* Prefill GEMM on the tensor cores over raw blocks [KES section 九: prefill moved to the
+ * tensor cores with the weights dequantized to fp16 inside the kernel; section 四, issue ⑮:
+ * prefill takes float activations, not int8 ones], for M tokens at once (M >> 16):
+ *   y[m][n] = sum_k fp16(w[n][k]) * fp16(x[m][k]), accumulated in fp32, where
+ *   w[n][k] is formed per 32-element unit in fp32 as A_u * c_e - B_u * mc_e (the factors and
+ *   codes of qg_block_dots: both products exact, one rounding) and rounded to the nearest
+ *   fp16 (ties to even), and fp16(x) is the nearest fp16 of x (ties to even).
+ *   fmt: qg_format.  W: N x K blocks (16-byte aligned).  x: M x K fp32.  y: M x N fp32.
+ *   Limits: 1 <= M <= 1048576 (QG_EINVAL otherwise); K a multiple of the block size.
+ *   ws: device, >= qg_workspace_size(QG_OP_PREFILL, fmt, M, N, K, 0, 0, 0) bytes, 16-byte
+ *   aligned: the fp16 activation tiles (about 2 x M x K bytes) and, for K-split shapes,
+ *   fp32 partial sums.  |x| beyond 65504 rounds to infinity in fp16 (the caller's range).
+ * Launches a conversion kernel, the tensor-core kernel (tcgen05.mma, fp32 accumulators in
+ * tensor memory) and, for K-split shapes, a reduction; asynchronous on stream like every
+ * call here. */
+int qg_prefill_gemm(int fmt, const void *W_blocks, const float *x, float *y, int N, int K, int M,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/* Test hook of the prefill operand: out[n][k] = the fp16 bit pattern of w[n][k] as formed by
+ * qg_prefill_gemm (same device decoders).  out: N x K uint16, device memory (or page-locked
+ * host memory), 4-byte aligned. */
+int qg_dequant_f16(int fmt, const void *W_blocks, int N, int K, uint16_t *out, void *stream);
+
 /* Bytes of workspace an operation needs; 0 means the call needs none (ws may then be
  * NULL); (size_t)-1 means the arguments are invalid.  The size depends on the shape and
  * on the current device's SM count (152 is assumed when no device is usable).
  *   QG_OP_GEMV / QG_OP_GEMV_Q: (fmt, M, N, K)            E, topk, I ignored
  *   QG_OP_MOE_FFN, QG_OP_MOE_FFN_S16: (fmt, M, N=H, K=H, E, topk, I)
- *   QG_OP_FFN_SUBLAYER:        (fmt, M, N=H, K=H, I)      E, topk ignored */
+ *   QG_OP_FFN_SUBLAYER:        (fmt, M, N=H, K=H, I)      E, topk ignored
+ *   QG_OP_PREFILL:             (fmt, M, N, K)             E, topk, I ignored */
 size_t qg_workspace_size(int op, int fmt, int M, int N, int K, int E, int topk, int I);
 
 /* Offsets (bytes from ws) of the MoE intermediates, written by qg_moe_ffn:
@@ -239,6 +270,13 @@ int qg_block_dots(int fmt, const void *W_blocks, const int8_t *xq, const int32_t
  * per-stage piece table and some rows were skipped (a library bug; results invalid).
  * Synchronizes the current device; for tests and diagnostics, not for the hot path. */
 int qg_device_error(unsigned int *err);
+
+/* Test hook of the failure detector (bounded waits): launches one thread that waits,
+ * through the same bounded wait routine as every kernel here, for an mbarrier phase that
+ * never completes, with a limit of limit_ns (1 us to 1 s; QG_EINVAL otherwise).  The wait
+ * gives up, records value 1 in the device error word (qg_device_error) and the kernel
+ * returns: the context stays usable.  Asynchronous on stream. */
+int qg_test_wait_expiry(unsigned long long limit_ns, void *stream);
 
 /* Human-readable text of a status code. */
 const char *qg_strerror(int status);

@@ -8,8 +8,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from qg_testlib import dev, qg_module
+from qg_testlib import assert_within, dev, host, qg_module
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +43,35 @@ def test_static_ws_two_calls_match_gemv(qg, fmt, N, K, M):
     assert torch.equal(y1, r1)
     assert torch.equal(y2, r2)
     assert not torch.equal(y1, y2)
+    assert qg.qg_device_error() == 0
+    # and against the oracle, not only against the workspace entry point
+    for W, x, y in ((W1, x1, y1), (W2, x2, y2)):
+        Wn, xn = host(W), host(x)
+        xq, xd, xs = oracle.quantize_act(xn)
+        assert_within(host(y), oracle.gemv_q(fmt, Wn, xq, xd, xs, N, K), oracle.absdot(fmt, Wn, xq, xd, N, K),
+                      "static-scratch gemv")
+
+
+def test_static_ws_leftover_scratch_from_a_larger_call(qg):
+    """A call that fills most of the scratch (split-K partial sums of 16 tokens) directly
+    followed by a smaller split-K call: the second call reads only what it wrote itself."""
+    big = (synth.Q4_0, 3, 131072 // 4, 16)
+    small = (synth.Q4_0, 5, 8192, 3)
+    need_big = qg.qg_workspace_size(qg.QG_OP_GEMV, big[0], big[3], big[1], big[2])
+    need_small = qg.qg_workspace_size(qg.QG_OP_GEMV, small[0], small[3], small[1], small[2])
+    assert need_small < need_big <= qg.QG_STATIC_WS_BYTES
+    g = np.random.default_rng(2024)
+    s = torch.cuda.current_stream()
+    outs = []
+    for fmt, N, K, M in (big, small, big, small):
+        W, x = synth.weights(fmt, N, K, g), synth.activations(M, K, g)
+        y = qg.qg_gemv_static_ws(fmt, dev(W), dev(x), N, stream=s)
+        outs.append((fmt, N, K, W, x, y))
+    torch.cuda.synchronize()
+    for fmt, N, K, W, x, y in outs:
+        xq, xd, xs = oracle.quantize_act(x)
+        assert_within(host(y), oracle.gemv_q(fmt, W, xq, xd, xs, N, K), oracle.absdot(fmt, W, xq, xd, N, K),
+                      f"static scratch {N}x{K} after a larger call")
     assert qg.qg_device_error() == 0
 
 
