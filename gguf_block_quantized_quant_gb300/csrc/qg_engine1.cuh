@@ -1,0 +1,144 @@
+// qg_engine1.cuh -- the one-token GEMV engine for rows that start 16-byte aligned.
+//
+// One token, one matrix, no K-split: a CTA owns the contiguous output rows [o0, o1), and
+// because every row is tpr tasks of TASK_BYTES bytes laid out back to back, the CTA's tasks
+// are one contiguous byte range: task f of the CTA starts at W + o0 * rb + f * TASK_BYTES.
+// With TASK_BYTES and rb multiples of 16 every stage is then a single aligned bulk copy, and
+// the bookkeeping of the general engine (run tables, widened pieces, segmented reductions
+// with carries across stages and warps) is not needed:
+//  * the CTA's tasks are split into NCW contiguous ranges, one per warp; a warp consumes its
+//    range in stages of 32 tasks (lane l takes task 32 s + l) through D ring slots of its
+//    own, lane 0 issuing one cp.async.bulk per stage, completion counted on the slot's
+//    mbarrier;
+//  * a lane copies its task from the slot into registers, the warp refills the slot with
+//    the stage D ahead, and the lane decodes its task against the activation tiles (written
+//    by the preparation kernel, copied once into shared memory, with the first 31 tiles
+//    repeated after the row so that the 32 lanes of a stage read consecutive tiles even
+//    where the stage wraps into the next row);
+//  * each task's fp32 sum goes to part[row][task] in shared memory; after the last stage
+//    the CTA adds every row's tpr partial sums in task order and writes y.  The order of
+//    every addition is fixed, so results are deterministic.
+#pragma once
+
+#include "qg_engine.cuh"
+
+namespace qg {
+
+struct Gemv1Args {
+    const uint8_t *W;      // N rows of rb bytes
+    float *y;              // N outputs (one token)
+    const uint8_t *ximg;   // activation tile image of the token's row: tpr tiles
+    int N, tpr, depth, xrep;
+    uint32_t rb, slot_bytes, x_bytes;
+};
+
+// shared memory: ring (S slots), activation tiles, partial sums, S + 1 mbarriers
+__host__ __device__ constexpr uint32_t engine1_smem(int S, uint32_t slot_bytes, uint32_t x_bytes, int part_floats) {
+    return (uint32_t)S * slot_bytes + x_bytes + 4u * (uint32_t)part_floats + 8u * (uint32_t)(S + 1) + 16u;
+}
+
+template <int FMT, int T, int NCW>
+__global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a) {
+    using F = FT<FMT, T>;
+    using TL = Tile<F::XGT>;
+    constexpr uint32_t TB = F::TASK_BYTES;
+    static_assert(TB % 16 == 0, "stages are single aligned bulk copies");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = a.depth, S = NCW * D;
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t xa = ring + (uint32_t)S * a.slot_bytes;
+    float *part = reinterpret_cast<float *>(smem + (uint32_t)S * a.slot_bytes + a.x_bytes);
+    const int o0 = split_point(a.N, (int)blockIdx.x, (int)gridDim.x);
+    const int o1 = split_point(a.N, (int)blockIdx.x + 1, (int)gridDim.x);
+    const int tpr = a.tpr;
+    const int ntask = (o1 - o0) * tpr;
+    const uint32_t bars = ring + (uint32_t)S * a.slot_bytes + a.x_bytes + 4u * (uint32_t)ntask;
+    const uint32_t bars8 = (bars + 7u) & ~7u;
+    auto full_bar = [&](int s) { return bars8 + 8u * (uint32_t)s; };
+    const uint32_t xbar = bars8 + 8u * (uint32_t)S;
+    const uint8_t *base = a.W + (size_t)o0 * a.rb;
+
+    griddep_launch_dependents();
+    if (lane == 0) {
+        for (int j = 0; j < D; ++j) mbar_init(full_bar(j * NCW + warp), 1);
+        if (warp == 0) mbar_init(xbar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int wa = split_point(ntask, warp, NCW), wb = split_point(ntask, warp + 1, NCW);
+    const int nst = (wb - wa + 31) / 32;  // this warp's stages
+
+    // stage j of this warp into its slot (lane 0; the slot must be free)
+    auto issue = [&](int j) {
+        if (lane == 0) {
+            const int fa = wa + 32 * j, fb = min(wb, fa + 32);
+            const uint32_t slot = (uint32_t)((j % D) * NCW + warp);
+            const uint32_t bytes = (uint32_t)(fb - fa) * TB;
+            bulk_g2s(ring + slot * a.slot_bytes, base + (size_t)fa * TB, bytes, full_bar((int)slot));
+            mbar_arrive_expect_tx(full_bar((int)slot), bytes);
+        }
+    };
+    const int jfirst = min(D, nst);
+    for (int j = 0; j < jfirst; ++j) issue(j);
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        griddep_wait();
+        const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
+        uint32_t tx = 0;
+        if (ntask > 0) {
+            bulk_g2s(xa, a.ximg, row_bytes, xbar);
+            tx += row_bytes;
+            // the row's first xrep tiles again after it
+            for (int v = tpr; v < tpr + a.xrep; v += tpr) {
+                const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
+                bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
+                tx += rb2;
+            }
+        }
+        mbar_arrive_expect_tx(xbar, tx);
+    }
+    const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
+    mbar_wait(xbar, 0);
+
+    for (int j = 0; j < nst; ++j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = wa + 32 * j, fb = min(wb, fa + 32);
+        mbar_wait(full_bar(slot), (uint32_t)((j / D) & 1));
+        const int f = fa + lane;
+        const bool valid = f < fb;
+        uint32_t w[F::WW];
+        if (valid) F::load(smem + (uint32_t)slot * a.slot_bytes + (uint32_t)lane * TB, w);
+        __syncwarp();
+        if (j + D < nst) {
+            fence_proxy_async_smem();
+            issue(j + D);
+        }
+        if (valid) {
+            const int o = (int)tpr_div.div((uint32_t)f), tt = f - o * tpr;
+            // with repeated tiles lane l reads virtual column (column of the stage's first
+            // task) + l, past the row's end where the stage wraps
+            const int xc = a.xrep ? fa - (int)tpr_div.div((uint32_t)fa) * tpr + lane : tt;
+            AccSink<1> sink;
+            sink.acc[0] = 0.0f;
+            F::compute(w, 0u, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
+            part[f] = sink.acc[0];
+        }
+    }
+    // every stage was consumed; copies still in flight after a wait gave up land first
+    if (lane == 0) {
+        for (int d = 0; d < D && d < nst; ++d)
+            mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nst - 1 - d) / D)) / D) & 1), DRAIN_NS);
+        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
+    }
+    __syncthreads();
+    for (int r = tid; r < o1 - o0; r += NCW * 32) {
+        const float *p = part + (size_t)r * tpr;
+        float s = 0.0f;
+        for (int t = 0; t < tpr; ++t) s += p[t];
+        a.y[o0 + r] = s;
+    }
+}
+
+}  // namespace qg

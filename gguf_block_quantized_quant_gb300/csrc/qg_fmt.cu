@@ -135,6 +135,45 @@ int with_t(const TaskGeo &g, Fn &&fn) {
     }
 }
 
+// The one-token engine (engine1_kernel) with ncw warps, for task sizes that are multiples of
+// 16 bytes.
+template <int FMT, int T>
+int launch_engine1(int ncw, const Gemv1Args &a, int grid, uint32_t smem, cudaStream_t s) {
+    if constexpr (FT<FMT, T>::TASK_BYTES % 16 != 0 || FT<FMT, T>::TPB != 1) {
+        return -1;
+    } else {
+        static std::mutex mu;
+        static bool ready[64][3] = {};
+        const int v = ncw == 16 ? 2 : ncw == NCW_WIDE ? 1 : 0;
+        auto kern = v == 2 ? engine1_kernel<FMT, T, 16> : v == 1 ? engine1_kernel<FMT, T, NCW_WIDE> : engine1_kernel<FMT, T, 8>;
+        if (ncw != 16 && ncw != NCW_WIDE && ncw != 8) return -1;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!ready[dev][v]) {
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) != cudaSuccess ||
+                    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                    return -4;
+                ready[dev][v] = true;
+            }
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(ncw * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return -4;
+        return cudaGetLastError() == cudaSuccess ? 0 : -4;
+    }
+}
+
 template <class J>
 void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
     j.depth = r.depth;
@@ -193,6 +232,22 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (p.pair)
         return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y,
                                   p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : nullptr, c.stream);
+    if (p.one)
+        return with_t<true>(p.geo, [&](auto Tc) {
+            constexpr int T = decltype(Tc)::value;
+            Gemv1Args a{};
+            a.W = c.W;
+            a.y = c.y;
+            a.ximg = ximg;
+            a.N = c.N;
+            a.tpr = p.geo.tpr;
+            a.depth = p.one_depth;
+            a.xrep = p.xrep;
+            a.rb = p.geo.rb;
+            a.slot_bytes = p.one_slot;
+            a.x_bytes = p.one_x;
+            return launch_engine1<FMT, T>(p.ncw, a, p.grid, p.one_smem, c.stream);
+        });
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;

@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "qg_engine.cuh"
+#include "qg_engine1.cuh"
 #include "qg_prefill.cuh"
 
 namespace qg {
@@ -201,8 +202,48 @@ struct GemvPlan {
     int MC = 0;         // row pairs: tokens per launch (launches over token chunks of MC)
     int xrep = 0;       // one-row engine: activation tiles repeated past a row's end
     Ring ring;
+    // one-token engine for 16-byte-aligned rows (engine1_kernel): ncw warps, depth slots each
+    bool one = false;
+    int one_depth = 0;
+    uint32_t one_slot = 0, one_x = 0, one_smem = 0;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_part = 0, ws_total = 0;
 };
+
+// Partial sums of one CTA of the one-token engine (rows x tasks per row) at most this many.
+constexpr int ONE_PART_MAX = 8192;
+
+// The one-token engine where it applies: one token, no K-split, every task and row a
+// multiple of 16 bytes (so each stage is one aligned bulk copy), and the CTA's partial sums
+// within ONE_PART_MAX.  Warps: 16 for tasks of at most 160 bytes, else 12; as many ring
+// slots per warp (up to DMAX) as shared memory holds.
+inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
+    const TaskGeo &g = p.geo;
+    if (p.pair || p.MT != 1 || p.KS != 1 || !g.aligned16() || g.TPB != 1) return;
+    const int grid = std::min(N, sms);
+    const long rows_max = (N + grid - 1) / grid;
+    const long part = rows_max * g.tpr;
+    if (part > ONE_PART_MAX) return;
+    const int ncw = g.task_bytes() <= 160 ? 16 : NCW_WIDE;
+    const uint32_t slot = (uint32_t)(32 * g.task_bytes());
+    const uint32_t xb = (uint32_t)align_up((size_t)(g.tpr + XREP) * g.stride, 16);
+    int depth = 0;
+    for (int d = DMAX; d >= 1; --d)
+        if (engine1_smem(ncw * d, slot, xb, (int)part) <= (uint32_t)SMEM_MAX) {
+            depth = d;
+            break;
+        }
+    if (depth < 1) return;
+    p.one = true;
+    p.ncw = ncw;
+    p.grid = grid;
+    p.groups = grid;
+    p.tpr_x = g.tpr;
+    p.xrep = XREP;
+    p.one_depth = depth;
+    p.one_slot = slot;
+    p.one_x = xb;
+    p.one_smem = engine1_smem(ncw * depth, slot, xb, (int)part);
+}
 
 inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
     GemvPlan p;
@@ -269,6 +310,7 @@ inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
             }
         }
     }
+    plan_gemv_one(p, N, sms);
     size_t o = 0;
     p.ximg_pitch = (size_t)g.tpr * g.stride;
     p.ws_ximg = o;

@@ -172,7 +172,7 @@ int main() {
     int Ks[] = {32, 96, 256, 512, 544, 768, 1056, 2048, 4096, 5120, 17408, 7168, 14336, 2816};
     int Ns[] = {1, 2, 3, 5, 37, 64, 75, 76, 151, 152, 153, 300, 1024, 2048, 4096, 5120, 17408};
     int Ms[] = {1, 2, 3, 4, 5, 8, 16};
-    int nplans = 0, npair = 0;
+    int nplans = 0, npair = 0, none = 0;
     char nm[160];
     for (int fmt : fmts) for (int K : Ks) for (int N : Ns) for (int M : Ms) {
         if (!task_geo(fmt, K, true).ok) continue;
@@ -191,6 +191,43 @@ int main() {
             ++npair;
             continue;
         }
+        if (p.one) {
+            // one-token engine: per CTA, warp and stage a single bulk copy of whole tasks
+            snprintf(nm, sizeof nm, "one f%d N%d K%d", fmt, N, K);
+            ++none;
+            CHECK(M == 1 && p.KS == 1 && g.task_bytes() % 16 == 0 && g.rb % 16 == 0 && g.TPB == 1, "%s eligibility", nm);
+            CHECK(p.one_smem <= (uint32_t)SMEM_MAX && p.one_depth >= 1, "%s smem %u", nm, p.one_smem);
+            CHECK(p.one_x >= (uint32_t)((g.tpr + p.xrep) * g.stride) && p.xrep >= 31, "%s x tiles", nm);
+            CHECK(p.one_slot == (uint32_t)(32 * g.task_bytes()), "%s slot", nm);
+            const int TB = g.task_bytes(), S = p.ncw * p.one_depth;
+            for (int b = 0; b < p.grid; ++b) {
+                const int o0 = (int)((long)b * N / p.grid), o1 = (int)((long)(b + 1) * N / p.grid);
+                const int ntask = (o1 - o0) * g.tpr;
+                CHECK(engine1_smem(S, p.one_slot, p.one_x, ntask) <= p.one_smem, "%s part of CTA %d", nm, b);
+                for (int w = 0; w < p.ncw; ++w) {
+                    const int wa = (int)((long)ntask * w / p.ncw), wb = (int)((long)ntask * (w + 1) / p.ncw);
+                    for (int fa = wa; fa < wb; fa += 32) {
+                        const int fb = std::min(wb, fa + 32);
+                        const uintptr_t src = BASE + (uintptr_t)o0 * g.rb + (uintptr_t)fa * TB;
+                        const uintptr_t end = src + (uintptr_t)(fb - fa) * TB;
+                        CHECK(src % 16 == 0 && (end - src) % 16 == 0, "%s copy alignment", nm);
+                        CHECK(end <= BASE + (uintptr_t)N * g.rb && src >= BASE, "%s copy range", nm);
+                        CHECK((uint32_t)((fb - fa) * TB) <= p.one_slot, "%s slot overflow", nm);
+                        for (int f = fa; f < fb; ++f) {
+                            const int o = f / g.tpr, tt = f % g.tpr;
+                            CHECK(o0 + o < o1, "%s row", nm);
+                            // the task's bytes: row o, task tt
+                            CHECK(BASE + (uintptr_t)(o0 + o) * g.rb + (uintptr_t)tt * TB == src + (uintptr_t)(f - fa) * TB,
+                                  "%s contiguity", nm);
+                            const int xc = fa % g.tpr + (f - fa);
+                            CHECK(xc < g.tpr + p.xrep && xc % g.tpr == tt, "%s virtual column %d", nm, xc);
+                            CHECK(f < ntask, "%s part index", nm);
+                        }
+                    }
+                }
+            }
+            continue;
+        }
         snprintf(nm, sizeof nm, "gemv f%d N%d K%d M%d KS%d", fmt, N, K, M, p.KS);
         CHECK(p.ring.x_bytes >= (uint32_t)(M * (p.tpr_x + p.xrep) * g.stride), "%s x bytes", nm);
         // repeated tiles: a stage's last lane reads virtual column (tpr - 1) + 31 at most
@@ -203,7 +240,7 @@ int main() {
                          CHECK(c.tpr <= p.tpr_x, "slice tpr"); return c; },
             [&](int o, int tt, uintptr_t &lim) { lim = BASE + (uintptr_t)N * g.rb; return BASE + (uintptr_t)o * g.rb + toff(g, tt); });
     }
-    printf("gemv plans %d (row pairs %d)\n", nplans, npair);
+    printf("gemv plans %d (row pairs %d, one-token %d)\n", nplans, npair, none);
     int Hs[] = {512, 1024, 2048, 4096, 5120, 7168}, Is[] = {256, 512, 1536, 2048, 14336, 17408};
     for (int fmt : fmts) for (int H : Hs) for (int I : Is) for (int M : Ms) {
         if (!task_geo(fmt, H, false).ok || !task_geo(fmt, I, false).ok) continue;
