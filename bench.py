@@ -53,6 +53,9 @@ M_TOKENS = 1
 ROTATE = 2                    # weight copies per matrix
 STEPS_PER_GRAPH = 16          # steps captured in one CUDA graph
 FALLBACK_HBM_GBS = 6800.0     # used only when no measured peak is available
+# Integer roof of the batched decode: dp4a issues at 64 lanes per SM per clock (4 int8 MACs
+# each) on 152 SMs at 2.07 GHz
+DP4A_MAC_PER_S = 152 * 64 * 4 * 2.07e9
 CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -126,7 +129,7 @@ def kernel_source_sha() -> str:
 def dram_traffic_per_launch():
     """DRAM bytes (read + write) of one engine launch from the committed ncu summary, or
     None when the kernel sources changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "engine_q4k_17408x5120_m1.txt")
+    path = os.path.join(ROOT, "profiles", "engine1_q4k_17408x5120_m1.txt")
     try:
         with open(path) as f:
             kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
@@ -219,12 +222,22 @@ def time_oracle(sample, min_seconds: float):
 
 
 def cpu_baseline_block(seconds: float = 10.0):
+    """The oracle on all host cores (the reported baseline) and, beside it, single-threaded."""
+    import oracle
     rows = 256
     sample = oracle_sample(rows)
     gbs, cores, reps, el = time_oracle(sample, seconds)
+    nthreads = oracle.get_threads()
+    oracle.set_threads(1)
+    try:
+        gbs1, _, reps1, el1 = time_oracle(oracle_sample(32), max(2.0, seconds / 4))
+    finally:
+        oracle.set_threads(0 if nthreads == cores else nthreads)
     return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} rows of each of the 4 matrices ({sum(synth.matrix_bytes(f, r, k) for f, r, k, _, _ in sample)} "
-                      f"weight bytes), repeated {reps}x in {el:.1f} s, fp64 oracle with OpenMP over rows"}
+                      f"weight bytes), repeated {reps}x in {el:.1f} s, fp64 oracle with OpenMP over rows",
+            "single_thread": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                              "sample": f"first 32 rows of each matrix, repeated {reps1}x in {el1:.1f} s"}}
 
 
 def run_reference(args, budget_s: float = 150.0):
@@ -349,6 +362,22 @@ def run_ours(args):
     ms_local = e0.elapsed_time(e1)
     ms, total_bytes = aggregate(ms_local, step_weight_bytes * args.steps, world)
     gbs = total_bytes / (ms * 1e-3) / 1e9
+    # the same K steps timed again (spread of the measurement; value is the first region)
+    rep_gbs = [gbs]
+    for _ in range(args.repeats - 1):
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            r0.record(s)
+            for _ in range(args.steps // G):
+                g_full.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            r1.record(s)
+        torch.cuda.synchronize()
+        rms, rtb = aggregate(r0.elapsed_time(r1), step_weight_bytes * args.steps, world)
+        rep_gbs.append(rtb / (rms * 1e-3) / 1e9)
 
     # ---- e2e: public API, host buffers, transfers inside the timed region.  Every step the
     # four calls take their activation rows from page-locked host memory and write their
@@ -425,7 +454,7 @@ def run_ours(args):
     achieved = algo / (launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": dram_traffic_per_launch(), "peak_source": peak_kind,
-                "kernel": "engine_kernel (GEMV) + activation tile preparation, per call",
+                "kernel": "engine1_kernel (one-token GEMV) + activation tile preparation, per call",
                 "algorithmic_bytes_per_launch": algo}
 
     line = {
@@ -440,7 +469,11 @@ def run_ours(args):
                          f"{ROTATE * step_weight_bytes} weight bytes in rotation",
                    "timing": f"CUDA graphs of {G} steps (weight copies alternating inside), replayed to K steps "
                              "between CUDA events on the launch stream",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "value_gib_s": gbs / 2 ** 30 * 1e9,
+                   "repeats": {"n": len(rep_gbs), "unit": "GB/s", "median": statistics.median(rep_gbs),
+                               "min": min(rep_gbs), "max": max(rep_gbs),
+                               "note": "the K timed steps repeated; value is the first repeat"}},
         "roofline": roofline,
         "cpu_baseline": None,
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -526,6 +559,9 @@ def secondary(qg, torch, dev, s):
         out[f"{synth.FORMAT_NAMES[fmt]} {N}x{K} M=1 cold"] = {"us": us, "GB/s": nb / us / 1e3,
                                                             "GiB/s": nb / us * 1e6 / 2 ** 30,
                                                             "frac_of_hbm": nb / us / 1e3 / peak}
+        # warm: the same buffer every call (it stays in L2), for context beside the cold figure
+        uw = _graph_time_us(torch, s, lambda: qg.qg_gemv(fmt, base, x, N, y=y, ws=ws, stream=s), 40)
+        out[f"{synth.FORMAT_NAMES[fmt]} {N}x{K} M=1 warm"] = {"us": uw, "GB/s": nb / uw / 1e3}
         del Ws, base
     # MoE FFN: Q4_K experts, H=2048, E=256 routed (I=512) + 1 shared, top-8
     H, E, I, topk = 2048, 256, 512, 8
@@ -543,12 +579,18 @@ def secondary(qg, torch, dev, s):
         y = torch.empty((M, H), dtype=torch.float32, device=dev)
         ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_MOE_FFN, fq, M, H, H, E, topk, I), dtype=torch.uint8,
                          device=dev)
-        call = lambda: qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y, ws=ws, stream=s)  # noqa
+        ids = torch.empty((M, topk), dtype=torch.int32, device=dev)
+        call = lambda: qg.qg_moe_ffn(fq, x, Wr, topk, Wg, Wu, Wd, Wgs, Wus, Wds, I, y=y, topk_ids=ids, ws=ws, stream=s)  # noqa
         us = _graph_time_us(torch, s, call, 200)
         # the same chain launched from the host call by call: the launch gaps a graph removes
         ue = _eager_time_us(torch, s, call, 200)
+        # algorithmic bytes: every distinct routed expert once, the shared expert, the router
+        nb = (len(set(ids.cpu().numpy().ravel().tolist())) + 1) * 3 * synth.matrix_bytes(fq, I, H) + 4 * E * H
+        peak, _ = measured_peak()
         out[f"MoE FFN Q4_K H=2048 E=256+1 I=512 top-8 M={M}"] = {"us": us, "tokens/s": M / (us * 1e-6),
-                                                                  "us_eager": ue}
+                                                                  "us_eager": ue, "GB/s": nb / us / 1e3,
+                                                                  "frac_of_hbm": nb / us / 1e3 / peak,
+                                                                  "algorithmic_bytes": nb}
         # the same with s16 activations (two int8 planes per activation row)
         ws16 = torch.empty(qg.qg_workspace_size(qg.QG_OP_MOE_FFN_S16, fq, M, H, H, E, topk, I), dtype=torch.uint8,
                            device=dev)
@@ -572,8 +614,14 @@ def secondary(qg, torch, dev, s):
             call = lambda: qg.qg_ffn_sublayer(fmt, Wg, Wu, Wd, x, I, y=y, ws=ws, stream=s)  # noqa: E731
             us = _graph_time_us(torch, s, call, 20)
             ue = _eager_time_us(torch, s, call, 20)
-            out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {"us": us, "GB/s": nb / us / 1e3,
-                                                                                 "us_eager": ue}
+            peak, _ = measured_peak()
+            hbm_us = nb / (peak * 1e3)
+            alu_us = 3.0 * M * H * I / DP4A_MAC_PER_S * 1e6
+            roof_us = max(hbm_us, alu_us)
+            out[f"FFN sublayer {synth.FORMAT_NAMES[fmt]} H=5120 I=17408 M={M}"] = {
+                "us": us, "GB/s": nb / us / 1e3, "us_eager": ue,
+                "roof": {"bound": "hbm" if hbm_us >= alu_us else "alu", "hbm_us": hbm_us, "alu_us": alu_us,
+                         "frac": roof_us / us}}
         del Wg, Wu, Wd
     out.update(prefill_secondary(qg, torch, dev, s))
     return out
@@ -679,6 +727,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of cpu_baseline")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of K steps (spread)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--one", metavar="FMT:NxK:M", help="three untimed GEMV calls of one shape, then exit")

@@ -214,7 +214,8 @@ constexpr int ONE_PART_MAX = 8192;
 
 // The one-token engine where it applies: one token, no K-split, every task and row a
 // multiple of 16 bytes (so each stage is one aligned bulk copy), and the CTA's partial sums
-// within ONE_PART_MAX.  Warps: 16 for tasks of at most 160 bytes, else 12; as many ring
+// within ONE_PART_MAX.  Warps as the general engine (plan_ncw): 16 for tasks of at most 160
+// bytes, else 12 where every warp gets at least two stages and 8 otherwise; as many ring
 // slots per warp (up to DMAX) as shared memory holds.
 inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
     const TaskGeo &g = p.geo;
@@ -223,7 +224,8 @@ inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
     const long rows_max = (N + grid - 1) / grid;
     const long part = rows_max * g.tpr;
     if (part > ONE_PART_MAX) return;
-    const int ncw = g.task_bytes() <= 160 ? 16 : NCW_WIDE;
+    // the general engine's warp count: 12 only where every warp gets two stages or more
+    const int ncw = plan_ncw(g, 1, part);
     const uint32_t slot = (uint32_t)(32 * g.task_bytes());
     const uint32_t xb = (uint32_t)align_up((size_t)(g.tpr + XREP) * g.stride, 16);
     int depth = 0;
