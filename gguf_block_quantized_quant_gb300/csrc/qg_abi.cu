@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
 }
 
 // fp16 activation image of the prefill GEMM (see launch_prefill_x16): one thread per 16-byte
-// chunk of the image, in image order (coalesced stores).  Chunk position p of row r of a
-// tile holds the 8 elements of logical chunk p ^ (r & 7) (the 128-byte swizzle).  Launched
-// like prep_tiles_kernel.
-__global__ void __launch_bounds__(256) prefill_x16_kernel(const float *x, int M, int K, int BT, int nkt, long chunks,
+// chunk of the image, in image order (coalesced stores).  Tiles are ordered K tile major,
+// token tile minor; chunk position p of row r of a tile holds the 8 elements of logical chunk
+// p ^ (r & 7) (the 128-byte swizzle).  Launched like prep_tiles_kernel.
+__global__ void __launch_bounds__(256) prefill_x16_kernel(const float *x, int M, int K, int BT, int ntt, long chunks,
                                                           uint4 *img) {
     griddep_launch_dependents();
     griddep_wait();
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(256) prefill_x16_kernel(const float *x, int M,
         const long tile = c / (BT * 8);
         const int within = (int)(c - tile * (BT * 8));
         const int r = within >> 3, pos = within & 7;
-        const int tt = (int)(tile / nkt), kt = (int)(tile - (long)tt * nkt);
+        const int kt = (int)(tile / ntt), tt = (int)(tile - (long)kt * ntt);
         const int m = tt * BT + r, k0 = kt * 64 + 8 * (pos ^ (r & 7));
         float v[8];
 #pragma unroll
@@ -263,7 +263,7 @@ int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t
 int launch_prefill_x16(const float *x, int M, int K, int BT, int ntt, int nkt, uint8_t *img, cudaStream_t s) {
     const long chunks = (long)ntt * nkt * BT * 8;
     const int grid = (int)std::min<long>((chunks + 255) / 256, 4096);
-    return launch_pdl(prefill_x16_kernel, grid, 256, s, x, M, K, BT, nkt, chunks, reinterpret_cast<uint4 *>(img));
+    return launch_pdl(prefill_x16_kernel, grid, 256, s, x, M, K, BT, ntt, chunks, reinterpret_cast<uint4 *>(img));
 }
 
 int launch_router_prep(const float *x, int M, int H, const float *Wr, int E, float *logits, int xgt_log2,

@@ -44,15 +44,6 @@ __device__ __forceinline__ uint4 ldg_u128(const uint8_t *p) { return __ldg(reint
 __device__ __forceinline__ uint32_t ldg_w2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
 
 __device__ __forceinline__ uint32_t byte_at(uint32_t w, int k) { return (w >> (8 * k)) & 255u; }
-// Byte b of a word array; b may be a run-time value (a select chain keeps w in registers).
-template <int NW>
-__device__ __forceinline__ uint32_t byte_of_words(const uint32_t (&w)[NW], int b) {
-    uint32_t word = w[0];
-#pragma unroll
-    for (int i = 1; i < NW; ++i)
-        if ((b >> 2) == i) word = w[i];
-    return byte_at(word, b & 3);
-}
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
@@ -67,6 +58,41 @@ __device__ __forceinline__ int codebook(uint32_t idx) {
     return (int)(int8_t)((idx & 8u) ? hi : lo);
 }
 
+// The NW words at byte address p (2-byte aligned, p + 2 * NB16 the end of the bytes that are
+// needed: NB16 16-bit units) read through the aligned 16-byte chunks that cover them, when
+// those chunks lie below lim (the end of the tensor), and realigned in registers: shifts by
+// 8, 4 and 2 bytes of the offset within the first chunk (MAXO: the largest such offset the
+// caller can have).  Otherwise (a window reaching past the tensor's end) the needed 16-bit
+// units are loaded one by one and the rest of the words are zero.
+template <int NW, int NB16, int MAXO>
+__device__ __forceinline__ void fetch_words(const uint8_t *p, const uint8_t *lim, uint32_t (&out)[NW]) {
+    constexpr int NC = (MAXO + 2 * NB16 + 15) / 16;  // chunks covering the needed bytes at the worst offset
+    const uint8_t *base = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)15);
+    const uint32_t o = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 15u);
+    if (base + 16 * NC <= lim) {
+        uint32_t w[4 * NC + 3];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 v = ldg_u128(base + 16 * c);
+            w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+        w[4 * NC] = w[4 * NC + 1] = w[4 * NC + 2] = 0u;
+#pragma unroll
+        for (int i = 0; i < 4 * NC + 1; ++i) w[i] = (o & 8u) ? w[i + 2] : w[i];
+#pragma unroll
+        for (int i = 0; i < 4 * NC; ++i) w[i] = (o & 4u) ? w[i + 1] : w[i];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], 8u * (o & 2u));
+    } else {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const uint32_t lo = 2 * i < NB16 ? ldg_u16(p + 4 * i) : 0u;
+            const uint32_t hi = 2 * i + 1 < NB16 ? ldg_u16(p + 4 * i + 2) : 0u;
+            out[i] = lo | (hi << 16);
+        }
+    }
+}
+
 // Packs fp32 values v[0..31] into 16 words of two fp16 (round to nearest even).
 __device__ __forceinline__ void pack_f16(const float (&v)[32], uint32_t (&h)[16]) {
 #pragma unroll
@@ -76,16 +102,44 @@ __device__ __forceinline__ void pack_f16(const float (&v)[32], uint32_t (&h)[16]
     }
 }
 
-// Q4_K / Q5_K: 6-bit scale and min of sub-block j from the 12 packed bytes sc (bytes 4..15 of
-// the block, i.e. bytes 0..11 of the 16-byte header words h[1..3]).
-__device__ __forceinline__ void kq_scale_min(const uint32_t (&hdr)[4], int j, int &S, int &M) {
-    auto sc = [&](int b) { return (int)byte_of_words(hdr, 4 + b); };
+// Byte k (k = 0..3) of w as the fp32 value 2^23 + byte: the byte becomes the low mantissa
+// bits of 2^23 (exponent byte 0x4B), so subtracting 2^23 (+ an offset) afterwards is exact.
+constexpr float MAGIC = 8388608.0f;  // 2^23
+__device__ __forceinline__ float byte_magic(uint32_t w, int k) {
+    return __uint_as_float(prmt(w, 0x4B000000u, 0x7440u + (uint32_t)k));
+}
+// Four small unsigned integers held in the bytes of w, minus off, as exact fp32 values.
+__device__ __forceinline__ void bytes4_to_f32(uint32_t w, float off, float *f) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f[k] = byte_magic(w, k) - (MAGIC + off);
+}
+
+// The codebook values of the 8 indices in q (byte b: low nibble = element b of the unit's
+// first half, high nibble = element b of its second half), each plus 128: lo holds elements
+// 0..3 of the first half, hi elements 0..3 of the second half, one per byte.
+__device__ __forceinline__ void codebook8_biased(uint32_t q, uint32_t &lo, uint32_t &hi) {
+    const uint32_t i7 = q & 0x77777777u;
+    const uint32_t pick = ((q >> 1) & 0x44444444u) | 0x32103210u;
+    const uint32_t a0 = prmt(cb4(0), cb4(4), i7), b0 = prmt(cb4(8), cb4(12), i7);
+    const uint32_t a1 = prmt(cb4(0), cb4(4), i7 >> 16), b1 = prmt(cb4(8), cb4(12), i7 >> 16);
+    const uint32_t A = prmt(a0, b0, pick), B = prmt(a1, b1, pick >> 16);
+    lo = prmt(A, B, 0x6420u) ^ 0x80808080u;
+    hi = prmt(A, B, 0x7531u) ^ 0x80808080u;
+}
+
+// Q4_K / Q5_K: 6-bit scale S and min M of sub-block j (0..7) from the 12 packed scale bytes
+// sc[0..11] = the header words h1 (sc 0..3), h2 (sc 4..7), h3 (sc 8..11):
+//   j < 4:  S = sc[j] & 63,                          M = sc[j+4] & 63
+//   j >= 4: S = (sc[j+4] & 15) | (sc[j-4] >> 6) << 4,  M = (sc[j+4] >> 4) | (sc[j] >> 6) << 4
+// (run-time shifts of the words; no array indexing).
+__device__ __forceinline__ void kq_scale_min(uint32_t h1, uint32_t h2, uint32_t h3, int j, int &S, int &M) {
+    const int e = 8 * (j & 3);
     if (j < 4) {
-        S = sc(j) & 63;
-        M = sc(j + 4) & 63;
+        S = (int)((h1 >> e) & 63u);
+        M = (int)((h2 >> e) & 63u);
     } else {
-        S = (sc(j + 4) & 15) | ((sc(j - 4) >> 6) << 4);
-        M = (sc(j + 4) >> 4) | ((sc(j) >> 6) << 4);
+        S = (int)(((h3 >> e) & 15u) | (((h1 >> (e + 6)) & 3u) << 4));
+        M = (int)(((h3 >> (e + 4)) & 15u) | (((h2 >> (e + 6)) & 3u) << 4));
     }
 }
 
@@ -103,20 +157,26 @@ struct DeqLegacy {
     static constexpr int RW = 2 + NQ;                 // w[0] d (| m << 16), w[1] qh, w[2..] codes
     using Raw = uint32_t[RW];
 
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    // the block's words through aligned 16-byte loads of its window (fetch_words), then the
+    // fields: w[0] = d (| m << 16), w[1] = qh, w[2..] = code words
+    static constexpr int NWB = FMT == F_Q8_0 ? 9 : (FMT == F_Q5_0 || FMT == F_Q5_1) ? 6 : 5;  // words used
+    static constexpr int MAXO = FMT == F_Q5_1 ? 8 : FMT == F_Q4_1 ? 12 : 14;
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *lim, Raw &r) {
         const uint8_t *b = row + (size_t)u * BS;
-        if constexpr (FMT == F_Q4_1 || FMT == F_Q5_1) {  // 4- and 8-byte-aligned blocks
-            r[0] = ldg_u32(b);
-            r[1] = FMT == F_Q5_1 ? ldg_u32(b + 4) : 0u;
-            const int qs = FMT == F_Q5_1 ? 8 : 4;
+        uint32_t w[NWB];
+        fetch_words<NWB, BS / 2, MAXO>(b, lim, w);
+        if constexpr (FMT == F_Q4_1 || FMT == F_Q5_1) {  // 4-byte-aligned fields
+            r[0] = w[0];
+            r[1] = FMT == F_Q5_1 ? w[1] : 0u;
+            const int qs = FMT == F_Q5_1 ? 2 : 1;
 #pragma unroll
-            for (int i = 0; i < NQ; ++i) r[2 + i] = ldg_u32(b + qs + 4 * i);
-        } else {  // 2-byte-aligned blocks
-            r[0] = ldg_u16(b);
-            r[1] = FMT == F_Q5_0 ? ldg_w2(b + 2) : 0u;
-            const int qs = FMT == F_Q5_0 ? 6 : 2;
+            for (int i = 0; i < NQ; ++i) r[2 + i] = w[qs + i];
+        } else {  // fields after the 2-byte d: realigned by 16 bits
+            r[0] = w[0] & 0xffffu;
+            r[1] = FMT == F_Q5_0 ? __funnelshift_r(w[0], w[1], 16) : 0u;
+            const int qs = FMT == F_Q5_0 ? 1 : 0;  // word holding the code bytes' first half
 #pragma unroll
-            for (int i = 0; i < NQ; ++i) r[2 + i] = ldg_w2(b + qs + 4 * i);
+            for (int i = 0; i < NQ; ++i) r[2 + i] = __funnelshift_r(w[qs + i], w[qs + i + 1], 16);
         }
     }
 
@@ -124,22 +184,37 @@ struct DeqLegacy {
         const float d = half_lo(r[0]);
         const float m = HAS_M ? half_hi(r[0]) : 0.0f;
         float v[32];
+        // element codes four per word, then exact fp32 values: d * c (one exact product), or
+        // RN(d * c + m) for the additive-min formats
+        auto emit = [&](int e0, uint32_t w, float off) {
+            float f[4];
+            bytes4_to_f32(w, off, f);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            int c;
-            if constexpr (FMT == F_Q8_0) {
-                c = (int)(int8_t)byte_at(r[2 + e / 4], e % 4);
-            } else {
-                const int k = e % 16;
-                const uint32_t byte = byte_at(r[2 + k / 4], k % 4);
-                c = (int)(e < 16 ? (byte & 15u) : (byte >> 4));
-                if constexpr (HAS_QH) c |= (int)((r[1] >> e) & 1u) << 4;
-                if constexpr (FMT == F_Q4_0) c -= 8;
-                if constexpr (FMT == F_Q5_0) c -= 16;
-                if constexpr (FMT == F_IQ4_NL) c = codebook((uint32_t)c);
+            for (int k = 0; k < 4; ++k) v[e0 + k] = HAS_M ? fmaf(d, f[k], m) : d * f[k];
+        };
+        if constexpr (FMT == F_Q8_0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) emit(4 * k, r[2 + k] ^ 0x80808080u, 128.0f);  // int8 + 128
+        } else if constexpr (FMT == F_IQ4_NL) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t lo, hi;  // codebook values + 128 of elements 4k.. and 16 + 4k..
+                codebook8_biased(r[2 + k], lo, hi);
+                emit(4 * k, lo, 128.0f);
+                emit(16 + 4 * k, hi, 128.0f);
             }
-            // d * c is exact in fp32; with the additive min one rounding: RN(d*c + m)
-            v[e] = HAS_M ? fmaf(d, (float)c, m) : d * (float)c;
+        } else {
+            constexpr float OFF = FMT == F_Q4_0 ? 8.0f : FMT == F_Q5_0 ? 16.0f : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t lo = r[2 + k] & 0x0f0f0f0fu, hi = (r[2 + k] >> 4) & 0x0f0f0f0fu;
+                if constexpr (HAS_QH) {  // the fifth bits of elements 4k.. and 16 + 4k..
+                    lo |= ((((r[1] >> (4 * k)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+                    hi |= ((((r[1] >> (16 + 4 * k)) & 15u) * 0x00204081u) & 0x01010101u) << 4;
+                }
+                emit(4 * k, lo, OFF);
+                emit(16 + 4 * k, hi, OFF);
+            }
         }
         pack_f16(v, h);
     }
@@ -156,7 +231,7 @@ template <>
 struct Deq<F_Q2_K> {
     static constexpr int BS = 84, QK = 256, RW = 10;  // sc pair, d|dmin, 8 code words
     using Raw = uint32_t[RW];
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *, Raw &r) {
         const uint8_t *b = row + (size_t)(u / 8) * BS;
         const int v = u % 8, hh = v / 4;
         r[0] = ldg_u16(b + 2 * v);   // scale|min bytes of sub-blocks 2v, 2v + 1
@@ -169,11 +244,17 @@ struct Deq<F_Q2_K> {
         const float d = half_lo(r[1]), dmin = half_hi(r[1]);
         float v[32];
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            const uint32_t sm = byte_at(r[0], l / 16);
-            const int q = (int)((byte_at(r[2 + l / 4], l % 4) >> (2 * j)) & 3u);
-            const float bm = dmin * (float)(sm >> 4);      // exact
-            v[l] = fmaf(d, (float)((int)(sm & 15u) * q), -bm);
+        for (int hh = 0; hh < 2; ++hh) {  // 16-element sub-blocks of the unit
+            const uint32_t sm = byte_at(r[0], hh);
+            const float dS = d * (float)(sm & 15u), bm = dmin * (float)(sm >> 4);  // exact
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float f[4];
+                bytes4_to_f32((r[2 + 4 * hh + k] >> (2 * j)) & 0x03030303u, 0.0f, f);
+                // RN(d * (S q) - dmin * M): the product d S q is exact
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[16 * hh + 4 * k + i] = fmaf(dS, f[i], -bm);
+            }
         }
         pack_f16(v, h);
     }
@@ -183,7 +264,7 @@ template <>
 struct Deq<F_Q3_K> {
     static constexpr int BS = 110, QK = 256, RW = 18;  // 8 hmask, 8 code words, scale bytes, d
     using Raw = uint32_t[RW];
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *, Raw &r) {
         const uint8_t *b = row + (size_t)(u / 8) * BS;
         const int v = u % 8, hh = v / 4;
 #pragma unroll
@@ -197,20 +278,25 @@ struct Deq<F_Q3_K> {
     __device__ __forceinline__ static void convert_u(const Raw &r, int u, uint32_t (&h)[16]) {
         const int v = u % 8, hh = v / 4, j = v % 4;
         const float d = half_lo(r[17]);
-        int scale[2];
+        float vv[32];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < 2; ++s) {  // 16-element sub-blocks 2v + s
             const int i = 2 * v + s;
             const int low4 = (int)(i < 8 ? (byte_at(r[16], s) & 15u) : (byte_at(r[16], s) >> 4));
             const int high2 = (int)((byte_at(r[16], 2 + s) >> (2 * (i / 4))) & 3u);
-            scale[s] = (low4 | (high2 << 4)) - 32;
-        }
-        float vv[32];
+            const float sc = (float)((low4 | (high2 << 4)) - 32);
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            const int q = (int)((byte_at(r[8 + l / 4], l % 4) >> (2 * j)) & 3u);
-            const int hb = (int)((byte_at(r[l / 4], l % 4) >> (4 * hh + j)) & 1u);
-            vv[l] = d * (float)(scale[l / 16] * (q - (hb ? 0 : 4)));
+            for (int k = 0; k < 4; ++k) {
+                // code byte q | hb << 2 in 0..7; the value is q - 4 * (1 - hb) = byte - 4
+                const uint32_t q = (r[8 + 4 * s + k] >> (2 * j)) & 0x03030303u;
+                const uint32_t hb = (r[4 * s + k] >> (4 * hh + j)) & 0x01010101u;
+                float f[4];
+                bytes4_to_f32(q | (hb << 2), 4.0f, f);
+                // the integer code c = scale * (byte - 4) (adding +0 makes a zero +0, as the
+                // integer product is), then d * c
+#pragma unroll
+                for (int e = 0; e < 4; ++e) vv[16 * s + 4 * k + e] = d * fmaf(sc, f[e], 0.0f);
+            }
         }
         pack_f16(vv, h);
     }
@@ -221,7 +307,7 @@ struct DeqKQ {  // Q4_K, Q5_K
     static constexpr bool Q5 = FMT == F_Q5_K;
     static constexpr int BS = Q5 ? 176 : 144, QK = 256, RW = Q5 ? 20 : 12;
     using Raw = uint32_t[RW];  // header (d, dmin, sc12), [qh 32 B], qs 32 B
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *, Raw &r) {
         const uint8_t *b = row + (size_t)(u / 8) * BS;
         const int j = u % 8;
         auto put = [&](int at, uint4 x) { r[at] = x.x; r[at + 1] = x.y; r[at + 2] = x.z; r[at + 3] = x.w; };
@@ -236,17 +322,19 @@ struct DeqKQ {  // Q4_K, Q5_K
     }
     __device__ __forceinline__ static void convert_u(const Raw &r, int u, uint32_t (&h)[16]) {
         const int j = u % 8;
-        uint32_t hdr[4] = {r[0], r[1], r[2], r[3]};
         int S, M;
-        kq_scale_min(hdr, j, S, M);
+        kq_scale_min(r[1], r[2], r[3], j, S, M);
         const float A = half_lo(r[0]) * (float)S, Bm = half_hi(r[0]) * (float)M;  // exact
+        const int sh = 4 * (j & 1);
         float v[32];
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            const uint32_t byte = byte_at(r[4 + l / 4], l % 4);
-            int c = (int)((j & 1) ? (byte >> 4) : (byte & 15u));
-            if constexpr (Q5) c += 16 * (int)((byte_at(r[12 + l / 4], l % 4) >> j) & 1u);
-            v[l] = fmaf(A, (float)c, -Bm);
+        for (int k = 0; k < 8; ++k) {
+            uint32_t c = (r[4 + k] >> sh) & 0x0f0f0f0fu;
+            if constexpr (Q5) c |= ((r[12 + k] >> j) & 0x01010101u) << 4;
+            float f[4];
+            bytes4_to_f32(c, 0.0f, f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[4 * k + i] = fmaf(A, f[i], -Bm);
         }
         pack_f16(v, h);
     }
@@ -258,7 +346,7 @@ template <>
 struct Deq<F_Q6_K> {
     static constexpr int BS = 210, QK = 256, RW = 18;  // 8 ql words, 8 qh words, sc pair, d
     using Raw = uint32_t[RW];
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *, Raw &r) {
         const uint8_t *b = row + (size_t)(u / 8) * BS;
         const int v = u % 8, hh = v / 4, t = v % 4;
 #pragma unroll
@@ -273,12 +361,19 @@ struct Deq<F_Q6_K> {
         const float d = half_lo(r[17]);
         float v[32];
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            const uint32_t lb = byte_at(r[l / 4], l % 4);
-            const int low4 = (int)(t < 2 ? (lb & 15u) : (lb >> 4));
-            const int hi2 = (int)((byte_at(r[8 + l / 4], l % 4) >> (2 * t)) & 3u);
-            const int sc = (int)(int8_t)byte_at(r[16], l / 16);
-            v[l] = d * (float)(sc * ((low4 | (hi2 << 4)) - 32));  // exact
+        for (int hh = 0; hh < 2; ++hh) {  // 16-element sub-blocks: their int8 scales
+            const float sc = (float)(int)(int8_t)byte_at(r[16], hh);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t lw = r[4 * hh + k], qw = r[8 + 4 * hh + k];
+                const uint32_t q6 = ((t < 2 ? lw : (lw >> 4)) & 0x0f0f0f0fu) | (((qw >> (2 * t)) & 0x03030303u) << 4);
+                float f[4];
+                bytes4_to_f32(q6, 32.0f, f);
+                // the integer code c = sc * (q6 - 32) (a zero made +0, as the integer product
+                // is), then d * c: both products exact
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[16 * hh + 4 * k + i] = d * fmaf(sc, f[i], 0.0f);
+            }
         }
         pack_f16(v, h);
     }
@@ -288,7 +383,7 @@ template <>
 struct Deq<F_IQ4_XS> {
     static constexpr int BS = 136, QK = 256, RW = 6;  // d | scales_h, scales_l, 4 index words
     using Raw = uint32_t[RW];
-    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, Raw &r) {
+    __device__ __forceinline__ static void fetch(const uint8_t *row, int u, const uint8_t *, Raw &r) {
         const uint8_t *b = row + (size_t)(u / 8) * BS;
         const int ib = u % 8;
         r[0] = ldg_u32(b);
@@ -302,10 +397,16 @@ struct Deq<F_IQ4_XS> {
         const float A = half_lo(r[0]) * (float)(ls - 32);  // exact
         float v[32];
 #pragma unroll
-        for (int l = 0; l < 32; ++l) {
-            const int k = l % 16;
-            const uint32_t byte = byte_at(r[2 + k / 4], k % 4);
-            v[l] = A * (float)codebook(l < 16 ? (byte & 15u) : (byte >> 4));
+        for (int k = 0; k < 4; ++k) {
+            uint32_t lo, hi;
+            codebook8_biased(r[2 + k], lo, hi);
+            float f[4];
+            bytes4_to_f32(lo, 128.0f, f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[4 * k + i] = A * f[i];
+            bytes4_to_f32(hi, 128.0f, f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[16 + 4 * k + i] = A * f[i];
         }
         pack_f16(v, h);
     }

@@ -543,6 +543,8 @@ int prefill_run(const PrefillCall &c, int sms) {
     a.K = c.K;
     a.M = c.M;
     a.BT = p.BT;
+    a.NT = p.NT;
+    a.ntt = p.ntt;
     a.nkt = p.nkt;
     a.ktps = p.ktps;
     a.stages = p.stages;
@@ -551,7 +553,7 @@ int prefill_run(const PrefillCall &c, int sms) {
     a.ximg = ximg;
     a.out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.nn, (unsigned)p.ntt, (unsigned)p.KS);
+    cfg.gridDim = dim3((unsigned)p.nn, (unsigned)p.ngrp, (unsigned)p.KS);
     cfg.blockDim = dim3(PF_THREADS);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = c.stream;

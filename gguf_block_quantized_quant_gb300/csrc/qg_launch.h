@@ -99,9 +99,9 @@ int launch_splitk_reduce(const float *part, int KS, long MN, float *y, cudaStrea
 int launch_prep_tiles(const float *x, const float *u, float *h_out, const int8_t *xq, const float *xd,
                       const int32_t *xs, int rows, int K, int xgt_log2, uint8_t *img, int8_t *mq, float *md,
                       int32_t *ms, cudaStream_t s);
-// fp16 activation image of the prefill GEMM: M x K fp32 rows -> ntt tiles of BT tokens x nkt
-// tiles of 64 elements, each BT x 128 bytes in the tensor cores' K-major 128-byte-swizzled
-// layout (rows past M and elements past K are zero).
+// fp16 activation image of the prefill GEMM: M x K fp32 rows -> nkt tiles of 64 elements x
+// ntt tiles of BT tokens (K tile major), each BT x 128 bytes in the tensor cores' K-major
+// 128-byte-swizzled layout (rows past M and elements past K are zero).
 int launch_prefill_x16(const float *x, int M, int K, int BT, int ntt, int nkt, uint8_t *img, cudaStream_t s);
 // Router logits (fp32) and the activation tile image of x (s16: two planes per row) in one
 // launch.

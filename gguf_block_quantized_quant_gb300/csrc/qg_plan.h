@@ -432,14 +432,16 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, 
 }
 
 // ----------------------------------------------------------------------------- prefill GEMM
-// Tiles of 128 weight rows x BT tokens (BT = 256, or M rounded up to 16 when M < 256) over
-// K-slices of whole 64-element K tiles.  The slice count KS minimises an estimate of the
-// critical path in K-tile times: (waves of CTAs over the SMs) x (K tiles per CTA), plus for
-// KS > 1 the partial sums' traffic (KS x M x N x 8 bytes at about 6 TB/s) in K-tile times
-// (one K tile of one CTA is 2 x 128 x BT x 64 flops at 1/SM of about 1.8 PFLOP/s).
+// Tiles of 128 weight rows x NT token tiles of BT tokens (BT = 256, or M rounded up to 16 when
+// M < 256; NT = 1 or 2) over K-slices of whole 64-element K tiles.  NT and the slice count KS
+// minimise an estimate of the critical path in K-tile times of one token tile: (waves of CTAs
+// over the SMs) x (K tiles per CTA) x max(NT, 1.5) -- a K tile's dequantization costs about
+// 1.5 MMA steps of one token tile and overlaps them -- plus for KS > 1 the partial sums'
+// traffic (KS x M x N x 8 bytes at about 6 TB/s; one K-tile time is 2 x 128 x BT x 64 flops
+// at 1/SM of about 1.8 PFLOP/s).
 struct PrefillPlan {
     bool ok = false;
-    int BT = 0, ntt = 0, nn = 0, nkt = 0, KS = 1, ktps = 0, stages = 0, tmem_cols = 0;
+    int BT = 0, NT = 1, ntt = 0, ngrp = 0, nn = 0, nkt = 0, KS = 1, ktps = 0, stages = 0, tmem_cols = 0;
     uint32_t rb = 0, smem = 0, idesc = 0;
     size_t ws_ximg = 0, ws_part = 0, ws_total = 0;
 };
@@ -458,26 +460,31 @@ inline PrefillPlan plan_prefill(int fmt, int N, int K, int M, int sms) {
     const double ktile_s = 2.0 * PF_BM * p.BT * PF_BK * sms / 1.8e15;
     const double part_s = (double)M * N * 8.0 / 6.0e12;
     double best = 1e300;
-    for (int ks = 1; ks <= 16 && ks <= p.nkt; ++ks) {
-        const int ktps = (p.nkt + ks - 1) / ks;
-        const int kse = (p.nkt + ktps - 1) / ktps;  // slices that are not empty
-        if (kse != ks) continue;
-        if (ks > 1 && ktps < 4) break;
-        const long ctas = (long)p.nn * p.ntt * ks;
-        const long waves = (ctas + sms - 1) / sms;
-        const double cost = (double)waves * ktps + (ks > 1 ? ks * part_s / ktile_s : 0.0);
-        if (cost < best - 1e-9) {
-            best = cost;
-            p.KS = ks;
-            p.ktps = ktps;
+    for (int nt = 1; nt <= 2 && nt <= p.ntt; ++nt) {
+        const int ngrp = (p.ntt + nt - 1) / nt;
+        for (int ks = 1; ks <= 16 && ks <= p.nkt; ++ks) {
+            const int ktps = (p.nkt + ks - 1) / ks;
+            const int kse = (p.nkt + ktps - 1) / ktps;  // slices that are not empty
+            if (kse != ks) continue;
+            if (ks > 1 && ktps < 4) break;
+            const long ctas = (long)p.nn * ngrp * ks;
+            const long waves = (ctas + sms - 1) / sms;
+            const double cost = (double)waves * ktps * std::max(1.5, (double)nt) + (ks > 1 ? ks * part_s / ktile_s : 0.0);
+            if (cost < best - 1e-9) {
+                best = cost;
+                p.NT = nt;
+                p.KS = ks;
+                p.ktps = ktps;
+            }
         }
     }
     if (p.ktps < 1) return p;
+    p.ngrp = (p.ntt + p.NT - 1) / p.NT;
     p.stages = 4;
-    while (p.stages > 2 && prefill_smem_bytes(p.BT, p.stages) > (uint32_t)SMEM_MAX) --p.stages;
-    p.smem = prefill_smem_bytes(p.BT, p.stages);
+    while (p.stages > 2 && prefill_smem_bytes(p.BT, p.NT, p.stages) > (uint32_t)SMEM_MAX) --p.stages;
+    p.smem = prefill_smem_bytes(p.BT, p.NT, p.stages);
     if (p.smem > (uint32_t)SMEM_MAX || !umma_shape_ok(PF_BM, p.BT)) return p;
-    p.tmem_cols = tmem_cols_for(p.BT);
+    p.tmem_cols = tmem_cols_for(p.NT * p.BT);
     p.idesc = umma_idesc_f16(PF_BM, p.BT);
     size_t o = 0;
     p.ws_ximg = o;

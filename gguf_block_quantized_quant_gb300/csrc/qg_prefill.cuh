@@ -8,16 +8,19 @@
 // with w formed per 32-element unit as in qg_dequant.cuh and x rounded to fp16 by a small
 // preparation kernel that writes the activation tiles in the tensor cores' operand layout.
 //
-// One CTA computes a tile of 128 weight rows x BT tokens (BT <= 256) over a range of K:
+// One CTA computes a tile of 128 weight rows x NT token tiles of BT tokens (BT <= 256, NT 1
+// or 2: each dequantized weight tile then serves up to 512 tokens) over a range of K:
 //   * warps 0-7 (dequant): thread t owns row t % 128 and, per K step of 64, the unit t / 128
 //     (32 elements); it fetches the raw words of the unit two steps ahead, converts them to
 //     fp16 and stores them as four 16-byte chunks of the swizzled weight tile of the stage;
 //   * warp 8 lane 0 (producer): one 1-D bulk copy per stage of the activation tile
-//     (BT rows x 128 bytes, laid out by the preparation kernel exactly as it must sit in
-//     shared memory); warp 8 also allocates and frees the tensor memory;
-//   * warp 9 lane 0 (MMA): per stage, four tcgen05.mma of M = 128, N = BT, K = 16 into one
-//     fp32 accumulator in tensor memory (128 lanes x BT columns), then tcgen05.commit to the
-//     stage's "empty" barrier, which frees the stage for both producers;
+//     (NT tiles of BT rows x 128 bytes, adjacent in the image and laid out by the preparation
+//     kernel exactly as they must sit in shared memory); warp 8 also allocates and frees the
+//     tensor memory;
+//   * warp 9 lane 0 (MMA): per stage and token tile, four tcgen05.mma of M = 128, N = BT,
+//     K = 16 into that tile's fp32 accumulator in tensor memory (128 lanes x BT columns each),
+//     then tcgen05.commit to the stage's "empty" barrier, which frees the stage for both
+//     producers;
 //   * after the last stage the MMA thread commits to "done"; warps 0-7 read the accumulator
 //     with tcgen05.ld (warp w: lanes 32 (w % 4) .., half of the columns) and write y (or a
 //     K-slice's partial sums, added by the split-K reduction).
@@ -38,19 +41,23 @@ struct PrefillArgs {
     const uint8_t *W;
     uint32_t rb;          // bytes per weight row
     int N, K, M;
-    int BT;               // tokens per CTA (MMA N): a multiple of 16, at most 256
+    int BT;               // tokens per token tile (MMA N): a multiple of 16, at most 256
+    int NT;               // token tiles per CTA (1 or 2)
+    int ntt;              // token tiles of the whole batch
     int nkt;              // K tiles of 64 (the last one zero-padded when K % 64 == 32)
     int ktps;             // K tiles per K-slice (blockIdx.z)
     int stages;
     int tmem_cols;
     uint32_t idesc;
-    const uint8_t *ximg;  // [token tile][K tile][BT x 128 bytes]
+    const uint8_t *ximg;  // [K tile][token tile][BT x 128 bytes]
     float *out;           // y, or partials [KS][M][N]
 };
 
-__host__ __device__ constexpr uint32_t prefill_stage_bytes(int BT) { return (uint32_t)(PF_BM * 128 + BT * 128); }
-__host__ __device__ constexpr uint32_t prefill_smem_bytes(int BT, int stages) {
-    return (uint32_t)stages * prefill_stage_bytes(BT) + UMMA_ATOM_BYTES /* alignment slack */ +
+__host__ __device__ constexpr uint32_t prefill_stage_bytes(int BT, int NT) {
+    return (uint32_t)(PF_BM * 128 + NT * BT * 128);
+}
+__host__ __device__ constexpr uint32_t prefill_smem_bytes(int BT, int NT, int stages) {
+    return (uint32_t)stages * prefill_stage_bytes(BT, NT) + UMMA_ATOM_BYTES /* alignment slack */ +
            8u * (uint32_t)(3 * stages + 1) + 16u;
 }
 
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
     extern __shared__ __align__(16) uint8_t pf_smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.stages;
-    const uint32_t wtile = PF_BM * 128, xtile = (uint32_t)a.BT * 128;
+    const uint32_t wtile = PF_BM * 128, ttile = (uint32_t)a.BT * 128, xtile = (uint32_t)a.NT * ttile;
     const uint32_t base = (smem_addr(pf_smem) + (UMMA_ATOM_BYTES - 1)) & ~(UMMA_ATOM_BYTES - 1);
     const uint32_t wt0 = base, xt0 = base + (uint32_t)S * wtile;
     const uint32_t bars = xt0 + (uint32_t)S * xtile;
@@ -113,7 +120,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
     const uint32_t done = bars + 8u * (uint32_t)(3 * S);
     const uint32_t taddr_slot = done + 8u;
 
-    const int n0 = (int)blockIdx.x * PF_BM, tt = (int)blockIdx.y, ks = (int)blockIdx.z;
+    const int n0 = (int)blockIdx.x * PF_BM, tt0 = (int)blockIdx.y * a.NT, ks = (int)blockIdx.z;
+    const int ntc = min(a.NT, a.ntt - tt0);  // token tiles of this CTA
     const int kt0 = ks * a.ktps;
     const int nk = min(a.nkt, kt0 + a.ktps) - kt0;  // >= 1 by the plan
 
@@ -142,11 +150,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
         const int n = n0 + r;
         const bool row_ok = n < a.N;
         const uint8_t *row = a.W + (size_t)(row_ok ? n : 0) * a.rb;
+        const uint8_t *lim = a.W + (size_t)a.N * a.rb;  // end of the tensor
         const int nunits = a.K / 32;
         typename D::Raw raw[PF_LOOKAHEAD + 1];
         auto fetch = [&](int i, typename D::Raw &rw) {
             const int u = 2 * (kt0 + i) + hsel;
-            if (row_ok && i < nk && u < nunits) D::fetch(row, u, rw);
+            if (row_ok && i < nk && u < nunits) D::fetch(row, u, lim, rw);
         };
 #pragma unroll
         for (int p = 0; p < PF_LOOKAHEAD; ++p) fetch(p, raw[p]);
@@ -178,12 +187,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
     } else if (warp == PF_DEQ_WARPS) {
         // ------------------------------------------------------------ activation producer
         if (lane == 0) {
-            const uint8_t *src = a.ximg + ((size_t)tt * a.nkt + kt0) * xtile;
+            const uint32_t bytes = (uint32_t)ntc * ttile;
             for (int i = 0; i < nk; ++i) {
                 const int s = i % S;
                 if (i >= S) mbar_wait(empty(s), (uint32_t)((i / S - 1) & 1));
-                mbar_arrive_expect_tx(xfull(s), xtile);
-                bulk_g2s(xt0 + (uint32_t)s * xtile, src + (size_t)i * xtile, xtile, xfull(s));
+                mbar_arrive_expect_tx(xfull(s), bytes);
+                bulk_g2s(xt0 + (uint32_t)s * xtile, a.ximg + ((size_t)(kt0 + i) * a.ntt + tt0) * ttile, bytes,
+                         xfull(s));
             }
         }
     } else {
@@ -196,10 +206,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
                 mbar_wait(xfull(s), ph);
                 tc_fence_after();
                 const uint64_t ad = umma_desc_kmajor_sw128(wt0 + (uint32_t)s * wtile);
-                const uint64_t bd = umma_desc_kmajor_sw128(xt0 + (uint32_t)s * xtile);
+                for (int t = 0; t < ntc; ++t) {
+                    const uint64_t bd = umma_desc_kmajor_sw128(xt0 + (uint32_t)s * xtile + (uint32_t)t * ttile);
 #pragma unroll
-                for (int kk = 0; kk < PF_BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the row
-                    umma_f16(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), a.idesc, (i | kk) != 0);
+                    for (int kk = 0; kk < PF_BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the row
+                        umma_f16(tmem + (uint32_t)(t * a.BT), ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
+                                 a.idesc, (i | kk) != 0);
+                }
                 umma_commit(empty(s));
             }
             umma_commit(done);
@@ -211,8 +224,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
         mbar_wait(done, 0);
         tc_fence_after();
         const int q = warp & 3, hf = warp >> 2;
-        const int split = ((a.BT / 2 + 15) / 16) * 16;
-        const int c0 = hf ? split : 0, c1 = hf ? a.BT : split;
+        const int cols = ntc * a.BT;  // token columns of the CTA's accumulators
+        const int split = ((cols / 2 + 15) / 16) * 16;
+        const int c0 = hf ? split : 0, c1 = hf ? cols : split;
         const int n = n0 + 32 * q + lane;
         float *out = a.out + (size_t)ks * a.M * a.N;
         for (int c = c0; c < c1; c += 16) {
@@ -221,7 +235,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
             if (n < a.N) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int m = tt * a.BT + c + j;
+                    const int m = tt0 * a.BT + c + j;
                     if (m < a.M) out[(size_t)m * a.N + n] = __uint_as_float(v[j]);
                 }
             }
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(256) dequant_f16_kernel(const uint8_t *W, uint
     for (long t = (long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (long)gridDim.x * blockDim.x) {
         const int n = (int)(t / nu), u = (int)(t % nu);
         typename D::Raw raw;
-        D::fetch(W + (size_t)n * rb, u, raw);
+        D::fetch(W + (size_t)n * rb, u, W + (size_t)N * rb, raw);
         uint32_t h[16];
         deq_convert<FMT>(raw, u, h);
         uint32_t *o = reinterpret_cast<uint32_t *>(out + (size_t)n * K + 32 * u);

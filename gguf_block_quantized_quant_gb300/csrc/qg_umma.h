@@ -51,11 +51,14 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t k) {
 }
 
 // Shapes the prefill GEMM issues: M = 128 rows per CTA (cta_group::1); N a multiple of 16 up
-// to 256; K = 16 per instruction; TMEM columns: the power of two >= N, at least 32.
+// to 256; K = 16 per instruction; TMEM columns: the power of two >= the CTA's accumulator
+// columns (up to two accumulators of N), at least 32.
 constexpr int PF_BM = 128;
 constexpr int PF_BK = 64;
 constexpr int PF_MAX_BT = 256;
 __host__ __device__ constexpr bool umma_shape_ok(int M, int N) { return M == 128 && N >= 16 && N <= 256 && N % 16 == 0; }
-__host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+__host__ __device__ constexpr int tmem_cols_for(int n) {
+    return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
 
 }  // namespace qg

@@ -95,18 +95,11 @@ static std::vector<Rd> fetch_reads(int fmt, int u) {
     fmt_info(fmt, f);
     auto add = [&](long off, int size, int align) { v.push_back({off, size, align}); };
     if (f.qk == 32) {
+        // legacy blocks: read by fetch_words through the aligned 16-byte chunks covering the
+        // block (checked separately, check_legacy_windows); the slow path near the tensor's
+        // end reads the block's own 16-bit units
         const long b = (long)u * f.bs;
-        if (fmt == 3 || fmt == 7) {  // Q4_1, Q5_1: 32-bit loads
-            add(b, 4, 4);
-            if (fmt == 7) add(b + 4, 4, 4);
-            const int qs = fmt == 7 ? 8 : 4, nq = 4;
-            for (int i = 0; i < nq; ++i) add(b + qs + 4 * i, 4, 4);
-        } else {  // 16-bit loads
-            add(b, 2, 2);
-            if (fmt == 6) add(b + 2, 4, 2);
-            const int qs = fmt == 6 ? 6 : 2, nq = fmt == 8 ? 8 : 4;
-            for (int i = 0; i < nq; ++i) add(b + qs + 4 * i, 4, 2);
-        }
+        for (int i = 0; i < f.bs / 2; ++i) add(b + 2 * i, 2, 2);
         return v;
     }
     const long b = (long)(u / 8) * f.bs;
@@ -170,45 +163,77 @@ static void check_fetches(int fmt, int K) {
         }
 }
 
+// fetch_words of the 32-element block formats over a tensor of N rows: the covering window
+// of NC chunks (MAXO = the largest offset of a block within its first chunk) holds every byte
+// of the block, and is only read when it lies inside the tensor.
+static void check_legacy_windows(int fmt, int K, int N) {
+    FmtInfo f;
+    fmt_info(fmt, f);
+    if (f.qk != 32) return;
+    const int maxo = fmt == 7 ? 8 : fmt == 3 ? 12 : 14;
+    const int nc = (maxo + f.bs + 15) / 16;
+    const long rb = (long)(K / 32) * f.bs, end = (long)N * rb;
+    for (int n = 0; n < N; ++n)
+        for (int u = 0; u < K / 32; ++u) {
+            const long p = (long)n * rb + (long)u * f.bs;  // tensor offsets (the tensor is 16-byte aligned)
+            const long base = p & ~15L, o = p - base;
+            CHECK(p % 2 == 0, "fmt %d block offset %ld odd", fmt, p);
+            CHECK(o <= maxo, "fmt %d K %d block offset %ld in its chunk > %d", fmt, K, o, maxo);
+            CHECK(o + f.bs <= 16L * nc, "fmt %d window of %d chunks misses block bytes", fmt, nc);
+            if (base + 16L * nc <= end) CHECK(base >= 0 && base % 16 == 0, "fmt %d window", fmt);
+        }
+}
+
 static void check_plan(int fmt, int N, int K, int M, int sms) {
     const PrefillPlan p = plan_prefill(fmt, N, K, M, sms);
     CHECK(p.ok, "plan fmt %d N %d K %d M %d not ok", fmt, N, K, M);
     if (!p.ok) return;
     CHECK(p.BT % 16 == 0 && p.BT >= 16 && p.BT <= 256 && umma_shape_ok(PF_BM, p.BT), "BT %d", p.BT);
     CHECK(p.BT >= 256 || p.BT >= M, "BT %d < M %d", p.BT, M);
-    CHECK(p.tmem_cols >= p.BT && p.tmem_cols <= 256, "tmem cols %d", p.tmem_cols);
+    CHECK(p.NT >= 1 && p.NT <= 2 && p.NT <= p.ntt && p.ngrp == (p.ntt + p.NT - 1) / p.NT, "NT %d ngrp %d", p.NT, p.ngrp);
+    CHECK(p.tmem_cols >= p.NT * p.BT && p.tmem_cols <= 512 && (p.tmem_cols & (p.tmem_cols - 1)) == 0, "tmem cols %d",
+          p.tmem_cols);
     CHECK(p.idesc == umma_idesc_f16(PF_BM, p.BT), "idesc");
     CHECK(p.stages >= 2 && p.smem <= (uint32_t)SMEM_MAX, "stages %d smem %u", p.stages, p.smem);
     // the kernel's layout inside its dynamic shared memory (worst-case alignment slack)
-    const uint32_t used = (UMMA_ATOM_BYTES - 16) + (uint32_t)p.stages * prefill_stage_bytes(p.BT) +
+    const uint32_t used = (UMMA_ATOM_BYTES - 16) + (uint32_t)p.stages * prefill_stage_bytes(p.BT, p.NT) +
                           8u * (uint32_t)(3 * p.stages) + 8u + 4u;
     CHECK(used <= p.smem, "smem layout %u > %u", used, p.smem);
-    CHECK(prefill_stage_bytes(p.BT) % UMMA_ATOM_BYTES == 0, "tiles keep 1024-byte alignment");
-    CHECK((p.BT * 128) % 16 == 0, "copy size");
+    CHECK(prefill_stage_bytes(p.BT, p.NT) % UMMA_ATOM_BYTES == 0 && (p.BT * 128) % UMMA_ATOM_BYTES == 0,
+          "tiles keep 1024-byte alignment");
     CHECK(p.nn == (N + 127) / 128 && p.ntt == (M + p.BT - 1) / p.BT && p.nkt == (K + 63) / 64, "grid");
-    CHECK(p.ntt <= 65535 && p.KS <= 65535, "grid y/z");
+    CHECK(p.ngrp <= 65535 && p.KS <= 65535, "grid y/z");
     CHECK(p.KS >= 1 && p.ktps >= 1 && (long)p.KS * p.ktps >= p.nkt && (long)(p.KS - 1) * p.ktps < p.nkt,
           "slices KS %d ktps %d nkt %d", p.KS, p.ktps, p.nkt);
     const size_t img = (size_t)p.ntt * p.nkt * p.BT * 128;
     CHECK(p.ws_ximg + img <= p.ws_total, "image in workspace");
     if (p.KS > 1) CHECK(p.ws_part >= p.ws_ximg + img && p.ws_part + 4ull * p.KS * M * N <= p.ws_total, "partials");
     CHECK(p.ws_ximg % 256 == 0 && p.ws_part % 16 == 0, "workspace alignment");
-    // every CTA: its copies and its outputs
+    // every CTA: its copies (K tile major image: a stage copies the CTA's ntc adjacent token
+    // tiles of one K tile) and its outputs
     for (int ks = 0; ks < p.KS; ++ks) {
         const int kt0 = ks * p.ktps, nk = std::min(p.nkt, kt0 + p.ktps) - kt0;
         CHECK(nk >= 1, "empty slice");
-        for (int tt = 0; tt < p.ntt; ++tt) {
-            const size_t first = ((size_t)tt * p.nkt + kt0) * p.BT * 128;
-            const size_t last_end = first + (size_t)nk * p.BT * 128;
-            CHECK(last_end <= img, "activation copies of CTA (tt %d, ks %d) end at %zu > %zu", tt, ks, last_end, img);
-            const long m_hi = std::min<long>(M, (long)(tt + 1) * p.BT) - 1;
+        for (int gy = 0; gy < p.ngrp; ++gy) {
+            const int tt0 = gy * p.NT, ntc = std::min(p.NT, p.ntt - tt0);
+            CHECK(ntc >= 1, "empty token group");
+            for (int i = 0; i < nk; ++i) {
+                const size_t off = ((size_t)(kt0 + i) * p.ntt + tt0) * p.BT * 128, bytes = (size_t)ntc * p.BT * 128;
+                CHECK(off + bytes <= img && bytes <= (size_t)p.NT * p.BT * 128, "activation copy of CTA (%d, %d) stage %d",
+                      gy, ks, i);
+            }
+            const long m_hi = std::min<long>(M, (long)(tt0 + ntc) * p.BT) - 1;
             const size_t out_hi = (size_t)ks * M * N + (size_t)m_hi * N + (N - 1);
             CHECK(out_hi < (size_t)(p.KS > 1 ? p.KS : 1) * M * N, "output index");
+            // accumulator columns: ntc tiles of BT columns inside the allocation
+            CHECK(ntc * p.BT <= p.tmem_cols, "accumulator columns");
         }
     }
-    // the epilogue's column split: multiples of 16 covering [0, BT)
-    const int split = ((p.BT / 2 + 15) / 16) * 16;
-    CHECK(split % 16 == 0 && split <= p.BT && (p.BT - split) % 16 == 0, "epilogue split %d of %d", split, p.BT);
+    // the epilogue's column split: multiples of 16 covering [0, ntc * BT)
+    for (int ntc = 1; ntc <= p.NT; ++ntc) {
+        const int cols = ntc * p.BT, split = ((cols / 2 + 15) / 16) * 16;
+        CHECK(split % 16 == 0 && split <= cols && (cols - split) % 16 == 0, "epilogue split %d of %d", split, cols);
+    }
 }
 
 int main() {
@@ -219,8 +244,10 @@ int main() {
     for (int fmt : fmts) {
         FmtInfo f;
         fmt_info(fmt, f);
-        for (int K : {f.qk, 2 * f.qk, 3 * f.qk, 1024, 2048, 4096, 5120, 17408, 96 * f.qk})
+        for (int K : {f.qk, 2 * f.qk, 3 * f.qk, 1024, 2048, 4096, 5120, 17408, 96 * f.qk}) {
             check_fetches(fmt, K);
+            for (int N : {1, 2, 3, 7}) check_legacy_windows(fmt, K, N);
+        }
         for (int K : {f.qk, 3 * f.qk, 1024, 5120, 17408})
             for (int N : {1, 5, 128, 129, 300, 5120, 17408})
                 for (int M : {1, 2, 15, 16, 17, 100, 255, 256, 257, 512, 1000, 2048})

@@ -80,3 +80,22 @@ def test_prefill_rejects_bad_arguments(qg):
     with pytest.raises(qg.QGError) as e:
         qg.qg_prefill_gemm(synth.Q4_K, W, x, 4, ws=torch.zeros(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == qg.QG_EWORKSPACE
+
+
+GROUPS = [(synth.Q4_K, 400), (synth.Q4_0, 600), (synth.Q6_K, 600)]
+
+
+@pytest.mark.parametrize("fmt,M", GROUPS, ids=[f"{synth.FORMAT_NAMES[f]}-M{m}" for f, m in GROUPS])
+def test_prefill_two_token_tiles_per_cta(qg, fmt, M):
+    """Shapes whose plan gives every CTA two token tiles of 256 (two accumulators): M = 400
+    (the second tile ragged) and M = 600 (the last CTA group holding one tile of 88)."""
+    N, K = 17408, 1024
+    g = np.random.default_rng(7000 + M + fmt)
+    W = synth.weights(fmt, N, K, g)
+    x = synth.activations(M, K, g)
+    y = host(qg.qg_prefill_gemm(fmt, dev(W), dev(x), N))
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 28)]))
+    rb = synth.row_bytes(fmt, K)
+    y_ref, sabs = oracle.prefill_gemm(fmt, np.ascontiguousarray(W.reshape(N, rb)[rows]), x, len(rows), K)
+    assert_within(y[:, rows], y_ref, sabs, f"prefill {synth.FORMAT_NAMES[fmt]} {N}x{K} M={M}")
+    assert qg.qg_device_error() == 0
