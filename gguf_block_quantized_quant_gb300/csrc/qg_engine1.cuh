@@ -142,3 +142,155 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
 }
 
 }  // namespace qg
+
+namespace qg {
+
+// The FFN sublayer's gate and up projections at one token with SwiGLU and the
+// requantization of h in the epilogue ("为什么专家缓存救不了稠密模型", "原位量化计算与单流
+// 融合的实际收益": the sublayer on one stream).  A CTA owns whole units of 32 positions j of
+// the intermediate (rows 32 u .. 32 u + 31 of Wg and of Wu): its gate rows and its up rows
+// are two contiguous byte ranges, consumed as in engine1_kernel (a stage that crosses from
+// the gate range to the up range is two bulk copies).  After the last stage the CTA adds
+// each row's partial sums in task order (g and u), forms h = silu(g) u, quantizes every
+// unit of h as one activation block and writes it into the down projection's tile image,
+// so the down GEMV needs no preparation kernel; g, u and h also go to the workspace.
+struct FfnGateUp1Args {
+    const uint8_t *Wg, *Wu;  // I rows of rb bytes each
+    const uint8_t *ximg;     // activation tile image of x: tpr tiles
+    float *g_out, *u_out, *h_out;
+    uint8_t *himg;           // the down projection's tile image (one row)
+    int I, tpr, depth, xrep, himg_tpr, himg_xgt_log2;
+    uint32_t rb, slot_bytes, x_bytes;
+};
+
+// partial sums of a CTA with nu units: 2 * 32 * nu rows of tpr tasks, then 2 * 32 * nu row sums
+__host__ __device__ constexpr int ffn1_part_floats(int nu, int tpr) { return 64 * nu * tpr + 64 * nu; }
+
+template <int FMT, int T, int NCW>
+__global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateUp1Args a) {
+    using F = FT<FMT, T>;
+    using TL = Tile<F::XGT>;
+    constexpr uint32_t TB = F::TASK_BYTES;
+    static_assert(TB % 16 == 0, "stages are aligned bulk copies");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int D = a.depth, S = NCW * D;
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t xa = ring + (uint32_t)S * a.slot_bytes;
+    float *part = reinterpret_cast<float *>(smem + (uint32_t)S * a.slot_bytes + a.x_bytes);
+    const int U = a.I / 32;
+    const int u0 = split_point(U, (int)blockIdx.x, (int)gridDim.x);
+    const int u1 = split_point(U, (int)blockIdx.x + 1, (int)gridDim.x);
+    const int nu = u1 - u0, nr = 32 * nu, tpr = a.tpr;
+    const int G = nr * tpr, ntask = 2 * G;  // gate tasks [0, G), up tasks [G, 2G)
+    float *rsum = part + ntask;             // row sums: gate rows, then up rows
+    const uint32_t bars = smem_addr(part + ffn1_part_floats(nu, tpr));
+    const uint32_t bars8 = (bars + 7u) & ~7u;
+    auto full_bar = [&](int s) { return bars8 + 8u * (uint32_t)s; };
+    const uint32_t xbar = bars8 + 8u * (uint32_t)S;
+    const uint8_t *gbase = a.Wg + (size_t)(32 * u0) * a.rb, *ubase = a.Wu + (size_t)(32 * u0) * a.rb;
+
+    griddep_launch_dependents();
+    if (lane == 0) {
+        for (int j = 0; j < D; ++j) mbar_init(full_bar(j * NCW + warp), 1);
+        if (warp == 0) mbar_init(xbar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int wa = split_point(ntask, warp, NCW), wb = split_point(ntask, warp + 1, NCW);
+    const int nst = (wb - wa + 31) / 32;
+
+    auto issue = [&](int j) {
+        if (lane == 0) {
+            const int fa = wa + 32 * j, fb = min(wb, fa + 32);
+            const uint32_t slot = (uint32_t)((j % D) * NCW + warp);
+            const uint32_t dst = ring + slot * a.slot_bytes;
+            const int g1 = min(fb, G);  // gate tasks [fa, g1), up tasks [max(fa, G), fb)
+            uint32_t bytes = 0;
+            if (fa < g1) {
+                bulk_g2s(dst, gbase + (size_t)fa * TB, (uint32_t)(g1 - fa) * TB, full_bar((int)slot));
+                bytes += (uint32_t)(g1 - fa) * TB;
+            }
+            const int ua = max(fa, G);
+            if (ua < fb) {
+                bulk_g2s(dst + bytes, ubase + (size_t)(ua - G) * TB, (uint32_t)(fb - ua) * TB, full_bar((int)slot));
+                bytes += (uint32_t)(fb - ua) * TB;
+            }
+            mbar_arrive_expect_tx(full_bar((int)slot), bytes);
+        }
+    };
+    const int jfirst = min(D, nst);
+    for (int j = 0; j < jfirst; ++j) issue(j);
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        griddep_wait();
+        const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
+        uint32_t tx = 0;
+        if (ntask > 0) {
+            bulk_g2s(xa, a.ximg, row_bytes, xbar);
+            tx += row_bytes;
+            for (int v = tpr; v < tpr + a.xrep; v += tpr) {
+                const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
+                bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
+                tx += rb2;
+            }
+        }
+        mbar_arrive_expect_tx(xbar, tx);
+    }
+    const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
+    mbar_wait(xbar, 0);
+
+    for (int j = 0; j < nst; ++j) {
+        const int slot = (j % D) * NCW + warp;
+        const int fa = wa + 32 * j, fb = min(wb, fa + 32);
+        mbar_wait(full_bar(slot), (uint32_t)((j / D) & 1));
+        const int f = fa + lane;
+        const bool valid = f < fb;
+        uint32_t w[F::WW];
+        if (valid) F::load(smem + (uint32_t)slot * a.slot_bytes + (uint32_t)lane * TB, w);
+        __syncwarp();
+        if (j + D < nst) {
+            fence_proxy_async_smem();
+            issue(j + D);
+        }
+        if (valid) {
+            // G is a multiple of tpr: a task's column is its index modulo tpr in both ranges
+            const int o = (int)tpr_div.div((uint32_t)f), tt = f - o * tpr;
+            const int xc = a.xrep ? fa - (int)tpr_div.div((uint32_t)fa) * tpr + lane : tt;
+            AccSink<1> sink;
+            sink.acc[0] = 0.0f;
+            F::compute(w, 0u, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
+            part[f] = sink.acc[0];
+        }
+    }
+    if (lane == 0) {
+        for (int d = 0; d < D && d < nst; ++d)
+            mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nst - 1 - d) / D)) / D) & 1), DRAIN_NS);
+        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
+    }
+    __syncthreads();
+    // row sums in task order: g of the CTA's gate rows, then u of its up rows
+    for (int r = tid; r < 2 * nr; r += NCW * 32) {
+        const float *p = part + (size_t)r * tpr;
+        float s = 0.0f;
+        for (int t = 0; t < tpr; ++t) s += p[t];
+        rsum[r] = s;
+    }
+    __syncthreads();
+    // per unit: h = silu(g) u, quantized as one activation block into the down tile image
+    for (int u = warp; u < nu; u += NCW) {
+        const int j = 32 * (u0 + u) + lane;
+        const float g = rsum[32 * u + lane], uu = rsum[nr + 32 * u + lane];
+        const float h = silu_mul(g, uu);
+        a.g_out[j] = g;
+        a.u_out[j] = uu;
+        a.h_out[j] = h;
+        int q, s;
+        float d;
+        quant_block_warp(h, q, d, s);
+        put_block(a.himg, 0, a.himg_tpr, u0 + u, a.himg_xgt_log2, lane, q, d, s);
+    }
+}
+
+}  // namespace qg

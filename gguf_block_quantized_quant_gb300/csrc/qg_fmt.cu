@@ -174,6 +174,45 @@ int launch_engine1(int ncw, const Gemv1Args &a, int grid, uint32_t smem, cudaStr
     }
 }
 
+// The FFN gate/up one-token kernel (ffn_gateup1_kernel) with ncw warps.
+template <int FMT, int T>
+int launch_ffn1(int ncw, const FfnGateUp1Args &a, int grid, uint32_t smem, cudaStream_t s) {
+    if constexpr (FT<FMT, T>::TASK_BYTES % 16 != 0 || FT<FMT, T>::TPB != 1) {
+        return -1;
+    } else {
+        static std::mutex mu;
+        static bool ready[64][3] = {};
+        const int v = ncw == 16 ? 2 : ncw == NCW_WIDE ? 1 : 0;
+        auto kern = v == 2 ? ffn_gateup1_kernel<FMT, T, 16>
+                           : v == 1 ? ffn_gateup1_kernel<FMT, T, NCW_WIDE> : ffn_gateup1_kernel<FMT, T, 8>;
+        if (ncw != 16 && ncw != NCW_WIDE && ncw != 8) return -1;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -4;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (!ready[dev][v]) {
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX) != cudaSuccess ||
+                    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                    return -4;
+                ready[dev][v] = true;
+            }
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(ncw * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return -4;
+        return cudaGetLastError() == cudaSuccess ? 0 : -4;
+    }
+}
+
 template <class J>
 void set_engine(J &j, const Ring &r, int tpr_x, int ntok) {
     j.depth = r.depth;
@@ -222,6 +261,27 @@ int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8
     return 0;
 }
 
+// A one-token plan (p.one) of N rows against an activation tile image that is already
+// written: y = W x on engine1_kernel.
+template <int FMT>
+int gemv_one_run(const GemvPlan &p, const uint8_t *W, int N, const uint8_t *ximg, float *y, cudaStream_t stream) {
+    return with_t<true>(p.geo, [&](auto Tc) {
+        constexpr int T = decltype(Tc)::value;
+        Gemv1Args a{};
+        a.W = W;
+        a.y = y;
+        a.ximg = ximg;
+        a.N = N;
+        a.tpr = p.geo.tpr;
+        a.depth = p.one_depth;
+        a.xrep = p.xrep;
+        a.rb = p.geo.rb;
+        a.slot_bytes = p.one_slot;
+        a.x_bytes = p.one_x;
+        return launch_engine1<FMT, T>(p.ncw, a, p.grid, p.one_smem, stream);
+    });
+}
+
 template <int FMT>
 int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
@@ -232,22 +292,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (p.pair)
         return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y,
                                   p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : nullptr, c.stream);
-    if (p.one)
-        return with_t<true>(p.geo, [&](auto Tc) {
-            constexpr int T = decltype(Tc)::value;
-            Gemv1Args a{};
-            a.W = c.W;
-            a.y = c.y;
-            a.ximg = ximg;
-            a.N = c.N;
-            a.tpr = p.geo.tpr;
-            a.depth = p.one_depth;
-            a.xrep = p.xrep;
-            a.rb = p.geo.rb;
-            a.slot_bytes = p.one_slot;
-            a.x_bytes = p.one_x;
-            return launch_engine1<FMT, T>(p.ncw, a, p.grid, p.one_smem, c.stream);
-        });
+    if (p.one) return gemv_one_run<FMT>(p, c.W, c.N, ximg, c.y, c.stream);
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
@@ -292,6 +337,34 @@ int ffn_run(const FfnCall &c, int sms) {
     int rc = launch_prep_tiles(c.x, nullptr, nullptr, nullptr, nullptr, nullptr, c.M, c.H, log2i(xgt), ximg, nullptr,
                                nullptr, nullptr, c.stream);
     if (rc) return rc;
+    if (p.one) {
+        // one token: gate/up with SwiGLU and the requantization of h in its epilogue, which
+        // writes the down projection's tile image; then the down GEMV on it
+        uint8_t *himg = c.ws + p.ws_down + p.down.ws_ximg;
+        rc = with_t<true>(p.geo, [&](auto Tc) {
+            constexpr int T = decltype(Tc)::value;
+            FfnGateUp1Args a{};
+            a.Wg = c.Wg;
+            a.Wu = c.Wu;
+            a.ximg = ximg;
+            a.g_out = g;
+            a.u_out = u;
+            a.h_out = h;
+            a.himg = himg;
+            a.I = c.I;
+            a.tpr = p.geo.tpr;
+            a.depth = p.one_depth;
+            a.xrep = XREP;
+            a.himg_tpr = p.down.geo.tpr;
+            a.himg_xgt_log2 = log2i(p.down.geo.XGT);
+            a.rb = p.geo.rb;
+            a.slot_bytes = p.one_slot;
+            a.x_bytes = p.one_x;
+            return launch_ffn1<FMT, T>(p.one_ncw, a, p.one_grid, p.one_smem, c.stream);
+        });
+        if (rc) return rc;
+        return gemv_one_run<FMT>(p.down, c.Wd, c.H, himg, c.y, c.stream);
+    }
     if (p.gate.pair) {
         // several tokens: gate and up as two row-pair launches on the same tile image
         rc = gemv_pair_run<FMT>(p.gate, c.Wg, c.I, c.M, ximg, p.ximg_pitch, g, nullptr, c.stream);

@@ -334,6 +334,11 @@ struct FfnPlan {
     Ring ring;
     GemvPlan gate;  // several tokens: gate and up as two row-pair GEMV launches (gate.pair)
     GemvPlan down;  // y = Wd h; h = silu(g) * u is formed by its activation preparation
+    // one token: gate/up on the one-token engine with SwiGLU and the requantization of h in
+    // its epilogue (ffn_gateup1_kernel), writing the down projection's tile image
+    bool one = false;
+    int one_grid = 0, one_ncw = 0, one_depth = 0;
+    uint32_t one_slot = 0, one_x = 0, one_smem = 0;
     size_t ws_ximg = 0, ximg_pitch = 0, ws_g = 0, ws_u = 0, ws_h = 0, ws_down = 0, ws_total = 0;
 };
 
@@ -355,6 +360,25 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     if (!p.down.ok) return p;
     if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
     if (p.gate.pair && p.gate.KS > 1) p.gate.pair = false;  // its partial sums have no workspace here
+    if (M == 1 && p.down.one && g.aligned16() && g.TPB == 1 && I % 32 == 0) {
+        const int U = I / 32, grid = std::min(U, sms), nu = (U + grid - 1) / grid;
+        const int part = ffn1_part_floats(nu, g.tpr);
+        const int ncw = plan_ncw(g, 1, 64L * nu * g.tpr);
+        const uint32_t slot = (uint32_t)(32 * g.task_bytes());
+        const uint32_t xb = (uint32_t)align_up((size_t)(g.tpr + XREP) * g.stride, 16);
+        for (int d = DMAX; d >= 1 && !p.one; --d) {
+            const uint32_t sm = engine1_smem(ncw * d, slot, xb, part);
+            if (part <= 4 * ONE_PART_MAX && sm <= (uint32_t)SMEM_MAX) {
+                p.one = true;
+                p.one_grid = grid;
+                p.one_ncw = ncw;
+                p.one_depth = d;
+                p.one_slot = slot;
+                p.one_x = xb;
+                p.one_smem = sm;
+            }
+        }
+    }
     size_t o = 0;
     p.ximg_pitch = (size_t)(p.gate.pair ? p.gate.ximg_pitch : tiles);
     p.ws_ximg = o; o = align_up(o + p.ximg_pitch * M, 256);

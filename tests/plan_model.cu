@@ -172,7 +172,7 @@ int main() {
     int Ks[] = {32, 96, 256, 512, 544, 768, 1056, 2048, 4096, 5120, 17408, 7168, 14336, 2816};
     int Ns[] = {1, 2, 3, 5, 37, 64, 75, 76, 151, 152, 153, 300, 1024, 2048, 4096, 5120, 17408};
     int Ms[] = {1, 2, 3, 4, 5, 8, 16};
-    int nplans = 0, npair = 0, none = 0;
+    int nplans = 0, npair = 0, none = 0, nffn1 = 0;
     char nm[160];
     for (int fmt : fmts) for (int K : Ks) for (int N : Ns) for (int M : Ms) {
         if (!task_geo(fmt, K, true).ok) continue;
@@ -253,6 +253,47 @@ int main() {
             ++npair;
         }
         const TaskGeo &g = p.geo;
+        if (p.one) {
+            // one-token gate/up with the SwiGLU epilogue: units of 32 rows per CTA, the gate
+            // rows then the up rows as two contiguous ranges; a stage at most two copies
+            ++nffn1;
+            CHECK(M == 1 && p.down.one && g.aligned16() && g.TPB == 1, "%s one eligibility", nm);
+            CHECK(p.one_smem <= (uint32_t)SMEM_MAX && p.one_depth >= 1, "%s one smem", nm);
+            CHECK(p.one_x >= (uint32_t)((g.tpr + XREP) * g.stride), "%s one x tiles", nm);
+            const int U = I / 32, TB = g.task_bytes(), S = p.one_ncw * p.one_depth;
+            for (int b = 0; b < p.one_grid; ++b) {
+                const int u0 = (int)((long)U * b / p.one_grid), u1 = (int)((long)U * (b + 1) / p.one_grid);
+                const int nu = u1 - u0, G = 32 * nu * g.tpr, ntask = 2 * G;
+                CHECK(engine1_smem(S, p.one_slot, p.one_x, ffn1_part_floats(nu, g.tpr)) <= p.one_smem, "%s part %d", nm, b);
+                for (int w = 0; w < p.one_ncw; ++w) {
+                    const int wa = (int)((long)ntask * w / p.one_ncw), wb = (int)((long)ntask * (w + 1) / p.one_ncw);
+                    for (int fa = wa; fa < wb; fa += 32) {
+                        const int fb = std::min(wb, fa + 32), g1 = std::min(fb, G), ua = std::max(fa, G);
+                        long bytes = 0;
+                        if (fa < g1) {
+                            const long off = (long)32 * u0 * g.rb + (long)fa * TB, n = (long)(g1 - fa) * TB;
+                            CHECK(off % 16 == 0 && n % 16 == 0 && off + n <= (long)I * g.rb, "%s gate copy", nm);
+                            bytes += n;
+                        }
+                        if (ua < fb) {
+                            const long off = (long)32 * u0 * g.rb + (long)(ua - G) * TB, n = (long)(fb - ua) * TB;
+                            CHECK(off % 16 == 0 && n % 16 == 0 && off + n <= (long)I * g.rb, "%s up copy", nm);
+                            bytes += n;
+                        }
+                        CHECK(bytes == (long)(fb - fa) * TB && bytes <= (long)p.one_slot, "%s slot", nm);
+                        for (int f = fa; f < fb; ++f) {
+                            const int ff = f < G ? f : f - G, o = ff / g.tpr;
+                            CHECK(o < 32 * nu && f < ntask, "%s task row", nm);
+                            const int xc = fa % g.tpr + (f - fa);
+                            CHECK(xc < g.tpr + XREP && xc % g.tpr == f % g.tpr && f % g.tpr == ff % g.tpr, "%s column", nm);
+                        }
+                    }
+                }
+                // h units into the down projection's tile image: tile (u >> xgt_log2) of one row
+                CHECK((u1 - 1) / p.down.geo.XGT < p.down.geo.tpr, "%s h tile", nm);
+            }
+            CHECK(p.down.ximg_pitch >= (size_t)p.down.geo.tpr * p.down.geo.stride, "%s h image", nm);
+        }
         sim(nm, g, p.ring, p.grid, p.ncw,
             [&](int b) { Cta c; c.o0 = (int)((long)b * 2 * I / p.grid); c.o1 = (int)((long)(b + 1) * 2 * I / p.grid);
                          c.tpr = g.tpr; c.grp = I; return c; },
@@ -318,6 +359,6 @@ int main() {
         const MoePlan m1 = plan_moe(12, 1, 2048, 256, 8, 512, sms), m2 = plan_moe(12, 1, 2048, 256, 8, 512, sms, true);
         CHECK(m1.ok && m1.P == 1 && m1.gu_grid == 144 && m2.ok && m2.P == 2, "MoE plans");
     }
-    printf("fails %d\n", fails);
+    printf("one-token FFN plans %d\nfails %d\n", nffn1, fails);
     return fails != 0;
 }
