@@ -38,7 +38,10 @@
 namespace qg {
 
 constexpr int NPIECE_MAX = 8;      // weight pieces per stage
-constexpr int SCRATCH_INTS = 256;  // prologue scratch (MoE top-k ids)
+// Prologue scratch: the MoE launches' routed expert ids (up to SCRATCH_W of them), and in
+// the down launch their routing weights (float bits) from SCRATCH_W on.
+constexpr int SCRATCH_W = 256;
+constexpr int SCRATCH_INTS = 2 * SCRATCH_W;
 constexpr int BND_FLOATS = 1 + 16; // boundary entry: row, then one sum per token
 
 // Unsigned division by a run-time constant (n < 2^31, d < 2^31): 32-bit reciprocal
@@ -232,8 +235,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
         job.prologue(warp, NCW, lane, scratch);
     }
     __syncthreads();
-    if constexpr (Job::HAS_PROLOGUE)
-        for (int j = 0; j < jfirst; ++j) issue(j);
+    // the activation tiles (their own copies, after the previous kernel has finished); a job
+    // with a prologue issues them before its weight stages, which the prologue also gated
     if (warp == 0) {
         if (lane == 0) {
             griddep_wait();
@@ -255,6 +258,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
         }
         __syncwarp();
     }
+    if constexpr (Job::HAS_PROLOGUE)
+        for (int j = 0; j < jfirst; ++j) issue(j);
 
     // ---------------------------------------------------------------------- consume
     const int ra = (int)tpr_div.div((uint32_t)a);
@@ -363,28 +368,25 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine_kernel(const Job job) {
         for (int m = 0; m < MT; ++m) e[1 + m] = carry[m];
     }
     consumer_sync<NCONS>();
-    // rows shared by consecutive warps: their sums added in warp order
+    // rows shared by consecutive warps: their sums added in warp order.  Lane l of warp 0
+    // holds boundary entry l (warp l / 2, side l % 2); the entries of one row are the lanes
+    // that match its index (they are consecutive among the used entries, as the warps' rows
+    // ascend), and the first of them adds them up in lane order and stores the sums.
+    static_assert(2 * NCW <= 32, "one lane per boundary entry");
     if (warp == 0) {
-        int cur = -1;
-        float acc = 0.0f;
-        for (int w = 0; w < NCW; ++w) {
-            for (int side = 0; side < 2; ++side) {
-                const float *e = bsum + (w * 2 + side) * BND_FLOATS;
-                const int r = __float_as_int(e[0]);
-                if (r < 0) continue;
-                if (r != cur) {
-                    if (cur >= 0 && lane < ntok) job.store(cx, o0 + cur, lane, acc, jarea);
-                    cur = r;
-                    acc = 0.0f;
-                }
-                if (lane < ntok) acc += e[1 + lane];
+        const int r = lane < 2 * NCW ? __float_as_int(bsum[lane * BND_FLOATS]) : -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, r);
+        if (r >= 0 && lane == __ffs(same) - 1) {
+            for (int m = 0; m < ntok; ++m) {
+                float acc = 0.0f;
+                for (uint32_t k = same; k; k &= k - 1) acc += bsum[(__ffs(k) - 1) * BND_FLOATS + 1 + m];
+                job.store(cx, o0 + r, m, acc, jarea);
             }
         }
-        if (cur >= 0 && lane < ntok) job.store(cx, o0 + cur, lane, acc, jarea);
     }
     if (Job::HAS_FINISH) {
         consumer_sync<NCONS>();
-        job.finish(cx, jarea, tid, NCONS);
+        job.finish(cx, jarea, tid, NCONS, scratch);
     }
 }
 

@@ -85,7 +85,7 @@ struct GemvJob : EngineFields {
     __device__ uint32_t xrow(const Ctx &, int, const FastDiv &) const { return 0; }
     __device__ void store(const Ctx &c, int o, int m, float v, float *) const { c.out[(long)m * N + o] = v; }
     __device__ void init(float *, int) const {}
-    __device__ void finish(const Ctx &, float *, int, int) const {}
+    __device__ void finish(const Ctx &, float *, int, int, const int *) const {}
     __device__ void prologue(int, int, int, int *) const {}
 };
 
@@ -125,7 +125,7 @@ struct FfnGateUpJob : EngineFields {
             u_out[(long)(m0 + m) * I + o - I] = v;
     }
     __device__ void init(float *, int) const {}
-    __device__ void finish(const Ctx &, float *, int, int) const {}
+    __device__ void finish(const Ctx &, float *, int, int, const int *) const {}
     __device__ void prologue(int, int, int, int *) const {}
 };
 
@@ -220,7 +220,7 @@ struct MoeGateUpJob : EngineFields {
     // One warp per unit: h = silu(g) * u for its 32 positions (g, u: the planes' partial
     // rows added in plane order), quantized by the activation rule of the call and written
     // into the down projection's tile image and the workspace.
-    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads) const {
+    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads, const int *scratch) const {
         const int lane = tid & 31;
         for (int i = tid >> 5; i < c.nu; i += nthreads >> 5) {
             int jb;
@@ -255,15 +255,107 @@ struct MoeGateUpJob : EngineFields {
     // Router tail, after the logits kernel has finished: softmax over E logits, the topk
     // largest (ties: lower id), weights renormalized over the picks; one warp per token.
     // exp(l - max) / sum over the picks equals p / sum(p over the picks) for the softmax
-    // probabilities p.  A round of the selection is two warp reductions: the largest logit
-    // (as an order-preserving integer key), then the lowest expert id holding it.
+    // probabilities p; the sum runs over the picks in pick order.
     __device__ void prologue(int warp, int nwarps, int lane, int *ids) const {
         griddep_wait();
+        if (E <= 256 && topk <= 8)
+            select_topk8(warp, nwarps, lane, ids);
+        else if (E <= 256)
+            select_topk<256 / 32>(warp, nwarps, lane, ids);
+        else
+            select_topk<E_MAX / 32>(warp, nwarps, lane, ids);
+    }
+    // Pick order as one 64-bit key: the logit's order-preserving bits above, the complement
+    // of the expert id below (so that of equal logits the lower id ranks higher).
+    __device__ static __forceinline__ uint64_t pick_key(float v, int e) {
+        const uint32_t b = __float_as_uint(v);
+        const uint32_t u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        return ((uint64_t)u << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+    }
+    __device__ static __forceinline__ float pick_value(uint64_t k) {
+        const uint32_t u = (uint32_t)(k >> 32);
+        return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+    }
+    __device__ static __forceinline__ int pick_id(uint64_t k) { return (int)(0xffffffffu - (uint32_t)k); }
+    __device__ static __forceinline__ void cas_desc(uint64_t &a, uint64_t &b) {
+        const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+        a = hi;
+        b = lo;
+    }
+    // E <= 256, topk <= 8.  Each lane sorts the keys of its 8 logits (a 19-comparator
+    // network), then five butterfly rounds merge the lists of lane pairs keeping the best 8
+    // (the larger of a[i] and b[7 - i] form a bitonic sequence holding the 8 best of both
+    // lists, sorted by three rounds of compare-exchanges); every lane ends with the row's 8
+    // best keys in pick order.  The keys are distinct, so the picks, their order and the
+    // weights are those of taking the largest remaining logit topk times.
+    __device__ void select_topk8(int warp, int nwarps, int lane, int *ids) const {
         for (int m = warp; m < M; m += nwarps) {
-            float v[E_MAX / 32];
+            uint64_t c[8];
             float lmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < E_MAX / 32; ++i) {
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                const float v = e < E ? logits[(long)m * E + e] + 0.0f : -INFINITY;  // + 0: -0 as +0
+                lmax = fmaxf(lmax, v);
+                c[i] = e < E ? pick_key(v, e) : 0ull;  // 0: below every logit's key
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            cas_desc(c[0], c[2]); cas_desc(c[1], c[3]); cas_desc(c[4], c[6]); cas_desc(c[5], c[7]);
+            cas_desc(c[0], c[4]); cas_desc(c[1], c[5]); cas_desc(c[2], c[6]); cas_desc(c[3], c[7]);
+            cas_desc(c[0], c[1]); cas_desc(c[2], c[3]); cas_desc(c[4], c[5]); cas_desc(c[6], c[7]);
+            cas_desc(c[2], c[4]); cas_desc(c[3], c[5]);
+            cas_desc(c[1], c[4]); cas_desc(c[3], c[6]);
+            cas_desc(c[1], c[2]); cas_desc(c[3], c[4]); cas_desc(c[5], c[6]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                uint64_t b[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b[i] = __shfl_xor_sync(0xffffffffu, c[i], o);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c[i] = c[i] > b[7 - i] ? c[i] : b[7 - i];
+#pragma unroll
+                for (int d = 4; d > 0; d >>= 1)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if ((i & d) == 0) cas_desc(c[i], c[i + d]);
+            }
+            float esum = 0.0f, my_ev = 0.0f;
+            int my_sel = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (r < topk) {
+                    const float ev = expf(pick_value(c[r]) - lmax);
+                    esum += ev;
+                    if (lane == r) {
+                        my_sel = pick_id(c[r]);
+                        my_ev = ev;
+                    }
+                }
+            }
+            if (lane < topk) {
+                const float w = my_ev / esum;
+                ids[m * topk + lane] = my_sel;
+                if (blockIdx.x == 0) {
+                    ids_ws[m * topk + lane] = my_sel;
+                    w_ws[m * topk + lane] = w;
+                    if (ids_out) ids_out[m * topk + lane] = my_sel;
+                    if (w_out) w_out[m * topk + lane] = w;
+                }
+            }
+            __syncwarp();
+        }
+    }
+    // General E and topk: a round of the selection is two warp reductions, the largest logit
+    // (as an order-preserving integer key), then the lowest expert id holding it.  Each lane
+    // keeps the best of its own NV logits; only the lane whose logit was taken rescans.
+    template <int NV>
+    __device__ void select_topk(int warp, int nwarps, int lane, int *ids) const {
+        for (int m = warp; m < M; m += nwarps) {
+            float v[NV];
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
                 const int e = lane + 32 * i;
                 v[i] = e < E ? logits[(long)m * E + e] + 0.0f : -INFINITY;  // + 0: -0 as +0
                 lmax = fmaxf(lmax, v[i]);
@@ -271,31 +363,39 @@ struct MoeGateUpJob : EngineFields {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
             uint32_t taken = 0;
-            float esum = 0.0f;
-            int my_sel = 0;
-            float my_ev = 0.0f;
-            for (int r = 0; r < topk; ++r) {
-                // this lane's largest remaining logit (its lowest id on ties)
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
+            float bv;
+            int be;
+            // this lane's largest remaining logit (its lowest id on ties)
+            auto rescan = [&]() {
+                bv = -INFINITY;
+                be = 0x7fffffff;
 #pragma unroll
-                for (int i = 0; i < E_MAX / 32; ++i) {
+                for (int i = 0; i < NV; ++i) {
                     const int e = lane + 32 * i;
                     if (e < E && !((taken >> i) & 1u) && (v[i] > bv || be == 0x7fffffff)) {
                         bv = v[i];
                         be = e;
                     }
                 }
+            };
+            rescan();
+            float esum = 0.0f;
+            int my_sel = 0;
+            float my_ev = 0.0f;
+            for (int r = 0; r < topk; ++r) {
                 const int bits = __float_as_int(bv);
                 const int key = be == 0x7fffffff ? (int)0x80000000 : (bits >= 0 ? bits : bits ^ 0x7fffffff);
                 const int kmax = __reduce_max_sync(0xffffffffu, key);
-                be = __reduce_min_sync(0xffffffffu, key == kmax ? be : 0x7fffffff);
-                bv = __int_as_float(kmax >= 0 ? kmax : kmax ^ 0x7fffffff);
-                if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                const float ev = expf(bv - lmax);
+                const int sel = __reduce_min_sync(0xffffffffu, key == kmax ? be : 0x7fffffff);
+                const float sv = __int_as_float(kmax >= 0 ? kmax : kmax ^ 0x7fffffff);
+                if ((sel & 31) == lane) {
+                    taken |= 1u << (sel >> 5);
+                    rescan();
+                }
+                const float ev = expf(sv - lmax);
                 esum += ev;
                 if (lane == r) {
-                    my_sel = be;
+                    my_sel = sel;
                     my_ev = ev;
                 }
             }
@@ -350,11 +450,11 @@ struct MoeDownJob : EngineFields {
         tpr = tpr_x;
         grp = c.nloc;
     }
-    __device__ const uint8_t *seg_src(const Ctx &c, int o, int tt, const uint8_t *&lim, const int *) const {
+    __device__ const uint8_t *seg_src(const Ctx &c, int o, int tt, const uint8_t *&lim, const int *ids) const {
         const int q = (int)c.dnloc.div((uint32_t)o), r = o - q * c.nloc;
         const int m = (int)c.dslots.div((uint32_t)q), s = q - m * slots();
         if (s < topk) {
-            const size_t e = (size_t)min(max(ids_ws[(m0 + m) * topk + s], 0), E - 1);
+            const size_t e = (size_t)min(max(ids[m * topk + s], 0), E - 1);
             lim = Wd_exps_end;
             return Wd_exps + e * ebytes + (size_t)(c.n0 + r) * rb + task_off<F>(tt);
         }
@@ -371,13 +471,14 @@ struct MoeDownJob : EngineFields {
     }
     __device__ void store(const Ctx &, int o, int m, float v, float *part) const { part[o * P + m] = v; }
     __device__ void init(float *, int) const {}
-    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads) const {
+    __device__ void finish(const Ctx &c, float *part, int tid, int nthreads, const int *scratch) const {
         const int nloc = c.nloc;
         for (int i = tid; i < M * nloc; i += nthreads) {
             const int m = i / nloc, r = i - m * nloc;
             float acc = 0.0f;
             for (int s = 0; s < slots(); ++s) {
-                const float ws = s < topk ? w_ws[(m0 + m) * topk + s] : 1.0f;  // shared expert: weight 1
+                // shared expert: weight 1
+                const float ws = s < topk ? __int_as_float(scratch[SCRATCH_W + m * topk + s]) : 1.0f;
                 const float *o = part + ((m * slots() + s) * nloc + r) * P;
                 float v = o[0];
 #pragma unroll
@@ -388,8 +489,16 @@ struct MoeDownJob : EngineFields {
         }
     }
     // The weight copies need the routed expert ids, written two kernels earlier: wait for
-    // the previous kernel (and so for everything before it) before any copy is issued.
-    __device__ void prologue(int, int, int, int *) const { griddep_wait(); }
+    // the previous kernel (and so for everything before it) before any copy is issued, then
+    // bring this launch's ids and routing weights into shared memory (scratch[i] and
+    // scratch[SCRATCH_W + i] for pick i of the launch's tokens).
+    __device__ void prologue(int warp, int nwarps, int lane, int *scratch) const {
+        griddep_wait();
+        for (int i = warp * 32 + lane; i < M * topk; i += nwarps * 32) {
+            scratch[i] = ids_ws[m0 * topk + i];
+            scratch[SCRATCH_W + i] = __float_as_int(w_ws[m0 * topk + i]);
+        }
+    }
 };
 
 }  // namespace qg

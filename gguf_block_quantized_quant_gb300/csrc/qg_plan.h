@@ -105,6 +105,22 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
 }
 inline int geo_ncw(const TaskGeo &g, int MT) { return engine_ncw(g.task_bytes(), MT); }
 
+// The rows of task_geo cut into one-superblock tasks where task_geo pairs superblocks (Q2_K,
+// Q4_K, IQ4_XS with an even superblock count): twice the tasks, each half the decode chain,
+// and 16 warps instead of 8 where the task drops to 160 bytes or less.  For launches whose
+// CTAs have too few tasks to keep 8 warps' decode chains overlapped.
+inline TaskGeo short_task_geo(int fmt, int K) {
+    TaskGeo g = task_geo(fmt, K, false);
+    if (!g.ok || g.T != 2 || g.BPT != 2) return g;
+    g.T = 1;
+    g.BPT = 1;
+    g.XGT = 8;
+    g.gpr = g.nbr;
+    g.tpr = g.gpr * g.TPB;
+    g.stride = tile_stride(g.XGT);
+    return g;
+}
+
 // Geometry of one row's part of a row-pair task (engine_pair_kernel): one Q4_K, Q5_K, Q6_K
 // or IQ4_XS superblock, eight Q4_0 or IQ4_NL blocks, or four Q8_0 / Q4_1 / Q5_0 / Q5_1
 // blocks (rows whose block count is a multiple of that); not ok otherwise (Q2_K and Q3_K,
@@ -143,7 +159,10 @@ struct Ring {
 // run: the fewest tasks in one run of adjacent rows that any CTA of the launch sees (0: the
 // whole CTA range is one run); a stage of t tasks then spans at most t / run + 2 runs.
 // ncw: warps of the launch (geo_ncw).
-inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_bytes, int ncw) {
+// tasks_per_cta (0: unknown): the most tasks one CTA of the launch holds; the ring then has
+// no more slots per warp than a warp has stages, so that a CTA with little work keeps its
+// shared memory small and the next kernel's CTAs can be resident beside it.
+inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_bytes, int ncw, long tasks_per_cta = 0) {
     Ring r;
     r.x_bytes = (uint32_t)align_up(x_bytes, 16);
     r.j_bytes = (uint32_t)align_up(j_bytes, 16);
@@ -164,6 +183,11 @@ inline Ring plan_ring(const TaskGeo &g, long run, uint32_t x_bytes, uint32_t j_b
             r.tps = t;
             r.slot_bytes = slot;
             r.depth = (int)std::min<long>(DMAX, d);
+            if (tasks_per_cta > 0) {
+                // a warp's tasks are whole units of TPB: at most ceil(units / ncw) units
+                const long per_warp = ((tasks_per_cta + g.TPB - 1) / g.TPB + ncw - 1) / ncw * g.TPB;
+                r.depth = (int)std::min<long>(r.depth, std::max<long>(1, (per_warp + t - 1) / t));
+            }
             break;
         }
     }
@@ -406,10 +430,12 @@ struct MoePlan {
 inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, bool s16 = false) {
     MoePlan p;
     p.P = s16 ? 2 : 1;
-    p.gh = task_geo(fmt, H, false);
-    p.gi = task_geo(fmt, I, false);
+    // one-superblock tasks: an expert's rows are few per CTA at every batch size (measured
+    // faster than superblock pairs from 1 to 16 tokens)
+    p.gh = short_task_geo(fmt, H);
+    p.gi = short_task_geo(fmt, I);
     if (!p.gh.ok || !p.gi.ok || M < 1 || M > M_MAX || E < 1 || E > 1024 || topk < 1 || topk > 16 || topk > E ||
-        sms < 1 || M * topk > SCRATCH_INTS)
+        sms < 1 || M * topk > SCRATCH_W)
         return p;
     p.S = topk + 1;
     // gate/up: units of 32 positions j of one (token, slot), each its 32 gate and 32 up rows;
@@ -420,7 +446,8 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, 
     p.gu_grid = (int)std::min<long>(sms, gu_units);
     const long upc = (gu_units + p.gu_grid - 1) / p.gu_grid;  // most units of one CTA
     p.gu_ncw = plan_ncw(p.gh, p.P, upc * 64 * p.gh.tpr);
-    p.gu_ring = plan_ring(p.gh, 32L * p.gh.tpr, (uint32_t)gu_x, (uint32_t)(upc * 64 * p.P * 4), p.gu_ncw);
+    p.gu_ring = plan_ring(p.gh, 32L * p.gh.tpr, (uint32_t)gu_x, (uint32_t)(upc * 64 * p.P * 4), p.gu_ncw,
+                          upc * 64 * p.gh.tpr);
     if (!p.gu_ring.ok) return p;
     // down: per CTA a range of hidden rows; output rows (token, slot, row) in shared memory
     const long tiles_tok = (long)p.S * p.P * p.gi.tpr * p.gi.stride;
@@ -431,8 +458,9 @@ inline MoePlan plan_moe(int fmt, int M, int H, int E, int topk, int I, int sms, 
     if (p.dn_MC < 1) return p;
     p.dn_nchunk = (M + p.dn_MC - 1) / p.dn_MC;
     // CTAs own floor or ceil of H / dn_grid rows: runs are at least the floor long
+    p.dn_ncw = geo_ncw(p.gi, p.P);
     p.dn_ring = plan_ring(p.gi, (long)(H / p.dn_grid) * p.gi.tpr, (uint32_t)(p.dn_MC * tiles_tok),
-                          (uint32_t)(p.dn_MC * part_tok), p.dn_ncw = geo_ncw(p.gi, p.P));
+                          (uint32_t)(p.dn_MC * part_tok), p.dn_ncw, (long)p.dn_MC * p.S * nloc * p.gi.tpr);
     if (!p.dn_ring.ok) return p;
     // workspace
     const size_t Rw = (size_t)M * p.S;

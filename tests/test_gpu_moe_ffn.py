@@ -129,6 +129,61 @@ def test_moe_other_formats_small(qg, fmt):
     _check_moe(fmt, inp, out, M, H, E, topk, I)
 
 
+def _expected_picks(logits, topk):
+    """Pick order on the GPU's own logits: largest first, of equal logits the lower id
+    (-0 equals +0); weights exp(l - max over all E) renormalized over the picks."""
+    ids = np.zeros((logits.shape[0], topk), np.int32)
+    w = np.zeros((logits.shape[0], topk))
+    for m, row in enumerate(logits.astype(np.float64)):
+        order = np.lexsort((np.arange(row.size), -row))[:topk]
+        ids[m] = order
+        ev = np.exp(row[order] - row.max())
+        w[m] = ev / ev.sum()
+    return ids, w
+
+
+@pytest.mark.parametrize("E,topk,ties", [(256, 8, False), (256, 8, True), (256, 2, True), (200, 5, True),
+                                         (256, 12, False), (300, 6, True), (300, 2, True), (64, 16, False)])
+def test_moe_topk_selection(qg, E, topk, ties):
+    """Every selection path (E <= 256 with topk <= 8, and the general one) against the pick
+    order taken on the GPU's own logits, ids exactly.  With ties, three identical router rows
+    (scaled up so that they rank first) give bitwise-equal logits: they are picked in id
+    order, and with topk = 2 only the two lower ids are.  A second equal pair ranks lower."""
+    fmt, M, H, I = synth.Q4_K, 3, 512, 256
+    g = np.random.default_rng(900 + E + topk)
+    Wr = synth.router_weights(E, H, g)
+    if ties:
+        big = 4.0 * Wr[0]
+        for e in (E - 1, E // 2, 7):        # three equal rows, the largest logits of the row
+            Wr[e] = big
+        for e in (3, E - 5):                # an equal pair just below them
+            Wr[e] = 3.0 * Wr[1]
+    x = synth.activations(M, H, g)
+    if ties:
+        x[:] = np.abs(x) * np.sign(Wr[0])   # positive logits for the scaled rows
+    Wg, Wu = synth.stacked_experts(fmt, E, I, H, g), synth.stacked_experts(fmt, E, I, H, g)
+    Wd = synth.stacked_experts(fmt, E, H, I, g)
+    sg, su, sd = synth.weights(fmt, I, H, g), synth.weights(fmt, I, H, g), synth.weights(fmt, H, I, g)
+    import torch
+    ws = torch.zeros(qg.qg_workspace_size(qg.QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), dtype=torch.uint8,
+                     device="cuda")
+    ids = torch.empty((M, topk), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, topk), dtype=torch.float32, device="cuda")
+    qg.qg_moe_ffn(fmt, dev(x), dev(Wr), topk, dev(Wg), dev(Wu), dev(Wd), dev(sg), dev(su), dev(sd), I,
+                  topk_ids=ids, topk_w=w, ws=ws)
+    torch.cuda.synchronize()
+    off = qg.qg_moe_ws_layout(M, H, E, topk, I)
+    logits = _ws_view(ws, off[6], M * E, np.float32).reshape(M, E)
+    ids_ref, w_ref = _expected_picks(logits, topk)
+    np.testing.assert_array_equal(host(ids), ids_ref)
+    np.testing.assert_allclose(host(w), w_ref, rtol=1e-6, atol=1e-9)
+    if ties:
+        for m in range(M):
+            assert logits[m, 7] == logits[m, E // 2] == logits[m, E - 1]
+            k = min(3, topk)
+            assert list(host(ids)[m, :k]) == sorted([7, E // 2, E - 1])[:k]
+
+
 def test_moe_large_batch_unfused_paths(qg):
     """16 tokens x 9 slots of h exceed the shared-memory budget: h is requantized by a
     separate kernel into the workspace."""
