@@ -315,6 +315,17 @@ int planning_sms() {
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// Whether p points into device memory (activations in page-locked host memory are read by
+// one preparation kernel, not once per CTA).
+bool device_memory(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice;
+}
+
 template <class Fn>
 int by_format(int fmt, Fn &&fn) {
     switch (fmt) {
@@ -486,6 +497,7 @@ static int gemv_common(int fmt, const void *W, const float *x, const int8_t *xq,
     c.K = K;
     c.M = M;
     c.x = x;
+    c.x_device = x && device_memory(x);
     c.xq = x ? nullptr : xq;
     c.xd = x ? nullptr : xd;
     c.xs = x ? nullptr : xs;

@@ -28,9 +28,108 @@ struct Gemv1Args {
     const uint8_t *W;      // N rows of rb bytes
     float *y;              // N outputs (one token)
     const uint8_t *ximg;   // activation tile image of the token's row: tpr tiles
-    int N, tpr, depth, xrep;
+    const float *x;        // or (non-null): the fp32 row of K elements, quantized by every CTA
+    int N, K, tpr, depth, xrep;
     uint32_t rb, slot_bytes, x_bytes;
 };
+
+// The activation row x (K fp32 elements, 16-byte aligned) quantized by the NTH threads of a
+// CTA straight into the shared tile image xs: tpr tiles of XGT blocks, the first xrep tiles
+// repeated after the row, each unit laid out as put_tile_unit writes it.  The rule is
+// quant_block_warp's (d = amax / 127 rounded to nearest, q = round(v / d) clamped to
+// +-127, v / d the rounded quotient), taken by eight lanes per 32-element block, four
+// elements each: the block's maximum and code sums are exact in any order, so the tiles
+// equal those of the preparation kernel bit for bit.  A thread takes XCH blocks at a time
+// side by side (their loads, reductions and divisions interleave), and v / d goes through
+// the rounded reciprocal: |v * inv - fl(v / d)| < 2e-5 for |v| <= amax (both lie within a
+// few 2^-24 relative of v / d <= 127), so rounding it gives round(fl(v / d)) unless it lies
+// within 2^-14 of a half-integer; there, and for a subnormal d (no finite reciprocal), the
+// rounded division decides.  after_loads() runs once, right after the first loads.
+template <int XGT, int NTH, class AfterLoads>
+__device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *xs, int tpr, int xrep, int tid,
+                                                AfterLoads &&after_loads) {
+    constexpr int XCH = 4, NG = NTH / 8, STRIDE = tile_stride(XGT);
+    const int nb = K / 32, grp = tid >> 3, sub = tid & 7;
+    for (int b0 = 0; b0 < nb; b0 += NG * XCH) {
+        float e[XCH][4];
+#pragma unroll
+        for (int i = 0; i < XCH; ++i) {
+            const int b = b0 + grp + i * NG;
+            const float4 v =
+                b < nb ? __ldg(reinterpret_cast<const float4 *>(x + 32L * b) + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+            e[i][0] = v.x, e[i][1] = v.y, e[i][2] = v.z, e[i][3] = v.w;
+        }
+        if (b0 == 0) after_loads();
+        float a[XCH];
+#pragma unroll
+        for (int i = 0; i < XCH; ++i)
+            a[i] = fmaxf(fmaxf(fabsf(e[i][0]), fabsf(e[i][1])), fmaxf(fabsf(e[i][2]), fabsf(e[i][3])));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < XCH; ++i) a[i] = fmaxf(a[i], __shfl_xor_sync(0xffffffffu, a[i], o));
+        float d[XCH];
+        int q[XCH][4];
+        uint32_t need = 0;  // bit 4 i + k: element k of block i takes the rounded division
+#pragma unroll
+        for (int i = 0; i < XCH; ++i) {
+            d[i] = __fdiv_rn(a[i], 127.0f);
+            const float inv = __frcp_rn(d[i]);
+            const bool div_only = d[i] < 1.17549435e-38f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float t = e[i][k] * inv, m = fabsf(t);
+                if (d[i] != 0.0f && (div_only || fabsf(m - floorf(m) - 0.5f) < 6.103515625e-05f))
+                    need |= 1u << (4 * i + k);
+                q[i][k] = d[i] != 0.0f && !div_only ? (int)roundf(t) : 0;
+            }
+        }
+        if (__any_sync(0xffffffffu, need != 0)) {
+#pragma unroll
+            for (int i = 0; i < XCH; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if ((need >> (4 * i + k)) & 1u) q[i][k] = (int)roundf(__fdiv_rn(e[i][k], d[i]));
+        }
+        int sum[XCH], half[XCH];
+#pragma unroll
+        for (int i = 0; i < XCH; ++i) {
+            sum[i] = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                q[i][k] = q[i][k] > 127 ? 127 : (q[i][k] < -127 ? -127 : q[i][k]);
+                sum[i] += q[i][k];
+            }
+            half[i] = sub < 4 ? sum[i] : 0;  // elements 0..15 of the block
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < XCH; ++i) {
+                sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], o);
+                half[i] += __shfl_xor_sync(0xffffffffu, half[i], o);
+            }
+#pragma unroll
+        for (int i = 0; i < XCH; ++i) {
+            const int b = b0 + grp + i * NG;
+            if (b >= nb) continue;
+            const uint32_t codes = (uint32_t)(q[i][0] & 0xff) | ((uint32_t)(q[i][1] & 0xff) << 8) |
+                                   ((uint32_t)(q[i][2] & 0xff) << 16) | ((uint32_t)(q[i][3] & 0xff) << 24);
+            const int u = b & (XGT - 1);
+            for (int ti = b / XGT; ti < tpr + xrep; ti += tpr) {
+                uint8_t *t = xs + (size_t)ti * STRIDE;
+                reinterpret_cast<uint32_t *>(t + 32 * u)[sub] = codes;
+                if (sub == 0) {
+                    reinterpret_cast<float *>(t + 32 * XGT)[u] = d[i];
+                    reinterpret_cast<int32_t *>(t + 36 * XGT)[u] = sum[i];
+                    reinterpret_cast<uint32_t *>(t + 40 * XGT)[u] =
+                        ((uint32_t)half[i] & 0xffffu) | ((uint32_t)(sum[i] - half[i]) << 16);
+                    reinterpret_cast<float *>(t + 44 * XGT)[u] = d[i] * (float)sum[i];
+                }
+            }
+        }
+    }
+}
 
 // shared memory: ring (S slots), activation tiles, partial sums, S + 1 mbarriers
 __host__ __device__ constexpr uint32_t engine1_smem(int S, uint32_t slot_bytes, uint32_t x_bytes, int part_floats) {
@@ -80,27 +179,39 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
             mbar_arrive_expect_tx(full_bar((int)slot), bytes);
         }
     };
-    const int jfirst = min(D, nst);
-    for (int j = 0; j < jfirst; ++j) issue(j);
+    // the first D stages; with x, right after the activation row's loads rather than before
+    // them (a load queues behind the bulk copies this SM has in flight)
+    const int jfirst = min(D, nst), jpre = a.x ? 0 : jfirst;
+    for (int j = 0; j < jpre; ++j) issue(j);
     __syncthreads();
-    if (warp == 0 && lane == 0) {
+    if (a.x) {
+        // the activation row, from the previous kernel: quantized here, by every thread
         griddep_wait();
-        const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
-        uint32_t tx = 0;
-        if (ntask > 0) {
-            bulk_g2s(xa, a.ximg, row_bytes, xbar);
-            tx += row_bytes;
-            // the row's first xrep tiles again after it
-            for (int v = tpr; v < tpr + a.xrep; v += tpr) {
-                const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
-                bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
-                tx += rb2;
+        auto rest = [&] {
+            for (int j = jpre; j < jfirst; ++j) issue(j);
+        };
+        if (ntask > 0) quant_row_tiles<F::XGT, NCW * 32>(a.x, a.K, smem + (xa - ring), tpr, a.xrep, tid, rest);
+        __syncthreads();
+    } else {
+        if (warp == 0 && lane == 0) {
+            griddep_wait();
+            const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
+            uint32_t tx = 0;
+            if (ntask > 0) {
+                bulk_g2s(xa, a.ximg, row_bytes, xbar);
+                tx += row_bytes;
+                // the row's first xrep tiles again after it
+                for (int v = tpr; v < tpr + a.xrep; v += tpr) {
+                    const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
+                    bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
+                    tx += rb2;
+                }
             }
+            mbar_arrive_expect_tx(xbar, tx);
         }
-        mbar_arrive_expect_tx(xbar, tx);
+        mbar_wait(xbar, 0);
     }
     const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
-    mbar_wait(xbar, 0);
 
     for (int j = 0; j < nst; ++j) {
         const int slot = (j % D) * NCW + warp;
@@ -130,7 +241,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
     if (lane == 0) {
         for (int d = 0; d < D && d < nst; ++d)
             mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nst - 1 - d) / D)) / D) & 1), DRAIN_NS);
-        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
+        if (warp == 0 && !a.x) mbar_drain(xbar, 0, DRAIN_NS);
     }
     __syncthreads();
     for (int r = tid; r < o1 - o0; r += NCW * 32) {

@@ -264,13 +264,18 @@ int gemv_pair_run(const GemvPlan &p, const uint8_t *W, int N, int M, const uint8
 // A one-token plan (p.one) of N rows against an activation tile image that is already
 // written: y = W x on engine1_kernel.
 template <int FMT>
-int gemv_one_run(const GemvPlan &p, const uint8_t *W, int N, const uint8_t *ximg, float *y, cudaStream_t stream) {
+// ximg: the token's activation tile image, or nullptr with x: the fp32 row of K elements
+// (device memory, 16-byte aligned), which every CTA quantizes itself.
+int gemv_one_run(const GemvPlan &p, const uint8_t *W, int N, const uint8_t *ximg, const float *x, int K, float *y,
+                 cudaStream_t stream) {
     return with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
         Gemv1Args a{};
         a.W = W;
         a.y = y;
         a.ximg = ximg;
+        a.x = ximg ? nullptr : x;
+        a.K = K;
         a.N = N;
         a.tpr = p.geo.tpr;
         a.depth = p.one_depth;
@@ -285,6 +290,10 @@ int gemv_one_run(const GemvPlan &p, const uint8_t *W, int N, const uint8_t *ximg
 template <int FMT>
 int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (c.ws == nullptr || c.ws_bytes < p.ws_total) return -2;
+    // one token of plain fp32 activations in device memory, rows of up to ONE_FUSED_K_MAX: the
+    // one-token engine quantizes the row in every CTA, with no preparation kernel on the chain
+    if (p.one && c.K <= ONE_FUSED_K_MAX && c.x && !c.u && !c.h_out && c.x_device && ((uintptr_t)c.x & 15u) == 0)
+        return gemv_one_run<FMT>(p, c.W, c.N, nullptr, c.x, c.K, c.y, c.stream);
     uint8_t *ximg = c.ws + p.ws_ximg;
     int rc = launch_prep_tiles(c.x, c.u, c.h_out, c.xq, c.xd, c.xs, c.M, c.K, log2i(p.geo.XGT), ximg, nullptr,
                                nullptr, nullptr, c.stream);
@@ -292,7 +301,7 @@ int gemv_run_planned(const GemvPlan &p, const GemvCall &c) {
     if (p.pair)
         return gemv_pair_run<FMT>(p, c.W, c.N, c.M, ximg, p.ximg_pitch, c.y,
                                   p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : nullptr, c.stream);
-    if (p.one) return gemv_one_run<FMT>(p, c.W, c.N, ximg, c.y, c.stream);
+    if (p.one) return gemv_one_run<FMT>(p, c.W, c.N, ximg, nullptr, c.K, c.y, c.stream);
     float *out = p.KS > 1 ? reinterpret_cast<float *>(c.ws + p.ws_part) : c.y;
     rc = with_t<true>(p.geo, [&](auto Tc) {
         constexpr int T = decltype(Tc)::value;
@@ -363,7 +372,7 @@ int ffn_run(const FfnCall &c, int sms) {
             return launch_ffn1<FMT, T>(p.one_ncw, a, p.one_grid, p.one_smem, c.stream);
         });
         if (rc) return rc;
-        return gemv_one_run<FMT>(p.down, c.Wd, c.H, himg, c.y, c.stream);
+        return gemv_one_run<FMT>(p.down, c.Wd, c.H, himg, nullptr, c.I, c.y, c.stream);
     }
     if (p.gate.pair) {
         // several tokens: gate and up as two row-pair launches on the same tile image

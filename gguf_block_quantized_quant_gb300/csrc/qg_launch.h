@@ -23,6 +23,7 @@ struct GemvCall {
     uint8_t *ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    bool x_device;      // x is device memory (not host memory mapped for the device)
 };
 
 struct FfnCall {

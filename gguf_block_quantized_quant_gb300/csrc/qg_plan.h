@@ -235,6 +235,10 @@ struct GemvPlan {
 
 // Partial sums of one CTA of the one-token engine (rows x tasks per row) at most this many.
 constexpr int ONE_PART_MAX = 8192;
+// Rows up to this length are quantized inside the one-token engine (every CTA quantizes the
+// whole row, a cost that grows with K; beyond this the preparation kernel and its extra
+// kernel boundary were measured faster).
+constexpr int ONE_FUSED_K_MAX = 8192;
 
 // The one-token engine where it applies: one token, no K-split, every task and row a
 // multiple of 16 bytes (so each stage is one aligned bulk copy), and the CTA's partial sums

@@ -41,6 +41,44 @@ def test_quantize_act_bit_exact(qg, M, K):
     np.testing.assert_array_equal(host(xs), os_)
 
 
+def _near_tie_x(K, g):
+    """Blocks whose quotients v / d lie within a few 1e-7 of half-integers (and some exactly
+    on them), besides the special blocks: the cases where rounding v / d needs the exact
+    quotient."""
+    x = _special_x(1, K, g)
+    nb = K // 32
+    for b in range(8, nb, 3):
+        a = np.float32(abs(g.standard_normal()) * 10.0 ** g.uniform(-3, 3)) + np.float32(1e-3)
+        d = np.float32(a / np.float32(127))
+        k = g.integers(-126, 126, size=32)
+        v = (k + 0.5) * np.float64(d) * (1 + g.uniform(-3e-7, 3e-7, size=32) * (b % 2))
+        v[0] = a
+        x[0, 32 * b:32 * b + 32] = v.astype(np.float32)
+    return x
+
+
+@pytest.mark.parametrize("fmt,N,K", [(synth.Q4_K, 17408, 5120), (synth.Q4_K, 3000, 8192), (synth.Q4_0, 2048, 8192),
+                                     (synth.Q6_K, 4096, 4096), (synth.IQ4_XS, 1000, 4096), (synth.Q8_0, 300, 2048),
+                                     (synth.Q4_K, 5120, 17408)])
+def test_one_token_in_kernel_quantization(qg, fmt, N, K):
+    """At one token with the activations in device memory (rows up to 8192) the one-token
+    engine quantizes x in every CTA; with them in page-locked host memory (or longer rows) a
+    preparation kernel does.  The two must
+    give the same y bit for bit (same tiles, same deterministic sums), on blocks that take
+    every branch of the quantization rule, and y must be within bound of the oracle."""
+    import torch
+    g = np.random.default_rng(4242 + K + fmt)
+    Wn = synth.weights(fmt, N, K, g)
+    W = dev(Wn)
+    x = _near_tie_x(K, g)
+    y_dev = host(qg.qg_gemv(fmt, W, dev(x), N))
+    y_host = qg.qg_gemv(fmt, W, torch.from_numpy(x).pin_memory(), N)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(y_dev, y_host.numpy())
+    xq, xd, xs = oracle.quantize_act(x)
+    assert_within(y_dev, oracle.gemv_q(fmt, Wn, xq, xd, xs, N, K), oracle.absdot(fmt, Wn, xq, xd, N, K), "fused y")
+
+
 # ----------------------------------------------------------------------------- integer contract
 @pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 def test_block_dots_bit_exact(qg, fmt):
