@@ -316,14 +316,31 @@ int planning_sms() {
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // Whether p points into device memory (activations in page-locked host memory are read by
-// one preparation kernel, not once per CTA).
+// one preparation kernel, not once per CTA).  The answer is cached per 2 MiB region of the
+// address: under unified addressing device and host ranges never share such a region, and
+// the answer only chooses between two paths that give the same results, so a stale entry
+// (a region freed and reused) costs time at worst.  The query itself takes microseconds.
 bool device_memory(const void *p) {
-    cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
+    constexpr int SLOTS = 64;
+    static std::mutex mu;
+    static uintptr_t key[SLOTS];  // region + 1 (0: empty)
+    static bool val[SLOTS];
+    const uintptr_t k = ((uintptr_t)p >> 21) + 1;
+    const int i = (int)(k % SLOTS);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (key[i] == k) return val[i];
     }
-    return a.type == cudaMemoryTypeDevice;
+    cudaPointerAttributes a{};
+    bool dev = false;
+    if (cudaPointerGetAttributes(&a, p) == cudaSuccess)
+        dev = a.type == cudaMemoryTypeDevice;
+    else
+        cudaGetLastError();
+    std::lock_guard<std::mutex> lock(mu);
+    key[i] = k;
+    val[i] = dev;
+    return dev;
 }
 
 template <class Fn>
@@ -547,6 +564,7 @@ int qg_ffn_sublayer(int fmt, const void *Wg, const void *Wu, const void *Wd, con
     c.Wu = static_cast<const uint8_t *>(Wu);
     c.Wd = static_cast<const uint8_t *>(Wd);
     c.x = x;
+    c.x_device = device_memory(x);
     c.y = y;
     c.M = M;
     c.H = H;

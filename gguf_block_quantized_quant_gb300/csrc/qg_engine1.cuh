@@ -268,6 +268,8 @@ namespace qg {
 struct FfnGateUp1Args {
     const uint8_t *Wg, *Wu;  // I rows of rb bytes each
     const uint8_t *ximg;     // activation tile image of x: tpr tiles
+    const float *x;          // or (non-null): the fp32 row of K elements, quantized by every CTA
+    int K;
     float *g_out, *u_out, *h_out;
     uint8_t *himg;           // the down projection's tile image (one row)
     int I, tpr, depth, xrep, himg_tpr, himg_xgt_log2;
@@ -331,26 +333,36 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
             mbar_arrive_expect_tx(full_bar((int)slot), bytes);
         }
     };
-    const int jfirst = min(D, nst);
-    for (int j = 0; j < jfirst; ++j) issue(j);
+    // as in engine1_kernel: with x, the first stages go out right after the row's loads
+    const int jfirst = min(D, nst), jpre = a.x ? 0 : jfirst;
+    for (int j = 0; j < jpre; ++j) issue(j);
     __syncthreads();
-    if (warp == 0 && lane == 0) {
+    if (a.x) {
         griddep_wait();
-        const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
-        uint32_t tx = 0;
-        if (ntask > 0) {
-            bulk_g2s(xa, a.ximg, row_bytes, xbar);
-            tx += row_bytes;
-            for (int v = tpr; v < tpr + a.xrep; v += tpr) {
-                const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
-                bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
-                tx += rb2;
+        auto rest = [&] {
+            for (int j = jpre; j < jfirst; ++j) issue(j);
+        };
+        if (ntask > 0) quant_row_tiles<F::XGT, NCW * 32>(a.x, a.K, smem + (xa - ring), tpr, a.xrep, tid, rest);
+        __syncthreads();
+    } else {
+        if (warp == 0 && lane == 0) {
+            griddep_wait();
+            const uint32_t row_bytes = (uint32_t)tpr * TL::STRIDE;
+            uint32_t tx = 0;
+            if (ntask > 0) {
+                bulk_g2s(xa, a.ximg, row_bytes, xbar);
+                tx += row_bytes;
+                for (int v = tpr; v < tpr + a.xrep; v += tpr) {
+                    const uint32_t rb2 = (uint32_t)(min(tpr, tpr + a.xrep - v) * TL::STRIDE);
+                    bulk_g2s(xa + (uint32_t)v * TL::STRIDE, a.ximg, rb2, xbar);
+                    tx += rb2;
+                }
             }
+            mbar_arrive_expect_tx(xbar, tx);
         }
-        mbar_arrive_expect_tx(xbar, tx);
+        mbar_wait(xbar, 0);
     }
     const FastDiv tpr_div = FastDiv::make((uint32_t)tpr);
-    mbar_wait(xbar, 0);
 
     for (int j = 0; j < nst; ++j) {
         const int slot = (j % D) * NCW + warp;
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
     if (lane == 0) {
         for (int d = 0; d < D && d < nst; ++d)
             mbar_drain(full_bar(d * NCW + warp), (uint32_t)(((d + D * ((nst - 1 - d) / D)) / D) & 1), DRAIN_NS);
-        if (warp == 0) mbar_drain(xbar, 0, DRAIN_NS);
+        if (warp == 0 && !a.x) mbar_drain(xbar, 0, DRAIN_NS);
     }
     __syncthreads();
     // row sums in task order: g of the CTA's gate rows, then u of its up rows

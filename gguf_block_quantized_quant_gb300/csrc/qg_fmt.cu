@@ -343,9 +343,14 @@ int ffn_run(const FfnCall &c, int sms) {
     float *u = reinterpret_cast<float *>(c.ws + p.ws_u);
     float *h = reinterpret_cast<float *>(c.ws + p.ws_h);
     const int xgt = p.gate.pair ? p.gate.geo.XGT : p.geo.XGT;
-    int rc = launch_prep_tiles(c.x, nullptr, nullptr, nullptr, nullptr, nullptr, c.M, c.H, log2i(xgt), ximg, nullptr,
+    // one token in device memory with rows up to ONE_FUSED_K_MAX: the gate/up kernel quantizes x
+    const bool fuse_x = p.one && c.H <= ONE_FUSED_K_MAX && c.x_device && ((uintptr_t)c.x & 15u) == 0;
+    int rc = 0;
+    if (!fuse_x) {
+        rc = launch_prep_tiles(c.x, nullptr, nullptr, nullptr, nullptr, nullptr, c.M, c.H, log2i(xgt), ximg, nullptr,
                                nullptr, nullptr, c.stream);
-    if (rc) return rc;
+        if (rc) return rc;
+    }
     if (p.one) {
         // one token: gate/up with SwiGLU and the requantization of h in its epilogue, which
         // writes the down projection's tile image; then the down GEMV on it
@@ -355,7 +360,9 @@ int ffn_run(const FfnCall &c, int sms) {
             FfnGateUp1Args a{};
             a.Wg = c.Wg;
             a.Wu = c.Wu;
-            a.ximg = ximg;
+            a.ximg = fuse_x ? nullptr : ximg;
+            a.x = fuse_x ? c.x : nullptr;
+            a.K = c.H;
             a.g_out = g;
             a.u_out = u;
             a.h_out = h;

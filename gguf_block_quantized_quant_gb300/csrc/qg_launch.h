@@ -34,6 +34,7 @@ struct FfnCall {
     uint8_t *ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    bool x_device;  // x is device memory
 };
 
 struct MoeCall {

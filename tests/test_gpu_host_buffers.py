@@ -55,9 +55,12 @@ def test_quantize_and_gemv_q_host(qg):
     np.testing.assert_array_equal(y_host.numpy(), y_dev)
 
 
-def test_ffn_sublayer_host(qg):
-    fmt, M, H, I = synth.Q4_K, 2, 1024, 2816
-    g = np.random.default_rng(902)
+@pytest.mark.parametrize("M", [1, 2])
+def test_ffn_sublayer_host(qg, M):
+    """At one token the device-memory call quantizes x inside the gate/up kernel and the
+    host-memory call through the preparation kernel: the same y bit for bit."""
+    fmt, H, I = synth.Q4_K, 1024, 2816
+    g = np.random.default_rng(902 + M)
     Wg, Wu, Wd = (dev(synth.weights(fmt, I, H, g)), dev(synth.weights(fmt, I, H, g)),
                   dev(synth.weights(fmt, H, I, g)))
     x = synth.activations(M, H, g)
