@@ -116,17 +116,31 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
         const int k0 = (int)((long)q * H / ROUTER_SPLIT), k1 = (int)((long)(q + 1) * H / ROUTER_SPLIT);
         if ((((uintptr_t)wr | (uintptr_t)x) & 15u) == 0 && ((k0 | k1) & 3) == 0) {
             const float4 *w4 = reinterpret_cast<const float4 *>(wr);
-#pragma unroll 4
-            for (int k = (k0 >> 2) + lane; k < (k1 >> 2); k += 32) {
-                const float4 wv = __ldg(w4 + k);
+            // RCH 16-byte loads of the row per lane in flight at once, then, token by
+            // token, the same number of loads of x; the products are added in k order
+            constexpr int RCH = 4;
+            for (int kb = (k0 >> 2) + lane; kb < (k1 >> 2); kb += 32 * RCH) {
+                float4 wv[RCH];
+#pragma unroll
+                for (int i = 0; i < RCH; ++i)
+                    wv[i] = kb + 32 * i < (k1 >> 2) ? __ldg(w4 + kb + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int m = 0; m < M_MAX; ++m) {
                     if (m < M) {
-                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (long)m * H) + k);
-                        acc[m] = fmaf(wv.x, xv.x, acc[m]);
-                        acc[m] = fmaf(wv.y, xv.y, acc[m]);
-                        acc[m] = fmaf(wv.z, xv.z, acc[m]);
-                        acc[m] = fmaf(wv.w, xv.w, acc[m]);
+                        const float4 *x4 = reinterpret_cast<const float4 *>(x + (long)m * H);
+                        float4 xv[RCH];
+#pragma unroll
+                        for (int i = 0; i < RCH; ++i)
+                            xv[i] = kb + 32 * i < (k1 >> 2) ? __ldg(x4 + kb + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < RCH; ++i) {
+                            if (kb + 32 * i < (k1 >> 2)) {
+                                acc[m] = fmaf(wv[i].x, xv[i].x, acc[m]);
+                                acc[m] = fmaf(wv[i].y, xv[i].y, acc[m]);
+                                acc[m] = fmaf(wv[i].z, xv[i].z, acc[m]);
+                                acc[m] = fmaf(wv[i].w, xv[i].w, acc[m]);
+                            }
+                        }
                     }
                 }
             }
