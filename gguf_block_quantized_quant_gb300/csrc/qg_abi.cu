@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
         if ((((uintptr_t)wr | (uintptr_t)x) & 15u) == 0 && ((k0 | k1) & 3) == 0) {
             const float4 *w4 = reinterpret_cast<const float4 *>(wr);
             // RCH 16-byte loads of the row per lane in flight at once, then, token by
-            // token, the same number of loads of x; the products are added in k order
+            // token, the same number of loads of x (from L2: the previous kernel may have
+            // written it); the products are added in k order
             constexpr int RCH = 4;
             for (int kb = (k0 >> 2) + lane; kb < (k1 >> 2); kb += 32 * RCH) {
                 float4 wv[RCH];
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
                         float4 xv[RCH];
 #pragma unroll
                         for (int i = 0; i < RCH; ++i)
-                            xv[i] = kb + 32 * i < (k1 >> 2) ? __ldg(x4 + kb + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            xv[i] = kb + 32 * i < (k1 >> 2) ? __ldcg(x4 + kb + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int i = 0; i < RCH; ++i) {
                             if (kb + 32 * i < (k1 >> 2)) {
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float *x, int M,
                 const float wv = __ldg(wr + k);
 #pragma unroll
                 for (int m = 0; m < M_MAX; ++m)
-                    if (m < M) acc[m] = fmaf(wv, __ldg(x + (long)m * H + k), acc[m]);
+                    if (m < M) acc[m] = fmaf(wv, __ldcg(x + (long)m * H + k), acc[m]);
             }
         }
     }

@@ -44,7 +44,8 @@ struct Gemv1Args {
 // the rounded reciprocal: |v * inv - fl(v / d)| < 2e-5 for |v| <= amax (both lie within a
 // few 2^-24 relative of v / d <= 127), so rounding it gives round(fl(v / d)) unless it lies
 // within 2^-14 of a half-integer; there, and for a subnormal d (no finite reciprocal), the
-// rounded division decides.  after_loads() runs once, right after the first loads.
+// rounded division decides.  The row is read from L2 (it may have been written by the
+// previous kernel).  after_loads() runs once, right after the first loads.
 template <int XGT, int NTH, class AfterLoads>
 __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *xs, int tpr, int xrep, int tid,
                                                 AfterLoads &&after_loads) {
@@ -56,7 +57,7 @@ __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *
         for (int i = 0; i < XCH; ++i) {
             const int b = b0 + grp + i * NG;
             const float4 v =
-                b < nb ? __ldg(reinterpret_cast<const float4 *>(x + 32L * b) + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+                b < nb ? __ldcg(reinterpret_cast<const float4 *>(x + 32L * b) + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
             e[i][0] = v.x, e[i][1] = v.y, e[i][2] = v.z, e[i][3] = v.w;
         }
         if (b0 == 0) after_loads();

@@ -71,6 +71,33 @@ def test_gemv_graph_replay(qg, fmt, M):
     _replays(lambda s: qg.qg_gemv(fmt, W, x, N, y=y, ws=ws, stream=s), [x], fresh, [y], check)
 
 
+@pytest.mark.parametrize("fmt,N,K", [(synth.Q4_K, 2048, 4096), (synth.Q4_0, 1000, 2048)])
+def test_gemv_first_call_inside_capture(qg, fmt, N, K):
+    """A one-token call made first inside a stream capture, on buffers just allocated (64 MB
+    of fresh device memory, so that the activations' memory-type query of the call most
+    likely runs during the capture): the replay must be within bound of the oracle."""
+    import torch
+    g = np.random.default_rng(51 + K)
+    Wn = synth.weights(fmt, N, K, g)
+    W = dev(Wn)
+    fresh = torch.empty(16 << 20, dtype=torch.float32, device="cuda")
+    x = fresh[(8 << 20):(8 << 20) + K].view(1, K)
+    x.copy_(dev(synth.activations(1, K, g)))
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(qg.qg_workspace_size(qg.QG_OP_GEMV, fmt, 1, N, K), 16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(gr, stream=s):
+            qg.qg_gemv(fmt, W, x, N, y=y, ws=ws, stream=s)
+    gr.replay()
+    torch.cuda.synchronize()
+    xq, xd, xs = oracle.quantize_act(host(x))
+    assert_within(host(y), oracle.gemv_q(fmt, Wn, xq, xd, xs, N, K), oracle.absdot(fmt, Wn, xq, xd, N, K),
+                  "first call captured")
+
+
 @pytest.mark.parametrize("M", [1, 2])
 def test_ffn_graph_replay(qg, M):
     import torch
