@@ -44,7 +44,8 @@ struct Gemv1Args {
 // the rounded reciprocal: |v * inv - fl(v / d)| < 2e-5 for |v| <= amax (both lie within a
 // few 2^-24 relative of v / d <= 127), so rounding it gives round(fl(v / d)) unless it lies
 // within 2^-14 of a half-integer; there, and for a subnormal d (no finite reciprocal), the
-// rounded division decides.  The row is read from L2 (it may have been written by the
+// rounded division decides.  The blocks are written once; the repeated tiles are copied
+// from them after a barrier of the CTA (every thread calls this).  The row is read from L2 (it may have been written by the
 // previous kernel).  after_loads() runs once, right after the first loads.
 template <int XGT, int NTH, class AfterLoads>
 __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *xs, int tpr, int xrep, int tid,
@@ -79,10 +80,13 @@ __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *
             const bool div_only = d[i] < 1.17549435e-38f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float t = e[i][k] * inv, m = fabsf(t);
-                if (d[i] != 0.0f && (div_only || fabsf(m - floorf(m) - 0.5f) < 6.103515625e-05f))
+                // r: t rounded to the nearest integer (ties to even); where t is not within
+                // 2^-14 of a half-integer that is also round(t) (ties away from zero)
+                const float t = e[i][k] * inv;
+                const int r = __float2int_rn(t);
+                if (d[i] != 0.0f && (div_only || fabsf(t - (float)r) > 0.5f - 6.103515625e-05f))
                     need |= 1u << (4 * i + k);
-                q[i][k] = d[i] != 0.0f && !div_only ? (int)roundf(t) : 0;
+                q[i][k] = d[i] != 0.0f && !div_only ? r : 0;
             }
         }
         if (__any_sync(0xffffffffu, need != 0)) {
@@ -117,18 +121,25 @@ __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *
             const uint32_t codes = (uint32_t)(q[i][0] & 0xff) | ((uint32_t)(q[i][1] & 0xff) << 8) |
                                    ((uint32_t)(q[i][2] & 0xff) << 16) | ((uint32_t)(q[i][3] & 0xff) << 24);
             const int u = b & (XGT - 1);
-            for (int ti = b / XGT; ti < tpr + xrep; ti += tpr) {
-                uint8_t *t = xs + (size_t)ti * STRIDE;
-                reinterpret_cast<uint32_t *>(t + 32 * u)[sub] = codes;
-                if (sub == 0) {
-                    reinterpret_cast<float *>(t + 32 * XGT)[u] = d[i];
-                    reinterpret_cast<int32_t *>(t + 36 * XGT)[u] = sum[i];
-                    reinterpret_cast<uint32_t *>(t + 40 * XGT)[u] =
-                        ((uint32_t)half[i] & 0xffffu) | ((uint32_t)(sum[i] - half[i]) << 16);
-                    reinterpret_cast<float *>(t + 44 * XGT)[u] = d[i] * (float)sum[i];
-                }
+            uint8_t *t = xs + (size_t)(b / XGT) * STRIDE;
+            reinterpret_cast<uint32_t *>(t + 32 * u)[sub] = codes;
+            if (sub == 0) {
+                reinterpret_cast<float *>(t + 32 * XGT)[u] = d[i];
+                reinterpret_cast<int32_t *>(t + 36 * XGT)[u] = sum[i];
+                reinterpret_cast<uint32_t *>(t + 40 * XGT)[u] =
+                    ((uint32_t)half[i] & 0xffffu) | ((uint32_t)(sum[i] - half[i]) << 16);
+                reinterpret_cast<float *>(t + 44 * XGT)[u] = d[i] * (float)sum[i];
             }
         }
+    }
+    // the repeated tiles: tile tpr + j is a copy of tile j mod tpr, in 16-byte chunks
+    __syncthreads();
+    constexpr int CPT = STRIDE / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(xs);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)tpr * STRIDE);
+    for (int c = tid; c < xrep * CPT; c += NTH) {
+        const int j = c / CPT;
+        dst[c] = src[(j % tpr) * CPT + (c - j * CPT)];
     }
 }
 
