@@ -33,6 +33,19 @@ struct Gemv1Args {
     uint32_t rb, slot_bytes, x_bytes;
 };
 
+// Tiles tpr .. tpr + xrep - 1 of a row image in shared memory (16-byte aligned) as copies
+// of tiles (j mod tpr), in 16-byte chunks spread over nth threads.
+template <int STRIDE>
+__device__ __forceinline__ void repeat_tiles(uint8_t *xs, int tpr, int xrep, int tid, int nth) {
+    constexpr int CPT = STRIDE / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(xs);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)tpr * STRIDE);
+    for (int c = tid; c < xrep * CPT; c += nth) {
+        const int j = c / CPT;
+        dst[c] = src[(j % tpr) * CPT + (c - j * CPT)];
+    }
+}
+
 // The activation row x (K fp32 elements, 16-byte aligned) quantized by the NTH threads of a
 // CTA straight into the shared tile image xs: tpr tiles of XGT blocks, the first xrep tiles
 // repeated after the row, each unit laid out as put_tile_unit writes it.  The rule is
@@ -132,15 +145,9 @@ __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *
             }
         }
     }
-    // the repeated tiles: tile tpr + j is a copy of tile j mod tpr, in 16-byte chunks
+    // the repeated tiles: tile tpr + j is a copy of tile j mod tpr
     __syncthreads();
-    constexpr int CPT = STRIDE / 16;
-    const uint4 *src = reinterpret_cast<const uint4 *>(xs);
-    uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)tpr * STRIDE);
-    for (int c = tid; c < xrep * CPT; c += NTH) {
-        const int j = c / CPT;
-        dst[c] = src[(j % tpr) * CPT + (c - j * CPT)];
-    }
+    repeat_tiles<STRIDE>(xs, tpr, xrep, tid, NTH);
 }
 
 // shared memory: ring (S slots), activation tiles, partial sums, S + 1 mbarriers

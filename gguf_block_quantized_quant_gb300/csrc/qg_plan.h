@@ -389,7 +389,8 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
     if (p.gate.pair && p.gate.KS > 1) p.gate.pair = false;  // its partial sums have no workspace here
     if (M == 1 && p.down.one && g.aligned16() && g.TPB == 1 && I % 32 == 0) {
-        const int U = I / 32, grid = std::min(U, sms), nu = (U + grid - 1) / grid;
+        // every CTA the same number of units (nu): the launch takes as long as its fullest CTA
+        const int U = I / 32, nu = (U + std::min(U, sms) - 1) / std::min(U, sms), grid = (U + nu - 1) / nu;
         const int part = ffn1_part_floats(nu, g.tpr);
         const int ncw = plan_ncw(g, 1, 64L * nu * g.tpr);
         const uint32_t slot = (uint32_t)(32 * g.task_bytes());
