@@ -79,6 +79,27 @@ def test_one_token_in_kernel_quantization(qg, fmt, N, K):
     assert_within(y_dev, oracle.gemv_q(fmt, Wn, xq, xd, xs, N, K), oracle.absdot(fmt, Wn, xq, xd, N, K), "fused y")
 
 
+@pytest.mark.parametrize("fmt,N,K", [(synth.Q4_K, 2048, 5120), (synth.Q4_0, 1000, 4096)])
+def test_activations_only_4_byte_aligned(qg, fmt, N, K):
+    """Activations 4-byte but not 16-byte aligned (a view one element into a buffer) take the
+    preparation kernel instead of the in-kernel quantization: the same y bit for bit as the
+    16-byte-aligned call, within bound of the oracle."""
+    import torch
+    g = np.random.default_rng(4343 + K)
+    Wn = synth.weights(fmt, N, K, g)
+    W = dev(Wn)
+    xn = synth.activations(1, K, g)
+    buf = torch.zeros(K + 4, dtype=torch.float32, device="cuda")
+    buf[1:K + 1] = dev(xn)[0]
+    x_off = buf[1:K + 1].view(1, K)
+    assert x_off.data_ptr() % 16 == 4
+    y_off = host(qg.qg_gemv(fmt, W, x_off, N))
+    y_al = host(qg.qg_gemv(fmt, W, dev(xn), N))
+    np.testing.assert_array_equal(y_off, y_al)
+    xq, xd, xs = oracle.quantize_act(xn)
+    assert_within(y_off, oracle.gemv_q(fmt, Wn, xq, xd, xs, N, K), oracle.absdot(fmt, Wn, xq, xd, N, K), "4-byte x")
+
+
 # ----------------------------------------------------------------------------- integer contract
 @pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 def test_block_dots_bit_exact(qg, fmt):
