@@ -392,6 +392,11 @@ def run_ours(args):
     xs_host = [m["x_host"].pin_memory() for m in mats]
     ys_host = [torch.empty(m["y_host"].shape, dtype=torch.float32, pin_memory=True) for m in mats]
     z0, z1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):  # untimed: the same calls once (host buffers seen, code paths warm)
+        for i in range(max(args.warmup, 1)):
+            c = i % ROTATE
+            for m, xh, yh in zip(mats, xs_host, ys_host):
+                qg.qg_gemv(m["fmt"], m["W"][c], xh, m["N"], y=yh, ws=m["ws"], stream=s)
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
@@ -425,6 +430,11 @@ def run_ours(args):
     h2d = sum(m["x_host"].numel() * 4 for m in mats)
     d2h = sum(m["y_host"].numel() * 4 for m in mats)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):  # untimed: the staged steps once
+        x_all.copy_(x_all_h, non_blocking=True)
+        for m, xd_, yd_ in zip(mats, xs_dev, ys_dev):
+            qg.qg_gemv(m["fmt"], m["W"][0], xd_, m["N"], y=yd_, ws=m["ws"], stream=s)
+        y_all_h.copy_(y_all, non_blocking=True)
     barrier(world)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
