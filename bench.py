@@ -626,8 +626,8 @@ def secondary(qg, torch, dev, s):
             ws = torch.empty(qg.qg_workspace_size(qg.QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), dtype=torch.uint8,
                              device=dev)
             call = lambda: qg.qg_ffn_sublayer(fmt, Wg, Wu, Wd, x, I, y=y, ws=ws, stream=s)  # noqa: E731
-            us = _graph_time_us(torch, s, call, 20)
-            ue = _eager_time_us(torch, s, call, 20)
+            us = _graph_time_us(torch, s, call, 80)
+            ue = _eager_time_us(torch, s, call, 40)
             peak, _ = measured_peak()
             hbm_us = nb / (peak * 1e3)
             alu_us = 3.0 * M * H * I / DP4A_MAC_PER_S * 1e6
