@@ -31,6 +31,7 @@ struct Gemv1Args {
     const float *x;        // or (non-null): the fp32 row of K elements, quantized by every CTA
     int N, K, tpr, depth, xrep;
     uint32_t rb, slot_bytes, x_bytes;
+    int ra, nra;           // CTA row ranges start at multiples of ra rows (ra * rb: 16-byte multiple); nra = N / ra
 };
 
 // Tiles tpr .. tpr + xrep - 1 of a row image in shared memory (16-byte aligned) as copies
@@ -150,6 +151,17 @@ __device__ __forceinline__ void quant_row_tiles(const float *x, int K, uint8_t *
     repeat_tiles<STRIDE>(xs, tpr, xrep, tid, NTH);
 }
 
+// Tasks whose bytes make a multiple of 16: a warp's task range starts at a multiple of this
+// many tasks, so that every stage (a whole number of such groups, or the rest of a range
+// that ends on one) is a single 16-byte-aligned bulk copy of a 16-byte multiple.  1 for task
+// sizes that are multiples of 16; 8 for Q6_K and Q3_K superblocks (210, 110 bytes).
+__host__ __device__ constexpr int task_align_unit(int task_bytes) {
+    return task_bytes % 16 == 0 ? 1 : task_bytes % 8 == 0 ? 2 : task_bytes % 4 == 0 ? 4 : task_bytes % 2 == 0 ? 8 : 16;
+}
+// The same for rows of rb bytes: CTA row ranges start at multiples of this many rows (2 for
+// Q6_K rows of 5120 or 17408 elements, 4200 and 14280 bytes).
+__host__ __device__ constexpr int row_align_unit(uint32_t rb) { return task_align_unit((int)(rb & 15u)); }
+
 // shared memory: ring (S slots), activation tiles, partial sums, S + 1 mbarriers
 __host__ __device__ constexpr uint32_t engine1_smem(int S, uint32_t slot_bytes, uint32_t x_bytes, int part_floats) {
     return (uint32_t)S * slot_bytes + x_bytes + 4u * (uint32_t)part_floats + 8u * (uint32_t)(S + 1) + 16u;
@@ -160,15 +172,19 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
     using F = FT<FMT, T>;
     using TL = Tile<F::XGT>;
     constexpr uint32_t TB = F::TASK_BYTES;
-    static_assert(TB % 16 == 0, "stages are single aligned bulk copies");
+    constexpr int AU = task_align_unit((int)TB);
+    static_assert((32 * TB) % 16 == 0, "stages are single aligned bulk copies");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int D = a.depth, S = NCW * D;
     const uint32_t ring = smem_addr(smem);
     const uint32_t xa = ring + (uint32_t)S * a.slot_bytes;
     float *part = reinterpret_cast<float *>(smem + (uint32_t)S * a.slot_bytes + a.x_bytes);
-    const int o0 = split_point(a.N, (int)blockIdx.x, (int)gridDim.x);
-    const int o1 = split_point(a.N, (int)blockIdx.x + 1, (int)gridDim.x);
+    // tasks of a multiple of 16 bytes: rows too (ra = 1)
+    const int o0 = AU == 1 ? split_point(a.N, (int)blockIdx.x, (int)gridDim.x)
+                           : a.ra * split_point(a.nra, (int)blockIdx.x, (int)gridDim.x);
+    const int o1 = AU == 1 ? split_point(a.N, (int)blockIdx.x + 1, (int)gridDim.x)
+                           : a.ra * split_point(a.nra, (int)blockIdx.x + 1, (int)gridDim.x);
     const int tpr = a.tpr;
     const int ntask = (o1 - o0) * tpr;
     const uint32_t bars = ring + (uint32_t)S * a.slot_bytes + a.x_bytes + 4u * (uint32_t)ntask;
@@ -185,7 +201,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
     }
     __syncwarp();
 
-    const int wa = split_point(ntask, warp, NCW), wb = split_point(ntask, warp + 1, NCW);
+    // ntask is a multiple of AU (the CTA's rows make a multiple of 16 bytes)
+    const int wa = AU * split_point(ntask / AU, warp, NCW), wb = AU * split_point(ntask / AU, warp + 1, NCW);
     const int nst = (wb - wa + 31) / 32;  // this warp's stages
 
     // stage j of this warp into its slot (lane 0; the slot must be free)
@@ -239,6 +256,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
         const int f = fa + lane;
         const bool valid = f < fb;
         uint32_t w[F::WW];
+        // a task starts 2-byte aligned at worst (Q6_K, Q3_K): the decoder realigns by aoff
+        const uint32_t aoff = ((uint32_t)lane * TB) & 3u;
         if (valid) F::load(smem + (uint32_t)slot * a.slot_bytes + (uint32_t)lane * TB, w);
         __syncwarp();
         if (j + D < nst) {
@@ -252,7 +271,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) engine1_kernel(const Gemv1Args a)
             const int xc = a.xrep ? fa - (int)tpr_div.div((uint32_t)fa) * tpr + lane : tt;
             AccSink<1> sink;
             sink.acc[0] = 0.0f;
-            F::compute(w, 0u, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
+            F::compute(w, aoff, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
             part[f] = sink.acc[0];
         }
     }
@@ -303,7 +322,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
     using F = FT<FMT, T>;
     using TL = Tile<F::XGT>;
     constexpr uint32_t TB = F::TASK_BYTES;
-    static_assert(TB % 16 == 0, "stages are aligned bulk copies");
+    constexpr int AU = task_align_unit((int)TB);
+    static_assert((32 * TB) % 16 == 0, "stages are aligned bulk copies");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int D = a.depth, S = NCW * D;
@@ -330,7 +350,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
     }
     __syncwarp();
 
-    const int wa = split_point(ntask, warp, NCW), wb = split_point(ntask, warp + 1, NCW);
+    // G (whole rows) is a multiple of AU: so are the warp ranges and the gate/up boundary
+    const int wa = AU * split_point(ntask / AU, warp, NCW), wb = AU * split_point(ntask / AU, warp + 1, NCW);
     const int nst = (wb - wa + 31) / 32;
 
     auto issue = [&](int j) {
@@ -390,6 +411,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
         const int f = fa + lane;
         const bool valid = f < fb;
         uint32_t w[F::WW];
+        const uint32_t aoff = ((uint32_t)lane * TB) & 3u;
         if (valid) F::load(smem + (uint32_t)slot * a.slot_bytes + (uint32_t)lane * TB, w);
         __syncwarp();
         if (j + D < nst) {
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) ffn_gateup1_kernel(const FfnGateU
             const int xc = a.xrep ? fa - (int)tpr_div.div((uint32_t)fa) * tpr + lane : tt;
             AccSink<1> sink;
             sink.acc[0] = 0.0f;
-            F::compute(w, 0u, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
+            F::compute(w, aoff, tt % F::TPB, XT{smem + (xa - ring) + (uint32_t)(xc * TL::STRIDE), 0u}, 1, sink);
             part[f] = sink.acc[0];
         }
     }

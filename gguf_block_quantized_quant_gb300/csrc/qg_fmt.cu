@@ -143,11 +143,11 @@ int with_t(const TaskGeo &g, Fn &&fn) {
     }
 }
 
-// The one-token engine (engine1_kernel) with ncw warps, for task sizes that are multiples of
-// 16 bytes.
+// The one-token engine (engine1_kernel) with ncw warps, for even task sizes (every stage one
+// aligned bulk copy: see task_align_unit).
 template <int FMT, int T>
 int launch_engine1(int ncw, const Gemv1Args &a, int grid, uint32_t smem, cudaStream_t s) {
-    if constexpr (FT<FMT, T>::TASK_BYTES % 16 != 0 || FT<FMT, T>::TPB != 1) {
+    if constexpr (FT<FMT, T>::TASK_BYTES % 2 != 0 || FT<FMT, T>::TPB != 1) {
         return -1;
     } else {
         static std::mutex mu;
@@ -185,7 +185,7 @@ int launch_engine1(int ncw, const Gemv1Args &a, int grid, uint32_t smem, cudaStr
 // The FFN gate/up one-token kernel (ffn_gateup1_kernel) with ncw warps.
 template <int FMT, int T>
 int launch_ffn1(int ncw, const FfnGateUp1Args &a, int grid, uint32_t smem, cudaStream_t s) {
-    if constexpr (FT<FMT, T>::TASK_BYTES % 16 != 0 || FT<FMT, T>::TPB != 1) {
+    if constexpr (FT<FMT, T>::TASK_BYTES % 2 != 0 || FT<FMT, T>::TPB != 1) {
         return -1;
     } else {
         static std::mutex mu;
@@ -288,6 +288,8 @@ int gemv_one_run(const GemvPlan &p, const uint8_t *W, int N, const uint8_t *ximg
         a.tpr = p.geo.tpr;
         a.depth = p.one_depth;
         a.xrep = p.xrep;
+        a.ra = row_align_unit(p.geo.rb);
+        a.nra = N / a.ra;
         a.rb = p.geo.rb;
         a.slot_bytes = p.one_slot;
         a.x_bytes = p.one_x;

@@ -70,6 +70,10 @@ struct TaskGeo {
     // every task of every row starts 16-byte aligned (rows start at multiples of rb from a
     // 16-byte-aligned tensor): runs need no widening
     bool aligned16() const { return task_bytes() % 16 == 0 && rb % 16 == 0; }
+    // every stage of the one-token engines is a 16-byte-aligned bulk copy: CTA row ranges cut
+    // at multiples of row_align_unit(rb) rows, task ranges at multiples of task_align_unit
+    // tasks (both at most 8 for even sizes)
+    bool stage_aligned() const { return TPB == 1 && task_bytes() % 2 == 0 && rb % 2 == 0; }
 };
 inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     TaskGeo g;
@@ -238,6 +242,11 @@ struct GemvPlan {
 
 // Partial sums of one CTA of the one-token engine (rows x tasks per row) at most this many.
 constexpr int ONE_PART_MAX = 8192;
+// Tasks that are not a multiple of 16 bytes (Q6_K, Q3_K and Q2_K superblocks, short legacy
+// groups) take the one-token engine only where a CTA streams at least this many bytes:
+// measured slower than the general engine at 4096 x 4096 (Q2_K, Q3_K: 36, 47 KB per CTA),
+// faster from 17408 x 5120 (190-480 KB per CTA).
+constexpr long ONE_UNALIGNED_MIN_BYTES = 128 * 1024;
 // Rows up to this length are quantized inside the one-token engine (every CTA quantizes the
 // whole row, a cost that grows with K; beyond this the preparation kernel and its extra
 // kernel boundary were measured faster).
@@ -250,9 +259,12 @@ constexpr int ONE_FUSED_K_MAX = 8192;
 // slots per warp (up to DMAX) as shared memory holds.
 inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
     const TaskGeo &g = p.geo;
-    if (p.pair || p.MT != 1 || p.KS != 1 || !g.aligned16() || g.TPB != 1) return;
-    const int grid = std::min(N, sms);
-    const long rows_max = (N + grid - 1) / grid;
+    if (p.pair || p.MT != 1 || p.KS != 1 || !g.stage_aligned()) return;
+    const int ra = row_align_unit(g.rb);
+    if (N % ra) return;
+    const int grid = std::min(N / ra, sms);
+    const long rows_max = (long)ra * ((N / ra + grid - 1) / grid);
+    if (g.task_bytes() % 16 != 0 && rows_max * (long)g.rb < ONE_UNALIGNED_MIN_BYTES) return;
     const long part = rows_max * g.tpr;
     if (part > ONE_PART_MAX) return;
     // the general engine's warp count: 12 only where every warp gets two stages or more
@@ -391,7 +403,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     if (!p.down.ok) return p;
     if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
     if (p.gate.pair && p.gate.KS > 1) p.gate.pair = false;  // its partial sums have no workspace here
-    if (M == 1 && p.down.one && g.aligned16() && g.TPB == 1 && I % 32 == 0) {
+    if (M == 1 && p.down.one && g.stage_aligned() && I % 32 == 0) {
         // every CTA the same number of units (nu): the launch takes as long as its fullest CTA
         const int U = I / 32, nu = (U + std::min(U, sms) - 1) / std::min(U, sms), grid = (U + nu - 1) / nu;
         const int part = ffn1_part_floats(nu, g.tpr);

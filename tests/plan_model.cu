@@ -195,17 +195,21 @@ int main() {
             // one-token engine: per CTA, warp and stage a single bulk copy of whole tasks
             snprintf(nm, sizeof nm, "one f%d N%d K%d", fmt, N, K);
             ++none;
-            CHECK(M == 1 && p.KS == 1 && g.task_bytes() % 16 == 0 && g.rb % 16 == 0 && g.TPB == 1, "%s eligibility", nm);
+            const int ra = row_align_unit(g.rb), AU = task_align_unit(g.task_bytes());
+            CHECK(M == 1 && p.KS == 1 && g.stage_aligned() && N % ra == 0 && 32 % AU == 0, "%s eligibility", nm);
             CHECK(p.one_smem <= (uint32_t)SMEM_MAX && p.one_depth >= 1, "%s smem %u", nm, p.one_smem);
             CHECK(p.one_x >= (uint32_t)((g.tpr + p.xrep) * g.stride) && p.xrep >= 31, "%s x tiles", nm);
             CHECK(p.one_slot == (uint32_t)(32 * g.task_bytes()), "%s slot", nm);
             const int TB = g.task_bytes(), S = p.ncw * p.one_depth;
             for (int b = 0; b < p.grid; ++b) {
-                const int o0 = (int)((long)b * N / p.grid), o1 = (int)((long)(b + 1) * N / p.grid);
+                // CTA rows at multiples of ra, warp ranges at multiples of AU (engine1_kernel)
+                const int o0 = ra * (int)((long)b * (N / ra) / p.grid), o1 = ra * (int)((long)(b + 1) * (N / ra) / p.grid);
                 const int ntask = (o1 - o0) * g.tpr;
+                CHECK(ntask % AU == 0, "%s CTA tasks %d not a multiple of %d", nm, ntask, AU);
                 CHECK(engine1_smem(S, p.one_slot, p.one_x, ntask) <= p.one_smem, "%s part of CTA %d", nm, b);
                 for (int w = 0; w < p.ncw; ++w) {
-                    const int wa = (int)((long)ntask * w / p.ncw), wb = (int)((long)ntask * (w + 1) / p.ncw);
+                    const int wa = AU * (int)((long)(ntask / AU) * w / p.ncw);
+                    const int wb = AU * (int)((long)(ntask / AU) * (w + 1) / p.ncw);
                     for (int fa = wa; fa < wb; fa += 32) {
                         const int fb = std::min(wb, fa + 32);
                         const uintptr_t src = BASE + (uintptr_t)o0 * g.rb + (uintptr_t)fa * TB;
@@ -257,16 +261,19 @@ int main() {
             // one-token gate/up with the SwiGLU epilogue: units of 32 rows per CTA, the gate
             // rows then the up rows as two contiguous ranges; a stage at most two copies
             ++nffn1;
-            CHECK(M == 1 && p.down.one && g.aligned16() && g.TPB == 1, "%s one eligibility", nm);
+            const int AU = task_align_unit(g.task_bytes());
+            CHECK(M == 1 && p.down.one && g.stage_aligned(), "%s one eligibility", nm);
             CHECK(p.one_smem <= (uint32_t)SMEM_MAX && p.one_depth >= 1, "%s one smem", nm);
             CHECK(p.one_x >= (uint32_t)((g.tpr + XREP) * g.stride), "%s one x tiles", nm);
             const int U = I / 32, TB = g.task_bytes(), S = p.one_ncw * p.one_depth;
             for (int b = 0; b < p.one_grid; ++b) {
                 const int u0 = (int)((long)U * b / p.one_grid), u1 = (int)((long)U * (b + 1) / p.one_grid);
                 const int nu = u1 - u0, G = 32 * nu * g.tpr, ntask = 2 * G;
+                CHECK(G % AU == 0, "%s gate tasks %d not a multiple of %d", nm, G, AU);
                 CHECK(engine1_smem(S, p.one_slot, p.one_x, ffn1_part_floats(nu, g.tpr)) <= p.one_smem, "%s part %d", nm, b);
                 for (int w = 0; w < p.one_ncw; ++w) {
-                    const int wa = (int)((long)ntask * w / p.one_ncw), wb = (int)((long)ntask * (w + 1) / p.one_ncw);
+                    const int wa = AU * (int)((long)(ntask / AU) * w / p.one_ncw);
+                    const int wb = AU * (int)((long)(ntask / AU) * (w + 1) / p.one_ncw);
                     for (int fa = wa; fa < wb; fa += 32) {
                         const int fb = std::min(wb, fa + 32), g1 = std::min(fb, G), ua = std::max(fa, G);
                         long bytes = 0;
