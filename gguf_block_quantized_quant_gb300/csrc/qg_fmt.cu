@@ -74,8 +74,9 @@ int launch_engine_ncw(int ncw, const Job &job, int grid, uint32_t smem, cudaStre
 
 template <int FMT, int T, class Job>
 int launch_engine_mt(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaStream_t s) {
-    if constexpr (T == 16 || (T == 8 && (FMT == F_Q5_0 || FMT == F_Q8_0))) {
-        // 16-block Q4_0 and 8-block Q5_0 / Q8_0 tasks are planned for one token per lane only
+    if constexpr (T == 16 || (T == 8 && (FMT == F_Q5_0 || FMT == F_Q8_0 || FMT == F_Q4_1 || FMT == F_Q5_1))) {
+        // 16-block Q4_0 and 8-block Q4_1 / Q5_0 / Q5_1 / Q8_0 tasks are planned for one token
+        // per lane only
         return MT == 1 ? launch_engine_ncw<FMT, T, 1>(ncw, job, grid, smem, s) : -1;
     }
     switch (MT) {
@@ -125,14 +126,11 @@ int with_t(const TaskGeo &g, Fn &&fn) {
         if (g.T == 8) return fn(ic<8>{});
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
-    } else if constexpr (QG_FMT == F_Q8_0 || QG_FMT == F_Q5_0) {
+    } else if constexpr (QG_FMT == F_Q8_0 || QG_FMT == F_Q5_0 || QG_FMT == F_Q4_1 || QG_FMT == F_Q5_1) {
         if constexpr (LONG) {
             if (g.T == 8) return fn(ic<8>{});
         }
         if (g.T == 8) return -1;
-        if (g.T == 4) return fn(ic<4>{});
-        return fn(ic<1>{});
-    } else if constexpr (QG_FMT == F_Q4_1 || QG_FMT == F_Q5_1) {
         if (g.T == 4) return fn(ic<4>{});
         return fn(ic<1>{});
     } else if constexpr (QG_FMT == F_Q3_K || QG_FMT == F_Q5_K || QG_FMT == F_Q6_K) {

@@ -161,7 +161,9 @@ struct FmtLegacy {
     static_assert(T != 16 || FMT == F_Q4_0, "16-block tasks are Q4_0 only");
     // T >= 4: per half, its words plus two (the last block's realignment reads past its
     // end); T == 1: the words that cover the block from its 4-byte-aligned start
-    static constexpr int NH = T == 16 ? 2 : 1, HB = T / NH;
+    // two halves (loaded in swapped order by every other group of 4 lanes): 16-block Q4_0 and
+    // 8-block Q4_1 / Q5_1 tasks, whose lane stride is an even number of 16-byte chunks
+    static constexpr int NH = (T == 16 || (T == 8 && (FMT == F_Q4_1 || FMT == F_Q5_1))) ? 2 : 1, HB = T / NH;
     static constexpr int HW = HB * BS / 4 + 2;
     static constexpr int WW = T >= 4 ? NH * HW : BS / 4 + 2;
 
@@ -169,10 +171,10 @@ struct FmtLegacy {
     // bytes) apart, so lanes l and l + 4 would hit the same banks on every 16-byte load;
     // lanes with bit 2 set load their second half first (a 9-chunk shift), so w[0..HW-1]
     // holds half swap() and w[HW..] the other one.
-    __device__ __forceinline__ static int swap() { return T == 16 ? (int)((threadIdx.x >> 2) & 1) : 0; }
+    __device__ __forceinline__ static int swap() { return NH == 2 ? (int)((threadIdx.x >> 2) & 1) : 0; }
 
     __device__ __forceinline__ static void load(SAddr addr, uint32_t (&w)[WW]) {
-        if constexpr (T == 16) {
+        if constexpr (NH == 2) {
             const int sw = swap();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {

@@ -53,14 +53,15 @@ inline int log2i(int v) {
 }
 
 // Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
-//   Q4_0: 16 (only with long_tasks), 8, 4 or 1 blocks per task; IQ4_NL: 8, 4 or 1; Q5_0,
-//   Q8_0: 8 (only with long_tasks), 4 or 1; Q4_1, Q5_1: 4 or 1; Q2_K, Q4_K, IQ4_XS: 2 or 1
+//   Q4_0: 16 (only with long_tasks), 8, 4 or 1 blocks per task; IQ4_NL: 8, 4 or 1; Q4_1,
+//   Q5_0, Q5_1, Q8_0: 8 (only with long_tasks), 4 or 1; Q2_K, Q4_K, IQ4_XS: 2 or 1
 //   superblocks (the largest that divides the row); Q3_K, Q5_K, Q6_K: one whole superblock.
 // long_tasks asks for 16-block Q4_0 tasks (288 bytes, the size of two Q4_K superblocks): with
 // one token per lane they leave the lane's decode fewer, longer loads and let the 12-warp
 // engine run; with several tokens per lane the 8-block tasks on 16 warps were faster.  It
 // also asks for 8-block Q5_0 and Q8_0 tasks (176 and 272 bytes, multiples of 16 where their
-// 4-block tasks of 88 and 136 bytes are not): one token then takes the one-token engine.
+// 4-block tasks of 88 and 136 bytes are not) and 8-block Q4_1 and Q5_1 tasks (160 and 192
+// bytes: fewer, longer tasks per lane).
 struct TaskGeo {
     bool ok = false;
     int T = 1, TPB = 1, BPT = 1, XGT = 8, nbr = 0, gpr = 0, tpr = 0, stride = 0, bs = 0;
@@ -85,7 +86,7 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     if (f.qk == 32) {
         g.T = (long_tasks && fmt == 2 && g.nbr % 16 == 0)                  ? 16
               : ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0)                ? 8
-              : (long_tasks && (fmt == 6 || fmt == 8) && g.nbr % 8 == 0) ? 8
+              : (long_tasks && (fmt == 3 || fmt == 6 || fmt == 7 || fmt == 8) && g.nbr % 8 == 0) ? 8
               : g.nbr % 4 == 0                                             ? 4
                                                                            : 1;
         g.BPT = g.T;
