@@ -119,7 +119,7 @@ int launch_pair(int MT, int ncw, const Job &job, int grid, uint32_t smem, cudaSt
 template <bool LONG, class Fn>
 int with_t(const TaskGeo &g, Fn &&fn) {
     if constexpr (QG_FMT == F_Q4_0 || QG_FMT == F_IQ4_NL) {
-        if constexpr (LONG && QG_FMT == F_Q4_0) {
+        if constexpr (LONG) {
             if (g.T == 16) return fn(ic<16>{});
         }
         if (g.T == 16) return -1;

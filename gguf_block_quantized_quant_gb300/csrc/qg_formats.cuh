@@ -158,7 +158,7 @@ struct FmtLegacy {
     static constexpr int QS_OFF = FMT == F_Q4_1 ? 4 : FMT == F_Q5_0 ? 6 : FMT == F_Q5_1 ? 8 : 2;
     static constexpr int NQW = FMT == F_Q8_0 ? 8 : 4;  // code words per block
     static constexpr int TASK_BYTES = T * BS;
-    static_assert(T != 16 || FMT == F_Q4_0, "16-block tasks are Q4_0 only");
+    static_assert(T != 16 || FMT == F_Q4_0 || FMT == F_IQ4_NL, "16-block tasks are Q4_0 and IQ4_NL only");
     // T >= 4: per half, its words plus two (the last block's realignment reads past its
     // end); T == 1: the words that cover the block from its 4-byte-aligned start
     // two halves (loaded in swapped order by every other group of 4 lanes): 16-block Q4_0 and

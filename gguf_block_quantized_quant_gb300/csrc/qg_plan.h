@@ -53,10 +53,10 @@ inline int log2i(int v) {
 }
 
 // Task geometry of a row of K elements (must match the format traits in qg_formats.cuh):
-//   Q4_0: 16 (only with long_tasks), 8, 4 or 1 blocks per task; IQ4_NL: 8, 4 or 1; Q4_1,
+//   Q4_0, IQ4_NL: 16 (only with long_tasks), 8, 4 or 1 blocks per task; Q4_1,
 //   Q5_0, Q5_1, Q8_0: 8 (only with long_tasks), 4 or 1; Q2_K, Q4_K, IQ4_XS: 2 or 1
 //   superblocks (the largest that divides the row); Q3_K, Q5_K, Q6_K: one whole superblock.
-// long_tasks asks for 16-block Q4_0 tasks (288 bytes, the size of two Q4_K superblocks): with
+// long_tasks asks for 16-block Q4_0 and IQ4_NL tasks (288 bytes, the size of two Q4_K superblocks): with
 // one token per lane they leave the lane's decode fewer, longer loads and let the 12-warp
 // engine run; with several tokens per lane the 8-block tasks on 16 warps were faster.  It
 // also asks for 8-block Q5_0 and Q8_0 tasks (176 and 272 bytes, multiples of 16 where their
@@ -84,7 +84,7 @@ inline TaskGeo task_geo(int fmt, int K, bool long_tasks) {
     g.nbr = K / f.qk;
     g.rb = (uint32_t)(g.nbr * f.bs);
     if (f.qk == 32) {
-        g.T = (long_tasks && fmt == 2 && g.nbr % 16 == 0)                  ? 16
+        g.T = (long_tasks && (fmt == 2 || fmt == 20) && g.nbr % 16 == 0)   ? 16
               : ((fmt == 2 || fmt == 20) && g.nbr % 8 == 0)                ? 8
               : (long_tasks && (fmt == 3 || fmt == 6 || fmt == 7 || fmt == 8) && g.nbr % 8 == 0) ? 8
               : g.nbr % 4 == 0                                             ? 4
@@ -291,9 +291,10 @@ inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
     p.one_smem = engine1_smem(ncw * depth, slot, xb, (int)part);
 }
 
-inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms) {
+// long_ok: one token may take the long tasks of task_geo
+inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms, bool long_ok = true) {
     GemvPlan p;
-    p.geo = task_geo(fmt, K, pick_mt(M) == 1);
+    p.geo = task_geo(fmt, K, long_ok && pick_mt(M) == 1);
     const TaskGeo &g = p.geo;
     if (!g.ok || N < 1 || M < 1 || M > M_MAX || sms < 1) return p;
     p.KS = N < G_PLAN / 2 ? std::min(g.gpr, (G_PLAN + N - 1) / N) : 1;
@@ -388,7 +389,10 @@ struct FfnPlan {
 
 inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     FfnPlan p;
-    p.geo = task_geo(fmt, H, M == 1);
+    // IQ4_NL in 8-block tasks here: with 16-block tasks (gate/up, down or both) the sublayer
+    // measured 1.4-1.7 us slower at H = 5120, I = 17408 (register spills), although the plain
+    // GEMV gains from them
+    p.geo = task_geo(fmt, H, M == 1 && fmt != 20);
     const TaskGeo &g = p.geo;
     if (!g.ok || !task_geo(fmt, I, false).ok || M < 1 || M > M_MAX || sms < 1) return p;
     const long tiles = (long)g.tpr * g.stride;
@@ -400,7 +404,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     p.ncw = plan_ncw(g, p.MT, (long)((2L * I + p.grid - 1) / p.grid) * g.tpr);
     p.ring = plan_ring(g, (long)I * g.tpr, (uint32_t)(p.MC * tiles), 0, p.ncw);
     if (!p.ring.ok) return p;
-    p.down = plan_gemv(fmt, H, I, M, sms);
+    p.down = plan_gemv(fmt, H, I, M, sms, fmt != 20);
     if (!p.down.ok) return p;
     if (M >= 2) p.gate = plan_gemv(fmt, I, H, M, sms);
     if (p.gate.pair && p.gate.KS > 1) p.gate.pair = false;  // its partial sums have no workspace here
