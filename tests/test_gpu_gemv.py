@@ -213,6 +213,10 @@ FULL = [
     (synth.Q6_K, 17408, 5120), (synth.Q6_K, 5120, 17408),
     (synth.Q4_1, 4096, 4096), (synth.Q5_0, 4096, 4096), (synth.Q5_1, 4096, 4096), (synth.IQ4_NL, 4096, 4096),
     (synth.Q2_K, 4096, 4096), (synth.Q3_K, 4096, 4096), (synth.Q2_K, 17408, 5120), (synth.Q3_K, 5120, 17408),
+    # one-token tasks of 8 blocks (Q4_1, Q5_0, Q5_1, Q8_0) and 16 blocks (IQ4_NL), and
+    # 110-byte Q3_K superblocks on the one-token engine (rows of 2200 bytes: 2-row groups)
+    (synth.Q4_1, 17408, 5120), (synth.Q5_0, 5120, 17408), (synth.Q5_1, 17408, 5120),
+    (synth.Q8_0, 17408, 5120), (synth.IQ4_NL, 17408, 5120), (synth.Q3_K, 17408, 5120),
 ]
 
 
