@@ -134,16 +134,17 @@ def _check(rc: int, what: str):
         raise QGError(rc, what)
 
 
-def _ws(ws, size_query, device):
+def _ws(ws, size_query, like):
     """The workspace and its byte count: the caller's (the C call checks its size), or a new
-    one of qg_workspace_size bytes (size_query() runs only then)."""
+    one of qg_workspace_size bytes on the device of the activations `like` (size_query()
+    and the device lookup run only then)."""
     if ws is not None:
         return ws, ws.numel()
     nbytes = size_query()
     if nbytes == WS_INVALID:
         raise QGError(QG_EINVAL, "qg_workspace_size")
     if nbytes > 0:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=_dev(like))
     return ws, (0 if ws is None else ws.numel())
 
 
@@ -175,7 +176,7 @@ def qg_quantize_act_s16(x, xq=None, xd=None, xs=None, stream=None):
 def qg_gemv(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
     M, K = x.shape
     y = _out((M, N), torch.float32, x) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), _dev(x))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_GEMV, fmt, M, N, K), x)
     _check(lib().qg_gemv(fmt, _ptr(W, False), _ptr(x), _ptr(y), N, K, M, _ptr(ws, False), nws, _stream(stream)), "qg_gemv")
     return y
 
@@ -196,7 +197,7 @@ def qg_gemv_static_ws(fmt: int, W, x, N: int, y=None, stream=None):
 def qg_gemv_q(fmt: int, W, xq, xd, xs, N: int, y=None, ws=None, stream=None):
     M, K = xq.shape
     y = _out((M, N), torch.float32, xq) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_GEMV_Q, fmt, M, N, K), _dev(xq))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_GEMV_Q, fmt, M, N, K), xq)
     _check(lib().qg_gemv_q(fmt, _ptr(W, False), _ptr(xq), _ptr(xd), _ptr(xs), _ptr(y), N, K, M, _ptr(ws, False), nws,
                            _stream(stream)), "qg_gemv_q")
     return y
@@ -207,7 +208,7 @@ def qg_moe_ffn(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh, Wu_
     M, H = x.shape
     E = Wr.shape[0]
     y = _out((M, H), torch.float32, x) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), _dev(x))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_MOE_FFN, fmt, M, H, H, E, topk, I), x)
     _check(lib().qg_moe_ffn(fmt, _ptr(x), M, H, _ptr(Wr, False), E, topk, _ptr(Wg_exps, False), _ptr(Wu_exps, False), _ptr(Wd_exps, False),
                             _ptr(Wg_sh, False), _ptr(Wu_sh, False), _ptr(Wd_sh, False), I, _ptr(y), _ptr(topk_ids), _ptr(topk_w),
                             _ptr(ws, False), nws, _stream(stream)), "qg_moe_ffn")
@@ -219,7 +220,7 @@ def qg_moe_ffn_s16(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh,
     M, H = x.shape
     E = Wr.shape[0]
     y = _out((M, H), torch.float32, x) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_MOE_FFN_S16, fmt, M, H, H, E, topk, I), _dev(x))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_MOE_FFN_S16, fmt, M, H, H, E, topk, I), x)
     _check(lib().qg_moe_ffn_s16(fmt, _ptr(x), M, H, _ptr(Wr, False), E, topk, _ptr(Wg_exps, False), _ptr(Wu_exps, False),
                                 _ptr(Wd_exps, False), _ptr(Wg_sh, False), _ptr(Wu_sh, False), _ptr(Wd_sh, False), I, _ptr(y), _ptr(topk_ids),
                                 _ptr(topk_w), _ptr(ws, False), nws, _stream(stream)), "qg_moe_ffn_s16")
@@ -229,7 +230,7 @@ def qg_moe_ffn_s16(fmt: int, x, Wr, topk: int, Wg_exps, Wu_exps, Wd_exps, Wg_sh,
 def qg_ffn_sublayer(fmt: int, Wg, Wu, Wd, x, I: int, y=None, ws=None, stream=None):
     M, H = x.shape
     y = _out((M, H), torch.float32, x) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), _dev(x))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_FFN_SUBLAYER, fmt, M, H, H, 0, 0, I), x)
     _check(lib().qg_ffn_sublayer(fmt, _ptr(Wg, False), _ptr(Wu, False), _ptr(Wd, False), _ptr(x), _ptr(y), M, H, I, _ptr(ws, False), nws,
                                  _stream(stream)), "qg_ffn_sublayer")
     return y
@@ -266,7 +267,7 @@ def qg_prefill_gemm(fmt: int, W, x, N: int, y=None, ws=None, stream=None):
     """Prefill GEMM on the tensor cores: y = fp16(W) fp16(x)^T in fp32, for M >> 16 tokens."""
     M, K = x.shape
     y = _out((M, N), torch.float32, x) if y is None else y
-    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_PREFILL, fmt, M, N, K), _dev(x))
+    ws, nws = _ws(ws, lambda: qg_workspace_size(QG_OP_PREFILL, fmt, M, N, K), x)
     _check(lib().qg_prefill_gemm(fmt, _ptr(W, False), _ptr(x), _ptr(y), N, K, M, _ptr(ws, False), nws,
                                  _stream(stream)), "qg_prefill_gemm")
     return y
