@@ -50,6 +50,7 @@ WORKLOAD_NAME = "Q4_0 + Q4_K GEMV, M=1, dense-27B FFN shapes (17408x5120 gate/up
 CONFIG_ID = 2  # seed id of this workload (synth.seed_for)
 MATRICES = [(synth.Q4_0, 17408, 5120), (synth.Q4_0, 5120, 17408), (synth.Q4_K, 17408, 5120), (synth.Q4_K, 5120, 17408)]
 M_TOKENS = 1
+ONE_FUSED_K_MAX = 8192        # rows up to this length are quantized inside the one-token engine
 ROTATE = 2                    # weight copies per matrix
 STEPS_PER_GRAPH = 16          # steps captured in one CUDA graph
 FALLBACK_HBM_GBS = 6800.0     # used only when no measured peak is available
@@ -311,7 +312,10 @@ def run_ours(args):
                          y_host=torch.empty((M_TOKENS, N), dtype=torch.float32).pin_memory(),
                          ws=torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)))
     step_weight_bytes = weight_bytes_per_step()
-    launches_per_step = 2 * len(MATRICES)  # activation tile preparation + engine, per GEMV
+    # kernels per GEMV call at one token with x in device memory: the engine alone where it
+    # quantizes the row itself (rows of up to 8192 elements), else the activation tile
+    # preparation and the engine
+    launches_per_step = sum(1 if K <= ONE_FUSED_K_MAX else 2 for _, _, K in MATRICES)
 
     s = torch.cuda.Stream(device=dev)
 

@@ -100,3 +100,15 @@ def test_traffic_is_null_when_sources_differ(monkeypatch):
 def test_weight_bytes_of_the_step():
     # four matrices of 50,135,040 bytes (4.5 bits per weight)
     assert bench.weight_bytes_per_step() == 4 * 50135040
+
+
+def test_launch_count_rule_matches_the_planner():
+    """bench.py counts one kernel per one-token call whose row is quantized inside the engine;
+    the row-length limit must be the planner's."""
+    import re
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = open(os.path.join(here, "..", "gguf_block_quantized_quant_gb300", "csrc", "qg_plan.h")).read()
+    m = re.search(r"constexpr int ONE_FUSED_K_MAX = (\d+);", src)
+    assert m is not None
+    import bench
+    assert bench.ONE_FUSED_K_MAX == int(m.group(1))
