@@ -292,17 +292,9 @@ inline void plan_gemv_one(GemvPlan &p, int N, int sms) {
 }
 
 // long_ok: one token may take the long tasks of task_geo
-// Q4_K at one token with the row quantized in the kernel and at least 64 rows per CTA: one
-// superblock per task (16 warps) instead of two (12 warps).  Measured per call: 17408x5120
-// 11.5 -> 11.0 us, FFN sublayer gate/up H = 5120, I = 17408 30.4 -> 30.0 us; with fewer rows
-// per CTA (4096 x 4096: 5.1 -> 5.7 us) or rows of 17408 (12.5 -> 12.7 us) two stay faster.
-inline bool q4k_short_one(int fmt, int rows, int K, int M, int sms) {
-    return fmt == 12 && M == 1 && K <= ONE_FUSED_K_MAX && (long)rows >= 64L * sms;
-}
-
 inline GemvPlan plan_gemv(int fmt, int N, int K, int M, int sms, bool long_ok = true) {
     GemvPlan p;
-    p.geo = q4k_short_one(fmt, N, K, M, sms) ? short_task_geo(fmt, K) : task_geo(fmt, K, long_ok && pick_mt(M) == 1);
+    p.geo = task_geo(fmt, K, long_ok && pick_mt(M) == 1);
     const TaskGeo &g = p.geo;
     if (!g.ok || N < 1 || M < 1 || M > M_MAX || sms < 1) return p;
     p.KS = N < G_PLAN / 2 ? std::min(g.gpr, (G_PLAN + N - 1) / N) : 1;
@@ -400,7 +392,7 @@ inline FfnPlan plan_ffn(int fmt, int M, int H, int I, int sms) {
     // IQ4_NL in 8-block tasks here: with 16-block tasks (gate/up, down or both) the sublayer
     // measured 1.4-1.7 us slower at H = 5120, I = 17408 (register spills), although the plain
     // GEMV gains from them
-    p.geo = q4k_short_one(fmt, 2 * I, H, M, sms) ? short_task_geo(fmt, H) : task_geo(fmt, H, M == 1 && fmt != 20);
+    p.geo = task_geo(fmt, H, M == 1 && fmt != 20);
     const TaskGeo &g = p.geo;
     if (!g.ok || !task_geo(fmt, I, false).ok || M < 1 || M > M_MAX || sms < 1) return p;
     const long tiles = (long)g.tpr * g.stride;

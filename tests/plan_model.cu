@@ -350,7 +350,7 @@ int main() {
     // choices; a change here changes the timings the documentation reports)
     {
         const GemvPlan a = plan_gemv(12, 17408, 5120, 1, sms), b = plan_gemv(12, 5120, 17408, 1, sms);
-        CHECK(!a.pair && a.KS == 1 && a.ncw == 16 && a.xrep == XREP && a.geo.T == 1 && a.one, "Q4_K 17408x5120 M1 plan");
+        CHECK(!a.pair && a.KS == 1 && a.ncw == 12 && a.xrep == XREP && a.geo.T == 2, "Q4_K 17408x5120 M1 plan");
         CHECK(!b.pair && b.KS == 1 && b.ncw == 12 && b.xrep == XREP, "Q4_K 5120x17408 M1 plan");
         const GemvPlan c = plan_gemv(2, 17408, 5120, 1, sms);
         CHECK(!c.pair && c.geo.T == 16 && c.xrep == XREP, "Q4_0 17408x5120 M1 plan");
